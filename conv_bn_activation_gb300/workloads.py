@@ -1,0 +1,124 @@
+"""Algorithmic bytes and FLOPs of each step of the hot path (the roofline numerators).
+
+"Algorithmic" means compulsory DRAM traffic: every input element read once,
+every output element written once, weights and per-channel scale/bias read
+once.  Halo re-reads, partial-sector traffic and L2 misses are not counted;
+measured DRAM traffic above these figures is waste.
+
+The preprocess ledger follows "A fused Ampere preprocess kernel" (the byte
+ledger per pass): the resize reads the u8 frame and writes a u8 resized frame,
+the normalize reads it and writes fp32, the layout pass reads and writes fp32;
+the fused pass reads the u8 frame once and writes the fp32 planar tensor once.
+FLOPs count one multiply and one add per multiply-accumulate of the
+convolution only (BN, activation and residual are not counted), which is the
+convention behind the depthwise arithmetic intensities quoted on "How I sped
+up convolutions" (about 0.87-2.2 FLOP/byte for its depthwise layers).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+F32 = 4
+
+
+def out_size(n: int, k: int, s: int, p: int) -> int:
+    return (n + 2 * p - k) // s + 1
+
+
+@dataclass(frozen=True)
+class Work:
+    bytes: int
+    flops: int
+
+    @property
+    def intensity(self) -> float:
+        return self.flops / self.bytes if self.bytes else 0.0
+
+    def __add__(self, other: "Work") -> "Work":
+        return Work(self.bytes + other.bytes, self.flops + other.flops)
+
+
+def conv_layer(N, H, W, Cin, Cout, k, s, p, groups=1, residual=False) -> Work:
+    """Fused conv + folded BN (+ residual) + activation: in + out (+ r) + w + scale/bias."""
+    OH, OW = out_size(H, k, s, p), out_size(W, k, s, p)
+    x = N * H * W * Cin * F32
+    y = N * OH * OW * Cout * F32
+    w = Cout * (Cin // groups) * k * k * F32
+    sb = 2 * Cout * F32
+    r = y if residual else 0
+    macs = N * OH * OW * Cout * (Cin // groups) * k * k
+    return Work(x + y + w + sb + r, 2 * macs)
+
+
+def depthwise_layer(N, H, W, C, s, k=3, p=1) -> Work:
+    return conv_layer(N, H, W, C, C, k, s, p, groups=C)
+
+
+# --- preprocess ledger ("A fused Ampere preprocess kernel", the theory) -----
+def preprocess_ledger(Hs, Ws, Hd, Wd, channels=3):
+    """Bytes through DRAM per frame for each pass of the unfused path and the fused path."""
+    src = Hs * Ws * channels                 # u8 frame
+    mid_u8 = Hd * Wd * channels              # u8 resized frame
+    f32 = Hd * Wd * channels * F32           # fp32 tensor (HWC or CHW)
+    passes = {
+        "resize": src + mid_u8,
+        "normalize": mid_u8 + f32,
+        "layout": f32 + f32,
+    }
+    return {"passes": passes, "unfused": sum(passes.values()), "fused": src + f32}
+
+
+def preprocess_fused(N, Hs, Ws, Hd, Wd) -> Work:
+    return Work(N * preprocess_ledger(Hs, Ws, Hd, Wd)["fused"], 0)
+
+
+def preprocess_unfused(N, Hs, Ws, Hd, Wd) -> Work:
+    return Work(N * preprocess_ledger(Hs, Ws, Hd, Wd)["unfused"], 0)
+
+
+# --- whole workloads -------------------------------------------------------
+def depthwise_workload(N=64, H=56, W=56, C=384):
+    """The depthwise 3x3 + BN + ReLU layer at stride 1 and stride 2."""
+    return {"s1": depthwise_layer(N, H, W, C, 1), "s2": depthwise_layer(N, H, W, C, 2)}
+
+
+def mnist_layers(N=64):
+    """Per-layer work of the DepthwiseMNIST forward (stem, 4 blocks, pool + fc)."""
+    from .synthetic import MNIST_BLOCKS
+    layers = [("stem", conv_layer(N, 28, 28, 1, 48, 3, 1, 1))]
+    H = 28
+    for i, (cin, cout, s) in enumerate(MNIST_BLOCKS):
+        OH = out_size(H, 3, s, 1)
+        layers.append((f"b{i}.dw", depthwise_layer(N, H, H, cin, s)))
+        skip = s != 1 or cin != cout
+        layers.append((f"b{i}.pw", conv_layer(N, OH, OH, cin, cout, 1, 1, 0, residual=True)))
+        if skip:
+            layers.append((f"b{i}.skip", conv_layer(N, H, H, cin, cout, 1, s, 0)))
+        H = OH
+    pool = Work(N * H * H * 192 * F32 + 10 * 192 * F32 + 10 * F32 + N * 10 * F32,
+                N * (H * H * 192 + 2 * 192 * 10))
+    layers.append(("pool_fc", pool))
+    return layers
+
+
+def yolo_layers(N=1, size=640):
+    """Per-layer work of the 20-conv YOLO-style chain."""
+    from .synthetic import YOLO_STAGES
+    layers = []
+    H = size
+    for i, (cin, c) in enumerate(YOLO_STAGES):
+        h = c // 2
+        OH = out_size(H, 3, 2, 1)
+        layers.append((f"s{i}.down", conv_layer(N, H, H, cin, c, 3, 2, 1)))
+        layers.append((f"s{i}.cv1", conv_layer(N, OH, OH, c, h, 1, 1, 0)))
+        layers.append((f"s{i}.cv2", conv_layer(N, OH, OH, h, h, 3, 1, 1)))
+        layers.append((f"s{i}.cv3", conv_layer(N, OH, OH, c, c, 1, 1, 0, residual=True)))
+        H = OH
+    return layers
+
+
+def total(layers) -> Work:
+    t = Work(0, 0)
+    for _, w in layers:
+        t = t + w
+    return t
