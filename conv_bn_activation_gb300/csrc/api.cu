@@ -1,0 +1,604 @@
+// The C ABI: argument validation, per-shape kernel choice, TMA descriptor
+// encoding and launches.  Host code only (the kernels live in the other .cu
+// files of this directory).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "cb.h"
+#include "internal.h"
+
+namespace cb {
+int dw_tma_blocks_per_sm(int stride, int threads, size_t smem);
+}
+
+using namespace cb;
+
+// Device error word: kernels record CB_ERR_TIMEOUT here when a bounded wait gives up.
+__device__ int g_cb_device_error;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+thread_local int t_last_cuda_error = 0;
+std::atomic<int> g_policy{0};
+
+cb_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return CB_ERR_CUDA;
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int* err = nullptr;
+};
+std::mutex g_mu;
+DeviceInfo g_devices[128];
+
+cb_status current_device(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 128) return CB_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_cb_device_error);
+    if (e != cudaSuccess) return cuda_fail(e);
+    d.err = static_cast<int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return CB_OK;
+}
+
+uint64_t timeout_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("CB_TIMEOUT_MS");
+    long long ms = s ? std::atoll(s) : 2000;
+    if (ms <= 0) ms = 2000;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return v;
+}
+
+// ---------------------------------------------------------- driver entry points
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using EncodeIm2colFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+void* driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return p;
+}
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(driver_fn("cuTensorMapEncodeTiled"));
+  return fn;
+}
+
+EncodeIm2colFn encode_im2col() {
+  static EncodeIm2colFn fn = reinterpret_cast<EncodeIm2colFn>(driver_fn("cuTensorMapEncodeIm2col"));
+  return fn;
+}
+
+// ------------------------------------------------------------------ validation
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool view_ok(const cb_tensor* t) {
+  if (!t) return false;
+  if (t->n < 0 || t->h < 1 || t->w < 1 || t->c < 1) return false;
+  if (t->layout != CB_LAYOUT_NHWC && t->layout != CB_LAYOUT_NCHW) return false;
+  if (t->stride_n < 0 || t->stride_h < 0 || t->stride_w < 0 || t->stride_c < 0) return false;
+  if (t->layout == CB_LAYOUT_NHWC && t->stride_c != 1) return false;
+  if (t->layout == CB_LAYOUT_NCHW && t->stride_w != 1) return false;
+  if (t->n > 0 && !t->data) return false;
+  return true;
+}
+
+// Byte range [lo, hi) spanned by a view (strides are non-negative).
+void view_range(const cb_tensor* t, uintptr_t* lo, uintptr_t* hi) {
+  const long long last = (static_cast<long long>(t->n) - 1) * t->stride_n + (t->h - 1LL) * t->stride_h +
+                         (t->w - 1LL) * t->stride_w + (t->c - 1LL) * t->stride_c;
+  *lo = reinterpret_cast<uintptr_t>(t->data);
+  *hi = *lo + static_cast<uintptr_t>(last + 1) * sizeof(float);
+}
+
+bool overlap(const cb_tensor* a, const cb_tensor* b) {
+  if (a->n == 0 || b->n == 0) return false;
+  uintptr_t alo, ahi, blo, bhi;
+  view_range(a, &alo, &ahi);
+  view_range(b, &blo, &bhi);
+  return alo < bhi && blo < ahi;
+}
+
+bool same_view(const cb_tensor* a, const cb_tensor* b) {
+  return a->data == b->data && a->n == b->n && a->h == b->h && a->w == b->w && a->c == b->c &&
+         a->stride_n == b->stride_n && a->stride_h == b->stride_h && a->stride_w == b->stride_w &&
+         a->stride_c == b->stride_c && a->layout == b->layout;
+}
+
+bool strides_mult4(const cb_tensor* t) {
+  return t->stride_n % 4 == 0 && t->stride_h % 4 == 0 && t->stride_w % 4 == 0;
+}
+
+Epilogue make_epilogue(const float* scale, const float* bias, cb_act act, const cb_tensor* r, cb_res_mode mode) {
+  Epilogue e{};
+  e.scale = scale;
+  e.bias = bias;
+  e.act = static_cast<int>(act);
+  e.res_mode = static_cast<int>(mode);
+  if (mode != CB_RES_NONE) {
+    e.r = static_cast<const float*>(r->data);
+    e.rs_n = r->stride_n;
+    e.rs_h = r->stride_h;
+    e.rs_w = r->stride_w;
+  }
+  return e;
+}
+
+OutView make_out(const cb_tensor* y) {
+  OutView o{};
+  o.y = static_cast<float*>(y->data);
+  o.ys_n = y->stride_n;
+  o.ys_h = y->stride_h;
+  o.ys_w = y->stride_w;
+  return o;
+}
+
+// ----------------------------------------------------------------- depthwise
+cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, int stride, int pad,
+                        const cb_tensor* y, cudaStream_t s) {
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  DwArgs a{};
+  a.x = static_cast<const float*>(x->data);
+  a.xs_n = x->stride_n;
+  a.xs_h = x->stride_h;
+  a.xs_w = x->stride_w;
+  a.w = w;
+  a.N = x->n;
+  a.H = x->h;
+  a.W = x->w;
+  a.C = x->c;
+  a.OH = y->h;
+  a.OW = y->w;
+  a.stride = stride;
+  a.pad = pad;
+  a.out = make_out(y);
+  a.ep = ep;
+  const bool vec = a.C % 4 == 0 && aligned16(a.x) && aligned16(w) && aligned16(ep.scale) && aligned16(ep.bias) &&
+                   aligned16(a.out.y) && strides_mult4(x) && strides_mult4(y) &&
+                   (ep.res_mode == 0 || (aligned16(ep.r) && ep.rs_n % 4 == 0 && ep.rs_h % 4 == 0 && ep.rs_w % 4 == 0));
+  const int policy = g_policy.load();
+  const bool tma_ok = vec && policy != 1 && encode_tiled() != nullptr && a.OW >= 1;
+  if (!tma_ok) {
+    cudaError_t e = launch_dw_simple(a, vec, s);
+    return e == cudaSuccess ? CB_OK : cuda_fail(e);
+  }
+
+  // Plan: output-column tiles of at most 60 columns (8 consumer threads per
+  // column), strips of output rows, 32-channel chunks; minimise the busiest
+  // SM's staged bytes.
+  const int chunks = (a.C + 31) / 32;
+  DwTmaPlan best{};
+  double best_cost = 1e300;
+  for (int wt = (a.OW + 59) / 60; wt <= std::max((a.OW + 59) / 60, a.OW / 8); ++wt) {
+    const int tile_w = (a.OW + wt - 1) / wt;
+    const int wtiles = (a.OW + tile_w - 1) / tile_w;
+    const int box_w = (tile_w - 1) * stride + 3;
+    if (box_w > 256) continue;
+    const int consumer_warps = (tile_w * 8 + 31) / 32;
+    const int threads = 32 * (1 + consumer_warps);
+    const int stage_bytes = box_w * 128;
+    int cps = dw_tma_blocks_per_sm(stride, threads, 96 * 1024) >= 2 ? 2 : 1;
+    const size_t ring = cps == 2 ? 96 * 1024 : 192 * 1024;
+    int stages = static_cast<int>(std::min<size_t>(32, ring / stage_bytes));
+    if (stages < 3) continue;
+    const size_t smem = static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t) + 16;
+    const int cap = dev->sms * cps;
+    for (int strips = 1; strips <= std::max(1, a.OH / 4); ++strips) {
+      const int R = (a.OH + strips - 1) / strips;
+      if (strips > 1 && (a.OH + R - 1) / R != strips) continue;
+      const long long items = static_cast<long long>(a.N) * chunks * strips * wtiles;
+      if (items > (1LL << 30)) continue;
+      const int grid = static_cast<int>(std::min<long long>(items, cap));
+      const long long per_cta = (items + grid - 1) / grid;
+      const double item_cost = (static_cast<double>((R - 1) * stride + 3) * box_w) + 64.0;  // + fixed cost
+      const double cost = static_cast<double>(cps) * per_cta * item_cost;
+      if (cost < best_cost) {
+        best_cost = cost;
+        best.rows_per_item = R;
+        best.num_items = static_cast<int>(items);
+        best.box_w = box_w;
+        best.stages = stages;
+        best.grid = grid;
+        best.consumer_warps = consumer_warps;
+        best.smem_bytes = smem;
+      }
+    }
+  }
+  if (best.grid == 0) {
+    cudaError_t e = launch_dw_simple(a, vec, s);
+    return e == cudaSuccess ? CB_OK : cuda_fail(e);
+  }
+  CUtensorMap map;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(a.C), static_cast<cuuint64_t>(a.W), static_cast<cuuint64_t>(a.H),
+                        static_cast<cuuint64_t>(a.N)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(a.xs_w) * 4, static_cast<cuuint64_t>(a.xs_h) * 4,
+                           static_cast<cuuint64_t>(a.xs_n) * 4};
+  cuuint32_t box[4] = {32, static_cast<cuuint32_t>(best.box_w), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode_tiled()(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(a.x), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    cudaError_t e = launch_dw_simple(a, vec, s);
+    return e == cudaSuccess ? CB_OK : cuda_fail(e);
+  }
+  cudaError_t e = launch_dw_tma(map, a, best, dev->err, timeout_ns(), s);
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+// -------------------------------------------------------------------- dense
+int pick_bn(int M, int Cout, int k_iters, int sms, int* n_tiles_out) {
+  static const int kBn[] = {16, 32, 48, 64, 96, 128, 192, 256};
+  const int m_tiles = (M + 127) / 128;
+  double best = 1e300;
+  int best_bn = 16, best_nt = (Cout + 15) / 16;
+  for (int bn : kBn) {
+    const int n_tiles = (Cout + bn - 1) / bn;
+    if (n_tiles > 1 && bn < 64 && Cout > 256) continue;
+    const long long tiles = static_cast<long long>(m_tiles) * n_tiles;
+    const long long waves = (tiles + sms - 1) / sms;
+    // per k-step: smem operand bytes / 128 B per clock vs tensor work (M=128, K=32, N=bn)
+    const double step = std::max(128.0 + bn, 2.2 * bn);
+    const double epi = 2.0 * bn;  // epilogue cycles per tile, roughly
+    const double cost = static_cast<double>(waves) * (k_iters * step + epi);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_bn = bn;
+      best_nt = n_tiles;
+    }
+  }
+  *n_tiles_out = best_nt;
+  return best_bn;
+}
+
+cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int k, int stride, int pad,
+                    const cb_tensor* y, cudaStream_t s) {
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  const int Ci = x->c, Co = y->c;
+  IgemmArgs a{};
+  a.M = x->n * y->h * y->w;
+  a.OHW = y->h * y->w;
+  a.OW = y->w;
+  a.Cout = Co;
+  a.kw = k;
+  a.taps = k * k;
+  a.num_kc = (Ci + 31) / 32;
+  a.k_iters = a.taps * a.num_kc;
+  a.stride = stride;
+  a.pad = pad;
+  a.out = make_out(y);
+  a.ep = ep;
+  a.err = dev->err;
+  a.timeout_ns = timeout_ns();
+  a.vec_store = (aligned16(a.out.y) && strides_mult4(y) && aligned16(ep.scale) && aligned16(ep.bias) &&
+                 (ep.res_mode == 0 || (aligned16(ep.r) && ep.rs_n % 4 == 0 && ep.rs_h % 4 == 0 && ep.rs_w % 4 == 0)))
+                    ? 1
+                    : 0;
+  int n_tiles = 1;
+  const int bn = pick_bn(a.M, Co, a.k_iters, dev->sms, &n_tiles);
+  a.m_tiles = (a.M + 127) / 128;
+  a.n_tiles = n_tiles;
+  a.stages = igemm_stages(bn);
+  const size_t smem = igemm_smem_bytes(bn, a.stages);
+  const long long tiles = static_cast<long long>(a.m_tiles) * a.n_tiles;
+  const int grid = static_cast<int>(std::min<long long>(tiles, dev->sms));
+
+  CUtensorMap amap, bmap;
+  {
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(x->w), static_cast<cuuint64_t>(x->h),
+                          static_cast<cuuint64_t>(x->n)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(x->stride_w) * 4, static_cast<cuuint64_t>(x->stride_h) * 4,
+                             static_cast<cuuint64_t>(x->stride_n) * 4};
+    int lower[2] = {-pad, -pad};
+    int upper[2] = {pad - (k - 1), pad - (k - 1)};
+    cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(stride), static_cast<cuuint32_t>(stride), 1};
+    CUresult r = encode_im2col()(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x->data, dims, strides, lower, upper, 32,
+                                 128, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
+  }
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(k * k), static_cast<cuuint64_t>(Co)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(Ci) * 4, static_cast<cuuint64_t>(k * k) * Ci * 4};
+    cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(bn)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode_tiled()(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(w), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
+  }
+  cudaError_t e = launch_igemm(amap, bmap, a, bn, grid, smem, s);
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+cb_status run_direct(const cb_tensor* x, const float* w, const Epilogue& ep, int k, int stride, int pad,
+                     const cb_tensor* y, cudaStream_t s) {
+  DirectArgs a{};
+  a.x = static_cast<const float*>(x->data);
+  a.xs_n = x->stride_n;
+  a.xs_h = x->stride_h;
+  a.xs_w = x->stride_w;
+  a.xs_c = x->stride_c;
+  a.w = w;
+  a.N = x->n;
+  a.H = x->h;
+  a.W = x->w;
+  a.Ci = x->c;
+  a.Co = y->c;
+  a.OH = y->h;
+  a.OW = y->w;
+  a.kh = k;
+  a.kw = k;
+  a.stride = stride;
+  a.pad = pad;
+  a.out = make_out(y);
+  a.ep = ep;
+  cudaError_t e = launch_direct(a, s);
+  if (e == cudaErrorInvalidValue) return CB_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+// =============================================================================
+extern "C" {
+
+cb_status cb_fold_bn(const float* gamma, const float* beta, const float* mean, const float* var, float eps, int C,
+                     float* scale, float* bias) {
+  if (!gamma || !beta || !mean || !var || !scale || !bias || C <= 0 || !(eps >= 0.0f)) return CB_ERR_INVALID_ARG;
+  for (int c = 0; c < C; ++c)
+    if (!(static_cast<double>(var[c]) + eps > 0.0)) return CB_ERR_INVALID_ARG;
+  for (int c = 0; c < C; ++c) {
+    const double sc = static_cast<double>(gamma[c]) / std::sqrt(static_cast<double>(var[c]) + static_cast<double>(eps));
+    scale[c] = static_cast<float>(sc);
+    bias[c] = static_cast<float>(static_cast<double>(beta[c]) - static_cast<double>(mean[c]) * sc);
+  }
+  return CB_OK;
+}
+
+cb_status cb_repack_weights(const float* w_oihw, int Co, int Ci_per_group, int kh, int kw, int groups,
+                            float* w_out) {
+  if (!w_oihw || !w_out || Co <= 0 || Ci_per_group <= 0 || kh <= 0 || kw <= 0 || groups <= 0)
+    return CB_ERR_INVALID_ARG;
+  if (groups == 1) {
+    for (int o = 0; o < Co; ++o)
+      for (int i = 0; i < kh; ++i)
+        for (int j = 0; j < kw; ++j)
+          for (int c = 0; c < Ci_per_group; ++c)
+            w_out[((static_cast<long long>(o) * kh + i) * kw + j) * Ci_per_group + c] =
+                w_oihw[((static_cast<long long>(o) * Ci_per_group + c) * kh + i) * kw + j];
+    return CB_OK;
+  }
+  if (groups == Co && Ci_per_group == 1) {
+    for (int o = 0; o < Co; ++o)
+      for (int i = 0; i < kh; ++i)
+        for (int j = 0; j < kw; ++j)
+          w_out[(static_cast<long long>(i) * kw + j) * Co + o] = w_oihw[(static_cast<long long>(o) * kh + i) * kw + j];
+    return CB_OK;
+  }
+  return CB_ERR_UNSUPPORTED;
+}
+
+cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale, const float* bias, int kh, int kw,
+                         int stride, int pad, int groups, cb_act act, const cb_tensor* residual,
+                         cb_res_mode res_mode, cb_tensor* y, void* stream) {
+  if (!view_ok(x) || !view_ok(y) || !w || !scale || !bias) return CB_ERR_INVALID_ARG;
+  if (act < CB_ACT_NONE || act > CB_ACT_SILU || res_mode < CB_RES_NONE || res_mode > CB_RES_POST_ACT)
+    return CB_ERR_INVALID_ARG;
+  if (kh != kw || (kh != 1 && kh != 3)) return CB_ERR_UNSUPPORTED;
+  if (stride != 1 && stride != 2) return CB_ERR_UNSUPPORTED;
+  if (pad < 0 || pad > kh / 2) return CB_ERR_UNSUPPORTED;
+  if (y->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
+  if (x->h + 2 * pad < kh || x->w + 2 * pad < kw) return CB_ERR_INVALID_ARG;
+  const int OH = (x->h + 2 * pad - kh) / stride + 1, OW = (x->w + 2 * pad - kw) / stride + 1;
+  if (y->n != x->n || y->h != OH || y->w != OW) return CB_ERR_INVALID_ARG;
+  const bool depthwise = groups == x->c && groups == y->c && groups > 1;
+  if (!depthwise && groups != 1) return CB_ERR_UNSUPPORTED;
+  if (res_mode != CB_RES_NONE) {
+    if (!view_ok(residual) || residual->layout != CB_LAYOUT_NHWC) return CB_ERR_INVALID_ARG;
+    if (residual->n != y->n || residual->h != y->h || residual->w != y->w || residual->c != y->c)
+      return CB_ERR_INVALID_ARG;
+    if (!same_view(residual, y) && overlap(residual, y)) return CB_ERR_INVALID_ARG;
+  }
+  if (overlap(x, y)) return CB_ERR_INVALID_ARG;
+  if (x->n == 0) return CB_OK;
+  const long long M = static_cast<long long>(x->n) * OH * OW;
+  if (M > (1LL << 31) - 129) return CB_ERR_UNSUPPORTED;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Epilogue ep = make_epilogue(scale, bias, act, residual, res_mode);
+  const int policy = g_policy.load();
+  if (depthwise) {
+    if (kh != 3 || x->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
+    return run_depthwise(x, w, ep, stride, pad, y, s);
+  }
+  const bool tc_ok = policy != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && x->c >= 16 && aligned16(x->data) &&
+                     aligned16(w) && strides_mult4(x) && x->n <= 65535 && x->w <= 65535 && x->h <= 65535 &&
+                     encode_tiled() && encode_im2col();
+  if (tc_ok) return run_igemm(x, w, ep, kh, stride, pad, y, s);
+  return run_direct(x, w, ep, kh, stride, pad, y, s);
+}
+
+cb_status cb_dw_separable_block_workspace(const cb_tensor* x, int c_out, int stride, size_t* bytes) {
+  if (!view_ok(x) || !bytes || c_out < 1 || (stride != 1 && stride != 2)) return CB_ERR_INVALID_ARG;
+  const long long OH = (x->h + 2 - 3) / stride + 1, OW = (x->w + 2 - 3) / stride + 1;
+  if (x->h < 1 || x->w < 1 || OH < 1 || OW < 1) return CB_ERR_INVALID_ARG;
+  const long long pix = static_cast<long long>(x->n) * OH * OW;
+  const size_t t_bytes = (static_cast<size_t>(pix) * x->c * sizeof(float) + 255) & ~size_t(255);
+  const size_t s_bytes = (static_cast<size_t>(pix) * c_out * sizeof(float) + 255) & ~size_t(255);
+  *bytes = t_bytes + s_bytes;
+  return CB_OK;
+}
+
+cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const float* dw_scale, const float* dw_bias,
+                                const float* pw_w, const float* pw_scale, const float* pw_bias, const float* skip_w,
+                                const float* skip_scale, const float* skip_bias, int stride, cb_tensor* y,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!view_ok(x) || !view_ok(y) || !dw_w || !dw_scale || !dw_bias || !pw_w || !pw_scale || !pw_bias)
+    return CB_ERR_INVALID_ARG;
+  if (x->layout != CB_LAYOUT_NHWC || y->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
+  if (stride != 1 && stride != 2) return CB_ERR_UNSUPPORTED;
+  const int Ci = x->c, Co = y->c;
+  const int OH = (x->h - 1) / stride + 1, OW = (x->w - 1) / stride + 1;
+  if (y->n != x->n || y->h != OH || y->w != OW) return CB_ERR_INVALID_ARG;
+  if (skip_w && (!skip_scale || !skip_bias)) return CB_ERR_INVALID_ARG;
+  if (!skip_w && (stride != 1 || Ci != Co)) return CB_ERR_INVALID_ARG;
+  if (overlap(x, y)) return CB_ERR_INVALID_ARG;
+  size_t need = 0;
+  cb_status st = cb_dw_separable_block_workspace(x, Co, stride, &need);
+  if (st != CB_OK) return st;
+  if (x->n == 0) return CB_OK;
+  if (!workspace || workspace_bytes < need) return CB_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CB_ERR_ALIGNMENT;
+
+  const long long pix = static_cast<long long>(x->n) * OH * OW;
+  const size_t t_bytes = (static_cast<size_t>(pix) * Ci * sizeof(float) + 255) & ~size_t(255);
+  cb_tensor t{workspace, x->n, OH, OW, Ci, static_cast<long long>(OH) * OW * Ci, static_cast<long long>(OW) * Ci,
+              Ci, 1, CB_LAYOUT_NHWC};
+  cb_tensor sk{static_cast<char*>(workspace) + t_bytes, x->n, OH, OW, Co, static_cast<long long>(OH) * OW * Co,
+               static_cast<long long>(OW) * Co, Co, 1, CB_LAYOUT_NHWC};
+  st = cb_conv_bn_act(x, dw_w, dw_scale, dw_bias, 3, 3, stride, 1, Ci, CB_ACT_RELU, nullptr, CB_RES_NONE, &t,
+                      stream);
+  if (st != CB_OK) return st;
+  const cb_tensor* r = x;
+  if (skip_w) {
+    st = cb_conv_bn_act(x, skip_w, skip_scale, skip_bias, 1, 1, stride, 0, 1, CB_ACT_NONE, nullptr, CB_RES_NONE, &sk,
+                        stream);
+    if (st != CB_OK) return st;
+    r = &sk;
+  }
+  return cb_conv_bn_act(&t, pw_w, pw_scale, pw_bias, 1, 1, 1, 0, 1, CB_ACT_RELU, r, CB_RES_PRE_ACT, y, stream);
+}
+
+cb_status cb_avgpool_linear(const cb_tensor* x, const float* fc_w, const float* fc_b, int out_features, float* out,
+                            void* stream) {
+  if (!view_ok(x) || x->layout != CB_LAYOUT_NHWC || !fc_w || !fc_b || !out || out_features < 1)
+    return CB_ERR_INVALID_ARG;
+  if (x->c > 12 * 1024) return CB_ERR_UNSUPPORTED;
+  if (x->n == 0) return CB_OK;
+  PoolFcArgs a{};
+  a.x = static_cast<const float*>(x->data);
+  a.xs_n = x->stride_n;
+  a.xs_h = x->stride_h;
+  a.xs_w = x->stride_w;
+  a.N = x->n;
+  a.H = x->h;
+  a.W = x->w;
+  a.C = x->c;
+  a.out_features = out_features;
+  a.fc_w = fc_w;
+  a.fc_b = fc_b;
+  a.out = out;
+  cudaError_t e = launch_pool_fc(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+static cb_status check_preprocess(const unsigned char* src, int n, int src_h, int src_w, long long src_pitch,
+                                  const float* dst, int dst_h, int dst_w) {
+  if (!src || !dst || n < 0 || src_h < 1 || src_w < 1 || dst_h < 1 || dst_w < 1) return CB_ERR_INVALID_ARG;
+  if (src_pitch < 3LL * src_w) return CB_ERR_INVALID_ARG;
+  if (2LL * ((3LL * src_w + 15) & ~15LL) > 200 * 1024) return CB_ERR_UNSUPPORTED;
+  if (dst_h > 65535 || n > 65535) return CB_ERR_UNSUPPORTED;
+  return CB_OK;
+}
+
+cb_status cb_preprocess_u8(const unsigned char* src, int n, int src_h, int src_w, long long src_pitch, float* dst,
+                           int dst_h, int dst_w, void* stream) {
+  cb_status st = check_preprocess(src, n, src_h, src_w, src_pitch, dst, dst_h, dst_w);
+  if (st != CB_OK) return st;
+  cudaError_t e = launch_preprocess_fused(src, n, src_h, src_w, src_pitch, dst, dst_h, dst_w,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+cb_status cb_preprocess_u8_three_pass(const unsigned char* src, int n, int src_h, int src_w, long long src_pitch,
+                                      unsigned char* tmp_u8, float* tmp_f32, float* dst, int dst_h, int dst_w,
+                                      void* stream) {
+  cb_status st = check_preprocess(src, n, src_h, src_w, src_pitch, dst, dst_h, dst_w);
+  if (st != CB_OK) return st;
+  if (!tmp_u8 || !tmp_f32) return CB_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_preprocess_resize(src, n, src_h, src_w, src_pitch, tmp_u8, dst_h, dst_w, s);
+  if (e == cudaSuccess) e = launch_preprocess_normalize(tmp_u8, static_cast<long long>(n) * dst_h * dst_w * 3, tmp_f32, s);
+  if (e == cudaSuccess) e = launch_preprocess_layout(tmp_f32, n, dst_h, dst_w, dst, s);
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+cb_status cb_get_device_error(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  int v = 0;
+  e = cudaMemcpy(&v, dev->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpy(dev->err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return static_cast<cb_status>(v);
+  }
+  return CB_OK;
+}
+
+int cb_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* cb_status_string(cb_status s) {
+  switch (s) {
+    case CB_OK: return "CB_OK";
+    case CB_ERR_INVALID_ARG: return "CB_ERR_INVALID_ARG";
+    case CB_ERR_UNSUPPORTED: return "CB_ERR_UNSUPPORTED";
+    case CB_ERR_ALIGNMENT: return "CB_ERR_ALIGNMENT";
+    case CB_ERR_CUDA: return "CB_ERR_CUDA";
+    case CB_ERR_TIMEOUT: return "CB_ERR_TIMEOUT";
+    case CB_ERR_WORKSPACE: return "CB_ERR_WORKSPACE";
+  }
+  return "CB_ERR_UNKNOWN";
+}
+
+int cb_version(void) { return kVersion; }
+
+cb_status cb_set_kernel_policy(int policy) {
+  if (policy < 0 || policy > 1) return CB_ERR_INVALID_ARG;
+  g_policy.store(policy);
+  return CB_OK;
+}
+
+}  // extern "C"

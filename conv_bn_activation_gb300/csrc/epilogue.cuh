@@ -1,0 +1,37 @@
+// The fused per-channel epilogue: folded BatchNorm (scale, bias), optional
+// residual before or after the activation, ReLU or SiLU.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace cb {
+
+__device__ __forceinline__ float act_apply(float z, int act) {
+  if (act == 1) return fmaxf(z, 0.0f);
+  if (act == 2) return z / (1.0f + expf(-z));
+  return z;
+}
+
+__device__ __forceinline__ float epi_apply(float acc, float sc, float bi, float r, int act, int res_mode) {
+  float z = fmaf(acc, sc, bi);
+  if (res_mode == 1) z += r;
+  z = act_apply(z, act);
+  if (res_mode == 2) z += r;
+  return z;
+}
+
+__device__ __forceinline__ float4 epi_apply4(float4 acc, float4 sc, float4 bi, float4 r, int act, int res_mode) {
+  return make_float4(epi_apply(acc.x, sc.x, bi.x, r.x, act, res_mode), epi_apply(acc.y, sc.y, bi.y, r.y, act, res_mode),
+                     epi_apply(acc.z, sc.z, bi.z, r.z, act, res_mode), epi_apply(acc.w, sc.w, bi.w, r.w, act, res_mode));
+}
+
+__device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+
+__device__ __forceinline__ void fma4(float4& acc, float4 a, float4 b) {
+  acc.x = fmaf(a.x, b.x, acc.x);
+  acc.y = fmaf(a.y, b.y, acc.y);
+  acc.z = fmaf(a.z, b.z, acc.z);
+  acc.w = fmaf(a.w, b.w, acc.w);
+}
+
+}  // namespace cb

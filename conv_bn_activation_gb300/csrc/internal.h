@@ -1,0 +1,105 @@
+// Internal launch interfaces between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace cb {
+
+// Per-channel epilogue shared by every conv kernel:
+//   z = acc * scale[c] + bias[c];  z += r (pre);  z = act(z);  z += r (post)
+struct Epilogue {
+  const float* scale;
+  const float* bias;
+  int act;       // 0 none, 1 relu, 2 silu
+  int res_mode;  // 0 none, 1 pre-act, 2 post-act
+  const float* r;
+  long long rs_n, rs_h, rs_w;  // residual strides (elements, c stride 1)
+};
+
+struct OutView {
+  float* y;
+  long long ys_n, ys_h, ys_w;  // c stride 1
+};
+
+// ------------------------------------------------------------ depthwise 3x3
+struct DwArgs {
+  const float* x;
+  long long xs_n, xs_h, xs_w;  // NHWC, c stride 1
+  const float* w;              // [3][3][C]
+  int N, H, W, C, OH, OW, stride, pad;
+  OutView out;
+  Epilogue ep;
+};
+// Plain CUDA-core kernel: one thread per (output pixel, 4 or 1 channels).
+cudaError_t launch_dw_simple(const DwArgs& a, bool vec4, cudaStream_t s);
+
+// TMA-fed kernel: persistent CTAs stream input rows (32-channel chunks,
+// full padded width) through a shared-memory ring; 3x3 windows slide down
+// the rows in registers.
+struct DwTmaPlan {
+  int rows_per_item;  // output rows per work item
+  int num_items;
+  int box_w;          // input columns per row copy (includes the halo)
+  int stages;
+  int grid;
+  int consumer_warps;
+  size_t smem_bytes;
+};
+cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaPlan& plan, int* err,
+                          uint64_t timeout_ns, cudaStream_t s);
+
+// ---------------------------------------------------------- direct (CUDA core)
+struct DirectArgs {
+  const float* x;
+  long long xs_n, xs_h, xs_w, xs_c;  // any layout
+  const float* w;                    // OHWI [Co][kh][kw][Ci]
+  int N, H, W, Ci, Co, OH, OW, kh, kw, stride, pad;
+  OutView out;
+  Epilogue ep;
+};
+cudaError_t launch_direct(const DirectArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------- implicit GEMM (tcgen05)
+struct IgemmArgs {
+  int M;         // N*OH*OW output pixels
+  int OHW, OW;   // OH*OW, OW
+  int Cout;
+  int kw, taps;  // filter width, kh*kw
+  int num_kc;    // ceil(Cin / 32)
+  int k_iters;   // taps * num_kc
+  int m_tiles, n_tiles;
+  int stride, pad;
+  int stages;
+  int vec_store;  // 1 when y / r rows allow 16-byte vector access
+  OutView out;
+  Epilogue ep;
+  int* err;
+  uint64_t timeout_ns;
+};
+cudaError_t launch_igemm(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int bn,
+                         int grid, size_t smem_bytes, cudaStream_t s);
+size_t igemm_smem_bytes(int bn, int stages);
+int igemm_stages(int bn);
+
+// -------------------------------------------------------------- preprocess
+cudaError_t launch_preprocess_fused(const uint8_t* src, int n, int hs, int ws, long long pitch, float* dst,
+                                    int hd, int wd, cudaStream_t s);
+cudaError_t launch_preprocess_resize(const uint8_t* src, int n, int hs, int ws, long long pitch,
+                                     uint8_t* out, int hd, int wd, cudaStream_t s);
+cudaError_t launch_preprocess_normalize(const uint8_t* in, long long count, float* out, cudaStream_t s);
+cudaError_t launch_preprocess_layout(const float* in, int n, int h, int w, float* out, cudaStream_t s);
+
+// ----------------------------------------------------------------- pool + fc
+struct PoolFcArgs {
+  const float* x;
+  long long xs_n, xs_h, xs_w;
+  int N, H, W, C, out_features;
+  const float* fc_w;
+  const float* fc_b;
+  float* out;
+};
+cudaError_t launch_pool_fc(const PoolFcArgs& a, cudaStream_t s);
+
+}  // namespace cb

@@ -1,0 +1,163 @@
+"""Layer objects and the three network chains, built from C-ABI calls.
+
+A layer folds its BatchNorm and repacks its weights once (cb_fold_bn,
+cb_repack_weights on the host), uploads them, and then every forward is one
+cb_* call on preallocated device buffers, so a whole chain can be captured
+in a CUDA graph (the pages' runtimes replay their inference as a graph; the
+tiny MNIST layers are launch-bound without it).
+
+  * MnistNet -- DepthwiseMNIST ("How I sped up convolutions", class listing):
+    stem conv3x3 1->48 + BN + ReLU, four DepthwiseSeparableConv blocks,
+    global average pool + fc 192->10.
+  * YoloChain -- five stages of conv3x3 s2 -> 1x1 (C->C/2) -> 3x3 (C/2->C/2)
+    -> 1x1 over the channel concat [a | b], post-activation residual; all
+    conv + BN + SiLU.  The concat is fused on the producer side: the two
+    branch convs write into the two channel halves of one NHWC buffer
+    ("YOLO26N Inference Optimisation", improvement #6).
+  * PreprocessStem -- fused u8 preprocess to planar fp32, then the stem conv
+    3x3 s2 3->16 + BN + SiLU reading the planar tensor directly.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as cb
+from .synthetic import MNIST_BLOCKS
+from .workloads import out_size
+
+
+def _dev(a, device):
+    return torch.from_numpy(a).to(device)
+
+
+class ConvBnAct:
+    def __init__(self, w_oihw, bn, stride, pad, act, groups=1, device="cuda", eps=1e-5):
+        scale, bias = cb.fold_bn(*bn, eps=eps)
+        self.w = _dev(cb.repack_weights(w_oihw, groups), device).contiguous()
+        self.scale = _dev(scale, device)
+        self.bias = _dev(bias, device)
+        self.cout, cin_g, self.k, _ = w_oihw.shape
+        self.cin = cin_g * groups
+        self.stride, self.pad, self.act, self.groups = stride, pad, act, groups
+
+    def out_hw(self, h, w):
+        return out_size(h, self.k, self.stride, self.pad), out_size(w, self.k, self.stride, self.pad)
+
+    def __call__(self, x, y, residual=None, res_mode=cb.RES_NONE, stream=None, x_layout=cb.LAYOUT_NHWC):
+        return cb.conv_bn_act(x, self.w, self.scale, self.bias, self.k, self.stride, self.pad, self.groups, self.act,
+                              y, residual=residual, res_mode=res_mode, stream=stream, x_layout=x_layout)
+
+
+class DwBlock:
+    """DepthwiseSeparableConv on device, run through cb_dw_separable_block."""
+
+    def __init__(self, p, cin, cout, stride, device="cuda"):
+        self.cin, self.cout, self.stride = cin, cout, stride
+        dws, dwb = cb.fold_bn(*p["bn1"])
+        pws, pwb = cb.fold_bn(*p["bn2"])
+        self.params = {
+            "dw_w": _dev(cb.repack_weights(p["dw_w"], groups=cin), device),
+            "dw_scale": _dev(dws, device), "dw_bias": _dev(dwb, device),
+            "pw_w": _dev(cb.repack_weights(p["pw_w"]), device),
+            "pw_scale": _dev(pws, device), "pw_bias": _dev(pwb, device),
+        }
+        if "skip_w" in p:
+            sks, skb = cb.fold_bn(*p["skip_bn"])
+            self.params.update({"skip_w": _dev(cb.repack_weights(p["skip_w"]), device),
+                                "skip_scale": _dev(sks, device), "skip_bias": _dev(skb, device)})
+
+    def __call__(self, x, y, workspace, stream=None):
+        return cb.dw_separable_block(x, self.params, self.stride, y, workspace, stream=stream)
+
+
+class MnistNet:
+    def __init__(self, params, batch, device="cuda"):
+        self.batch = batch
+        self.stem = ConvBnAct(params["stem_w"], params["stem_bn"], 1, 1, cb.ACT_RELU, device=device)
+        self.blocks = []
+        acts = [torch.empty(batch, 28, 28, 48, device=device)]
+        H = 28
+        ws = 0
+        for blk, (cin, cout, s) in zip(params["blocks"], MNIST_BLOCKS):
+            self.blocks.append(DwBlock(blk, cin, cout, s, device))
+            ws = max(ws, cb.dw_separable_block_workspace(acts[-1], cout, s))
+            H = out_size(H, 3, s, 1)
+            acts.append(torch.empty(batch, H, H, cout, device=device))
+        self.acts = acts
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.fc_w = _dev(params["fc_w"], device)
+        self.fc_b = _dev(params["fc_b"], device)
+        self.logits = torch.empty(batch, 10, device=device)
+
+    def forward(self, x, stream=None):
+        self.stem(x, self.acts[0], stream=stream)
+        for i, blk in enumerate(self.blocks):
+            blk(self.acts[i], self.acts[i + 1], self.workspace, stream=stream)
+        cb.avgpool_linear(self.acts[-1], self.fc_w, self.fc_b, self.logits, stream=stream)
+        return self.logits
+
+    launches_per_forward = 1 + 2 + 3 + 2 + 3 + 2 + 1  # stem, blocks (dw, [skip], pw), pool+fc
+
+
+class YoloChain:
+    def __init__(self, stages, batch, size=640, device="cuda"):
+        self.batch = batch
+        self.layers = []
+        self.bufs = []
+        H = size
+        for st in stages:
+            c = st["down_w"].shape[0]
+            h = c // 2
+            OH = out_size(H, 3, 2, 1)
+            L = {
+                "down": ConvBnAct(st["down_w"], st["down_bn"], 2, 1, cb.ACT_SILU, device=device),
+                "cv1": ConvBnAct(st["cv1_w"], st["cv1_bn"], 1, 0, cb.ACT_SILU, device=device),
+                "cv2": ConvBnAct(st["cv2_w"], st["cv2_bn"], 1, 1, cb.ACT_SILU, device=device),
+                "cv3": ConvBnAct(st["cv3_w"], st["cv3_bn"], 1, 0, cb.ACT_SILU, device=device),
+            }
+            B = {"x1": torch.empty(batch, OH, OH, c, device=device),
+                 "cat": torch.empty(batch, OH, OH, c, device=device),
+                 "out": torch.empty(batch, OH, OH, c, device=device), "half": h}
+            self.layers.append(L)
+            self.bufs.append(B)
+            H = OH
+
+    def forward(self, x, stream=None):
+        h = x
+        for L, B in zip(self.layers, self.bufs):
+            half = B["half"]
+            L["down"](h, B["x1"], stream=stream)
+            a = B["cat"][..., :half]
+            b = B["cat"][..., half:]
+            L["cv1"](B["x1"], a, stream=stream)
+            L["cv2"](a, b, stream=stream)
+            L["cv3"](B["cat"], B["out"], residual=B["x1"], res_mode=cb.RES_POST_ACT, stream=stream)
+            h = B["out"]
+        return h
+
+    launches_per_forward = 20
+
+
+class PreprocessStem:
+    def __init__(self, stem_w, stem_bn, batch, src_hw=(720, 1280), dst_hw=(480, 640), device="cuda"):
+        self.batch = batch
+        self.src_hw, self.dst_hw = src_hw, dst_hw
+        self.stem = ConvBnAct(stem_w, stem_bn, 2, 1, cb.ACT_SILU, device=device)
+        Hd, Wd = dst_hw
+        self.planar = torch.empty(batch, 3, Hd, Wd, device=device)
+        OH, OW = self.stem.out_hw(Hd, Wd)
+        self.out = torch.empty(batch, OH, OW, 16, device=device)
+        self.tmp_u8 = None
+        self.tmp_f32 = None
+
+    def forward(self, frames, stream=None, three_pass=False):
+        if three_pass:
+            if self.tmp_u8 is None:
+                Hd, Wd = self.dst_hw
+                self.tmp_u8 = torch.empty(self.batch, Hd, Wd, 3, dtype=torch.uint8, device=frames.device)
+                self.tmp_f32 = torch.empty(self.batch, Hd, Wd, 3, device=frames.device)
+            cb.preprocess_u8_three_pass(frames, self.tmp_u8, self.tmp_f32, self.planar, stream=stream)
+        else:
+            cb.preprocess_u8(frames, self.planar, stream=stream)
+        self.stem(self.planar, self.out, stream=stream, x_layout=cb.LAYOUT_NCHW)
+        return self.out

@@ -1,0 +1,207 @@
+/*
+ * cb.h -- C ABI of the fused convolution + BatchNorm + activation library
+ * for one GB300 GPU (sm_103a).
+ *
+ * The operation ("YOLO26N Inference Optimisation": nsys breakdown and
+ * improvement #7; "How I sped up convolutions": the Metal kernel walk-through,
+ * steps 1-5) is
+ *
+ *     y = act( scale[c] * conv(x, w)[n,oh,ow,c] + bias[c]  (+ r, pre-act) )  (+ r, post-act)
+ *
+ * where (scale, bias) is inference BatchNorm folded per output channel,
+ * act is identity, ReLU = max(0, z) or SiLU = z / (1 + exp(-z)).
+ *
+ * Conventions for every entry point:
+ *  - All memory is owned by the caller.  Tensor and weight pointers are
+ *    DEVICE pointers unless the argument says "host".  The library never
+ *    allocates device memory and never synchronises inside the compute calls
+ *    (cb_get_device_error is the one call that synchronises).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued asynchronously on it.
+ *  - Arguments are validated on the host before anything is launched.  Bad
+ *    pointers/shapes return CB_ERR_INVALID_ARG, shapes outside the supported
+ *    set CB_ERR_UNSUPPORTED, misaligned data CB_ERR_ALIGNMENT.  A failed
+ *    launch returns CB_ERR_CUDA (cb_last_cuda_error() gives the cudaError_t).
+ *  - Kernels that wait on barriers give up after a bounded time, record
+ *    CB_ERR_TIMEOUT in a device error word and return; cb_get_device_error()
+ *    reports and clears it.
+ *  - Activations are fp32.  Layout is NHWC (channel-last) unless a tensor
+ *    says CB_LAYOUT_NCHW.  Output rows may be padded: y->stride_h may exceed
+ *    y->w * y->stride_w; padding columns are never written (the OW tail of
+ *    the last tile is masked -- "YOLO26N Inference Optimisation", Bug fixed:
+ *    TMA overflow).
+ */
+#ifndef CB_H_
+#define CB_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CB_OK = 0,
+  CB_ERR_INVALID_ARG = 1,
+  CB_ERR_UNSUPPORTED = 2,
+  CB_ERR_ALIGNMENT = 3,
+  CB_ERR_CUDA = 4,
+  CB_ERR_TIMEOUT = 5,
+  CB_ERR_WORKSPACE = 6
+} cb_status;
+
+typedef enum { CB_ACT_NONE = 0, CB_ACT_RELU = 1, CB_ACT_SILU = 2 } cb_act;
+
+/* Where the residual r enters: act(z + r) or act(z) + r. */
+typedef enum { CB_RES_NONE = 0, CB_RES_PRE_ACT = 1, CB_RES_POST_ACT = 2 } cb_res_mode;
+
+typedef enum { CB_LAYOUT_NHWC = 0, CB_LAYOUT_NCHW = 1 } cb_layout;
+
+/*
+ * A 4-D fp32 activation tensor view.  Logical dims (n, h, w, c); element
+ * (n, h, w, c) lives at data + n*stride_n + h*stride_h + w*stride_w + c*stride_c
+ * (strides in ELEMENTS).  NHWC views need stride_c == 1; NCHW views need
+ * stride_w == 1.  A channel slice of a wider buffer (the producer side of a
+ * channel concat -- "YOLO26N Inference Optimisation", improvement #6) is a
+ * view whose data pointer is offset by the first channel and whose strides
+ * are the wide buffer's.
+ */
+typedef struct {
+  void* data;
+  int n, h, w, c;
+  long long stride_n, stride_h, stride_w, stride_c;
+  cb_layout layout;
+} cb_tensor;
+
+/*
+ * Fold inference BatchNorm into a per-channel affine map ("YOLO26N Inference
+ * Optimisation": baseline section, weight folding; "How I sped up
+ * convolutions": Metal kernel step 4):
+ *     scale[c] = gamma[c] / sqrt(var[c] + eps),  bias[c] = beta[c] - mean[c] * scale[c]
+ * computed in fp64 and stored as fp32.  All pointers are HOST pointers to C
+ * floats.  Returns CB_ERR_INVALID_ARG for NULL pointers, C <= 0, eps < 0 or
+ * var[c] + eps <= 0.
+ */
+cb_status cb_fold_bn(const float* gamma, const float* beta, const float* mean, const float* var,
+                     float eps, int C, float* scale, float* bias);
+
+/*
+ * Repack PyTorch OIHW conv weights [Co, Ci_per_group, kh, kw] (HOST) into the
+ * layout the kernels read (HOST output, Co*Ci_per_group*kh*kw floats):
+ *   groups == 1:                    OHWI [Co, kh, kw, Ci]  (K = kh*kw*Ci contiguous per
+ *                                   output channel -- "YOLO26N Inference Optimisation",
+ *                                   NHWC migration: weight layout);
+ *   groups == Co, Ci_per_group == 1 (depthwise): [kh, kw, C]  (channel-contiguous per tap).
+ * A pure permutation (bit-exact).  Other groupings: CB_ERR_UNSUPPORTED.
+ */
+cb_status cb_repack_weights(const float* w_oihw, int Co, int Ci_per_group, int kh, int kw,
+                            int groups, float* w_out);
+
+/*
+ * The fused layer.  x: input view (NHWC, or NCHW for the small-channel stem
+ * path); w: DEVICE weights in the cb_repack_weights layout; scale/bias:
+ * DEVICE fp32 [Co] from cb_fold_bn; kernel kh x kw (1 or 3), stride 1 or 2,
+ * zero padding `pad`; groups 1 (dense) or x->c (depthwise, then y->c == x->c).
+ * y: output view, NHWC, y->n == x->n, y->h == (x->h + 2*pad - kh)/stride + 1,
+ * y->w likewise, y->c == Co.  residual: NULL or an NHWC view with y's dims,
+ * added per res_mode.  x and y must not overlap; residual may alias y only
+ * element for element (in-place residual add).
+ *
+ * Paths (chosen on the host from the shape): dense layers with Ci % 4 == 0
+ * and Ci >= 16 run as an implicit GEMM on the tcgen05 tensor cores (TF32
+ * inputs, fp32 accumulate; needs 16-byte aligned x/w and strides that are
+ * multiples of 4 elements); depthwise 3x3 layers run on a channel-vectorised
+ * CUDA-core kernel; everything else (stems with 1 or 3 input channels, NCHW
+ * input, odd channel counts) runs on a direct CUDA-core kernel in fp32.
+ */
+cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale, const float* bias,
+                         int kh, int kw, int stride, int pad, int groups, cb_act act,
+                         const cb_tensor* residual, cb_res_mode res_mode, cb_tensor* y,
+                         void* stream);
+
+/*
+ * Workspace bytes cb_dw_separable_block needs for input x, Co output
+ * channels and the given stride (written to *bytes).
+ */
+cb_status cb_dw_separable_block_workspace(const cb_tensor* x, int c_out, int stride, size_t* bytes);
+
+/*
+ * One DepthwiseSeparableConv block ("How I sped up convolutions", class
+ * listing): with Ci = x->c, Co = y->c,
+ *     t = relu(dw_scale * dw3x3_stride(x) + dw_bias)          (pad 1, groups Ci)
+ *     u = pw_scale * pw1x1(t) + pw_bias
+ *     s = skip_scale * skip1x1_stride(x) + skip_bias          if skip_w != NULL
+ *       = x                                                    otherwise (needs stride 1, Ci == Co)
+ *     y = relu(u + s)
+ * dw_w: DEVICE [3, 3, Ci]; pw_w / skip_w: DEVICE OHWI [Co, 1, 1, Ci]; scales
+ * and biases DEVICE fp32.  workspace: DEVICE scratch of at least
+ * cb_dw_separable_block_workspace() bytes, 256-byte aligned; it holds t (and
+ * s) and is overwritten.  Returns CB_ERR_WORKSPACE if it is too small.
+ */
+cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const float* dw_scale,
+                                const float* dw_bias, const float* pw_w, const float* pw_scale,
+                                const float* pw_bias, const float* skip_w, const float* skip_scale,
+                                const float* skip_bias, int stride, cb_tensor* y, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * Global average pool then linear layer (the DepthwiseMNIST head, "How I sped
+ * up convolutions", class listing): out[n, o] = sum_c mean_hw(x[n,:,:,c]) *
+ * fc_w[o, c] + fc_b[o].  x: NHWC view; fc_w DEVICE [out_features, x->c]
+ * row-major; fc_b DEVICE [out_features]; out DEVICE [x->n, out_features].
+ */
+cb_status cb_avgpool_linear(const cb_tensor* x, const float* fc_w, const float* fc_b,
+                            int out_features, float* out, void* stream);
+
+/*
+ * The fused u8 frame preprocess ("A fused Ampere preprocess kernel", path B):
+ * reads each u8 HWC frame once, bilinear-resizes with half-pixel centres
+ * (f = (d + 0.5) * S/D - 0.5, clamped at the borders), rounds the value half
+ * up to u8, divides by 255 and writes fp32 planar NCHW once.
+ * src: DEVICE u8, n frames of src_h rows, row pitch src_pitch bytes
+ * (>= 3 * src_w), frame pitch src_h * src_pitch; dst: DEVICE fp32
+ * [n, 3, dst_h, dst_w] contiguous.  Coordinates and the bilinear value are
+ * evaluated in IEEE fp32 in the order written above (no fused multiply-add).
+ */
+cb_status cb_preprocess_u8(const unsigned char* src, int n, int src_h, int src_w, long long src_pitch,
+                           float* dst, int dst_h, int dst_w, void* stream);
+
+/*
+ * The same preprocess as three passes ("A fused Ampere preprocess kernel",
+ * path A: resize -> normalize -> layout), for comparison.  tmp_u8: DEVICE
+ * [n, dst_h, dst_w, 3] u8; tmp_f32: DEVICE [n, dst_h, dst_w, 3] fp32; dst as
+ * cb_preprocess_u8.  Produces bit-identical output to cb_preprocess_u8.
+ */
+cb_status cb_preprocess_u8_three_pass(const unsigned char* src, int n, int src_h, int src_w,
+                                      long long src_pitch, unsigned char* tmp_u8, float* tmp_f32,
+                                      float* dst, int dst_h, int dst_w, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error
+ * word: CB_ERR_TIMEOUT if a kernel gave up waiting on a barrier since the
+ * last call, CB_ERR_CUDA if the stream reported an error, else CB_OK.
+ */
+cb_status cb_get_device_error(void* stream);
+
+/* The cudaError_t (as int) of the last CB_ERR_CUDA returned on this thread. */
+int cb_last_cuda_error(void);
+
+/*
+ * Process-wide kernel choice.  0 (the default) picks the fastest eligible
+ * kernel for each shape; 1 restricts every layer to the plain CUDA-core
+ * kernels (direct convolution, simple depthwise), a cross-check of the
+ * TMA / tensor-core paths.  Returns CB_OK, or CB_ERR_INVALID_ARG.
+ */
+cb_status cb_set_kernel_policy(int policy);
+
+/* A static string naming a status code. */
+const char* cb_status_string(cb_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int cb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CB_H_ */

@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI (CPU only: no kernel is launched).
+
+The library must load and export every entry point include/cb.h declares;
+the host helpers (BN folding, weight repacking) are checked against the
+oracle and numpy; invalid arguments are rejected before any launch.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "cb.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(cb_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(cblib):
+    lib = cblib.load()
+    names = _declared()
+    assert "cb_conv_bn_act" in names and "cb_preprocess_u8" in names and "cb_fold_bn" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(cblib.EXPORTED)
+    assert cblib.version() >= 100
+
+
+def test_status_strings(cblib):
+    assert cblib.status_string(cblib.OK) == "CB_OK"
+    assert cblib.status_string(cblib.ERR_TIMEOUT) == "CB_ERR_TIMEOUT"
+
+
+def test_fold_bn_matches_unfolded_oracle(cblib, orc):
+    """Folded (scale, bias) applied to z equals the oracle's unfolded BN to fp32 rounding."""
+    g = np.random.default_rng(0)
+    C = 37
+    gamma, var = g.uniform(0.5, 1.5, C).astype(np.float32), g.uniform(0.5, 1.5, C).astype(np.float32)
+    beta, mean = (g.standard_normal(C) * 0.1).astype(np.float32), (g.standard_normal(C) * 0.1).astype(np.float32)
+    scale, bias = cblib.fold_bn(gamma, beta, mean, var, 1e-5)
+    z = g.standard_normal((50, C)) * 3
+    folded = z * scale.astype(np.float64) + bias.astype(np.float64)
+    unfolded = orc.batchnorm(z, gamma, beta, mean, var, 1e-5)
+    # only the fp32 storage of (scale, bias) separates them
+    assert np.max(np.abs(folded - unfolded)) < 4e-7 * (np.max(np.abs(unfolded)) + 1)
+
+
+def test_fold_bn_rejects_bad_args(cblib):
+    lib = cblib.load()
+    v = np.ones(4, np.float32)
+    out = np.empty(4, np.float32)
+    neg = np.full(4, -1.0, np.float32)
+    assert lib.cb_fold_bn(v.ctypes.data, v.ctypes.data, v.ctypes.data, neg.ctypes.data, ctypes.c_float(1e-5), 4,
+                          out.ctypes.data, out.ctypes.data) == cblib.ERR_INVALID_ARG
+    assert lib.cb_fold_bn(None, v.ctypes.data, v.ctypes.data, v.ctypes.data, ctypes.c_float(1e-5), 4,
+                          out.ctypes.data, out.ctypes.data) == cblib.ERR_INVALID_ARG
+    assert lib.cb_fold_bn(v.ctypes.data, v.ctypes.data, v.ctypes.data, v.ctypes.data, ctypes.c_float(1e-5), 0,
+                          out.ctypes.data, out.ctypes.data) == cblib.ERR_INVALID_ARG
+
+
+def test_repack_is_exact_permutation(cblib):
+    g = np.random.default_rng(1)
+    w = g.standard_normal((6, 5, 3, 3)).astype(np.float32)
+    np.testing.assert_array_equal(cblib.repack_weights(w), w.transpose(0, 2, 3, 1))
+    wd = g.standard_normal((7, 1, 3, 3)).astype(np.float32)
+    np.testing.assert_array_equal(cblib.repack_weights(wd, groups=7), wd[:, 0].transpose(1, 2, 0))
+    w1 = g.standard_normal((4, 8, 1, 1)).astype(np.float32)
+    np.testing.assert_array_equal(cblib.repack_weights(w1).reshape(4, 8), w1[:, :, 0, 0])
+    with pytest.raises(cblib.CbError):
+        cblib.repack_weights(g.standard_normal((8, 2, 3, 3)).astype(np.float32), groups=4)
+
+
+def _view(data, n, h, w, c, layout=0):
+    if layout == 0:
+        return __import__("conv_bn_activation_gb300").binding.CbTensor(data, n, h, w, c, h * w * c, w * c, c, 1, 0)
+    return __import__("conv_bn_activation_gb300").binding.CbTensor(data, n, h, w, c, c * h * w, w, 1, h * w, 1)
+
+
+def test_conv_rejects_invalid_arguments_before_launch(cblib):
+    lib = cblib.load()
+    T = ctypes.byref
+    base = 1 << 20  # fake, never dereferenced: validation fails first
+    x = _view(base, 1, 8, 8, 16)
+    y_ok = _view(base + (1 << 16), 1, 8, 8, 16)
+    w = s = b = base + (1 << 18)
+    call = lambda xv, yv, k=3, st=1, p=1, g=1, act=0, r=None, rm=0: lib.cb_conv_bn_act(
+        T(xv), w, s, b, k, k, st, p, g, act, T(r) if r is not None else None, rm, T(yv), None)
+    assert call(x, _view(base + (1 << 16), 1, 7, 8, 16)) == cblib.ERR_INVALID_ARG        # wrong OH
+    assert call(x, y_ok, k=5, p=2) == cblib.ERR_UNSUPPORTED                             # 5x5
+    assert call(x, y_ok, st=3) == cblib.ERR_UNSUPPORTED                                 # stride 3
+    assert call(x, y_ok, g=4) == cblib.ERR_UNSUPPORTED                                  # groups 4
+    assert call(x, y_ok, act=7) == cblib.ERR_INVALID_ARG                                # bad act
+    assert call(x, y_ok, rm=1) == cblib.ERR_INVALID_ARG                                 # residual missing
+    assert call(x, _view(base + 64, 1, 8, 8, 16)) == cblib.ERR_INVALID_ARG              # x / y overlap
+    assert call(x, y_ok, r=_view(base + (1 << 16) + 4, 1, 8, 8, 16), rm=1) == cblib.ERR_INVALID_ARG  # r partly on y
+    bad = _view(base, 1, 8, 8, 16)
+    bad.stride_c = 2
+    assert call(bad, y_ok) == cblib.ERR_INVALID_ARG                                     # NHWC needs unit c stride
+    assert lib.cb_conv_bn_act(T(x), None, s, b, 3, 3, 1, 1, 1, 0, None, 0, T(y_ok), None) == cblib.ERR_INVALID_ARG
+    # empty batch: valid, nothing to do, no launch
+    assert call(_view(base, 0, 8, 8, 16), _view(base + (1 << 16), 0, 8, 8, 16)) == cblib.OK
+
+
+def test_block_and_preprocess_validation(cblib):
+    lib = cblib.load()
+    T = ctypes.byref
+    base = 1 << 20
+    x = _view(base, 2, 14, 14, 48)
+    y = _view(base + (1 << 22), 2, 7, 7, 96)
+    n = ctypes.c_size_t(0)
+    assert lib.cb_dw_separable_block_workspace(T(x), 96, 2, T(n)) == cblib.OK
+    rup = lambda b: (b + 255) // 256 * 256
+    assert n.value == rup(2 * 7 * 7 * 48 * 4) + rup(2 * 7 * 7 * 96 * 4)
+    p = base + (1 << 24)
+    # too-small workspace
+    assert lib.cb_dw_separable_block(T(x), p, p, p, p, p, p, p, p, p, 2, T(y), p, 16, None) == cblib.ERR_WORKSPACE
+    # identity skip needs stride 1 and Cin == Cout
+    assert lib.cb_dw_separable_block(T(x), p, p, p, p, p, p, None, None, None, 2, T(y), p, n.value,
+                                     None) == cblib.ERR_INVALID_ARG
+    # preprocess: pitch smaller than a row
+    assert lib.cb_preprocess_u8(base, 1, 720, 1280, 1000, base + (1 << 24), 480, 640, None) == cblib.ERR_INVALID_ARG
+    assert lib.cb_preprocess_u8(None, 1, 720, 1280, 3840, base, 480, 640, None) == cblib.ERR_INVALID_ARG
