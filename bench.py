@@ -23,7 +23,6 @@ import json
 import os
 import re
 import statistics
-import subprocess
 import sys
 import time
 
@@ -49,51 +48,68 @@ def load_peaks():
 
 # ------------------------------------------------------------ clocks sampler
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples SM clock and clock-event reasons through NVML (ctypes) every ~1 ms on a
+    background thread while the timed region runs.  Read-only: changes no setting."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.path = None
+    def __init__(self, torch, device_index: int):
+        import ctypes
+        import threading
+        self.ctypes, self.threading = ctypes, threading
+        self.samples = []
+        self.ok = False
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            got = False
+            try:
+                uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+                got = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                got = False
+            if not got:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                idx = int(vis.split(",")[device_index]) if vis and vis.split(",")[0].isdigit() else device_index
+                got = lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) == 0
+            if not got:
+                return
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            self.lib, self.h, self.max_mhz = lib, h, mx.value
+            self.ok = True
+        except OSError:
+            return
+
+    def _loop(self):
+        c, r = self.ctypes.c_uint(), self.ctypes.c_ulonglong()
+        while not self.stop_flag:
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ctypes.byref(c)) == 0 and \
+                    self.reason_fn(self.h, self.ctypes.byref(r)) == 0:
+                self.samples.append((c.value, r.value))
+            time.sleep(0.001)
 
     def start(self):
-        try:
-            out_dir = os.path.join(ROOT, "gpurun_out")
-            os.makedirs(out_dir, exist_ok=True)
-            self.path = os.path.join(out_dir, f"clocks_rank{self.index}.csv")
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+        if not self.ok:
+            return
+        self.stop_flag = False
+        self.thread = self.threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
 
     def stop(self):
-        if self.proc is None:
+        if not self.ok:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.f.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
-            except ValueError:
-                continue
-        if not rows:
+        self.stop_flag = True
+        self.thread.join()
+        if not self.samples:
             return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({name for _, bits in self.samples for b, name in self.REASONS.items() if bits & b})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "source": "nvml"}
 
 
 # ------------------------------------------------------------ distributed
@@ -222,7 +238,7 @@ def run_ours(args):
 
     nl = len(wl.launches)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(torch, local)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -362,8 +378,8 @@ class ReferenceDepthwise:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="depthwise",
                     choices=["depthwise", "dense", "mnist", "yolo", "preprocess"])

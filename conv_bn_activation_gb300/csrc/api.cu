@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -123,12 +124,30 @@ void view_range(const cb_tensor* t, uintptr_t* lo, uintptr_t* hi) {
   *hi = *lo + static_cast<uintptr_t>(last + 1) * sizeof(float);
 }
 
+// Disjoint channel slices of one NHWC buffer (same n/h/w strides, both
+// slices inside one pixel's stride_w elements, every stride a multiple of
+// stride_w) share no element even though their byte ranges interleave.
+bool disjoint_channel_slices(const cb_tensor* a, const cb_tensor* b) {
+  if (a->layout != CB_LAYOUT_NHWC || b->layout != CB_LAYOUT_NHWC) return false;
+  if (a->stride_n != b->stride_n || a->stride_h != b->stride_h || a->stride_w != b->stride_w) return false;
+  const long long sw = a->stride_w;
+  if (sw <= 0 || a->stride_h % sw != 0 || a->stride_n % sw != 0) return false;
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a->data), pb = reinterpret_cast<uintptr_t>(b->data);
+  const uintptr_t base = pa < pb ? pa : pb;
+  if ((pa - base) % sizeof(float) != 0 || (pb - base) % sizeof(float) != 0) return false;
+  const long long da = static_cast<long long>((pa - base) / sizeof(float));
+  const long long db = static_cast<long long>((pb - base) / sizeof(float));
+  if (da + a->c > sw || db + b->c > sw) return false;
+  return da + a->c <= db || db + b->c <= da;
+}
+
 bool overlap(const cb_tensor* a, const cb_tensor* b) {
   if (a->n == 0 || b->n == 0) return false;
   uintptr_t alo, ahi, blo, bhi;
   view_range(a, &alo, &ahi);
   view_range(b, &blo, &bhi);
-  return alo < bhi && blo < ahi;
+  if (!(alo < bhi && blo < ahi)) return false;
+  return !disjoint_channel_slices(a, b);
 }
 
 bool same_view(const cb_tensor* a, const cb_tensor* b) {
@@ -201,10 +220,14 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
   // column), strips of output rows, 32-channel chunks; minimise the busiest
   // SM's staged bytes.
   const int chunks = (a.C + 31) / 32;
+  // Tuning override (CB_DW_FORCE="rows,tile_w,ctas_per_sm"; 0 = free), read per call.
+  int force_r = 0, force_tw = 0, force_cps = 0;
+  if (const char* f = std::getenv("CB_DW_FORCE")) std::sscanf(f, "%d,%d,%d", &force_r, &force_tw, &force_cps);
   DwTmaPlan best{};
   double best_cost = 1e300;
   for (int wt = (a.OW + 59) / 60; wt <= std::max((a.OW + 59) / 60, a.OW / 8); ++wt) {
     const int tile_w = (a.OW + wt - 1) / wt;
+    if (force_tw && tile_w != force_tw) continue;
     const int wtiles = (a.OW + tile_w - 1) / tile_w;
     const int box_w = (tile_w - 1) * stride + 3;
     if (box_w > 256) continue;
@@ -212,6 +235,7 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
     const int threads = 32 * (1 + consumer_warps);
     const int stage_bytes = box_w * 128;
     int cps = dw_tma_blocks_per_sm(stride, threads, 96 * 1024) >= 2 ? 2 : 1;
+    if (force_cps == 1 || force_cps == 2) cps = force_cps;
     const size_t ring = cps == 2 ? 96 * 1024 : 192 * 1024;
     int stages = static_cast<int>(std::min<size_t>(32, ring / stage_bytes));
     if (stages < 3) continue;
@@ -220,6 +244,7 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
     for (int strips = 1; strips <= std::max(1, a.OH / 4); ++strips) {
       const int R = (a.OH + strips - 1) / strips;
       if (strips > 1 && (a.OH + R - 1) / R != strips) continue;
+      if (force_r && R != force_r) continue;
       const long long items = static_cast<long long>(a.N) * chunks * strips * wtiles;
       if (items > (1LL << 30)) continue;
       const int grid = static_cast<int>(std::min<long long>(items, cap));
@@ -238,6 +263,10 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
       }
     }
   }
+  if (std::getenv("CB_DEBUG_PLAN"))
+    std::fprintf(stderr, "[cb] dw plan: N=%d H=%d W=%d C=%d s=%d -> rows=%d items=%d box_w=%d stages=%d grid=%d warps=%d smem=%zu\n",
+                 a.N, a.H, a.W, a.C, stride, best.rows_per_item, best.num_items, best.box_w, best.stages, best.grid,
+                 best.consumer_warps, best.smem_bytes);
   if (best.grid == 0) {
     cudaError_t e = launch_dw_simple(a, vec, s);
     return e == cudaSuccess ? CB_OK : cuda_fail(e);

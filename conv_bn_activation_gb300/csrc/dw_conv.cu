@@ -94,14 +94,17 @@ struct DwItem {
   int n, c0, oh0, oh1, ow0, ow1;
 };
 
+// Work items are numbered with the channel chunk fastest, so CTAs running at
+// the same time read the same input rows (whole 1536-byte pixels of DRAM
+// pages) rather than one 128-byte slice of many pixels.
 __device__ __forceinline__ DwItem dw_decode(const DwTmaParams& p, int item) {
   DwItem it;
-  const int wt = item % p.wtiles;
-  int rest = item / p.wtiles;
+  const int ch = item % p.chunks;
+  int rest = item / p.chunks;
+  const int wt = rest % p.wtiles;
+  rest /= p.wtiles;
   const int st = rest % p.strips;
-  rest /= p.strips;
-  const int ch = rest % p.chunks;
-  it.n = rest / p.chunks;
+  it.n = rest / p.strips;
   it.c0 = ch * 32;
   it.oh0 = st * p.rows_per_item;
   it.oh1 = min(it.oh0 + p.rows_per_item, p.a.OH);

@@ -70,4 +70,5 @@ def test_preprocess_full_batch_properties(gpu):
     sync_check()
     k = torch.round(dst * 255)
     assert bool(((k >= 0) & (k <= 255)).all())
-    assert bool((k / 255 == dst).all())
+    table = torch.from_numpy(np.arange(256, dtype=np.float32) / np.float32(255)).to(gpu)  # IEEE u / 255
+    assert bool((table[k.long()] == dst).all())
