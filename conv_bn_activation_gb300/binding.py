@@ -26,6 +26,7 @@ EXPORTED = (
     "cb_fold_bn", "cb_repack_weights", "cb_conv_bn_act", "cb_dw_separable_block_workspace",
     "cb_dw_separable_block", "cb_avgpool_linear", "cb_preprocess_u8", "cb_preprocess_u8_three_pass",
     "cb_get_device_error", "cb_last_cuda_error", "cb_set_kernel_policy", "cb_status_string", "cb_version",
+    "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_conv_uses_tensor_cores",
 )
 
 
@@ -72,6 +73,9 @@ def load():
                 "cb_get_device_error": [P],
                 "cb_last_cuda_error": [],
                 "cb_set_kernel_policy": [I],
+                "cb_get_kernel_policy": [],
+                "cb_round_weights_tf32": [P, LL, P],
+                "cb_conv_uses_tensor_cores": [T, I, I],
                 "cb_status_string": [I],
                 "cb_version": [],
             }
@@ -140,6 +144,23 @@ def repack_weights(w_oihw, groups=1):
 
 def set_kernel_policy(policy: int):
     _check(load().cb_set_kernel_policy(policy), "cb_set_kernel_policy")
+
+
+def get_kernel_policy() -> int:
+    return load().cb_get_kernel_policy()
+
+
+def round_weights_tf32(w):
+    """cb_round_weights_tf32 on a host array (any shape) -> rounded float32 copy."""
+    a = np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty_like(a)
+    _check(load().cb_round_weights_tf32(a.ctypes.data, a.size, out.ctypes.data), "cb_round_weights_tf32")
+    return out
+
+
+def uses_tensor_cores(x, k, groups=1, x_layout=LAYOUT_NHWC) -> bool:
+    xv = nchw(x) if x_layout == LAYOUT_NCHW else nhwc(x)
+    return bool(load().cb_conv_uses_tensor_cores(ctypes.byref(xv), k, groups))
 
 
 def version() -> int:

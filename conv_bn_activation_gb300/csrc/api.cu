@@ -216,22 +216,23 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
     return e == cudaSuccess ? CB_OK : cuda_fail(e);
   }
 
-  // Plan: output-column tiles of at most 60 columns (8 consumer threads per
-  // column), strips of output rows, 32-channel chunks; minimise the busiest
-  // SM's staged bytes.
+  // Plan: output-column tiles of at most 120 columns (8 consumer threads per
+  // column pair), strips of output rows, 32-channel chunks; minimise the
+  // busiest SM's staged bytes.
   const int chunks = (a.C + 31) / 32;
   // Tuning override (CB_DW_FORCE="rows,tile_w,ctas_per_sm"; 0 = free), read per call.
   int force_r = 0, force_tw = 0, force_cps = 0;
   if (const char* f = std::getenv("CB_DW_FORCE")) std::sscanf(f, "%d,%d,%d", &force_r, &force_tw, &force_cps);
   DwTmaPlan best{};
   double best_cost = 1e300;
-  for (int wt = (a.OW + 59) / 60; wt <= std::max((a.OW + 59) / 60, a.OW / 8); ++wt) {
+  for (int wt = (a.OW + 119) / 120; wt <= std::max((a.OW + 119) / 120, a.OW / 8); ++wt) {
     const int tile_w = (a.OW + wt - 1) / wt;
     if (force_tw && tile_w != force_tw) continue;
     const int wtiles = (a.OW + tile_w - 1) / tile_w;
-    const int box_w = (tile_w - 1) * stride + 3;
+    const int pairs = (tile_w + 1) / 2;
+    const int box_w = (2 * pairs - 1) * stride + 3;  // both columns of the last pair are covered
     if (box_w > 256) continue;
-    const int consumer_warps = (tile_w * 8 + 31) / 32;
+    const int consumer_warps = (pairs * 8 + 31) / 32;
     const int threads = 32 * (1 + consumer_warps);
     const int stage_bytes = box_w * 128;
     int cps = dw_tma_blocks_per_sm(stride, threads, 96 * 1024) >= 2 ? 2 : 1;
@@ -256,6 +257,7 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
         best.rows_per_item = R;
         best.num_items = static_cast<int>(items);
         best.box_w = box_w;
+        best.tile_w = tile_w;
         best.stages = stages;
         best.grid = grid;
         best.consumer_warps = consumer_warps;
@@ -444,6 +446,20 @@ cb_status cb_repack_weights(const float* w_oihw, int Co, int Ci_per_group, int k
   return CB_ERR_UNSUPPORTED;
 }
 
+cb_status cb_round_weights_tf32(const float* w, long long n, float* out) {
+  if (!w || !out || n < 0) return CB_ERR_INVALID_ARG;
+  for (long long i = 0; i < n; ++i) {
+    uint32_t b;
+    std::memcpy(&b, &w[i], sizeof(b));
+    if ((b & 0x7F800000u) != 0x7F800000u) {  // finite: round the low 13 bits to nearest, ties to even
+      const uint32_t lsb = (b >> 13) & 1u;
+      b = (b + 0x0FFFu + lsb) & ~0x1FFFu;
+    }
+    std::memcpy(&out[i], &b, sizeof(b));
+  }
+  return CB_OK;
+}
+
 cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale, const float* bias, int kh, int kw,
                          int stride, int pad, int groups, cb_act act, const cb_tensor* residual,
                          cb_res_mode res_mode, cb_tensor* y, void* stream) {
@@ -628,6 +644,16 @@ cb_status cb_set_kernel_policy(int policy) {
   if (policy < 0 || policy > 1) return CB_ERR_INVALID_ARG;
   g_policy.store(policy);
   return CB_OK;
+}
+
+int cb_get_kernel_policy(void) { return g_policy.load(); }
+
+int cb_conv_uses_tensor_cores(const cb_tensor* x, int kh, int groups) {
+  if (!view_ok(x) || groups != 1 || (kh != 1 && kh != 3)) return 0;
+  return g_policy.load() != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && x->c >= 16 &&
+                 aligned16(x->data) && strides_mult4(x)
+             ? 1
+             : 0;
 }
 
 }  // extern "C"

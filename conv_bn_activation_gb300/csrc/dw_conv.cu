@@ -95,7 +95,7 @@ struct DwItem {
 };
 
 // Work items are numbered with the channel chunk fastest, so CTAs running at
-// the same time read the same input rows (whole 1536-byte pixels of DRAM
+// the same time read the same input rows (whole pixels, i.e. whole DRAM
 // pages) rather than one 128-byte slice of many pixels.
 __device__ __forceinline__ DwItem dw_decode(const DwTmaParams& p, int item) {
   DwItem it;
@@ -113,9 +113,22 @@ __device__ __forceinline__ DwItem dw_decode(const DwTmaParams& p, int item) {
   return it;
 }
 
-template <int S>
+template <int ACT, int RES>
+__device__ __forceinline__ float epi_c(float acc, float sc, float bi, float r) {
+  float z = fmaf(acc, sc, bi);
+  if (RES == 1) z += r;
+  if (ACT == 1) z = fmaxf(z, 0.0f);
+  if (ACT == 2) z = z / (1.0f + expf(-z));
+  if (RES == 2) z += r;
+  return z;
+}
+
+// Each consumer thread owns two adjacent output columns x 4 channels; its
+// window needs NC = S + 3 input columns per row.
+template <int S, int ACT, int RES>
 __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ CUtensorMap xmap,
                                                         const DwTmaParams p) {
+  constexpr int NC = S + 3;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int stage_bytes = p.box_w * 128;
   uint8_t* ring = smem_raw;
@@ -168,86 +181,145 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
       for (int s = 0; s < p.stages; ++s)
         if (issued & (1u << s)) mbar_wait_drain(&full[s], (last_parity >> s) & 1u, 20000000ull);
     }
-  } else {
-    // ---------------------------------------------------------- consumers
-    const int t = threadIdx.x - 32;
-    const int owl = t >> 3, c4 = t & 7;
-    int slot = 0;
-    uint32_t phase = 0;
-    bool ok = true;
+    return;
+  }
 
-    auto fetch = [&](float4(&dst)[3], bool read) {
-      if (!ok) return;
-      bool got = mbar_wait(&full[slot], phase, wd);
-      got = __all_sync(0xffffffffu, got);
-      if (!got) {
-        ok = false;
-        return;
-      }
-      if (read) {
-        const float* row = reinterpret_cast<const float*>(ring + slot * stage_bytes) + c4 * 4;
-#pragma unroll
-        for (int kw = 0; kw < 3; ++kw) dst[kw] = *reinterpret_cast<const float4*>(row + (owl * S + kw) * 32);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-      if (++slot == p.stages) {
-        slot = 0;
-        phase ^= 1u;
-      }
-    };
+  // ------------------------------------------------------------ consumers
+  const int t = threadIdx.x - 32;
+  const int pair = t >> 3, c4 = t & 7;
+  int slot = 0;
+  uint32_t phase = 0;
+  bool ok = true;
 
-    for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
-      const DwItem it = dw_decode(p, item);
-      const int ow = it.ow0 + owl;
-      const int c = it.c0 + c4 * 4;
-      const bool in_tile = ow < it.ow1;
-      const bool active = in_tile && c < a.C;
-      float4 wv[9];
-      float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), bi = sc;
-      if (active) {
+  // Wait for the next ring row, copy this thread's NC window columns into
+  // registers, release the slot.
+  auto fetch = [&](float4(&dst)[NC], bool read) {
+    if (!ok) return;
+    bool got = mbar_wait(&full[slot], phase, wd);
+    got = __all_sync(0xffffffffu, got);
+    if (!got) {
+      ok = false;
+      return;
+    }
+    if (read) {
+      const float4* row =
+          reinterpret_cast<const float4*>(ring + slot * stage_bytes) + (2 * pair * S) * 8 + c4;
 #pragma unroll
-        for (int k = 0; k < 9; ++k) wv[k] = ldg4(a.w + k * a.C + c);
-        sc = ldg4(a.ep.scale + c);
-        bi = ldg4(a.ep.bias + c);
-      } else {
+      for (int k = 0; k < NC; ++k) dst[k] = row[k * 8];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (++slot == p.stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  };
+
+  for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    const DwItem it = dw_decode(p, item);
+    const int ow = it.ow0 + 2 * pair;
+    const int c = it.c0 + c4 * 4;
+    const bool in_tile = ow < it.ow1;            // the box covers both columns of every pair
+    const bool active = in_tile && c < a.C;
+    const bool second = active && ow + 1 < it.ow1;
+    float4 wv[9];
+    float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), bi = sc;
+    if (active) {
 #pragma unroll
-        for (int k = 0; k < 9; ++k) wv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      float4 ra[3], rb[3], rc[3];
-      fetch(ra, in_tile);
-      fetch(rb, in_tile);
-      for (int oh = it.oh0; oh < it.oh1; ++oh) {
-        fetch(rc, in_tile);
-        if (ok && active) {
+      for (int k = 0; k < 9; ++k) wv[k] = ldg4(a.w + k * a.C + c);
+      sc = ldg4(a.ep.scale + c);
+      bi = ldg4(a.ep.bias + c);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 9; ++k) wv[k] = sc;
+    }
+    float* yp = a.out.y + it.n * a.out.ys_n + it.oh0 * a.out.ys_h + ow * a.out.ys_w + c;
+    const float* rp = RES ? a.ep.r + it.n * a.ep.rs_n + it.oh0 * a.ep.rs_h + ow * a.ep.rs_w + c : nullptr;
+
+    // One output row from the window (top, mid, bottom); advances yp / rp.
+    auto compute = [&](const float4(&T)[NC], const float4(&M)[NC], const float4(&B)[NC]) {
+      if (ok && active) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int kw = 0; kw < 3; ++kw) {
-            fma4(acc, ra[kw], wv[kw]);
-            fma4(acc, rb[kw], wv[3 + kw]);
-            fma4(acc, rc[kw], wv[6 + kw]);
+            fma4(acc, T[j * S + kw], wv[kw]);
+            fma4(acc, M[j * S + kw], wv[3 + kw]);
+            fma4(acc, B[j * S + kw], wv[6 + kw]);
           }
-          float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (a.ep.res_mode)
-            r = *reinterpret_cast<const float4*>(a.ep.r + it.n * a.ep.rs_n + oh * a.ep.rs_h + ow * a.ep.rs_w + c);
-          const float4 o = epi_apply4(acc, sc, bi, r, a.ep.act, a.ep.res_mode);
-          *reinterpret_cast<float4*>(a.out.y + it.n * a.out.ys_n + oh * a.out.ys_h + ow * a.out.ys_w + c) = o;
-        }
-        if (S == 1) {
-#pragma unroll
-          for (int k = 0; k < 3; ++k) {
-            ra[k] = rb[k];
-            rb[k] = rc[k];
+          if (j == 0 || second) {
+            float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (RES) r = *reinterpret_cast<const float4*>(rp + j * a.ep.rs_w);
+            float4 o;
+            o.x = epi_c<ACT, RES>(acc.x, sc.x, bi.x, r.x);
+            o.y = epi_c<ACT, RES>(acc.y, sc.y, bi.y, r.y);
+            o.z = epi_c<ACT, RES>(acc.z, sc.z, bi.z, r.z);
+            o.w = epi_c<ACT, RES>(acc.w, sc.w, bi.w, r.w);
+            *reinterpret_cast<float4*>(yp + j * a.out.ys_w) = o;
           }
-        } else if (oh + 1 < it.oh1) {
-#pragma unroll
-          for (int k = 0; k < 3; ++k) ra[k] = rc[k];
-          fetch(rb, in_tile);
         }
+      }
+      yp += a.out.ys_h;
+      if (RES) rp += a.ep.rs_h;
+    };
+
+    float4 r0[NC], r1[NC], r2[NC];
+    fetch(r0, in_tile);
+    fetch(r1, in_tile);
+    fetch(r2, in_tile);
+    int oh = it.oh0;
+    if (S == 1) {
+      // window rows rotate r0,r1,r2 -> r1,r2,r0 -> r2,r0,r1: one new row per output row
+      for (;;) {
+        compute(r0, r1, r2);
+        if (++oh == it.oh1) break;
+        fetch(r0, in_tile);
+        compute(r1, r2, r0);
+        if (++oh == it.oh1) break;
+        fetch(r1, in_tile);
+        compute(r2, r0, r1);
+        if (++oh == it.oh1) break;
+        fetch(r2, in_tile);
+      }
+    } else {
+      // stride 2: the bottom row is the next window's top; two new rows per output row
+      for (;;) {
+        compute(r0, r1, r2);
+        if (++oh == it.oh1) break;
+        fetch(r0, in_tile);
+        fetch(r1, in_tile);
+        compute(r2, r0, r1);
+        if (++oh == it.oh1) break;
+        fetch(r2, in_tile);
+        fetch(r0, in_tile);
+        compute(r1, r2, r0);
+        if (++oh == it.oh1) break;
+        fetch(r1, in_tile);
+        fetch(r2, in_tile);
       }
     }
   }
-  __syncthreads();
+}
+
+template <int S, int ACT, int RES>
+static void dw_tma_launch(const CUtensorMap& xmap, const DwTmaParams& p, int grid, int threads, size_t smem,
+                          cudaStream_t s) {
+  cudaFuncSetAttribute(dw_tma_kernel<S, ACT, RES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(smem));
+  dw_tma_kernel<S, ACT, RES><<<grid, threads, smem, s>>>(xmap, p);
+}
+
+template <int S>
+static void dw_tma_dispatch(const CUtensorMap& xmap, const DwTmaParams& p, int grid, int threads, size_t smem,
+                            cudaStream_t s) {
+  const int act = p.a.ep.act, res = p.a.ep.res_mode;
+#define CB_DW_CASE(A, R) \
+  if (act == A && res == R) return dw_tma_launch<S, A, R>(xmap, p, grid, threads, smem, s);
+  CB_DW_CASE(0, 0) CB_DW_CASE(1, 0) CB_DW_CASE(2, 0)
+  CB_DW_CASE(0, 1) CB_DW_CASE(1, 1) CB_DW_CASE(2, 1)
+  CB_DW_CASE(0, 2) CB_DW_CASE(1, 2) CB_DW_CASE(2, 2)
+#undef CB_DW_CASE
 }
 
 cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaPlan& plan, int* err,
@@ -260,20 +332,15 @@ cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaP
   p.stages = plan.stages;
   p.chunks = (a.C + 31) / 32;
   p.strips = (a.OH + plan.rows_per_item - 1) / plan.rows_per_item;
-  p.tile_w = (plan.box_w - 3) / a.stride + 1;
+  p.tile_w = plan.tile_w;
   p.wtiles = (a.OW + p.tile_w - 1) / p.tile_w;
   p.err = err;
   p.timeout_ns = timeout_ns;
   const int threads = 32 * (1 + plan.consumer_warps);
-  if (a.stride == 1) {
-    cudaFuncSetAttribute(dw_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(plan.smem_bytes));
-    dw_tma_kernel<1><<<plan.grid, threads, plan.smem_bytes, s>>>(xmap, p);
-  } else {
-    cudaFuncSetAttribute(dw_tma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(plan.smem_bytes));
-    dw_tma_kernel<2><<<plan.grid, threads, plan.smem_bytes, s>>>(xmap, p);
-  }
+  if (a.stride == 1)
+    dw_tma_dispatch<1>(xmap, p, plan.grid, threads, plan.smem_bytes, s);
+  else
+    dw_tma_dispatch<2>(xmap, p, plan.grid, threads, plan.smem_bytes, s);
   return cudaGetLastError();
 }
 
@@ -281,11 +348,11 @@ cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaP
 int dw_tma_blocks_per_sm(int stride, int threads, size_t smem) {
   int n = 0;
   if (stride == 1) {
-    cudaFuncSetAttribute(dw_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dw_tma_kernel<1>, threads, smem);
+    cudaFuncSetAttribute(dw_tma_kernel<1, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dw_tma_kernel<1, 1, 0>, threads, smem);
   } else {
-    cudaFuncSetAttribute(dw_tma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dw_tma_kernel<2>, threads, smem);
+    cudaFuncSetAttribute(dw_tma_kernel<2, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dw_tma_kernel<2, 1, 0>, threads, smem);
   }
   return n;
 }

@@ -23,7 +23,11 @@
 //    releases each smem stage and, at the end of a tile, the accumulator.
 //  * warps 2-5: epilogue.  Each warp reads its 32 TMEM lanes (= 32 output
 //    pixels) with tcgen05.ld, applies scale/bias, residual and activation,
-//    and stores the row segment; rows past M and channels past Cout are
+//    rounds to the nearest TF32 value and stores the row segment.  (The MMA
+//    truncates its fp32 operands to TF32, which biases every product toward
+//    zero; storing round-to-nearest TF32 activations lets the next
+//    tensor-core layer read them exactly, so the bias does not compound
+//    along a chain.)  Rows past M and channels past Cout are
 //    masked, so nothing is written outside the logical output (padded
 //    output rows stay untouched -- "YOLO26N Inference Optimisation", Bug
 //    fixed: TMA overflow).
@@ -217,7 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tf32_kernel(const __grid_co
               if (a.ep.res_mode) r = *reinterpret_cast<const float4*>(rrow + c0 + j);
               const float4 accv = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
                                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-              *reinterpret_cast<float4*>(yrow + c0 + j) = epi_apply4(accv, sc, bi, r, a.ep.act, a.ep.res_mode);
+              float4 o = epi_apply4(accv, sc, bi, r, a.ep.act, a.ep.res_mode);
+              o = make_float4(round_tf32(o.x), round_tf32(o.y), round_tf32(o.z), round_tf32(o.w));
+              *reinterpret_cast<float4*>(yrow + c0 + j) = o;
             }
           } else {
 #pragma unroll
@@ -225,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_tf32_kernel(const __grid_co
               const int c = c0 + j;
               if (c < a.Cout) {
                 const float r = a.ep.res_mode ? rrow[c] : 0.0f;
-                yrow[c] = epi_apply(__uint_as_float(v[j]), __ldg(a.ep.scale + c), __ldg(a.ep.bias + c), r, a.ep.act,
-                                    a.ep.res_mode);
+                yrow[c] = round_tf32(epi_apply(__uint_as_float(v[j]), __ldg(a.ep.scale + c), __ldg(a.ep.bias + c), r,
+                                               a.ep.act, a.ep.res_mode));
               }
             }
           }

@@ -36,11 +36,13 @@ struct DwArgs {
 cudaError_t launch_dw_simple(const DwArgs& a, bool vec4, cudaStream_t s);
 
 // TMA-fed kernel: persistent CTAs stream input rows (32-channel chunks,
-// full padded width) through a shared-memory ring; 3x3 windows slide down
-// the rows in registers.
+// full padded width of a column tile) through a shared-memory ring; each
+// consumer thread owns two adjacent output columns x 4 channels and slides
+// its 3x3 windows down the rows in registers.
 struct DwTmaPlan {
   int rows_per_item;  // output rows per work item
   int num_items;
+  int tile_w;         // output columns per item
   int box_w;          // input columns per row copy (includes the halo)
   int stages;
   int grid;

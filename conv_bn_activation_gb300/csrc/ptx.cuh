@@ -180,6 +180,15 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// Round an fp32 value to the nearest TF32 value (10 explicit mantissa bits,
+// ties away from zero); the result is an fp32 bit pattern with the low 13
+// mantissa bits clear.
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
 // Shared-memory matrix descriptor for a K-major operand stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms
 // stacked along M/N (stride byte offset 1024).  Bits: start address >> 4

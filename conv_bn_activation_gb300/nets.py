@@ -31,9 +31,25 @@ def _dev(a, device):
 
 
 class ConvBnAct:
-    def __init__(self, w_oihw, bn, stride, pad, act, groups=1, device="cuda", eps=1e-5):
+    """One fused layer with folded BN and repacked weights on the device.
+
+    tc_weights: round the dense weights to the nearest TF32 value
+    (cb_round_weights_tf32) for the tensor-core path; None decides from the
+    shape rule of that path (groups 1, Cin % 4 == 0, Cin >= 16) and the
+    current kernel policy.
+    """
+
+    def __init__(self, w_oihw, bn, stride, pad, act, groups=1, device="cuda", eps=1e-5, tc_weights=None):
         scale, bias = cb.fold_bn(*bn, eps=eps)
-        self.w = _dev(cb.repack_weights(w_oihw, groups), device).contiguous()
+        cin = w_oihw.shape[1] * groups
+        if tc_weights is None:
+            tc_weights = (groups == 1 and cin % 4 == 0 and cin >= 16 and w_oihw.shape[2] in (1, 3)
+                          and cb.get_kernel_policy() == 0)
+        w = cb.repack_weights(w_oihw, groups)
+        if tc_weights:
+            w = cb.round_weights_tf32(w)
+        self.tc_weights = bool(tc_weights)
+        self.w = _dev(w, device).contiguous()
         self.scale = _dev(scale, device)
         self.bias = _dev(bias, device)
         self.cout, cin_g, self.k, _ = w_oihw.shape
@@ -55,15 +71,17 @@ class DwBlock:
         self.cin, self.cout, self.stride = cin, cout, stride
         dws, dwb = cb.fold_bn(*p["bn1"])
         pws, pwb = cb.fold_bn(*p["bn2"])
+        tc = cin % 4 == 0 and cin >= 16 and cb.get_kernel_policy() == 0
+        dense = cb.round_weights_tf32 if tc else (lambda a: a)
         self.params = {
             "dw_w": _dev(cb.repack_weights(p["dw_w"], groups=cin), device),
             "dw_scale": _dev(dws, device), "dw_bias": _dev(dwb, device),
-            "pw_w": _dev(cb.repack_weights(p["pw_w"]), device),
+            "pw_w": _dev(dense(cb.repack_weights(p["pw_w"])), device),
             "pw_scale": _dev(pws, device), "pw_bias": _dev(pwb, device),
         }
         if "skip_w" in p:
             sks, skb = cb.fold_bn(*p["skip_bn"])
-            self.params.update({"skip_w": _dev(cb.repack_weights(p["skip_w"]), device),
+            self.params.update({"skip_w": _dev(dense(cb.repack_weights(p["skip_w"])), device),
                                 "skip_scale": _dev(sks, device), "skip_bias": _dev(skb, device)})
 
     def __call__(self, x, y, workspace, stream=None):

@@ -98,6 +98,16 @@ cb_status cb_repack_weights(const float* w_oihw, int Co, int Ci_per_group, int k
                             int groups, float* w_out);
 
 /*
+ * Round n fp32 weights (HOST, any layout) to the nearest TF32 value (10
+ * explicit mantissa bits, ties to even), written to out (HOST; may equal w).
+ * The tensor cores read fp32 operands by truncating them to TF32, which
+ * shrinks every product toward zero; weights rounded once at load time
+ * enter the MMA exactly and carry an unbiased error instead.  Use it for
+ * layers that run on the tensor-core path (cb_conv_uses_tensor_cores).
+ */
+cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
+
+/*
  * The fused layer.  x: input view (NHWC, or NCHW for the small-channel stem
  * path); w: DEVICE weights in the cb_repack_weights layout; scale/bias:
  * DEVICE fp32 [Co] from cb_fold_bn; kernel kh x kw (1 or 3), stride 1 or 2,
@@ -109,10 +119,11 @@ cb_status cb_repack_weights(const float* w_oihw, int Co, int Ci_per_group, int k
  *
  * Paths (chosen on the host from the shape): dense layers with Ci % 4 == 0
  * and Ci >= 16 run as an implicit GEMM on the tcgen05 tensor cores (TF32
- * inputs, fp32 accumulate; needs 16-byte aligned x/w and strides that are
- * multiples of 4 elements); depthwise 3x3 layers run on a channel-vectorised
- * CUDA-core kernel; everything else (stems with 1 or 3 input channels, NCHW
- * input, odd channel counts) runs on a direct CUDA-core kernel in fp32.
+ * inputs, fp32 accumulate, outputs rounded to the nearest TF32 value; needs
+ * 16-byte aligned x/w and strides that are multiples of 4 elements);
+ * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;
+ * everything else (stems with 1 or 3 input channels, NCHW input, odd channel
+ * counts) runs on a direct CUDA-core kernel in fp32.
  */
 cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale, const float* bias,
                          int kh, int kw, int stride, int pad, int groups, cb_act act,
@@ -193,6 +204,17 @@ int cb_last_cuda_error(void);
  * TMA / tensor-core paths.  Returns CB_OK, or CB_ERR_INVALID_ARG.
  */
 cb_status cb_set_kernel_policy(int policy);
+
+/* The current kernel-choice policy (see cb_set_kernel_policy). */
+int cb_get_kernel_policy(void);
+
+/*
+ * 1 if cb_conv_bn_act with input view x, a kh x kh kernel and `groups` would
+ * run on the tensor-core implicit GEMM under the current policy, else 0.
+ * Tensor-core layers compute with TF32 inputs and store outputs rounded to
+ * the nearest TF32 value; the other paths are fp32 throughout.
+ */
+int cb_conv_uses_tensor_cores(const cb_tensor* x, int kh, int groups);
 
 /* A static string naming a status code. */
 const char* cb_status_string(cb_status s);

@@ -124,3 +124,23 @@ def test_block_and_preprocess_validation(cblib):
     # preprocess: pitch smaller than a row
     assert lib.cb_preprocess_u8(base, 1, 720, 1280, 1000, base + (1 << 24), 480, 640, None) == cblib.ERR_INVALID_ARG
     assert lib.cb_preprocess_u8(None, 1, 720, 1280, 3840, base, 480, 640, None) == cblib.ERR_INVALID_ARG
+
+
+def test_round_weights_tf32(cblib):
+    """Round to nearest TF32 (ties to even): low 13 mantissa bits clear, error <= half a TF32 ulp,
+    idempotent, and the tie cases go to the even neighbour."""
+    g = np.random.default_rng(2)
+    w = (g.standard_normal(10000) * np.exp(g.uniform(-20, 20, 10000))).astype(np.float32)
+    r = cblib.round_weights_tf32(w)
+    bits = r.view(np.uint32)
+    assert np.all(bits & 0x1FFF == 0)
+    ulp = np.spacing(np.abs(w)) * 2.0 ** 13   # one TF32 ulp at each value's exponent
+    assert np.all(np.abs(r.astype(np.float64) - w) <= ulp / 2)
+    np.testing.assert_array_equal(cblib.round_weights_tf32(r), r)
+    # ties: 1 + k*2^-10 + 2^-11 rounds to the even k
+    base = np.float32(1.0).view(np.uint32)
+    tie_even = np.array([base + 0x1000], np.uint32).view(np.float32)        # k = 0 -> 1.0
+    tie_odd = np.array([base + 0x2000 + 0x1000], np.uint32).view(np.float32)  # k = 1 -> k = 2
+    assert cblib.round_weights_tf32(tie_even)[0] == 1.0
+    assert cblib.round_weights_tf32(tie_odd).view(np.uint32)[0] == base + 0x4000
+    assert np.isinf(cblib.round_weights_tf32(np.array([np.inf], np.float32))[0])
