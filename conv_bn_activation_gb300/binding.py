@@ -27,7 +27,9 @@ EXPORTED = (
     "cb_dw_separable_block", "cb_avgpool_linear", "cb_preprocess_u8", "cb_preprocess_u8_three_pass",
     "cb_get_device_error", "cb_last_cuda_error", "cb_set_kernel_policy", "cb_status_string", "cb_version",
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_conv_uses_tensor_cores",
+    "cb_dw_separable_block_static",
 )
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
 
 class CbTensor(ctypes.Structure):
@@ -67,6 +69,7 @@ def load():
                 "cb_conv_bn_act": [T, P, P, P, I, I, I, I, I, I, T, I, T, P],
                 "cb_dw_separable_block_workspace": [T, I, I, ctypes.POINTER(S)],
                 "cb_dw_separable_block": [T, P, P, P, P, P, P, P, P, P, I, T, P, S, P],
+                "cb_dw_separable_block_static": [T, P, P, P, P, P, P, P, P, P, I, T, P],
                 "cb_avgpool_linear": [T, P, P, I, P, P],
                 "cb_preprocess_u8": [P, I, I, I, LL, P, I, I, P],
                 "cb_preprocess_u8_three_pass": [P, I, I, I, LL, P, P, P, I, I, P],
@@ -206,6 +209,20 @@ def dw_separable_block(x, p, stride, y, workspace, stream=None):
         _stream_ptr(stream))
     _check(st, "cb_dw_separable_block")
     return y
+
+
+def dw_separable_block_static(x, p, stride, y, stream=None):
+    """cb_dw_separable_block_static: the same block with the library's fixed scratch array
+    (no workspace argument, no allocation).  Returns the cb status without raising."""
+    xv, yv = nhwc(x), nhwc(y)
+    sk = p.get("skip_w")
+    return load().cb_dw_separable_block_static(
+        ctypes.byref(xv), p["dw_w"].data_ptr(), p["dw_scale"].data_ptr(), p["dw_bias"].data_ptr(),
+        p["pw_w"].data_ptr(), p["pw_scale"].data_ptr(), p["pw_bias"].data_ptr(),
+        sk.data_ptr() if sk is not None else None,
+        p["skip_scale"].data_ptr() if sk is not None else None,
+        p["skip_bias"].data_ptr() if sk is not None else None,
+        stride, ctypes.byref(yv), _stream_ptr(stream))
 
 
 def avgpool_linear(x, fc_w, fc_b, out, stream=None):

@@ -544,6 +544,42 @@ cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const flo
   return cb_conv_bn_act(&t, pw_w, pw_scale, pw_bias, 1, 1, 1, 0, 1, CB_ACT_RELU, r, CB_RES_PRE_ACT, y, stream);
 }
 
+// ------------------------------------------------ no-allocation block variant
+// The scratch of cb_dw_separable_block_static.  Host code cannot use this
+// name as a device address; it looks the address up per device below.
+static __device__ __align__(256) unsigned char g_block_scratch[CB_STATIC_SCRATCH_BYTES];
+
+static std::mutex g_scratch_mu;
+static void* g_scratch_addr[128];
+
+cb_status cb_dw_separable_block_static(const cb_tensor* x, const float* dw_w, const float* dw_scale,
+                                       const float* dw_bias, const float* pw_w, const float* pw_scale,
+                                       const float* pw_bias, const float* skip_w, const float* skip_scale,
+                                       const float* skip_bias, int stride, cb_tensor* y, void* stream) {
+  if (!view_ok(x) || !view_ok(y)) return CB_ERR_INVALID_ARG;
+  size_t need = 0;
+  cb_status st = cb_dw_separable_block_workspace(x, y->c, stride, &need);
+  if (st != CB_OK) return st;
+  if (need > CB_STATIC_SCRATCH_BYTES) return CB_ERR_WORKSPACE;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 128) return CB_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_block_scratch);
+      if (e != cudaSuccess) return cuda_fail(e);
+      g_scratch_addr[dev] = p;
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  return cb_dw_separable_block(x, dw_w, dw_scale, dw_bias, pw_w, pw_scale, pw_bias, skip_w, skip_scale, skip_bias,
+                               stride, y, scratch, CB_STATIC_SCRATCH_BYTES, stream);
+}
+
 cb_status cb_avgpool_linear(const cb_tensor* x, const float* fc_w, const float* fc_b, int out_features, float* out,
                             void* stream) {
   if (!view_ok(x) || x->layout != CB_LAYOUT_NHWC || !fc_w || !fc_b || !out || out_features < 1)

@@ -156,6 +156,41 @@ cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const flo
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * Size of the fixed scratch array behind cb_dw_separable_block_static.
+ */
+#define CB_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * cb_dw_separable_block without a caller workspace and without allocating.
+ * The pages have no counterpart; this is a convenience of this library.
+ * Some callers cannot call cudaMalloc at the point where they run a block:
+ *  - code inside a host framework that owns all device memory and forbids
+ *    other allocators;
+ *  - real-time loops that must not allocate after start-up;
+ *  - plain C hosts that link this library but not an allocator.
+ * Such callers pass only inputs, weights and the output.  The block's
+ * scratch (t and s of cb_dw_separable_block) lives in one file-scope device
+ * array of CB_STATIC_SCRATCH_BYTES that every GPU loading this library
+ * keeps until the process exits.
+ *  - The first call on a device looks the array's device address up
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.  Later calls reuse the address.
+ *  - A block needing more scratch than CB_STATIC_SCRATCH_BYTES (see
+ *    cb_dw_separable_block_workspace) is rejected with CB_ERR_WORKSPACE
+ *    before anything runs.
+ *  - Every call shares the one array and leaves its contents behind.
+ *    Nothing in it needs to start at zero, because each call writes t and s
+ *    in full before reading them.  Calls that may overlap on the GPU (other
+ *    streams, other host threads) race on the array: serialise them.
+ * Arguments, layouts and the remaining errors are those of
+ * cb_dw_separable_block.
+ */
+cb_status cb_dw_separable_block_static(const cb_tensor* x, const float* dw_w, const float* dw_scale,
+                                       const float* dw_bias, const float* pw_w, const float* pw_scale,
+                                       const float* pw_bias, const float* skip_w, const float* skip_scale,
+                                       const float* skip_bias, int stride, cb_tensor* y, void* stream);
+
+/*
  * Global average pool then linear layer (the DepthwiseMNIST head, "How I sped
  * up convolutions", class listing): out[n, o] = sum_c mean_hw(x[n,:,:,c]) *
  * fc_w[o, c] + fc_b[o].  x: NHWC view; fc_w DEVICE [out_features, x->c]
