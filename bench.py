@@ -3,10 +3,14 @@
 Default workload (N=1): the depthwise 3x3 + BN + ReLU layer, NHWC fp32,
 x = [64, 56, 56, 384] ~ N(0,1), at stride 1 and stride 2; one step = both
 launches over the batch.  ``value`` is algorithmic HBM bytes per second
-(input + output + weights + scale/bias, per workloads.py) over the timed
-steps, whole job (all ranks).  Other workloads (``--workload``) measure the
-dense 3x3 sweep, the DepthwiseMNIST forward, the YOLO-style chain and the
-preprocess -> stem pipeline.
+(input + output + weights + scale/bias, see conv_bn_activation_gb300/
+workloads.py) over the timed steps, whole job (all ranks).
+
+Other workloads (``--workload``) measure the rest of the hot path:
+  dense       the dense 3x3 + BN + SiLU sweep at batch 16 (TFLOP/s, tensor cores)
+  mnist       the DepthwiseMNIST forward at batch 64, replayed as a CUDA graph (images/s)
+  yolo        the 20-conv YOLO-style chain at batch 32, 640x640 (images/s)
+  preprocess  fused u8 preprocess -> stem conv at batch 32 (GB/s on the page's ledger)
 
 Multi-GPU (torchrun): images are independent, so every rank runs its own
 batch (weak scaling, no data-path collective); ranks meet only at the
@@ -31,9 +35,11 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+METRIC = "fused conv+BN+act: achieved GB/s or TFLOP/s vs roofline; images/sec"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rates
+UNIT_SCALE = {"GB/s": 1e9, "TFLOP/s": 1e12, "images/s": 1.0}
 
 
 def load_peaks():
@@ -44,6 +50,10 @@ def load_peaks():
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
     return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
             "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def tf32_peak(peaks, sustained=False):
+    return (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]) * TF32_OVER_BF16
 
 
 # ------------------------------------------------------------ clocks sampler
@@ -112,7 +122,6 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples), "source": "nvml"}
 
 
-# ------------------------------------------------------------ distributed
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -120,7 +129,6 @@ def dist_setup():
     return world, rank, local
 
 
-# ------------------------------------------------------------ workloads
 def kernel_source_hash(files):
     h = hashlib.sha256()
     for f in files:
@@ -141,38 +149,97 @@ def profiled_traffic(profile_name, src_files):
     return int(m_tr.group(1))
 
 
-class DepthwiseWorkload:
-    name = "depthwise3x3_bn_relu"
+# ------------------------------------------------------------ workloads
+class Launch:
+    def __init__(self, name, fn, work, kernel, bound):
+        self.name, self.fn, self.work, self.kernel, self.bound = name, fn, work, kernel, bound
+
+
+class Workload:
+    """A step = the listed launches, in order, on one stream."""
+    unit = "GB/s"
+    profile = None          # (profiles/ file, kernel source files) for the roofline's traffic figure
+    dominant = None         # launch name whose roofline is reported
+
+    def run(self, stream, events=None):
+        for i, L in enumerate(self.launches):
+            if events:
+                events[i].record(stream)
+            L.fn(stream)
+        if events:
+            events[len(self.launches)].record(stream)
+
+    def step_units(self):
+        if self.unit == "GB/s":
+            return sum(L.work.bytes for L in self.launches)
+        if self.unit == "TFLOP/s":
+            return sum(L.work.flops for L in self.launches)
+        return self.batch
+
+    def launch_roofline(self, L, ms, peaks):
+        if L.bound == "tensor":
+            achieved = L.work.flops / (ms * 1e-3) / 1e12
+            peak = tf32_peak(peaks)
+            bw_roof = L.work.bytes / (ms * 1e-3) / 1e9
+            return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4),
+                    "frac_of_min_roof": round(achieved / min(peak, L.work.intensity * peaks["hbm_gbs"] / 1e3), 4),
+                    "hbm_gbs": round(bw_roof, 1), "intensity": round(L.work.intensity, 2)}
+        achieved = L.work.bytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4)}
+
+    def roofline(self, launch_ms, peaks):
+        L = next(l for l in self.launches if l.name == self.dominant) if self.dominant else \
+            max(self.launches, key=lambda l: launch_ms[l.name])
+        r = self.launch_roofline(L, launch_ms[L.name], peaks)
+        r["kernel"] = f"{L.kernel} ({L.name})"
+        r["algorithmic_bytes" if r["bound"] == "hbm" else "algorithmic_flops"] = \
+            L.work.bytes if r["bound"] == "hbm" else L.work.flops
+        r["traffic"] = profiled_traffic(*self.profile) if self.profile else None
+        if r["bound"] == "hbm":
+            r["peak_source"] = f"{peaks['source']} hbm_gbs (copy-kernel burst)"
+        else:
+            r["peak_source"] = f"{peaks['source']} bf16_tflops x 1.1/2.25 (nominal TF32/BF16 ratio)"
+        return r
+
+    def per_launch(self, launch_ms, peaks):
+        out = {}
+        for L in self.launches:
+            r = self.launch_roofline(L, launch_ms[L.name], peaks)
+            out[L.name] = {"us": round(launch_ms[L.name] * 1e3, 2), "kernel": L.kernel, "bound": r["bound"],
+                           "achieved": r["achieved"], "unit": r["unit"], "frac": r["frac"]}
+            if "frac_of_min_roof" in r:
+                out[L.name]["frac_of_min_roof"] = r["frac_of_min_roof"]
+        return out
+
+
+def _t(torch, a, device):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class DepthwiseWorkload(Workload):
+    unit = "GB/s"
+    dominant = "s1"
+    profile = ("dw_tma_kernel_depthwise_64x56x56x384.md", ["dw_conv.cu", "ptx.cuh", "epilogue.cuh"])
 
     def __init__(self, torch, device, batch=64):
         from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
         from conv_bn_activation_gb300.nets import ConvBnAct
-        self.torch = torch
-        self.x_host, w, bn = synthetic.depthwise_layer(N=batch)
-        self.w, self.bn = w, bn
-        self.batch = batch
-        self.x = torch.from_numpy(self.x_host).to(device)
-        self.l1 = ConvBnAct(w, bn, 1, 1, cb.ACT_RELU, groups=384, device=device)
-        self.l2 = ConvBnAct(w, bn, 2, 1, cb.ACT_RELU, groups=384, device=device)
+        self.torch, self.batch = torch, batch
+        self.x_host, self.w, self.bn = synthetic.depthwise_layer(N=batch)
+        self.x = _t(torch, self.x_host, device)
+        self.l1 = ConvBnAct(self.w, self.bn, 1, 1, cb.ACT_RELU, groups=384, device=device)
+        self.l2 = ConvBnAct(self.w, self.bn, 2, 1, cb.ACT_RELU, groups=384, device=device)
         self.y1 = torch.empty(batch, 56, 56, 384, device=device)
         self.y2 = torch.empty(batch, 28, 28, 384, device=device)
         wl = workloads.depthwise_workload(N=batch)
-        self.work = {"s1": wl["s1"], "s2": wl["s2"]}
-        self.step_bytes = wl["s1"].bytes + wl["s2"].bytes
-        self.launches = ["s1", "s2"]
+        self.launches = [
+            Launch("s1", lambda s: self.l1(self.x, self.y1, stream=s), wl["s1"], "cb::dw_tma_kernel<1,RELU,NONE>", "hbm"),
+            Launch("s2", lambda s: self.l2(self.x, self.y2, stream=s), wl["s2"], "cb::dw_tma_kernel<2,RELU,NONE>", "hbm"),
+        ]
         self.config = {"workload": "depthwise 3x3 + BN + ReLU, NHWC fp32, N=64 C=384 56x56, stride 1 and 2",
                        "batch": batch, "l2": "inputs_larger_than_l2 (308 MB input, 129 MB L2)"}
-        self.unit, self.per_image = "GB/s", True
-
-    def run(self, stream, events=None):
-        if events:
-            events[0].record(stream)
-        self.l1(self.x, self.y1, stream=stream)
-        if events:
-            events[1].record(stream)
-        self.l2(self.x, self.y2, stream=stream)
-        if events:
-            events[2].record(stream)
 
     def e2e_setup(self):
         t = self.torch
@@ -187,30 +254,234 @@ class DepthwiseWorkload:
         self.y1_pin.copy_(self.y1, non_blocking=True)
         self.y2_pin.copy_(self.y2, non_blocking=True)
 
-    def roofline(self, launch_ms, peaks, gpu_launch_name="s1"):
-        ms = launch_ms[gpu_launch_name]
-        achieved = self.work[gpu_launch_name].bytes / (ms * 1e-3) / 1e9
-        traffic = profiled_traffic("dw_tma_kernel_depthwise_64x56x56x384.md", ["dw_conv.cu", "ptx.cuh", "epilogue.cuh"])
-        return {"bound": "hbm", "kernel": "cb::dw_tma_kernel<1> (stride 1 launch)", "achieved": round(achieved, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic, "algorithmic_bytes": self.work[gpu_launch_name].bytes,
-                "peak_source": f"{peaks['source']} hbm_gbs (copy-kernel burst)"}
-
-    def cpu_sample(self, n_images):
+    def cpu_sample(self, n):
         import oracle
-        x = self.x_host[:n_images]
+        x = self.x_host[:n]
         t0 = time.perf_counter()
         oracle.conv_bn_act(x, self.w, self.bn, stride=1, pad=1, groups=384, act=oracle.ACT_RELU)
         oracle.conv_bn_act(x, self.w, self.bn, stride=2, pad=1, groups=384, act=oracle.ACT_RELU)
-        dt = time.perf_counter() - t0
-        return dt, self.step_bytes * n_images / self.batch
+        return time.perf_counter() - t0, self.step_units() * n / self.batch, f"{n} of {self.batch} images"
 
 
-def make_workload(name, torch, device):
-    if name == "depthwise":
-        return DepthwiseWorkload(torch, device)
-    from bench_workloads import make  # the other measurement workloads
-    return make(name, torch, device)
+class DenseWorkload(Workload):
+    unit = "TFLOP/s"
+    dominant = "256-256@20_s1"
+
+    def __init__(self, torch, device, batch=16):
+        from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
+        from conv_bn_activation_gb300.nets import ConvBnAct
+        self.torch, self.batch = torch, batch
+        self.layers = []
+        self.launches = []
+        for (ci, co, H, s) in synthetic.DENSE_SWEEP:
+            x, w, bn = synthetic.dense_layer(ci, co, H, N=batch, k=3)
+            L = ConvBnAct(w, bn, s, 1, cb.ACT_SILU, device=device)
+            OH, OW = L.out_hw(H, H)
+            rec = {"x_host": x, "w": w, "bn": bn, "s": s, "x": _t(torch, x, device),
+                   "y": torch.empty(batch, OH, OW, co, device=device), "L": L}
+            self.layers.append(rec)
+            name = f"{ci}-{co}@{H}_s{s}"
+            tc = ci % 4 == 0 and ci >= 16
+            self.launches.append(Launch(name, (lambda r: lambda st: r["L"](r["x"], r["y"], stream=st))(rec),
+                                        workloads.conv_layer(batch, H, H, ci, co, 3, s, 1),
+                                        "cb::igemm_tf32_kernel" if tc else "cb::direct_conv_kernel",
+                                        "tensor" if tc else "hbm"))
+        self.config = {"workload": "dense 3x3 + BN + SiLU sweep, NHWC fp32 storage, TF32 tensor cores, batch 16",
+                       "batch": batch, "l2": "warm (per-layer working sets 15-180 MB; steps run back to back)"}
+
+    def e2e_setup(self):
+        t = self.torch
+        h2d = d2h = 0
+        for r in self.layers:
+            r["x_pin"] = t.from_numpy(r["x_host"]).pin_memory()
+            r["y_pin"] = t.empty(tuple(r["y"].shape), pin_memory=True)
+            h2d += r["x_pin"].numel() * 4
+            d2h += r["y_pin"].numel() * 4
+        return h2d, d2h
+
+    def e2e_step(self, stream):
+        for r in self.layers:
+            r["x"].copy_(r["x_pin"], non_blocking=True)
+        self.run(stream)
+        for r in self.layers:
+            r["y_pin"].copy_(r["y"], non_blocking=True)
+
+    def cpu_sample(self, n):
+        import oracle
+        t0 = time.perf_counter()
+        for r in self.layers:
+            oracle.conv_bn_act(r["x_host"][:n], r["w"], r["bn"], stride=r["s"], pad=1, act=oracle.ACT_SILU)
+        return time.perf_counter() - t0, self.step_units() * n / self.batch, f"{n} of {self.batch} images per layer"
+
+
+class MnistWorkload(Workload):
+    """The whole DepthwiseMNIST forward, replayed as one CUDA graph per step."""
+    unit = "images/s"
+
+    def __init__(self, torch, device, batch=64):
+        from conv_bn_activation_gb300 import synthetic, workloads
+        from conv_bn_activation_gb300.nets import MnistNet
+        self.torch, self.batch = torch, batch
+        self.params = synthetic.mnist_params()
+        self.x_host = synthetic.mnist_input(batch)
+        self.x = _t(torch, self.x_host, device)
+        self.net = MnistNet(self.params, batch, device=device)
+        self.net.forward(self.x)
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(side):
+            self.net.forward(self.x)
+        torch.cuda.current_stream(device).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.net.forward(self.x)
+        total = workloads.total(workloads.mnist_layers(N=batch))
+        self.launches = [Launch("forward_graph", lambda s: self.graph.replay(), total,
+                                "CUDA graph: stem + 4 blocks + pool/fc (13 kernels)", "hbm")]
+        self.kernels_per_step = 13
+        self.config = {"workload": "DepthwiseMNIST forward (stem, 4 depthwise-separable blocks, avgpool+fc), fp32",
+                       "batch": batch, "l2": "warm (whole net ~40 MB fits in L2; graph replay back to back)"}
+
+    def e2e_setup(self):
+        self.x_pin = self.torch.from_numpy(self.x_host).pin_memory()
+        self.out_pin = self.torch.empty(self.batch, 10, pin_memory=True)
+        return self.x_pin.numel() * 4, self.out_pin.numel() * 4
+
+    def e2e_step(self, stream):
+        self.x.copy_(self.x_pin, non_blocking=True)
+        self.run(stream)
+        self.out_pin.copy_(self.net.logits, non_blocking=True)
+
+    def cpu_sample(self, n):
+        import oracle
+        t0 = time.perf_counter()
+        oracle.mnist_model(self.x_host[:n], self.params)
+        return time.perf_counter() - t0, n, f"{n} of {self.batch} images"
+
+
+class YoloWorkload(Workload):
+    unit = "images/s"
+
+    def __init__(self, torch, device, batch=32):
+        from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
+        from conv_bn_activation_gb300.nets import YoloChain
+        self.torch, self.batch = torch, batch
+        self.stages = synthetic.yolo_params()
+        self.x_host = synthetic.yolo_input(batch)
+        self.x = _t(torch, self.x_host, device)
+        self.chain = YoloChain(self.stages, batch, device=device)
+        works = dict(workloads.yolo_layers(N=batch))
+        self.launches = []
+        prev = lambda: self.x
+        for i, (L, B) in enumerate(zip(self.chain.layers, self.chain.bufs)):
+            half = B["half"]
+            a, b = B["cat"][..., :half], B["cat"][..., half:]
+            x_in = prev
+            steps = [
+                ("down", (lambda L=L, B=B, x_in=x_in: lambda s: L["down"](x_in(), B["x1"], stream=s))()),
+                ("cv1", (lambda L=L, B=B, a=a: lambda s: L["cv1"](B["x1"], a, stream=s))()),
+                ("cv2", (lambda L=L, a=a, b=b: lambda s: L["cv2"](a, b, stream=s))()),
+                ("cv3", (lambda L=L, B=B: lambda s: L["cv3"](B["cat"], B["out"], residual=B["x1"],
+                                                             res_mode=cb.RES_POST_ACT, stream=s))()),
+            ]
+            for nm, fn in steps:
+                cin = L[nm].cin
+                tc = cin % 4 == 0 and cin >= 16
+                self.launches.append(Launch(f"s{i}.{nm}", fn, works[f"s{i}.{nm}"],
+                                            "cb::igemm_tf32_kernel" if tc else "cb::direct_conv_kernel",
+                                            "tensor" if tc else "hbm"))
+            prev = (lambda B=B: lambda: B["out"])()
+        self.config = {"workload": "YOLO-style 20-conv chain (5 stages, concat via channel views, post-act "
+                                   "residual), 640x640x3 fp32", "batch": batch,
+                       "l2": "inputs_larger_than_l2 (157 MB input, 1.2 GB of activations per step)"}
+
+    def e2e_setup(self):
+        self.x_pin = self.torch.from_numpy(self.x_host).pin_memory()
+        out = self.chain.bufs[-1]["out"]
+        self.out_pin = self.torch.empty(tuple(out.shape), pin_memory=True)
+        return self.x_pin.numel() * 4, self.out_pin.numel() * 4
+
+    def e2e_step(self, stream):
+        self.x.copy_(self.x_pin, non_blocking=True)
+        self.run(stream)
+        self.out_pin.copy_(self.chain.bufs[-1]["out"], non_blocking=True)
+
+    def cpu_sample(self, n):
+        import oracle
+        t0 = time.perf_counter()
+        h = self.x_host[:n]
+        for st in self.stages:
+            h = oracle.yolo_stage(h, st).astype(np.float32)
+        return time.perf_counter() - t0, n, f"{n} of {self.batch} images"
+
+
+class PreprocessWorkload(Workload):
+    unit = "GB/s"
+    dominant = "preprocess_fused"
+
+    def __init__(self, torch, device, batch=32):
+        from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
+        from conv_bn_activation_gb300.nets import PreprocessStem
+        self.torch, self.batch = torch, batch
+        self.frames_host = synthetic.preprocess_frames(N=batch)
+        self.frames = _t(torch, self.frames_host, device)
+        self.sw, self.sbn = synthetic.stem_params()
+        self.net = PreprocessStem(self.sw, self.sbn, batch, device=device)
+        self.net.tmp_u8 = torch.empty(batch, 480, 640, 3, dtype=torch.uint8, device=device)
+        self.net.tmp_f32 = torch.empty(batch, 480, 640, 3, device=device)
+        pre = workloads.preprocess_fused(batch, 720, 1280, 480, 640)
+        stem = workloads.conv_layer(batch, 480, 640, 3, 16, 3, 2, 1)
+        self.launches = [
+            Launch("preprocess_fused", lambda s: cb.preprocess_u8(self.frames, self.net.planar, stream=s), pre,
+                   "cb::preprocess_row_kernel<false>", "hbm"),
+            Launch("stem_conv", lambda s: self.net.stem(self.net.planar, self.net.out, stream=s,
+                                                        x_layout=cb.LAYOUT_NCHW), stem,
+                   "cb::direct_conv_kernel<16>", "hbm"),
+        ]
+        self.three_pass = workloads.preprocess_unfused(batch, 720, 1280, 480, 640)
+        self.config = {"workload": "fused u8 preprocess 1280x720 -> 640x480 NCHW fp32 + stem conv3x3 s2 3->16 "
+                                   "+ BN + SiLU", "batch": batch,
+                       "l2": "inputs_larger_than_l2 (88 MB frames + 118 MB planar + 157 MB stem out)"}
+
+    def extra(self, torch, stream, steps):
+        """The three-pass comparison path, timed the same way (not part of the step)."""
+        from conv_bn_activation_gb300 import binding as cb
+        fn = lambda: cb.preprocess_u8_three_pass(self.frames, self.net.tmp_u8, self.net.tmp_f32, self.net.planar,
+                                                 stream=stream)
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        return {"three_pass_us": round(ms * 1e3, 2),
+                "three_pass_gbs_on_its_ledger": round(self.three_pass.bytes / (ms * 1e-3) / 1e9, 1),
+                "ledger_bytes_per_frame": {"fused": 6451200, "three_pass": 15667200}}
+
+    def e2e_setup(self):
+        self.f_pin = self.torch.from_numpy(self.frames_host).pin_memory()
+        self.out_pin = self.torch.empty(tuple(self.net.out.shape), pin_memory=True)
+        return self.f_pin.numel(), self.out_pin.numel() * 4
+
+    def e2e_step(self, stream):
+        self.frames.copy_(self.f_pin, non_blocking=True)
+        self.run(stream)
+        self.out_pin.copy_(self.net.out, non_blocking=True)
+
+    def cpu_sample(self, n):
+        import oracle
+        t0 = time.perf_counter()
+        planar = oracle.preprocess_u8(self.frames_host[:n], 480, 640, oracle.PREC_F32)
+        oracle.conv_bn_act(planar, self.sw, self.sbn, stride=2, pad=1, act=oracle.ACT_SILU, layout=oracle.NCHW)
+        return time.perf_counter() - t0, self.step_units() * n / self.batch, f"{n} of {self.batch} frames"
+
+
+WORKLOADS = {"depthwise": DepthwiseWorkload, "dense": DenseWorkload, "mnist": MnistWorkload,
+             "yolo": YoloWorkload, "preprocess": PreprocessWorkload}
 
 
 # ------------------------------------------------------------ arms
@@ -228,7 +499,7 @@ def run_ours(args):
     binding.load()
     peaks = load_peaks()
 
-    wl = make_workload(args.workload, torch, device)
+    wl = WORKLOADS[args.workload](torch, device)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
         wl.run(stream)
@@ -243,24 +514,23 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    t_host0 = time.perf_counter()
     for k in range(args.steps):
         wl.run(stream, events[k])
     torch.cuda.synchronize()
-    t_host = time.perf_counter() - t_host0
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
     step_ms = [events[k][0].elapsed_time(events[k][nl]) for k in range(args.steps)]
     total_ms = events[0][0].elapsed_time(events[-1][nl])
-    launch_ms = {name: statistics.mean(events[k][i].elapsed_time(events[k][i + 1]) for k in range(args.steps))
-                 for i, name in enumerate(wl.launches)}
+    launch_ms = {L.name: statistics.mean(events[k][i].elapsed_time(events[k][i + 1]) for k in range(args.steps))
+                 for i, L in enumerate(wl.launches)}
     if binding.get_device_error() != binding.OK:
         raise RuntimeError("device error during the timed steps")
+    extra = wl.extra(torch, stream, args.steps) if hasattr(wl, "extra") else None
 
     # e2e: host buffers, copies inside the timed region
     h2d, d2h = wl.e2e_setup()
-    for _ in range(max(1, args.warmup // 2)):
+    for _ in range(3):
         wl.e2e_step(stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -275,39 +545,41 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
-    units = wl.step_bytes * args.steps
+    units = wl.step_units() * args.steps
+    e2e_units = wl.step_units()
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms, e2e_ms = float(t[0]), float(t[1])
-        u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+        u = torch.tensor([float(units), float(e2e_units)], dtype=torch.float64, device=device)
         dist.all_reduce(u)
-        units = float(u[0])
+        units, e2e_units = float(u[0]), float(u[1])
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
 
-    value = units / (total_ms * 1e-3) / 1e9
-    e2e_value = wl.step_bytes * world / (e2e_ms * 1e-3) / 1e9
+    scale = UNIT_SCALE[wl.unit]
+    value = units / (total_ms * 1e-3) / scale
     line = {
-        "metric": "fused conv+BN+act: achieved GB/s or TFLOP/s vs roofline; images/sec",
-        "value": round(value, 2), "unit": wl.unit, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": round(value, 3), "unit": wl.unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(wl.config, parallelism=f"replicas x{world} (independent images, no collective)"),
         "images_per_s": round(wl.batch * world * args.steps / (total_ms * 1e-3), 1),
+        "us_per_image": round(total_ms * 1e3 / args.steps / wl.batch, 3),
         "step_ms": {"median": round(statistics.median(step_ms), 4), "min": round(min(step_ms), 4),
                     "max": round(max(step_ms), 4)},
-        "launch_ms": {k: round(v, 4) for k, v in launch_ms.items()},
+        "launches": wl.per_launch(launch_ms, peaks),
         "roofline": wl.roofline(launch_ms, peaks),
-        "e2e": {"value": round(e2e_value, 3), "unit": wl.unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 3)},
-        "gpu_launches": nl * args.steps,
+        "e2e": {"value": round(e2e_units / (e2e_ms * 1e-3) / scale, 3), "unit": wl.unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": getattr(wl, "kernels_per_step", nl) * args.steps,
         "clocks": clocks,
-        "host_wall_s": round(t_host, 3),
     }
+    if extra:
+        line["comparison"] = extra
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     print(json.dumps(line), flush=True)
@@ -316,14 +588,14 @@ def run_ours(args):
 
 
 def cpu_baseline(wl, target_s=12.0):
+    """The oracle as it stands, on the host cores, on a bounded sample of the workload."""
     import oracle
     oracle.build()
-    dt1, _ = wl.cpu_sample(1)
+    dt1, _, _ = wl.cpu_sample(1)
     n = int(max(1, min(wl.batch, target_s / max(dt1, 1e-3))))
-    dt, nbytes = wl.cpu_sample(n)
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": wl.unit, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} of {wl.batch} images of the same workload (fp64 oracle, OpenMP)",
-            "seconds": round(dt, 2)}
+    dt, units, what = wl.cpu_sample(n) if n > 1 else wl.cpu_sample(1)
+    return {"value": round(units / dt / UNIT_SCALE[wl.unit], 6), "unit": wl.unit, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{what} of the same workload (fp64 oracle, OpenMP)", "seconds": round(dt, 2)}
 
 
 def run_reference(args):
@@ -333,46 +605,40 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
+    from conv_bn_activation_gb300 import synthetic, workloads
+    if args.workload != "depthwise":
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm is timed on the default "
+                          "(depthwise) workload only"}))
+        return
+    x, w, bn = synthetic.depthwise_layer()
+    wl = workloads.depthwise_workload()
+    n = 1
+    step_bytes = (wl["s1"].bytes + wl["s2"].bytes) * n // 64
 
-    wl = ReferenceDepthwise()
+    def step():
+        xs = x[:n]
+        oracle.conv_bn_act(xs, w, bn, stride=1, pad=1, groups=384, act=oracle.ACT_RELU)
+        oracle.conv_bn_act(xs, w, bn, stride=2, pad=1, groups=384, act=oracle.ACT_RELU)
+
     for _ in range(args.warmup):
-        wl.step()
+        step()
     t0 = time.perf_counter()
-    nbytes = 0
     for _ in range(args.steps):
-        nbytes += wl.step()
+        step()
     dt = time.perf_counter() - t0
-    value = nbytes / dt / 1e9
+    value = step_bytes * args.steps / dt / 1e9
     line = {
-        "impl": "reference",
-        "metric": "fused conv+BN+act: achieved GB/s or TFLOP/s vs roofline; images/sec",
-        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "depthwise 3x3 + BN + ReLU, NHWC fp32, N=64 C=384 56x56, stride 1 and 2",
                    "batch": 64, "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": f"{wl.n} image(s) of the 64-image batch per step, stride 1 and 2"},
+                         "sample": f"{n} image of the 64-image batch per step, stride 1 and 2"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
-
-
-class ReferenceDepthwise:
-    def __init__(self, n=1):
-        from conv_bn_activation_gb300 import synthetic, workloads
-        self.x, self.w, self.bn = synthetic.depthwise_layer()
-        self.n = n
-        wl = workloads.depthwise_workload()
-        self.bytes = (wl["s1"].bytes + wl["s2"].bytes) * n // 64
-
-    def step(self):
-        import oracle
-        x = self.x[:self.n]
-        oracle.conv_bn_act(x, self.w, self.bn, stride=1, pad=1, groups=384, act=oracle.ACT_RELU)
-        oracle.conv_bn_act(x, self.w, self.bn, stride=2, pad=1, groups=384, act=oracle.ACT_RELU)
-        return self.bytes
 
 
 def main():
@@ -381,12 +647,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="depthwise",
-                    choices=["depthwise", "dense", "mnist", "yolo", "preprocess"])
+    ap.add_argument("--workload", default="depthwise", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
+    args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference(args)
     else:
