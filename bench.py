@@ -387,7 +387,7 @@ class YoloWorkload(Workload):
             ]
             for nm, fn in steps:
                 cin = L[nm].cin
-                tc = cin % 4 == 0 and cin >= 16
+                tc = cin % 4 == 0 and cin >= (8 if L[nm].k == 1 else 16)
                 self.launches.append(Launch(f"s{i}.{nm}", fn, works[f"s{i}.{nm}"],
                                             "cb::igemm_tf32_kernel" if tc else "cb::direct_conv_kernel",
                                             "tensor" if tc else "hbm"))

@@ -32,8 +32,14 @@ def nvcc() -> str:
 
 
 def _flags():
+    extra = os.environ.get("CB_NVCC_EXTRA", "").split()  # e.g. -DCB_IGEMM_TRACE (profiling builds)
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
-                   "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
+                   "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"] + extra
+
+
+def _flag_tag():
+    import hashlib
+    return hashlib.sha1(" ".join(_flags()).encode()).hexdigest()[:8]
 
 
 def _headers():
@@ -49,7 +55,7 @@ def _stale(target: str, deps) -> bool:
 
 
 def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+    obj = os.path.join(BUILD, os.path.basename(src) + "." + _flag_tag() + ".o")
     if _stale(obj, [src] + _headers()):
         cmd = [nvcc()] + _flags() + ["-c", src, "-o", obj + ".tmp"]
         if verbose:
@@ -68,6 +74,10 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     with _lock:
         os.makedirs(BUILD, exist_ok=True)
         srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+        stamp = os.path.join(BUILD, "last_flags")
+        tag = _flag_tag()
+        if os.path.exists(stamp) and open(stamp).read() != tag:
+            force = True
         if force:
             for o in glob.glob(os.path.join(BUILD, "*.o")):
                 os.remove(o)
@@ -80,6 +90,7 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
             if r.returncode != 0:
                 raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
             os.replace(tmp, LIB)
+        open(stamp, "w").write(tag)
         return LIB
 
 

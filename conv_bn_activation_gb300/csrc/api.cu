@@ -184,6 +184,13 @@ OutView make_out(const cb_tensor* y) {
   return o;
 }
 
+// Which dense layers go to the tensor cores.  The copy engine's cost per
+// K step grows with the number of 128-pixel rows it gathers, not with their
+// width, so a 3x3 layer with under 16 input channels (nine narrow gathers
+// per tile) runs faster on the CUDA-core direct kernel; 1x1 layers take the
+// tensor cores from 8 channels on.
+bool tc_channels_ok(int ci, int k) { return k == 1 ? ci >= 8 : ci >= 16; }
+
 // ----------------------------------------------------------------- depthwise
 cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, int stride, int pad,
                         const cb_tensor* y, cudaStream_t s) {
@@ -322,7 +329,8 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
   a.Cout = Co;
   a.kw = k;
   a.taps = k * k;
-  a.num_kc = (Ci + 31) / 32;
+  const int kc = Ci <= 8 ? 8 : (Ci <= 16 ? 16 : 32);  // channels per K step: no padding channels for 8 / 16
+  a.num_kc = (Ci + kc - 1) / kc;
   a.k_iters = a.taps * a.num_kc;
   a.stride = stride;
   a.pad = pad;
@@ -330,18 +338,35 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
   a.ep = ep;
   a.err = dev->err;
   a.timeout_ns = timeout_ns();
+  if (const char* t = std::getenv("CB_IGEMM_TRACE")) {  // profiling aid: timeline of one CTA
+    a.trace = 1;
+    a.trace_cta = std::atoi(t);
+  }
   a.vec_store = (aligned16(a.out.y) && strides_mult4(y) && aligned16(ep.scale) && aligned16(ep.bias) &&
                  (ep.res_mode == 0 || (aligned16(ep.r) && ep.rs_n % 4 == 0 && ep.rs_h % 4 == 0 && ep.rs_w % 4 == 0)))
                     ? 1
                     : 0;
   int n_tiles = 1;
-  const int bn = pick_bn(a.M, Co, a.k_iters, dev->sms, &n_tiles);
+  int bn = pick_bn(a.M, Co, a.k_iters, dev->sms, &n_tiles);
+  // Tuning override (CB_IGEMM_FORCE="bn,stages,grid"; 0 = free), read per call.
+  int force_bn = 0, force_stages = 0, force_grid = 0;
+  if (const char* f = std::getenv("CB_IGEMM_FORCE")) std::sscanf(f, "%d,%d,%d", &force_bn, &force_stages, &force_grid);
+  if (force_bn == 16 || force_bn == 32 || force_bn == 48 || force_bn == 64 || force_bn == 96 || force_bn == 128 ||
+      force_bn == 192 || force_bn == 256) {
+    bn = force_bn;
+    n_tiles = (Co + bn - 1) / bn;
+  }
   a.m_tiles = (a.M + 127) / 128;
   a.n_tiles = n_tiles;
-  a.stages = igemm_stages(bn);
-  const size_t smem = igemm_smem_bytes(bn, a.stages);
+  a.stages = igemm_stages(bn, kc);
+  if (force_stages >= 2 && igemm_smem_bytes(bn, kc, force_stages) <= 227 * 1024) a.stages = force_stages;
+  const size_t smem = igemm_smem_bytes(bn, kc, a.stages);
   const long long tiles = static_cast<long long>(a.m_tiles) * a.n_tiles;
-  const int grid = static_cast<int>(std::min<long long>(tiles, dev->sms));
+  int grid = static_cast<int>(std::min<long long>(tiles, dev->sms));
+  if (force_grid > 0 && force_grid < grid) grid = force_grid;
+  if (std::getenv("CB_DEBUG_PLAN"))
+    std::fprintf(stderr, "[cb] igemm plan: M=%d Ci=%d Co=%d k=%d s=%d -> bn=%d kc=%d n_tiles=%d m_tiles=%d stages=%d grid=%d\n",
+                 a.M, Ci, Co, k, stride, bn, kc, n_tiles, a.m_tiles, a.stages, grid);
 
   CUtensorMap amap, bmap;
   {
@@ -352,22 +377,28 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
     int lower[2] = {-pad, -pad};
     int upper[2] = {pad - (k - 1), pad - (k - 1)};
     cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(stride), static_cast<cuuint32_t>(stride), 1};
-    CUresult r = encode_im2col()(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x->data, dims, strides, lower, upper, 32,
-                                 128, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    const CUtensorMapSwizzle swz = kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+    CUresult r = encode_im2col()(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x->data, dims, strides, lower, upper,
+                                 static_cast<cuuint32_t>(kc), 128, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(k * k), static_cast<cuuint64_t>(Co)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(Ci) * 4, static_cast<cuuint64_t>(k * k) * Ci * 4};
-    cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(bn)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kc), 1, static_cast<cuuint32_t>(bn)};
     cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle swz = kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
     CUresult r = encode_tiled()(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(w), dims, strides, box,
-                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
-  cudaError_t e = launch_igemm(amap, bmap, a, bn, grid, smem, s);
+  cudaError_t e = launch_igemm(amap, bmap, a, bn, kc, grid, smem, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
 
@@ -486,7 +517,8 @@ cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale,
     if (kh != 3 || x->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
     return run_depthwise(x, w, ep, stride, pad, y, s);
   }
-  const bool tc_ok = policy != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && x->c >= 16 && aligned16(x->data) &&
+  const bool tc_ok = policy != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && tc_channels_ok(x->c, kh) &&
+                     aligned16(x->data) &&
                      aligned16(w) && strides_mult4(x) && x->n <= 65535 && x->w <= 65535 && x->h <= 65535 &&
                      encode_tiled() && encode_im2col();
   if (tc_ok) return run_igemm(x, w, ep, kh, stride, pad, y, s);
@@ -677,9 +709,16 @@ cb_status cb_set_kernel_policy(int policy) {
 
 int cb_get_kernel_policy(void) { return g_policy.load(); }
 
+// Profiling aid (not part of cb.h): copies out the implicit-GEMM timeline
+// recorded while CB_IGEMM_TRACE is set; returns the number of records.
+int cb_debug_igemm_trace(unsigned long long* out, int max_records) {
+  cudaDeviceSynchronize();
+  return igemm_read_trace(out, max_records);
+}
+
 int cb_conv_uses_tensor_cores(const cb_tensor* x, int kh, int groups) {
   if (!view_ok(x) || groups != 1 || (kh != 1 && kh != 3)) return 0;
-  return g_policy.load() != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && x->c >= 16 &&
+  return g_policy.load() != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && tc_channels_ok(x->c, kh) &&
                  aligned16(x->data) && strides_mult4(x)
              ? 1
              : 0;

@@ -7,7 +7,8 @@
 //
 //  * dw_tma_kernel (the fast path): persistent CTAs.  A work item is one
 //    image, one 32-channel chunk (128 bytes per pixel), one strip of output
-//    rows and one tile of output columns.  A producer thread streams the
+//    rows and one tile of output columns.  Four producer lanes (taking rows
+//    in turn: one thread's copies complete one after another) stream the
 //    strip's input rows -- the full padded width of the tile, halo columns
 //    included -- into a shared-memory ring with 4-D TMA tile copies; the
 //    copy's out-of-range zero fill supplies the padding.  Each consumer
@@ -113,6 +114,8 @@ __device__ __forceinline__ DwItem dw_decode(const DwTmaParams& p, int item) {
   return it;
 }
 
+constexpr int kDwProducerLanes = 4;
+
 template <int ACT, int RES>
 __device__ __forceinline__ float epi_c(float acc, float sc, float bi, float r) {
   float z = fmaf(acc, sc, bi);
@@ -152,8 +155,12 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      tma_prefetch_desc(&xmap);
+    // Copies issued by one thread complete one after another, so
+    // kDwProducerLanes lanes share the rows, each owning the ring slots s with
+    // s % kDwProducerLanes == lane (one owner per slot keeps each lane's
+    // barrier phases its own).
+    if (lane < kDwProducerLanes) {
+      if (lane == 0) tma_prefetch_desc(&xmap);
       int slot = 0;
       uint32_t phase = 0, issued = 0, last_parity = 0;
       bool ok = true;
@@ -162,22 +169,24 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
         const int nrows = (it.oh1 - it.oh0 - 1) * S + 3;
         const int ih0 = it.oh0 * S - a.pad;
         const int iw0 = it.ow0 * S - a.pad;
-        for (int j = 0; j < nrows; ++j) {
-          if (!mbar_wait(&empty[slot], phase ^ 1u, wd)) {
-            ok = false;
-            break;
+        for (int r = 0; r < nrows; ++r) {
+          if (slot % kDwProducerLanes == lane) {
+            if (!mbar_wait(&empty[slot], phase ^ 1u, wd)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_bytes));
+            tma_load_4d(ring + slot * stage_bytes, &xmap, &full[slot], it.c0, iw0, ih0 + r, it.n);
+            issued |= 1u << slot;
+            last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
           }
-          mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(stage_bytes));
-          tma_load_4d(ring + slot * stage_bytes, &xmap, &full[slot], it.c0, iw0, ih0 + j, it.n);
-          issued |= 1u << slot;
-          last_parity = (last_parity & ~(1u << slot)) | (phase << slot);
           if (++slot == p.stages) {
             slot = 0;
             phase ^= 1u;
           }
         }
       }
-      // Let every copy this thread issued land before the CTA can exit.
+      // Let every copy this lane issued land before the CTA can exit.
       for (int s = 0; s < p.stages; ++s)
         if (issued & (1u << s)) mbar_wait_drain(&full[s], (last_parity >> s) & 1u, 20000000ull);
     }

@@ -1,0 +1,434 @@
+// Dense convolution (kh x kw = 1x1 or 3x3, stride 1 or 2, groups 1) as an
+// implicit GEMM on the 5th-generation tensor cores, with the folded-BN /
+// residual / activation epilogue fused.
+//
+// GEMM view ("YOLO26N Inference Optimisation", NHWC migration: implicit GEMM
+// mapping): A = im2col(x) [M = N*OH*OW, K = kh*kw*Cin], B = W [Cout, K],
+// D = A * B^T [M, Cout] -- which is the NHWC output.  NHWC keeps Cin
+// contiguous, so every K step is a dense row per output pixel.
+//
+// Tile: 128 output pixels (consecutive in (n, oh, ow) order, wrapping across
+// rows and images) x BN output channels.  K is walked tap by tap, KC input
+// channels at a time: KC = 32 (128-byte rows, 128-byte swizzle) in general,
+// KC = 16 or 8 (64- / 32-byte rows and swizzles) for layers with 16 or 8
+// input channels, so that the copy engine moves no padding channels.
+//  * warp 0 (four lanes taking K steps in turn): TMA producer.  The A tile comes from an im2col-mode
+//    tensor copy: the map's bounding box enumerates exactly the output pixel
+//    positions (lower corner -pad, upper corner pad - (k - 1), traversal
+//    stride = conv stride) and the per-copy offsets select the filter tap,
+//    so padding and the OW / OH / batch tails are handled by the copy engine
+//    (out-of-image pixels and channels >= Cin arrive as zeros).  The B tile
+//    is a 3-D tiled copy of the [Cout][tap][Cin] weights.
+//  * warp 1 (one thread): issues tcgen05.mma kind::tf32 (M=128, N=BN, K=8;
+//    KC/8 per step) into a TMEM accumulator; tcgen05.commit releases each
+//    smem stage and, at the end of a tile, the accumulator.
+//  * warps 2-9: epilogue, two groups of four warps (one per TMEM lane
+//    quarter = 32 output pixels).  Narrow tiles go to the groups in turn;
+//    wide tiles are split by columns between them.  Each warp reads its lanes with
+//    tcgen05.ld, applies scale/bias, residual and activation, rounds to the
+//    nearest TF32 value and stores its row segment.  (The MMA truncates its
+//    fp32 operands to TF32, which biases every product toward zero; storing
+//    round-to-nearest TF32 activations lets the next tensor-core layer read
+//    them exactly, so the bias does not compound along a chain.)  The
+//    residual of the next column chunk is loaded before the current one is
+//    finished, and the first chunk's before the accumulator is ready.  Rows
+//    past M and channels past Cout are masked, so nothing is written outside
+//    the logical output (padded output rows stay untouched -- "YOLO26N
+//    Inference Optimisation", Bug fixed: TMA overflow).
+// Two to four TMEM accumulators let the epilogues of earlier tiles overlap
+// the MMAs of later ones.  CTAs are persistent (one per SM) and stride over
+// the tiles.
+#pragma once
+
+#include "epilogue.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace cb {
+
+// Optional timeline of one CTA's pipeline (profiling aid, compiled in only
+// with -DCB_IGEMM_TRACE): each role keeps clock64 stamps in a local array and
+// copies them out when it finishes.
+#ifdef CB_IGEMM_TRACE
+constexpr int kTraceRecords = 512;
+static __device__ unsigned long long g_igemm_trace[3 * kTraceRecords];  // one copy per translation unit
+static __device__ int g_igemm_trace_n[3];
+struct TraceBuf {
+  unsigned long long t[kTraceRecords];
+  int n = 0;
+  __device__ __forceinline__ void add(bool on) {
+    if (on && n < kTraceRecords) t[n++] = clock64();
+  }
+  __device__ __forceinline__ void flush(bool on, int role) {
+    if (!on) return;
+    for (int i = 0; i < n; ++i) g_igemm_trace[role * kTraceRecords + i] = t[i];
+    g_igemm_trace_n[role] = n;
+  }
+};
+#else
+struct TraceBuf {
+  __device__ __forceinline__ void add(bool) {}
+  __device__ __forceinline__ void flush(bool, int) {}
+};
+#endif
+
+constexpr int kTileM = 128;
+constexpr int kEpiWarps = 8;
+constexpr int kProducerLanes = 4;
+constexpr int kIgemmThreads = 64 + 32 * kEpiWarps;
+
+__host__ __device__ constexpr int igemm_a_bytes(int kc) { return kTileM * kc * 4; }
+__host__ __device__ constexpr int igemm_b_bytes(int bn, int kc) { return ((bn * kc * 4) + 1023) / 1024 * 1024; }
+// TMEM accumulators per CTA: narrow tiles keep four in flight so the MMAs can
+// run ahead of the epilogue; wide tiles two.
+__host__ __device__ constexpr int igemm_naccs(int bn) { return bn <= 64 ? 4 : 2; }
+__host__ __device__ constexpr int tmem_cols_for(int cols) {
+  return cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+}
+
+// SiLU on the tensor-core path uses the fast exponential and division
+// (relative error ~1e-6, far inside this path's TF32 tolerance).
+__device__ __forceinline__ float tc_epi(float acc, float sc, float bi, float r, int act, int res_mode) {
+  float z = fmaf(acc, sc, bi);
+  if (res_mode == 1) z += r;
+  if (act == 1) z = fmaxf(z, 0.0f);
+  if (act == 2) z = __fdividef(z, 1.0f + __expf(-z));
+  if (res_mode == 2) z += r;
+  return round_tf32(z);
+}
+
+template <int CH>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&v)[CH]) {
+  if constexpr (CH == 16)
+    tmem_ld_x16(taddr, v);
+  else
+    tmem_ld_x8(taddr, v);
+}
+
+template <int BN, int KC>
+__global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __grid_constant__ CUtensorMap amap,
+                                                                      const __grid_constant__ CUtensorMap bmap,
+                                                                      const IgemmArgs a) {
+  constexpr int kABytes = igemm_a_bytes(KC);
+  constexpr int kBBytes = igemm_b_bytes(BN, KC);
+  constexpr int kRowBytes = KC * 4;
+  constexpr uint32_t kIdesc = idesc_tf32(kTileM, BN);
+  constexpr int NACC = igemm_naccs(BN);
+  constexpr uint32_t kTmemCols = tmem_cols_for(NACC * BN);
+  // Epilogue split: for narrow tiles the two 4-warp groups take alternate
+  // tiles (each warp all BN columns of its 32 rows); for wide tiles both
+  // groups take every tile and split its columns in halves.
+  constexpr bool kSplitTiles = BN < 64;
+  constexpr int kWidth = kSplitTiles ? BN : BN / 2;
+  constexpr int CH = (kWidth % 16 == 0) ? 16 : 8;
+  constexpr int kChunks = kWidth / CH;
+  constexpr int kEpiArrivals = kSplitTiles ? 4 : 8;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + a.stages * kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + a.stages * kBBytes);
+  uint64_t* empty = full + a.stages;
+  uint64_t* tfull = empty + a.stages;
+  uint64_t* tempty = tfull + NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + NACC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < NACC; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kEpiArrivals);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const Watchdog wd{a.err, abort_flag, a.timeout_ns};
+  const int num_tiles = a.m_tiles * a.n_tiles;
+  const bool tr_cta = a.trace && blockIdx.x == a.trace_cta;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Copies issued by one thread complete one after another (~400-500
+    // cycles each, measured on GB300), while copies from different lanes
+    // overlap; so kProducerLanes lanes share the work, each owning the ring
+    // stages s with s % kProducerLanes == lane.  Every lane walks the whole
+    // (tile, tap, chunk) sequence and issues the steps that land in its
+    // stages; one owner per stage keeps each lane's barrier phases its own.
+    if (lane < kProducerLanes) {
+      if (lane == 0) {
+        tma_prefetch_desc(&amap);
+        tma_prefetch_desc(&bmap);
+      }
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_parity = 0;
+      bool ok = true;
+      TraceBuf tr;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
+        const int m0 = m_tile * kTileM;
+        const int n_img = m0 / a.OHW;
+        const int rem = m0 - n_img * a.OHW;
+        const int oh = rem / a.OW, ow = rem - (rem / a.OW) * a.OW;
+        const int w0 = ow * a.stride - a.pad, h0 = oh * a.stride - a.pad;
+        for (int tap = 0; ok && tap < a.taps; ++tap) {
+          const uint16_t off_h = static_cast<uint16_t>(tap / a.kw);
+          const uint16_t off_w = static_cast<uint16_t>(tap % a.kw);
+          for (int kc = 0; kc < a.num_kc; ++kc) {
+            if (stage % kProducerLanes == lane) {
+              if (!mbar_wait(&empty[stage], phase ^ 1u, wd)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(kABytes + BN * KC * 4));
+              tma_load_im2col_4d(sA + stage * kABytes, &amap, &full[stage], kc * KC, w0, h0, n_img, off_w, off_h);
+              tma_load_3d(sB + stage * kBBytes, &bmap, &full[stage], kc * KC, tap, n_tile * BN);
+              tr.add(tr_cta && lane == 0);
+              issued |= 1u << stage;
+              last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+            }
+            if (++stage == a.stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // Let every copy this lane issued land before the CTA can exit.
+      for (int s = 0; s < a.stages; ++s)
+        if (issued & (1u << s)) mbar_wait_drain(&full[s], (last_parity >> s) & 1u, 20000000ull);
+      tr.flush(tr_cta && lane == 0, 0);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t committed = 0, commit_parity = 0;  // per smem stage: last commit's phase parity
+      uint32_t tcommitted = 0, tcommit_parity = 0;
+      bool ok = true;
+      int local = 0;
+      TraceBuf tr;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+        const int acc = local % NACC;
+        const uint32_t acc_phase = (local / NACC) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wd)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int k = 0; k < a.k_iters; ++k) {
+          if (!mbar_wait(&full[stage], phase, wd)) {
+            ok = false;
+            break;
+          }
+          tr.add(tr_cta);
+          tc_fence_after_sync();
+          const uint64_t adesc = kmajor_swizzled_desc(smem_u32(sA + stage * kABytes), kRowBytes);
+          const uint64_t bdesc = kmajor_swizzled_desc(smem_u32(sB + stage * kBBytes), kRowBytes);
+#pragma unroll
+          for (int kk = 0; kk < KC / 8; ++kk) {
+            // advance 8 tf32 (32 bytes) along K inside the swizzled row
+            mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (k | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          tr.add(tr_cta);
+          // the commit completes the barrier phase the producer waits on next
+          const uint32_t bit = 1u << stage;
+          commit_parity = (committed & bit) ? (commit_parity ^ bit) : (commit_parity & ~bit);
+          committed |= bit;
+          if (++stage == a.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        const uint32_t tbit = 1u << acc;
+        tcommit_parity = (tcommitted & tbit) ? (tcommit_parity ^ tbit) : (tcommit_parity & ~tbit);
+        tcommitted |= tbit;
+      }
+      // Let every MMA this thread issued finish before TMEM is released.
+      for (int s = 0; s < a.stages; ++s)
+        if (committed & (1u << s)) mbar_wait_drain(&empty[s], (commit_parity >> s) & 1u, 20000000ull);
+      for (int b = 0; b < NACC; ++b)
+        if (tcommitted & (1u << b)) mbar_wait_drain(&tfull[b], (tcommit_parity >> b) & 1u, 20000000ull);
+      tr.flush(tr_cta, 1);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int group = (warp - 2) >> 2;
+    const int col0 = kSplitTiles ? 0 : group * kWidth;
+    const int row = q * 32 + lane;          // tile row = output pixel within the tile
+    const bool res = a.ep.res_mode != 0;
+    int local = 0;
+    TraceBuf tr;
+    const bool tr_on = tr_cta && warp == 2 && lane == 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      if (kSplitTiles && (local & 1) != group) continue;
+      const int acc = local % NACC;
+      const uint32_t acc_phase = (local / NACC) & 1;
+      const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
+      const int m = m_tile * kTileM + row;
+      const bool valid = m < a.M;
+      int n_img = 0, oh = 0, ow = 0;
+      if (valid) {
+        n_img = m / a.OHW;
+        const int rem = m - n_img * a.OHW;
+        oh = rem / a.OW;
+        ow = rem - oh * a.OW;
+      }
+      float* yrow = a.out.y + n_img * a.out.ys_n + oh * a.out.ys_h + ow * a.out.ys_w;
+      const float* rrow = res ? a.ep.r + n_img * a.ep.rs_n + oh * a.ep.rs_h + ow * a.ep.rs_w : nullptr;
+      const int cbase = n_tile * BN + col0;
+      const bool vec = a.vec_store && cbase + kWidth <= a.Cout;
+
+      // residual of the first chunk, fetched while the accumulator is computed
+      float rcur[CH];
+#pragma unroll
+      for (int j = 0; j < CH; ++j) rcur[j] = 0.0f;
+      if (res && valid) {
+        if (vec) {
+#pragma unroll
+          for (int j = 0; j < CH; j += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(rrow + cbase + j);
+            rcur[j] = t.x, rcur[j + 1] = t.y, rcur[j + 2] = t.z, rcur[j + 3] = t.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < CH; ++j)
+            if (cbase + j < a.Cout) rcur[j] = rrow[cbase + j];
+        }
+      }
+
+      bool got = mbar_wait(&tfull[acc], acc_phase, wd);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) break;
+      tc_fence_after_sync();
+      tr.add(tr_on);
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + col0);
+#pragma unroll
+      for (int cidx = 0; cidx < kChunks; ++cidx) {
+        const int c0 = cbase + cidx * CH;
+        uint32_t v[CH];
+        tmem_ld_chunk<CH>(taddr + cidx * CH, v);
+        float rnext[CH];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) rnext[j] = 0.0f;
+        if (res && valid && cidx + 1 < kChunks) {
+          if (vec) {
+#pragma unroll
+            for (int j = 0; j < CH; j += 4) {
+              const float4 t = *reinterpret_cast<const float4*>(rrow + c0 + CH + j);
+              rnext[j] = t.x, rnext[j + 1] = t.y, rnext[j + 2] = t.z, rnext[j + 3] = t.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+              if (c0 + CH + j < a.Cout) rnext[j] = rrow[c0 + CH + j];
+          }
+        }
+        tmem_ld_wait();
+        if (valid) {
+          if (vec) {
+#pragma unroll
+            for (int j = 0; j < CH; j += 4) {
+              const float4 sc = ldg4(a.ep.scale + c0 + j), bi = ldg4(a.ep.bias + c0 + j);
+              float4 o;
+              o.x = tc_epi(__uint_as_float(v[j]), sc.x, bi.x, rcur[j], a.ep.act, a.ep.res_mode);
+              o.y = tc_epi(__uint_as_float(v[j + 1]), sc.y, bi.y, rcur[j + 1], a.ep.act, a.ep.res_mode);
+              o.z = tc_epi(__uint_as_float(v[j + 2]), sc.z, bi.z, rcur[j + 2], a.ep.act, a.ep.res_mode);
+              o.w = tc_epi(__uint_as_float(v[j + 3]), sc.w, bi.w, rcur[j + 3], a.ep.act, a.ep.res_mode);
+              *reinterpret_cast<float4*>(yrow + c0 + j) = o;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const int c = c0 + j;
+              if (c < a.Cout)
+                yrow[c] = tc_epi(__uint_as_float(v[j]), __ldg(a.ep.scale + c), __ldg(a.ep.bias + c), rcur[j],
+                                 a.ep.act, a.ep.res_mode);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < CH; ++j) rcur[j] = rnext[j];
+      }
+      tr.add(tr_on);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+    tr.flush(tr_on, 2);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Copies this translation unit's trace out (see TraceBuf); returns the record count.
+static inline int igemm_read_trace_tu(unsigned long long* out, int max_records) {
+#ifdef CB_IGEMM_TRACE
+  int n[3] = {0, 0, 0};
+  if (cudaMemcpyFromSymbol(n, g_igemm_trace_n, sizeof(n)) != cudaSuccess) return -1;
+  if (n[0] + n[1] + n[2] == 0) return 0;
+  if (max_records < 3 * kTraceRecords + 3) return -1;
+  if (cudaMemcpyFromSymbol(out + 3, g_igemm_trace, sizeof(unsigned long long) * 3 * kTraceRecords) != cudaSuccess)
+    return -1;
+  out[0] = n[0];
+  out[1] = n[1];
+  out[2] = n[2];
+  const int zero[3] = {0, 0, 0};
+  cudaMemcpyToSymbol(g_igemm_trace_n, zero, sizeof(zero));
+  return n[0] + n[1] + n[2];
+#else
+  (void)out;
+  (void)max_records;
+  return 0;
+#endif
+}
+
+template <int BN, int KC>
+cudaError_t igemm_launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int grid,
+                            size_t smem, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(igemm_tf32_kernel<BN, KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  igemm_tf32_kernel<BN, KC><<<grid, kIgemmThreads, smem, s>>>(amap, bmap, a);
+  return cudaGetLastError();
+}
+
+template <int KC>
+cudaError_t igemm_launch_kc(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int bn, int grid,
+                            size_t smem, cudaStream_t s) {
+  switch (bn) {
+    case 16: return igemm_launch_bn<16, KC>(amap, bmap, a, grid, smem, s);
+    case 32: return igemm_launch_bn<32, KC>(amap, bmap, a, grid, smem, s);
+    case 48: return igemm_launch_bn<48, KC>(amap, bmap, a, grid, smem, s);
+    case 64: return igemm_launch_bn<64, KC>(amap, bmap, a, grid, smem, s);
+    case 96: return igemm_launch_bn<96, KC>(amap, bmap, a, grid, smem, s);
+    case 128: return igemm_launch_bn<128, KC>(amap, bmap, a, grid, smem, s);
+    case 192: return igemm_launch_bn<192, KC>(amap, bmap, a, grid, smem, s);
+    case 256: return igemm_launch_bn<256, KC>(amap, bmap, a, grid, smem, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace cb

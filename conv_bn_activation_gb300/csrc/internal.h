@@ -69,7 +69,7 @@ struct IgemmArgs {
   int OHW, OW;   // OH*OW, OW
   int Cout;
   int kw, taps;  // filter width, kh*kw
-  int num_kc;    // ceil(Cin / 32)
+  int num_kc;    // ceil(Cin / KC), KC = channels per K step (8, 16 or 32)
   int k_iters;   // taps * num_kc
   int m_tiles, n_tiles;
   int stride, pad;
@@ -79,11 +79,14 @@ struct IgemmArgs {
   Epilogue ep;
   int* err;
   uint64_t timeout_ns;
+  int trace;      // 1: record the pipeline timeline of CTA trace_cta (profiling aid)
+  int trace_cta;
 };
-cudaError_t launch_igemm(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int bn,
+int igemm_read_trace(unsigned long long* out, int max_records);
+cudaError_t launch_igemm(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int bn, int kc,
                          int grid, size_t smem_bytes, cudaStream_t s);
-size_t igemm_smem_bytes(int bn, int stages);
-int igemm_stages(int bn);
+size_t igemm_smem_bytes(int bn, int kc, int stages);
+int igemm_stages(int bn, int kc);
 
 // -------------------------------------------------------------- preprocess
 cudaError_t launch_preprocess_fused(const uint8_t* src, int n, int hs, int ws, long long pitch, float* dst,

@@ -170,6 +170,13 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 32 bits, 8 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
 // 32 lanes x 32 bits, 16 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -189,19 +196,20 @@ __device__ __forceinline__ float round_tf32(float x) {
   return __uint_as_float(r);
 }
 
-// Shared-memory matrix descriptor for a K-major operand stored with the
-// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms
-// stacked along M/N (stride byte offset 1024).  Bits: start address >> 4
-// [0,14), leading byte offset >> 4 [16,30) (unused for swizzled K-major),
-// stride byte offset >> 4 [32,46), fixed 0b001 [46,49), swizzle mode
-// [61,64) with 2 = 128-byte swizzle.
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+// Shared-memory matrix descriptor for a K-major operand whose rows of
+// `row_bytes` (128, 64 or 32) are stored with the matching TMA swizzle, in
+// 8-row swizzle atoms stacked along M/N (stride byte offset = 8 rows).
+// Bits: start address >> 4 [0,14), leading byte offset >> 4 [16,30) (unused
+// for swizzled K-major), stride byte offset >> 4 [32,46), fixed 0b001
+// [46,49), swizzle mode [61,64): 2 = 128-byte, 4 = 64-byte, 6 = 32-byte.
+__device__ __forceinline__ uint64_t kmajor_swizzled_desc(uint32_t saddr, int row_bytes) {
+  const uint64_t mode = row_bytes == 128 ? 2 : row_bytes == 64 ? 4 : 6;
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(1) << 16;
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>((8 * row_bytes) >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= mode << 61;
   return d;
 }
 

@@ -35,7 +35,7 @@ class ConvBnAct:
 
     tc_weights: round the dense weights to the nearest TF32 value
     (cb_round_weights_tf32) for the tensor-core path; None decides from the
-    shape rule of that path (groups 1, Cin % 4 == 0, Cin >= 16) and the
+    shape rule of that path (groups 1, Cin % 4 == 0, Cin >= 8 for 1x1 and >= 16 for 3x3) and the
     current kernel policy.
     """
 
@@ -43,7 +43,7 @@ class ConvBnAct:
         scale, bias = cb.fold_bn(*bn, eps=eps)
         cin = w_oihw.shape[1] * groups
         if tc_weights is None:
-            tc_weights = (groups == 1 and cin % 4 == 0 and cin >= 16 and w_oihw.shape[2] in (1, 3)
+            tc_weights = (groups == 1 and cin % 4 == 0 and cin >= (8 if w_oihw.shape[2] == 1 else 16) and w_oihw.shape[2] in (1, 3)
                           and cb.get_kernel_policy() == 0)
         w = cb.repack_weights(w_oihw, groups)
         if tc_weights:
@@ -71,7 +71,7 @@ class DwBlock:
         self.cin, self.cout, self.stride = cin, cout, stride
         dws, dwb = cb.fold_bn(*p["bn1"])
         pws, pwb = cb.fold_bn(*p["bn2"])
-        tc = cin % 4 == 0 and cin >= 16 and cb.get_kernel_policy() == 0
+        tc = cin % 4 == 0 and cin >= 8 and cb.get_kernel_policy() == 0
         dense = cb.round_weights_tf32 if tc else (lambda a: a)
         self.params = {
             "dw_w": _dev(cb.repack_weights(p["dw_w"], groups=cin), device),

@@ -118,7 +118,7 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
  * element for element (in-place residual add).
  *
  * Paths (chosen on the host from the shape): dense layers with Ci % 4 == 0
- * and Ci >= 16 run as an implicit GEMM on the tcgen05 tensor cores (TF32
+ * and Ci >= 16 (3x3) or Ci >= 8 (1x1) run as an implicit GEMM on the tcgen05 tensor cores (TF32
  * inputs, fp32 accumulate, outputs rounded to the nearest TF32 value; needs
  * 16-byte aligned x/w and strides that are multiples of 4 elements);
  * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;

@@ -82,7 +82,7 @@ def test_yolo_chain_full_size_per_layer(gpu, orc):
             idx = rng.choice(got.size, min(got.size, 3000), replace=False)
             ref = orc.conv_bn_act_points(inp, w, bn, idx, stride=s, pad=p, act=orc.ACT_SILU, residual=res,
                                          res_mode=orc.RES_POST_ACT if res is not None else orc.RES_NONE)
-            tol = TOL_TF32 if inp.shape[-1] >= 16 else TOL_FP32
+            tol = TOL_TF32 if (inp.shape[-1] >= 16 or (inp.shape[-1] >= 8 and w.shape[2] == 1)) else TOL_FP32
             assert rel_err(got.reshape(-1)[idx], ref) <= tol
         h = out
 
