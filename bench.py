@@ -499,7 +499,7 @@ def run_ours(args):
     binding.load()
     peaks = load_peaks()
 
-    wl = WORKLOADS[args.workload](torch, device)
+    wl = WORKLOADS[args.workload](torch, device, **({"batch": args.batch} if args.batch else {}))
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
         wl.run(stream)
@@ -529,21 +529,24 @@ def run_ours(args):
     extra = wl.extra(torch, stream, args.steps) if hasattr(wl, "extra") else None
 
     # e2e: host buffers, copies inside the timed region
-    h2d, d2h = wl.e2e_setup()
-    for _ in range(3):
-        wl.e2e_step(stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 10))
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        wl.e2e_step(stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = d2h = 0
+    e2e_ms = float("nan")
+    if not args.no_e2e:
+        h2d, d2h = wl.e2e_setup()
+        for _ in range(3):
+            wl.e2e_step(stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(1, min(args.steps, 10))
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            wl.e2e_step(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     units = wl.step_units() * args.steps
     e2e_units = wl.step_units()
@@ -573,8 +576,9 @@ def run_ours(args):
                     "max": round(max(step_ms), 4)},
         "launches": wl.per_launch(launch_ms, peaks),
         "roofline": wl.roofline(launch_ms, peaks),
-        "e2e": {"value": round(e2e_units / (e2e_ms * 1e-3) / scale, 3), "unit": wl.unit,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "e2e": None if args.no_e2e else {"value": round(e2e_units / (e2e_ms * 1e-3) / scale, 3), "unit": wl.unit,
+                                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                                         "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": getattr(wl, "kernels_per_step", nl) * args.steps,
         "clocks": clocks,
     }
@@ -649,6 +653,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="depthwise", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

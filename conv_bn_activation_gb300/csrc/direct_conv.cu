@@ -128,10 +128,12 @@ __global__ void __launch_bounds__(256) direct_tile_kernel(const DirectArgs a, in
     const int co = co0 + q;
     ws[i] = co < a.Co ? __ldg(a.w + static_cast<long long>(co) * taps * Ci + tc) : 0.0f;
   }
-  // input tile with halo, zero outside the image
+  // input tile with halo, zero outside the image.  Each thread owns fixed
+  // (column, channel) positions of a staged row and copies them for all rows,
+  // eight rows' loads in flight at a time.
   const int per_row = cols_in * Ci;
-  for (int i = threadIdx.x; i < rows_in * per_row; i += blockDim.x) {
-    const int r = i / per_row, rem = i - r * per_row;
+  constexpr int U = 8;
+  for (int rem = threadIdx.x; rem < per_row; rem += blockDim.x) {
     int c, ci;
     if (a.xs_c == 1) {  // channel-contiguous input: walk (col, ci) so reads coalesce
       c = rem / Ci;
@@ -140,12 +142,22 @@ __global__ void __launch_bounds__(256) direct_tile_kernel(const DirectArgs a, in
       ci = rem / cols_in;
       c = rem - ci * cols_in;
     }
-    const int ih = ih0 + r, iw = iw0 + c;
-    float v = 0.0f;
-    if (ih >= 0 && ih < a.H && iw >= 0 && iw < a.W)
-      v = __ldg(a.x + n * a.xs_n + ih * a.xs_h + iw * a.xs_w + ci * a.xs_c);
-    const int sc = S == 2 ? (c & 1) * half + (c >> 1) : c;
-    xs[ci * plane + r * pitch + sc] = v;
+    const int iw = iw0 + c;
+    const bool col_ok = iw >= 0 && iw < a.W;
+    const float* gp = a.x + n * a.xs_n + static_cast<long long>(ci) * a.xs_c + static_cast<long long>(iw) * a.xs_w;
+    float* sp = xs + ci * plane + (S == 2 ? (c & 1) * half + (c >> 1) : c);
+    for (int r0 = 0; r0 < rows_in; r0 += U) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int ih = ih0 + r0 + u;
+        v[u] = (col_ok && r0 + u < rows_in && ih >= 0 && ih < a.H) ? __ldg(gp + static_cast<long long>(ih) * a.xs_h)
+                                                                  : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (r0 + u < rows_in) sp[(r0 + u) * pitch] = v[u];
+    }
   }
   __syncthreads();
 

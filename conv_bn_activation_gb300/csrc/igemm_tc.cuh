@@ -293,25 +293,28 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
       float* yrow = a.out.y + n_img * a.out.ys_n + oh * a.out.ys_h + ow * a.out.ys_w;
       const float* rrow = res ? a.ep.r + n_img * a.ep.rs_n + oh * a.ep.rs_h + ow * a.ep.rs_w : nullptr;
       const int cbase = n_tile * BN + col0;
-      const bool vec = a.vec_store && cbase + kWidth <= a.Cout;
+      // 4-column groups inside [0, Cout) go through 16-byte accesses when the
+      // views allow it; the rest element by element.
+      auto group_vec = [&](int c) { return a.vec_store && c + 4 <= a.Cout; };
 
       // residual of the first chunk, fetched while the accumulator is computed
       float rcur[CH];
 #pragma unroll
       for (int j = 0; j < CH; ++j) rcur[j] = 0.0f;
-      if (res && valid) {
-        if (vec) {
+      auto load_res = [&](float(&r)[CH], int c0) {
 #pragma unroll
-          for (int j = 0; j < CH; j += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(rrow + cbase + j);
-            rcur[j] = t.x, rcur[j + 1] = t.y, rcur[j + 2] = t.z, rcur[j + 3] = t.w;
+        for (int j = 0; j < CH; j += 4) {
+          if (group_vec(c0 + j)) {
+            const float4 t = *reinterpret_cast<const float4*>(rrow + c0 + j);
+            r[j] = t.x, r[j + 1] = t.y, r[j + 2] = t.z, r[j + 3] = t.w;
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              if (c0 + j + jj < a.Cout) r[j + jj] = rrow[c0 + j + jj];
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < CH; ++j)
-            if (cbase + j < a.Cout) rcur[j] = rrow[cbase + j];
         }
-      }
+      };
+      if (res && valid) load_res(rcur, cbase);
 
       bool got = mbar_wait(&tfull[acc], acc_phase, wd);
       got = __all_sync(0xffffffffu, got);
@@ -328,39 +331,26 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
         float rnext[CH];
 #pragma unroll
         for (int j = 0; j < CH; ++j) rnext[j] = 0.0f;
-        if (res && valid && cidx + 1 < kChunks) {
-          if (vec) {
-#pragma unroll
-            for (int j = 0; j < CH; j += 4) {
-              const float4 t = *reinterpret_cast<const float4*>(rrow + c0 + CH + j);
-              rnext[j] = t.x, rnext[j + 1] = t.y, rnext[j + 2] = t.z, rnext[j + 3] = t.w;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < CH; ++j)
-              if (c0 + CH + j < a.Cout) rnext[j] = rrow[c0 + CH + j];
-          }
-        }
+        if (res && valid && cidx + 1 < kChunks) load_res(rnext, c0 + CH);
         tmem_ld_wait();
         if (valid) {
-          if (vec) {
 #pragma unroll
-            for (int j = 0; j < CH; j += 4) {
-              const float4 sc = ldg4(a.ep.scale + c0 + j), bi = ldg4(a.ep.bias + c0 + j);
+          for (int j = 0; j < CH; j += 4) {
+            const int c = c0 + j;
+            if (group_vec(c)) {
+              const float4 sc = ldg4(a.ep.scale + c), bi = ldg4(a.ep.bias + c);
               float4 o;
               o.x = tc_epi(__uint_as_float(v[j]), sc.x, bi.x, rcur[j], a.ep.act, a.ep.res_mode);
               o.y = tc_epi(__uint_as_float(v[j + 1]), sc.y, bi.y, rcur[j + 1], a.ep.act, a.ep.res_mode);
               o.z = tc_epi(__uint_as_float(v[j + 2]), sc.z, bi.z, rcur[j + 2], a.ep.act, a.ep.res_mode);
               o.w = tc_epi(__uint_as_float(v[j + 3]), sc.w, bi.w, rcur[j + 3], a.ep.act, a.ep.res_mode);
-              *reinterpret_cast<float4*>(yrow + c0 + j) = o;
-            }
-          } else {
+              *reinterpret_cast<float4*>(yrow + c) = o;
+            } else {
 #pragma unroll
-            for (int j = 0; j < CH; ++j) {
-              const int c = c0 + j;
-              if (c < a.Cout)
-                yrow[c] = tc_epi(__uint_as_float(v[j]), __ldg(a.ep.scale + c), __ldg(a.ep.bias + c), rcur[j],
-                                 a.ep.act, a.ep.res_mode);
+              for (int jj = 0; jj < 4; ++jj)
+                if (c + jj < a.Cout)
+                  yrow[c + jj] = tc_epi(__uint_as_float(v[j + jj]), __ldg(a.ep.scale + c + jj),
+                                        __ldg(a.ep.bias + c + jj), rcur[j + jj], a.ep.act, a.ep.res_mode);
             }
           }
         }

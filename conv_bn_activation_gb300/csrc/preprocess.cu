@@ -27,16 +27,19 @@ struct AxisSample {
   float a;
 };
 
-__device__ __forceinline__ AxisSample axis_sample(int d, int S, int D) {
-  const float scale = __fdiv_rn(static_cast<float>(S), static_cast<float>(D));
-  const float f = __fsub_rn(__fmul_rn(__fadd_rn(static_cast<float>(d), 0.5f), scale), 0.5f);
-  const float fl = floorf(f);
-  int k = static_cast<int>(fl);
-  float t = __fsub_rn(f, fl);
-  if (k < 0) {
-    k = 0;
-    t = 0.0f;
-  }
+// Exact small-integer conversions without the quarter-rate convert unit:
+// adding 2^23 leaves an integer in the low mantissa bits.
+__device__ __forceinline__ float u8_to_float(uint32_t b) { return __int_as_float(0x4B000000 | b) - 8388608.0f; }
+// floor(x) for 0 <= x < 2^22: round the sum down, then read the integer back.
+__device__ __forceinline__ int floor_nonneg(float x) { return __float_as_int(__fadd_rd(x, 8388608.0f)) - 0x4B000000; }
+
+// scale = S / D (IEEE fp32 division, computed once per launch row).  A
+// negative f is clamped to 0 before the floor, which gives the same
+// (i0 = 0, a = 0) as flooring it and then clamping i0.
+__device__ __forceinline__ AxisSample axis_sample(int d, int S, float scale) {
+  const float f = fmaxf(__fsub_rn(__fmul_rn(__fadd_rn(static_cast<float>(d), 0.5f), scale), 0.5f), 0.0f);
+  int k = floor_nonneg(f);
+  float t = __fsub_rn(f, static_cast<float>(k));
   if (k >= S - 1) {
     k = S - 1;
     t = 0.0f;
@@ -55,10 +58,9 @@ __device__ __forceinline__ float bilinear(float p00, float p01, float p10, float
   return __fadd_rn(__fmul_rn(by, top), __fmul_rn(ay, bot));
 }
 
-__device__ __forceinline__ float round_u8(float v) {
-  float u = floorf(__fadd_rn(v, 0.5f));
-  return fminf(fmaxf(u, 0.0f), 255.0f);
-}
+// u8 code of a bilinear value: floor(v + 0.5); v is a convex combination of
+// u8 samples, so the code is already within [0, 255].
+__device__ __forceinline__ int round_u8(float v) { return floor_nonneg(__fadd_rn(v, 0.5f)); }
 
 // Copy `bytes` bytes of a source row into shared memory.
 __device__ __forceinline__ void stage_row(uint8_t* dst, const uint8_t* src, int bytes, bool vec) {
@@ -77,11 +79,17 @@ template <bool TO_U8>
 __global__ void __launch_bounds__(256) preprocess_row_kernel(const uint8_t* __restrict__ src, int hs, int ws,
                                                              long long pitch, void* __restrict__ out, int hd,
                                                              int wd, int vec_in, int vec_out) {
+  // u / 255 for every u8 code, each an IEEE fp32 division, looked up instead
+  // of divided per output.
+  __shared__ float inv255[256];
   extern __shared__ __align__(16) uint8_t rows[];
+  if (!TO_U8)
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) inv255[i] = __fdiv_rn(static_cast<float>(i), 255.0f);
   const int row_bytes = ws * 3;
   const int row_alloc = (row_bytes + 15) & ~15;
   const int dy = blockIdx.x, n = blockIdx.y;
-  const AxisSample sy = axis_sample(dy, hs, hd);
+  const float scale_x = __fdiv_rn(static_cast<float>(ws), static_cast<float>(wd));
+  const AxisSample sy = axis_sample(dy, hs, __fdiv_rn(static_cast<float>(hs), static_cast<float>(hd)));
   const uint8_t* frame = src + static_cast<long long>(n) * hs * pitch;
   uint8_t* r0 = rows;
   uint8_t* r1 = rows + row_alloc;
@@ -90,22 +98,46 @@ __global__ void __launch_bounds__(256) preprocess_row_kernel(const uint8_t* __re
   __syncthreads();
 
   const int groups = (wd + 3) >> 2;
+  // 2:1 horizontal ratio (the 1280 -> 640 workload): destination column dx
+  // samples source columns 2dx and 2dx + 1 with weight 1/2 (what axis_sample
+  // gives for it), so 4 destination pixels read 24 consecutive bytes per row,
+  // fetched as six 32-bit words.
+  const bool two_to_one = (ws == 2 * wd) && (row_alloc % 8 == 0);
   for (int g = threadIdx.x; g < groups; g += blockDim.x) {
-    float o[3][4];
+    int o[3][4];
+    if (two_to_one && g * 4 + 3 < wd) {
+      const uint32_t* w0 = reinterpret_cast<const uint32_t*>(r0 + g * 24);
+      const uint32_t* w1 = reinterpret_cast<const uint32_t*>(r1 + g * 24);
+      uint32_t a0[6], a1[6];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int dx = g * 4 + q;
-      if (dx < wd) {
-        const AxisSample sx = axis_sample(dx, ws, wd);
+      for (int i = 0; i < 6; ++i) a0[i] = w0[i], a1[i] = w1[i];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
 #pragma unroll
         for (int c = 0; c < 3; ++c) {
-          const float p00 = r0[sx.i0 * 3 + c], p01 = r0[sx.i1 * 3 + c];
-          const float p10 = r1[sx.i0 * 3 + c], p11 = r1[sx.i1 * 3 + c];
-          o[c][q] = round_u8(bilinear(p00, p01, p10, p11, sx.a, sy.a));
+          const int b0 = q * 6 + c, b1 = q * 6 + 3 + c;  // byte offsets of the two samples
+          const float p00 = u8_to_float((a0[b0 >> 2] >> ((b0 & 3) * 8)) & 0xFF);
+          const float p01 = u8_to_float((a0[b1 >> 2] >> ((b1 & 3) * 8)) & 0xFF);
+          const float p10 = u8_to_float((a1[b0 >> 2] >> ((b0 & 3) * 8)) & 0xFF);
+          const float p11 = u8_to_float((a1[b1 >> 2] >> ((b1 & 3) * 8)) & 0xFF);
+          o[c][q] = round_u8(bilinear(p00, p01, p10, p11, 0.5f, sy.a));
         }
-      } else {
+    } else {
 #pragma unroll
-        for (int c = 0; c < 3; ++c) o[c][q] = 0.0f;
+      for (int q = 0; q < 4; ++q) {
+        const int dx = g * 4 + q;
+        if (dx < wd) {
+          const AxisSample sx = axis_sample(dx, ws, scale_x);
+#pragma unroll
+          for (int c = 0; c < 3; ++c) {
+            const float p00 = u8_to_float(r0[sx.i0 * 3 + c]), p01 = u8_to_float(r0[sx.i1 * 3 + c]);
+            const float p10 = u8_to_float(r1[sx.i0 * 3 + c]), p11 = u8_to_float(r1[sx.i1 * 3 + c]);
+            o[c][q] = round_u8(bilinear(p00, p01, p10, p11, sx.a, sy.a));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 3; ++c) o[c][q] = 0;
+        }
       }
     }
     if (TO_U8) {
@@ -121,8 +153,7 @@ __global__ void __launch_bounds__(256) preprocess_row_kernel(const uint8_t* __re
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
         float* op = base + ((static_cast<long long>(n) * 3 + c) * hd + dy) * wd;
-        const float4 v = make_float4(__fdiv_rn(o[c][0], 255.0f), __fdiv_rn(o[c][1], 255.0f),
-                                     __fdiv_rn(o[c][2], 255.0f), __fdiv_rn(o[c][3], 255.0f));
+        const float4 v = make_float4(inv255[o[c][0]], inv255[o[c][1]], inv255[o[c][2]], inv255[o[c][3]]);
         if (vec_out && g * 4 + 3 < wd) {
           *reinterpret_cast<float4*>(op + g * 4) = v;
         } else {
