@@ -158,6 +158,7 @@ class Launch:
 class Workload:
     """A step = the listed launches, in order, on one stream."""
     unit = "GB/s"
+    capture = True          # time the K steps as one CUDA graph (no host gaps between launches)
     profile = None          # (profiles/ file, kernel source files) for the roofline's traffic figure
     dominant = None         # launch name whose roofline is reported
 
@@ -317,6 +318,7 @@ class DenseWorkload(Workload):
 class MnistWorkload(Workload):
     """The whole DepthwiseMNIST forward, replayed as one CUDA graph per step."""
     unit = "images/s"
+    capture = False  # already one graph launch per step
 
     def __init__(self, torch, device, batch=64):
         from conv_bn_activation_gb300 import synthetic, workloads
@@ -508,14 +510,36 @@ def run_ours(args):
         raise RuntimeError("device error during warm-up")
 
     nl = len(wl.launches)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
+    graph = None
+    if wl.capture and not args.eager:
+        # The K timed steps are captured as one CUDA graph, with the per-launch
+        # events inside it (recorded as graph nodes at replay), so that the
+        # device timeline has no host gaps between launches.
+        try:
+            events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)]
+                      for _ in range(args.steps)]
+        except TypeError:
+            events = None
+        if events is not None:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                cap = torch.cuda.current_stream(device)
+                for k in range(args.steps):
+                    wl.run(cap, events[k])
+            graph.replay()
+            torch.cuda.synchronize()
+    if graph is None:
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(torch, local)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    for k in range(args.steps):
-        wl.run(stream, events[k])
+    if graph is not None:
+        graph.replay()
+    else:
+        for k in range(args.steps):
+            wl.run(stream, events[k])
     torch.cuda.synchronize()
     clocks = sampler.stop()
     if world > 1:
@@ -580,6 +604,8 @@ def run_ours(args):
                                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                          "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": getattr(wl, "kernels_per_step", nl) * args.steps,
+        "timing": "one CUDA graph of the K steps, per-launch events inside it" if graph is not None
+        else "eager launches, per-launch events between them",
         "clocks": clocks,
     }
     if extra:
@@ -655,6 +681,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of one captured graph")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

@@ -21,13 +21,14 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_
 ACT_NONE, ACT_RELU, ACT_SILU = 0, 1, 2
 RES_NONE, RES_PRE_ACT, RES_POST_ACT = 0, 1, 2
 LAYOUT_NHWC, LAYOUT_NCHW = 0, 1
+PATH_DIRECT, PATH_DEPTHWISE, PATH_TC_IM2COL, PATH_TC_HALO = 1, 2, 3, 4
 
 EXPORTED = (
     "cb_fold_bn", "cb_repack_weights", "cb_conv_bn_act", "cb_dw_separable_block_workspace",
     "cb_dw_separable_block", "cb_avgpool_linear", "cb_preprocess_u8", "cb_preprocess_u8_three_pass",
     "cb_get_device_error", "cb_last_cuda_error", "cb_set_kernel_policy", "cb_status_string", "cb_version",
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_conv_uses_tensor_cores",
-    "cb_dw_separable_block_static",
+    "cb_dw_separable_block_static", "cb_conv_path",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
@@ -79,6 +80,7 @@ def load():
                 "cb_get_kernel_policy": [],
                 "cb_round_weights_tf32": [P, LL, P],
                 "cb_conv_uses_tensor_cores": [T, I, I],
+                "cb_conv_path": [T, T, I, I, I, I],
                 "cb_status_string": [I],
                 "cb_version": [],
             }
@@ -164,6 +166,13 @@ def round_weights_tf32(w):
 def uses_tensor_cores(x, k, groups=1, x_layout=LAYOUT_NHWC) -> bool:
     xv = nchw(x) if x_layout == LAYOUT_NCHW else nhwc(x)
     return bool(load().cb_conv_uses_tensor_cores(ctypes.byref(xv), k, groups))
+
+
+def conv_path(x, y, k, stride, pad, groups=1, x_layout=LAYOUT_NHWC) -> int:
+    """cb_conv_path: which kernel cb_conv_bn_act would run (PATH_*), 0 if unsupported."""
+    xv = nchw(x) if x_layout == LAYOUT_NCHW else nhwc(x)
+    yv = nhwc(y)
+    return load().cb_conv_path(ctypes.byref(xv), ctypes.byref(yv), k, stride, pad, groups)
 
 
 def version() -> int:

@@ -12,12 +12,15 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <string>
+#include <unordered_map>
 
 #include "cb.h"
 #include "internal.h"
 
 namespace cb {
 int dw_tma_blocks_per_sm(int stride, int threads, size_t smem);
+int igemm_read_spans_halo(unsigned long long* out, int max_ctas);
 }
 
 using namespace cb;
@@ -100,6 +103,74 @@ EncodeTiledFn encode_tiled() {
 EncodeIm2colFn encode_im2col() {
   static EncodeIm2colFn fn = reinterpret_cast<EncodeIm2colFn>(driver_fn("cuTensorMapEncodeIm2col"));
   return fn;
+}
+
+// Tensor maps, cached: encoding one costs microseconds, as much as the launch
+// itself, and a network calls the same layers with the same buffers over and
+// over.  The key is every argument of the encode call (the map is a pure
+// function of them), so a buffer freed and reallocated at the same address
+// with the same shape maps to the same, still correct, descriptor.
+struct MapCache {
+  std::mutex mu;
+  std::unordered_map<std::string, CUtensorMap> maps;
+};
+MapCache g_maps;
+
+template <typename... Parts>
+std::string map_key(const Parts&... parts) {
+  std::string k;
+  (k.append(reinterpret_cast<const char*>(&parts), sizeof(parts)), ...);
+  return k;
+}
+
+bool cached_map(const std::string& key, CUtensorMap* out) {
+  std::lock_guard<std::mutex> lock(g_maps.mu);
+  auto it = g_maps.maps.find(key);
+  if (it == g_maps.maps.end()) return false;
+  *out = it->second;
+  return true;
+}
+
+void store_map(const std::string& key, const CUtensorMap& m) {
+  std::lock_guard<std::mutex> lock(g_maps.mu);
+  if (g_maps.maps.size() >= 4096) g_maps.maps.clear();
+  g_maps.maps.emplace(key, m);
+}
+
+// fp32 tiled map of rank <= 5 (no interleave, 256-byte L2 promotion, zero fill).
+CUresult tiled_map(CUtensorMap* out, int rank, const void* ptr, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box, const cuuint32_t* estr, CUtensorMapSwizzle swz) {
+  cuuint64_t d[5] = {}, st[4] = {};
+  cuuint32_t b[5] = {}, e[5] = {};
+  for (int i = 0; i < rank; ++i) d[i] = dims[i], b[i] = box[i], e[i] = estr[i];
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  const int kind = 0;
+  const std::string key = map_key(kind, rank, ptr, d, st, b, e, swz);
+  if (cached_map(key, out)) return CUDA_SUCCESS;
+  const CUresult r = encode_tiled()(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<cuuint32_t>(rank),
+                                    const_cast<void*>(ptr), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) store_map(key, *out);
+  return r;
+}
+
+// fp32 4-D im2col map (same fixed options as tiled_map).
+CUresult im2col_map(CUtensorMap* out, const void* ptr, const cuuint64_t* dims, const cuuint64_t* strides,
+                    const int* lower, const int* upper, cuuint32_t channels, cuuint32_t pixels,
+                    const cuuint32_t* estr, CUtensorMapSwizzle swz) {
+  cuuint64_t d[4], st[3];
+  cuuint32_t e[4];
+  int lo[2] = {lower[0], lower[1]}, up[2] = {upper[0], upper[1]};
+  for (int i = 0; i < 4; ++i) d[i] = dims[i], e[i] = estr[i];
+  for (int i = 0; i < 3; ++i) st[i] = strides[i];
+  const int kind = 1;
+  const std::string key = map_key(kind, ptr, d, st, lo, up, channels, pixels, e, swz);
+  if (cached_map(key, out)) return CUDA_SUCCESS;
+  const CUresult r = encode_im2col()(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), d, st, lo, up,
+                                     channels, pixels, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) store_map(key, *out);
+  return r;
 }
 
 // ------------------------------------------------------------------ validation
@@ -280,9 +351,7 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
                            static_cast<cuuint64_t>(a.xs_n) * 4};
   cuuint32_t box[4] = {32, static_cast<cuuint32_t>(best.box_w), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = encode_tiled()(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(a.x), dims, strides, box,
-                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = tiled_map(&map, 4, a.x, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (r != CUDA_SUCCESS) {
     cudaError_t e = launch_dw_simple(a, vec, s);
     return e == cudaSuccess ? CB_OK : cuda_fail(e);
@@ -292,6 +361,16 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
 }
 
 // -------------------------------------------------------------------- dense
+struct HaloPlan {
+  int bn = 0, nb = 0, grid = 0;
+  size_t smem = 0;
+};
+bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out);
+
+// Kernel for a dense (groups 1) layer under the current policy; fills
+// *plan for the halo kernel.
+cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan);
+
 int pick_bn(int M, int Cout, int k_iters, int sms, int* n_tiles_out) {
   static const int kBn[] = {16, 32, 48, 64, 96, 128, 192, 256};
   const int m_tiles = (M + 127) / 128;
@@ -380,9 +459,7 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
     const CUtensorMapSwizzle swz = kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
                                               : CU_TENSOR_MAP_SWIZZLE_32B;
-    CUresult r = encode_im2col()(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x->data, dims, strides, lower, upper,
-                                 static_cast<cuuint32_t>(kc), 128, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = im2col_map(&amap, x->data, dims, strides, lower, upper, static_cast<cuuint32_t>(kc), 128, estr, swz);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   {
@@ -393,12 +470,141 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
     const CUtensorMapSwizzle swz = kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
                                               : CU_TENSOR_MAP_SWIZZLE_32B;
-    CUresult r = encode_tiled()(&bmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(w), dims, strides, box,
-                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = tiled_map(&bmap, 3, w, dims, strides, box, estr, swz);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   cudaError_t e = launch_igemm(amap, bmap, a, bn, kc, grid, smem, s);
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+// 3x3 stride-1 pad-1 layers with Cin % 32 == 0 and an image width whose
+// halo tile leaves room for a weight ring: the halo-tile kernel.
+bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
+  if (Ci % 32 != 0 || W + 2 > 256) return false;
+  const int wp = W + 2;
+  const int rows = halo_rows(wp);
+  if (rows > 256) return false;
+  const int hb = halo_buffer_bytes(wp);
+  const int tiles_per_img = (H * wp + 127) / 128;
+  const long long m_tiles = static_cast<long long>(N) * tiles_per_img;
+  if (m_tiles * ((Co + 31) / 32) >= (1LL << 31)) return false;
+  const int num_kc = Ci / 32;
+  constexpr size_t kSmemMax = 227 * 1024;
+  double best = 1e300;
+  HaloPlan plan;
+  for (int bn : {256, 128, 64, 32}) {
+    int nb = 8;
+    while (nb >= 3 && halo_smem_bytes(bn, hb, nb) > kSmemMax) --nb;
+    if (nb < 3) continue;
+    const long long tiles = m_tiles * ((Co + bn - 1) / bn);
+    const long long grid = std::min<long long>(tiles, sms);
+    const long long per_cta = (tiles + grid - 1) / grid;
+    // Cycles per (tile, chunk): nine taps of tensor work (M=128, N=bn, K=32)
+    // against the bytes the copy engine brings in (halo + nine weight
+    // slices) at ~64 B per clock per SM when every SM pulls from L2.
+    const double mma = 9.0 * 2.55 * bn;
+    const double copy = (hb + 9.0 * bn * 128.0) / 64.0;
+    const double cost = static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 600.0) + 8.0 * bn;
+    if (cost < best * 0.97) {
+      best = cost;
+      plan.bn = bn;
+      plan.nb = nb;
+      plan.grid = static_cast<int>(grid);
+      plan.smem = halo_smem_bytes(bn, hb, nb);
+    }
+  }
+  if (plan.bn == 0) return false;
+  // Tuning override (CB_HALO_FORCE="bn,stages"; 0 = free), read per call.
+  if (const char* f = std::getenv("CB_HALO_FORCE")) {
+    int fb = 0, fs = 0;
+    std::sscanf(f, "%d,%d", &fb, &fs);
+    if (fb == 32 || fb == 64 || fb == 128 || fb == 256) {
+      const int nb = fs >= 2 ? fs : 8;
+      int n = nb;
+      while (n >= 2 && halo_smem_bytes(fb, hb, n) > kSmemMax) --n;
+      if (n >= 2) {
+        plan.bn = fb;
+        plan.nb = n;
+        plan.smem = halo_smem_bytes(fb, hb, n);
+        const long long tiles = m_tiles * ((Co + fb - 1) / fb);
+        plan.grid = static_cast<int>(std::min<long long>(tiles, sms));
+      }
+    }
+  }
+  *out = plan;
+  return true;
+}
+
+cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan) {
+  const int policy = g_policy.load();
+  const bool tc_ok = policy != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && tc_channels_ok(x->c, kh) &&
+                     aligned16(x->data) && strides_mult4(x) && x->n <= 65535 && x->w <= 65535 &&
+                     x->h <= 65535 && encode_tiled() && encode_im2col();
+  if (!tc_ok) return CB_PATH_DIRECT;
+  if (policy == 0 && kh == 3 && stride == 1 && pad == 1) {
+    DeviceInfo* dev = nullptr;
+    HaloPlan tmp;
+    if (current_device(&dev) == CB_OK && plan_halo(x->n, x->h, x->w, x->c, y->c, dev->sms, plan ? plan : &tmp))
+      return CB_PATH_TC_HALO;
+  }
+  return CB_PATH_TC_IM2COL;
+}
+
+cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep, const HaloPlan& plan,
+                         const cb_tensor* y, cudaStream_t s) {
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  const int Ci = x->c, Co = y->c;
+  HaloArgs a{};
+  a.H = x->h;
+  a.W = x->w;
+  a.Wp = x->w + 2;
+  a.Cout = Co;
+  a.num_kc = Ci / 32;
+  a.tiles_per_img = (a.H * a.Wp + 127) / 128;
+  a.m_tiles = x->n * a.tiles_per_img;
+  a.n_tiles = (Co + plan.bn - 1) / plan.bn;
+  a.rows = halo_rows(a.Wp);
+  a.halo_bytes = halo_buffer_bytes(a.Wp);
+  a.nb_stages = plan.nb;
+  a.out = make_out(y);
+  a.ep = ep;
+  a.err = dev->err;
+  a.timeout_ns = timeout_ns();
+  a.vec_store = (aligned16(a.out.y) && strides_mult4(y) && aligned16(ep.scale) && aligned16(ep.bias) &&
+                 (ep.res_mode == 0 || (aligned16(ep.r) && ep.rs_n % 4 == 0 && ep.rs_h % 4 == 0 && ep.rs_w % 4 == 0)))
+                    ? 1
+                    : 0;
+  if (const char* t = std::getenv("CB_IGEMM_TRACE")) {  // profiling aid: timeline of one CTA
+    a.trace = 1;
+    a.trace_cta = std::atoi(t);
+    if (const char* sl = std::getenv("CB_SPAN_SLOT")) a.trace = std::atoi(sl) == 2 ? 2 : 1;
+  }
+  if (std::getenv("CB_DEBUG_PLAN"))
+    std::fprintf(stderr, "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d -> bn=%d nb=%d rows=%d halo=%d tiles=%d grid=%d smem=%zu\n",
+                 x->n, a.H, a.W, Ci, Co, plan.bn, plan.nb, a.rows, a.halo_bytes, a.m_tiles * a.n_tiles, plan.grid,
+                 plan.smem);
+  CUtensorMap xmap, wmap;
+  {
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(x->w), static_cast<cuuint64_t>(x->h),
+                          static_cast<cuuint64_t>(x->n)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(x->stride_w) * 4, static_cast<cuuint64_t>(x->stride_h) * 4,
+                             static_cast<cuuint64_t>(x->stride_n) * 4};
+    cuuint32_t box[4] = {32, static_cast<cuuint32_t>(a.Wp), static_cast<cuuint32_t>(a.rows), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = tiled_map(&xmap, 4, x->data, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
+  }
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), 9, static_cast<cuuint64_t>(Co)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(Ci) * 4, static_cast<cuuint64_t>(9) * Ci * 4};
+    cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(plan.bn)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = tiled_map(&wmap, 3, w, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
+  }
+  cudaError_t e = launch_igemm_halo(xmap, wmap, a, plan.bn, plan.grid, plan.smem, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
 
@@ -517,12 +723,16 @@ cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale,
     if (kh != 3 || x->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
     return run_depthwise(x, w, ep, stride, pad, y, s);
   }
-  const bool tc_ok = policy != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && tc_channels_ok(x->c, kh) &&
-                     aligned16(x->data) &&
-                     aligned16(w) && strides_mult4(x) && x->n <= 65535 && x->w <= 65535 && x->h <= 65535 &&
-                     encode_tiled() && encode_im2col();
-  if (tc_ok) return run_igemm(x, w, ep, kh, stride, pad, y, s);
-  return run_direct(x, w, ep, kh, stride, pad, y, s);
+  if (!aligned16(w) && dense_path(x, y, kh, stride, pad, nullptr) != CB_PATH_DIRECT) {
+    // the tensor-core paths read w through TMA: an unaligned copy goes to the direct kernel
+    return run_direct(x, w, ep, kh, stride, pad, y, s);
+  }
+  HaloPlan plan;
+  switch (dense_path(x, y, kh, stride, pad, &plan)) {
+    case CB_PATH_TC_HALO: return run_igemm_halo(x, w, ep, plan, y, s);
+    case CB_PATH_TC_IM2COL: return run_igemm(x, w, ep, kh, stride, pad, y, s);
+    default: return run_direct(x, w, ep, kh, stride, pad, y, s);
+  }
 }
 
 cb_status cb_dw_separable_block_workspace(const cb_tensor* x, int c_out, int stride, size_t* bytes) {
@@ -702,7 +912,7 @@ const char* cb_status_string(cb_status s) {
 int cb_version(void) { return kVersion; }
 
 cb_status cb_set_kernel_policy(int policy) {
-  if (policy < 0 || policy > 1) return CB_ERR_INVALID_ARG;
+  if (policy < 0 || policy > 2) return CB_ERR_INVALID_ARG;
   g_policy.store(policy);
   return CB_OK;
 }
@@ -714,6 +924,22 @@ int cb_get_kernel_policy(void) { return g_policy.load(); }
 int cb_debug_igemm_trace(unsigned long long* out, int max_records) {
   cudaDeviceSynchronize();
   return igemm_read_trace(out, max_records);
+}
+
+// Profiling aid (not part of cb.h): per-CTA (start ns, end ns, SM) of the
+// traced halo-kernel launches in slots 1 and 2 (CB_SPAN_SLOT), then cleared;
+// returns the number of CTA rows copied (2 x 1024).
+int cb_debug_igemm_spans(unsigned long long* out, int max_ctas) {
+  cudaDeviceSynchronize();
+  return igemm_read_spans_halo(out, max_ctas);
+}
+
+int cb_conv_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, int groups) {
+  if (!view_ok(x) || !view_ok(y) || (kh != 1 && kh != 3) || (stride != 1 && stride != 2)) return 0;
+  if (pad < 0 || pad > kh / 2) return 0;
+  if (groups == x->c && groups == y->c && groups > 1) return kh == 3 ? CB_PATH_DEPTHWISE : 0;
+  if (groups != 1) return 0;
+  return dense_path(x, y, kh, stride, pad, nullptr);
 }
 
 int cb_conv_uses_tensor_cores(const cb_tensor* x, int kh, int groups) {

@@ -15,6 +15,7 @@
 //  * the input read through arbitrary strides, so NHWC and NCHW inputs share
 //    the kernel.
 #include "epilogue.cuh"
+#include "launch_util.h"
 #include "internal.h"
 
 namespace cb {
@@ -231,9 +232,10 @@ cudaError_t launch_tile(const DirectArgs& a, int vec_out, cudaStream_t s) {
   while (th > PX && smem_for(th) > 64 * 1024) th -= PX;
   const size_t smem = smem_for(th);
   if (smem > 64 * 1024) return cudaErrorInvalidValue;
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(direct_tile_kernel<S, KS, COB, PX, CI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
+  if (smem > 48 * 1024) {
+    const cudaError_t e = smem_attr_once<direct_tile_kernel<S, KS, COB, PX, CI>>(smem);
+    if (e != cudaSuccess) return e;
+  }
   const int co_blocks = (a.Co + COB - 1) / COB;
   dim3 grid((a.OW + kTileW - 1) / kTileW, (a.OH + th - 1) / th, a.N * co_blocks);
   direct_tile_kernel<S, KS, COB, PX, CI><<<grid, kTileW * (th / PX), smem, s>>>(a, th, vec_out);
@@ -264,8 +266,10 @@ template <int COB>
 cudaError_t launch_cob(const DirectArgs& a, int vec_out, cudaStream_t s) {
   const long long M = static_cast<long long>(a.N) * a.OH * a.OW;
   const size_t smem = static_cast<size_t>(a.kh) * a.kw * a.Ci * COB * sizeof(float);
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(direct_conv_kernel<COB>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (smem > 48 * 1024) {
+    const cudaError_t e = smem_attr_once<direct_conv_kernel<COB>>(smem);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid(static_cast<unsigned>((M + 255) / 256), static_cast<unsigned>((a.Co + COB - 1) / COB));
   direct_conv_kernel<COB><<<grid, 256, smem, s>>>(a, vec_out);
   return cudaGetLastError();

@@ -19,6 +19,7 @@
 //    channel, direct global loads.  Used for views the TMA path cannot
 //    describe (unaligned data, channel counts that are not multiples of 4).
 #include "epilogue.cuh"
+#include "launch_util.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -314,8 +315,7 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
 template <int S, int ACT, int RES>
 static void dw_tma_launch(const CUtensorMap& xmap, const DwTmaParams& p, int grid, int threads, size_t smem,
                           cudaStream_t s) {
-  cudaFuncSetAttribute(dw_tma_kernel<S, ACT, RES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       static_cast<int>(smem));
+  if (smem_attr_once<dw_tma_kernel<S, ACT, RES>>(smem) != cudaSuccess) return;
   dw_tma_kernel<S, ACT, RES><<<grid, threads, smem, s>>>(xmap, p);
 }
 
@@ -354,15 +354,25 @@ cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaP
 }
 
 // Occupancy query used by the planner (registers decide how many CTAs fit).
+// Cached per (stride, warps, shared-memory size in KB): occupancy is a
+// function of the kernel and these alone.
 int dw_tma_blocks_per_sm(int stride, int threads, size_t smem) {
+  static std::atomic<int> cache[2][33][229];
+  const int si = stride == 1 ? 0 : 1, wi = threads / 32, ki = static_cast<int>(smem / 1024);
+  const bool cacheable = threads % 32 == 0 && wi <= 32 && smem % 1024 == 0 && ki <= 228;
+  if (cacheable) {
+    const int v = cache[si][wi][ki].load(std::memory_order_relaxed);
+    if (v > 0) return v - 1;
+  }
   int n = 0;
   if (stride == 1) {
-    cudaFuncSetAttribute(dw_tma_kernel<1, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    smem_attr_once<dw_tma_kernel<1, 1, 0>>(smem);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dw_tma_kernel<1, 1, 0>, threads, smem);
   } else {
-    cudaFuncSetAttribute(dw_tma_kernel<2, 1, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    smem_attr_once<dw_tma_kernel<2, 1, 0>>(smem);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dw_tma_kernel<2, 1, 0>, threads, smem);
   }
+  if (cacheable) cache[si][wi][ki].store(n + 1, std::memory_order_relaxed);
   return n;
 }
 

@@ -1,0 +1,320 @@
+// Dense 3x3 stride-1 pad-1 convolution as an implicit GEMM on the
+// 5th-generation tensor cores, with the A operand taken from one shared-memory
+// halo tile per input-channel chunk instead of one im2col gather per filter
+// tap.
+//
+// GEMM view ("YOLO26N Inference Optimisation", NHWC migration: implicit GEMM
+// mapping): D[pixel, co] = sum over taps and Cin of x[shifted pixel, ci] *
+// W[co, tap, ci].  Here the output pixels of an image are numbered over a
+// padded width Wp = W + 2: q = oy * Wp + ox, ox in [0, Wp); the two columns
+// ox = W, W + 1 are computed and discarded.  In that numbering the input
+// pixel that tap (dy, dx) needs for output q sits at a constant offset
+//     (q - y_lo * Wp) + dy * Wp + dx
+// inside a halo tile holding input rows y_lo - 1 ... of the image, each
+// padded by one zero column on both sides (y_lo = first output row of the
+// tile).  So the nine taps of a 128-pixel tile are nine row offsets into ONE
+// tile in shared memory: the copy engine fetches each input element about
+// once per (tile, chunk) instead of nine times, and the tensor core reads
+// the shifted rows straight from the swizzled tile (the 128-byte swizzle is
+// a function of the shared-memory address, so a descriptor may start at any
+// 128-byte row of a tile that TMA wrote).
+//
+// Tile: 128 consecutive q of one image x BN output channels; K walks 32-channel
+// chunks, and inside a chunk the nine taps (K = 32 each, four MMAs of K = 8).
+//  * warp 0: TMA producer.  Lane 0 loads the halo tile of each (tile, chunk)
+//    -- a 4-D tiled copy of R input rows x Wp columns x 32 channels starting
+//    at (column -1, row y_lo - 1): rows and columns outside the image arrive
+//    as zeros, which is the convolution's zero padding.  Lanes 1-3 load the
+//    [BN x 32] weight slices, one per tap, each lane owning every third ring
+//    stage (copies from different lanes overlap; one lane's complete one
+//    after another).
+//  * warp 1 (one thread): tcgen05.mma kind::tf32 (M = 128, N = BN, K = 8)
+//    into one of NACC TMEM accumulators; tcgen05.commit releases weight
+//    stages, halo tiles and, at the end of a tile, the accumulator.
+//  * warps 2-9: epilogue (two groups of four warps, one per TMEM lane
+//    quarter), written back through TileStore: coalesced pixel-major stores,
+//    columns ox >= W and rows past the image masked.
+// CTAs are persistent and stride over the (pixel tile, channel tile) pairs.
+#pragma once
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_store.cuh"
+#include "trace.cuh"
+
+namespace cb {
+
+constexpr int kHaloThreads = 320;
+constexpr int kHaloKc = 32;              // input channels per K chunk (128-byte rows)
+constexpr int kHaloStagingBytes = 8 * TileStore<32>::kBufBytes;  // 8 epilogue warps x 4 KB
+
+// TMEM accumulators per CTA (the epilogue of one tile overlaps the MMAs of
+// the next ones) and the power-of-two column count they occupy.
+__host__ __device__ constexpr int halo_naccs(int bn) { return bn >= 256 ? 2 : 4; }
+__host__ __device__ constexpr int halo_tmem_cols(int bn) {
+  return halo_naccs(bn) * bn <= 128 ? 128 : halo_naccs(bn) * bn <= 256 ? 256 : 512;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                     const __grid_constant__ CUtensorMap wmap,
+                                                                     const HaloArgs a) {
+  static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "tile width");
+  const unsigned long long t_start = a.trace ? trace_globaltimer() : 0;
+  constexpr int NACC = halo_naccs(BN);
+  constexpr uint32_t kTmemCols = halo_tmem_cols(BN);
+  constexpr int kBBytes = BN * kHaloKc * 4;
+  constexpr uint32_t kIdesc = idesc_tf32(128, BN);
+  // Narrow tiles go to the two epilogue groups in turn; wider ones are split
+  // by columns, 32-column chunks.
+  constexpr bool kSplitTiles = BN == 32;
+  constexpr int kWidth = kSplitTiles ? BN : BN / 2;
+  constexpr int kChunks = kWidth / 32;
+  constexpr int kEpiArrivals = kSplitTiles ? 4 : 8;
+  constexpr int kBLanes = 3;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sHalo = smem;                                  // 2 x halo_bytes
+  uint8_t* sB = sHalo + 2 * a.halo_bytes;                 // nb x kBBytes
+  uint8_t* sStage = sB + a.nb_stages * kBBytes;           // epilogue staging
+  uint64_t* hfull = reinterpret_cast<uint64_t*>(sStage + kHaloStagingBytes);
+  uint64_t* hempty = hfull + 2;
+  uint64_t* bfull = hempty + 2;
+  uint64_t* bempty = bfull + a.nb_stages;
+  uint64_t* tfull = bempty + a.nb_stages;
+  uint64_t* tempty = tfull + NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + NACC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&hfull[h], 1);
+      mbar_init(&hempty[h], 1);
+    }
+    for (int s = 0; s < a.nb_stages; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
+    }
+    for (int b = 0; b < NACC; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kEpiArrivals);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const Watchdog wd{a.err, abort_flag, a.timeout_ns};
+  const int num_tiles = a.m_tiles * a.n_tiles;
+  const uint32_t halo_tx = static_cast<uint32_t>(kHaloKc * 4 * a.Wp * a.rows);
+  const bool tr_cta = a.trace && blockIdx.x == a.trace_cta;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane <= kBLanes) {
+      if (lane == 0) {
+        tma_prefetch_desc(&xmap);
+        tma_prefetch_desc(&wmap);
+      }
+      int h = 0, s = 0;
+      uint32_t hphase = 0, bphase = 0, issued = 0, last_parity = 0;
+      bool ok = true;
+      TraceBuf tr;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
+        const int n_img = m_tile / a.tiles_per_img;
+        const int q0 = (m_tile - n_img * a.tiles_per_img) * 128;
+        const int y_lo = q0 / a.Wp;
+        for (int kc = 0; ok && kc < a.num_kc; ++kc) {
+          if (lane == 0) {
+            if (!mbar_wait(&hempty[h], hphase ^ 1u, wd)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&hfull[h], halo_tx);
+            tma_load_4d(sHalo + h * a.halo_bytes, &xmap, &hfull[h], kc * kHaloKc, -1, y_lo - 1, n_img);
+            issued |= 1u << h;
+            last_parity = (last_parity & ~(1u << h)) | (hphase << h);
+          }
+          if (++h == 2) {
+            h = 0;
+            hphase ^= 1u;
+          }
+          for (int tap = 0; tap < 9; ++tap) {
+            if (lane != 0 && s % kBLanes == lane - 1) {
+              if (!mbar_wait(&bempty[s], bphase ^ 1u, wd)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&bfull[s], static_cast<uint32_t>(kBBytes));
+              tma_load_3d(sB + s * kBBytes, &wmap, &bfull[s], kc * kHaloKc, tap, n_tile * BN);
+              tr.add(tr_cta && lane == 1);
+              issued |= 1u << s;
+              last_parity = (last_parity & ~(1u << s)) | (bphase << s);
+            }
+            if (++s == a.nb_stages) {
+              s = 0;
+              bphase ^= 1u;
+            }
+          }
+        }
+      }
+      // Let every copy this lane issued land before the CTA can exit.
+      if (lane == 0) {
+        for (int hh = 0; hh < 2; ++hh)
+          if (issued & (1u << hh)) mbar_wait_drain(&hfull[hh], (last_parity >> hh) & 1u, 20000000ull);
+      } else {
+        for (int ss = 0; ss < a.nb_stages; ++ss)
+          if (issued & (1u << ss)) mbar_wait_drain(&bfull[ss], (last_parity >> ss) & 1u, 20000000ull);
+      }
+      tr.flush(tr_cta && lane == 1, 0);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int h = 0, s = 0;
+      uint32_t hphase = 0, bphase = 0;
+      uint32_t bcommitted = 0, bparity = 0, hcommitted = 0, hparity = 0, tcommitted = 0, tparity = 0;
+      bool ok = true;
+      int local = 0;
+      TraceBuf tr;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+        const int acc = local % NACC;
+        const uint32_t acc_phase = (local / NACC) & 1;
+        const int m_tile = tile / a.n_tiles;
+        const int n_img = m_tile / a.tiles_per_img;
+        const int q0 = (m_tile - n_img * a.tiles_per_img) * 128;
+        const int base_row = q0 - (q0 / a.Wp) * a.Wp;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wd)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kc = 0; ok && kc < a.num_kc; ++kc) {
+          if (!mbar_wait(&hfull[h], hphase, wd)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t halo_addr = smem_u32(sHalo + h * a.halo_bytes);
+          for (int tap = 0; tap < 9; ++tap) {
+            const int dy = tap / 3, dx = tap - 3 * (tap / 3);
+            if (!mbar_wait(&bfull[s], bphase, wd)) {
+              ok = false;
+              break;
+            }
+            tr.add(tr_cta);
+            tc_fence_after_sync();
+            const uint32_t a_addr = halo_addr + static_cast<uint32_t>((base_row + dy * a.Wp + dx) * 128);
+            const uint64_t adesc = kmajor_swizzled_desc(a_addr, 128);
+            const uint64_t bdesc = kmajor_swizzled_desc(smem_u32(sB + s * kBBytes), 128);
+#pragma unroll
+            for (int kk = 0; kk < kHaloKc / 8; ++kk)
+              mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kc | tap | kk) != 0 ? 1u : 0u);
+            mma_commit(&bempty[s]);
+            tr.add(tr_cta);
+            const uint32_t bit = 1u << s;
+            bparity = (bcommitted & bit) ? (bparity ^ bit) : (bparity & ~bit);
+            bcommitted |= bit;
+            if (++s == a.nb_stages) {
+              s = 0;
+              bphase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&hempty[h]);
+          const uint32_t hbit = 1u << h;
+          hparity = (hcommitted & hbit) ? (hparity ^ hbit) : (hparity & ~hbit);
+          hcommitted |= hbit;
+          if (++h == 2) {
+            h = 0;
+            hphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        const uint32_t tbit = 1u << acc;
+        tparity = (tcommitted & tbit) ? (tparity ^ tbit) : (tparity & ~tbit);
+        tcommitted |= tbit;
+      }
+      // Let every MMA this thread issued finish before TMEM is released.
+      for (int ss = 0; ss < a.nb_stages; ++ss)
+        if (bcommitted & (1u << ss)) mbar_wait_drain(&bempty[ss], (bparity >> ss) & 1u, 20000000ull);
+      for (int hh = 0; hh < 2; ++hh)
+        if (hcommitted & (1u << hh)) mbar_wait_drain(&hempty[hh], (hparity >> hh) & 1u, 20000000ull);
+      for (int b = 0; b < NACC; ++b)
+        if (tcommitted & (1u << b)) mbar_wait_drain(&tfull[b], (tparity >> b) & 1u, 20000000ull);
+      tr.flush(tr_cta, 1);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int group = (warp - 2) >> 2;
+    const int col0 = kSplitTiles ? 0 : group * kWidth;
+    uint8_t* stage_buf = sStage + (warp - 2) * TileStore<32>::kBufBytes;
+    const bool res = a.ep.res_mode != 0;
+    const bool vec = a.vec_store != 0;
+    int local = 0;
+    TraceBuf tr;
+    const bool tr_on = tr_cta && warp == 2 && lane == 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      if (kSplitTiles && (local & 1) != group) continue;
+      const int acc = local % NACC;
+      const uint32_t acc_phase = (local / NACC) & 1;
+      const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
+      const int n_img = m_tile / a.tiles_per_img;
+      const int qq = (m_tile - n_img * a.tiles_per_img) * 128 + q * 32 + lane;  // this thread's row
+      const int oy = qq / a.Wp, ox = qq - (qq / a.Wp) * a.Wp;
+      const bool valid = oy < a.H && ox < a.W;
+      const long long yoff =
+          valid ? n_img * a.out.ys_n + oy * a.out.ys_h + static_cast<long long>(ox) * a.out.ys_w : -1;
+      const long long roff = (valid && res) ? n_img * a.ep.rs_n + oy * a.ep.rs_h + static_cast<long long>(ox) * a.ep.rs_w : 0;
+      const int cbase = n_tile * BN + col0;
+
+      bool got = mbar_wait(&tfull[acc], acc_phase, wd);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) break;
+      tc_fence_after_sync();
+      tr.add(tr_on);
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + col0);
+#pragma unroll 1
+      for (int cidx = 0; cidx < kChunks; ++cidx) {
+        uint32_t v[32];
+        tmem_ld_cols<32>(taddr + cidx * 32, v);
+        tmem_ld_wait();
+        if (cidx == kChunks - 1) {
+          // every column of this warp's quarter is in registers: release the accumulator
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+        __syncwarp();  // the previous chunk's readers are done with the staging buffer
+        TileStore<32>::stage(stage_buf, lane, v);
+        __syncwarp();
+        TileStore<32>::write(stage_buf, lane, yoff, roff, cbase + cidx * 32, a.Cout, vec, a.out, a.ep);
+      }
+      tr.add(tr_on);
+    }
+    tr.flush(tr_on, 2);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    trace_cta_span(a.trace, 0, t_start);
+    trace_cta_span(a.trace, 1, trace_globaltimer());
+  }
+}
+
+}  // namespace cb

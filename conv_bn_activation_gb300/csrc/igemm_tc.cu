@@ -13,18 +13,20 @@ cudaError_t launch_igemm_kc32(const CUtensorMap&, const CUtensorMap&, const Igem
 int igemm_read_trace_kc8(unsigned long long* out, int max_records);
 int igemm_read_trace_kc16(unsigned long long* out, int max_records);
 int igemm_read_trace_kc32(unsigned long long* out, int max_records);
+int igemm_read_trace_halo(unsigned long long* out, int max_records);
 
 // The trace of whichever instantiation recorded one (profiling builds only).
 int igemm_read_trace(unsigned long long* out, int max_records) {
   int n = igemm_read_trace_kc32(out, max_records);
   if (n == 0) n = igemm_read_trace_kc16(out, max_records);
   if (n == 0) n = igemm_read_trace_kc8(out, max_records);
+  if (n == 0) n = igemm_read_trace_halo(out, max_records);
   return n;
 }
 
 int igemm_stages(int bn, int kc) {
   const int per = igemm_a_bytes(kc) + igemm_b_bytes(bn, kc);
-  int s = (224 * 1024 - 2048) / per;
+  int s = (224 * 1024 - 2048 - kIgemmStagingBytes) / per;
   if (s > 16) s = 16;
   if (s < 2) s = 2;
   return s;
@@ -32,6 +34,7 @@ int igemm_stages(int bn, int kc) {
 
 size_t igemm_smem_bytes(int bn, int kc, int stages) {
   return 1024 /*alignment slack*/ + static_cast<size_t>(stages) * (igemm_a_bytes(kc) + igemm_b_bytes(bn, kc)) +
+         kIgemmStagingBytes +
          (2 * stages + 2 * 4) * sizeof(uint64_t) + 16;
 }
 

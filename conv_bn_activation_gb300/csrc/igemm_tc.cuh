@@ -24,17 +24,13 @@
 //    smem stage and, at the end of a tile, the accumulator.
 //  * warps 2-9: epilogue, two groups of four warps (one per TMEM lane
 //    quarter = 32 output pixels).  Narrow tiles go to the groups in turn;
-//    wide tiles are split by columns between them.  Each warp reads its lanes with
-//    tcgen05.ld, applies scale/bias, residual and activation, rounds to the
-//    nearest TF32 value and stores its row segment.  (The MMA truncates its
-//    fp32 operands to TF32, which biases every product toward zero; storing
-//    round-to-nearest TF32 activations lets the next tensor-core layer read
-//    them exactly, so the bias does not compound along a chain.)  The
-//    residual of the next column chunk is loaded before the current one is
-//    finished, and the first chunk's before the accumulator is ready.  Rows
-//    past M and channels past Cout are masked, so nothing is written outside
-//    the logical output (padded output rows stay untouched -- "YOLO26N
-//    Inference Optimisation", Bug fixed: TMA overflow).
+//    wide tiles are split by columns between them.  Each warp reads its
+//    lanes with tcgen05.ld and writes them back through TileStore: staged in
+//    shared memory, then scale/bias, residual, activation and TF32 rounding
+//    applied pixel-major with coalesced stores.  Rows past M and channels
+//    past Cout are masked, so nothing is written outside the logical output
+//    (padded output rows stay untouched -- "YOLO26N Inference Optimisation",
+//    Bug fixed: TMA overflow).
 // Two to four TMEM accumulators let the epilogues of earlier tiles overlap
 // the MMAs of later ones.  CTAs are persistent (one per SM) and stride over
 // the tiles.
@@ -42,41 +38,19 @@
 
 #include "epilogue.cuh"
 #include "internal.h"
+#include "launch_util.h"
 #include "ptx.cuh"
+#include "tc_store.cuh"
+#include "trace.cuh"
 
 namespace cb {
-
-// Optional timeline of one CTA's pipeline (profiling aid, compiled in only
-// with -DCB_IGEMM_TRACE): each role keeps clock64 stamps in a local array and
-// copies them out when it finishes.
-#ifdef CB_IGEMM_TRACE
-constexpr int kTraceRecords = 512;
-static __device__ unsigned long long g_igemm_trace[3 * kTraceRecords];  // one copy per translation unit
-static __device__ int g_igemm_trace_n[3];
-struct TraceBuf {
-  unsigned long long t[kTraceRecords];
-  int n = 0;
-  __device__ __forceinline__ void add(bool on) {
-    if (on && n < kTraceRecords) t[n++] = clock64();
-  }
-  __device__ __forceinline__ void flush(bool on, int role) {
-    if (!on) return;
-    for (int i = 0; i < n; ++i) g_igemm_trace[role * kTraceRecords + i] = t[i];
-    g_igemm_trace_n[role] = n;
-  }
-};
-#else
-struct TraceBuf {
-  __device__ __forceinline__ void add(bool) {}
-  __device__ __forceinline__ void flush(bool, int) {}
-};
-#endif
 
 constexpr int kTileM = 128;
 constexpr int kEpiWarps = 8;
 constexpr int kProducerLanes = 4;
 constexpr int kIgemmThreads = 64 + 32 * kEpiWarps;
 
+constexpr int kIgemmStagingBytes = kEpiWarps * TileStore<16>::kBufBytes;  // chunks of at most 16 columns
 __host__ __device__ constexpr int igemm_a_bytes(int kc) { return kTileM * kc * 4; }
 __host__ __device__ constexpr int igemm_b_bytes(int bn, int kc) { return ((bn * kc * 4) + 1023) / 1024 * 1024; }
 // TMEM accumulators per CTA: narrow tiles keep four in flight so the MMAs can
@@ -84,25 +58,6 @@ __host__ __device__ constexpr int igemm_b_bytes(int bn, int kc) { return ((bn * 
 __host__ __device__ constexpr int igemm_naccs(int bn) { return bn <= 64 ? 4 : 2; }
 __host__ __device__ constexpr int tmem_cols_for(int cols) {
   return cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
-}
-
-// SiLU on the tensor-core path uses the fast exponential and division
-// (relative error ~1e-6, far inside this path's TF32 tolerance).
-__device__ __forceinline__ float tc_epi(float acc, float sc, float bi, float r, int act, int res_mode) {
-  float z = fmaf(acc, sc, bi);
-  if (res_mode == 1) z += r;
-  if (act == 1) z = fmaxf(z, 0.0f);
-  if (act == 2) z = __fdividef(z, 1.0f + __expf(-z));
-  if (res_mode == 2) z += r;
-  return round_tf32(z);
-}
-
-template <int CH>
-__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&v)[CH]) {
-  if constexpr (CH == 16)
-    tmem_ld_x16(taddr, v);
-  else
-    tmem_ld_x8(taddr, v);
 }
 
 template <int BN, int KC>
@@ -128,7 +83,8 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + a.stages * kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + a.stages * kBBytes);
+  uint8_t* sStage = sB + a.stages * kBBytes;  // epilogue staging, one buffer per epilogue warp
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kIgemmStagingBytes);
   uint64_t* empty = full + a.stages;
   uint64_t* tfull = empty + a.stages;
   uint64_t* tempty = tfull + NACC;
@@ -272,7 +228,9 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
     const int group = (warp - 2) >> 2;
     const int col0 = kSplitTiles ? 0 : group * kWidth;
     const int row = q * 32 + lane;          // tile row = output pixel within the tile
+    uint8_t* stage_buf = sStage + (warp - 2) * TileStore<CH>::kBufBytes;
     const bool res = a.ep.res_mode != 0;
+    const bool vec = a.vec_store != 0;
     int local = 0;
     TraceBuf tr;
     const bool tr_on = tr_cta && warp == 2 && lane == 0;
@@ -282,39 +240,15 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
       const uint32_t acc_phase = (local / NACC) & 1;
       const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
       const int m = m_tile * kTileM + row;
-      const bool valid = m < a.M;
-      int n_img = 0, oh = 0, ow = 0;
-      if (valid) {
-        n_img = m / a.OHW;
+      long long yoff = -1, roff = 0;
+      if (m < a.M) {
+        const int n_img = m / a.OHW;
         const int rem = m - n_img * a.OHW;
-        oh = rem / a.OW;
-        ow = rem - oh * a.OW;
+        const int oh = rem / a.OW, ow = rem - (rem / a.OW) * a.OW;
+        yoff = n_img * a.out.ys_n + oh * a.out.ys_h + static_cast<long long>(ow) * a.out.ys_w;
+        if (res) roff = n_img * a.ep.rs_n + oh * a.ep.rs_h + static_cast<long long>(ow) * a.ep.rs_w;
       }
-      float* yrow = a.out.y + n_img * a.out.ys_n + oh * a.out.ys_h + ow * a.out.ys_w;
-      const float* rrow = res ? a.ep.r + n_img * a.ep.rs_n + oh * a.ep.rs_h + ow * a.ep.rs_w : nullptr;
       const int cbase = n_tile * BN + col0;
-      // 4-column groups inside [0, Cout) go through 16-byte accesses when the
-      // views allow it; the rest element by element.
-      auto group_vec = [&](int c) { return a.vec_store && c + 4 <= a.Cout; };
-
-      // residual of the first chunk, fetched while the accumulator is computed
-      float rcur[CH];
-#pragma unroll
-      for (int j = 0; j < CH; ++j) rcur[j] = 0.0f;
-      auto load_res = [&](float(&r)[CH], int c0) {
-#pragma unroll
-        for (int j = 0; j < CH; j += 4) {
-          if (group_vec(c0 + j)) {
-            const float4 t = *reinterpret_cast<const float4*>(rrow + c0 + j);
-            r[j] = t.x, r[j + 1] = t.y, r[j + 2] = t.z, r[j + 3] = t.w;
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-              if (c0 + j + jj < a.Cout) r[j + jj] = rrow[c0 + j + jj];
-          }
-        }
-      };
-      if (res && valid) load_res(rcur, cbase);
 
       bool got = mbar_wait(&tfull[acc], acc_phase, wd);
       got = __all_sync(0xffffffffu, got);
@@ -323,44 +257,23 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
       tr.add(tr_on);
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + col0);
-#pragma unroll
+#pragma unroll 1
       for (int cidx = 0; cidx < kChunks; ++cidx) {
-        const int c0 = cbase + cidx * CH;
         uint32_t v[CH];
-        tmem_ld_chunk<CH>(taddr + cidx * CH, v);
-        float rnext[CH];
-#pragma unroll
-        for (int j = 0; j < CH; ++j) rnext[j] = 0.0f;
-        if (res && valid && cidx + 1 < kChunks) load_res(rnext, c0 + CH);
+        tmem_ld_cols<CH>(taddr + cidx * CH, v);
         tmem_ld_wait();
-        if (valid) {
-#pragma unroll
-          for (int j = 0; j < CH; j += 4) {
-            const int c = c0 + j;
-            if (group_vec(c)) {
-              const float4 sc = ldg4(a.ep.scale + c), bi = ldg4(a.ep.bias + c);
-              float4 o;
-              o.x = tc_epi(__uint_as_float(v[j]), sc.x, bi.x, rcur[j], a.ep.act, a.ep.res_mode);
-              o.y = tc_epi(__uint_as_float(v[j + 1]), sc.y, bi.y, rcur[j + 1], a.ep.act, a.ep.res_mode);
-              o.z = tc_epi(__uint_as_float(v[j + 2]), sc.z, bi.z, rcur[j + 2], a.ep.act, a.ep.res_mode);
-              o.w = tc_epi(__uint_as_float(v[j + 3]), sc.w, bi.w, rcur[j + 3], a.ep.act, a.ep.res_mode);
-              *reinterpret_cast<float4*>(yrow + c) = o;
-            } else {
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj)
-                if (c + jj < a.Cout)
-                  yrow[c + jj] = tc_epi(__uint_as_float(v[j + jj]), __ldg(a.ep.scale + c + jj),
-                                        __ldg(a.ep.bias + c + jj), rcur[j + jj], a.ep.act, a.ep.res_mode);
-            }
-          }
+        if (cidx == kChunks - 1) {
+          // every column of this warp's quarter is in registers: release the accumulator
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
         }
-#pragma unroll
-        for (int j = 0; j < CH; ++j) rcur[j] = rnext[j];
+        __syncwarp();  // the previous chunk's readers are done with the staging buffer
+        TileStore<CH>::stage(stage_buf, lane, v);
+        __syncwarp();
+        TileStore<CH>::write(stage_buf, lane, yoff, roff, cbase + cidx * CH, a.Cout, vec, a.out, a.ep);
       }
       tr.add(tr_on);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
     }
     tr.flush(tr_on, 2);
   }
@@ -373,33 +286,10 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
   }
 }
 
-// Copies this translation unit's trace out (see TraceBuf); returns the record count.
-static inline int igemm_read_trace_tu(unsigned long long* out, int max_records) {
-#ifdef CB_IGEMM_TRACE
-  int n[3] = {0, 0, 0};
-  if (cudaMemcpyFromSymbol(n, g_igemm_trace_n, sizeof(n)) != cudaSuccess) return -1;
-  if (n[0] + n[1] + n[2] == 0) return 0;
-  if (max_records < 3 * kTraceRecords + 3) return -1;
-  if (cudaMemcpyFromSymbol(out + 3, g_igemm_trace, sizeof(unsigned long long) * 3 * kTraceRecords) != cudaSuccess)
-    return -1;
-  out[0] = n[0];
-  out[1] = n[1];
-  out[2] = n[2];
-  const int zero[3] = {0, 0, 0};
-  cudaMemcpyToSymbol(g_igemm_trace_n, zero, sizeof(zero));
-  return n[0] + n[1] + n[2];
-#else
-  (void)out;
-  (void)max_records;
-  return 0;
-#endif
-}
-
 template <int BN, int KC>
 cudaError_t igemm_launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int grid,
                             size_t smem, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(igemm_tf32_kernel<BN, KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = smem_attr_once<igemm_tf32_kernel<BN, KC>>(smem);
   if (e != cudaSuccess) return e;
   igemm_tf32_kernel<BN, KC><<<grid, kIgemmThreads, smem, s>>>(amap, bmap, a);
   return cudaGetLastError();

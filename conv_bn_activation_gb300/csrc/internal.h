@@ -88,6 +88,36 @@ cudaError_t launch_igemm(const CUtensorMap& amap, const CUtensorMap& bmap, const
 size_t igemm_smem_bytes(int bn, int kc, int stages);
 int igemm_stages(int bn, int kc);
 
+// Halo-tile variant for 3x3 stride-1 pad-1 layers with Cin % 32 == 0: one
+// shared-memory tile of input rows per 32-channel chunk serves all nine taps
+// (igemm_halo.cuh).
+struct HaloArgs {
+  int H, W, Wp;        // input = output height / width; Wp = W + 2 (padded width)
+  int Cout;
+  int num_kc;          // Cin / 32
+  int tiles_per_img;   // ceil(H * Wp / 128)
+  int m_tiles;         // N * tiles_per_img
+  int n_tiles;         // ceil(Cout / BN)
+  int rows;            // input rows per halo copy
+  int halo_bytes;      // shared-memory bytes of one halo buffer (multiple of 1024)
+  int nb_stages;       // weight-slice ring depth
+  int vec_store;       // 1 when y / r rows allow 16-byte vector access
+  OutView out;
+  Epilogue ep;
+  int* err;
+  uint64_t timeout_ns;
+  int trace;           // 1: record the pipeline timeline of CTA trace_cta (profiling aid)
+  int trace_cta;
+};
+// Input rows one halo copy spans for a 128-pixel tile at padded width wp,
+// and the buffer bytes (rows * wp pixels of 128 bytes, plus 8 rows that only
+// the discarded padding columns of the last rows read).
+int halo_rows(int wp);
+int halo_buffer_bytes(int wp);
+size_t halo_smem_bytes(int bn, int halo_bytes, int nb_stages);
+cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int bn, int grid,
+                              size_t smem_bytes, cudaStream_t s);
+
 // -------------------------------------------------------------- preprocess
 cudaError_t launch_preprocess_fused(const uint8_t* src, int n, int hs, int ws, long long pitch, float* dst,
                                     int hd, int wd, cudaStream_t s);

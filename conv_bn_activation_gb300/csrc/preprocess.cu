@@ -19,6 +19,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "launch_util.h"
 
 namespace cb {
 
@@ -174,9 +175,10 @@ static cudaError_t launch_rows(const uint8_t* src, int n, int hs, int ws, long l
   if (n == 0 || hd == 0 || wd == 0) return cudaSuccess;
   const bool vec_in = (reinterpret_cast<uintptr_t>(src) % 16 == 0) && (pitch % 16 == 0);
   const size_t smem = row_smem(ws);
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(preprocess_row_kernel<TO_U8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
+  if (smem > 48 * 1024) {
+    const cudaError_t e = smem_attr_once<preprocess_row_kernel<TO_U8>>(smem);
+    if (e != cudaSuccess) return e;
+  }
   int threads = ((wd + 3) / 4 + 31) / 32 * 32;
   if (threads > 256) threads = 256;
   if (threads < 64) threads = 64;

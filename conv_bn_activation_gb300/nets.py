@@ -44,7 +44,7 @@ class ConvBnAct:
         cin = w_oihw.shape[1] * groups
         if tc_weights is None:
             tc_weights = (groups == 1 and cin % 4 == 0 and cin >= (8 if w_oihw.shape[2] == 1 else 16) and w_oihw.shape[2] in (1, 3)
-                          and cb.get_kernel_policy() == 0)
+                          and cb.get_kernel_policy() != 1)
         w = cb.repack_weights(w_oihw, groups)
         if tc_weights:
             w = cb.round_weights_tf32(w)
@@ -71,7 +71,7 @@ class DwBlock:
         self.cin, self.cout, self.stride = cin, cout, stride
         dws, dwb = cb.fold_bn(*p["bn1"])
         pws, pwb = cb.fold_bn(*p["bn2"])
-        tc = cin % 4 == 0 and cin >= 8 and cb.get_kernel_policy() == 0
+        tc = cin % 4 == 0 and cin >= 8 and cb.get_kernel_policy() != 1
         dense = cb.round_weights_tf32 if tc else (lambda a: a)
         self.params = {
             "dw_w": _dev(cb.repack_weights(p["dw_w"], groups=cin), device),

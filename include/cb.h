@@ -118,9 +118,12 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
  * element for element (in-place residual add).
  *
  * Paths (chosen on the host from the shape): dense layers with Ci % 4 == 0
- * and Ci >= 16 (3x3) or Ci >= 8 (1x1) run as an implicit GEMM on the tcgen05 tensor cores (TF32
- * inputs, fp32 accumulate, outputs rounded to the nearest TF32 value; needs
- * 16-byte aligned x/w and strides that are multiples of 4 elements);
+ * and Ci >= 16 (3x3) or Ci >= 8 (1x1) run as an implicit GEMM on the tcgen05
+ * tensor cores (TF32 inputs, fp32 accumulate, outputs rounded to the nearest
+ * TF32 value; needs 16-byte aligned x/w and strides that are multiples of 4
+ * elements).  Among those, 3x3 stride-1 pad-1 layers with Ci % 32 == 0 and
+ * W <= 254 take one shared-memory halo tile per 32-channel chunk for all
+ * nine taps; the others gather one im2col tile per tap;
  * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;
  * everything else (stems with 1 or 3 input channels, NCHW input, odd channel
  * counts) runs on a direct CUDA-core kernel in fp32.
@@ -236,7 +239,10 @@ int cb_last_cuda_error(void);
  * Process-wide kernel choice.  0 (the default) picks the fastest eligible
  * kernel for each shape; 1 restricts every layer to the plain CUDA-core
  * kernels (direct convolution, simple depthwise), a cross-check of the
- * TMA / tensor-core paths.  Returns CB_OK, or CB_ERR_INVALID_ARG.
+ * TMA / tensor-core paths; 2 is 0 without the halo-tile tensor-core kernel
+ * (3x3 stride-1 layers gather one im2col tile per tap instead), a
+ * cross-check of the two tensor-core kernels.  Returns CB_OK, or
+ * CB_ERR_INVALID_ARG.
  */
 cb_status cb_set_kernel_policy(int policy);
 
@@ -250,6 +256,22 @@ int cb_get_kernel_policy(void);
  * the nearest TF32 value; the other paths are fp32 throughout.
  */
 int cb_conv_uses_tensor_cores(const cb_tensor* x, int kh, int groups);
+
+/* Kernels behind cb_conv_bn_act (see cb_conv_path). */
+typedef enum {
+  CB_PATH_DIRECT = 1,     /* CUDA-core direct convolution, fp32 */
+  CB_PATH_DEPTHWISE = 2,  /* depthwise 3x3, fp32 */
+  CB_PATH_TC_IM2COL = 3,  /* tensor-core implicit GEMM, one im2col tile per filter tap */
+  CB_PATH_TC_HALO = 4     /* tensor-core implicit GEMM, one halo tile per 32-channel chunk (3x3, stride 1) */
+} cb_path;
+
+/*
+ * The cb_path that cb_conv_bn_act would take for input view x, output view
+ * y, a kh x kh kernel, stride, pad and groups under the current policy
+ * (with 16-byte aligned weights), or 0 if those arguments are unsupported.
+ * Host only; launches nothing.
+ */
+int cb_conv_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, int groups);
 
 /* A static string naming a status code. */
 const char* cb_status_string(cb_status s);

@@ -1,0 +1,144 @@
+"""GPU parity of the halo-tile tensor-core kernel (3x3, stride 1, pad 1, Cin % 32 == 0).
+
+Each output is checked against the fp64 oracle at the TF32 bar (5e-3 of max|oracle|).  The
+shapes cover one and several tiles per image, tiles that wrap across output rows, images narrower
+than a tile row and wider than one, channel counts that leave a ragged last channel tile, every
+tile width the kernel has (forced through CB_HALO_FORCE), the epilogue variants, channel-slice
+output views with padded rows (canaries must survive) and the in-place residual.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from conv_bn_activation_gb300 import binding as cb, synthetic
+from conv_bn_activation_gb300.nets import ConvBnAct
+from gpu_util import TOL_TF32, canary_buffer, is_canary, rel_err, sync_check, to_dev
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # N, H, W, Cin, Cout
+    (1, 1, 1, 32, 32), (2, 3, 5, 32, 16), (1, 20, 20, 64, 64), (2, 7, 40, 32, 40),
+    (1, 5, 80, 96, 128), (1, 4, 126, 32, 32), (1, 6, 150, 32, 32), (3, 9, 13, 64, 100),
+    (1, 20, 20, 256, 256), (2, 11, 17, 128, 384), (1, 40, 40, 128, 128), (1, 2, 2, 32, 8),
+]
+
+
+@pytest.fixture
+def halo_force():
+    old = os.environ.pop("CB_HALO_FORCE", None)
+    yield lambda v: os.environ.__setitem__("CB_HALO_FORCE", v)
+    os.environ.pop("CB_HALO_FORCE", None)
+    if old is not None:
+        os.environ["CB_HALO_FORCE"] = old
+
+
+def _run(x, w, bn, act=cb.ACT_SILU, residual=None, res_mode=0, y=None):
+    N, H, W, _ = x.shape
+    layer = ConvBnAct(w, bn, 1, 1, act)
+    if y is None:
+        y = torch.empty(N, H, W, w.shape[0], device="cuda")
+    xd = to_dev(x)
+    assert cb.conv_path(xd, y, 3, 1, 1) == cb.PATH_TC_HALO
+    layer(xd, y, residual=residual, res_mode=res_mode)
+    sync_check()
+    return y
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda s: "x".join(map(str, s)))
+def test_halo_silu(gpu, orc, case):
+    N, H, W, Ci, Co = case
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=sum(case))
+    y = _run(x, w, bn)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("bn_force", ["32,0", "64,0", "128,0", "256,0", "128,3", "64,16"])
+def test_halo_tile_widths(gpu, orc, halo_force, bn_force):
+    halo_force(bn_force)
+    x, w, bn = synthetic.dense_layer(64, 200, 10, 23, N=2, k=3, seed=3)
+    y = _run(x, w, bn)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("act,res_mode", [(0, 0), (1, 0), (1, 1), (2, 2), (0, 2), (2, 1)])
+def test_halo_epilogue_variants(gpu, orc, act, res_mode):
+    N, H, W, Ci, Co = 2, 9, 30, 32, 48
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=act + 5 * res_mode)
+    r = np.random.default_rng(4).standard_normal((N, H, W, Co)).astype(np.float32)
+    y = _run(x, w, bn, act=act, residual=to_dev(r) if res_mode else None, res_mode=res_mode)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=act, residual=r if res_mode else None,
+                          res_mode=res_mode)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+def test_halo_channel_slice_views_padded_rows(gpu, orc):
+    """Output into channels [36, 36+Co) of a wider buffer whose rows are padded: every element
+    outside the view keeps its canary."""
+    N, H, W, Ci, Co = 2, 13, 21, 64, 40
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=11)
+    buf = canary_buffer((N, H, W + 3, 36 + Co + 20))
+    y = buf[:, :, :W, 36:36 + Co]
+    _run(x, w, bn, y=y)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+    assert is_canary(buf[:, :, W:, :]) and is_canary(buf[:, :, :W, :36]) and is_canary(buf[:, :, :W, 36 + Co:])
+
+
+def test_halo_inplace_residual(gpu, orc):
+    N, H, W, C = 1, 16, 24, 64
+    x, w, bn = synthetic.dense_layer(C, C, H, W, N=N, k=3, seed=12)
+    r = np.random.default_rng(5).standard_normal((N, H, W, C)).astype(np.float32)
+    y = to_dev(r)
+    _run(x, w, bn, residual=y, res_mode=cb.RES_POST_ACT, y=y)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU, residual=r, res_mode=orc.RES_POST_ACT)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+def test_halo_matches_im2col_kernel(gpu):
+    """The two tensor-core kernels compute the same TF32 products in a different order; both
+    round their outputs to TF32 (10 stored mantissa bits), so a different fp32 sum may flip the
+    last stored bit: 2^-10 of a value at most."""
+    x, w, bn = synthetic.dense_layer(128, 128, 40, N=2, k=3, seed=13)
+    y0 = _run(x, w, bn)
+    cb.set_kernel_policy(2)
+    try:
+        layer = ConvBnAct(w, bn, 1, 1, cb.ACT_SILU)
+        y1 = torch.empty_like(y0)
+        xd = to_dev(x)
+        assert cb.conv_path(xd, y1, 3, 1, 1) == cb.PATH_TC_IM2COL
+        layer(xd, y1)
+        sync_check()
+    finally:
+        cb.set_kernel_policy(0)
+    assert rel_err(y0.cpu().numpy(), y1.cpu().numpy()) <= 2.0 ** -10
+
+
+def test_halo_not_taken_outside_its_shapes(gpu):
+    x = torch.empty(1, 8, 8, 48, device="cuda")  # Cin % 32 != 0
+    y = torch.empty(1, 8, 8, 32, device="cuda")
+    assert cb.conv_path(x, y, 3, 1, 1) == cb.PATH_TC_IM2COL
+    x = torch.empty(1, 8, 300, 32, device="cuda")  # too wide for two halo buffers
+    y = torch.empty(1, 8, 300, 32, device="cuda")
+    assert cb.conv_path(x, y, 3, 1, 1) == cb.PATH_TC_IM2COL
+    x = torch.empty(1, 8, 8, 32, device="cuda")
+    y = torch.empty(1, 4, 4, 32, device="cuda")
+    assert cb.conv_path(x, y, 3, 2, 1) == cb.PATH_TC_IM2COL
+
+
+@pytest.mark.parametrize("case", [(64, 64, 80), (128, 128, 40), (256, 256, 20)], ids=lambda s: "%d-%d@%d" % s)
+def test_halo_dense_sweep_batch16_sampled(gpu, orc, case):
+    """The stride-1 layers of the dense sweep at batch 16, in the launch configuration the
+    benchmark times; sampled outputs against the oracle point by point."""
+    Ci, Co, H = case
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, N=16, k=3)
+    y = _run(x, w, bn)
+    idx = np.random.default_rng(Ci).choice(y.numel(), 6000, replace=False)
+    idx = np.concatenate([idx, [0, y.numel() - 1]])
+    ref = orc.conv_bn_act_points(x, w, bn, idx, stride=1, pad=1, act=orc.ACT_SILU)
+    got = y.reshape(-1)[torch.from_numpy(idx).to("cuda")].cpu().numpy()
+    assert rel_err(got, ref) <= TOL_TF32
