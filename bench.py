@@ -170,6 +170,36 @@ class Workload:
         if events:
             events[len(self.launches)].record(stream)
 
+    def time_launches(self, torch, stream, device, reps=20, eager=False):
+        """ms per launch: `reps` back-to-back launches of each step entry (one CUDA
+        graph unless eager), timed with events around them."""
+        out = {}
+        for L in self.launches:
+            g = None
+            if self.capture and not eager:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    cap = torch.cuda.current_stream(device)
+                    for _ in range(reps):
+                        L.fn(cap)
+                g.replay()
+            else:
+                for _ in range(2):
+                    L.fn(stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if g is not None:
+                g.replay()
+            else:
+                for _ in range(reps):
+                    L.fn(stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out[L.name] = e0.elapsed_time(e1) / reps
+            del g
+        return out
+
     def step_units(self):
         if self.unit == "GB/s":
             return sum(L.work.bytes for L in self.launches)
@@ -512,44 +542,42 @@ def run_ours(args):
     nl = len(wl.launches)
     graph = None
     if wl.capture and not args.eager:
-        # The K timed steps are captured as one CUDA graph, with the per-launch
-        # events inside it (recorded as graph nodes at replay), so that the
-        # device timeline has no host gaps between launches.
-        try:
-            events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nl + 1)]
-                      for _ in range(args.steps)]
-        except TypeError:
-            events = None
-        if events is not None:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                cap = torch.cuda.current_stream(device)
-                for k in range(args.steps):
-                    wl.run(cap, events[k])
-            graph.replay()
-            torch.cuda.synchronize()
-    if graph is None:
-        events = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(args.steps)]
+        # The K timed steps are captured as one CUDA graph with no event
+        # between launches: the library launches each kernel with
+        # programmatic dependent launch, and an event between two kernels
+        # would serialise them again.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream(device)
+            for _ in range(args.steps):
+                wl.run(cap)
+        graph.replay()
+        torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch, local)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.start()
+    e_start.record(stream)
     if graph is not None:
         graph.replay()
     else:
-        for k in range(args.steps):
-            wl.run(stream, events[k])
+        for _ in range(args.steps):
+            wl.run(stream)
+    e_end.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [events[k][0].elapsed_time(events[k][nl]) for k in range(args.steps)]
-    total_ms = events[0][0].elapsed_time(events[-1][nl])
-    launch_ms = {L.name: statistics.mean(events[k][i].elapsed_time(events[k][i + 1]) for k in range(args.steps))
-                 for i, L in enumerate(wl.launches)}
+    total_ms = e_start.elapsed_time(e_end)
     if binding.get_device_error() != binding.OK:
         raise RuntimeError("device error during the timed steps")
+    # Per-kernel durations (the roofline's denominators): each launch of the
+    # step repeated back to back, events around the repetitions only.
+    launch_ms = wl.time_launches(torch, stream, device, reps=args.launch_reps, eager=args.eager)
+    if binding.get_device_error() != binding.OK:
+        raise RuntimeError("device error while timing the launches")
     extra = wl.extra(torch, stream, args.steps) if hasattr(wl, "extra") else None
 
     # e2e: host buffers, copies inside the timed region
@@ -596,16 +624,17 @@ def run_ours(args):
         "config": dict(wl.config, parallelism=f"replicas x{world} (independent images, no collective)"),
         "images_per_s": round(wl.batch * world * args.steps / (total_ms * 1e-3), 1),
         "us_per_image": round(total_ms * 1e3 / args.steps / wl.batch, 3),
-        "step_ms": {"median": round(statistics.median(step_ms), 4), "min": round(min(step_ms), 4),
-                    "max": round(max(step_ms), 4)},
         "launches": wl.per_launch(launch_ms, peaks),
         "roofline": wl.roofline(launch_ms, peaks),
         "e2e": None if args.no_e2e else {"value": round(e2e_units / (e2e_ms * 1e-3) / scale, 3), "unit": wl.unit,
                                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                          "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": getattr(wl, "kernels_per_step", nl) * args.steps,
-        "timing": "one CUDA graph of the K steps, per-launch events inside it" if graph is not None
-        else "eager launches, per-launch events between them",
+        "timing": {"steps": "one CUDA graph of the K steps, events around it" if graph is not None
+                   else "K eager steps, events around them",
+                   "launches": f"each launch repeated {args.launch_reps}x back to back "
+                               f"({'eager' if args.eager or not wl.capture else 'one CUDA graph'}), "
+                               "events around the repetitions"},
         "clocks": clocks,
     }
     if extra:
@@ -682,6 +711,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of one captured graph")
+    ap.add_argument("--launch-reps", type=int, default=20, help="back-to-back repetitions per kernel timing")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

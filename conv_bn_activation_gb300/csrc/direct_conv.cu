@@ -17,11 +17,14 @@
 #include "epilogue.cuh"
 #include "launch_util.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace cb {
 
 template <int COB>
 __global__ void __launch_bounds__(256) direct_conv_kernel(const DirectArgs a, int vec_out) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ __align__(16) float sw[];
   const int K = a.kh * a.kw * a.Ci;
   const int co0 = blockIdx.y * COB;
@@ -106,6 +109,8 @@ constexpr int kTileW = 32;
 
 template <int S, int KS, int COB, int PX, int CI>
 __global__ void __launch_bounds__(256) direct_tile_kernel(const DirectArgs a, int th, int vec_out) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ __align__(16) float sm[];
   const int Ci = CI ? CI : a.Ci;  // compile-time for the common channel counts
   const int rows_in = (th - 1) * S + KS;
@@ -238,8 +243,7 @@ cudaError_t launch_tile(const DirectArgs& a, int vec_out, cudaStream_t s) {
   }
   const int co_blocks = (a.Co + COB - 1) / COB;
   dim3 grid((a.OW + kTileW - 1) / kTileW, (a.OH + th - 1) / th, a.N * co_blocks);
-  direct_tile_kernel<S, KS, COB, PX, CI><<<grid, kTileW * (th / PX), smem, s>>>(a, th, vec_out);
-  return cudaGetLastError();
+  return launch_pdl(direct_tile_kernel<S, KS, COB, PX, CI>, grid, dim3(kTileW * (th / PX)), smem, s, a, th, vec_out);
 }
 
 template <int S, int KS, int COB>
@@ -271,8 +275,7 @@ cudaError_t launch_cob(const DirectArgs& a, int vec_out, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   dim3 grid(static_cast<unsigned>((M + 255) / 256), static_cast<unsigned>((a.Co + COB - 1) / COB));
-  direct_conv_kernel<COB><<<grid, 256, smem, s>>>(a, vec_out);
-  return cudaGetLastError();
+  return launch_pdl(direct_conv_kernel<COB>, grid, dim3(256), smem, s, a, vec_out);
 }
 }  // namespace
 

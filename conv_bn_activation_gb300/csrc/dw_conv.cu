@@ -28,6 +28,8 @@ namespace cb {
 // --------------------------------------------------------------- simple path
 template <bool VEC>
 __global__ void __launch_bounds__(256) dw_simple_kernel(const DwArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   constexpr int V = VEC ? 4 : 1;
   const int CV = a.C / V;
   const long long total = static_cast<long long>(a.N) * a.OH * a.OW * CV;
@@ -77,10 +79,9 @@ cudaError_t launch_dw_simple(const DwArgs& a, bool vec4, cudaStream_t s) {
   long long blocks = (total + 255) / 256;
   if (blocks > (1 << 20)) blocks = 1 << 20;
   if (vec4)
-    dw_simple_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    return launch_pdl(dw_simple_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
   else
-    dw_simple_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
-  return cudaGetLastError();
+    return launch_pdl(dw_simple_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, a);
 }
 
 // ------------------------------------------------------------------ TMA path
@@ -151,6 +152,8 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();
   const Watchdog wd{p.err, abort_flag, p.timeout_ns};
   const DwArgs& a = p.a;
 
@@ -316,7 +319,7 @@ template <int S, int ACT, int RES>
 static void dw_tma_launch(const CUtensorMap& xmap, const DwTmaParams& p, int grid, int threads, size_t smem,
                           cudaStream_t s) {
   if (smem_attr_once<dw_tma_kernel<S, ACT, RES>>(smem) != cudaSuccess) return;
-  dw_tma_kernel<S, ACT, RES><<<grid, threads, smem, s>>>(xmap, p);
+  launch_pdl(dw_tma_kernel<S, ACT, RES>, dim3(grid), dim3(threads), smem, s, xmap, p);
 }
 
 template <int S>

@@ -25,8 +25,7 @@ static cudaError_t halo_launch_bn(const CUtensorMap& xmap, const CUtensorMap& wm
                                   size_t smem, cudaStream_t s) {
   cudaError_t e = smem_attr_once<igemm_halo_kernel<BN>>(smem);
   if (e != cudaSuccess) return e;
-  igemm_halo_kernel<BN><<<grid, kHaloThreads, smem, s>>>(xmap, wmap, a);
-  return cudaGetLastError();
+  return launch_pdl(igemm_halo_kernel<BN>, dim3(grid), dim3(kHaloThreads), smem, s, xmap, wmap, a);
 }
 
 int igemm_read_trace_halo(unsigned long long* out, int max_records) { return igemm_read_trace_tu(out, max_records); }

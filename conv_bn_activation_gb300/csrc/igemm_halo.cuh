@@ -111,6 +111,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // This CTA holds its TMEM: the next kernel may launch (its CTAs cannot
+  // take TMEM this one still needs); then wait for the previous kernel.
+  pdl_launch_dependents();
+  pdl_wait();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{a.err, abort_flag, a.timeout_ns};
   const int num_tiles = a.m_tiles * a.n_tiles;

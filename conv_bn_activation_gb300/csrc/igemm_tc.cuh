@@ -111,6 +111,10 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // This CTA holds its TMEM: the next kernel may launch (its CTAs cannot
+  // take TMEM this one still needs); then wait for the previous kernel.
+  pdl_launch_dependents();
+  pdl_wait();
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{a.err, abort_flag, a.timeout_ns};
   const int num_tiles = a.m_tiles * a.n_tiles;
@@ -291,8 +295,7 @@ cudaError_t igemm_launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, co
                             size_t smem, cudaStream_t s) {
   cudaError_t e = smem_attr_once<igemm_tf32_kernel<BN, KC>>(smem);
   if (e != cudaSuccess) return e;
-  igemm_tf32_kernel<BN, KC><<<grid, kIgemmThreads, smem, s>>>(amap, bmap, a);
-  return cudaGetLastError();
+  return launch_pdl(igemm_tf32_kernel<BN, KC>, dim3(grid), dim3(kIgemmThreads), smem, s, amap, bmap, a);
 }
 
 template <int KC>

@@ -5,6 +5,8 @@
 
 #include <atomic>
 #include <cstddef>
+#include <cstdlib>
+#include <utility>
 
 namespace cb {
 
@@ -27,6 +29,34 @@ cudaError_t smem_attr_once(size_t smem) {
   while (cur < smem && !raised[dev].compare_exchange_weak(cur, smem, std::memory_order_acq_rel)) {
   }
   return cudaSuccess;
+}
+
+// Programmatic dependent launch is on unless CB_PDL=0 (read once).
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char* s = std::getenv("CB_PDL");
+    return !(s && s[0] == '0');
+  }();
+  return on;
+}
+
+// Launches `kernel` on stream s with programmatic stream serialisation: the
+// kernel may be launched before the previous kernel of the stream has
+// finished and must call pdl_wait() before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace cb

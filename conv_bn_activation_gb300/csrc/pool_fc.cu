@@ -6,10 +6,14 @@
 // memory.  The whole head moves ~38 KB per image; it exists so that the
 // network's last step also runs on the GPU.
 #include "internal.h"
+#include "launch_util.h"
+#include "ptx.cuh"
 
 namespace cb {
 
 __global__ void __launch_bounds__(256) pool_fc_kernel(const PoolFcArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ float pooled[];
   const int n = blockIdx.x;
   const float inv = 1.0f / static_cast<float>(a.H * a.W);
@@ -30,7 +34,8 @@ __global__ void __launch_bounds__(256) pool_fc_kernel(const PoolFcArgs a) {
 
 cudaError_t launch_pool_fc(const PoolFcArgs& a, cudaStream_t s) {
   if (a.N == 0) return cudaSuccess;
-  pool_fc_kernel<<<a.N, 256, a.C * sizeof(float), s>>>(a);
+  const cudaError_t e = launch_pdl(pool_fc_kernel, dim3(a.N), dim3(256), a.C * sizeof(float), s, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -20,6 +20,7 @@
 
 #include "internal.h"
 #include "launch_util.h"
+#include "ptx.cuh"
 
 namespace cb {
 
@@ -80,6 +81,8 @@ template <bool TO_U8>
 __global__ void __launch_bounds__(256) preprocess_row_kernel(const uint8_t* __restrict__ src, int hs, int ws,
                                                              long long pitch, void* __restrict__ out, int hd,
                                                              int wd, int vec_in, int vec_out) {
+  pdl_wait();
+  pdl_launch_dependents();
   // u / 255 for every u8 code, each an IEEE fp32 division, looked up instead
   // of divided per output.
   __shared__ float inv255[256];
@@ -183,9 +186,8 @@ static cudaError_t launch_rows(const uint8_t* src, int n, int hs, int ws, long l
   if (threads > 256) threads = 256;
   if (threads < 64) threads = 64;
   dim3 grid(hd, n);
-  preprocess_row_kernel<TO_U8><<<grid, threads, smem, s>>>(src, hs, ws, pitch, out, hd, wd, vec_in ? 1 : 0,
-                                                           vec_out ? 1 : 0);
-  return cudaGetLastError();
+  return launch_pdl(preprocess_row_kernel<TO_U8>, grid, dim3(threads), smem, s, src, hs, ws, pitch, out, hd, wd,
+                    vec_in ? 1 : 0, vec_out ? 1 : 0);
 }
 
 cudaError_t launch_preprocess_fused(const uint8_t* src, int n, int hs, int ws, long long pitch, float* dst, int hd,
@@ -202,6 +204,8 @@ cudaError_t launch_preprocess_resize(const uint8_t* src, int n, int hs, int ws, 
 // Pass 2: u8 -> fp32 / 255 (HWC kept).
 __global__ void __launch_bounds__(256) normalize_kernel(const uint8_t* __restrict__ in, long long count,
                                                         float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < count; i += stride)
     out[i] = __fdiv_rn(static_cast<float>(in[i]), 255.0f);
@@ -211,13 +215,14 @@ cudaError_t launch_preprocess_normalize(const uint8_t* in, long long count, floa
   if (count == 0) return cudaSuccess;
   long long blocks = (count + 255) / 256;
   if (blocks > 65536) blocks = 65536;
-  normalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(in, count, out);
-  return cudaGetLastError();
+  return launch_pdl(normalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, in, count, out);
 }
 
 // Pass 3: fp32 HWC [n, h, w, 3] -> fp32 CHW [n, 3, h, w].
 __global__ void __launch_bounds__(256) layout_kernel(const float* __restrict__ in, int n, int h, int w,
                                                      float* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long plane = static_cast<long long>(h) * w;
   const long long total = static_cast<long long>(n) * plane;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -236,7 +241,8 @@ cudaError_t launch_preprocess_layout(const float* in, int n, int h, int w, float
   if (total == 0) return cudaSuccess;
   long long blocks = (total + 255) / 256;
   if (blocks > 65536) blocks = 65536;
-  layout_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(in, n, h, w, out);
+  const cudaError_t e = launch_pdl(layout_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, in, n, h, w, out);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

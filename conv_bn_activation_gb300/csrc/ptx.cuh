@@ -90,6 +90,19 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// Kernels of this library are launched with programmatic stream
+// serialisation (launch_pdl), so that the next kernel of a stream is
+// launched -- its CTAs placed, barriers set up, TMEM allocated -- while the
+// previous one drains, instead of after a launch gap of several
+// microseconds.  pdl_wait blocks until the grid this launch depends on has
+// completed and its writes are visible (it returns at once when there is
+// none); every thread calls it before its first global-memory access.
+// pdl_launch_dependents lets the next grid launch; its CTAs still stop in
+// pdl_wait until this grid has completed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // -------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
