@@ -21,7 +21,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_
 ACT_NONE, ACT_RELU, ACT_SILU = 0, 1, 2
 RES_NONE, RES_PRE_ACT, RES_POST_ACT = 0, 1, 2
 LAYOUT_NHWC, LAYOUT_NCHW = 0, 1
-PATH_DIRECT, PATH_DEPTHWISE, PATH_TC_IM2COL, PATH_TC_HALO = 1, 2, 3, 4
+PATH_DIRECT, PATH_DEPTHWISE, PATH_TC_IM2COL, PATH_TC_HALO, PATH_TC_HALO_CM = 1, 2, 3, 4, 5
 
 EXPORTED = (
     "cb_fold_bn", "cb_repack_weights", "cb_conv_bn_act", "cb_dw_separable_block_workspace",

@@ -362,7 +362,9 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
 
 // -------------------------------------------------------------------- dense
 struct HaloPlan {
-  int bn = 0, nb = 0, grid = 0;
+  int px = 0, co = 0;  // tile: px pixels x co output channels
+  bool cm = false;     // channel-major accumulator (px = 256, co = 128)
+  int nb = 0, grid = 0;
   size_t smem = 0;
 };
 bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out);
@@ -482,55 +484,63 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
 bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
   if (Ci % 32 != 0 || W + 2 > 256) return false;
   const int wp = W + 2;
-  const int rows = halo_rows(wp);
-  if (rows > 256) return false;
-  const int hb = halo_buffer_bytes(wp);
-  const int tiles_per_img = (H * wp + 127) / 128;
-  const long long m_tiles = static_cast<long long>(N) * tiles_per_img;
-  if (m_tiles * ((Co + 31) / 32) >= (1LL << 31)) return false;
   const int num_kc = Ci / 32;
   constexpr size_t kSmemMax = 227 * 1024;
+  struct Shape {
+    int px, co;
+    bool cm;
+  };
+  static const Shape kShapes[] = {{256, 128, true}, {128, 256, false}, {128, 128, false}, {128, 64, false},
+                                  {128, 32, false}};
+  // Tuning override (CB_HALO_FORCE = "cm[,stages]" or "co[,stages]"), read per call.
+  int force_co = 0, force_nb = 0;
+  bool force_cm = false;
+  if (const char* f = std::getenv("CB_HALO_FORCE")) {
+    if (f[0] == 'c' && f[1] == 'm') {
+      force_cm = true;
+      if (f[2] == ',') force_nb = std::atoi(f + 3);
+    } else {
+      std::sscanf(f, "%d,%d", &force_co, &force_nb);
+    }
+  }
   double best = 1e300;
   HaloPlan plan;
-  for (int bn : {256, 128, 64, 32}) {
-    int nb = 8;
-    while (nb >= 3 && halo_smem_bytes(bn, hb, nb) > kSmemMax) --nb;
-    if (nb < 3) continue;
-    const long long tiles = m_tiles * ((Co + bn - 1) / bn);
+  for (const Shape& sh : kShapes) {
+    if (force_cm && !sh.cm) continue;
+    if (force_co && (sh.cm || sh.co != force_co)) continue;
+    const int rows = halo_rows(wp, sh.px);
+    if (rows > 256) continue;
+    const int hb = halo_buffer_bytes(wp, sh.px);
+    const int nb_max = force_nb >= 2 ? std::min(force_nb, 16) : 8;
+    int nb = nb_max;
+    while (nb >= 2 && halo_smem_bytes(sh.co, hb, nb) > kSmemMax) --nb;
+    if (nb < (force_nb >= 2 ? 2 : 3)) continue;
+    const long long m_tiles = static_cast<long long>(N) * ((H * wp + sh.px - 1) / sh.px);
+    const long long tiles = m_tiles * ((Co + sh.co - 1) / sh.co);
+    if (tiles >= (1LL << 31)) continue;
     const long long grid = std::min<long long>(tiles, sms);
     const long long per_cta = (tiles + grid - 1) / grid;
-    // Cycles per (tile, chunk): nine taps of tensor work (M=128, N=bn, K=32)
-    // against the bytes the copy engine brings in (halo + nine weight
-    // slices) at ~64 B per clock per SM when every SM pulls from L2.
-    const double mma = 9.0 * 2.55 * bn;
-    const double copy = (hb + 9.0 * bn * 128.0) / 64.0;
-    const double cost = static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 600.0) + 8.0 * bn;
+    // Cycles per (tile, chunk): nine taps of four K = 8 MMAs, each about
+    // 111 issue cycles for N <= 128 and 128 for N = 256 (measured), plus the
+    // per-tap barrier round trip; against the bytes the copy engine brings
+    // in (halo + nine weight slices) at ~64 B per clock per SM when every SM
+    // pulls from L2.  Plus the pipeline fill per tile and one exposed epilogue.
+    const int n = sh.cm ? sh.px : sh.co;
+    const double mma = 9.0 * (4.0 * (n > 128 ? 128.0 : 111.0) + 100.0);
+    const double copy = (hb + 9.0 * sh.co * 128.0) / 64.0;
+    const double cost =
+        static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 1500.0) + sh.px * sh.co / 2.3;
     if (cost < best * 0.97) {
       best = cost;
-      plan.bn = bn;
+      plan.px = sh.px;
+      plan.co = sh.co;
+      plan.cm = sh.cm;
       plan.nb = nb;
       plan.grid = static_cast<int>(grid);
-      plan.smem = halo_smem_bytes(bn, hb, nb);
+      plan.smem = halo_smem_bytes(sh.co, hb, nb);
     }
   }
-  if (plan.bn == 0) return false;
-  // Tuning override (CB_HALO_FORCE="bn,stages"; 0 = free), read per call.
-  if (const char* f = std::getenv("CB_HALO_FORCE")) {
-    int fb = 0, fs = 0;
-    std::sscanf(f, "%d,%d", &fb, &fs);
-    if (fb == 32 || fb == 64 || fb == 128 || fb == 256) {
-      const int nb = fs >= 2 ? fs : 8;
-      int n = nb;
-      while (n >= 2 && halo_smem_bytes(fb, hb, n) > kSmemMax) --n;
-      if (n >= 2) {
-        plan.bn = fb;
-        plan.nb = n;
-        plan.smem = halo_smem_bytes(fb, hb, n);
-        const long long tiles = m_tiles * ((Co + fb - 1) / fb);
-        plan.grid = static_cast<int>(std::min<long long>(tiles, sms));
-      }
-    }
-  }
+  if (plan.px == 0) return false;
   *out = plan;
   return true;
 }
@@ -544,8 +554,9 @@ cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, i
   if (policy == 0 && kh == 3 && stride == 1 && pad == 1) {
     DeviceInfo* dev = nullptr;
     HaloPlan tmp;
-    if (current_device(&dev) == CB_OK && plan_halo(x->n, x->h, x->w, x->c, y->c, dev->sms, plan ? plan : &tmp))
-      return CB_PATH_TC_HALO;
+    HaloPlan& p = plan ? *plan : tmp;
+    if (current_device(&dev) == CB_OK && plan_halo(x->n, x->h, x->w, x->c, y->c, dev->sms, &p))
+      return p.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
   }
   return CB_PATH_TC_IM2COL;
 }
@@ -562,11 +573,11 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   a.Wp = x->w + 2;
   a.Cout = Co;
   a.num_kc = Ci / 32;
-  a.tiles_per_img = (a.H * a.Wp + 127) / 128;
+  a.tiles_per_img = (a.H * a.Wp + plan.px - 1) / plan.px;
   a.m_tiles = x->n * a.tiles_per_img;
-  a.n_tiles = (Co + plan.bn - 1) / plan.bn;
-  a.rows = halo_rows(a.Wp);
-  a.halo_bytes = halo_buffer_bytes(a.Wp);
+  a.n_tiles = (Co + plan.co - 1) / plan.co;
+  a.rows = halo_rows(a.Wp, plan.px);
+  a.halo_bytes = halo_buffer_bytes(a.Wp, plan.px);
   a.nb_stages = plan.nb;
   a.out = make_out(y);
   a.ep = ep;
@@ -582,9 +593,11 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
     if (const char* sl = std::getenv("CB_SPAN_SLOT")) a.trace = std::atoi(sl) == 2 ? 2 : 1;
   }
   if (std::getenv("CB_DEBUG_PLAN"))
-    std::fprintf(stderr, "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d -> bn=%d nb=%d rows=%d halo=%d tiles=%d grid=%d smem=%zu\n",
-                 x->n, a.H, a.W, Ci, Co, plan.bn, plan.nb, a.rows, a.halo_bytes, a.m_tiles * a.n_tiles, plan.grid,
-                 plan.smem);
+    std::fprintf(stderr,
+                 "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d -> %s px=%d co=%d nb=%d rows=%d halo=%d tiles=%d "
+                 "grid=%d smem=%zu\n",
+                 x->n, a.H, a.W, Ci, Co, plan.cm ? "channel-major" : "pixel-major", plan.px, plan.co, plan.nb, a.rows,
+                 a.halo_bytes, a.m_tiles * a.n_tiles, plan.grid, plan.smem);
   CUtensorMap xmap, wmap;
   {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(x->w), static_cast<cuuint64_t>(x->h),
@@ -599,12 +612,12 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), 9, static_cast<cuuint64_t>(Co)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(Ci) * 4, static_cast<cuuint64_t>(9) * Ci * 4};
-    cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(plan.bn)};
+    cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(plan.co)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = tiled_map(&wmap, 3, w, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
-  cudaError_t e = launch_igemm_halo(xmap, wmap, a, plan.bn, plan.grid, plan.smem, s);
+  cudaError_t e = launch_igemm_halo(xmap, wmap, a, plan.px, plan.co, plan.cm, plan.grid, plan.smem, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
 
@@ -729,7 +742,8 @@ cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale,
   }
   HaloPlan plan;
   switch (dense_path(x, y, kh, stride, pad, &plan)) {
-    case CB_PATH_TC_HALO: return run_igemm_halo(x, w, ep, plan, y, s);
+    case CB_PATH_TC_HALO:
+    case CB_PATH_TC_HALO_CM: return run_igemm_halo(x, w, ep, plan, y, s);
     case CB_PATH_TC_IM2COL: return run_igemm(x, w, ep, kh, stride, pad, y, s);
     default: return run_direct(x, w, ep, kh, stride, pad, y, s);
   }

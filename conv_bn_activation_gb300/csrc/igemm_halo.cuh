@@ -19,21 +19,32 @@
 // a function of the shared-memory address, so a descriptor may start at any
 // 128-byte row of a tile that TMA wrote).
 //
-// Tile: 128 consecutive q of one image x BN output channels; K walks 32-channel
+// Tile: PX consecutive q of one image x CO output channels; K walks 32-channel
 // chunks, and inside a chunk the nine taps (K = 32 each, four MMAs of K = 8).
+// Two operand orders share this kernel:
+//  * pixel-major (PX = 128, CO = BN in 32..256): the accumulator holds
+//    pixels x channels, A = shifted halo rows, B = weights (M = 128, N = BN);
+//  * channel-major (PX = 256, CO = 128): the accumulator holds channels x
+//    pixels, A = weights, B = shifted halo rows (M = 128, N = 256).  On
+//    GB300 a kind::tf32 MMA costs about the same issue time for N = 64 and
+//    N = 128 and only a little more for N = 256 (111 / 111 / 128 cycles per
+//    K = 8 step, measured), so a layer with 128 output channels runs its
+//    tensor cores ~1.7x faster with 256 pixels as N than with its 128
+//    channels as N.
 //  * warp 0: TMA producer.  Lane 0 loads the halo tile of each (tile, chunk)
 //    -- a 4-D tiled copy of R input rows x Wp columns x 32 channels starting
 //    at (column -1, row y_lo - 1): rows and columns outside the image arrive
 //    as zeros, which is the convolution's zero padding.  Lanes 1-3 load the
-//    [BN x 32] weight slices, one per tap, each lane owning every third ring
+//    [CO x 32] weight slices, one per tap, each lane owning every third ring
 //    stage (copies from different lanes overlap; one lane's complete one
 //    after another).
-//  * warp 1 (one thread): tcgen05.mma kind::tf32 (M = 128, N = BN, K = 8)
+//  * warp 1 (one thread): tcgen05.mma kind::tf32 (M = 128, N = CO or PX, K = 8)
 //    into one of NACC TMEM accumulators; tcgen05.commit releases weight
 //    stages, halo tiles and, at the end of a tile, the accumulator.
 //  * warps 2-9: epilogue (two groups of four warps, one per TMEM lane
 //    quarter), written back through TileStore: coalesced pixel-major stores,
-//    columns ox >= W and rows past the image masked.
+//    columns ox >= W and rows past the image masked.  Channel-major tiles are
+//    transposed in the staging buffer (TileStore::stage_columns).
 // CTAs are persistent and stride over the (pixel tile, channel tile) pairs.
 #pragma once
 
@@ -49,26 +60,31 @@ constexpr int kHaloKc = 32;              // input channels per K chunk (128-byte
 constexpr int kHaloStagingBytes = 8 * TileStore<32>::kBufBytes;  // 8 epilogue warps x 4 KB
 
 // TMEM accumulators per CTA (the epilogue of one tile overlaps the MMAs of
-// the next ones) and the power-of-two column count they occupy.
-__host__ __device__ constexpr int halo_naccs(int bn) { return bn >= 256 ? 2 : 4; }
-__host__ __device__ constexpr int halo_tmem_cols(int bn) {
-  return halo_naccs(bn) * bn <= 128 ? 128 : halo_naccs(bn) * bn <= 256 ? 256 : 512;
+// the next ones) and the power-of-two column count they occupy, for an
+// accumulator of acc_cols columns.
+__host__ __device__ constexpr int halo_naccs(int acc_cols) { return acc_cols >= 256 ? 2 : 4; }
+__host__ __device__ constexpr int halo_tmem_cols(int acc_cols) {
+  return halo_naccs(acc_cols) * acc_cols <= 128 ? 128 : halo_naccs(acc_cols) * acc_cols <= 256 ? 256 : 512;
 }
 
-template <int BN>
+template <int PX, int CO, bool CM>
 __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                      const __grid_constant__ CUtensorMap wmap,
                                                                      const HaloArgs a) {
-  static_assert(BN == 32 || BN == 64 || BN == 128 || BN == 256, "tile width");
+  static_assert(CM ? (PX == 256 && CO == 128) : (PX == 128 && (CO == 32 || CO == 64 || CO == 128 || CO == 256)),
+                "tile shape");
   const unsigned long long t_start = a.trace ? trace_globaltimer() : 0;
-  constexpr int NACC = halo_naccs(BN);
-  constexpr uint32_t kTmemCols = halo_tmem_cols(BN);
-  constexpr int kBBytes = BN * kHaloKc * 4;
-  constexpr uint32_t kIdesc = idesc_tf32(128, BN);
-  // Narrow tiles go to the two epilogue groups in turn; wider ones are split
-  // by columns, 32-column chunks.
-  constexpr bool kSplitTiles = BN == 32;
-  constexpr int kWidth = kSplitTiles ? BN : BN / 2;
+  constexpr int kAccCols = CM ? PX : CO;  // TMEM columns of one accumulator
+  constexpr int NACC = halo_naccs(kAccCols);
+  constexpr uint32_t kTmemCols = halo_tmem_cols(kAccCols);
+  constexpr int kBBytes = CO * kHaloKc * 4;  // one tap's weight slice
+  constexpr uint32_t kIdesc = CM ? idesc_tf32(CO, PX) : idesc_tf32(PX, CO);
+  // Epilogue split of a tile between the two groups of four warps:
+  // pixel-major tiles of 32 channels alternate between the groups, wider
+  // ones are split into column halves; channel-major tiles give the groups
+  // alternate 32-pixel chunks.  Either way in 32-column chunks.
+  constexpr bool kSplitTiles = !CM && CO == 32;
+  constexpr int kWidth = CM ? PX / 2 : (kSplitTiles ? CO : CO / 2);
   constexpr int kChunks = kWidth / 32;
   constexpr int kEpiArrivals = kSplitTiles ? 4 : 8;
   constexpr int kBLanes = 3;
@@ -135,7 +151,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
         const int n_img = m_tile / a.tiles_per_img;
-        const int q0 = (m_tile - n_img * a.tiles_per_img) * 128;
+        const int q0 = (m_tile - n_img * a.tiles_per_img) * PX;
         const int y_lo = q0 / a.Wp;
         for (int kc = 0; ok && kc < a.num_kc; ++kc) {
           if (lane == 0) {
@@ -159,7 +175,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
                 break;
               }
               mbar_arrive_expect_tx(&bfull[s], static_cast<uint32_t>(kBBytes));
-              tma_load_3d(sB + s * kBBytes, &wmap, &bfull[s], kc * kHaloKc, tap, n_tile * BN);
+              tma_load_3d(sB + s * kBBytes, &wmap, &bfull[s], kc * kHaloKc, tap, n_tile * CO);
               tr.add(tr_cta && lane == 1);
               issued |= 1u << s;
               last_parity = (last_parity & ~(1u << s)) | (bphase << s);
@@ -195,11 +211,11 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
         const uint32_t acc_phase = (local / NACC) & 1;
         const int m_tile = tile / a.n_tiles;
         const int n_img = m_tile / a.tiles_per_img;
-        const int q0 = (m_tile - n_img * a.tiles_per_img) * 128;
+        const int q0 = (m_tile - n_img * a.tiles_per_img) * PX;
         const int base_row = q0 - (q0 / a.Wp) * a.Wp;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wd)) break;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         for (int kc = 0; ok && kc < a.num_kc; ++kc) {
           if (!mbar_wait(&hfull[h], hphase, wd)) {
             ok = false;
@@ -215,9 +231,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
             }
             tr.add(tr_cta);
             tc_fence_after_sync();
-            const uint32_t a_addr = halo_addr + static_cast<uint32_t>((base_row + dy * a.Wp + dx) * 128);
-            const uint64_t adesc = kmajor_swizzled_desc(a_addr, 128);
-            const uint64_t bdesc = kmajor_swizzled_desc(smem_u32(sB + s * kBBytes), 128);
+            const uint32_t x_addr = halo_addr + static_cast<uint32_t>((base_row + dy * a.Wp + dx) * 128);
+            const uint64_t xdesc = kmajor_swizzled_desc(x_addr, 128);
+            const uint64_t wdesc = kmajor_swizzled_desc(smem_u32(sB + s * kBBytes), 128);
+            const uint64_t adesc = CM ? wdesc : xdesc, bdesc = CM ? xdesc : wdesc;
 #pragma unroll
             for (int kk = 0; kk < kHaloKc / 8; ++kk)
               mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kc | tap | kk) != 0 ? 1u : 0u);
@@ -260,7 +277,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int group = (warp - 2) >> 2;
-    const int col0 = kSplitTiles ? 0 : group * kWidth;
+    const int col0 = (CM || kSplitTiles) ? 0 : group * kWidth;
     uint8_t* stage_buf = sStage + (warp - 2) * TileStore<32>::kBufBytes;
     const bool res = a.ep.res_mode != 0;
     const bool vec = a.vec_store != 0;
@@ -273,36 +290,76 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       const uint32_t acc_phase = (local / NACC) & 1;
       const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
       const int n_img = m_tile / a.tiles_per_img;
-      const int qq = (m_tile - n_img * a.tiles_per_img) * 128 + q * 32 + lane;  // this thread's row
-      const int oy = qq / a.Wp, ox = qq - (qq / a.Wp) * a.Wp;
-      const bool valid = oy < a.H && ox < a.W;
-      const long long yoff =
-          valid ? n_img * a.out.ys_n + oy * a.out.ys_h + static_cast<long long>(ox) * a.out.ys_w : -1;
-      const long long roff = (valid && res) ? n_img * a.ep.rs_n + oy * a.ep.rs_h + static_cast<long long>(ox) * a.ep.rs_w : 0;
-      const int cbase = n_tile * BN + col0;
+      const int q0 = (m_tile - n_img * a.tiles_per_img) * PX;
+      // Element offsets of output pixel q (-1: a padding column or past the image).
+      auto pixel_offsets = [&](int qq, long long& yoff, long long& roff) {
+        const int oy = qq / a.Wp, ox = qq - (qq / a.Wp) * a.Wp;
+        const bool valid = oy < a.H && ox < a.W;
+        yoff = valid ? n_img * a.out.ys_n + oy * a.out.ys_h + static_cast<long long>(ox) * a.out.ys_w : -1;
+        roff = (valid && res) ? n_img * a.ep.rs_n + oy * a.ep.rs_h + static_cast<long long>(ox) * a.ep.rs_w : 0;
+      };
 
       bool got = mbar_wait(&tfull[acc], acc_phase, wd);
       got = __all_sync(0xffffffffu, got);
       if (!got) break;
       tc_fence_after_sync();
       tr.add(tr_on);
-      const uint32_t taddr =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + col0);
+      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
+      if constexpr (!CM) {
+        // thread = pixel row q0 + 32q + lane; chunks of 32 channels
+        // The scale / bias of chunk k + 1 are in flight while chunk k is
+        // staged and stored.
+        long long yoff, roff;
+        pixel_offsets(q0 + q * 32 + lane, yoff, roff);
+        const int cbase = n_tile * CO + col0;
+        TileStore<32>::Consts k = TileStore<32>::consts(lane, cbase, a.Cout, vec, a.ep);
 #pragma unroll 1
-      for (int cidx = 0; cidx < kChunks; ++cidx) {
-        uint32_t v[32];
-        tmem_ld_cols<32>(taddr + cidx * 32, v);
-        tmem_ld_wait();
-        if (cidx == kChunks - 1) {
-          // every column of this warp's quarter is in registers: release the accumulator
-          tc_fence_before_sync();
+        for (int cidx = 0; cidx < kChunks; ++cidx) {
+          uint32_t v[32];
+          tmem_ld_cols<32>(lane_base + col0 + cidx * 32, v);
+          tmem_wait_regs(v);
+          TileStore<32>::Consts kn = k;
+          if (cidx + 1 < kChunks) {
+            kn = TileStore<32>::consts(lane, cbase + (cidx + 1) * 32, a.Cout, vec, a.ep);
+          } else {
+            // every column of this warp's quarter is in registers: release the accumulator
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          __syncwarp();  // the previous chunk's readers are done with the staging buffer
+          TileStore<32>::stage(stage_buf, lane, v);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[acc]);
+          TileStore<32>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+          k = kn;
         }
-        __syncwarp();  // the previous chunk's readers are done with the staging buffer
-        TileStore<32>::stage(stage_buf, lane, v);
-        __syncwarp();
-        TileStore<32>::write(stage_buf, lane, yoff, roff, cbase + cidx * 32, a.Cout, vec, a.out, a.ep);
+      } else {
+        // thread = output channel n_tile * CO + 32q + lane; chunks of 32
+        // pixels, group g taking chunks g, g + 2, ...
+        // This warp's 32 channels are the same in every chunk: their scale /
+        // bias are loaded once per tile.
+        const TileStore<32>::Consts k = TileStore<32>::consts(lane, n_tile * CO + q * 32, a.Cout, vec, a.ep);
+#pragma unroll 1
+        for (int kk = 0; kk < kChunks; ++kk) {
+          const int cidx = group + 2 * kk;
+          uint32_t v[32];
+          tmem_ld_cols<32>(lane_base + cidx * 32, v);
+          tmem_wait_regs(v);
+          if (kk == kChunks - 1) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+          }
+          tr.add(tr_on);
+          long long yoff, roff;
+          pixel_offsets(q0 + cidx * 32 + lane, yoff, roff);  // lane = pixel of the chunk for write()
+          __syncwarp();
+          TileStore<32>::stage_columns(stage_buf, lane, v);
+          __syncwarp();
+          tr.add(tr_on);
+          TileStore<32>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+          tr.add(tr_on);
+        }
       }
       tr.add(tr_on);
     }

@@ -261,12 +261,18 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
       tr.add(tr_on);
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + col0);
+      // The scale / bias of chunk k + 1 are in flight while chunk k is
+      // staged and stored.
+      typename TileStore<CH>::Consts k = TileStore<CH>::consts(lane, cbase, a.Cout, vec, a.ep);
 #pragma unroll 1
       for (int cidx = 0; cidx < kChunks; ++cidx) {
         uint32_t v[CH];
         tmem_ld_cols<CH>(taddr + cidx * CH, v);
-        tmem_ld_wait();
-        if (cidx == kChunks - 1) {
+        tmem_wait_regs(v);
+        typename TileStore<CH>::Consts kn = k;
+        if (cidx + 1 < kChunks) {
+          kn = TileStore<CH>::consts(lane, cbase + (cidx + 1) * CH, a.Cout, vec, a.ep);
+        } else {
           // every column of this warp's quarter is in registers: release the accumulator
           tc_fence_before_sync();
           __syncwarp();
@@ -275,7 +281,8 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
         __syncwarp();  // the previous chunk's readers are done with the staging buffer
         TileStore<CH>::stage(stage_buf, lane, v);
         __syncwarp();
-        TileStore<CH>::write(stage_buf, lane, yoff, roff, cbase + cidx * CH, a.Cout, vec, a.out, a.ep);
+        TileStore<CH>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+        k = kn;
       }
       tr.add(tr_on);
     }

@@ -109,14 +109,15 @@ struct HaloArgs {
   int trace;           // 1: record the pipeline timeline of CTA trace_cta (profiling aid)
   int trace_cta;
 };
-// Input rows one halo copy spans for a 128-pixel tile at padded width wp,
-// and the buffer bytes (rows * wp pixels of 128 bytes, plus 8 rows that only
-// the discarded padding columns of the last rows read).
-int halo_rows(int wp);
-int halo_buffer_bytes(int wp);
-size_t halo_smem_bytes(int bn, int halo_bytes, int nb_stages);
-cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int bn, int grid,
-                              size_t smem_bytes, cudaStream_t s);
+// Input rows one halo copy spans for a tile of px pixels at padded width
+// wp, and the buffer bytes (rows * wp pixels of 128 bytes, plus 8 rows that
+// only the discarded padding columns of the last rows read).
+int halo_rows(int wp, int px);
+int halo_buffer_bytes(int wp, int px);
+size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages);
+// px x co tile: 128 x {32, 64, 128, 256} pixel-major, or 256 x 128 channel-major (cm).
+cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
+                              bool cm, int grid, size_t smem_bytes, cudaStream_t s);
 
 // -------------------------------------------------------------- preprocess
 cudaError_t launch_preprocess_fused(const uint8_t* src, int n, int hs, int ws, long long pitch, float* dst,

@@ -65,6 +65,36 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// tcgen05.wait::ld that names the destination registers of the loads it
+// waits for, so that no use of them can be scheduled above it.
+__device__ __forceinline__ void tmem_wait_regs(uint32_t (&r)[32]) {
+  __syncwarp();
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_regs(uint32_t (&r)[16]) {
+  __syncwarp();
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_regs(uint32_t (&r)[8]) {
+  __syncwarp();
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+
 template <int CH>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[CH]) {
   static_assert(CH == 8 || CH == 16 || CH == 32, "chunk width");
@@ -100,75 +130,116 @@ struct TileStore {
       *reinterpret_cast<uint4*>(rowp + ((j ^ s) << 4)) = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   }
 
-  // yoff / roff: this lane's row's element offsets into y / r (yoff < 0:
-  // row masked).  c0: first output channel of the chunk.  One uniform
-  // branch per chunk picks the compile-time epilogue.
-  __device__ static __forceinline__ void write(const uint8_t* buf, int lane, long long yoff, long long roff, int c0,
-                                               int Cout, bool vec, const OutView& out, const Epilogue& ep) {
-    switch (ep.act * 3 + ep.res_mode) {
-      case 0: write_t<0, 0>(buf, lane, yoff, roff, c0, Cout, vec, out, ep); break;
-      case 1: write_t<0, 1>(buf, lane, yoff, roff, c0, Cout, vec, out, ep); break;
-      case 2: write_t<0, 2>(buf, lane, yoff, roff, c0, Cout, vec, out, ep); break;
-      case 3: write_t<1, 0>(buf, lane, yoff, roff, c0, Cout, vec, out, ep); break;
-      case 4: write_t<1, 1>(buf, lane, yoff, roff, c0, Cout, vec, out, ep); break;
-      case 5: write_t<1, 2>(buf, lane, yoff, roff, c0, Cout, vec, out, ep); break;
-      case 6: write_t<2, 0>(buf, lane, yoff, roff, c0, Cout, vec, out, ep); break;
-      case 7: write_t<2, 1>(buf, lane, yoff, roff, c0, Cout, vec, out, ep); break;
-      default: write_t<2, 2>(buf, lane, yoff, roff, c0, Cout, vec, out, ep); break;
-    }
+  // The transpose of stage(): thread `lane` holds column `lane` (one output
+  // channel) for 32 rows (pixels), v[p] being row p; it lands where write()
+  // reads it.  For each p the 32 lanes hit 32 different banks.
+  __device__ static __forceinline__ void stage_columns(uint8_t* buf, int lane, const uint32_t (&v)[CH]) {
+    static_assert(CH == 32, "square 32 x 32 block");
+    const int j = lane >> 2, e = (lane & 3) * 4;
+#pragma unroll
+    for (int p = 0; p < 32; ++p) *reinterpret_cast<uint32_t*>(buf + p * kRowBytes + ((j ^ swz(p)) << 4) + e) = v[p];
   }
 
-  template <int ACT, int RES>
-  __device__ static __forceinline__ void write_t(const uint8_t* buf, int lane, long long yoff, long long roff,
-                                                 int c0, int Cout, bool vec, const OutView& out,
-                                                 const Epilogue& ep) {
-    const int j = lane % kLpp;
-    const int c = c0 + 4 * j;
-    const bool cvec = vec && c + 4 <= Cout;
-    constexpr bool res = RES != 0;
+  // Per-lane epilogue constants of one chunk: the lane's 16-byte channel
+  // group c .. c + 3 (c = c0 + 4 * (lane % kLpp)) and its folded-BN scale
+  // and bias.  Loaded once per chunk position -- for a channel-major tile
+  // once per tile -- ahead of the chunk they serve.
+  struct Consts {
     float sc[4], bi[4];
-    if (cvec) {
-      const float4 s4 = __ldg(reinterpret_cast<const float4*>(ep.scale + c));
-      const float4 b4 = __ldg(reinterpret_cast<const float4*>(ep.bias + c));
-      sc[0] = s4.x, sc[1] = s4.y, sc[2] = s4.z, sc[3] = s4.w;
-      bi[0] = b4.x, bi[1] = b4.y, bi[2] = b4.z, bi[3] = b4.w;
+    int c;
+    bool cvec, cin;
+  };
+  __device__ static __forceinline__ Consts consts(int lane, int c0, int Cout, bool vec, const Epilogue& ep) {
+    Consts k;
+    k.c = c0 + 4 * (lane % kLpp);
+    k.cvec = vec && k.c + 4 <= Cout;
+    k.cin = k.c < Cout;
+    if (k.cvec) {
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(ep.scale + k.c));
+      const float4 b4 = __ldg(reinterpret_cast<const float4*>(ep.bias + k.c));
+      k.sc[0] = s4.x, k.sc[1] = s4.y, k.sc[2] = s4.z, k.sc[3] = s4.w;
+      k.bi[0] = b4.x, k.bi[1] = b4.y, k.bi[2] = b4.z, k.bi[3] = b4.w;
     } else {
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
-        sc[jj] = c + jj < Cout ? __ldg(ep.scale + c + jj) : 0.0f;
-        bi[jj] = c + jj < Cout ? __ldg(ep.bias + c + jj) : 0.0f;
+        k.sc[jj] = k.c + jj < Cout ? __ldg(ep.scale + k.c + jj) : 0.0f;
+        k.bi[jj] = k.c + jj < Cout ? __ldg(ep.bias + k.c + jj) : 0.0f;
       }
     }
+    return k;
+  }
+
+  // yoff / roff: this lane's row's element offsets into y / r (yoff < 0:
+  // row masked).  One uniform branch per chunk picks the compile-time
+  // epilogue.
+  __device__ static __forceinline__ void write(const uint8_t* buf, int lane, long long yoff, long long roff,
+                                               const Consts& k, int Cout, const OutView& out, const Epilogue& ep) {
+    switch (ep.act * 3 + ep.res_mode) {
+      case 0: write_t<0, 0>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 1: write_t<0, 1>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 2: write_t<0, 2>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 3: write_t<1, 0>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 4: write_t<1, 1>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 5: write_t<1, 2>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 6: write_t<2, 0>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 7: write_t<2, 1>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      default: write_t<2, 2>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+    }
+  }
+
+  // Straight-line over the kLpp passes: all loads first, then all the math,
+  // then the (predicated) stores, so that the exponentials and reciprocals of
+  // different pixels overlap instead of each pass waiting on the last.
+  template <int ACT, int RES>
+  __device__ static __forceinline__ void write_t(const uint8_t* buf, int lane, long long yoff, long long roff,
+                                                 const Consts& k, int Cout, const OutView& out,
+                                                 const Epilogue& ep) {
+    const int j = lane % kLpp;
+    const int c = k.c;
+    long long yo[kLpp], ro[kLpp];
+    float z[kLpp][4];
 #pragma unroll
     for (int pass = 0; pass < kLpp; ++pass) {
       const int p = pass * kPpi + lane / kLpp;
-      const long long yo = __shfl_sync(0xffffffffu, yoff, p);
-      const long long ro = res ? __shfl_sync(0xffffffffu, roff, p) : 0;
-      if (yo < 0 || c >= Cout) continue;
+      yo[pass] = __shfl_sync(0xffffffffu, yoff, p);
+      ro[pass] = RES != 0 ? __shfl_sync(0xffffffffu, roff, p) : 0;
       const uint4 u = *reinterpret_cast<const uint4*>(buf + p * kRowBytes + ((j ^ swz(p)) << 4));
-      const float acc[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
-      float r[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if constexpr (res) {
-        const float* rp = ep.r + ro + c;
-        if (cvec) {
-          const float4 t = *reinterpret_cast<const float4*>(rp);
-          r[0] = t.x, r[1] = t.y, r[2] = t.z, r[3] = t.w;
-        } else {
+      z[pass][0] = __uint_as_float(u.x), z[pass][1] = __uint_as_float(u.y);
+      z[pass][2] = __uint_as_float(u.z), z[pass][3] = __uint_as_float(u.w);
+    }
+    float r[kLpp][4];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-            if (c + jj < Cout) r[jj] = rp[jj];
+    for (int pass = 0; pass < kLpp; ++pass) {
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) r[pass][jj] = 0.0f;
+      if constexpr (RES != 0) {
+        if (yo[pass] >= 0 && k.cin) {
+          const float* rp = ep.r + ro[pass] + c;
+          if (k.cvec) {
+            const float4 t = *reinterpret_cast<const float4*>(rp);
+            r[pass][0] = t.x, r[pass][1] = t.y, r[pass][2] = t.z, r[pass][3] = t.w;
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              if (c + jj < Cout) r[pass][jj] = rp[jj];
+          }
         }
       }
-      float o[4];
+    }
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) o[jj] = tc_epi_t<ACT, RES>(acc[jj], sc[jj], bi[jj], r[jj]);
-      float* yp = out.y + yo + c;
-      if (cvec) {
-        *reinterpret_cast<float4*>(yp) = make_float4(o[0], o[1], o[2], o[3]);
+    for (int pass = 0; pass < kLpp; ++pass)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) z[pass][jj] = tc_epi_t<ACT, RES>(z[pass][jj], k.sc[jj], k.bi[jj], r[pass][jj]);
+#pragma unroll
+    for (int pass = 0; pass < kLpp; ++pass) {
+      if (yo[pass] < 0 || !k.cin) continue;
+      float* yp = out.y + yo[pass] + c;
+      if (k.cvec) {
+        *reinterpret_cast<float4*>(yp) = make_float4(z[pass][0], z[pass][1], z[pass][2], z[pass][3]);
       } else {
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
-          if (c + jj < Cout) yp[jj] = o[jj];
+          if (c + jj < Cout) yp[jj] = z[pass][jj];
       }
     }
   }

@@ -262,7 +262,9 @@ typedef enum {
   CB_PATH_DIRECT = 1,     /* CUDA-core direct convolution, fp32 */
   CB_PATH_DEPTHWISE = 2,  /* depthwise 3x3, fp32 */
   CB_PATH_TC_IM2COL = 3,  /* tensor-core implicit GEMM, one im2col tile per filter tap */
-  CB_PATH_TC_HALO = 4     /* tensor-core implicit GEMM, one halo tile per 32-channel chunk (3x3, stride 1) */
+  CB_PATH_TC_HALO = 4,    /* tensor-core implicit GEMM, one halo tile per 32-channel chunk (3x3, stride 1),
+                             128 pixels x up to 256 channels per tile */
+  CB_PATH_TC_HALO_CM = 5  /* the same with 256 pixels x 128 channels per tile, channels as the MMA's M */
 } cb_path;
 
 /*

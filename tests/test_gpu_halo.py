@@ -1,4 +1,6 @@
-"""GPU parity of the halo-tile tensor-core kernel (3x3, stride 1, pad 1, Cin % 32 == 0).
+"""GPU parity of the halo-tile tensor-core kernel (3x3, stride 1, pad 1, Cin % 32 == 0), in both of
+its tile shapes: pixel-major (128 pixels x up to 256 channels) and channel-major (256 pixels x 128
+channels, the channels as the MMA's M).
 
 Each output is checked against the fp64 oracle at the TF32 bar (5e-3 of max|oracle|).  The
 shapes cover one and several tiles per image, tiles that wrap across output rows, images narrower
@@ -41,7 +43,7 @@ def _run(x, w, bn, act=cb.ACT_SILU, residual=None, res_mode=0, y=None):
     if y is None:
         y = torch.empty(N, H, W, w.shape[0], device="cuda")
     xd = to_dev(x)
-    assert cb.conv_path(xd, y, 3, 1, 1) == cb.PATH_TC_HALO
+    assert cb.conv_path(xd, y, 3, 1, 1) in (cb.PATH_TC_HALO, cb.PATH_TC_HALO_CM)
     layer(xd, y, residual=residual, res_mode=res_mode)
     sync_check()
     return y
@@ -56,7 +58,7 @@ def test_halo_silu(gpu, orc, case):
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
 
 
-@pytest.mark.parametrize("bn_force", ["32,0", "64,0", "128,0", "256,0", "128,3", "64,16"])
+@pytest.mark.parametrize("bn_force", ["32,0", "64,0", "128,0", "256,0", "128,3", "64,16", "cm", "cm,2"])
 def test_halo_tile_widths(gpu, orc, halo_force, bn_force):
     halo_force(bn_force)
     x, w, bn = synthetic.dense_layer(64, 200, 10, 23, N=2, k=3, seed=3)
@@ -142,3 +144,44 @@ def test_halo_dense_sweep_batch16_sampled(gpu, orc, case):
     ref = orc.conv_bn_act_points(x, w, bn, idx, stride=1, pad=1, act=orc.ACT_SILU)
     got = y.reshape(-1)[torch.from_numpy(idx).to("cuda")].cpu().numpy()
     assert rel_err(got, ref) <= TOL_TF32
+
+
+CM_CASES = [
+    # N, H, W, Cin, Cout: one and several 256-pixel tiles, ragged channel tiles, tiny images
+    (1, 1, 1, 32, 128), (2, 3, 5, 32, 128), (1, 20, 20, 128, 128), (2, 9, 40, 64, 200),
+    (1, 16, 16, 256, 256), (3, 7, 13, 32, 100), (1, 5, 60, 96, 384),
+]
+
+
+@pytest.mark.parametrize("case", CM_CASES, ids=lambda s: "x".join(map(str, s)))
+def test_halo_channel_major(gpu, orc, halo_force, case):
+    halo_force("cm")
+    N, H, W, Ci, Co = case
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=sum(case) + 7)
+    layer = ConvBnAct(w, bn, 1, 1, cb.ACT_SILU)
+    y = torch.empty(N, H, W, Co, device="cuda")
+    xd = to_dev(x)
+    assert cb.conv_path(xd, y, 3, 1, 1) == cb.PATH_TC_HALO_CM
+    layer(xd, y)
+    sync_check()
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("act,res_mode", [(1, 1), (2, 2), (0, 0)])
+def test_halo_channel_major_epilogues_and_views(gpu, orc, halo_force, act, res_mode):
+    """Channel-major tiles into a channel slice of a padded buffer, with a residual."""
+    halo_force("cm")
+    N, H, W, Ci, Co = 2, 11, 19, 64, 128
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=31 + act)
+    r = np.random.default_rng(6).standard_normal((N, H, W, Co)).astype(np.float32)
+    buf = canary_buffer((N, H, W + 5, Co + 36))
+    y = buf[:, :, :W, 32:32 + Co]
+    layer = ConvBnAct(w, bn, 1, 1, act)
+    xd = to_dev(x)
+    assert cb.conv_path(xd, y, 3, 1, 1) == cb.PATH_TC_HALO_CM
+    layer(xd, y, residual=to_dev(r) if res_mode else None, res_mode=res_mode)
+    sync_check()
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=act, residual=r if res_mode else None, res_mode=res_mode)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+    assert is_canary(buf[:, :, W:, :]) and is_canary(buf[:, :, :W, :32]) and is_canary(buf[:, :, :W, 32 + Co:])
