@@ -150,6 +150,16 @@ def profiled_traffic(profile_name, src_files):
 
 
 # ------------------------------------------------------------ workloads
+PATH_KERNELS = {1: ("cb::direct_tile_kernel / direct_conv_kernel", "hbm"), 2: ("cb::dw_tma_kernel", "hbm"),
+                3: ("cb::igemm_tf32_kernel", "tensor"), 4: ("cb::igemm_halo_kernel (pixel-major)", "tensor"),
+                5: ("cb::igemm_halo_kernel (channel-major)", "tensor"), 6: ("cb::pw_small_kernel", "hbm")}
+
+
+def kernel_of(binding, x, y, k, stride, pad, x_layout=0):
+    """(kernel name, roofline bound) of the path the library takes for this layer."""
+    return PATH_KERNELS.get(binding.conv_path(x, y, k, stride, pad, x_layout=x_layout), ("?", "hbm"))
+
+
 class Launch:
     def __init__(self, name, fn, work, kernel, bound):
         self.name, self.fn, self.work, self.kernel, self.bound = name, fn, work, kernel, bound
@@ -312,11 +322,9 @@ class DenseWorkload(Workload):
                    "y": torch.empty(batch, OH, OW, co, device=device), "L": L}
             self.layers.append(rec)
             name = f"{ci}-{co}@{H}_s{s}"
-            tc = ci % 4 == 0 and ci >= 16
+            kname, bound = kernel_of(cb, rec["x"], rec["y"], 3, s, 1)
             self.launches.append(Launch(name, (lambda r: lambda st: r["L"](r["x"], r["y"], stream=st))(rec),
-                                        workloads.conv_layer(batch, H, H, ci, co, 3, s, 1),
-                                        "cb::igemm_tf32_kernel" if tc else "cb::direct_conv_kernel",
-                                        "tensor" if tc else "hbm"))
+                                        workloads.conv_layer(batch, H, H, ci, co, 3, s, 1), kname, bound))
         self.config = {"workload": "dense 3x3 + BN + SiLU sweep, NHWC fp32 storage, TF32 tensor cores, batch 16",
                        "batch": batch, "l2": "warm (per-layer working sets 15-180 MB; steps run back to back)"}
 
@@ -417,12 +425,11 @@ class YoloWorkload(Workload):
                 ("cv3", (lambda L=L, B=B: lambda s: L["cv3"](B["cat"], B["out"], residual=B["x1"],
                                                              res_mode=cb.RES_POST_ACT, stream=s))()),
             ]
+            views = {"down": (x_in(), B["x1"]), "cv1": (B["x1"], a), "cv2": (a, b), "cv3": (B["cat"], B["out"])}
             for nm, fn in steps:
-                cin = L[nm].cin
-                tc = cin % 4 == 0 and cin >= (8 if L[nm].k == 1 else 16)
-                self.launches.append(Launch(f"s{i}.{nm}", fn, works[f"s{i}.{nm}"],
-                                            "cb::igemm_tf32_kernel" if tc else "cb::direct_conv_kernel",
-                                            "tensor" if tc else "hbm"))
+                xv, yv = views[nm]
+                kname, bound = kernel_of(cb, xv, yv, L[nm].k, L[nm].stride, L[nm].pad)
+                self.launches.append(Launch(f"s{i}.{nm}", fn, works[f"s{i}.{nm}"], kname, bound))
             prev = (lambda B=B: lambda: B["out"])()
         self.config = {"workload": "YOLO-style 20-conv chain (5 stages, concat via channel views, post-act "
                                    "residual), 640x640x3 fp32", "batch": batch,

@@ -21,13 +21,13 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_
 ACT_NONE, ACT_RELU, ACT_SILU = 0, 1, 2
 RES_NONE, RES_PRE_ACT, RES_POST_ACT = 0, 1, 2
 LAYOUT_NHWC, LAYOUT_NCHW = 0, 1
-PATH_DIRECT, PATH_DEPTHWISE, PATH_TC_IM2COL, PATH_TC_HALO, PATH_TC_HALO_CM = 1, 2, 3, 4, 5
+PATH_DIRECT, PATH_DEPTHWISE, PATH_TC_IM2COL, PATH_TC_HALO, PATH_TC_HALO_CM, PATH_POINTWISE = 1, 2, 3, 4, 5, 6
 
 EXPORTED = (
     "cb_fold_bn", "cb_repack_weights", "cb_conv_bn_act", "cb_dw_separable_block_workspace",
     "cb_dw_separable_block", "cb_avgpool_linear", "cb_preprocess_u8", "cb_preprocess_u8_three_pass",
     "cb_get_device_error", "cb_last_cuda_error", "cb_set_kernel_policy", "cb_status_string", "cb_version",
-    "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_conv_uses_tensor_cores",
+    "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_layer_uses_tensor_cores",
     "cb_dw_separable_block_static", "cb_conv_path",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
@@ -79,7 +79,7 @@ def load():
                 "cb_set_kernel_policy": [I],
                 "cb_get_kernel_policy": [],
                 "cb_round_weights_tf32": [P, LL, P],
-                "cb_conv_uses_tensor_cores": [T, I, I],
+                "cb_layer_uses_tensor_cores": [I, I, I, I, I],
                 "cb_conv_path": [T, T, I, I, I, I],
                 "cb_status_string": [I],
                 "cb_version": [],
@@ -163,9 +163,9 @@ def round_weights_tf32(w):
     return out
 
 
-def uses_tensor_cores(x, k, groups=1, x_layout=LAYOUT_NHWC) -> bool:
-    xv = nchw(x) if x_layout == LAYOUT_NCHW else nhwc(x)
-    return bool(load().cb_conv_uses_tensor_cores(ctypes.byref(xv), k, groups))
+def layer_uses_tensor_cores(ci, co, k, stride=1, groups=1) -> bool:
+    """cb_layer_uses_tensor_cores: the layer computes in TF32 on the tensor cores (round its weights)."""
+    return bool(load().cb_layer_uses_tensor_cores(ci, co, k, stride, groups))
 
 
 def conv_path(x, y, k, stride, pad, groups=1, x_layout=LAYOUT_NHWC) -> int:

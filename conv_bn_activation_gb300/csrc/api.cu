@@ -545,9 +545,24 @@ bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
   return true;
 }
 
+// A 1x1 stride-1 layer with at most 32 input and output channels: the
+// streaming CUDA-core kernel (the tensor cores do less useful work per cycle
+// at these widths, and the layer is HBM-bound).
+bool pointwise_shape(int ci, int co, int kh, int stride, int pad) {
+  return g_policy.load() != 1 && kh == 1 && stride == 1 && pad == 0 && pointwise_small_ok(ci, co);
+}
+
+// Shape rule of the tensor-core paths (views aside).
+bool tc_shape(int ci, int co, int kh, int stride, int pad) {
+  return g_policy.load() != 1 && ci % 4 == 0 && tc_channels_ok(ci, kh) && !pointwise_shape(ci, co, kh, stride, pad);
+}
+
 cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan) {
   const int policy = g_policy.load();
-  const bool tc_ok = policy != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && tc_channels_ok(x->c, kh) &&
+  if (pointwise_shape(x->c, y->c, kh, stride, pad) && x->layout == CB_LAYOUT_NHWC && aligned16(x->data) &&
+      strides_mult4(x) && aligned16(y->data) && strides_mult4(y))
+    return CB_PATH_POINTWISE;
+  const bool tc_ok = tc_shape(x->c, y->c, kh, stride, pad) && x->layout == CB_LAYOUT_NHWC &&
                      aligned16(x->data) && strides_mult4(x) && x->n <= 65535 && x->w <= 65535 &&
                      x->h <= 65535 && encode_tiled() && encode_im2col();
   if (!tc_ok) return CB_PATH_DIRECT;
@@ -618,6 +633,46 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   cudaError_t e = launch_igemm_halo(xmap, wmap, a, plan.px, plan.co, plan.cm, plan.grid, plan.smem, s);
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+cb_status run_direct(const cb_tensor* x, const float* w, const Epilogue& ep, int k, int stride, int pad,
+                     const cb_tensor* y, cudaStream_t s);
+
+bool pixel_flat(const cb_tensor* t) {
+  return t->stride_h == static_cast<long long>(t->w) * t->stride_w &&
+         t->stride_n == static_cast<long long>(t->h) * t->stride_h;
+}
+
+cb_status run_pointwise(const cb_tensor* x, const float* w, const Epilogue& ep, const cb_tensor* residual,
+                        const cb_tensor* y, cudaStream_t s) {
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  DirectArgs a{};
+  a.x = static_cast<const float*>(x->data);
+  a.xs_n = x->stride_n;
+  a.xs_h = x->stride_h;
+  a.xs_w = x->stride_w;
+  a.xs_c = 1;
+  a.w = w;
+  a.N = x->n;
+  a.H = x->h;
+  a.W = x->w;
+  a.Ci = x->c;
+  a.Co = y->c;
+  a.OH = y->h;
+  a.OW = y->w;
+  a.kh = a.kw = 1;
+  a.stride = 1;
+  a.pad = 0;
+  a.out = make_out(y);
+  a.ep = ep;
+  const bool flat = pixel_flat(x) && pixel_flat(y) && (ep.res_mode == 0 || pixel_flat(residual));
+  cudaError_t e = launch_pointwise_small(a, flat, dev->sms, s);
+  // a residual ring that does not fit in shared memory (4 input channels with
+  // 16 or more outputs): the direct kernel
+  if (e == cudaErrorInvalidValue) return run_direct(x, w, ep, 1, 1, 0, y, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
 
@@ -736,12 +791,19 @@ cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale,
     if (kh != 3 || x->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
     return run_depthwise(x, w, ep, stride, pad, y, s);
   }
-  if (!aligned16(w) && dense_path(x, y, kh, stride, pad, nullptr) != CB_PATH_DIRECT) {
+  HaloPlan plan;
+  const cb_path path = dense_path(x, y, kh, stride, pad, &plan);
+  if (path == CB_PATH_POINTWISE) {
+    // 16-byte weight, scale / bias and residual accesses, else the direct kernel
+    const bool vec = aligned16(w) && aligned16(scale) && aligned16(bias) &&
+                     (res_mode == CB_RES_NONE || (aligned16(residual->data) && strides_mult4(residual)));
+    return vec ? run_pointwise(x, w, ep, residual, y, s) : run_direct(x, w, ep, kh, stride, pad, y, s);
+  }
+  if (!aligned16(w) && path != CB_PATH_DIRECT) {
     // the tensor-core paths read w through TMA: an unaligned copy goes to the direct kernel
     return run_direct(x, w, ep, kh, stride, pad, y, s);
   }
-  HaloPlan plan;
-  switch (dense_path(x, y, kh, stride, pad, &plan)) {
+  switch (path) {
     case CB_PATH_TC_HALO:
     case CB_PATH_TC_HALO_CM: return run_igemm_halo(x, w, ep, plan, y, s);
     case CB_PATH_TC_IM2COL: return run_igemm(x, w, ep, kh, stride, pad, y, s);
@@ -956,12 +1018,9 @@ int cb_conv_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int
   return dense_path(x, y, kh, stride, pad, nullptr);
 }
 
-int cb_conv_uses_tensor_cores(const cb_tensor* x, int kh, int groups) {
-  if (!view_ok(x) || groups != 1 || (kh != 1 && kh != 3)) return 0;
-  return g_policy.load() != 1 && x->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 && tc_channels_ok(x->c, kh) &&
-                 aligned16(x->data) && strides_mult4(x)
-             ? 1
-             : 0;
+int cb_layer_uses_tensor_cores(int ci, int co, int kh, int stride, int groups) {
+  if (ci < 1 || co < 1 || groups != 1 || (kh != 1 && kh != 3) || (stride != 1 && stride != 2)) return 0;
+  return tc_shape(ci, co, kh, stride, kh / 2) ? 1 : 0;
 }
 
 }  // extern "C"

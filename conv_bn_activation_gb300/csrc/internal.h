@@ -62,6 +62,11 @@ struct DirectArgs {
   Epilogue ep;
 };
 cudaError_t launch_direct(const DirectArgs& a, cudaStream_t s);
+// 1x1 stride-1 layers with Ci, Co in {4, 8, 16, 32} (pointwise.cu): needs
+// NHWC views with 16-byte aligned pixels; flat = every view's pixels are
+// evenly spaced (stride_h = W * stride_w, stride_n = H * stride_h).
+bool pointwise_small_ok(int ci, int co);
+cudaError_t launch_pointwise_small(const DirectArgs& a, bool flat, int sms, cudaStream_t s);
 
 // ------------------------------------------------------- implicit GEMM (tcgen05)
 struct IgemmArgs {

@@ -1,0 +1,253 @@
+// 1x1 convolution + folded BN + activation (+ residual) for layers with at
+// most 32 input and output channels, on the fp32 CUDA cores ("YOLO26N
+// Inference Optimisation", the 1x1 C -> C/2 and C -> C convs of the stage
+// blocks; "How I sped up convolutions", the pointwise conv).
+//
+// At these widths the layer is HBM-bound (16 -> 16 moves 128 bytes per
+// pixel for 256 FMAs), and a tcgen05 MMA, whose issue costs at least ~111
+// cycles for a 128 x N x 8 step, does less useful work per cycle than the
+// CUDA cores.  So this kernel streams pixels (and their residual rows)
+// through a shared-memory ring of 16 KB tiles (cp.async, every thread
+// copying different bytes, several tiles in flight per CTA so that enough
+// bytes are in flight to cover HBM latency); then each thread computes
+// 4 pixels x 4 output channels from shared memory (register blocking: 64
+// FMAs per 8 shared loads) and stores each pixel's four channels as one
+// 16-byte store, so a warp's stores are whole pixel segments.  The weights
+// sit in shared memory as [ci][co/4] float4s.
+#include "epilogue.cuh"
+#include "internal.h"
+#include "launch_util.h"
+#include "ptx.cuh"
+
+namespace cb {
+
+namespace {
+
+__device__ __forceinline__ float comp(const float4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Four output channels of one pixel; the activation is picked once per pixel
+// (a uniform branch) so the four exponentials overlap.  SiLU uses the fast
+// exponential and division (relative error ~1e-6, inside this fp32 path's
+// 1e-5 bar).
+__device__ __forceinline__ float4 pw_epilogue(float4 acc, float4 sc, float4 bi, float4 r, int act, int res_mode) {
+  float z[4] = {fmaf(acc.x, sc.x, bi.x), fmaf(acc.y, sc.y, bi.y), fmaf(acc.z, sc.z, bi.z), fmaf(acc.w, sc.w, bi.w)};
+  const float rr[4] = {r.x, r.y, r.z, r.w};
+  if (res_mode == 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z[i] += rr[i];
+  if (act == 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z[i] = fmaxf(z[i], 0.0f);
+  } else if (act == 2) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z[i] = __fdividef(z[i], 1.0f + __expf(-z[i]));
+  }
+  if (res_mode == 2)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) z[i] += rr[i];
+  return make_float4(z[0], z[1], z[2], z[3]);
+}
+
+// 16-byte asynchronous global -> shared copy; src_bytes == 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+constexpr int kPwThreads = 256;
+constexpr int kPwU = 4;       // pixels per thread (register blocking)
+constexpr int kPwStages = 3;  // tiles in flight per CTA (ring depth)
+
+template <int CI, int CO>
+struct PwShape {
+  static constexpr int G = CO / 4;                                // channel groups of 4 outputs
+  static constexpr int kVec = CI / 4;                             // 16-byte input pieces per pixel
+  static constexpr int kPitch = kVec >= 4 ? kVec + 1 : kVec;      // staged input row, float4s (padded)
+  static constexpr int kRPitch = G >= 4 ? G + 1 : G;              // staged residual row, float4s
+  static constexpr int kTile = 4096 / CI;                         // pixels per tile (16 KB of input)
+  static constexpr int kGroups = kTile / kPwU;                    // pixel groups per tile
+  static constexpr int kItems = kGroups * G;                      // (pixel group, channel group) items
+  static constexpr int kXFloat4 = kTile * kPitch;
+  static constexpr int kRFloat4 = kTile * kRPitch;
+  static size_t smem_bytes(bool res) {
+    return 16 * (static_cast<size_t>(CI) * G + 2 * G +
+                 static_cast<size_t>(kPwStages) * (kXFloat4 + (res ? kRFloat4 : 0)));
+  }
+};
+
+// A ring of kPwStages tiles per CTA: a tile is kTile pixels whose CI inputs
+// are 16 KB (plus their residual rows when there is a residual), copied
+// with 16-byte cp.async by all threads (different bytes per thread).  The
+// staged rows of 64 bytes or more are padded by 16 bytes so that the
+// pixel-strided reads below hit distinct bank groups.  Each thread computes
+// 4 pixels x 4 output channels: per 4 input channels it reads 4 pixel
+// float4s and 4 weight float4s and does 64 FMAs.
+template <int CI, int CO>
+__global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a, int flat) {
+  static_assert(CI % 4 == 0 && CO % 4 == 0 && CI <= 32 && CO <= 32, "channel counts");
+  using Sh = PwShape<CI, CO>;
+  constexpr int G = Sh::G, kVec = Sh::kVec, kPitch = Sh::kPitch, kRPitch = Sh::kRPitch;
+  constexpr int kTile = Sh::kTile, kGroups = Sh::kGroups, kItems = Sh::kItems;
+  static_assert(kTile * kVec == 4 * kPwThreads && kPwThreads % G == 0, "tile shape");
+  extern __shared__ float4 pw_smem[];
+  const bool res = a.ep.res_mode != 0;
+  float4* ws = pw_smem;             // [CI][G]
+  float4* ssc = ws + CI * G;        // [G]
+  float4* sbi = ssc + G;            // [G]
+  float4* ring = sbi + G;           // kPwStages x (x tile, residual tile)
+  const int stage_f4 = Sh::kXFloat4 + (res ? Sh::kRFloat4 : 0);
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = threadIdx.x; i < CI * G; i += kPwThreads) {
+    const int ci = i / G, g = i - (i / G) * G;
+    const float* wp = a.w + (4 * g) * CI + ci;  // [co][ci]
+    ws[i] = make_float4(__ldg(wp), __ldg(wp + CI), __ldg(wp + 2 * CI), __ldg(wp + 3 * CI));
+  }
+  for (int g = threadIdx.x; g < G; g += kPwThreads) {
+    ssc[g] = ldg4(a.ep.scale + 4 * g);
+    sbi[g] = ldg4(a.ep.bias + 4 * g);
+  }
+
+  const long long HW = static_cast<long long>(a.H) * a.W;
+  const long long M = a.N * HW;
+  const long long num_tiles = (M + kTile - 1) / kTile;
+  auto pixel_off = [&](long long p, long long sn, long long sh, long long sw) -> long long {
+    if (flat) return p * sw;
+    const long long n = p / HW;
+    const long long rem = p - n * HW;
+    const long long h = rem / a.W;
+    return n * sn + h * sh + (rem - h * a.W) * sw;
+  };
+  auto stage = [&](long long tile, int slot) {
+    float4* xs = ring + slot * stage_f4;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int piece = threadIdx.x + k * kPwThreads;
+      const int lp = piece / kVec, lj = piece - (piece / kVec) * kVec;
+      const long long p = tile * kTile + lp;
+      const bool in = p < M;
+      const float* src = in ? a.x + pixel_off(p, a.xs_n, a.xs_h, a.xs_w) + 4 * lj : a.x;
+      cp_async16(&xs[lp * kPitch + lj], src, in ? 16 : 0);
+    }
+    if (res) {
+      float4* rs = xs + Sh::kXFloat4;
+      for (int piece = threadIdx.x; piece < kTile * G; piece += kPwThreads) {
+        const int lp = piece / G, lg = piece - (piece / G) * G;
+        const long long p = tile * kTile + lp;
+        const bool in = p < M;
+        const float* src = in ? a.ep.r + pixel_off(p, a.ep.rs_n, a.ep.rs_h, a.ep.rs_w) + 4 * lg : a.x;
+        cp_async16(&rs[lp * kRPitch + lg], src, in ? 16 : 0);
+      }
+    }
+  };
+
+  // prologue: the first kPwStages - 1 tiles of this CTA in flight
+  long long tile = blockIdx.x;
+#pragma unroll
+  for (int k = 0; k < kPwStages - 1; ++k) {
+    const long long t = tile + static_cast<long long>(k) * gridDim.x;
+    if (t < num_tiles) stage(t, k);
+    cp_async_commit();
+  }
+  __syncthreads();  // weights and constants visible
+  for (int it = 0; tile < num_tiles; tile += gridDim.x, ++it) {
+    const int slot = it % kPwStages;
+    const long long ahead = tile + static_cast<long long>(kPwStages - 1) * gridDim.x;
+    if (ahead < num_tiles) stage(ahead, (it + kPwStages - 1) % kPwStages);
+    cp_async_commit();
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPwStages - 1) : "memory");  // this tile has landed
+    __syncthreads();
+    const float4* xs = ring + slot * stage_f4;
+    const float4* rs = xs + Sh::kXFloat4;
+#pragma unroll
+    for (int item = threadIdx.x; item < kItems; item += kPwThreads) {
+      const int pg = item / G, g = item - (item / G) * G;  // pixels pg + u * kGroups
+      float4 acc[kPwU];
+#pragma unroll
+      for (int u = 0; u < kPwU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c4 = 0; c4 < kVec; ++c4) {
+        float4 xv[kPwU];
+#pragma unroll
+        for (int u = 0; u < kPwU; ++u) xv[u] = xs[(pg + u * kGroups) * kPitch + c4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 w4 = ws[(4 * c4 + e) * G + g];
+#pragma unroll
+          for (int u = 0; u < kPwU; ++u) {
+            const float xsv = comp(xv[u], e);
+            acc[u].x = fmaf(xsv, w4.x, acc[u].x);
+            acc[u].y = fmaf(xsv, w4.y, acc[u].y);
+            acc[u].z = fmaf(xsv, w4.z, acc[u].z);
+            acc[u].w = fmaf(xsv, w4.w, acc[u].w);
+          }
+        }
+      }
+      const float4 sc = ssc[g], bi = sbi[g];
+#pragma unroll
+      for (int u = 0; u < kPwU; ++u) {
+        const int lp = pg + u * kGroups;
+        const long long p = tile * kTile + lp;
+        if (p >= M) continue;
+        const float4 r = res ? rs[lp * kRPitch + g] : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(a.out.y + pixel_off(p, a.out.ys_n, a.out.ys_h, a.out.ys_w) + 4 * g) =
+            pw_epilogue(acc[u], sc, bi, r, a.ep.act, a.ep.res_mode);
+      }
+    }
+    __syncthreads();  // a later iteration's copies overwrite this slot
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+template <int CI, int CO>
+cudaError_t pw_launch(const DirectArgs& a, int flat, int sms, cudaStream_t s) {
+  using Sh = PwShape<CI, CO>;
+  const size_t smem = Sh::smem_bytes(a.ep.res_mode != 0);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e = smem_attr_once<pw_small_kernel<CI, CO>>(smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pw_small_kernel<CI, CO>, kPwThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const long long M = static_cast<long long>(a.N) * a.H * a.W;
+  const long long tiles = (M + Sh::kTile - 1) / Sh::kTile;
+  const long long cap = static_cast<long long>(sms) * per_sm;
+  const unsigned blocks = static_cast<unsigned>(tiles < cap ? tiles : cap);
+  return launch_pdl(pw_small_kernel<CI, CO>, dim3(blocks), dim3(kPwThreads), smem, s, a, flat);
+}
+
+template <int CI>
+cudaError_t pw_launch_co(const DirectArgs& a, int flat, int sms, cudaStream_t s) {
+  switch (a.Co) {
+    case 4: return pw_launch<CI, 4>(a, flat, sms, s);
+    case 8: return pw_launch<CI, 8>(a, flat, sms, s);
+    case 16: return pw_launch<CI, 16>(a, flat, sms, s);
+    case 32: return pw_launch<CI, 32>(a, flat, sms, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+bool pointwise_small_ok(int ci, int co) {
+  return (ci == 4 || ci == 8 || ci == 16 || ci == 32) && (co == 4 || co == 8 || co == 16 || co == 32);
+}
+
+cudaError_t launch_pointwise_small(const DirectArgs& a, bool flat, int sms, cudaStream_t s) {
+  if (static_cast<long long>(a.N) * a.H * a.W == 0) return cudaSuccess;
+  const int f = flat ? 1 : 0;
+  switch (a.Ci) {
+    case 4: return pw_launch_co<4>(a, f, sms, s);
+    case 8: return pw_launch_co<8>(a, f, sms, s);
+    case 16: return pw_launch_co<16>(a, f, sms, s);
+    case 32: return pw_launch_co<32>(a, f, sms, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace cb

@@ -34,17 +34,15 @@ class ConvBnAct:
     """One fused layer with folded BN and repacked weights on the device.
 
     tc_weights: round the dense weights to the nearest TF32 value
-    (cb_round_weights_tf32) for the tensor-core path; None decides from the
-    shape rule of that path (groups 1, Cin % 4 == 0, Cin >= 8 for 1x1 and >= 16 for 3x3) and the
-    current kernel policy.
+    (cb_round_weights_tf32) for the tensor-core path; None asks the library
+    (cb_layer_uses_tensor_cores) under the current kernel policy.
     """
 
     def __init__(self, w_oihw, bn, stride, pad, act, groups=1, device="cuda", eps=1e-5, tc_weights=None):
         scale, bias = cb.fold_bn(*bn, eps=eps)
         cin = w_oihw.shape[1] * groups
         if tc_weights is None:
-            tc_weights = (groups == 1 and cin % 4 == 0 and cin >= (8 if w_oihw.shape[2] == 1 else 16) and w_oihw.shape[2] in (1, 3)
-                          and cb.get_kernel_policy() != 1)
+            tc_weights = cb.layer_uses_tensor_cores(cin, w_oihw.shape[0], w_oihw.shape[2], stride, groups)
         w = cb.repack_weights(w_oihw, groups)
         if tc_weights:
             w = cb.round_weights_tf32(w)
@@ -71,8 +69,10 @@ class DwBlock:
         self.cin, self.cout, self.stride = cin, cout, stride
         dws, dwb = cb.fold_bn(*p["bn1"])
         pws, pwb = cb.fold_bn(*p["bn2"])
-        tc = cin % 4 == 0 and cin >= 8 and cb.get_kernel_policy() != 1
-        dense = cb.round_weights_tf32 if tc else (lambda a: a)
+        pw_tc = cb.layer_uses_tensor_cores(cin, cout, 1, 1)
+        skip_tc = cb.layer_uses_tensor_cores(cin, cout, 1, stride)
+        dense = cb.round_weights_tf32 if pw_tc else (lambda a: a)
+        dense_skip = cb.round_weights_tf32 if skip_tc else (lambda a: a)
         self.params = {
             "dw_w": _dev(cb.repack_weights(p["dw_w"], groups=cin), device),
             "dw_scale": _dev(dws, device), "dw_bias": _dev(dwb, device),
@@ -81,7 +81,7 @@ class DwBlock:
         }
         if "skip_w" in p:
             sks, skb = cb.fold_bn(*p["skip_bn"])
-            self.params.update({"skip_w": _dev(dense(cb.repack_weights(p["skip_w"])), device),
+            self.params.update({"skip_w": _dev(dense_skip(cb.repack_weights(p["skip_w"])), device),
                                 "skip_scale": _dev(sks, device), "skip_bias": _dev(skb, device)})
 
     def __call__(self, x, y, workspace, stream=None):

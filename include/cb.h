@@ -103,7 +103,7 @@ cb_status cb_repack_weights(const float* w_oihw, int Co, int Ci_per_group, int k
  * The tensor cores read fp32 operands by truncating them to TF32, which
  * shrinks every product toward zero; weights rounded once at load time
  * enter the MMA exactly and carry an unbiased error instead.  Use it for
- * layers that run on the tensor-core path (cb_conv_uses_tensor_cores).
+ * layers that run on the tensor-core path (cb_layer_uses_tensor_cores).
  */
 cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
 
@@ -123,7 +123,9 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
  * TF32 value; needs 16-byte aligned x/w and strides that are multiples of 4
  * elements).  Among those, 3x3 stride-1 pad-1 layers with Ci % 32 == 0 and
  * W <= 254 take one shared-memory halo tile per 32-channel chunk for all
- * nine taps; the others gather one im2col tile per tap;
+ * nine taps; the others gather one im2col tile per tap.  1x1 stride-1
+ * layers with Ci and Co in {4, 8, 16, 32} run instead on a streaming fp32
+ * CUDA-core kernel (HBM-bound at these widths);
  * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;
  * everything else (stems with 1 or 3 input channels, NCHW input, odd channel
  * counts) runs on a direct CUDA-core kernel in fp32.
@@ -250,12 +252,15 @@ cb_status cb_set_kernel_policy(int policy);
 int cb_get_kernel_policy(void);
 
 /*
- * 1 if cb_conv_bn_act with input view x, a kh x kh kernel and `groups` would
- * run on the tensor-core implicit GEMM under the current policy, else 0.
- * Tensor-core layers compute with TF32 inputs and store outputs rounded to
- * the nearest TF32 value; the other paths are fp32 throughout.
+ * 1 if a dense layer with ci input and co output channels, a kh x kh kernel,
+ * this stride and `groups` runs on the tensor cores under the current
+ * policy (for NHWC views with 16-byte aligned data and strides that are
+ * multiples of 4 elements), else 0.  Tensor-core layers compute with TF32
+ * inputs and store outputs rounded to the nearest TF32 value, so their
+ * weights should go through cb_round_weights_tf32; the other paths are fp32
+ * throughout.  Host only.
  */
-int cb_conv_uses_tensor_cores(const cb_tensor* x, int kh, int groups);
+int cb_layer_uses_tensor_cores(int ci, int co, int kh, int stride, int groups);
 
 /* Kernels behind cb_conv_bn_act (see cb_conv_path). */
 typedef enum {
@@ -264,7 +269,8 @@ typedef enum {
   CB_PATH_TC_IM2COL = 3,  /* tensor-core implicit GEMM, one im2col tile per filter tap */
   CB_PATH_TC_HALO = 4,    /* tensor-core implicit GEMM, one halo tile per 32-channel chunk (3x3, stride 1),
                              128 pixels x up to 256 channels per tile */
-  CB_PATH_TC_HALO_CM = 5  /* the same with 256 pixels x 128 channels per tile, channels as the MMA's M */
+  CB_PATH_TC_HALO_CM = 5, /* the same with 256 pixels x 128 channels per tile, channels as the MMA's M */
+  CB_PATH_POINTWISE = 6   /* streaming fp32 CUDA-core 1x1 kernel for at most 32 input and output channels */
 } cb_path;
 
 /*

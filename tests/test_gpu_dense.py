@@ -28,8 +28,8 @@ DENSE = [
 ]
 
 
-def _is_tc(cin, k=3):
-    return cin % 4 == 0 and cin >= (8 if k == 1 else 16)
+def _is_tc(cin, cout, k=3, stride=1):
+    return cb.layer_uses_tensor_cores(cin, cout, k, stride)
 
 
 @pytest.fixture(params=[0, 1, 2], ids=["auto", "direct", "im2col"])
@@ -50,7 +50,7 @@ def test_dense_silu(gpu, policy, orc, case):
     layer(to_dev(x), y)
     sync_check()
     ref = orc.conv_bn_act(x, w, bn, stride=s, pad=pad, act=orc.ACT_SILU)
-    tol = TOL_TF32 if (policy != 1 and _is_tc(Ci, k)) else TOL_FP32
+    tol = TOL_TF32 if _is_tc(Ci, Co, k, s) else TOL_FP32
     assert rel_err(y.cpu().numpy(), ref) <= tol
 
 
@@ -66,7 +66,7 @@ def test_dense_epilogue_variants(gpu, policy, orc, act, res_mode, k):
     sync_check()
     ref = orc.conv_bn_act(x, w, bn, stride=1, pad=k // 2, act=act, residual=r if res_mode else None,
                           res_mode=res_mode)
-    assert rel_err(y.cpu().numpy(), ref) <= (TOL_TF32 if policy != 1 else TOL_FP32)
+    assert rel_err(y.cpu().numpy(), ref) <= (TOL_TF32 if _is_tc(Ci, Co, k) else TOL_FP32)
 
 
 @pytest.mark.parametrize("stem", [(1, 48, 28, 1), (3, 16, 64, 2), (3, 16, 33, 2), (8, 8, 20, 1)])
@@ -120,7 +120,7 @@ def test_dense_sweep_batch1_full(gpu, orc, case):
     layer(to_dev(x), y)
     sync_check()
     ref = orc.conv_bn_act(x, w, bn, stride=s, pad=1, act=orc.ACT_SILU)
-    assert rel_err(y.cpu().numpy(), ref) <= (TOL_TF32 if _is_tc(Ci) else TOL_FP32)
+    assert rel_err(y.cpu().numpy(), ref) <= (TOL_TF32 if _is_tc(Ci, Co, 3, s) else TOL_FP32)
 
 
 @pytest.mark.parametrize("case", synthetic.DENSE_SWEEP, ids=lambda s: "%d-%d@%d_s%d" % s)
@@ -136,4 +136,4 @@ def test_dense_sweep_batch16_sampled(gpu, orc, case):
     idx = np.concatenate([idx, [y.numel() - 1]])
     ref = orc.conv_bn_act_points(x, w, bn, idx, stride=s, pad=1, act=orc.ACT_SILU)
     got = y.reshape(-1)[torch.from_numpy(idx).to(gpu)].cpu().numpy()
-    assert rel_err(got, ref) <= (TOL_TF32 if _is_tc(Ci) else TOL_FP32)
+    assert rel_err(got, ref) <= (TOL_TF32 if _is_tc(Ci, Co, 3, s) else TOL_FP32)
