@@ -925,7 +925,7 @@ static cb_status check_preprocess(const unsigned char* src, int n, int src_h, in
                                   const float* dst, int dst_h, int dst_w) {
   if (!src || !dst || n < 0 || src_h < 1 || src_w < 1 || dst_h < 1 || dst_w < 1) return CB_ERR_INVALID_ARG;
   if (src_pitch < 3LL * src_w) return CB_ERR_INVALID_ARG;
-  if (2LL * ((3LL * src_w + 15) & ~15LL) > 200 * 1024) return CB_ERR_UNSUPPORTED;
+  if (8LL * ((3LL * src_w + 15) & ~15LL) > 224 * 1024) return CB_ERR_UNSUPPORTED;  // two buffers of four rows
   if (dst_h > 65535 || n > 65535) return CB_ERR_UNSUPPORTED;
   return CB_OK;
 }
@@ -934,7 +934,10 @@ cb_status cb_preprocess_u8(const unsigned char* src, int n, int src_h, int src_w
                            int dst_h, int dst_w, void* stream) {
   cb_status st = check_preprocess(src, n, src_h, src_w, src_pitch, dst, dst_h, dst_w);
   if (st != CB_OK) return st;
-  cudaError_t e = launch_preprocess_fused(src, n, src_h, src_w, src_pitch, dst, dst_h, dst_w,
+  DeviceInfo* dev = nullptr;
+  st = current_device(&dev);
+  if (st != CB_OK) return st;
+  cudaError_t e = launch_preprocess_fused(src, n, src_h, src_w, src_pitch, dst, dst_h, dst_w, dev->sms,
                                           static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }

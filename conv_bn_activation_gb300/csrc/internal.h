@@ -126,7 +126,7 @@ cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, 
 
 // -------------------------------------------------------------- preprocess
 cudaError_t launch_preprocess_fused(const uint8_t* src, int n, int hs, int ws, long long pitch, float* dst,
-                                    int hd, int wd, cudaStream_t s);
+                                    int hd, int wd, int sms, cudaStream_t s);
 cudaError_t launch_preprocess_resize(const uint8_t* src, int n, int hs, int ws, long long pitch,
                                      uint8_t* out, int hd, int wd, cudaStream_t s);
 cudaError_t launch_preprocess_normalize(const uint8_t* in, long long count, float* out, cudaStream_t s);

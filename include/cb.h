@@ -213,6 +213,8 @@ cb_status cb_avgpool_linear(const cb_tensor* x, const float* fc_w, const float* 
  * (>= 3 * src_w), frame pitch src_h * src_pitch; dst: DEVICE fp32
  * [n, 3, dst_h, dst_w] contiguous.  Coordinates and the bilinear value are
  * evaluated in IEEE fp32 in the order written above (no fused multiply-add).
+ * Source rows up to 9557 pixels wide (eight staged rows fit in shared
+ * memory), dst_h and n up to 65535: else CB_ERR_UNSUPPORTED.
  */
 cb_status cb_preprocess_u8(const unsigned char* src, int n, int src_h, int src_w, long long src_pitch,
                            float* dst, int dst_h, int dst_w, void* stream);

@@ -14,7 +14,9 @@ from gpu_util import sync_check, to_dev
 pytestmark = pytest.mark.gpu
 
 SIZES = [(720, 1280, 480, 640), (13, 17, 7, 9), (100, 37, 41, 100), (64, 64, 64, 64), (9, 5, 31, 33),
-         (480, 640, 480, 640), (1, 1, 3, 4), (5, 1000, 3, 333)]
+         (480, 640, 480, 640), (1, 1, 3, 4), (5, 1000, 3, 333),
+         # exact 2:1 widths (the pair-sum path) with odd, equal, upscaled and downscaled heights
+         (15, 64, 7, 32), (8, 40, 20, 20), (31, 80, 31, 40), (9, 16, 2, 8), (2, 24, 5, 12)]
 
 
 @pytest.mark.parametrize("size", SIZES, ids=lambda s: "%dx%d-%dx%d" % s)
