@@ -698,7 +698,10 @@ cb_status run_direct(const cb_tensor* x, const float* w, const Epilogue& ep, int
   a.pad = pad;
   a.out = make_out(y);
   a.ep = ep;
-  cudaError_t e = launch_direct(a, s);
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  cudaError_t e = launch_direct(a, dev->sms, s);
   if (e == cudaErrorInvalidValue) return CB_ERR_UNSUPPORTED;
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }

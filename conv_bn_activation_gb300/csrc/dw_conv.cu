@@ -123,7 +123,7 @@ __device__ __forceinline__ float epi_c(float acc, float sc, float bi, float r) {
   float z = fmaf(acc, sc, bi);
   if (RES == 1) z += r;
   if (ACT == 1) z = fmaxf(z, 0.0f);
-  if (ACT == 2) z = z / (1.0f + expf(-z));
+  if (ACT == 2) z = silu(z);
   if (RES == 2) z += r;
   return z;
 }

@@ -61,7 +61,7 @@ struct DirectArgs {
   OutView out;
   Epilogue ep;
 };
-cudaError_t launch_direct(const DirectArgs& a, cudaStream_t s);
+cudaError_t launch_direct(const DirectArgs& a, int sms, cudaStream_t s);
 // 1x1 stride-1 layers with Ci, Co in {4, 8, 16, 32} (pointwise.cu): needs
 // NHWC views with 16-byte aligned pixels; flat = every view's pixels are
 // evenly spaced (stride_h = W * stride_w, stride_n = H * stride_h).
