@@ -28,7 +28,7 @@ EXPORTED = (
     "cb_dw_separable_block", "cb_avgpool_linear", "cb_preprocess_u8", "cb_preprocess_u8_three_pass",
     "cb_get_device_error", "cb_last_cuda_error", "cb_set_kernel_policy", "cb_status_string", "cb_version",
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_layer_uses_tensor_cores",
-    "cb_dw_separable_block_static", "cb_conv_path",
+    "cb_dw_separable_block_static", "cb_conv_path", "cb_debug_timeout_probe",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
@@ -81,6 +81,7 @@ def load():
                 "cb_round_weights_tf32": [P, LL, P],
                 "cb_layer_uses_tensor_cores": [I, I, I, I, I],
                 "cb_conv_path": [T, T, I, I, I, I],
+                "cb_debug_timeout_probe": [I, P],
                 "cb_status_string": [I],
                 "cb_version": [],
             }
@@ -259,6 +260,11 @@ def preprocess_u8_three_pass(src, tmp_u8, tmp_f32, dst, stream=None):
                                               tmp_f32.data_ptr(), dst.data_ptr(), Hd, Wd, _stream_ptr(stream)),
            "cb_preprocess_u8_three_pass")
     return dst
+
+
+def debug_timeout_probe(timeout_ms, stream=None):
+    """cb_debug_timeout_probe: a bounded wait that nothing satisfies (tests the timeout report)."""
+    _check(load().cb_debug_timeout_probe(int(timeout_ms), _stream_ptr(stream)), "cb_debug_timeout_probe")
 
 
 def get_device_error(stream=None) -> int:

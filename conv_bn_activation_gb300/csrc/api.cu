@@ -976,6 +976,16 @@ cb_status cb_get_device_error(void* stream) {
   return CB_OK;
 }
 
+cb_status cb_debug_timeout_probe(int timeout_ms, void* stream) {
+  if (timeout_ms < 1 || timeout_ms > 10000) return CB_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  cudaError_t e = launch_timeout_probe(dev->err, static_cast<uint64_t>(timeout_ms) * 1000000ull,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
 int cb_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char* cb_status_string(cb_status s) {

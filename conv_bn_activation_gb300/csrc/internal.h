@@ -132,6 +132,9 @@ cudaError_t launch_preprocess_resize(const uint8_t* src, int n, int hs, int ws, 
 cudaError_t launch_preprocess_normalize(const uint8_t* in, long long count, float* out, cudaStream_t s);
 cudaError_t launch_preprocess_layout(const float* in, int n, int h, int w, float* out, cudaStream_t s);
 
+// ------------------------------------------------------------ watchdog hook
+cudaError_t launch_timeout_probe(int* err, uint64_t limit_ns, cudaStream_t s);
+
 // ----------------------------------------------------------------- pool + fc
 struct PoolFcArgs {
   const float* x;

@@ -236,6 +236,17 @@ cb_status cb_preprocess_u8_three_pass(const unsigned char* src, int n, int src_h
  */
 cb_status cb_get_device_error(void* stream);
 
+/*
+ * Test hook for the failure path of the bounded waits (no counterpart on the
+ * pages): launches on `stream` one CTA that waits, with the same bounded
+ * mbarrier wait every pipeline kernel uses, on a barrier nothing ever
+ * arrives on, giving up after timeout_ms (1..10000).  The next
+ * cb_get_device_error on that stream then returns CB_ERR_TIMEOUT (and clears
+ * it); nothing hangs or faults and the context stays usable.  Returns
+ * CB_ERR_INVALID_ARG for an out-of-range timeout, else the launch status.
+ */
+cb_status cb_debug_timeout_probe(int timeout_ms, void* stream);
+
 /* The cudaError_t (as int) of the last CB_ERR_CUDA returned on this thread. */
 int cb_last_cuda_error(void);
 
