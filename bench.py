@@ -469,6 +469,7 @@ class YoloWorkload(Workload):
 class PreprocessWorkload(Workload):
     unit = "GB/s"
     dominant = "preprocess_fused"
+    profile = ("preprocess_pair_kernel_32x1280x720.md", ["preprocess.cu", "ptx.cuh", "launch_util.h"])
 
     def __init__(self, torch, device, batch=32):
         from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
@@ -484,10 +485,10 @@ class PreprocessWorkload(Workload):
         stem = workloads.conv_layer(batch, 480, 640, 3, 16, 3, 2, 1)
         self.launches = [
             Launch("preprocess_fused", lambda s: cb.preprocess_u8(self.frames, self.net.planar, stream=s), pre,
-                   "cb::preprocess_row_kernel<false>", "hbm"),
+                   "cb::preprocess_pair_kernel", "hbm"),
             Launch("stem_conv", lambda s: self.net.stem(self.net.planar, self.net.out, stream=s,
                                                         x_layout=cb.LAYOUT_NCHW), stem,
-                   "cb::direct_conv_kernel<16>", "hbm"),
+                   "cb::direct_tile_kernel<2,3,16,2,3>", "hbm"),
         ]
         self.three_pass = workloads.preprocess_unfused(batch, 720, 1280, 480, 640)
         self.config = {"workload": "fused u8 preprocess 1280x720 -> 640x480 NCHW fp32 + stem conv3x3 s2 3->16 "
