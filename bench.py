@@ -38,6 +38,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fused conv+BN+act: achieved GB/s or TFLOP/s vs roofline; images/sec"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+AUTOTUNE = True  # measure the tile plans of tensor-core layers at setup (cb_autotune_conv)
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rates
 UNIT_SCALE = {"GB/s": 1e9, "TFLOP/s": 1e12, "images/s": 1.0}
 
@@ -331,13 +332,16 @@ class DenseWorkload(Workload):
             OH, OW = L.out_hw(H, H)
             rec = {"x_host": x, "w": w, "bn": bn, "s": s, "x": _t(torch, x, device),
                    "y": torch.empty(batch, OH, OW, co, device=device), "L": L}
+            if AUTOTUNE:
+                L.autotune(rec["x"], rec["y"])
             self.layers.append(rec)
             name = f"{ci}-{co}@{H}_s{s}"
             kname, bound = kernel_of(cb, rec["x"], rec["y"], 3, s, 1)
             self.launches.append(Launch(name, (lambda r: lambda st: r["L"](r["x"], r["y"], stream=st))(rec),
                                         workloads.conv_layer(batch, H, H, ci, co, 3, s, 1), kname, bound))
         self.config = {"workload": "dense 3x3 + BN + SiLU sweep, NHWC fp32 storage, TF32 tensor cores, batch 16",
-                       "batch": batch, "l2": "warm (per-layer working sets 15-180 MB; steps run back to back)"}
+                       "batch": batch, "l2": "warm (per-layer working sets 15-180 MB; steps run back to back)",
+                       "autotune": AUTOTUNE}
 
     def e2e_setup(self):
         t = self.torch
@@ -422,6 +426,8 @@ class YoloWorkload(Workload):
         self.x_host = synthetic.yolo_input(batch)
         self.x = _t(torch, self.x_host, device)
         self.chain = YoloChain(self.stages, batch, device=device)
+        if AUTOTUNE:
+            self.chain.forward(self.x, tune=True)
         works = dict(workloads.yolo_layers(N=batch))
         self.launches = []
         prev = lambda: self.x
@@ -444,7 +450,8 @@ class YoloWorkload(Workload):
             prev = (lambda B=B: lambda: B["out"])()
         self.config = {"workload": "YOLO-style 20-conv chain (5 stages, concat via channel views, post-act "
                                    "residual), 640x640x3 fp32", "batch": batch,
-                       "l2": "inputs_larger_than_l2 (157 MB input, 1.2 GB of activations per step)"}
+                       "l2": "inputs_larger_than_l2 (157 MB input, 1.2 GB of activations per step)",
+                       "autotune": AUTOTUNE}
 
     def e2e_setup(self):
         self.x_pin = self.torch.from_numpy(self.x_host).pin_memory()
@@ -550,6 +557,8 @@ def run_ours(args):
     binding.load()
     peaks = load_peaks()
 
+    global AUTOTUNE
+    AUTOTUNE = not args.no_autotune
     wl = WORKLOADS[args.workload](torch, device, **({"batch": args.batch} if args.batch else {}))
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
@@ -732,6 +741,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of one captured graph")
     ap.add_argument("--launch-reps", type=int, default=20, help="back-to-back repetitions per kernel timing")
+    ap.add_argument("--no-autotune", action="store_true",
+                    help="dense / yolo: keep the built-in tile cost model instead of measuring plans at setup")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

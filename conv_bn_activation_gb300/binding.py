@@ -28,7 +28,8 @@ EXPORTED = (
     "cb_dw_separable_block", "cb_avgpool_linear", "cb_preprocess_u8", "cb_preprocess_u8_three_pass",
     "cb_get_device_error", "cb_last_cuda_error", "cb_set_kernel_policy", "cb_status_string", "cb_version",
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_layer_uses_tensor_cores",
-    "cb_dw_separable_block_static", "cb_conv_path", "cb_debug_timeout_probe",
+    "cb_dw_separable_block_static", "cb_conv_path", "cb_debug_timeout_probe", "cb_autotune_conv",
+    "cb_autotune_clear", "cb_autotune_entries",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
@@ -82,6 +83,9 @@ def load():
                 "cb_layer_uses_tensor_cores": [I, I, I, I, I],
                 "cb_conv_path": [T, T, I, I, I, I],
                 "cb_debug_timeout_probe": [I, P],
+                "cb_autotune_conv": [T, P, P, P, I, I, I, I, I, I, T, I, T, P],
+                "cb_autotune_clear": [],
+                "cb_autotune_entries": [],
                 "cb_status_string": [I],
                 "cb_version": [],
             }
@@ -194,6 +198,28 @@ def conv_bn_act(x, w, scale, bias, k, stride, pad, groups, act, y, residual=None
                                ctypes.byref(yv), _stream_ptr(stream))
     _check(st, "cb_conv_bn_act")
     return y
+
+
+def autotune_conv(x, w, scale, bias, k, stride, pad, groups, act, y, residual=None, res_mode=RES_NONE,
+                  stream=None, x_layout=LAYOUT_NHWC):
+    """cb_autotune_conv: time the layer's tile plans on these buffers, keep the fastest for the
+    shape; y holds the result.  Synchronises the stream (not inside graph capture)."""
+    xv = nchw(x) if x_layout == LAYOUT_NCHW else nhwc(x)
+    yv = nhwc(y)
+    rv = nhwc(residual) if residual is not None else None
+    st = load().cb_autotune_conv(ctypes.byref(xv), w.data_ptr(), scale.data_ptr(), bias.data_ptr(), k, k, stride,
+                                 pad, groups, act, ctypes.byref(rv) if rv is not None else None, res_mode,
+                                 ctypes.byref(yv), _stream_ptr(stream))
+    _check(st, "cb_autotune_conv")
+    return y
+
+
+def autotune_clear():
+    load().cb_autotune_clear()
+
+
+def autotune_entries() -> int:
+    return load().cb_autotune_entries()
 
 
 def dw_separable_block_workspace(x, c_out, stride) -> int:

@@ -14,6 +14,7 @@
 #include <mutex>
 #include <string>
 #include <unordered_map>
+#include <vector>
 
 #include "cb.h"
 #include "internal.h"
@@ -367,11 +368,58 @@ struct HaloPlan {
   int nb = 0, grid = 0;
   size_t smem = 0;
 };
+struct ImPlan {        // im2col kernel choices (0 = the cost model's)
+  int bn = 0, stages = 0;
+};
 bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out);
 
+// ------------------------------------------------------------ autotuner
+// Plans measured by cb_autotune_conv, per layer shape (and device, policy):
+// they override the cost models for that shape.  The tuner only chooses
+// among kernels of the path's own arithmetic class (tensor-core variants for
+// a tensor-core layer), so cb_layer_uses_tensor_cores stays true.
+struct ConvPlan {
+  cb_path path = CB_PATH_DIRECT;
+  HaloPlan halo;
+  ImPlan im;
+};
+struct ConvKey {
+  int dev, policy, n, h, w, ci, co, kh, stride, pad;
+  bool operator==(const ConvKey& o) const { return std::memcmp(this, &o, sizeof(ConvKey)) == 0; }
+};
+struct ConvKeyHash {
+  size_t operator()(const ConvKey& k) const {
+    uint64_t h = 1469598103934665603ull;
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+    for (size_t i = 0; i < sizeof(ConvKey); ++i) h = (h ^ p[i]) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+std::mutex g_tune_mu;
+std::unordered_map<ConvKey, ConvPlan, ConvKeyHash> g_tuned;
+
+ConvKey conv_key(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad) {
+  ConvKey k;
+  std::memset(&k, 0, sizeof(k));
+  cudaGetDevice(&k.dev);
+  k.policy = g_policy.load();
+  k.n = x->n, k.h = x->h, k.w = x->w, k.ci = x->c, k.co = y->c, k.kh = kh, k.stride = stride, k.pad = pad;
+  return k;
+}
+
+bool tuned_plan(const ConvKey& k, ConvPlan* out) {
+  std::lock_guard<std::mutex> lock(g_tune_mu);
+  auto it = g_tuned.find(k);
+  if (it == g_tuned.end()) return false;
+  *out = it->second;
+  return true;
+}
+
 // Kernel for a dense (groups 1) layer under the current policy; fills
-// *plan for the halo kernel.
-cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan);
+// *plan for the halo kernel and *im for the im2col kernel (a measured plan
+// for the shape, when the tuner made one, else the cost models').
+cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan,
+                   ImPlan* im = nullptr);
 
 int pick_bn(int M, int Cout, int k_iters, int sms, int* n_tiles_out) {
   static const int kBn[] = {16, 32, 48, 64, 96, 128, 192, 256};
@@ -398,7 +446,7 @@ int pick_bn(int M, int Cout, int k_iters, int sms, int* n_tiles_out) {
 }
 
 cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int k, int stride, int pad,
-                    const cb_tensor* y, cudaStream_t s) {
+                    const cb_tensor* y, cudaStream_t s, const ImPlan& im = ImPlan{}) {
   DeviceInfo* dev = nullptr;
   cb_status st = current_device(&dev);
   if (st != CB_OK) return st;
@@ -429,9 +477,10 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
                     : 0;
   int n_tiles = 1;
   int bn = pick_bn(a.M, Co, a.k_iters, dev->sms, &n_tiles);
-  // Tuning override (CB_IGEMM_FORCE="bn,stages,grid"; 0 = free), read per call.
-  int force_bn = 0, force_stages = 0, force_grid = 0;
-  if (const char* f = std::getenv("CB_IGEMM_FORCE")) std::sscanf(f, "%d,%d,%d", &force_bn, &force_stages, &force_grid);
+  // Tuning override (a measured plan, else CB_IGEMM_FORCE="bn,stages,grid"; 0 = free).
+  int force_bn = im.bn, force_stages = im.stages, force_grid = 0;
+  if (im.bn == 0)
+    if (const char* f = std::getenv("CB_IGEMM_FORCE")) std::sscanf(f, "%d,%d,%d", &force_bn, &force_stages, &force_grid);
   if (force_bn == 16 || force_bn == 32 || force_bn == 48 || force_bn == 64 || force_bn == 96 || force_bn == 128 ||
       force_bn == 192 || force_bn == 256) {
     bn = force_bn;
@@ -557,8 +606,19 @@ bool tc_shape(int ci, int co, int kh, int stride, int pad) {
   return g_policy.load() != 1 && ci % 4 == 0 && tc_channels_ok(ci, kh) && !pointwise_shape(ci, co, kh, stride, pad);
 }
 
-cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan) {
+cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan, ImPlan* im) {
   const int policy = g_policy.load();
+  {
+    ConvPlan cp;
+    const bool tc_views = policy != 1 && x->layout == CB_LAYOUT_NHWC && aligned16(x->data) && strides_mult4(x) &&
+                          x->n <= 65535 && x->w <= 65535 && x->h <= 65535 && encode_tiled() && encode_im2col();
+    if (tc_views && tuned_plan(conv_key(x, y, kh, stride, pad), &cp) &&
+        (cp.path == CB_PATH_TC_HALO || cp.path == CB_PATH_TC_HALO_CM || cp.path == CB_PATH_TC_IM2COL)) {
+      if (plan) *plan = cp.halo;
+      if (im) *im = cp.im;
+      return cp.path;
+    }
+  }
   if (pointwise_shape(x->c, y->c, kh, stride, pad) && x->layout == CB_LAYOUT_NHWC && aligned16(x->data) &&
       strides_mult4(x) && aligned16(y->data) && strides_mult4(y))
     return CB_PATH_POINTWISE;
@@ -761,9 +821,11 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out) {
   return CB_OK;
 }
 
-cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale, const float* bias, int kh, int kw,
-                         int stride, int pad, int groups, cb_act act, const cb_tensor* residual,
-                         cb_res_mode res_mode, cb_tensor* y, void* stream) {
+namespace {
+// Argument checks of cb_conv_bn_act (no launch).  *empty: nothing to compute.
+cb_status validate_conv(const cb_tensor* x, const float* w, const float* scale, const float* bias, int kh, int kw,
+                        int stride, int pad, int groups, cb_act act, const cb_tensor* residual, cb_res_mode res_mode,
+                        const cb_tensor* y, bool* depthwise_out, bool* empty) {
   if (!view_ok(x) || !view_ok(y) || !w || !scale || !bias) return CB_ERR_INVALID_ARG;
   if (act < CB_ACT_NONE || act > CB_ACT_SILU || res_mode < CB_RES_NONE || res_mode > CB_RES_POST_ACT)
     return CB_ERR_INVALID_ARG;
@@ -783,19 +845,25 @@ cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale,
     if (!same_view(residual, y) && overlap(residual, y)) return CB_ERR_INVALID_ARG;
   }
   if (overlap(x, y)) return CB_ERR_INVALID_ARG;
-  if (x->n == 0) return CB_OK;
   const long long M = static_cast<long long>(x->n) * OH * OW;
   if (M > (1LL << 31) - 129) return CB_ERR_UNSUPPORTED;
+  if (depthwise && (kh != 3 || x->layout != CB_LAYOUT_NHWC)) return CB_ERR_UNSUPPORTED;
+  *depthwise_out = depthwise;
+  *empty = x->n == 0;
+  return CB_OK;
+}
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+// One launch of a validated layer: the depthwise kernel, or the dense path
+// (a forced plan when `force` is given, else the tuned or modelled one).
+cb_status launch_conv(const cb_tensor* x, const float* w, const float* scale, const float* bias, int kh, int stride,
+                      int pad, bool depthwise, cb_act act, const cb_tensor* residual, cb_res_mode res_mode,
+                      const cb_tensor* y, cudaStream_t s, const ConvPlan* force) {
   const Epilogue ep = make_epilogue(scale, bias, act, residual, res_mode);
-  const int policy = g_policy.load();
-  if (depthwise) {
-    if (kh != 3 || x->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
-    return run_depthwise(x, w, ep, stride, pad, y, s);
-  }
+  if (depthwise) return run_depthwise(x, w, ep, stride, pad, y, s);
   HaloPlan plan;
-  const cb_path path = dense_path(x, y, kh, stride, pad, &plan);
+  ImPlan im;
+  const cb_path path = force ? force->path : dense_path(x, y, kh, stride, pad, &plan, &im);
+  if (force) plan = force->halo, im = force->im;
   if (path == CB_PATH_POINTWISE) {
     // 16-byte weight, scale / bias and residual accesses, else the direct kernel
     const bool vec = aligned16(w) && aligned16(scale) && aligned16(bias) &&
@@ -809,9 +877,143 @@ cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale,
   switch (path) {
     case CB_PATH_TC_HALO:
     case CB_PATH_TC_HALO_CM: return run_igemm_halo(x, w, ep, plan, y, s);
-    case CB_PATH_TC_IM2COL: return run_igemm(x, w, ep, kh, stride, pad, y, s);
+    case CB_PATH_TC_IM2COL: return run_igemm(x, w, ep, kh, stride, pad, y, s, im);
     default: return run_direct(x, w, ep, kh, stride, pad, y, s);
   }
+}
+
+// Every plan of the dense tensor-core paths that fits this layer.
+std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, int sms) {
+  std::vector<ConvPlan> out;
+  const int Ci = x->c, Co = y->c;
+  if (kh == 3 && stride == 1 && pad == 1 && Ci % 32 == 0 && x->w + 2 <= 256 && g_policy.load() == 0) {
+    const int wp = x->w + 2;
+    struct Shape {
+      int px, co;
+      bool cm;
+    };
+    static const Shape kShapes[] = {{256, 128, true}, {128, 256, false}, {128, 128, false}, {128, 64, false},
+                                    {128, 32, false}};
+    for (const Shape& sh : kShapes) {
+      if (!sh.cm && sh.co > 2 * ((Co + 15) / 16 * 16)) continue;  // a tile mostly beyond Co
+      const int hb = halo_buffer_bytes(wp, sh.px);
+      if (halo_rows(wp, sh.px) > 256) continue;
+      int nb_max = 8;
+      while (nb_max >= 2 && halo_smem_bytes(sh.co, hb, nb_max) > 227 * 1024) --nb_max;
+      for (int nb : {nb_max, 3}) {
+        if (nb < 2 || nb > nb_max || (nb == 3 && nb_max == 3)) continue;
+        ConvPlan p;
+        p.path = sh.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
+        p.halo.px = sh.px;
+        p.halo.co = sh.co;
+        p.halo.cm = sh.cm;
+        p.halo.nb = nb;
+        p.halo.smem = halo_smem_bytes(sh.co, hb, nb);
+        const long long tiles = static_cast<long long>(x->n) * ((x->h * wp + sh.px - 1) / sh.px) *
+                                ((Co + sh.co - 1) / sh.co);
+        if (tiles >= (1LL << 31)) continue;
+        p.halo.grid = static_cast<int>(std::min<long long>(tiles, sms));
+        out.push_back(p);
+      }
+    }
+  }
+  for (int bn : {16, 32, 48, 64, 96, 128, 192, 256}) {
+    if (bn > 2 * ((Co + 15) / 16 * 16) && bn > 16) continue;
+    ConvPlan p;
+    p.path = CB_PATH_TC_IM2COL;
+    p.im.bn = bn;
+    out.push_back(p);
+  }
+  return out;
+}
+}  // namespace
+
+cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale, const float* bias, int kh, int kw,
+                         int stride, int pad, int groups, cb_act act, const cb_tensor* residual,
+                         cb_res_mode res_mode, cb_tensor* y, void* stream) {
+  bool depthwise = false, empty = false;
+  cb_status st = validate_conv(x, w, scale, bias, kh, kw, stride, pad, groups, act, residual, res_mode, y,
+                               &depthwise, &empty);
+  if (st != CB_OK || empty) return st;
+  return launch_conv(x, w, scale, bias, kh, stride, pad, depthwise, act, residual, res_mode, y,
+                     static_cast<cudaStream_t>(stream), nullptr);
+}
+
+cb_status cb_autotune_conv(const cb_tensor* x, const float* w, const float* scale, const float* bias, int kh, int kw,
+                           int stride, int pad, int groups, cb_act act, const cb_tensor* residual,
+                           cb_res_mode res_mode, cb_tensor* y, void* stream) {
+  bool depthwise = false, empty = false;
+  cb_status st = validate_conv(x, w, scale, bias, kh, kw, stride, pad, groups, act, residual, res_mode, y,
+                               &depthwise, &empty);
+  if (st != CB_OK || empty) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const ConvKey key = conv_key(x, y, kh, stride, pad);
+  {
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    g_tuned.erase(key);  // decide afresh
+  }
+  HaloPlan hp;
+  const cb_path path = depthwise ? CB_PATH_DEPTHWISE : dense_path(x, y, kh, stride, pad, &hp);
+  const bool tc = path == CB_PATH_TC_HALO || path == CB_PATH_TC_HALO_CM || path == CB_PATH_TC_IM2COL;
+  if (!tc || !aligned16(w)) {  // one kernel only: nothing to choose
+    return launch_conv(x, w, scale, bias, kh, stride, pad, depthwise, act, residual, res_mode, y, s, nullptr);
+  }
+  DeviceInfo* dev = nullptr;
+  st = current_device(&dev);
+  if (st != CB_OK) return st;
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess) return cuda_fail(cudaGetLastError());
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return cuda_fail(cudaGetLastError());
+  }
+  constexpr int kReps = 5;
+  float best_ms = 1e30f;
+  ConvPlan best;
+  bool found = false;
+  for (const ConvPlan& cand : tc_candidates(x, y, kh, stride, pad, dev->sms)) {
+    // warm-up launch (also rejects plans this layer cannot take), then kReps timed ones
+    if (launch_conv(x, w, scale, bias, kh, stride, pad, false, act, residual, res_mode, y, s, &cand) != CB_OK)
+      continue;
+    cudaEventRecord(e0, s);
+    bool ok = true;
+    for (int r = 0; r < kReps && ok; ++r)
+      ok = launch_conv(x, w, scale, bias, kh, stride, pad, false, act, residual, res_mode, y, s, &cand) == CB_OK;
+    cudaEventRecord(e1, s);
+    if (cudaEventSynchronize(e1) != cudaSuccess || !ok) continue;
+    float ms = 0.0f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    if (ms < best_ms) {
+      best_ms = ms;
+      best = cand;
+      found = true;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (found) {
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    g_tuned[key] = best;
+  }
+  if (std::getenv("CB_DEBUG_PLAN") && found)
+    std::fprintf(stderr, "[cb] autotune: Ci=%d Co=%d %dx%d k=%d s=%d -> path %d (px=%d co=%d nb=%d bn=%d) %.1f us\n",
+                 x->c, y->c, x->h, x->w, kh, stride, static_cast<int>(best.path), best.halo.px, best.halo.co,
+                 best.halo.nb, best.im.bn, 1000.0f * best_ms / kReps);
+  // leave y holding the chosen plan's result
+  st = launch_conv(x, w, scale, bias, kh, stride, pad, false, act, residual, res_mode, y, s, found ? &best : nullptr);
+  if (st != CB_OK) return st;
+  const cudaError_t e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+void cb_autotune_clear(void) {
+  std::lock_guard<std::mutex> lock(g_tune_mu);
+  g_tuned.clear();
+}
+
+int cb_autotune_entries(void) {
+  std::lock_guard<std::mutex> lock(g_tune_mu);
+  return static_cast<int>(g_tuned.size());
 }
 
 cb_status cb_dw_separable_block_workspace(const cb_tensor* x, int c_out, int stride, size_t* bytes) {

@@ -61,6 +61,12 @@ class ConvBnAct:
         return cb.conv_bn_act(x, self.w, self.scale, self.bias, self.k, self.stride, self.pad, self.groups, self.act,
                               y, residual=residual, res_mode=res_mode, stream=stream, x_layout=x_layout)
 
+    def autotune(self, x, y, residual=None, res_mode=cb.RES_NONE, stream=None, x_layout=cb.LAYOUT_NHWC):
+        """Measure this layer's tile plans on these buffers (cb_autotune_conv); later calls with the
+        same shapes run the fastest.  y holds the result."""
+        return cb.autotune_conv(x, self.w, self.scale, self.bias, self.k, self.stride, self.pad, self.groups,
+                                self.act, y, residual=residual, res_mode=res_mode, stream=stream, x_layout=x_layout)
+
 
 class DwBlock:
     """DepthwiseSeparableConv on device, run through cb_dw_separable_block."""
@@ -140,16 +146,19 @@ class YoloChain:
             self.bufs.append(B)
             H = OH
 
-    def forward(self, x, stream=None):
+    def forward(self, x, stream=None, tune=False):
+        """The chain on x; tune=True measures each layer's tile plans on the way (cb_autotune_conv),
+        synchronising after every layer, so that later forwards run the fastest."""
         h = x
         for L, B in zip(self.layers, self.bufs):
             half = B["half"]
-            L["down"](h, B["x1"], stream=stream)
             a = B["cat"][..., :half]
             b = B["cat"][..., half:]
-            L["cv1"](B["x1"], a, stream=stream)
-            L["cv2"](a, b, stream=stream)
-            L["cv3"](B["cat"], B["out"], residual=B["x1"], res_mode=cb.RES_POST_ACT, stream=stream)
+            run = {k: (v.autotune if tune else v) for k, v in L.items()}
+            run["down"](h, B["x1"], stream=stream)
+            run["cv1"](B["x1"], a, stream=stream)
+            run["cv2"](a, b, stream=stream)
+            run["cv3"](B["cat"], B["out"], residual=B["x1"], res_mode=cb.RES_POST_ACT, stream=stream)
             h = B["out"]
         return h
 

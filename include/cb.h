@@ -294,6 +294,32 @@ typedef enum {
  */
 int cb_conv_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, int groups);
 
+/*
+ * Per-shape autotuner for cb_conv_bn_act (same arguments).  For a layer on
+ * the tensor-core path it runs every tile plan that fits the shape (halo
+ * tiles of 128 pixels x 32..256 channels or 256 pixels x 128 channels with
+ * two weight-ring depths, im2col tiles of 16..256 channels) on the given
+ * buffers, one warm-up and five timed launches each with events on
+ * `stream`, and records the fastest for the key (device, policy, N, H, W,
+ * Ci, Co, kh, stride, pad); later cb_conv_bn_act and cb_conv_path calls with
+ * that key take it in place of the built-in cost model.  Every candidate
+ * computes the same TF32 products, so results stay within the tensor-core
+ * tolerance of each other.  Other layers (depthwise, CUDA-core paths) have
+ * one kernel and are launched once.  y holds the layer's result on return.
+ * Synchronises `stream`; must not be called while the stream is being
+ * captured into a graph.  Thread-safe; host table only, no device memory.
+ */
+cb_status cb_autotune_conv(const cb_tensor* x, const float* w, const float* scale, const float* bias,
+                           int kh, int kw, int stride, int pad, int groups, cb_act act,
+                           const cb_tensor* residual, cb_res_mode res_mode, cb_tensor* y,
+                           void* stream);
+
+/* Forget every plan cb_autotune_conv recorded. */
+void cb_autotune_clear(void);
+
+/* Number of layer shapes with a recorded plan. */
+int cb_autotune_entries(void);
+
 /* A static string naming a status code. */
 const char* cb_status_string(cb_status s);
 
