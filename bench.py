@@ -164,7 +164,8 @@ def profiled_traffic(profile_name, src_files):
 # ------------------------------------------------------------ workloads
 PATH_KERNELS = {1: ("cb::direct_tile_kernel / direct_conv_kernel", "hbm"), 2: ("cb::dw_tma_kernel", "hbm"),
                 3: ("cb::igemm_tf32_kernel", "tensor"), 4: ("cb::igemm_halo_kernel (pixel-major)", "tensor"),
-                5: ("cb::igemm_halo_kernel (channel-major)", "tensor"), 6: ("cb::pw_small_kernel", "hbm")}
+                5: ("cb::igemm_halo_kernel (channel-major)", "tensor"), 6: ("cb::pw_small_kernel", "hbm"),
+                7: ("cb::stem_kernel", "hbm")}
 
 
 def kernel_of(binding, x, y, k, stride, pad, x_layout=0):
@@ -474,9 +475,13 @@ class YoloWorkload(Workload):
 
 
 class PreprocessWorkload(Workload):
+    """u8 frames -> resize + /255 -> stem conv, as one kernel (the preprocess fused into the stem's
+    input staging).  The preprocess kernel alone (its own byte ledger), the two-kernel path
+    (preprocess to memory, then the stem) and the three-pass path are timed beside it."""
     unit = "GB/s"
-    dominant = "preprocess_fused"
-    profile = ("preprocess_pair_kernel_32x1280x720.md", ["preprocess.cu", "ptx.cuh", "launch_util.h"])
+    dominant = "preprocess_stem"
+    profile = ("stem_kernel_preprocess_32x1280x720.md",
+               ["stem.cu", "resample.cuh", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"])
 
     def __init__(self, torch, device, batch=32):
         from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
@@ -488,37 +493,53 @@ class PreprocessWorkload(Workload):
         self.net = PreprocessStem(self.sw, self.sbn, batch, device=device)
         self.net.tmp_u8 = torch.empty(batch, 480, 640, 3, dtype=torch.uint8, device=device)
         self.net.tmp_f32 = torch.empty(batch, 480, 640, 3, device=device)
-        pre = workloads.preprocess_fused(batch, 720, 1280, 480, 640)
-        stem = workloads.conv_layer(batch, 480, 640, 3, 16, 3, 2, 1)
+        work = workloads.preprocess_stem_fused(batch, 720, 1280, 480, 640)
         self.launches = [
-            Launch("preprocess_fused", lambda s: cb.preprocess_u8(self.frames, self.net.planar, stream=s), pre,
-                   "cb::preprocess_pair_kernel", "hbm"),
-            Launch("stem_conv", lambda s: self.net.stem(self.net.planar, self.net.out, stream=s,
-                                                        x_layout=cb.LAYOUT_NCHW), stem,
-                   "cb::direct_tile_kernel<2,3,16,2,3>", "hbm"),
+            Launch("preprocess_stem", lambda s: self.net.forward(self.frames, stream=s), work,
+                   "cb::stem_kernel (u8 frames: preprocess in the input staging)", "hbm"),
         ]
+        self.pre = workloads.preprocess_fused(batch, 720, 1280, 480, 640)
+        self.stem = workloads.conv_layer(batch, 480, 640, 3, 16, 3, 2, 1)
         self.three_pass = workloads.preprocess_unfused(batch, 720, 1280, 480, 640)
-        self.config = {"workload": "fused u8 preprocess 1280x720 -> 640x480 NCHW fp32 + stem conv3x3 s2 3->16 "
-                                   "+ BN + SiLU", "batch": batch,
-                       "l2": "inputs_larger_than_l2 (88 MB frames + 118 MB planar + 157 MB stem out)"}
+        self.config = {"workload": "u8 frames 1280x720 -> bilinear 640x480 -> /255 -> stem conv3x3 s2 3->16 + BN + "
+                                   "SiLU (NHWC fp32 out), preprocess fused into the stem", "batch": batch,
+                       "l2": "inputs_larger_than_l2 (88 MB frames + 157 MB stem out)",
+                       "bytes_per_frame": work.bytes // batch}
 
     def extra(self, torch, stream, steps):
-        """The three-pass comparison path, timed the same way (not part of the step)."""
+        """The preprocess kernel alone, the two-kernel path and the three-pass path, timed the same
+        way (not part of the step)."""
         from conv_bn_activation_gb300 import binding as cb
-        fn = lambda: cb.preprocess_u8_three_pass(self.frames, self.net.tmp_u8, self.net.tmp_f32, self.net.planar,
-                                                 stream=stream)
-        for _ in range(3):
-            fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
-        return {"three_pass_us": round(ms * 1e3, 2),
-                "three_pass_gbs_on_its_ledger": round(self.three_pass.bytes / (ms * 1e-3) / 1e9, 1),
-                "ledger_bytes_per_frame": {"fused": 6451200, "three_pass": 15667200}}
+        net = self.net
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / steps
+
+        pre_ms = timed(lambda: cb.preprocess_u8(self.frames, net.planar, stream=stream))
+        stem_ms = timed(lambda: net.stem(net.planar, net.out, stream=stream, x_layout=cb.LAYOUT_NCHW))
+        two_ms = timed(lambda: net.forward(self.frames, stream=stream, fused=False))
+        three_ms = timed(lambda: cb.preprocess_u8_three_pass(self.frames, net.tmp_u8, net.tmp_f32, net.planar,
+                                                             stream=stream))
+        hbm = load_peaks()["hbm_gbs"]
+        pre_gbs = self.pre.bytes / (pre_ms * 1e-3) / 1e9
+        return {"preprocess_kernel_us": round(pre_ms * 1e3, 2),
+                "preprocess_kernel_gbs_on_its_ledger": round(pre_gbs, 1),
+                "preprocess_kernel_frac": round(pre_gbs / hbm, 4),
+                "stem_kernel_planar_us": round(stem_ms * 1e3, 2),
+                "stem_kernel_planar_gbs": round(self.stem.bytes / (stem_ms * 1e-3) / 1e9, 1),
+                "two_kernel_path_us": round(two_ms * 1e3, 2),
+                "three_pass_us": round(three_ms * 1e3, 2),
+                "three_pass_gbs_on_its_ledger": round(self.three_pass.bytes / (three_ms * 1e-3) / 1e9, 1),
+                "ledger_bytes_per_frame": {"fused_preprocess": 6451200, "three_pass": 15667200,
+                                           "preprocess_stem": self.launches[0].work.bytes // self.batch}}
 
     def e2e_setup(self):
         self.f_pin = self.torch.from_numpy(self.frames_host).pin_memory()

@@ -21,7 +21,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_
 ACT_NONE, ACT_RELU, ACT_SILU = 0, 1, 2
 RES_NONE, RES_PRE_ACT, RES_POST_ACT = 0, 1, 2
 LAYOUT_NHWC, LAYOUT_NCHW = 0, 1
-PATH_DIRECT, PATH_DEPTHWISE, PATH_TC_IM2COL, PATH_TC_HALO, PATH_TC_HALO_CM, PATH_POINTWISE = 1, 2, 3, 4, 5, 6
+PATH_DIRECT, PATH_DEPTHWISE, PATH_TC_IM2COL, PATH_TC_HALO, PATH_TC_HALO_CM, PATH_POINTWISE, PATH_STEM = range(1, 8)
 
 EXPORTED = (
     "cb_fold_bn", "cb_repack_weights", "cb_conv_bn_act", "cb_dw_separable_block_workspace",
@@ -29,7 +29,7 @@ EXPORTED = (
     "cb_get_device_error", "cb_last_cuda_error", "cb_set_kernel_policy", "cb_status_string", "cb_version",
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_layer_uses_tensor_cores",
     "cb_dw_separable_block_static", "cb_conv_path", "cb_debug_timeout_probe", "cb_autotune_conv",
-    "cb_autotune_clear", "cb_autotune_entries",
+    "cb_autotune_clear", "cb_autotune_entries", "cb_preprocess_stem_u8",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
@@ -85,6 +85,7 @@ def load():
                 "cb_debug_timeout_probe": [I, P],
                 "cb_autotune_conv": [T, P, P, P, I, I, I, I, I, I, T, I, T, P],
                 "cb_autotune_clear": [],
+                "cb_preprocess_stem_u8": [P, I, I, I, LL, I, I, P, P, P, I, T, P],
                 "cb_autotune_entries": [],
                 "cb_status_string": [I],
                 "cb_version": [],
@@ -277,6 +278,19 @@ def preprocess_u8(src, dst, stream=None):
     _check(load().cb_preprocess_u8(src.data_ptr(), N, Hs, Ws, src.stride(1), dst.data_ptr(), Hd, Wd,
                                    _stream_ptr(stream)), "cb_preprocess_u8")
     return dst
+
+
+def preprocess_stem_u8(src, dst_hw, w, scale, bias, act, y, stream=None):
+    """cb_preprocess_stem_u8: u8 frames [N, Hs, Ws, 3] (rows may be padded) resized to dst_hw, /255,
+    straight into the 3 -> 16 stride-2 stem; y: [N, OH, OW, 16] NHWC view; w, scale, bias: device
+    tensors in the cb_repack_weights / cb_fold_bn layouts."""
+    N, Hs, Ws, _ = src.shape
+    assert src.stride(0) == Hs * src.stride(1) and src.stride(2) == 3 and src.stride(3) == 1
+    yv = nhwc(y)
+    _check(load().cb_preprocess_stem_u8(src.data_ptr(), N, Hs, Ws, src.stride(1), dst_hw[0], dst_hw[1],
+                                        w.data_ptr(), scale.data_ptr(), bias.data_ptr(), act, ctypes.byref(yv),
+                                        _stream_ptr(stream)), "cb_preprocess_stem_u8")
+    return y
 
 
 def preprocess_u8_three_pass(src, tmp_u8, tmp_f32, dst, stream=None):

@@ -601,6 +601,18 @@ bool pointwise_shape(int ci, int co, int kh, int stride, int pad) {
   return g_policy.load() != 1 && kh == 1 && stride == 1 && pad == 0 && pointwise_small_ok(ci, co);
 }
 
+// The 3 -> 16 stride-2 stem kernel: planar (NCHW) or packed NHWC input with
+// 16-byte aligned rows of a multiple of 4 pixels, 16-byte aligned output.
+bool stem_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad) {
+  if (g_policy.load() == 1 || x->c != 3 || y->c != 16 || kh != 3 || stride != 2 || pad != 1) return false;
+  if (x->w % 4 != 0 || !aligned16(x->data) || !aligned16(y->data) || !strides_mult4(y)) return false;
+  if (x->n > 65535 || static_cast<long long>(x->n) * ((y->h + 7) / 8) * ((y->w + 63) / 64) >= (1LL << 31))
+    return false;
+  if (x->layout == CB_LAYOUT_NCHW)
+    return x->stride_n % 4 == 0 && x->stride_h % 4 == 0 && x->stride_c % 4 == 0;
+  return x->stride_w == 3 && x->stride_n % 4 == 0 && x->stride_h % 4 == 0;
+}
+
 // Shape rule of the tensor-core paths (views aside).
 bool tc_shape(int ci, int co, int kh, int stride, int pad) {
   return g_policy.load() != 1 && ci % 4 == 0 && tc_channels_ok(ci, kh) && !pointwise_shape(ci, co, kh, stride, pad);
@@ -619,6 +631,7 @@ cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, i
       return cp.path;
     }
   }
+  if (stem_path(x, y, kh, stride, pad)) return CB_PATH_STEM;
   if (pointwise_shape(x->c, y->c, kh, stride, pad) && x->layout == CB_LAYOUT_NHWC && aligned16(x->data) &&
       strides_mult4(x) && aligned16(y->data) && strides_mult4(y))
     return CB_PATH_POINTWISE;
@@ -733,6 +746,29 @@ cb_status run_pointwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
   // a residual ring that does not fit in shared memory (4 input channels with
   // 16 or more outputs): the direct kernel
   if (e == cudaErrorInvalidValue) return run_direct(x, w, ep, 1, 1, 0, y, s);
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+cb_status run_stem(const cb_tensor* x, const float* w, const Epilogue& ep, const cb_tensor* y, cudaStream_t s) {
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  StemArgs a{};
+  a.src = x->data;
+  a.xs_n = x->stride_n;
+  a.xs_h = x->stride_h;
+  a.xs_c = x->stride_c;
+  a.N = x->n;
+  a.H = x->h;
+  a.W = x->w;
+  a.OH = y->h;
+  a.OW = y->w;
+  a.w = w;
+  a.ep = ep;
+  a.out = make_out(y);
+  stem_tile_grid(a.OH, a.OW, &a.tiles_y, &a.tiles_x);
+  const int kind = x->layout == CB_LAYOUT_NCHW ? 0 : 1;
+  const cudaError_t e = launch_stem(a, kind, stem_smem_bytes(kind, 0, 0), dev->sms, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
 
@@ -864,6 +900,11 @@ cb_status launch_conv(const cb_tensor* x, const float* w, const float* scale, co
   ImPlan im;
   const cb_path path = force ? force->path : dense_path(x, y, kh, stride, pad, &plan, &im);
   if (force) plan = force->halo, im = force->im;
+  if (path == CB_PATH_STEM) {
+    // 16-byte residual accesses, else the direct kernel
+    const bool vec = res_mode == CB_RES_NONE || (aligned16(residual->data) && strides_mult4(residual));
+    return vec ? run_stem(x, w, ep, y, s) : run_direct(x, w, ep, kh, stride, pad, y, s);
+  }
   if (path == CB_PATH_POINTWISE) {
     // 16-byte weight, scale / bias and residual accesses, else the direct kernel
     const bool vec = aligned16(w) && aligned16(scale) && aligned16(bias) &&
@@ -1144,6 +1185,51 @@ cb_status cb_preprocess_u8(const unsigned char* src, int n, int src_h, int src_w
   if (st != CB_OK) return st;
   cudaError_t e = launch_preprocess_fused(src, n, src_h, src_w, src_pitch, dst, dst_h, dst_w, dev->sms,
                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
+cb_status cb_preprocess_stem_u8(const unsigned char* src, int n, int src_h, int src_w, long long src_pitch,
+                                int dst_h, int dst_w, const float* w, const float* scale, const float* bias, cb_act act,
+                                cb_tensor* y, void* stream) {
+  if (!src || !w || !scale || !bias || !view_ok(y) || n < 0 || src_h < 1 || src_w < 1 || dst_h < 1 || dst_w < 1)
+    return CB_ERR_INVALID_ARG;
+  if (src_pitch < 3LL * src_w || act < CB_ACT_NONE || act > CB_ACT_SILU) return CB_ERR_INVALID_ARG;
+  if (y->layout != CB_LAYOUT_NHWC || y->n != n || y->c != 16 || y->h != (dst_h - 1) / 2 + 1 ||
+      y->w != (dst_w - 1) / 2 + 1)
+    return CB_ERR_INVALID_ARG;
+  if (n == 0) return CB_OK;
+  if (!aligned16(src) || src_pitch % 16 != 0 || (3LL * src_w) % 16 != 0 || dst_w % 4 != 0) return CB_ERR_ALIGNMENT;
+  if (!aligned16(y->data) || !strides_mult4(y)) return CB_ERR_ALIGNMENT;
+  if (n > 65535 || src_h > (1 << 22) || src_w > (1 << 20) || dst_h > (1 << 22) || dst_w > (1 << 20))
+    return CB_ERR_UNSUPPORTED;
+  uintptr_t ylo, yhi;
+  view_range(y, &ylo, &yhi);
+  const uintptr_t slo = reinterpret_cast<uintptr_t>(src);
+  const uintptr_t shi = slo + static_cast<uintptr_t>((static_cast<long long>(n) * src_h - 1) * src_pitch + 3LL * src_w);
+  if (slo < yhi && ylo < shi) return CB_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  StemArgs a{};
+  a.src = src;
+  a.N = n;
+  a.H = dst_h;
+  a.W = dst_w;
+  a.OH = y->h;
+  a.OW = y->w;
+  a.hs = src_h;
+  a.ws = src_w;
+  a.pitch = src_pitch;
+  int rows = 0;
+  stem_src_bounds(src_h, src_w, dst_h, dst_w, &rows, &a.row_cap);
+  a.w = w;
+  a.ep = make_epilogue(scale, bias, act, nullptr, CB_RES_NONE);
+  a.out = make_out(y);
+  stem_tile_grid(a.OH, a.OW, &a.tiles_y, &a.tiles_x);
+  if (static_cast<long long>(n) * a.tiles_y * a.tiles_x >= (1LL << 31)) return CB_ERR_UNSUPPORTED;
+  const size_t smem = stem_smem_bytes(2, rows, a.row_cap);
+  if (smem > 227 * 1024) return CB_ERR_UNSUPPORTED;  // too strong a downscale for one tile's source rows
+  const cudaError_t e = launch_stem(a, 2, smem, dev->sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
 

@@ -124,6 +124,32 @@ size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages);
 cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
                               bool cm, int grid, size_t smem_bytes, cudaStream_t s);
 
+// ------------------------------------------------------------------- stem
+// 3 -> 16 channels, 3x3, stride 2, pad 1, CUDA cores (stem.cu).  Input:
+// planar fp32 (src_kind 0: x[n*xs_n + c*xs_c + h*xs_h + w]), packed NHWC
+// fp32 (1: x[n*xs_n + h*xs_h + 3*w + c]) or u8 frames preprocessed on the
+// fly (2: [n][hs][pitch] bytes, 3 channels per pixel, resized to H x W).
+// Needs W % 4 == 0, 16-byte aligned bases and strides that are multiples of
+// 4 elements (of 16 bytes for the frames, whose rows are a multiple of 16
+// bytes), a 16-byte aligned output view with strides that are multiples of 4.
+struct StemArgs {
+  const void* src;
+  long long xs_n, xs_h, xs_c;
+  int N, H, W, OH, OW;
+  int hs, ws;          // u8 frames: source size
+  long long pitch;     // u8 frames: bytes per source row
+  int row_cap;         // u8 frames: bytes per staged source row
+  const float* w;      // OHWI [16][3][3][3]
+  Epilogue ep;         // residual (if any): 16-byte aligned, strides multiples of 4
+  OutView out;
+  int tiles_x, tiles_y;
+};
+void stem_tile_grid(int OH, int OW, int* tiles_y, int* tiles_x);
+// Staged source rows per tile and bytes per staged row for a hs x ws -> hd x wd resize.
+void stem_src_bounds(int hs, int ws, int hd, int wd, int* rows, int* row_cap);
+size_t stem_smem_bytes(int src_kind, int src_rows, int row_cap);
+cudaError_t launch_stem(const StemArgs& a, int src_kind, size_t smem, int sms, cudaStream_t s);
+
 // -------------------------------------------------------------- preprocess
 cudaError_t launch_preprocess_fused(const uint8_t* src, int n, int hs, int ws, long long pitch, float* dst,
                                     int hd, int wd, int sms, cudaStream_t s);

@@ -177,7 +177,14 @@ class PreprocessStem:
         self.tmp_u8 = None
         self.tmp_f32 = None
 
-    def forward(self, frames, stream=None, three_pass=False):
+    def forward(self, frames, stream=None, three_pass=False, fused=True):
+        """frames -> stem output.  fused: one kernel (cb_preprocess_stem_u8), the planar image never
+        leaves shared memory; else the preprocess writes self.planar (in one pass, or in three with
+        three_pass) and the stem reads it."""
+        if fused and not three_pass:
+            cb.preprocess_stem_u8(frames, self.dst_hw, self.stem.w, self.stem.scale, self.stem.bias, self.stem.act,
+                                  self.out, stream=stream)
+            return self.out
         if three_pass:
             if self.tmp_u8 is None:
                 Hd, Wd = self.dst_hw

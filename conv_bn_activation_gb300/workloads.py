@@ -72,6 +72,14 @@ def preprocess_fused(N, Hs, Ws, Hd, Wd) -> Work:
     return Work(N * preprocess_ledger(Hs, Ws, Hd, Wd)["fused"], 0)
 
 
+def preprocess_stem_fused(N, Hs, Ws, Hd, Wd, Cout=16) -> Work:
+    """The preprocess fused into the 3x3 stride-2 stem: the u8 frames read once, the stem's fp32
+    output written once (plus its weights and scale/bias); FLOPs of the stem convolution."""
+    stem = conv_layer(N, Hd, Wd, 3, Cout, 3, 2, 1)
+    planar_in = N * Hd * Wd * 3 * F32
+    return Work(N * Hs * Ws * 3 + stem.bytes - planar_in, stem.flops)
+
+
 def preprocess_unfused(N, Hs, Ws, Hd, Wd) -> Work:
     return Work(N * preprocess_ledger(Hs, Ws, Hd, Wd)["unfused"], 0)
 

@@ -127,6 +127,11 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
  * layers with Ci and Co in {4, 8, 16, 32} run instead on a streaming fp32
  * CUDA-core kernel (HBM-bound at these widths);
  * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;
+ * 3 -> 16 channel 3x3 stride-2 pad-1 stems run on a dedicated fp32 CUDA-core
+ * kernel when the input is planar (NCHW) or packed NHWC (stride_w == 3) with
+ * W % 4 == 0, 16-byte aligned data and n / h (/ c) strides that are
+ * multiples of 4 elements, and the output (and residual) is 16-byte aligned
+ * with strides that are multiples of 4;
  * everything else (stems with 1 or 3 input channels, NCHW input, odd channel
  * counts) runs on a direct CUDA-core kernel in fp32.
  */
@@ -225,6 +230,27 @@ cb_status cb_preprocess_u8(const unsigned char* src, int n, int src_h, int src_w
  * [n, dst_h, dst_w, 3] u8; tmp_f32: DEVICE [n, dst_h, dst_w, 3] fp32; dst as
  * cb_preprocess_u8.  Produces bit-identical output to cb_preprocess_u8.
  */
+/*
+ * The preprocess of cb_preprocess_u8 fused into the stem conv that reads its
+ * output (conv 3 -> 16 channels, 3x3, stride 2, pad 1, folded BN, act): one
+ * kernel reads the u8 frames and writes the stem's NHWC output; the fp32
+ * planar image exists only in shared memory, tile by tile, with the values
+ * cb_preprocess_u8 would have stored (same arithmetic, bit for bit).
+ * src: DEVICE u8 frames as for cb_preprocess_u8; dst_h x dst_w: the resize
+ * target (the stem's input size); w: DEVICE weights [16][3][3][3] (OHWI, as
+ * cb_repack_weights writes them); scale / bias: DEVICE fp32 [16]; y: NHWC
+ * view [n, (dst_h - 1) / 2 + 1, (dst_w - 1) / 2 + 1, 16], which must not
+ * overlap the frames.  Needs a 16-byte aligned src, src_pitch and
+ * 3 * src_w multiples of 16, dst_w % 4 == 0, a 16-byte aligned y with
+ * strides that are multiples of 4 (else CB_ERR_ALIGNMENT), and a downscale
+ * whose per-tile source rows fit in shared memory (about 8x vertically at a
+ * 3840-byte source row; else CB_ERR_UNSUPPORTED).  fp32 CUDA cores,
+ * asynchronous on `stream`.
+ */
+cb_status cb_preprocess_stem_u8(const unsigned char* src, int n, int src_h, int src_w, long long src_pitch,
+                                int dst_h, int dst_w, const float* w, const float* scale, const float* bias,
+                                cb_act act, cb_tensor* y, void* stream);
+
 cb_status cb_preprocess_u8_three_pass(const unsigned char* src, int n, int src_h, int src_w,
                                       long long src_pitch, unsigned char* tmp_u8, float* tmp_f32,
                                       float* dst, int dst_h, int dst_w, void* stream);
@@ -283,7 +309,8 @@ typedef enum {
   CB_PATH_TC_HALO = 4,    /* tensor-core implicit GEMM, one halo tile per 32-channel chunk (3x3, stride 1),
                              128 pixels x up to 256 channels per tile */
   CB_PATH_TC_HALO_CM = 5, /* the same with 256 pixels x 128 channels per tile, channels as the MMA's M */
-  CB_PATH_POINTWISE = 6   /* streaming fp32 CUDA-core 1x1 kernel for at most 32 input and output channels */
+  CB_PATH_POINTWISE = 6,  /* streaming fp32 CUDA-core 1x1 kernel for at most 32 input and output channels */
+  CB_PATH_STEM = 7        /* fp32 CUDA-core 3 -> 16 channel 3x3 stride-2 stem kernel */
 } cb_path;
 
 /*

@@ -87,14 +87,15 @@ def test_yolo_chain_full_size_per_layer(gpu, orc):
         h = out
 
 
-@pytest.mark.parametrize("three_pass", [False, True])
-def test_preprocess_stem(gpu, orc, three_pass):
+@pytest.mark.parametrize("mode", ["fused", "two_kernel", "three_pass"])
+def test_preprocess_stem(gpu, orc, mode):
     frames = synthetic.preprocess_frames(N=2)
     w, bn = synthetic.stem_params()
     net = PreprocessStem(w, bn, 2)
-    out = net.forward(to_dev(frames), three_pass=three_pass)
+    out = net.forward(to_dev(frames), three_pass=mode == "three_pass", fused=mode == "fused")
     sync_check()
     planar = orc.preprocess_u8(frames, 480, 640, orc.PREC_F32)
-    np.testing.assert_array_equal(net.planar.cpu().numpy(), planar)
+    if mode != "fused":
+        np.testing.assert_array_equal(net.planar.cpu().numpy(), planar)
     ref = orc.conv_bn_act(planar, w, bn, stride=2, pad=1, act=orc.ACT_SILU, layout=orc.NCHW)
     assert rel_err(out.cpu().numpy(), ref) <= TOL_FP32

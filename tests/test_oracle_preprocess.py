@@ -163,3 +163,15 @@ def test_byte_ledger_matches_page():
     assert abs(led["unfused"] / (m["path_a_mean_us"] * 1e-6) / 1e9 - m["path_a_gbps"]) < 0.01
     assert abs(led["fused"] / (m["path_b_mean_us"] * 1e-6) / 1e9 - m["path_b_gbps"]) < 0.01
     assert round(m["path_a_mean_us"] / m["path_b_mean_us"], 3) == m["speedup"]
+
+
+def test_preprocess_stem_ledger():
+    """The fused preprocess + stem moves the u8 frame in and the stem's 16-channel fp32 output out:
+    the fused preprocess's ledger minus its fp32 planar write, plus the stem output (half the
+    resolution in each direction, 16 channels), weights and scale/bias once."""
+    led = workloads.preprocess_ledger(720, 1280, 480, 640)
+    planar = 480 * 640 * 3 * 4
+    stem_out = 240 * 320 * 16 * 4
+    w = workloads.preprocess_stem_fused(32, 720, 1280, 480, 640)
+    assert w.bytes == 32 * (led["fused"] - planar + stem_out) + (16 * 27 + 2 * 16) * 4
+    assert w.flops == 2 * 32 * 240 * 320 * 16 * 27
