@@ -55,7 +55,7 @@ __device__ __forceinline__ int round_u8(float v) { return floor_nonneg(__fadd_rn
 // column dx samples source columns 2dx and 2dx + 1 with weight 1/2 each, so
 // the bilinear row value 0.5 * p0 + 0.5 * p1 is exactly (p0 + p1) / 2; this
 // keeps the integer sum p0 + p1 (as a float) per channel and pixel.
-__device__ __forceinline__ void pair_sums(const uint8_t* row, int g, float (&h)[12]) {
+__device__ __forceinline__ void pair_sums_int(const uint8_t* row, int g, uint32_t (&h)[12]) {
   const uint2* w2 = reinterpret_cast<const uint2*>(row + g * 24);
   uint32_t w[6];
 #pragma unroll
@@ -68,9 +68,41 @@ __device__ __forceinline__ void pair_sums(const uint8_t* row, int g, float (&h)[
 #pragma unroll
     for (int c = 0; c < 3; ++c) {
       const int b0 = q * 6 + c, b1 = q * 6 + 3 + c;  // byte offsets of the two samples
-      const uint32_t sum = __byte_perm(w[b0 >> 2], 0u, 0x4440u | (b0 & 3)) + __byte_perm(w[b1 >> 2], 0u, 0x4440u | (b1 & 3));
-      h[q * 3 + c] = u8_to_float(sum);  // sum <= 510: exact
+      h[q * 3 + c] = __byte_perm(w[b0 >> 2], 0u, 0x4440u | (b0 & 3)) + __byte_perm(w[b1 >> 2], 0u, 0x4440u | (b1 & 3));
     }
+}
+
+__device__ __forceinline__ void pair_sums(const uint8_t* row, int g, float (&h)[12]) {
+  uint32_t s[12];
+  pair_sums_int(row, g, s);
+#pragma unroll
+  for (int i = 0; i < 12; ++i) h[i] = u8_to_float(s[i]);  // sum <= 510: exact
+}
+
+// The u8 codes of 2:1-width samples from the pair sums of the top (ht) and
+// bottom (hb) source rows at vertical weight ay:
+//   u = floor(hbw * ht + haw * hb + 0.5), hbw = (1 - ay) / 2, haw = ay / 2,
+// each fp32 operation rounded.  When ay is a multiple of 2^-14 (the 720 ->
+// 480 ratio gives 1/4 and 3/4) every one of those operations is exact --
+// products of a 9-bit integer and a 15-bit dyadic fraction, and a sum below
+// 256 on a 2^-15 grid, all within fp32's 24 bits -- so the same code comes out
+// of integer arithmetic: u = (hbI * ht + haI * hb + 2^14) >> 15 with
+// haI = ay * 2^14, hbI = 2^14 - haI.  Otherwise the fp32 operations run.
+__device__ __forceinline__ void blend_pairs(const uint8_t* top, const uint8_t* bot, float ay, int (&o)[12]) {
+  uint32_t ht[12], hb[12];
+  pair_sums_int(top, 0, ht);
+  pair_sums_int(bot, 0, hb);
+  const float t = __fmul_rn(ay, 16384.0f);
+  if (t == truncf(t)) {
+    const uint32_t wa = static_cast<uint32_t>(t), wt = 16384u - wa;
+#pragma unroll
+    for (int k = 0; k < 12; ++k) o[k] = static_cast<int>((wt * ht[k] + wa * hb[k] + 16384u) >> 15);
+  } else {
+    const float wt = __fmul_rn(0.5f, __fsub_rn(1.0f, ay)), wb = __fmul_rn(0.5f, ay);
+#pragma unroll
+    for (int k = 0; k < 12; ++k)
+      o[k] = round_u8(__fadd_rn(__fmul_rn(wt, u8_to_float(ht[k])), __fmul_rn(wb, u8_to_float(hb[k]))));
+  }
 }
 
 }  // namespace cb

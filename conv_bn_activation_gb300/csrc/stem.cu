@@ -160,49 +160,39 @@ __device__ __forceinline__ void fill_tile(int t, const StemArgs& a, const float*
     for (int i = threadIdx.x; i < kRows * kChunks; i += kThreads) {
       const int r = i / kChunks, g = i - r * kChunks;
       const int y = p.ih0 + r, xf = p.iw0 + 4 * g;
-      int o[12];  // [pixel q][channel c] u8 codes; -1 = padding (zero)
+      float* d = pl + r * kCols + 4 * g;
       if (y < 0 || y >= a.H) {
 #pragma unroll
-        for (int k = 0; k < 12; ++k) o[k] = -1;
+        for (int c = 0; c < 3; ++c) *reinterpret_cast<float4*>(d + c * kPlane) = make_float4(0.f, 0.f, 0.f, 0.f);
+        continue;
+      }
+      const AxisSample sy = axis_sample(y, a.hs, scale_y);
+      const uint8_t* ra = slots + (sy.i0 - s.r_lo) * a.row_cap;  // byte b of a source row at ra[b - b_lo]
+      const uint8_t* rb = slots + (sy.i1 - s.r_lo) * a.row_cap;
+      if (two_to_one && xf >= 0 && xf + 3 < a.W) {
+        // exact 2:1 width: the horizontal weights are 1/2, folded into the
+        // row weights (as the preprocess kernel does)
+        int o[12];  // [pixel q][channel c]
+        blend_pairs(ra + 6 * xf - s.b_lo, rb + 6 * xf - s.b_lo, sy.a, o);
+#pragma unroll
+        for (int c = 0; c < 3; ++c)
+          *reinterpret_cast<float4*>(d + c * kPlane) =
+              make_float4(inv255[o[c]], inv255[o[3 + c]], inv255[o[6 + c]], inv255[o[9 + c]]);
       } else {
-        const AxisSample sy = axis_sample(y, a.hs, scale_y);
-        const uint8_t* ra = slots + (sy.i0 - s.r_lo) * a.row_cap;  // byte b of a source row at ra[b - b_lo]
-        const uint8_t* rb = slots + (sy.i1 - s.r_lo) * a.row_cap;
-        if (two_to_one && xf >= 0 && xf + 3 < a.W) {
-          // exact 2:1 width: the horizontal weights are 1/2, folded into
-          // the row weights (as the preprocess kernel does)
-          float ht[12], hb[12];
-          pair_sums(ra + 6 * xf - s.b_lo, 0, ht);
-          pair_sums(rb + 6 * xf - s.b_lo, 0, hb);
-          const float wt = __fmul_rn(0.5f, __fsub_rn(1.0f, sy.a)), wb = __fmul_rn(0.5f, sy.a);
+        // other ratios and the image edges, one pixel at a time (kept out of line: code size)
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          const int x = xf + q;
+          const bool in = x >= 0 && x < a.W;
+          const AxisSample sx = axis_sample(in ? x : 0, a.ws, scale_x);
 #pragma unroll
-          for (int k = 0; k < 12; ++k) o[k] = round_u8(__fadd_rn(__fmul_rn(wt, ht[k]), __fmul_rn(wb, hb[k])));
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int x = xf + q;
-            if (x < 0 || x >= a.W) {
-#pragma unroll
-              for (int c = 0; c < 3; ++c) o[q * 3 + c] = -1;
-            } else {
-              const AxisSample sx = axis_sample(x, a.ws, scale_x);
-#pragma unroll
-              for (int c = 0; c < 3; ++c) {
-                const int i0 = 3 * sx.i0 + c - s.b_lo, i1 = 3 * sx.i1 + c - s.b_lo;
-                o[q * 3 + c] = round_u8(bilinear(u8_to_float(ra[i0]), u8_to_float(ra[i1]), u8_to_float(rb[i0]),
-                                                 u8_to_float(rb[i1]), sx.a, sy.a));
-              }
-            }
+          for (int c = 0; c < 3; ++c) {
+            const int i0 = 3 * sx.i0 + c - s.b_lo, i1 = 3 * sx.i1 + c - s.b_lo;
+            const int u = round_u8(bilinear(u8_to_float(ra[i0]), u8_to_float(ra[i1]), u8_to_float(rb[i0]),
+                                             u8_to_float(rb[i1]), sx.a, sy.a));
+            d[c * kPlane + q] = in ? inv255[u] : 0.0f;
           }
         }
-      }
-      float* d = pl + r * kCols + 4 * g;
-#pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        float v[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = o[q * 3 + c] < 0 ? 0.0f : inv255[o[q * 3 + c]];
-        *reinterpret_cast<float4*>(d + c * kPlane) = make_float4(v[0], v[1], v[2], v[3]);
       }
     }
   }
@@ -210,7 +200,7 @@ __device__ __forceinline__ void fill_tile(int t, const StemArgs& a, const float*
 
 // The 2 x 2 output pixels x 16 channels of thread (tx, ty) in tile t, from
 // the staged planes, through the epilogue to memory.
-template <int ACT>
+template <int ACT, bool RES>
 __device__ __forceinline__ void conv_tile(int t, const StemArgs& a, const float* pl, const float* ws,
                                           const float* sc, const float* bi) {
   const TilePos p = tile_pos(t, a);
@@ -269,13 +259,13 @@ __device__ __forceinline__ void conv_tile(int t, const StemArgs& a, const float*
       const int ow = p.ow0 + 2 * tx + q;
       if (ow >= a.OW) continue;
       float* yp = y + oh * a.out.ys_h + ow * a.out.ys_w;
-      const float* rp = a.ep.res_mode ? a.ep.r + p.n * a.ep.rs_n + oh * a.ep.rs_h + ow * a.ep.rs_w : nullptr;
+      const float* rp = RES ? a.ep.r + p.n * a.ep.rs_n + oh * a.ep.rs_h + ow * a.ep.rs_w : nullptr;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float4 s4 = reinterpret_cast<const float4*>(sc)[j], b4 = reinterpret_cast<const float4*>(bi)[j];
         const float2 lo = acc[r][q][2 * j], hi = acc[r][q][2 * j + 1];
         float4 o;
-        if (a.ep.res_mode == 0) {  // uniform
+        if (!RES) {
           o = make_float4(epi_t<ACT, 0>(lo.x, s4.x, b4.x, 0.0f), epi_t<ACT, 0>(lo.y, s4.y, b4.y, 0.0f),
                           epi_t<ACT, 0>(hi.x, s4.z, b4.z, 0.0f), epi_t<ACT, 0>(hi.y, s4.w, b4.w, 0.0f));
         } else {
@@ -329,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, 4) stem_kernel(const StemArgs a) {
       asm volatile("cp.async.commit_group;" ::: "memory");
       asm volatile("cp.async.wait_group 1;" ::: "memory");  // this tile's planes are in place
       __syncthreads();
-      conv_tile<ACT>(tile, a, cur, ws, sc, bi);
+      if (a.ep.res_mode) conv_tile<ACT, true>(tile, a, cur, ws, sc, bi);
+      else conv_tile<ACT, false>(tile, a, cur, ws, sc, bi);
       __syncthreads();  // the copies of a later tile overwrite these planes
     }
   } else {
@@ -343,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 4) stem_kernel(const StemArgs a) {
       const int next = tile + gridDim.x;
       if (next < num_tiles) issue_tile<SRC>(next, a, nullptr, pl1, scale_y, scale_x);
       asm volatile("cp.async.commit_group;" ::: "memory");
-      conv_tile<ACT>(tile, a, pl0, ws, sc, bi);
+      if (SRC != 2 && a.ep.res_mode) conv_tile<ACT, true>(tile, a, pl0, ws, sc, bi);  // frames: no residual
+      else conv_tile<ACT, false>(tile, a, pl0, ws, sc, bi);
     }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");

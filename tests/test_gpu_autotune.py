@@ -97,13 +97,13 @@ def test_autotune_with_residual_and_slice_views(gpu, orc, fresh_table):
 
 
 def test_autotune_single_kernel_layers_record_nothing(gpu, orc, fresh_table):
-    """Depthwise and CUDA-core layers have one kernel: launched once, nothing recorded."""
-    x, w, bn = synthetic.dense_layer(3, 16, 24, N=1, k=3, seed=2)  # stem: direct kernel
+    """Depthwise and other CUDA-core layers have one kernel: launched once, nothing recorded."""
+    x, w, bn = synthetic.dense_layer(3, 16, 24, N=1, k=3, seed=2)  # stem: the stem kernel
     layer = ConvBnAct(w, bn, 2, 1, cb.ACT_SILU)
     OH, OW = layer.out_hw(24, 24)
     y = torch.empty(1, OH, OW, 16, device="cuda")
     xd = to_dev(x)
-    assert cb.conv_path(xd, y, 3, 2, 1) == cb.PATH_DIRECT
+    assert cb.conv_path(xd, y, 3, 2, 1) == cb.PATH_STEM
     layer.autotune(xd, y)
     sync_check()
     assert cb.autotune_entries() == 0
