@@ -366,6 +366,7 @@ struct HaloPlan {
   int px = 0, co = 0;  // tile: px pixels x co output channels
   bool cm = false;     // channel-major accumulator (px = 256, co = 128)
   int nb = 0, grid = 0;
+  int split = 1;       // 2: clusters of two CTAs split each tile's channel chunks
   size_t smem = 0;
 };
 struct ImPlan {        // im2col kernel choices (0 = the cost model's)
@@ -541,15 +542,16 @@ bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
   };
   static const Shape kShapes[] = {{256, 128, true}, {128, 256, false}, {128, 128, false}, {128, 64, false},
                                   {128, 32, false}};
-  // Tuning override (CB_HALO_FORCE = "cm[,stages]" or "co[,stages]"), read per call.
-  int force_co = 0, force_nb = 0;
+  // Tuning override (CB_HALO_FORCE = "cm[,stages[,split]]" or "co[,stages[,split]]";
+  // 0 = free), read per call.
+  int force_co = 0, force_nb = 0, force_split = 0;
   bool force_cm = false;
   if (const char* f = std::getenv("CB_HALO_FORCE")) {
     if (f[0] == 'c' && f[1] == 'm') {
       force_cm = true;
-      if (f[2] == ',') force_nb = std::atoi(f + 3);
+      if (f[2] == ',') std::sscanf(f + 3, "%d,%d", &force_nb, &force_split);
     } else {
-      std::sscanf(f, "%d,%d", &force_co, &force_nb);
+      std::sscanf(f, "%d,%d,%d", &force_co, &force_nb, &force_split);
     }
   }
   double best = 1e300;
@@ -570,23 +572,40 @@ bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
     const long long grid = std::min<long long>(tiles, sms);
     const long long per_cta = (tiles + grid - 1) / grid;
     // Cycles per (tile, chunk): nine taps of four K = 8 MMAs, each about
-    // 111 issue cycles for N <= 128 and 128 for N = 256 (measured), plus the
+    // 120 issue cycles for N <= 128 and 128 for N = 256 (measured), plus the
     // per-tap barrier round trip; against the bytes the copy engine brings
     // in (halo + nine weight slices) at ~64 B per clock per SM when every SM
     // pulls from L2.  Plus the pipeline fill per tile and one exposed epilogue.
     const int n = sh.cm ? sh.px : sh.co;
-    const double mma = 9.0 * (4.0 * (n > 128 ? 128.0 : 111.0) + 100.0);
+    const double mma = 9.0 * (4.0 * (n > 128 ? 128.0 : 120.0) + 100.0);
     const double copy = (hb + 9.0 * sh.co * 128.0) / 64.0;
-    const double cost =
-        static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 1500.0) + sh.px * sh.co / 2.3;
-    if (cost < best * 0.97) {
-      best = cost;
-      plan.px = sh.px;
-      plan.co = sh.co;
-      plan.cm = sh.cm;
-      plan.nb = nb;
-      plan.grid = static_cast<int>(grid);
-      plan.smem = halo_smem_bytes(sh.co, hb, nb);
+    const double epi = sh.px * sh.co / 2.3;
+    const size_t smem = halo_smem_bytes(sh.co, hb, nb);
+    for (int split = 1; split <= 2; ++split) {
+      if (force_split && split != force_split) continue;
+      double cost;
+      if (split == 1) {
+        cost = static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 1500.0) + epi;
+      } else {
+        // one tile per CTA pair, each CTA half of the chunks; the partner's
+        // half accumulator comes over distributed shared memory (~16 B per
+        // clock) and each CTA stores half the tile
+        const size_t recv = halo_split_recv_bytes(sh.px, sh.co, sh.cm);
+        if (num_kc < 2 || (!sh.cm && sh.co < 64) || recv > 2 * static_cast<size_t>(hb) + nb * sh.co * 128ull ||
+            2 * tiles > sms || halo_max_pairs(sh.px, sh.co, sh.cm, smem) < tiles)
+          continue;
+        cost = (num_kc - num_kc / 2) * std::max(mma, copy) + 1500.0 + recv / 16.0 + 1000.0 + epi / 2;
+      }
+      if (cost < best * 0.97) {
+        best = cost;
+        plan.px = sh.px;
+        plan.co = sh.co;
+        plan.cm = sh.cm;
+        plan.nb = nb;
+        plan.split = split;
+        plan.grid = static_cast<int>(split == 2 ? 2 * tiles : grid);
+        plan.smem = smem;
+      }
     }
   }
   if (plan.px == 0) return false;
@@ -667,6 +686,7 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   a.rows = halo_rows(a.Wp, plan.px);
   a.halo_bytes = halo_buffer_bytes(a.Wp, plan.px);
   a.nb_stages = plan.nb;
+  a.split_k = plan.split;
   a.out = make_out(y);
   a.ep = ep;
   a.err = dev->err;
@@ -682,10 +702,10 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   }
   if (std::getenv("CB_DEBUG_PLAN"))
     std::fprintf(stderr,
-                 "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d -> %s px=%d co=%d nb=%d rows=%d halo=%d tiles=%d "
-                 "grid=%d smem=%zu\n",
-                 x->n, a.H, a.W, Ci, Co, plan.cm ? "channel-major" : "pixel-major", plan.px, plan.co, plan.nb, a.rows,
-                 a.halo_bytes, a.m_tiles * a.n_tiles, plan.grid, plan.smem);
+                 "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d -> %s px=%d co=%d nb=%d split=%d rows=%d halo=%d "
+                 "tiles=%d grid=%d smem=%zu\n",
+                 x->n, a.H, a.W, Ci, Co, plan.cm ? "channel-major" : "pixel-major", plan.px, plan.co, plan.nb,
+                 plan.split, a.rows, a.halo_bytes, a.m_tiles * a.n_tiles, plan.grid, plan.smem);
   CUtensorMap xmap, wmap;
   {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(x->w), static_cast<cuuint64_t>(x->h),
@@ -955,6 +975,14 @@ std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int 
         if (tiles >= (1LL << 31)) continue;
         p.halo.grid = static_cast<int>(std::min<long long>(tiles, sms));
         out.push_back(p);
+        // split K over a CTA pair, when every tile gets a pair at once
+        const size_t recv = halo_split_recv_bytes(sh.px, sh.co, sh.cm);
+        if (Ci / 32 >= 2 && (sh.cm || sh.co >= 64) && recv <= 2 * static_cast<size_t>(hb) + nb * sh.co * 128ull &&
+            2 * tiles <= sms && halo_max_pairs(sh.px, sh.co, sh.cm, p.halo.smem) >= tiles) {
+          p.halo.split = 2;
+          p.halo.grid = static_cast<int>(2 * tiles);
+          out.push_back(p);
+        }
       }
     }
   }
@@ -1037,9 +1065,10 @@ cb_status cb_autotune_conv(const cb_tensor* x, const float* w, const float* scal
     g_tuned[key] = best;
   }
   if (std::getenv("CB_DEBUG_PLAN") && found)
-    std::fprintf(stderr, "[cb] autotune: Ci=%d Co=%d %dx%d k=%d s=%d -> path %d (px=%d co=%d nb=%d bn=%d) %.1f us\n",
+    std::fprintf(stderr,
+                 "[cb] autotune: Ci=%d Co=%d %dx%d k=%d s=%d -> path %d (px=%d co=%d nb=%d split=%d bn=%d) %.1f us\n",
                  x->c, y->c, x->h, x->w, kh, stride, static_cast<int>(best.path), best.halo.px, best.halo.co,
-                 best.halo.nb, best.im.bn, 1000.0f * best_ms / kReps);
+                 best.halo.nb, best.halo.split, best.im.bn, 1000.0f * best_ms / kReps);
   // leave y holding the chosen plan's result
   st = launch_conv(x, w, scale, bias, kh, stride, pad, false, act, residual, res_mode, y, s, found ? &best : nullptr);
   if (st != CB_OK) return st;

@@ -1,6 +1,10 @@
 // Host-side sizing and dispatch of the halo-tile implicit GEMM
 // (igemm_halo.cuh).  The pixel-major tiles are instantiated here, the
 // channel-major one in igemm_halo_cm.cu, so that they compile in parallel.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "igemm_halo.cuh"
 #include "launch_util.h"
 
@@ -18,8 +22,10 @@ int halo_buffer_bytes(int wp, int px) {
 size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages) {
   return 1024 /*alignment slack*/ + 2 * static_cast<size_t>(halo_bytes) +
          static_cast<size_t>(nb_stages) * co * kHaloKc * 4 + kHaloStagingBytes +
-         (4 + 2 * nb_stages + 2 * 4) * sizeof(uint64_t) + 16;
+         (4 + 2 * nb_stages + 2 * 4 + 2) * sizeof(uint64_t) + 16;
 }
+
+size_t halo_split_recv_bytes(int px, int co, bool cm) { return static_cast<size_t>(cm ? px : co) / 2 * 128 * 4; }
 
 int igemm_read_trace_halo(unsigned long long* out, int max_records) { return igemm_read_trace_tu(out, max_records); }
 int igemm_read_spans_halo(unsigned long long* out, int max_ctas) { return igemm_read_spans_tu(out, max_ctas); }
@@ -29,7 +35,55 @@ cudaError_t halo_launch(const CUtensorMap& xmap, const CUtensorMap& wmap, const 
                         cudaStream_t s) {
   cudaError_t e = smem_attr_once<igemm_halo_kernel<PX, CO, CM>>(smem);
   if (e != cudaSuccess) return e;
+  if (a.split_k == 2)
+    return launch_pdl_cluster(igemm_halo_kernel<PX, CO, CM>, dim3(grid), dim3(kHaloThreads), smem, s, 2, xmap, wmap,
+                              a);
   return launch_pdl(igemm_halo_kernel<PX, CO, CM>, dim3(grid), dim3(kHaloThreads), smem, s, xmap, wmap, a);
+}
+
+template <int PX, int CO, bool CM>
+int halo_pairs(size_t smem) {
+  if (smem_attr_once<igemm_halo_kernel<PX, CO, CM>>(smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kHaloThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, igemm_halo_kernel<PX, CO, CM>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int halo_max_pairs_cm(size_t smem);
+
+int halo_max_pairs(int px, int co, bool cm, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int, size_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, px, co, cm ? 1 : 0, smem);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int n = 0;
+  if (cm) n = px == 256 && co == 128 ? halo_max_pairs_cm(smem) : 0;
+  else if (px == 128 && co == 64) n = halo_pairs<128, 64, false>(smem);
+  else if (px == 128 && co == 128) n = halo_pairs<128, 128, false>(smem);
+  else if (px == 128 && co == 256) n = halo_pairs<128, 256, false>(smem);
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = n;
+  return n;
 }
 
 cudaError_t launch_igemm_halo_cm(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int grid,
@@ -38,6 +92,15 @@ cudaError_t launch_igemm_halo_cm(const CUtensorMap& xmap, const CUtensorMap& wma
 cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
                               bool cm, int grid, size_t smem, cudaStream_t s) {
   if (a.nb_stages < 2 || a.nb_stages > 16) return cudaErrorInvalidValue;
+  if (a.split_k != 1 && a.split_k != 2) return cudaErrorInvalidValue;
+  if (a.split_k == 2) {
+    // one tile per cluster, a channel-chunk per CTA at least, the partner's
+    // half accumulator within the operand buffers, a shape that splits
+    if (grid != 2 * a.m_tiles * a.n_tiles || a.num_kc < 2 || (!cm && co < 64) ||
+        halo_split_recv_bytes(px, co, cm) > 2 * static_cast<size_t>(a.halo_bytes) +
+                                                static_cast<size_t>(a.nb_stages) * co * kHaloKc * 4)
+      return cudaErrorInvalidValue;
+  }
   if (cm) return px == 256 && co == 128 ? launch_igemm_halo_cm(xmap, wmap, a, grid, smem, s) : cudaErrorInvalidValue;
   if (px != 128) return cudaErrorInvalidValue;
   switch (co) {

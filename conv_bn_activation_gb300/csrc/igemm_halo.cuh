@@ -46,6 +46,17 @@
 //    columns ox >= W and rows past the image masked.  Channel-major tiles are
 //    transposed in the staging buffer (TileStore::stage_columns).
 // CTAs are persistent and stride over the (pixel tile, channel tile) pairs.
+//
+// Split K (split_k = 2, layers with fewer tiles than half the SMs): CTA
+// pairs launched as clusters of two share each tile, CTA r taking half of
+// the 32-channel chunks.  After its MMAs each CTA tells its partner that its
+// operand buffers are free (a remote mbarrier arrive); each then stores the
+// half of its accumulator that the partner finalises into the partner's
+// shared memory (distributed shared memory, over the free buffers), arrives
+// on the partner's data barrier, waits for the partner's half, adds it to
+// its own (fp32, a + b in either CTA) and runs the epilogue on its half of
+// the columns.  Every wait is bounded; a cluster barrier at exit keeps
+// either CTA from leaving while its partner may still write to it.
 #pragma once
 
 #include "internal.h"
@@ -100,7 +111,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   uint64_t* bempty = bfull + a.nb_stages;
   uint64_t* tfull = bempty + a.nb_stages;
   uint64_t* tempty = tfull + NACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + NACC);
+  uint64_t* xfree = tempty + NACC;  // split K: the partner's operand buffers are free
+  uint64_t* xdata = xfree + 1;      // split K: the partner's half accumulator has landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xdata + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -117,6 +130,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], kEpiArrivals);
     }
+    mbar_init(xfree, 1);
+    mbar_init(xdata, 256);  // every epilogue thread of the partner
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -127,6 +142,12 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  const int split = kSplitTiles ? 1 : a.split_k;  // 1, or 2: a cluster of two CTAs per tile
+  if (split == 2) cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
+  const uint32_t rank = split == 2 ? cluster_ctarank() : 0u;
+  const int kc_begin = rank ? a.num_kc / 2 : 0;
+  const int kc_end = (split == 2 && rank == 0) ? a.num_kc / 2 : a.num_kc;
+  const int tile0 = static_cast<int>(blockIdx.x) / split, tile_step = static_cast<int>(gridDim.x) / split;
   // This CTA holds its TMEM: the next kernel may launch (its CTAs cannot
   // take TMEM this one still needs); then wait for the previous kernel.
   pdl_launch_dependents();
@@ -148,12 +169,12 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       uint32_t hphase = 0, bphase = 0, issued = 0, last_parity = 0;
       bool ok = true;
       TraceBuf tr;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
         const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
         const int n_img = m_tile / a.tiles_per_img;
         const int q0 = (m_tile - n_img * a.tiles_per_img) * PX;
         const int y_lo = q0 / a.Wp;
-        for (int kc = 0; ok && kc < a.num_kc; ++kc) {
+        for (int kc = kc_begin; ok && kc < kc_end; ++kc) {
           if (lane == 0) {
             if (!mbar_wait(&hempty[h], hphase ^ 1u, wd)) {
               ok = false;
@@ -206,7 +227,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       bool ok = true;
       int local = 0;
       TraceBuf tr;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+      for (int tile = tile0; ok && tile < num_tiles; tile += tile_step, ++local) {
         const int acc = local % NACC;
         const uint32_t acc_phase = (local / NACC) & 1;
         const int m_tile = tile / a.n_tiles;
@@ -216,7 +237,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wd)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
-        for (int kc = 0; ok && kc < a.num_kc; ++kc) {
+        for (int kc = kc_begin; ok && kc < kc_end; ++kc) {
           if (!mbar_wait(&hfull[h], hphase, wd)) {
             ok = false;
             break;
@@ -237,7 +258,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
             const uint64_t adesc = CM ? wdesc : xdesc, bdesc = CM ? xdesc : wdesc;
 #pragma unroll
             for (int kk = 0; kk < kHaloKc / 8; ++kk)
-              mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kc | tap | kk) != 0 ? 1u : 0u);
+              mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kc != kc_begin || tap || kk) ? 1u : 0u);
             mma_commit(&bempty[s]);
             tr.add(tr_cta);
             const uint32_t bit = 1u << s;
@@ -284,7 +305,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
     int local = 0;
     TraceBuf tr;
     const bool tr_on = tr_cta && warp == 2 && lane == 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = tile0; tile < num_tiles; tile += tile_step, ++local) {
       if (kSplitTiles && (local & 1) != group) continue;
       const int acc = local % NACC;
       const uint32_t acc_phase = (local / NACC) & 1;
@@ -305,6 +326,57 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       tc_fence_after_sync();
       tr.add(tr_on);
       const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
+      if (!kSplitTiles && split == 2) {
+        // One tile per cluster (the host guarantees it): exchange halves.
+        constexpr int kHalf = kAccCols / 2, kHalfChunks = kHalf / 32;
+        float* recv = reinterpret_cast<float*>(smem);  // [kHalf columns][128 lanes], over the halo / weight buffers
+        const uint32_t partner = rank ^ 1u;
+        const int own0 = static_cast<int>(rank) * kHalf, exp0 = kHalf - own0;
+        // every MMA of this CTA is done (tfull): its operand buffers are free
+        if (warp == 2 && lane == 0) mbar_arrive_remote(map_shared_rank(smem_u32(xfree), partner));
+        bool ready = mbar_wait_cluster(xfree, 0, wd);
+        ready = __all_sync(0xffffffffu, ready);
+        if (ready) {
+          const uint32_t rrecv = map_shared_rank(smem_u32(recv), partner);
+          for (int i = group; i < kHalfChunks; i += 2) {
+            uint32_t v[32];
+            tmem_ld_cols<32>(lane_base + exp0 + i * 32, v);
+            tmem_wait_regs(v);
+            const uint32_t dst = rrecv + static_cast<uint32_t>((i * 32 * 128 + q * 32 + lane) * 4);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) st_cluster_u32(dst + static_cast<uint32_t>(j * 128 * 4), v[j]);
+          }
+          mbar_arrive_remote(map_shared_rank(smem_u32(xdata), partner));
+        }
+        bool have = mbar_wait_cluster(xdata, 0, wd);
+        have = __all_sync(0xffffffffu, have);
+        if (!have) break;
+        for (int i = group; i < kHalfChunks; i += 2) {
+          uint32_t v[32];
+          tmem_ld_cols<32>(lane_base + own0 + i * 32, v);
+          tmem_wait_regs(v);
+          const float* rp = recv + i * 32 * 128 + q * 32 + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + rp[j * 128]);
+          long long yoff, roff;
+          __syncwarp();
+          if constexpr (!CM) {
+            pixel_offsets(q0 + q * 32 + lane, yoff, roff);
+            const TileStore<32>::Consts k =
+                TileStore<32>::consts(lane, n_tile * CO + own0 + i * 32, a.Cout, vec, a.ep);
+            TileStore<32>::stage(stage_buf, lane, v);
+            __syncwarp();
+            TileStore<32>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+          } else {
+            pixel_offsets(q0 + own0 + i * 32 + lane, yoff, roff);
+            const TileStore<32>::Consts k = TileStore<32>::consts(lane, n_tile * CO + q * 32, a.Cout, vec, a.ep);
+            TileStore<32>::stage_columns(stage_buf, lane, v);
+            __syncwarp();
+            TileStore<32>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+          }
+        }
+        continue;
+      }
       if constexpr (!CM) {
         // thread = pixel row q0 + 32q + lane; chunks of 32 channels
         // The scale / bias of chunk k + 1 are in flight while chunk k is
@@ -368,6 +440,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
 
   tc_fence_before_sync();
   __syncthreads();
+  if (split == 2) cluster_sync();  // the partner no longer touches this CTA's shared memory
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);

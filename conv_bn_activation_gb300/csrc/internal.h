@@ -106,6 +106,7 @@ struct HaloArgs {
   int rows;            // input rows per halo copy
   int halo_bytes;      // shared-memory bytes of one halo buffer (multiple of 1024)
   int nb_stages;       // weight-slice ring depth
+  int split_k;         // 1, or 2: clusters of two CTAs split each tile's chunks (one tile per cluster)
   int vec_store;       // 1 when y / r rows allow 16-byte vector access
   OutView out;
   Epilogue ep;
@@ -120,6 +121,12 @@ struct HaloArgs {
 int halo_rows(int wp, int px);
 int halo_buffer_bytes(int wp, int px);
 size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages);
+// Shared-memory bytes a split-K CTA receives from its partner (half of one
+// accumulator), which must fit in its halo and weight buffers.
+size_t halo_split_recv_bytes(int px, int co, bool cm);
+// Clusters of two CTAs of this tile shape and shared-memory size that the
+// device runs at once (0 if it cannot run them).
+int halo_max_pairs(int px, int co, bool cm, size_t smem_bytes);
 // px x co tile: 128 x {32, 64, 128, 256} pixel-major, or 256 x 128 channel-major (cm).
 cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
                               bool cm, int grid, size_t smem_bytes, cudaStream_t s);

@@ -185,3 +185,43 @@ def test_halo_channel_major_epilogues_and_views(gpu, orc, halo_force, act, res_m
     ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=act, residual=r if res_mode else None, res_mode=res_mode)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
     assert is_canary(buf[:, :, W:, :]) and is_canary(buf[:, :, :W, :32]) and is_canary(buf[:, :, :W, 32 + Co:])
+
+
+SPLIT_CASES = [
+    # N, H, W, Cin, Cout, CB_HALO_FORCE: one tile per CTA pair, K chunks split between the pair
+    (1, 20, 20, 128, 256, "256,0,2"), (1, 9, 13, 96, 128, "128,0,2"), (2, 5, 7, 64, 64, "64,0,2"),
+    (1, 20, 20, 256, 256, "cm,0,2"), (1, 11, 17, 96, 200, "cm,0,2"), (2, 12, 12, 64, 100, "128,0,2"),
+]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda s: "x".join(map(str, s[:5])) + "-" + s[5])
+def test_halo_split_k(gpu, orc, halo_force, case):
+    """Clusters of two CTAs sharing each tile's channel chunks (odd chunk counts included) and
+    exchanging half accumulators through distributed shared memory."""
+    N, H, W, Ci, Co, force = case
+    halo_force(force)
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=sum(case[:5]))
+    y = _run(x, w, bn)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("force", ["128,0,2", "cm,0,2"])
+@pytest.mark.parametrize("act,res_mode", [(1, 1), (2, 2)])
+def test_halo_split_k_epilogues_and_views(gpu, orc, halo_force, force, act, res_mode):
+    """Split-K tiles into a channel slice of a padded buffer, with a residual: nothing outside
+    the view is written."""
+    halo_force(force)
+    N, H, W, Ci, Co = 1, 10, 18, 64, 128
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=41 + act)
+    r = np.random.default_rng(7).standard_normal((N, H, W, Co)).astype(np.float32)
+    buf = canary_buffer((N, H, W + 3, Co + 40))
+    y = buf[:, :, :W, 8:8 + Co]
+    layer = ConvBnAct(w, bn, 1, 1, act)
+    xd = to_dev(x)
+    assert cb.conv_path(xd, y, 3, 1, 1) in (cb.PATH_TC_HALO, cb.PATH_TC_HALO_CM)
+    layer(xd, y, residual=to_dev(r), res_mode=res_mode)
+    sync_check()
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=act, residual=r, res_mode=res_mode)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+    assert is_canary(buf[:, :, W:, :]) and is_canary(buf[:, :, :W, :8]) and is_canary(buf[:, :, :W, 8 + Co:])
