@@ -329,35 +329,48 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       if (!kSplitTiles && split == 2) {
         // One tile per cluster (the host guarantees it): exchange halves.
         constexpr int kHalf = kAccCols / 2, kHalfChunks = kHalf / 32;
-        float* recv = reinterpret_cast<float*>(smem);  // [kHalf columns][128 lanes], over the halo / weight buffers
+        // [kHalf / 4 column quads][128 lanes][4], over the halo / weight
+        // buffers: each 16-byte store or load of a warp covers 512
+        // contiguous bytes
+        float* recv = reinterpret_cast<float*>(smem);
         const uint32_t partner = rank ^ 1u;
         const int own0 = static_cast<int>(rank) * kHalf, exp0 = kHalf - own0;
         // every MMA of this CTA is done (tfull): its operand buffers are free
         if (warp == 2 && lane == 0) mbar_arrive_remote(map_shared_rank(smem_u32(xfree), partner));
         bool ready = mbar_wait_cluster(xfree, 0, wd);
         ready = __all_sync(0xffffffffu, ready);
+        tr.add(tr_on);
         if (ready) {
           const uint32_t rrecv = map_shared_rank(smem_u32(recv), partner);
           for (int i = group; i < kHalfChunks; i += 2) {
             uint32_t v[32];
             tmem_ld_cols<32>(lane_base + exp0 + i * 32, v);
             tmem_wait_regs(v);
-            const uint32_t dst = rrecv + static_cast<uint32_t>((i * 32 * 128 + q * 32 + lane) * 4);
+            const uint32_t dst = rrecv + static_cast<uint32_t>((i * 8 * 128 + q * 32 + lane) * 16);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) st_cluster_u32(dst + static_cast<uint32_t>(j * 128 * 4), v[j]);
+            for (int j = 0; j < 32; j += 4)
+              st_cluster_v4(dst + static_cast<uint32_t>(j / 4 * 128 * 16), v[j], v[j + 1], v[j + 2], v[j + 3]);
           }
           mbar_arrive_remote(map_shared_rank(smem_u32(xdata), partner));
         }
+        tr.add(tr_on);
         bool have = mbar_wait_cluster(xdata, 0, wd);
         have = __all_sync(0xffffffffu, have);
+        tr.add(tr_on);
         if (!have) break;
         for (int i = group; i < kHalfChunks; i += 2) {
           uint32_t v[32];
           tmem_ld_cols<32>(lane_base + own0 + i * 32, v);
           tmem_wait_regs(v);
-          const float* rp = recv + i * 32 * 128 + q * 32 + lane;
+          const float4* rp = reinterpret_cast<const float4*>(recv) + i * 8 * 128 + q * 32 + lane;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + rp[j * 128]);
+          for (int j = 0; j < 32; j += 4) {
+            const float4 r4 = rp[j / 4 * 128];
+            v[j] = __float_as_uint(__uint_as_float(v[j]) + r4.x);
+            v[j + 1] = __float_as_uint(__uint_as_float(v[j + 1]) + r4.y);
+            v[j + 2] = __float_as_uint(__uint_as_float(v[j + 2]) + r4.z);
+            v[j + 3] = __float_as_uint(__uint_as_float(v[j + 3]) + r4.w);
+          }
           long long yoff, roff;
           __syncwarp();
           if constexpr (!CM) {
@@ -374,6 +387,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
             __syncwarp();
             TileStore<32>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
           }
+          tr.add(tr_on);
         }
         continue;
       }
