@@ -29,7 +29,7 @@ EXPORTED = (
     "cb_get_device_error", "cb_last_cuda_error", "cb_set_kernel_policy", "cb_status_string", "cb_version",
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_layer_uses_tensor_cores",
     "cb_dw_separable_block_static", "cb_conv_path", "cb_debug_timeout_probe", "cb_autotune_conv",
-    "cb_autotune_clear", "cb_autotune_entries", "cb_preprocess_stem_u8",
+    "cb_autotune_clear", "cb_autotune_entries", "cb_preprocess_stem_u8", "cb_dw_separable_block_fused",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
@@ -86,6 +86,7 @@ def load():
                 "cb_autotune_conv": [T, P, P, P, I, I, I, I, I, I, T, I, T, P],
                 "cb_autotune_clear": [],
                 "cb_preprocess_stem_u8": [P, I, I, I, LL, I, I, P, P, P, I, T, P],
+                "cb_dw_separable_block_fused": [T, T, P, P],
                 "cb_autotune_entries": [],
                 "cb_status_string": [I],
                 "cb_version": [],
@@ -246,6 +247,14 @@ def dw_separable_block(x, p, stride, y, workspace, stream=None):
         _stream_ptr(stream))
     _check(st, "cb_dw_separable_block")
     return y
+
+
+def dw_separable_block_fused(x, p, y) -> bool:
+    """cb_dw_separable_block_fused: the block would run as one kernel."""
+    xv, yv = nhwc(x), nhwc(y)
+    sk = p.get("skip_w")
+    return bool(load().cb_dw_separable_block_fused(ctypes.byref(xv), ctypes.byref(yv), p["pw_w"].data_ptr(),
+                                                   sk.data_ptr() if sk is not None else None))
 
 
 def dw_separable_block_static(x, p, stride, y, stream=None):

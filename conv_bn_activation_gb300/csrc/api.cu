@@ -1086,6 +1086,31 @@ int cb_autotune_entries(void) {
   return static_cast<int>(g_tuned.size());
 }
 
+namespace {
+// The one-kernel block (dw_block.cu) takes these shapes and views.  It is
+// chosen where it measured faster than the three layer kernels: blocks with
+// a conv skip (three launches become one) and at least 64 tiles of 128
+// pixels.  Its CTAs gather the depthwise taps from L2 with plain loads, one
+// round trip per pixel and chunk, so with fewer tiles (or only two layer
+// kernels to replace) the TMA-fed layer kernels win.
+// Tuning override: CB_DW_BLOCK_FORCE=1 takes the one kernel wherever its
+// shape rule allows, =0 never (read per call).
+bool dw_block_fusable(const cb_tensor* x, const cb_tensor* y, const float* pw_w, const float* skip_w) {
+  const long long pix = static_cast<long long>(y->n) * y->h * y->w;
+  bool pick = skip_w && (pix + 127) / 128 >= 64;
+  if (const char* f = std::getenv("CB_DW_BLOCK_FORCE")) pick = f[0] == '1';
+  return g_policy.load() == 0 && pick && x->layout == CB_LAYOUT_NHWC && y->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 &&
+         x->c <= 1024 && y->c % 32 == 0 && y->c <= 256 && pix < (1LL << 31) && aligned16(x->data) &&
+         strides_mult4(x) && aligned16(y->data) && strides_mult4(y) && aligned16(pw_w) &&
+         (!skip_w || aligned16(skip_w)) && x->n <= 65535 && encode_tiled();
+}
+}  // namespace
+
+int cb_dw_separable_block_fused(const cb_tensor* x, const cb_tensor* y, const float* pw_w, const float* skip_w) {
+  if (!view_ok(x) || !view_ok(y) || !pw_w) return 0;
+  return dw_block_fusable(x, y, pw_w, skip_w) ? 1 : 0;
+}
+
 cb_status cb_dw_separable_block_workspace(const cb_tensor* x, int c_out, int stride, size_t* bytes) {
   if (!view_ok(x) || !bytes || c_out < 1 || (stride != 1 && stride != 2)) return CB_ERR_INVALID_ARG;
   const long long OH = (x->h + 2 - 3) / stride + 1, OW = (x->w + 2 - 3) / stride + 1;
@@ -1119,6 +1144,57 @@ cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const flo
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CB_ERR_ALIGNMENT;
 
   const long long pix = static_cast<long long>(x->n) * OH * OW;
+  // The whole block in one kernel when the views, weights and channel counts
+  // allow it (policy 0); else three layer calls through the workspace.
+  if (dw_block_fusable(x, y, pw_w, skip_w)) {
+    DeviceInfo* dev = nullptr;
+    st = current_device(&dev);
+    if (st != CB_OK) return st;
+    DwBlockArgs a{};
+    a.x = static_cast<const float*>(x->data);
+    a.xs_n = x->stride_n;
+    a.xs_h = x->stride_h;
+    a.xs_w = x->stride_w;
+    a.N = x->n;
+    a.H = x->h;
+    a.W = x->w;
+    a.Ci = Ci;
+    a.Co = Co;
+    a.OH = OH;
+    a.OW = OW;
+    a.stride = stride;
+    a.M = static_cast<int>(pix);
+    a.dw_w = dw_w;
+    a.dw_scale = dw_scale;
+    a.dw_bias = dw_bias;
+    a.pw_scale = pw_scale;
+    a.pw_bias = pw_bias;
+    a.skip_conv = skip_w ? 1 : 0;
+    a.sk_scale = skip_scale;
+    a.sk_bias = skip_bias;
+    a.num_kc = (Ci + 31) / 32;
+    const int cols = skip_w ? 2 * Co : Co;
+    a.tmem_cols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+    a.out = make_out(y);
+    a.err = dev->err;
+    a.timeout_ns = timeout_ns();
+    if (const char* t = std::getenv("CB_IGEMM_TRACE")) {  // profiling aid: timeline of one CTA
+      a.trace = 1;
+      a.trace_cta = std::atoi(t);
+    }
+    CUtensorMap pw_map, sk_map;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), 1, static_cast<cuuint64_t>(Co)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(Ci) * 4, static_cast<cuuint64_t>(Ci) * 4};
+    cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(Co)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (tiled_map(&pw_map, 3, pw_w, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return CB_ERR_UNSUPPORTED;
+    sk_map = pw_map;
+    if (skip_w && tiled_map(&sk_map, 3, skip_w, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return CB_ERR_UNSUPPORTED;
+    const cudaError_t e = launch_dw_block(pw_map, sk_map, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaErrorInvalidValue) return e == cudaSuccess ? CB_OK : cuda_fail(e);
+  }
   const size_t t_bytes = (static_cast<size_t>(pix) * Ci * sizeof(float) + 255) & ~size_t(255);
   cb_tensor t{workspace, x->n, OH, OW, Ci, static_cast<long long>(OH) * OW * Ci, static_cast<long long>(OW) * Ci,
               Ci, 1, CB_LAYOUT_NHWC};

@@ -131,6 +131,35 @@ int halo_max_pairs(int px, int co, bool cm, size_t smem_bytes);
 cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
                               bool cm, int grid, size_t smem_bytes, cudaStream_t s);
 
+// ------------------------------------------- depthwise-separable block
+// One block in one kernel (dw_block.cu): NHWC fp32 x and y with 16-byte
+// aligned pixels, Ci % 4 == 0, Co % 32 == 0 and Co <= 256; pointwise and
+// skip weights OHWI [Co][Ci] read by TMA (maps of dims (Ci, 1, Co), box
+// (32, 1, Co), 128-byte swizzle).
+struct DwBlockArgs {
+  const float* x;
+  long long xs_n, xs_h, xs_w;
+  int N, H, W, Ci, Co, OH, OW, stride, M;
+  const float* dw_w;       // [9][Ci]
+  const float* dw_scale;
+  const float* dw_bias;
+  const float* pw_scale;
+  const float* pw_bias;
+  const float* sk_scale;   // skip conv only
+  const float* sk_bias;
+  int skip_conv;           // 1: 1x1 conv skip (second accumulator); 0: identity
+  int num_kc;              // ceil(Ci / 32)
+  uint32_t tmem_cols;      // power of two >= Co (x 2 with a conv skip)
+  OutView out;
+  int* err;
+  uint64_t timeout_ns;
+  int trace;           // 1: record the pipeline timeline of CTA trace_cta (profiling aid)
+  int trace_cta;
+};
+size_t dw_block_smem_bytes(int ci, int co);
+cudaError_t launch_dw_block(const CUtensorMap& pw_map, const CUtensorMap& sk_map, const DwBlockArgs& a,
+                            cudaStream_t s);
+
 // ------------------------------------------------------------------- stem
 // 3 -> 16 channels, 3x3, stride 2, pad 1, CUDA cores (stem.cu).  Input:
 // planar fp32 (src_kind 0: x[n*xs_n + c*xs_c + h*xs_h + w]), packed NHWC

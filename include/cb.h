@@ -166,6 +166,22 @@ cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const flo
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * 1 if cb_dw_separable_block with these views and (DEVICE) pointwise / skip
+ * weights runs as one kernel under the current policy, else 0 (it then runs
+ * the depthwise, skip and pointwise layers through the workspace).  The one
+ * kernel needs policy 0, NHWC x and y with 16-byte aligned data and strides
+ * that are multiples of 4 elements, Ci % 4 == 0 and Ci <= 1024, Co % 32 == 0
+ * and Co <= 256, and 16-byte aligned pointwise / skip weights; it is chosen
+ * for blocks with a conv skip and at least 64 tiles of 128 output pixels,
+ * where it measured faster than the layer kernels.  It keeps the
+ * depthwise output in shared memory as the A operand of the pointwise MMAs
+ * (TF32, like the tensor-core layers: the depthwise output and the block
+ * output are rounded to the nearest TF32 value; a conv skip adds its fp32
+ * accumulator).  Host only; launches nothing.
+ */
+int cb_dw_separable_block_fused(const cb_tensor* x, const cb_tensor* y, const float* pw_w, const float* skip_w);
+
+/*
  * Size of the fixed scratch array behind cb_dw_separable_block_static.
  */
 #define CB_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
