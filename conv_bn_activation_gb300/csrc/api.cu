@@ -367,10 +367,13 @@ struct HaloPlan {
   bool cm = false;     // channel-major accumulator (px = 256, co = 128)
   int nb = 0, grid = 0;
   int split = 1;       // 2: clusters of two CTAs split each tile's channel chunks
+  int tps = 1;         // filter taps per weight-ring stage (one copy per stage)
+  int kc = 32;         // input channels per chunk (32, or 16 for Ci % 32 == 16)
   size_t smem = 0;
 };
 struct ImPlan {        // im2col kernel choices (0 = the cost model's)
   int bn = 0, stages = 0;
+  int blocks = 0;      // 1: 128 consecutive pixels (im2col copies); 2: pixel blocks (tiled copies)
 };
 bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out);
 
@@ -421,6 +424,25 @@ bool tuned_plan(const ConvKey& k, ConvPlan* out) {
 // for the shape, when the tuner made one, else the cost models').
 cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan,
                    ImPlan* im = nullptr);
+
+// Pixel blocks of bw x bh = 128 output pixels for the tiled-copy A operand:
+// the shape that covers OH x OW with the fewest wasted rows (*waste = covered
+// / real pixels); stride * bw and stride * bh stay within a copy box (256).
+void pick_blocks(int OH, int OW, int stride, int* bw_out, int* bh_out, double* waste) {
+  double best = 1e300;
+  for (int bw = 128; bw >= 1; bw >>= 1) {
+    const int bh = 128 / bw;
+    if (stride * bw > 256 || stride * bh > 256) continue;
+    const double cov = static_cast<double>((OW + bw - 1) / bw) * bw * static_cast<double>((OH + bh - 1) / bh) * bh;
+    const double w = cov / (static_cast<double>(OW) * OH);
+    if (w < best - 1e-9) {
+      best = w;
+      *bw_out = bw;
+      *bh_out = bh;
+    }
+  }
+  *waste = best;
+}
 
 int pick_bn(int M, int Cout, int k_iters, int sms, int* n_tiles_out) {
   static const int kBn[] = {16, 32, 48, 64, 96, 128, 192, 256};
@@ -487,7 +509,28 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
     bn = force_bn;
     n_tiles = (Co + bn - 1) / bn;
   }
-  a.m_tiles = (a.M + 127) / 128;
+  // Pixel blocks (tiled copies, ~1 row per clock) unless they would waste
+  // more than 15 % of the tile rows on the image edges; then 128 consecutive
+  // pixels gathered in im2col mode.  CB_IGEMM_BLOCKS=0/1 overrides (per call).
+  int bw = 0, bh = 0;
+  double waste = 1e300;
+  pick_blocks(y->h, y->w, stride, &bw, &bh, &waste);
+  int blocks = im.blocks;
+  if (blocks == 0) {
+    blocks = waste <= 1.15 ? 2 : 1;
+    if (const char* f = std::getenv("CB_IGEMM_BLOCKS")) blocks = f[0] == '1' ? 2 : 1;
+  }
+  if (blocks == 2 && bw > 0) {
+    a.blk_w = bw;
+    a.blk_h = bh;
+    a.blocks_x = (y->w + bw - 1) / bw;
+    a.blocks_y = (y->h + bh - 1) / bh;
+    const long long mt = static_cast<long long>(x->n) * a.blocks_x * a.blocks_y;
+    if (mt >= (1LL << 31)) return CB_ERR_UNSUPPORTED;
+    a.m_tiles = static_cast<int>(mt);
+  } else {
+    a.m_tiles = (a.M + 127) / 128;
+  }
   a.n_tiles = n_tiles;
   a.stages = igemm_stages(bn, kc);
   if (force_stages >= 2 && igemm_smem_bytes(bn, kc, force_stages) <= 227 * 1024) a.stages = force_stages;
@@ -496,8 +539,10 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
   int grid = static_cast<int>(std::min<long long>(tiles, dev->sms));
   if (force_grid > 0 && force_grid < grid) grid = force_grid;
   if (std::getenv("CB_DEBUG_PLAN"))
-    std::fprintf(stderr, "[cb] igemm plan: M=%d Ci=%d Co=%d k=%d s=%d -> bn=%d kc=%d n_tiles=%d m_tiles=%d stages=%d grid=%d\n",
-                 a.M, Ci, Co, k, stride, bn, kc, n_tiles, a.m_tiles, a.stages, grid);
+    std::fprintf(stderr,
+                 "[cb] igemm plan: M=%d Ci=%d Co=%d k=%d s=%d -> bn=%d kc=%d n_tiles=%d m_tiles=%d stages=%d grid=%d "
+                 "blocks=%dx%d\n",
+                 a.M, Ci, Co, k, stride, bn, kc, n_tiles, a.m_tiles, a.stages, grid, a.blk_h, a.blk_w);
 
   CUtensorMap amap, bmap;
   {
@@ -511,7 +556,14 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
     const CUtensorMapSwizzle swz = kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
                                               : CU_TENSOR_MAP_SWIZZLE_32B;
-    CUresult r = im2col_map(&amap, x->data, dims, strides, lower, upper, static_cast<cuuint32_t>(kc), 128, estr, swz);
+    CUresult r;
+    if (a.blk_w) {
+      cuuint32_t box[4] = {static_cast<cuuint32_t>(kc), static_cast<cuuint32_t>(stride * a.blk_w),
+                           static_cast<cuuint32_t>(stride * a.blk_h), 1};
+      r = tiled_map(&amap, 4, x->data, dims, strides, box, estr, swz);
+    } else {
+      r = im2col_map(&amap, x->data, dims, strides, lower, upper, static_cast<cuuint32_t>(kc), 128, estr, swz);
+    }
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   {
@@ -531,27 +583,49 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
 
 // 3x3 stride-1 pad-1 layers with Cin % 32 == 0 and an image width whose
 // halo tile leaves room for a weight ring: the halo-tile kernel.
-bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
-  if (Ci % 32 != 0 || W + 2 > 256) return false;
-  const int wp = W + 2;
-  const int num_kc = Ci / 32;
+// Weight ring of a halo tile shape: the most filter taps per stage (9, 3 or
+// 1) that leaves at least two stages (three for single taps) in shared memory.
+// An SM completes about one copy per 400-700 cycles whatever its size up to
+// ~48 KB (measured), so fewer, larger weight copies keep the MMAs fed.
+bool halo_ring(int co, int hb, int force_nb, int force_tps, int* nb_out, int* tps_out, int kc = 32) {
   constexpr size_t kSmemMax = 227 * 1024;
+  for (int tps : {9, 3, 1}) {
+    if (force_tps && tps != force_tps) continue;
+    const int nb_max = force_nb >= 2 ? std::min(force_nb, 16) : (tps == 1 ? 8 : 4);
+    int nb = nb_max;
+    while (nb >= 2 && halo_smem_bytes(co, hb, nb, tps, kc) > kSmemMax) --nb;
+    if (nb >= ((force_nb >= 2 || tps > 1) ? 2 : 3)) {
+      *nb_out = nb;
+      *tps_out = tps;
+      return true;
+    }
+  }
+  return false;
+}
+
+bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
+  // 32-channel chunks (128-byte rows); layers with Ci % 32 == 16 take 16-channel
+  // chunks (64-byte rows) in the pixel-major 128 x {32, 64} tiles
+  const int kc = Ci % 32 == 0 ? 32 : (Ci % 16 == 0 ? 16 : 0);
+  if (kc == 0 || W + 2 > 256) return false;
+  const int wp = W + 2;
+  const int num_kc = Ci / kc;
   struct Shape {
     int px, co;
     bool cm;
   };
   static const Shape kShapes[] = {{256, 128, true}, {128, 256, false}, {128, 128, false}, {128, 64, false},
                                   {128, 32, false}};
-  // Tuning override (CB_HALO_FORCE = "cm[,stages[,split]]" or "co[,stages[,split]]";
-  // 0 = free), read per call.
-  int force_co = 0, force_nb = 0, force_split = 0;
+  // Tuning override (CB_HALO_FORCE = "cm[,stages[,split[,taps]]]" or
+  // "co[,stages[,split[,taps]]]"; 0 = free), read per call.
+  int force_co = 0, force_nb = 0, force_split = 0, force_tps = 0;
   bool force_cm = false;
   if (const char* f = std::getenv("CB_HALO_FORCE")) {
     if (f[0] == 'c' && f[1] == 'm') {
       force_cm = true;
-      if (f[2] == ',') std::sscanf(f + 3, "%d,%d", &force_nb, &force_split);
+      if (f[2] == ',') std::sscanf(f + 3, "%d,%d,%d", &force_nb, &force_split, &force_tps);
     } else {
-      std::sscanf(f, "%d,%d,%d", &force_co, &force_nb, &force_split);
+      std::sscanf(f, "%d,%d,%d,%d", &force_co, &force_nb, &force_split, &force_tps);
     }
   }
   double best = 1e300;
@@ -559,13 +633,12 @@ bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
   for (const Shape& sh : kShapes) {
     if (force_cm && !sh.cm) continue;
     if (force_co && (sh.cm || sh.co != force_co)) continue;
+    if (kc == 16 && (sh.cm || sh.co > 64)) continue;
     const int rows = halo_rows(wp, sh.px);
     if (rows > 256) continue;
-    const int hb = halo_buffer_bytes(wp, sh.px);
-    const int nb_max = force_nb >= 2 ? std::min(force_nb, 16) : 8;
-    int nb = nb_max;
-    while (nb >= 2 && halo_smem_bytes(sh.co, hb, nb) > kSmemMax) --nb;
-    if (nb < (force_nb >= 2 ? 2 : 3)) continue;
+    const int hb = halo_buffer_bytes(wp, sh.px, kc);
+    int nb = 0, tps = 1;
+    if (!halo_ring(sh.co, hb, force_nb, force_tps, &nb, &tps, kc)) continue;
     const long long m_tiles = static_cast<long long>(N) * ((H * wp + sh.px - 1) / sh.px);
     const long long tiles = m_tiles * ((Co + sh.co - 1) / sh.co);
     if (tiles >= (1LL << 31)) continue;
@@ -577,10 +650,10 @@ bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
     // in (halo + nine weight slices) at ~64 B per clock per SM when every SM
     // pulls from L2.  Plus the pipeline fill per tile and one exposed epilogue.
     const int n = sh.cm ? sh.px : sh.co;
-    const double mma = 9.0 * (4.0 * (n > 128 ? 128.0 : 120.0) + 100.0);
-    const double copy = (hb + 9.0 * sh.co * 128.0) / 64.0;
+    const double mma = 9.0 * (kc / 8) * (n > 128 ? 128.0 : 120.0) + (9.0 / tps) * 100.0;
+    const double copy = (1.0 + 9.0 / tps) * 550.0;  // one halo copy and 9 / tps weight copies
     const double epi = sh.px * sh.co / 2.3;
-    const size_t smem = halo_smem_bytes(sh.co, hb, nb);
+    const size_t smem = halo_smem_bytes(sh.co, hb, nb, tps, kc);
     for (int split = 1; split <= 2; ++split) {
       if (force_split && split != force_split) continue;
       double cost;
@@ -591,7 +664,8 @@ bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
         // half accumulator comes over distributed shared memory (~16 B per
         // clock) and each CTA stores half the tile
         const size_t recv = halo_split_recv_bytes(sh.px, sh.co, sh.cm);
-        if (num_kc < 2 || (!sh.cm && sh.co < 64) || recv > 2 * static_cast<size_t>(hb) + nb * sh.co * 128ull ||
+        if (kc != 32 || num_kc < 2 || (!sh.cm && sh.co < 64) ||
+            recv > 2 * static_cast<size_t>(hb) + nb * tps * sh.co * 128ull ||
             2 * tiles > sms || halo_max_pairs(sh.px, sh.co, sh.cm, smem) < tiles)
           continue;
         cost = (num_kc - num_kc / 2) * std::max(mma, copy) + 1500.0 + recv / 16.0 + 1000.0 + epi / 2;
@@ -602,6 +676,8 @@ bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
         plan.co = sh.co;
         plan.cm = sh.cm;
         plan.nb = nb;
+        plan.tps = tps;
+        plan.kc = kc;
         plan.split = split;
         plan.grid = static_cast<int>(split == 2 ? 2 * tiles : grid);
         plan.smem = smem;
@@ -679,13 +755,15 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   a.W = x->w;
   a.Wp = x->w + 2;
   a.Cout = Co;
-  a.num_kc = Ci / 32;
+  a.kc = plan.kc;
+  a.num_kc = Ci / plan.kc;
   a.tiles_per_img = (a.H * a.Wp + plan.px - 1) / plan.px;
   a.m_tiles = x->n * a.tiles_per_img;
   a.n_tiles = (Co + plan.co - 1) / plan.co;
   a.rows = halo_rows(a.Wp, plan.px);
-  a.halo_bytes = halo_buffer_bytes(a.Wp, plan.px);
+  a.halo_bytes = halo_buffer_bytes(a.Wp, plan.px, plan.kc);
   a.nb_stages = plan.nb;
+  a.taps_per_stage = plan.tps;
   a.split_k = plan.split;
   a.out = make_out(y);
   a.ep = ep;
@@ -702,27 +780,33 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   }
   if (std::getenv("CB_DEBUG_PLAN"))
     std::fprintf(stderr,
-                 "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d -> %s px=%d co=%d nb=%d split=%d rows=%d halo=%d "
-                 "tiles=%d grid=%d smem=%zu\n",
+                 "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d -> %s px=%d co=%d nb=%d tps=%d split=%d rows=%d "
+                 "halo=%d tiles=%d grid=%d smem=%zu\n",
                  x->n, a.H, a.W, Ci, Co, plan.cm ? "channel-major" : "pixel-major", plan.px, plan.co, plan.nb,
-                 plan.split, a.rows, a.halo_bytes, a.m_tiles * a.n_tiles, plan.grid, plan.smem);
+                 plan.tps, plan.split, a.rows, a.halo_bytes, a.m_tiles * a.n_tiles, plan.grid, plan.smem);
   CUtensorMap xmap, wmap;
   {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(x->w), static_cast<cuuint64_t>(x->h),
                           static_cast<cuuint64_t>(x->n)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(x->stride_w) * 4, static_cast<cuuint64_t>(x->stride_h) * 4,
                              static_cast<cuuint64_t>(x->stride_n) * 4};
-    cuuint32_t box[4] = {32, static_cast<cuuint32_t>(a.Wp), static_cast<cuuint32_t>(a.rows), 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(plan.kc), static_cast<cuuint32_t>(a.Wp),
+                         static_cast<cuuint32_t>(a.rows), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = tiled_map(&xmap, 4, x->data, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
+    CUresult r = tiled_map(&xmap, 4, x->data, dims, strides, box, estr,
+                           plan.kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), 9, static_cast<cuuint64_t>(Co)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(Ci) * 4, static_cast<cuuint64_t>(9) * Ci * 4};
-    cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(plan.co)};
+    // OHWI weights viewed as (Ci, Co, tap): a box of plan.tps taps lands as
+    // plan.tps consecutive [co x 32] slices
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(Co), 9};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(9) * Ci * 4, static_cast<cuuint64_t>(Ci) * 4};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(plan.kc), static_cast<cuuint32_t>(plan.co),
+                         static_cast<cuuint32_t>(plan.tps)};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = tiled_map(&wmap, 3, w, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B);
+    CUresult r = tiled_map(&wmap, 3, w, dims, strides, box, estr,
+                           plan.kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   cudaError_t e = launch_igemm_halo(xmap, wmap, a, plan.px, plan.co, plan.cm, plan.grid, plan.smem, s);
@@ -947,7 +1031,8 @@ cb_status launch_conv(const cb_tensor* x, const float* w, const float* scale, co
 std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, int sms) {
   std::vector<ConvPlan> out;
   const int Ci = x->c, Co = y->c;
-  if (kh == 3 && stride == 1 && pad == 1 && Ci % 32 == 0 && x->w + 2 <= 256 && g_policy.load() == 0) {
+  const int hkc = Ci % 32 == 0 ? 32 : (Ci % 16 == 0 ? 16 : 0);
+  if (kh == 3 && stride == 1 && pad == 1 && hkc && x->w + 2 <= 256 && g_policy.load() == 0) {
     const int wp = x->w + 2;
     struct Shape {
       int px, co;
@@ -957,19 +1042,21 @@ std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int 
                                     {128, 32, false}};
     for (const Shape& sh : kShapes) {
       if (!sh.cm && sh.co > 2 * ((Co + 15) / 16 * 16)) continue;  // a tile mostly beyond Co
-      const int hb = halo_buffer_bytes(wp, sh.px);
+      if (hkc == 16 && (sh.cm || sh.co > 64)) continue;
+      const int hb = halo_buffer_bytes(wp, sh.px, hkc);
       if (halo_rows(wp, sh.px) > 256) continue;
-      int nb_max = 8;
-      while (nb_max >= 2 && halo_smem_bytes(sh.co, hb, nb_max) > 227 * 1024) --nb_max;
-      for (int nb : {nb_max, 3}) {
-        if (nb < 2 || nb > nb_max || (nb == 3 && nb_max == 3)) continue;
+      for (int tps : {9, 3, 1}) {
+        int nb = 0, t = 0;
+        if (!halo_ring(sh.co, hb, 0, tps, &nb, &t, hkc)) continue;
         ConvPlan p;
         p.path = sh.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
         p.halo.px = sh.px;
         p.halo.co = sh.co;
         p.halo.cm = sh.cm;
         p.halo.nb = nb;
-        p.halo.smem = halo_smem_bytes(sh.co, hb, nb);
+        p.halo.tps = tps;
+        p.halo.kc = hkc;
+        p.halo.smem = halo_smem_bytes(sh.co, hb, nb, tps, hkc);
         const long long tiles = static_cast<long long>(x->n) * ((x->h * wp + sh.px - 1) / sh.px) *
                                 ((Co + sh.co - 1) / sh.co);
         if (tiles >= (1LL << 31)) continue;
@@ -977,7 +1064,8 @@ std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int 
         out.push_back(p);
         // split K over a CTA pair, when every tile gets a pair at once
         const size_t recv = halo_split_recv_bytes(sh.px, sh.co, sh.cm);
-        if (Ci / 32 >= 2 && (sh.cm || sh.co >= 64) && recv <= 2 * static_cast<size_t>(hb) + nb * sh.co * 128ull &&
+        if (hkc == 32 && Ci / 32 >= 2 && (sh.cm || sh.co >= 64) &&
+            recv <= 2 * static_cast<size_t>(hb) + nb * tps * sh.co * 128ull &&
             2 * tiles <= sms && halo_max_pairs(sh.px, sh.co, sh.cm, p.halo.smem) >= tiles) {
           p.halo.split = 2;
           p.halo.grid = static_cast<int>(2 * tiles);

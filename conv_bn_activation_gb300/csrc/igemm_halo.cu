@@ -14,14 +14,14 @@ namespace cb {
 // (px - 1) / Wp + 2 output rows, plus one halo row above and below.
 int halo_rows(int wp, int px) { return (px - 1) / wp + 4; }
 
-int halo_buffer_bytes(int wp, int px) {
-  const int bytes = (halo_rows(wp, px) * wp + 8) * kHaloKc * 4;
+int halo_buffer_bytes(int wp, int px, int kc) {
+  const int bytes = (halo_rows(wp, px) * wp + 8) * kc * 4;
   return (bytes + 1023) / 1024 * 1024;
 }
 
-size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages) {
+size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages, int taps_per_stage, int kc) {
   return 1024 /*alignment slack*/ + 2 * static_cast<size_t>(halo_bytes) +
-         static_cast<size_t>(nb_stages) * co * kHaloKc * 4 + kHaloStagingBytes +
+         static_cast<size_t>(nb_stages) * taps_per_stage * co * kc * 4 + kHaloStagingBytes +
          (4 + 2 * nb_stages + 2 * 4 + 2) * sizeof(uint64_t) + 16;
 }
 
@@ -88,19 +88,24 @@ int halo_max_pairs(int px, int co, bool cm, size_t smem) {
 
 cudaError_t launch_igemm_halo_cm(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int grid,
                                  size_t smem, cudaStream_t s);
+cudaError_t launch_igemm_halo_kc16(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int co,
+                                   int grid, size_t smem, cudaStream_t s);
 
 cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
                               bool cm, int grid, size_t smem, cudaStream_t s) {
   if (a.nb_stages < 2 || a.nb_stages > 16) return cudaErrorInvalidValue;
+  if (a.taps_per_stage != 1 && a.taps_per_stage != 3 && a.taps_per_stage != 9) return cudaErrorInvalidValue;
   if (a.split_k != 1 && a.split_k != 2) return cudaErrorInvalidValue;
   if (a.split_k == 2) {
     // one tile per cluster, a channel-chunk per CTA at least, the partner's
     // half accumulator within the operand buffers, a shape that splits
     if (grid != 2 * a.m_tiles * a.n_tiles || a.num_kc < 2 || (!cm && co < 64) ||
         halo_split_recv_bytes(px, co, cm) > 2 * static_cast<size_t>(a.halo_bytes) +
-                                                static_cast<size_t>(a.nb_stages) * co * kHaloKc * 4)
+                                                static_cast<size_t>(a.nb_stages) * a.taps_per_stage * co * a.kc * 4)
       return cudaErrorInvalidValue;
   }
+  if (a.kc == 16) return !cm && px == 128 ? launch_igemm_halo_kc16(xmap, wmap, a, co, grid, smem, s) : cudaErrorInvalidValue;
+  if (a.kc != 32) return cudaErrorInvalidValue;
   if (cm) return px == 256 && co == 128 ? launch_igemm_halo_cm(xmap, wmap, a, grid, smem, s) : cudaErrorInvalidValue;
   if (px != 128) return cudaErrorInvalidValue;
   switch (co) {

@@ -67,7 +67,7 @@
 namespace cb {
 
 constexpr int kHaloThreads = 320;
-constexpr int kHaloKc = 32;              // input channels per K chunk (128-byte rows)
+constexpr int kHaloKc = 32;              // input channels per K chunk (128-byte rows), or KC = 16 (64-byte rows)
 constexpr int kHaloStagingBytes = 8 * TileStore<32>::kBufBytes;  // 8 epilogue warps x 4 KB
 
 // TMEM accumulators per CTA (the epilogue of one tile overlaps the MMAs of
@@ -78,17 +78,21 @@ __host__ __device__ constexpr int halo_tmem_cols(int acc_cols) {
   return halo_naccs(acc_cols) * acc_cols <= 128 ? 128 : halo_naccs(acc_cols) * acc_cols <= 256 ? 256 : 512;
 }
 
-template <int PX, int CO, bool CM>
+template <int PX, int CO, bool CM, int KC = kHaloKc>
 __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                      const __grid_constant__ CUtensorMap wmap,
                                                                      const HaloArgs a) {
+  static_assert(KC == 32 || KC == 16, "channels per chunk");
+  constexpr int kRowBytes = KC * 4;  // one pixel's chunk: 128 or 64 bytes, swizzled to match
   static_assert(CM ? (PX == 256 && CO == 128) : (PX == 128 && (CO == 32 || CO == 64 || CO == 128 || CO == 256)),
                 "tile shape");
   const unsigned long long t_start = a.trace ? trace_globaltimer() : 0;
   constexpr int kAccCols = CM ? PX : CO;  // TMEM columns of one accumulator
   constexpr int NACC = halo_naccs(kAccCols);
   constexpr uint32_t kTmemCols = halo_tmem_cols(kAccCols);
-  constexpr int kBBytes = CO * kHaloKc * 4;  // one tap's weight slice
+  constexpr int kTapBytes = CO * KC * 4;  // one tap's weight slice
+  const int tps = a.taps_per_stage;            // taps per weight-ring stage: 1, 3 or 9 (one copy each)
+  const int kBBytes = tps * kTapBytes;
   constexpr uint32_t kIdesc = CM ? idesc_tf32(CO, PX) : idesc_tf32(PX, CO);
   // Epilogue split of a tile between the two groups of four warps:
   // pixel-major tiles of 32 channels alternate between the groups, wider
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{a.err, abort_flag, a.timeout_ns};
   const int num_tiles = a.m_tiles * a.n_tiles;
-  const uint32_t halo_tx = static_cast<uint32_t>(kHaloKc * 4 * a.Wp * a.rows);
+  const uint32_t halo_tx = static_cast<uint32_t>(kRowBytes * a.Wp * a.rows);
   const bool tr_cta = a.trace && blockIdx.x == a.trace_cta;
 
   if (warp == 0) {
@@ -181,7 +185,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
               break;
             }
             mbar_arrive_expect_tx(&hfull[h], halo_tx);
-            tma_load_4d(sHalo + h * a.halo_bytes, &xmap, &hfull[h], kc * kHaloKc, -1, y_lo - 1, n_img);
+            tma_load_4d(sHalo + h * a.halo_bytes, &xmap, &hfull[h], kc * KC, -1, y_lo - 1, n_img);
             issued |= 1u << h;
             last_parity = (last_parity & ~(1u << h)) | (hphase << h);
           }
@@ -189,14 +193,15 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
             h = 0;
             hphase ^= 1u;
           }
-          for (int tap = 0; tap < 9; ++tap) {
+          for (int tap = 0; tap < 9; tap += tps) {
             if (lane != 0 && s % kBLanes == lane - 1) {
               if (!mbar_wait(&bempty[s], bphase ^ 1u, wd)) {
                 ok = false;
                 break;
               }
               mbar_arrive_expect_tx(&bfull[s], static_cast<uint32_t>(kBBytes));
-              tma_load_3d(sB + s * kBBytes, &wmap, &bfull[s], kc * kHaloKc, tap, n_tile * CO);
+              // weights viewed as (Ci, Co, tap): one box of tps taps lands as tps [CO x 32] slices
+              tma_load_3d(sB + s * kBBytes, &wmap, &bfull[s], kc * KC, n_tile * CO, tap);
               tr.add(tr_cta && lane == 1);
               issued |= 1u << s;
               last_parity = (last_parity & ~(1u << s)) | (bphase << s);
@@ -244,21 +249,24 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
           }
           tc_fence_after_sync();
           const uint32_t halo_addr = smem_u32(sHalo + h * a.halo_bytes);
-          for (int tap = 0; tap < 9; ++tap) {
-            const int dy = tap / 3, dx = tap - 3 * (tap / 3);
+          for (int tap0 = 0; tap0 < 9; tap0 += tps) {
             if (!mbar_wait(&bfull[s], bphase, wd)) {
               ok = false;
               break;
             }
             tr.add(tr_cta);
             tc_fence_after_sync();
-            const uint32_t x_addr = halo_addr + static_cast<uint32_t>((base_row + dy * a.Wp + dx) * 128);
-            const uint64_t xdesc = kmajor_swizzled_desc(x_addr, 128);
-            const uint64_t wdesc = kmajor_swizzled_desc(smem_u32(sB + s * kBBytes), 128);
-            const uint64_t adesc = CM ? wdesc : xdesc, bdesc = CM ? xdesc : wdesc;
+            for (int t = 0; t < tps; ++t) {
+              const int tap = tap0 + t;
+              const int dy = tap / 3, dx = tap - 3 * (tap / 3);
+              const uint32_t x_addr = halo_addr + static_cast<uint32_t>((base_row + dy * a.Wp + dx) * kRowBytes);
+              const uint64_t xdesc = kmajor_swizzled_desc(x_addr, kRowBytes);
+              const uint64_t wdesc = kmajor_swizzled_desc(smem_u32(sB + s * kBBytes + t * kTapBytes), kRowBytes);
+              const uint64_t adesc = CM ? wdesc : xdesc, bdesc = CM ? xdesc : wdesc;
 #pragma unroll
-            for (int kk = 0; kk < kHaloKc / 8; ++kk)
-              mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kc != kc_begin || tap || kk) ? 1u : 0u);
+              for (int kk = 0; kk < KC / 8; ++kk)
+                mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kc != kc_begin || tap || kk) ? 1u : 0u);
+            }
             mma_commit(&bempty[s]);
             tr.add(tr_cta);
             const uint32_t bit = 1u << s;

@@ -1,0 +1,29 @@
+// The 16-channel-chunk instantiations of the halo-tile implicit GEMM
+// (igemm_halo.cuh): layers whose input channels are a multiple of 16 but not
+// of 32 (64-byte pixel rows, 64-byte swizzle), pixel-major 128 x {32, 64}.
+#include "igemm_halo.cuh"
+#include "launch_util.h"
+
+namespace cb {
+
+int igemm_read_trace_halo_kc16(unsigned long long* out, int max_records) {
+  return igemm_read_trace_tu(out, max_records);
+}
+
+template <int CO>
+static cudaError_t launch_co(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int grid,
+                             size_t smem, cudaStream_t s) {
+  cudaError_t e = smem_attr_once<igemm_halo_kernel<128, CO, false, 16>>(smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(igemm_halo_kernel<128, CO, false, 16>, dim3(grid), dim3(kHaloThreads), smem, s, xmap, wmap, a);
+}
+
+cudaError_t launch_igemm_halo_kc16(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int co,
+                                   int grid, size_t smem, cudaStream_t s) {
+  if (a.split_k != 1) return cudaErrorInvalidValue;
+  if (co == 32) return launch_co<32>(xmap, wmap, a, grid, smem, s);
+  if (co == 64) return launch_co<64>(xmap, wmap, a, grid, smem, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cb

@@ -12,7 +12,14 @@
 // channels at a time: KC = 32 (128-byte rows, 128-byte swizzle) in general,
 // KC = 16 or 8 (64- / 32-byte rows and swizzles) for layers with 16 or 8
 // input channels, so that the copy engine moves no padding channels.
-//  * warp 0 (four lanes taking K steps in turn): TMA producer.  The A tile comes from an im2col-mode
+//  * warp 0 (four lanes taking K steps in turn): TMA producer.  For tiles of
+//    blk_h x blk_w output pixels of one image (blk_w != 0) the A tile of a
+//    (tap, chunk) is one tiled copy: a box of KC channels x (stride * blk_w)
+//    x (stride * blk_h) input elements traversed with element strides equal
+//    to the conv stride, started at the tap's offset (the copy engine takes
+//    about one 128-byte row per clock this way, against several per row in
+//    im2col mode; zero fill outside the image is the padding).  Otherwise:
+//    The A tile comes from an im2col-mode
 //    tensor copy: the map's bounding box enumerates exactly the output pixel
 //    positions (lower corner -pad, upper corner pad - (k - 1), traversal
 //    stride = conv stride) and the per-copy offsets select the filter tap,
@@ -139,11 +146,22 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
       TraceBuf tr;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
         const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
-        const int m0 = m_tile * kTileM;
-        const int n_img = m0 / a.OHW;
-        const int rem = m0 - n_img * a.OHW;
-        const int oh = rem / a.OW, ow = rem - (rem / a.OW) * a.OW;
-        const int w0 = ow * a.stride - a.pad, h0 = oh * a.stride - a.pad;
+        int n_img, w0, h0;
+        if (a.blk_w) {
+          const int per_img = a.blocks_x * a.blocks_y;
+          n_img = m_tile / per_img;
+          const int rem = m_tile - n_img * per_img;
+          const int by = rem / a.blocks_x, bx = rem - by * a.blocks_x;
+          w0 = bx * a.blk_w * a.stride - a.pad;
+          h0 = by * a.blk_h * a.stride - a.pad;
+        } else {
+          const int m0 = m_tile * kTileM;
+          n_img = m0 / a.OHW;
+          const int rem = m0 - n_img * a.OHW;
+          const int oh = rem / a.OW, ow = rem - (rem / a.OW) * a.OW;
+          w0 = ow * a.stride - a.pad;
+          h0 = oh * a.stride - a.pad;
+        }
         for (int tap = 0; ok && tap < a.taps; ++tap) {
           const uint16_t off_h = static_cast<uint16_t>(tap / a.kw);
           const uint16_t off_w = static_cast<uint16_t>(tap % a.kw);
@@ -154,7 +172,10 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
                 break;
               }
               mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(kABytes + BN * KC * 4));
-              tma_load_im2col_4d(sA + stage * kABytes, &amap, &full[stage], kc * KC, w0, h0, n_img, off_w, off_h);
+              if (a.blk_w)
+                tma_load_4d(sA + stage * kABytes, &amap, &full[stage], kc * KC, w0 + off_w, h0 + off_h, n_img);
+              else
+                tma_load_im2col_4d(sA + stage * kABytes, &amap, &full[stage], kc * KC, w0, h0, n_img, off_w, off_h);
               tma_load_3d(sB + stage * kBBytes, &bmap, &full[stage], kc * KC, tap, n_tile * BN);
               tr.add(tr_cta && lane == 0);
               issued |= 1u << stage;
@@ -243,12 +264,28 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
       const int acc = local % NACC;
       const uint32_t acc_phase = (local / NACC) & 1;
       const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
-      const int m = m_tile * kTileM + row;
       long long yoff = -1, roff = 0;
-      if (m < a.M) {
-        const int n_img = m / a.OHW;
-        const int rem = m - n_img * a.OHW;
-        const int oh = rem / a.OW, ow = rem - (rem / a.OW) * a.OW;
+      int n_img = 0, oh = 0, ow = 0;
+      bool valid;
+      if (a.blk_w) {
+        const int per_img = a.blocks_x * a.blocks_y;
+        n_img = m_tile / per_img;
+        const int rem = m_tile - n_img * per_img;
+        const int by = rem / a.blocks_x, bx = rem - by * a.blocks_x;
+        oh = by * a.blk_h + row / a.blk_w;
+        ow = bx * a.blk_w + row % a.blk_w;
+        valid = oh < a.OHW / a.OW && ow < a.OW;
+      } else {
+        const int m = m_tile * kTileM + row;
+        valid = m < a.M;
+        if (valid) {
+          n_img = m / a.OHW;
+          const int rem = m - n_img * a.OHW;
+          oh = rem / a.OW;
+          ow = rem - (rem / a.OW) * a.OW;
+        }
+      }
+      if (valid) {
         yoff = n_img * a.out.ys_n + oh * a.out.ys_h + static_cast<long long>(ow) * a.out.ys_w;
         if (res) roff = n_img * a.ep.rs_n + oh * a.ep.rs_h + static_cast<long long>(ow) * a.ep.rs_w;
       }

@@ -80,6 +80,11 @@ struct IgemmArgs {
   int stride, pad;
   int stages;
   int vec_store;  // 1 when y / r rows allow 16-byte vector access
+  // Pixel tiles: blk_w == 0 -> 128 consecutive output pixels in (n, oh, ow)
+  // order, A gathered by an im2col-mode copy; else blocks of blk_h x blk_w
+  // output pixels (blk_h * blk_w == 128) of one image, A loaded per filter
+  // tap by a tiled copy with element strides = conv stride.
+  int blk_w, blk_h, blocks_x, blocks_y;
   OutView out;
   Epilogue ep;
   int* err;
@@ -99,13 +104,15 @@ int igemm_stages(int bn, int kc);
 struct HaloArgs {
   int H, W, Wp;        // input = output height / width; Wp = W + 2 (padded width)
   int Cout;
-  int num_kc;          // Cin / 32
+  int kc;              // input channels per chunk: 32, or 16 (64-byte rows)
+  int num_kc;          // Cin / kc
   int tiles_per_img;   // ceil(H * Wp / 128)
   int m_tiles;         // N * tiles_per_img
   int n_tiles;         // ceil(Cout / BN)
   int rows;            // input rows per halo copy
   int halo_bytes;      // shared-memory bytes of one halo buffer (multiple of 1024)
   int nb_stages;       // weight-slice ring depth
+  int taps_per_stage;  // filter taps per weight-ring stage (1, 3 or 9): one copy each
   int split_k;         // 1, or 2: clusters of two CTAs split each tile's chunks (one tile per cluster)
   int vec_store;       // 1 when y / r rows allow 16-byte vector access
   OutView out;
@@ -119,8 +126,8 @@ struct HaloArgs {
 // wp, and the buffer bytes (rows * wp pixels of 128 bytes, plus 8 rows that
 // only the discarded padding columns of the last rows read).
 int halo_rows(int wp, int px);
-int halo_buffer_bytes(int wp, int px);
-size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages);
+int halo_buffer_bytes(int wp, int px, int kc = 32);
+size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages, int taps_per_stage = 1, int kc = 32);
 // Shared-memory bytes a split-K CTA receives from its partner (half of one
 // accumulator), which must fit in its halo and weight buffers.
 size_t halo_split_recv_bytes(int px, int co, bool cm);

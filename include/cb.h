@@ -121,9 +121,9 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
  * and Ci >= 16 (3x3) or Ci >= 8 (1x1) run as an implicit GEMM on the tcgen05
  * tensor cores (TF32 inputs, fp32 accumulate, outputs rounded to the nearest
  * TF32 value; needs 16-byte aligned x/w and strides that are multiples of 4
- * elements).  Among those, 3x3 stride-1 pad-1 layers with Ci % 32 == 0 and
- * W <= 254 take one shared-memory halo tile per 32-channel chunk for all
- * nine taps; the others gather one im2col tile per tap.  1x1 stride-1
+ * elements).  Among those, 3x3 stride-1 pad-1 layers with Ci % 16 == 0 and
+ * W <= 254 take one shared-memory halo tile per 32- (or 16-) channel chunk
+ * for all nine taps; the others gather one tile per tap.  1x1 stride-1
  * layers with Ci and Co in {4, 8, 16, 32} run instead on a streaming fp32
  * CUDA-core kernel (HBM-bound at these widths);
  * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;

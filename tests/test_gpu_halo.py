@@ -58,7 +58,10 @@ def test_halo_silu(gpu, orc, case):
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
 
 
-@pytest.mark.parametrize("bn_force", ["32,0", "64,0", "128,0", "256,0", "128,3", "64,16", "cm", "cm,2"])
+@pytest.mark.parametrize("bn_force", ["32,0", "64,0", "128,0", "256,0", "128,3", "64,16", "cm", "cm,2",
+                                      # taps per weight-ring stage (one copy each): 9, 3 and 1
+                                      "32,0,1,9", "64,0,1,3", "128,0,1,3", "128,0,1,1", "cm,0,1,3", "cm,0,1,1",
+                                      "256,0,1,1"])
 def test_halo_tile_widths(gpu, orc, halo_force, bn_force):
     halo_force(bn_force)
     x, w, bn = synthetic.dense_layer(64, 200, 10, 23, N=2, k=3, seed=3)
@@ -121,7 +124,7 @@ def test_halo_matches_im2col_kernel(gpu):
 
 
 def test_halo_not_taken_outside_its_shapes(gpu):
-    x = torch.empty(1, 8, 8, 48, device="cuda")  # Cin % 32 != 0
+    x = torch.empty(1, 8, 8, 40, device="cuda")  # Cin % 16 != 0
     y = torch.empty(1, 8, 8, 32, device="cuda")
     assert cb.conv_path(x, y, 3, 1, 1) == cb.PATH_TC_IM2COL
     x = torch.empty(1, 8, 300, 32, device="cuda")  # too wide for two halo buffers
@@ -225,3 +228,40 @@ def test_halo_split_k_epilogues_and_views(gpu, orc, halo_force, force, act, res_
     ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=act, residual=r, res_mode=res_mode)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
     assert is_canary(buf[:, :, W:, :]) and is_canary(buf[:, :, :W, :8]) and is_canary(buf[:, :, :W, 8 + Co:])
+
+
+KC16_CASES = [
+    # N, H, W, Cin, Cout: 16-channel chunks (Cin % 32 == 16), pixel-major 128 x {32, 64} tiles
+    (2, 7, 40, 16, 32), (1, 20, 20, 48, 64), (2, 9, 13, 16, 16), (1, 5, 80, 80, 64), (3, 11, 17, 16, 40),
+    (1, 1, 1, 16, 32),
+]
+
+
+@pytest.mark.parametrize("case", KC16_CASES, ids=lambda s: "x".join(map(str, s)))
+def test_halo_16_channel_chunks(gpu, orc, case):
+    """64-byte pixel rows with the 64-byte swizzle: the nine taps start their descriptors at any
+    64-byte row of the halo tile."""
+    N, H, W, Ci, Co = case
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=sum(case) + 3)
+    y = _run(x, w, bn)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("force", ["32,0,1,9", "64,0,1,3", "64,0,1,1"])
+@pytest.mark.parametrize("act,res_mode", [(1, 1), (2, 2)])
+def test_halo_16_channel_chunks_epilogues_and_views(gpu, orc, halo_force, force, act, res_mode):
+    halo_force(force)
+    N, H, W, Ci, Co = 2, 10, 33, 48, 64
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=61 + act)
+    r = np.random.default_rng(8).standard_normal((N, H, W, Co)).astype(np.float32)
+    buf = canary_buffer((N, H, W + 2, Co + 16))
+    y = buf[:, :, :W, 4:4 + Co]
+    layer = ConvBnAct(w, bn, 1, 1, act)
+    xd = to_dev(x)
+    assert cb.conv_path(xd, y, 3, 1, 1) == cb.PATH_TC_HALO
+    layer(xd, y, residual=to_dev(r), res_mode=res_mode)
+    sync_check()
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=act, residual=r, res_mode=res_mode)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+    assert is_canary(buf[:, :, W:, :]) and is_canary(buf[:, :, :W, :4]) and is_canary(buf[:, :, :W, 4 + Co:])
