@@ -368,14 +368,24 @@ struct HaloPlan {
   int nb = 0, grid = 0;
   int split = 1;       // 2: clusters of two CTAs split each tile's channel chunks
   int tps = 1;         // filter taps per weight-ring stage (one copy per stage)
-  int kc = 32;         // input channels per chunk (32, or 16 for Ci % 32 == 16)
+  int kc = 32;         // input channels per chunk (32, or 16 for Ci % 32 == 16 and for stride 2)
+  int stride = 1;      // 2: four phase tiles per chunk
+  int blk_w = 0, n_blk = 1, wp = 0;  // column blocks and the padded width of the pixel numbering
   size_t smem = 0;
 };
 struct ImPlan {        // im2col kernel choices (0 = the cost model's)
   int bn = 0, stages = 0;
   int blocks = 0;      // 1: 128 consecutive pixels (im2col copies); 2: pixel blocks (tiled copies)
 };
-bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out);
+// Constraints on a halo plan (0 / false = free): tile shape, ring depth,
+// split K, taps per weight stage.
+struct HaloForce {
+  int co = 0;
+  bool cm = false;
+  int nb = 0, split = 0, tps = 0;
+};
+HaloForce halo_force_env();
+bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, const HaloForce& f, HaloPlan* out);
 
 // ------------------------------------------------------------ autotuner
 // Plans measured by cb_autotune_conv, per layer shape (and device, policy):
@@ -603,85 +613,106 @@ bool halo_ring(int co, int hb, int force_nb, int force_tps, int* nb_out, int* tp
   return false;
 }
 
-bool plan_halo(int N, int H, int W, int Ci, int Co, int sms, HaloPlan* out) {
-  // 32-channel chunks (128-byte rows); layers with Ci % 32 == 16 take 16-channel
-  // chunks (64-byte rows) in the pixel-major 128 x {32, 64} tiles
-  const int kc = Ci % 32 == 0 ? 32 : (Ci % 16 == 0 ? 16 : 0);
-  if (kc == 0 || W + 2 > 256) return false;
-  const int wp = W + 2;
+HaloForce halo_force_env() {
+  // CB_HALO_FORCE = "cm[,stages[,split[,taps]]]" or "co[,stages[,split[,taps]]]", read per call
+  HaloForce f;
+  if (const char* e = std::getenv("CB_HALO_FORCE")) {
+    if (e[0] == 'c' && e[1] == 'm') {
+      f.cm = true;
+      if (e[2] == ',') std::sscanf(e + 3, "%d,%d,%d", &f.nb, &f.split, &f.tps);
+    } else {
+      std::sscanf(e, "%d,%d,%d,%d", &f.co, &f.nb, &f.split, &f.tps);
+    }
+  }
+  return f;
+}
+
+bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, const HaloForce& f, HaloPlan* out) {
+  const int N = x->n, Ci = x->c, Co = y->c, OH = y->h, OW = y->w;
+  // 32-channel chunks (128-byte rows); 16-channel chunks (64-byte rows) for
+  // Ci % 32 == 16 and at stride 2 (four phase tiles per chunk), in the
+  // pixel-major 128 x {32, 64, 128} tiles
+  const int kc = (stride == 1 && Ci % 32 == 0) ? 32 : (Ci % 16 == 0 ? 16 : 0);
+  if (kc == 0) return false;
   const int num_kc = Ci / kc;
+  constexpr size_t kSmemMax = 227 * 1024;
   struct Shape {
     int px, co;
     bool cm;
   };
   static const Shape kShapes[] = {{256, 128, true}, {128, 256, false}, {128, 128, false}, {128, 64, false},
                                   {128, 32, false}};
-  // Tuning override (CB_HALO_FORCE = "cm[,stages[,split[,taps]]]" or
-  // "co[,stages[,split[,taps]]]"; 0 = free), read per call.
-  int force_co = 0, force_nb = 0, force_split = 0, force_tps = 0;
-  bool force_cm = false;
-  if (const char* f = std::getenv("CB_HALO_FORCE")) {
-    if (f[0] == 'c' && f[1] == 'm') {
-      force_cm = true;
-      if (f[2] == ',') std::sscanf(f + 3, "%d,%d,%d", &force_nb, &force_split, &force_tps);
-    } else {
-      std::sscanf(f, "%d,%d,%d,%d", &force_co, &force_nb, &force_split, &force_tps);
-    }
-  }
+  // Column blocks: the padded width of the pixel numbering must fit a copy
+  // box (256 elements traversed: blk_w + 2 at stride 1, 2 (blk_w + 1) at
+  // stride 2); more blocks shrink the halo when it does not fit.
+  const int max_blk = stride == 1 ? 254 : 127;
+  const int min_blocks = (OW + max_blk - 1) / max_blk;
   double best = 1e300;
   HaloPlan plan;
   for (const Shape& sh : kShapes) {
-    if (force_cm && !sh.cm) continue;
-    if (force_co && (sh.cm || sh.co != force_co)) continue;
-    if (kc == 16 && (sh.cm || sh.co > 64)) continue;
-    const int rows = halo_rows(wp, sh.px);
-    if (rows > 256) continue;
-    const int hb = halo_buffer_bytes(wp, sh.px, kc);
-    int nb = 0, tps = 1;
-    if (!halo_ring(sh.co, hb, force_nb, force_tps, &nb, &tps, kc)) continue;
-    const long long m_tiles = static_cast<long long>(N) * ((H * wp + sh.px - 1) / sh.px);
-    const long long tiles = m_tiles * ((Co + sh.co - 1) / sh.co);
-    if (tiles >= (1LL << 31)) continue;
-    const long long grid = std::min<long long>(tiles, sms);
-    const long long per_cta = (tiles + grid - 1) / grid;
-    // Cycles per (tile, chunk): nine taps of four K = 8 MMAs, each about
-    // 120 issue cycles for N <= 128 and 128 for N = 256 (measured), plus the
-    // per-tap barrier round trip; against the bytes the copy engine brings
-    // in (halo + nine weight slices) at ~64 B per clock per SM when every SM
-    // pulls from L2.  Plus the pipeline fill per tile and one exposed epilogue.
-    const int n = sh.cm ? sh.px : sh.co;
-    const double mma = 9.0 * (kc / 8) * (n > 128 ? 128.0 : 120.0) + (9.0 / tps) * 100.0;
-    const double copy = (1.0 + 9.0 / tps) * 550.0;  // one halo copy and 9 / tps weight copies
-    const double epi = sh.px * sh.co / 2.3;
-    const size_t smem = halo_smem_bytes(sh.co, hb, nb, tps, kc);
-    for (int split = 1; split <= 2; ++split) {
-      if (force_split && split != force_split) continue;
-      double cost;
-      if (split == 1) {
-        cost = static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 1500.0) + epi;
-      } else {
-        // one tile per CTA pair, each CTA half of the chunks; the partner's
-        // half accumulator comes over distributed shared memory (~16 B per
-        // clock) and each CTA stores half the tile
-        const size_t recv = halo_split_recv_bytes(sh.px, sh.co, sh.cm);
-        if (kc != 32 || num_kc < 2 || (!sh.cm && sh.co < 64) ||
-            recv > 2 * static_cast<size_t>(hb) + nb * tps * sh.co * 128ull ||
-            2 * tiles > sms || halo_max_pairs(sh.px, sh.co, sh.cm, smem) < tiles)
-          continue;
-        cost = (num_kc - num_kc / 2) * std::max(mma, copy) + 1500.0 + recv / 16.0 + 1000.0 + epi / 2;
+    if (f.cm && !sh.cm) continue;
+    if (f.co && (sh.cm || sh.co != f.co)) continue;
+    if (kc == 16 && (sh.cm || sh.co > 128)) continue;
+    if (kc == 16 && sh.co == 128 && stride == 1) continue;
+    for (int n_blk = min_blocks; n_blk <= min_blocks + 3 && n_blk <= OW; ++n_blk) {
+      const int blk_w = (OW + n_blk - 1) / n_blk;
+      const int wp = blk_w + (stride == 1 ? 2 : 1);
+      const int rows = halo_rows(wp, sh.px, stride);
+      if (rows * stride > 256) continue;
+      const int hb = halo_buffer_bytes(wp, sh.px, kc, stride);
+      int nb = 0, tps = 1;
+      if (!halo_ring(sh.co, hb, f.nb, f.tps, &nb, &tps, kc)) continue;
+      const long long m_tiles = static_cast<long long>(N) * n_blk * ((OH * wp + sh.px - 1) / sh.px);
+      const long long tiles = m_tiles * ((Co + sh.co - 1) / sh.co);
+      if (tiles >= (1LL << 31)) continue;
+      const long long grid = std::min<long long>(tiles, sms);
+      const long long per_cta = (tiles + grid - 1) / grid;
+      // Cycles per (tile, chunk): nine taps of kc / 8 MMAs, each about 120
+      // issue cycles for N <= 128 and 128 for N = 256 (measured), plus the
+      // barrier round trip per weight stage; against the copies (an SM
+      // completes about one per 400-700 cycles): one halo (four phase tiles
+      // at stride 2) and 9 / tps weight stages.  Plus the pipeline fill per
+      // tile and one exposed epilogue.
+      const int n = sh.cm ? sh.px : sh.co;
+      const double mma = 9.0 * (kc / 8) * (n > 128 ? 128.0 : 120.0) + (9.0 / tps) * 100.0;
+      const double copy = ((stride == 1 ? 1.0 : 4.0) + 9.0 / tps) * 550.0;
+      const double epi = sh.px * sh.co / 2.3;
+      const size_t smem = halo_smem_bytes(sh.co, hb, nb, tps, kc);
+      for (int split = 1; split <= 2; ++split) {
+        if (f.split && split != f.split) continue;
+        double cost;
+        if (split == 1) {
+          cost = static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 1500.0) + epi;
+        } else {
+          // one tile per CTA pair, each CTA half of the chunks; the partner's
+          // half accumulator comes over distributed shared memory (~16 B per
+          // clock) and each CTA stores half the tile
+          const size_t recv = halo_split_recv_bytes(sh.px, sh.co, sh.cm);
+          if (stride != 1 || kc != 32 || num_kc < 2 || (!sh.cm && sh.co < 64) ||
+              recv > 2 * static_cast<size_t>(hb) + nb * tps * sh.co * 128ull || 2 * tiles > sms ||
+              halo_max_pairs(sh.px, sh.co, sh.cm, smem) < tiles)
+            continue;
+          cost = (num_kc - num_kc / 2) * std::max(mma, copy) + 1500.0 + recv / 16.0 + 1000.0 + epi / 2;
+        }
+        cost *= 1.0 + 0.02 * (n_blk - min_blocks);  // fewer blocks: less halo overlap
+        if (cost < best * 0.97) {
+          best = cost;
+          plan.px = sh.px;
+          plan.co = sh.co;
+          plan.cm = sh.cm;
+          plan.nb = nb;
+          plan.tps = tps;
+          plan.kc = kc;
+          plan.stride = stride;
+          plan.blk_w = blk_w;
+          plan.n_blk = n_blk;
+          plan.wp = wp;
+          plan.split = split;
+          plan.grid = static_cast<int>(split == 2 ? 2 * tiles : grid);
+          plan.smem = smem;
+        }
       }
-      if (cost < best * 0.97) {
-        best = cost;
-        plan.px = sh.px;
-        plan.co = sh.co;
-        plan.cm = sh.cm;
-        plan.nb = nb;
-        plan.tps = tps;
-        plan.kc = kc;
-        plan.split = split;
-        plan.grid = static_cast<int>(split == 2 ? 2 * tiles : grid);
-        plan.smem = smem;
-      }
+      break;  // the fewest blocks that fit
     }
   }
   if (plan.px == 0) return false;
@@ -734,11 +765,11 @@ cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, i
                      aligned16(x->data) && strides_mult4(x) && x->n <= 65535 && x->w <= 65535 &&
                      x->h <= 65535 && encode_tiled() && encode_im2col();
   if (!tc_ok) return CB_PATH_DIRECT;
-  if (policy == 0 && kh == 3 && stride == 1 && pad == 1) {
+  if (policy == 0 && kh == 3 && pad == 1) {
     DeviceInfo* dev = nullptr;
     HaloPlan tmp;
     HaloPlan& p = plan ? *plan : tmp;
-    if (current_device(&dev) == CB_OK && plan_halo(x->n, x->h, x->w, x->c, y->c, dev->sms, &p))
+    if (current_device(&dev) == CB_OK && plan_halo(x, y, stride, dev->sms, halo_force_env(), &p))
       return p.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
   }
   return CB_PATH_TC_IM2COL;
@@ -753,15 +784,22 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   HaloArgs a{};
   a.H = x->h;
   a.W = x->w;
-  a.Wp = x->w + 2;
+  a.stride = plan.stride;
+  a.OH = y->h;
+  a.OW = y->w;
+  a.blk_w = plan.blk_w;
+  a.n_blk = plan.n_blk;
+  a.Wp = plan.wp;
   a.Cout = Co;
   a.kc = plan.kc;
   a.num_kc = Ci / plan.kc;
-  a.tiles_per_img = (a.H * a.Wp + plan.px - 1) / plan.px;
+  a.tiles_per_blk = (a.OH * a.Wp + plan.px - 1) / plan.px;
+  a.tiles_per_img = a.n_blk * a.tiles_per_blk;
   a.m_tiles = x->n * a.tiles_per_img;
   a.n_tiles = (Co + plan.co - 1) / plan.co;
-  a.rows = halo_rows(a.Wp, plan.px);
-  a.halo_bytes = halo_buffer_bytes(a.Wp, plan.px, plan.kc);
+  a.rows = halo_rows(a.Wp, plan.px, plan.stride);
+  a.halo_bytes = halo_buffer_bytes(a.Wp, plan.px, plan.kc, plan.stride);
+  a.phase_bytes = plan.stride == 2 ? a.halo_bytes / 4 : 0;
   a.nb_stages = plan.nb;
   a.taps_per_stage = plan.tps;
   a.split_k = plan.split;
@@ -780,19 +818,23 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   }
   if (std::getenv("CB_DEBUG_PLAN"))
     std::fprintf(stderr,
-                 "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d -> %s px=%d co=%d nb=%d tps=%d split=%d rows=%d "
-                 "halo=%d tiles=%d grid=%d smem=%zu\n",
-                 x->n, a.H, a.W, Ci, Co, plan.cm ? "channel-major" : "pixel-major", plan.px, plan.co, plan.nb,
-                 plan.tps, plan.split, a.rows, a.halo_bytes, a.m_tiles * a.n_tiles, plan.grid, plan.smem);
+                 "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d s=%d -> %s px=%d co=%d kc=%d nb=%d tps=%d split=%d "
+                 "blocks=%dx%d rows=%d halo=%d tiles=%d grid=%d smem=%zu\n",
+                 x->n, a.H, a.W, Ci, Co, plan.stride, plan.cm ? "channel-major" : "pixel-major", plan.px, plan.co,
+                 plan.kc, plan.nb, plan.tps, plan.split, plan.n_blk, plan.blk_w, a.rows, a.halo_bytes,
+                 a.m_tiles * a.n_tiles, plan.grid, plan.smem);
   CUtensorMap xmap, wmap;
   {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(x->w), static_cast<cuuint64_t>(x->h),
                           static_cast<cuuint64_t>(x->n)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(x->stride_w) * 4, static_cast<cuuint64_t>(x->stride_h) * 4,
                              static_cast<cuuint64_t>(x->stride_n) * 4};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(plan.kc), static_cast<cuuint32_t>(a.Wp),
-                         static_cast<cuuint32_t>(a.rows), 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
+    // stride 2: each phase tile traverses 2 Wp columns and 2 rows rows of the
+    // input with element strides 2
+    const cuuint32_t st = static_cast<cuuint32_t>(plan.stride);
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(plan.kc), st * static_cast<cuuint32_t>(a.Wp),
+                         st * static_cast<cuuint32_t>(a.rows), 1};
+    cuuint32_t estr[4] = {1, st, st, 1};
     CUresult r = tiled_map(&xmap, 4, x->data, dims, strides, box, estr,
                            plan.kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
@@ -1031,47 +1073,28 @@ cb_status launch_conv(const cb_tensor* x, const float* w, const float* scale, co
 std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, int sms) {
   std::vector<ConvPlan> out;
   const int Ci = x->c, Co = y->c;
-  const int hkc = Ci % 32 == 0 ? 32 : (Ci % 16 == 0 ? 16 : 0);
-  if (kh == 3 && stride == 1 && pad == 1 && hkc && x->w + 2 <= 256 && g_policy.load() == 0) {
-    const int wp = x->w + 2;
+  if (kh == 3 && pad == 1 && Ci % 16 == 0 && g_policy.load() == 0) {
+    // every halo tile shape x taps per weight stage x split, each planned
+    // under those constraints (ring depth, column blocks and grid follow)
     struct Shape {
-      int px, co;
+      int co;
       bool cm;
     };
-    static const Shape kShapes[] = {{256, 128, true}, {128, 256, false}, {128, 128, false}, {128, 64, false},
-                                    {128, 32, false}};
+    static const Shape kShapes[] = {{128, true}, {256, false}, {128, false}, {64, false}, {32, false}};
     for (const Shape& sh : kShapes) {
       if (!sh.cm && sh.co > 2 * ((Co + 15) / 16 * 16)) continue;  // a tile mostly beyond Co
-      if (hkc == 16 && (sh.cm || sh.co > 64)) continue;
-      const int hb = halo_buffer_bytes(wp, sh.px, hkc);
-      if (halo_rows(wp, sh.px) > 256) continue;
-      for (int tps : {9, 3, 1}) {
-        int nb = 0, t = 0;
-        if (!halo_ring(sh.co, hb, 0, tps, &nb, &t, hkc)) continue;
-        ConvPlan p;
-        p.path = sh.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
-        p.halo.px = sh.px;
-        p.halo.co = sh.co;
-        p.halo.cm = sh.cm;
-        p.halo.nb = nb;
-        p.halo.tps = tps;
-        p.halo.kc = hkc;
-        p.halo.smem = halo_smem_bytes(sh.co, hb, nb, tps, hkc);
-        const long long tiles = static_cast<long long>(x->n) * ((x->h * wp + sh.px - 1) / sh.px) *
-                                ((Co + sh.co - 1) / sh.co);
-        if (tiles >= (1LL << 31)) continue;
-        p.halo.grid = static_cast<int>(std::min<long long>(tiles, sms));
-        out.push_back(p);
-        // split K over a CTA pair, when every tile gets a pair at once
-        const size_t recv = halo_split_recv_bytes(sh.px, sh.co, sh.cm);
-        if (hkc == 32 && Ci / 32 >= 2 && (sh.cm || sh.co >= 64) &&
-            recv <= 2 * static_cast<size_t>(hb) + nb * tps * sh.co * 128ull &&
-            2 * tiles <= sms && halo_max_pairs(sh.px, sh.co, sh.cm, p.halo.smem) >= tiles) {
-          p.halo.split = 2;
-          p.halo.grid = static_cast<int>(2 * tiles);
+      for (int tps : {9, 3, 1})
+        for (int split : {1, 2}) {
+          HaloForce f;
+          f.co = sh.cm ? 0 : sh.co;
+          f.cm = sh.cm;
+          f.tps = tps;
+          f.split = split;
+          ConvPlan p;
+          if (!plan_halo(x, y, stride, sms, f, &p.halo)) continue;
+          p.path = p.halo.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
           out.push_back(p);
         }
-      }
     }
   }
   for (int bn : {16, 32, 48, 64, 96, 128, 192, 256}) {

@@ -11,12 +11,16 @@
 namespace cb {
 
 // A tile covers q in [q0, q0 + px) with q0 - y_lo * Wp in [0, Wp): at most
-// (px - 1) / Wp + 2 output rows, plus one halo row above and below.
-int halo_rows(int wp, int px) { return (px - 1) / wp + 4; }
+// (px - 1) / Wp + 2 output rows, plus one halo row above and below (stride 1);
+// at stride 2 a phase tile holds those output rows and the one above.
+int halo_rows(int wp, int px, int stride) { return (px - 1) / wp + (stride == 1 ? 4 : 3); }
 
-int halo_buffer_bytes(int wp, int px, int kc) {
-  const int bytes = (halo_rows(wp, px) * wp + 8) * kc * 4;
-  return (bytes + 1023) / 1024 * 1024;
+// Bytes of one halo buffer: one tile (stride 1) or four phase tiles (stride
+// 2) of rows x Wp pixels of kc channels, plus 8 pixels that only the
+// discarded padding columns of the last rows read; 1 KB multiples.
+int halo_buffer_bytes(int wp, int px, int kc, int stride) {
+  const int bytes = ((halo_rows(wp, px, stride) * wp + 8) * kc * 4 + 1023) / 1024 * 1024;
+  return stride == 1 ? bytes : 4 * bytes;
 }
 
 size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages, int taps_per_stage, int kc) {
@@ -96,6 +100,9 @@ cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, 
   if (a.nb_stages < 2 || a.nb_stages > 16) return cudaErrorInvalidValue;
   if (a.taps_per_stage != 1 && a.taps_per_stage != 3 && a.taps_per_stage != 9) return cudaErrorInvalidValue;
   if (a.split_k != 1 && a.split_k != 2) return cudaErrorInvalidValue;
+  if (a.stride != 1 && a.stride != 2) return cudaErrorInvalidValue;
+  if (a.stride == 2 && (a.kc != 16 || a.phase_bytes * 4 != a.halo_bytes || a.Wp * 2 > 256 || a.rows * 2 > 256))
+    return cudaErrorInvalidValue;
   if (a.split_k == 2) {
     // one tile per cluster, a channel-chunk per CTA at least, the partner's
     // half accumulator within the operand buffers, a shape that splits

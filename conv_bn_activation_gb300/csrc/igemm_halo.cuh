@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   const uint32_t tmem_base = *tmem_slot;
   const Watchdog wd{a.err, abort_flag, a.timeout_ns};
   const int num_tiles = a.m_tiles * a.n_tiles;
-  const uint32_t halo_tx = static_cast<uint32_t>(kRowBytes * a.Wp * a.rows);
+  const uint32_t halo_tx = static_cast<uint32_t>(kRowBytes * a.Wp * a.rows * (a.stride == 2 ? 4 : 1));
   const bool tr_cta = a.trace && blockIdx.x == a.trace_cta;
 
   if (warp == 0) {
@@ -176,8 +176,11 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
         const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
         const int n_img = m_tile / a.tiles_per_img;
-        const int q0 = (m_tile - n_img * a.tiles_per_img) * PX;
+        const int rem = m_tile - n_img * a.tiles_per_img;
+        const int blk = rem / a.tiles_per_blk;
+        const int q0 = (rem - blk * a.tiles_per_blk) * PX;
         const int y_lo = q0 / a.Wp;
+        const int x0 = blk * a.blk_w - 1;  // first column of the tile (phase column at stride 2)
         for (int kc = kc_begin; ok && kc < kc_end; ++kc) {
           if (lane == 0) {
             if (!mbar_wait(&hempty[h], hphase ^ 1u, wd)) {
@@ -185,7 +188,14 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
               break;
             }
             mbar_arrive_expect_tx(&hfull[h], halo_tx);
-            tma_load_4d(sHalo + h * a.halo_bytes, &xmap, &hfull[h], kc * KC, -1, y_lo - 1, n_img);
+            if (a.stride == 1) {
+              tma_load_4d(sHalo + h * a.halo_bytes, &xmap, &hfull[h], kc * KC, x0, y_lo - 1, n_img);
+            } else {
+              // four phase tiles: input rows 2i + py, columns 2j + px (element strides 2)
+              for (int ph = 0; ph < 4; ++ph)
+                tma_load_4d(sHalo + h * a.halo_bytes + ph * a.phase_bytes, &xmap, &hfull[h], kc * KC,
+                            2 * x0 + (ph & 1), 2 * (y_lo - 1) + (ph >> 1), n_img);
+            }
             issued |= 1u << h;
             last_parity = (last_parity & ~(1u << h)) | (hphase << h);
           }
@@ -237,7 +247,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
         const uint32_t acc_phase = (local / NACC) & 1;
         const int m_tile = tile / a.n_tiles;
         const int n_img = m_tile / a.tiles_per_img;
-        const int q0 = (m_tile - n_img * a.tiles_per_img) * PX;
+        const int rem = m_tile - n_img * a.tiles_per_img;
+        const int q0 = (rem - (rem / a.tiles_per_blk) * a.tiles_per_blk) * PX;
         const int base_row = q0 - (q0 / a.Wp) * a.Wp;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wd)) break;
         tc_fence_after_sync();
@@ -259,7 +270,15 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
             for (int t = 0; t < tps; ++t) {
               const int tap = tap0 + t;
               const int dy = tap / 3, dx = tap - 3 * (tap / 3);
-              const uint32_t x_addr = halo_addr + static_cast<uint32_t>((base_row + dy * a.Wp + dx) * kRowBytes);
+              uint32_t x_addr;
+              if (a.stride == 1) {
+                x_addr = halo_addr + static_cast<uint32_t>((base_row + dy * a.Wp + dx) * kRowBytes);
+              } else {
+                // input row 2 oy + dy - 1 is phase row (dy != 1) at oy - 1 + (dy != 0); columns alike
+                const int ph = (dy != 1 ? 2 : 0) + (dx != 1 ? 1 : 0);
+                x_addr = halo_addr + static_cast<uint32_t>(ph * a.phase_bytes) +
+                         static_cast<uint32_t>((base_row + (dy != 0) * a.Wp + (dx != 0)) * kRowBytes);
+              }
               const uint64_t xdesc = kmajor_swizzled_desc(x_addr, kRowBytes);
               const uint64_t wdesc = kmajor_swizzled_desc(smem_u32(sB + s * kBBytes + t * kTapBytes), kRowBytes);
               const uint64_t adesc = CM ? wdesc : xdesc, bdesc = CM ? xdesc : wdesc;
@@ -319,11 +338,14 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       const uint32_t acc_phase = (local / NACC) & 1;
       const int m_tile = tile / a.n_tiles, n_tile = tile % a.n_tiles;
       const int n_img = m_tile / a.tiles_per_img;
-      const int q0 = (m_tile - n_img * a.tiles_per_img) * PX;
+      const int rem = m_tile - n_img * a.tiles_per_img;
+      const int blk = rem / a.tiles_per_blk;
+      const int q0 = (rem - blk * a.tiles_per_blk) * PX;
       // Element offsets of output pixel q (-1: a padding column or past the image).
       auto pixel_offsets = [&](int qq, long long& yoff, long long& roff) {
-        const int oy = qq / a.Wp, ox = qq - (qq / a.Wp) * a.Wp;
-        const bool valid = oy < a.H && ox < a.W;
+        const int oy = qq / a.Wp, oxl = qq - (qq / a.Wp) * a.Wp;
+        const int ox = blk * a.blk_w + oxl;
+        const bool valid = oy < a.OH && oxl < a.blk_w && ox < a.OW;
         yoff = valid ? n_img * a.out.ys_n + oy * a.out.ys_h + static_cast<long long>(ox) * a.out.ys_w : -1;
         roff = (valid && res) ? n_img * a.ep.rs_n + oy * a.ep.rs_h + static_cast<long long>(ox) * a.ep.rs_w : 0;
       };

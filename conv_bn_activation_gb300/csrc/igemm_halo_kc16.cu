@@ -1,6 +1,7 @@
 // The 16-channel-chunk instantiations of the halo-tile implicit GEMM
 // (igemm_halo.cuh): layers whose input channels are a multiple of 16 but not
-// of 32 (64-byte pixel rows, 64-byte swizzle), pixel-major 128 x {32, 64}.
+// of 32, and stride-2 layers (64-byte pixel rows, 64-byte swizzle),
+// pixel-major 128 x {32, 64, 128}.
 #include "igemm_halo.cuh"
 #include "launch_util.h"
 
@@ -23,6 +24,7 @@ cudaError_t launch_igemm_halo_kc16(const CUtensorMap& xmap, const CUtensorMap& w
   if (a.split_k != 1) return cudaErrorInvalidValue;
   if (co == 32) return launch_co<32>(xmap, wmap, a, grid, smem, s);
   if (co == 64) return launch_co<64>(xmap, wmap, a, grid, smem, s);
+  if (co == 128) return launch_co<128>(xmap, wmap, a, grid, smem, s);
   return cudaErrorInvalidValue;
 }
 

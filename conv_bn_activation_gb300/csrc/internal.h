@@ -102,11 +102,20 @@ int igemm_stages(int bn, int kc);
 // shared-memory tile of input rows per 32-channel chunk serves all nine taps
 // (igemm_halo.cuh).
 struct HaloArgs {
-  int H, W, Wp;        // input = output height / width; Wp = W + 2 (padded width)
+  // Stride 1: input = output size; output pixels of a column block of blk_w
+  // columns are numbered over Wp = blk_w + 2.  Stride 2: the input is loaded
+  // as four phase tiles (even / odd rows x columns) and the output pixels are
+  // numbered over Wp = blk_w + 1.  n_blk column blocks per image.
+  int H, W, Wp;        // input height / width; Wp = padded width of the pixel numbering
+  int stride;          // 1 or 2
+  int OH, OW;          // output height / width
+  int blk_w, n_blk;    // output columns per block, blocks per image row
+  int tiles_per_blk;   // ceil(OH * Wp / PX)
+  int phase_bytes;     // stride 2: shared-memory bytes of one phase tile (halo_bytes = 4 of them)
   int Cout;
   int kc;              // input channels per chunk: 32, or 16 (64-byte rows)
   int num_kc;          // Cin / kc
-  int tiles_per_img;   // ceil(H * Wp / 128)
+  int tiles_per_img;   // n_blk * tiles_per_blk
   int m_tiles;         // N * tiles_per_img
   int n_tiles;         // ceil(Cout / BN)
   int rows;            // input rows per halo copy
@@ -125,8 +134,8 @@ struct HaloArgs {
 // Input rows one halo copy spans for a tile of px pixels at padded width
 // wp, and the buffer bytes (rows * wp pixels of 128 bytes, plus 8 rows that
 // only the discarded padding columns of the last rows read).
-int halo_rows(int wp, int px);
-int halo_buffer_bytes(int wp, int px, int kc = 32);
+int halo_rows(int wp, int px, int stride = 1);
+int halo_buffer_bytes(int wp, int px, int kc = 32, int stride = 1);
 size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages, int taps_per_stage = 1, int kc = 32);
 // Shared-memory bytes a split-K CTA receives from its partner (half of one
 // accumulator), which must fit in its halo and weight buffers.

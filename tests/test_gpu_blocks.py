@@ -20,6 +20,14 @@ from gpu_util import TOL_TF32, canary_buffer, is_canary, rel_err, sync_check, to
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True)
+def no_halo_tiles():
+    """Policy 2 (tensor cores without the halo kernel) keeps every case on the im2col-path kernel."""
+    cb.set_kernel_policy(2)
+    yield
+    cb.set_kernel_policy(0)
+
+
 @pytest.fixture
 def blocks_mode():
     old = os.environ.pop("CB_IGEMM_BLOCKS", None)
@@ -83,10 +91,10 @@ def test_pixel_blocks_epilogues_and_views(gpu, orc, blocks_mode, act, res_mode):
 @pytest.mark.parametrize("case", [(16, 320, 320, 16, 32, 3, 2), (32, 160, 160, 16, 16, 3, 1)],
                          ids=["dense-16-32@320s2-b16", "yolo-16-16@160-b32"])
 def test_pixel_blocks_workload_layers_sampled(gpu, orc, case):
-    """The 16-channel layers of the dense sweep and the YOLO chain at full batch, in the launch
-    configuration the benchmarks time (the stride-1 one takes the halo tiles); sampled outputs."""
+    """The 16-channel layers of the dense sweep and the YOLO chain at full batch on the im2col-path
+    kernel (the benchmarks run them on halo tiles); sampled outputs."""
     N, H, W, Ci, Co, k, s = case
-    x, w, bn, y = _layer_out(case, seed=5, paths=(cb.PATH_TC_IM2COL, cb.PATH_TC_HALO))
+    x, w, bn, y = _layer_out(case, seed=5)
     idx = np.random.default_rng(Ci + H).choice(y.numel(), 6000, replace=False)
     idx = np.concatenate([idx, [0, y.numel() - 1]])
     ref = orc.conv_bn_act_points(x, w, bn, idx, stride=s, pad=1, act=orc.ACT_SILU)

@@ -127,12 +127,12 @@ def test_halo_not_taken_outside_its_shapes(gpu):
     x = torch.empty(1, 8, 8, 40, device="cuda")  # Cin % 16 != 0
     y = torch.empty(1, 8, 8, 32, device="cuda")
     assert cb.conv_path(x, y, 3, 1, 1) == cb.PATH_TC_IM2COL
-    x = torch.empty(1, 8, 300, 32, device="cuda")  # too wide for two halo buffers
-    y = torch.empty(1, 8, 300, 32, device="cuda")
-    assert cb.conv_path(x, y, 3, 1, 1) == cb.PATH_TC_IM2COL
-    x = torch.empty(1, 8, 8, 32, device="cuda")
+    x = torch.empty(1, 8, 8, 40, device="cuda")  # stride 2 with Cin % 16 != 0
     y = torch.empty(1, 4, 4, 32, device="cuda")
     assert cb.conv_path(x, y, 3, 2, 1) == cb.PATH_TC_IM2COL
+    x = torch.empty(1, 8, 8, 32, device="cuda")  # 1x1
+    y = torch.empty(1, 8, 8, 48, device="cuda")
+    assert cb.conv_path(x, y, 1, 1, 0) == cb.PATH_TC_IM2COL
 
 
 @pytest.mark.parametrize("case", [(64, 64, 80), (128, 128, 40), (256, 256, 20)], ids=lambda s: "%d-%d@%d" % s)
@@ -265,3 +265,70 @@ def test_halo_16_channel_chunks_epilogues_and_views(gpu, orc, halo_force, force,
     ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=act, residual=r, res_mode=res_mode)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
     assert is_canary(buf[:, :, W:, :]) and is_canary(buf[:, :, :W, :4]) and is_canary(buf[:, :, :W, 4 + Co:])
+
+
+def _run_s(x, w, bn, s, act=cb.ACT_SILU, residual=None, res_mode=0, y=None):
+    N, H, W, _ = x.shape
+    layer = ConvBnAct(w, bn, s, 1, act)
+    OH, OW = layer.out_hw(H, W)
+    if y is None:
+        y = torch.empty(N, OH, OW, w.shape[0], device="cuda")
+    xd = to_dev(x)
+    assert cb.conv_path(xd, y, 3, s, 1) in (cb.PATH_TC_HALO, cb.PATH_TC_HALO_CM)
+    layer(xd, y, residual=residual, res_mode=res_mode)
+    sync_check()
+    return y
+
+
+S2_CASES = [
+    # N, H, W, Cin, Cout: stride 2 as four phase tiles per 16-channel chunk; one and several
+    # column blocks, odd sizes, tiny images, 128 output channels
+    (2, 32, 32, 16, 32), (1, 40, 40, 16, 64), (2, 21, 23, 32, 64), (1, 9, 13, 48, 128), (1, 30, 300, 16, 32),
+    (1, 2, 5, 16, 32), (3, 17, 33, 64, 100), (1, 1, 1, 16, 16),
+]
+
+
+@pytest.mark.parametrize("case", S2_CASES, ids=lambda s: "x".join(map(str, s)))
+def test_halo_stride2_phases(gpu, orc, case):
+    N, H, W, Ci, Co = case
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=sum(case) + 11)
+    y = _run_s(x, w, bn, 2)
+    ref = orc.conv_bn_act(x, w, bn, stride=2, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("act,res_mode", [(1, 1), (2, 2), (0, 0)])
+def test_halo_stride2_epilogues_and_views(gpu, orc, act, res_mode):
+    N, H, W, Ci, Co = 2, 26, 70, 32, 48
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=91 + act)
+    OH, OW = (H - 1) // 2 + 1, (W - 1) // 2 + 1
+    r = np.random.default_rng(12).standard_normal((N, OH, OW, Co)).astype(np.float32)
+    buf = canary_buffer((N, OH, OW + 5, Co + 24))
+    y = buf[:, :, :OW, 8:8 + Co]
+    _run_s(x, w, bn, 2, act=act, residual=to_dev(r) if res_mode else None, res_mode=res_mode, y=y)
+    ref = orc.conv_bn_act(x, w, bn, stride=2, pad=1, act=act, residual=r if res_mode else None, res_mode=res_mode)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+    assert is_canary(buf[:, :, OW:, :]) and is_canary(buf[:, :, :OW, :8]) and is_canary(buf[:, :, :OW, 8 + Co:])
+
+
+def test_halo_stride1_column_blocks(gpu, orc):
+    """Images wider than one halo copy (W + 2 > 256): column blocks."""
+    x, w, bn = synthetic.dense_layer(32, 48, 5, 300, N=2, k=3, seed=17)
+    y = _run(x, w, bn)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("case", [(16, 320, 16, 32), (16, 160, 32, 64), (16, 80, 64, 128), (32, 320, 16, 32)],
+                         ids=["16-32@320-b16", "32-64@160-b16", "64-128@80-b16", "16-32@320-b32"])
+def test_halo_stride2_workload_layers_sampled(gpu, orc, case):
+    """The stride-2 layers of the dense sweep and the YOLO chain at full batch, in the launch
+    configuration the benchmarks time; sampled outputs."""
+    N, H, Ci, Co = case
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, N=N, k=3, seed=H + Ci)
+    y = _run_s(x, w, bn, 2)
+    idx = np.random.default_rng(Ci).choice(y.numel(), 6000, replace=False)
+    idx = np.concatenate([idx, [0, y.numel() - 1]])
+    ref = orc.conv_bn_act_points(x, w, bn, idx, stride=2, pad=1, act=orc.ACT_SILU)
+    got = y.reshape(-1)[torch.from_numpy(idx).to("cuda")].cpu().numpy()
+    assert rel_err(got, ref) <= TOL_TF32
