@@ -372,6 +372,7 @@ struct HaloPlan {
   int stride = 1;      // 2: four phase tiles per chunk
   int blk_w = 0, n_blk = 1, wp = 0;  // column blocks and the padded width of the pixel numbering
   size_t smem = 0;
+  double cost = 0;     // the cost model's cycles per CTA
 };
 struct ImPlan {        // im2col kernel choices (0 = the cost model's)
   int bn = 0, stages = 0;
@@ -675,7 +676,11 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
       // tile and one exposed epilogue.
       const int n = sh.cm ? sh.px : sh.co;
       const double mma = 9.0 * (kc / 8) * (n > 128 ? 128.0 : 120.0) + (9.0 / tps) * 100.0;
-      const double copy = ((stride == 1 ? 1.0 : 4.0) + 9.0 / tps) * 550.0;
+      // measured: ~550 cycles per stride-1 halo copy or weight copy of up to
+      // 256 rows (longer boxes in proportion), ~800 per phase tile (a wider
+      // strided box)
+      const double wcopy = 550.0 * std::max(1.0, sh.co * tps / 256.0);
+      const double copy = (stride == 1 ? 550.0 : 4.0 * 800.0) + 9.0 / tps * wcopy;
       const double epi = sh.px * sh.co / 2.3;
       const size_t smem = halo_smem_bytes(sh.co, hb, nb, tps, kc);
       for (int split = 1; split <= 2; ++split) {
@@ -710,6 +715,7 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
           plan.split = split;
           plan.grid = static_cast<int>(split == 2 ? 2 * tiles : grid);
           plan.smem = smem;
+          plan.cost = cost;
         }
       }
       break;  // the fewest blocks that fit
@@ -769,8 +775,22 @@ cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, i
     DeviceInfo* dev = nullptr;
     HaloPlan tmp;
     HaloPlan& p = plan ? *plan : tmp;
-    if (current_device(&dev) == CB_OK && plan_halo(x, y, stride, dev->sms, halo_force_env(), &p))
-      return p.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
+    const HaloForce f = halo_force_env();
+    if (current_device(&dev) == CB_OK && plan_halo(x, y, stride, dev->sms, f, &p)) {
+      // against the im2col-path kernel: two copies (~570 cycles each) per
+      // (tap, chunk) of 128 pixels, or the MMAs of the step
+      const long long M = static_cast<long long>(y->n) * y->h * y->w;
+      const int kc = x->c <= 8 ? 8 : (x->c <= 16 ? 16 : 32);
+      const int k_iters = 9 * ((x->c + kc - 1) / kc);
+      int n_tiles = 1;
+      const int bn = pick_bn(static_cast<int>(std::min<long long>(M, 1LL << 30)), y->c, k_iters, dev->sms, &n_tiles);
+      const long long tiles = (M + 127) / 128 * n_tiles;
+      const long long per_cta = (tiles + dev->sms - 1) / dev->sms;
+      const double im = per_cta * (k_iters * std::max(1140.0, kc / 8 * (bn > 128 ? 128.0 : 120.0) + 100.0) + 1500.0) +
+                        128.0 * bn / 2.3;
+      const bool forced = f.co || f.cm || f.nb || f.split || f.tps;
+      if (forced || stride == 1 || p.cost <= im) return p.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
+    }
   }
   return CB_PATH_TC_IM2COL;
 }

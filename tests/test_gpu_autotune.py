@@ -39,9 +39,11 @@ def igemm_force():
 
 
 @pytest.mark.parametrize("bn", [16, 32, 48, 64, 96, 128, 192, 256])
-def test_im2col_every_tile_width(gpu, orc, igemm_force, bn):
-    """Stride 2, a ragged last pixel tile and a ragged last channel tile for each width."""
+def test_im2col_every_tile_width(gpu, orc, igemm_force, fresh_table, bn):
+    """Stride 2, a ragged last pixel tile and a ragged last channel tile for each width (policy 2
+    keeps the layer on the im2col-path kernel)."""
     igemm_force(f"{bn},0")
+    cb.set_kernel_policy(2)
     N, H, Ci, Co = 2, 23, 32, 200
     x, w, bn_p = synthetic.dense_layer(Ci, Co, H, N=N, k=3, seed=bn)
     layer = ConvBnAct(w, bn_p, 2, 1, cb.ACT_SILU)
