@@ -256,12 +256,17 @@ OutView make_out(const cb_tensor* y) {
   return o;
 }
 
-// Which dense layers go to the tensor cores.  The copy engine's cost per
-// K step grows with the number of 128-pixel rows it gathers, not with their
-// width, so a 3x3 layer with under 16 input channels (nine narrow gathers
-// per tile) runs faster on the CUDA-core direct kernel; 1x1 layers take the
-// tensor cores from 8 channels on.
-bool tc_channels_ok(int ci, int k) { return k == 1 ? ci >= 8 : ci >= 16; }
+// Which dense layers go to the tensor cores.  A 3x3 layer with under 16
+// input channels runs faster on the CUDA-core direct kernel: on the im2col
+// path it spends nine narrow gathers per tile (an SM completes about one
+// copy per 400-700 cycles), and a halo tile of 8-channel rows over a wide
+// image moves four 32-byte rows per output pixel (measured on 8 -> 8 at
+// 320x320: 457 us against 155 us direct).  1x1 layers take the tensor cores
+// from 8 channels on.
+bool tc_channels_ok(int ci, int k, int stride) {
+  (void)stride;
+  return k == 1 ? ci >= 8 : ci >= 16;
+}
 
 // ----------------------------------------------------------------- depthwise
 cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, int stride, int pad,
@@ -633,7 +638,7 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
   // 32-channel chunks (128-byte rows); 16-channel chunks (64-byte rows) for
   // Ci % 32 == 16 and at stride 2 (four phase tiles per chunk), in the
   // pixel-major 128 x {32, 64, 128} tiles
-  const int kc = (stride == 1 && Ci % 32 == 0) ? 32 : (Ci % 16 == 0 ? 16 : 0);
+  const int kc = (stride == 1 && Ci % 32 == 0) ? 32 : Ci % 16 == 0 ? 16 : (stride == 1 && Ci % 8 == 0) ? 8 : 0;
   if (kc == 0) return false;
   const int num_kc = Ci / kc;
   constexpr size_t kSmemMax = 227 * 1024;
@@ -655,6 +660,7 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
     if (f.co && (sh.cm || sh.co != f.co)) continue;
     if (kc == 16 && (sh.cm || sh.co > 128)) continue;
     if (kc == 16 && sh.co == 128 && stride == 1) continue;
+    if (kc == 8 && (sh.cm || sh.co != 32)) continue;
     for (int n_blk = min_blocks; n_blk <= min_blocks + 3 && n_blk <= OW; ++n_blk) {
       const int blk_w = (OW + n_blk - 1) / n_blk;
       const int wp = blk_w + (stride == 1 ? 2 : 1);
@@ -747,7 +753,8 @@ bool stem_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int p
 
 // Shape rule of the tensor-core paths (views aside).
 bool tc_shape(int ci, int co, int kh, int stride, int pad) {
-  return g_policy.load() != 1 && ci % 4 == 0 && tc_channels_ok(ci, kh) && !pointwise_shape(ci, co, kh, stride, pad);
+  return g_policy.load() != 1 && ci % 4 == 0 && tc_channels_ok(ci, kh, stride) &&
+         !pointwise_shape(ci, co, kh, stride, pad);
 }
 
 cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan, ImPlan* im) {
@@ -856,7 +863,9 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
                          st * static_cast<cuuint32_t>(a.rows), 1};
     cuuint32_t estr[4] = {1, st, st, 1};
     CUresult r = tiled_map(&xmap, 4, x->data, dims, strides, box, estr,
-                           plan.kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                           plan.kc == 32   ? CU_TENSOR_MAP_SWIZZLE_128B
+                           : plan.kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_32B);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   {
@@ -868,7 +877,9 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
                          static_cast<cuuint32_t>(plan.tps)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = tiled_map(&wmap, 3, w, dims, strides, box, estr,
-                           plan.kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                           plan.kc == 32   ? CU_TENSOR_MAP_SWIZZLE_128B
+                           : plan.kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                           : CU_TENSOR_MAP_SWIZZLE_32B);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   cudaError_t e = launch_igemm_halo(xmap, wmap, a, plan.px, plan.co, plan.cm, plan.grid, plan.smem, s);
@@ -1093,7 +1104,7 @@ cb_status launch_conv(const cb_tensor* x, const float* w, const float* scale, co
 std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, int sms) {
   std::vector<ConvPlan> out;
   const int Ci = x->c, Co = y->c;
-  if (kh == 3 && pad == 1 && Ci % 16 == 0 && g_policy.load() == 0) {
+  if (kh == 3 && pad == 1 && Ci % 8 == 0 && g_policy.load() == 0) {
     // every halo tile shape x taps per weight stage x split, each planned
     // under those constraints (ring depth, column blocks and grid follow)
     struct Shape {

@@ -94,6 +94,8 @@ cudaError_t launch_igemm_halo_cm(const CUtensorMap& xmap, const CUtensorMap& wma
                                  size_t smem, cudaStream_t s);
 cudaError_t launch_igemm_halo_kc16(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int co,
                                    int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_igemm_halo_kc8(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int co,
+                                  int grid, size_t smem, cudaStream_t s);
 
 cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
                               bool cm, int grid, size_t smem, cudaStream_t s) {
@@ -112,6 +114,7 @@ cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, 
       return cudaErrorInvalidValue;
   }
   if (a.kc == 16) return !cm && px == 128 ? launch_igemm_halo_kc16(xmap, wmap, a, co, grid, smem, s) : cudaErrorInvalidValue;
+  if (a.kc == 8) return !cm && px == 128 ? launch_igemm_halo_kc8(xmap, wmap, a, co, grid, smem, s) : cudaErrorInvalidValue;
   if (a.kc != 32) return cudaErrorInvalidValue;
   if (cm) return px == 256 && co == 128 ? launch_igemm_halo_cm(xmap, wmap, a, grid, smem, s) : cudaErrorInvalidValue;
   if (px != 128) return cudaErrorInvalidValue;

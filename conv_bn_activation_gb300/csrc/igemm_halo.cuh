@@ -82,8 +82,8 @@ template <int PX, int CO, bool CM, int KC = kHaloKc>
 __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                      const __grid_constant__ CUtensorMap wmap,
                                                                      const HaloArgs a) {
-  static_assert(KC == 32 || KC == 16, "channels per chunk");
-  constexpr int kRowBytes = KC * 4;  // one pixel's chunk: 128 or 64 bytes, swizzled to match
+  static_assert(KC == 32 || KC == 16 || KC == 8, "channels per chunk");
+  constexpr int kRowBytes = KC * 4;  // one pixel's chunk: 128, 64 or 32 bytes, swizzled to match
   static_assert(CM ? (PX == 256 && CO == 128) : (PX == 128 && (CO == 32 || CO == 64 || CO == 128 || CO == 256)),
                 "tile shape");
   const unsigned long long t_start = a.trace ? trace_globaltimer() : 0;

@@ -78,7 +78,8 @@ def test_small_channel_direct(gpu, orc, stem):
     y = torch.empty(2, OH, OW, Co, device=gpu)
     layer(to_dev(x), y)
     sync_check()
-    assert rel_err(y.cpu().numpy(), orc.conv_bn_act(x, w, bn, stride=s, pad=1, act=orc.ACT_SILU)) <= TOL_FP32
+    tol = TOL_TF32 if _is_tc(Ci, Co, 3, s) else TOL_FP32  # 8-channel stride-1 layers take halo tiles
+    assert rel_err(y.cpu().numpy(), orc.conv_bn_act(x, w, bn, stride=s, pad=1, act=orc.ACT_SILU)) <= tol
 
 
 def test_nchw_input_stem(gpu, orc):

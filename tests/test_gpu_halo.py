@@ -124,7 +124,7 @@ def test_halo_matches_im2col_kernel(gpu):
 
 
 def test_halo_not_taken_outside_its_shapes(gpu):
-    x = torch.empty(1, 8, 8, 40, device="cuda")  # Cin % 16 != 0
+    x = torch.empty(1, 8, 8, 36, device="cuda")  # Cin % 8 != 0
     y = torch.empty(1, 8, 8, 32, device="cuda")
     assert cb.conv_path(x, y, 3, 1, 1) == cb.PATH_TC_IM2COL
     x = torch.empty(1, 8, 8, 40, device="cuda")  # stride 2 with Cin % 16 != 0
@@ -321,10 +321,12 @@ def test_halo_stride1_column_blocks(gpu, orc):
 
 @pytest.mark.parametrize("case", [(16, 320, 16, 32), (16, 160, 32, 64), (16, 80, 64, 128), (32, 320, 16, 32)],
                          ids=["16-32@320-b16", "32-64@160-b16", "64-128@80-b16", "16-32@320-b32"])
-def test_halo_stride2_workload_layers_sampled(gpu, orc, case):
-    """The stride-2 layers of the dense sweep and the YOLO chain at full batch, in the launch
-    configuration the benchmarks time; sampled outputs."""
+def test_halo_stride2_workload_layers_sampled(gpu, orc, halo_force, case):
+    """The stride-2 layers of the dense sweep and the YOLO chain at full batch on stride-2 halo
+    tiles of their channel width (the cost model may send the wider ones to the im2col-path
+    kernel); sampled outputs."""
     N, H, Ci, Co = case
+    halo_force(str(Co))
     x, w, bn = synthetic.dense_layer(Ci, Co, H, N=N, k=3, seed=H + Ci)
     y = _run_s(x, w, bn, 2)
     idx = np.random.default_rng(Ci).choice(y.numel(), 6000, replace=False)
@@ -332,3 +334,14 @@ def test_halo_stride2_workload_layers_sampled(gpu, orc, case):
     ref = orc.conv_bn_act_points(x, w, bn, idx, stride=2, pad=1, act=orc.ACT_SILU)
     got = y.reshape(-1)[torch.from_numpy(idx).to("cuda")].cpu().numpy()
     assert rel_err(got, ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("case", [(2, 9, 40, 24, 8), (1, 20, 20, 40, 32), (3, 7, 13, 24, 16), (1, 1, 1, 56, 8)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_halo_8_channel_chunks(gpu, orc, case):
+    """32-byte pixel rows with the 32-byte swizzle (Cin % 16 == 8), pixel-major 128 x 32 tiles."""
+    N, H, W, Ci, Co = case
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=sum(case) + 5)
+    y = _run(x, w, bn)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32

@@ -82,7 +82,8 @@ def test_yolo_chain_full_size_per_layer(gpu, orc):
             idx = rng.choice(got.size, min(got.size, 3000), replace=False)
             ref = orc.conv_bn_act_points(inp, w, bn, idx, stride=s, pad=p, act=orc.ACT_SILU, residual=res,
                                          res_mode=orc.RES_POST_ACT if res is not None else orc.RES_NONE)
-            tol = TOL_TF32 if (inp.shape[-1] >= 16 or (inp.shape[-1] >= 8 and w.shape[2] == 1)) else TOL_FP32
+            tc = cb.layer_uses_tensor_cores(inp.shape[-1], w.shape[0], w.shape[2], s)
+            tol = TOL_TF32 if tc else TOL_FP32
             assert rel_err(got.reshape(-1)[idx], ref) <= tol
         h = out
 
