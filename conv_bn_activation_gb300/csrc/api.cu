@@ -376,6 +376,7 @@ struct HaloPlan {
   int kc = 32;         // input channels per chunk (32, or 16 for Ci % 32 == 16 and for stride 2)
   int stride = 1;      // 2: four phase tiles per chunk
   int blk_w = 0, n_blk = 1, wp = 0;  // column blocks and the padded width of the pixel numbering
+  int sub = 1;         // 128-pixel sub-tiles per tile sharing one halo copy
   size_t smem = 0;
   double cost = 0;     // the cost model's cycles per CTA
 };
@@ -388,7 +389,7 @@ struct ImPlan {        // im2col kernel choices (0 = the cost model's)
 struct HaloForce {
   int co = 0;
   bool cm = false;
-  int nb = 0, split = 0, tps = 0;
+  int nb = 0, split = 0, tps = 0, sub = 0;
 };
 HaloForce halo_force_env();
 bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, const HaloForce& f, HaloPlan* out);
@@ -620,14 +621,14 @@ bool halo_ring(int co, int hb, int force_nb, int force_tps, int* nb_out, int* tp
 }
 
 HaloForce halo_force_env() {
-  // CB_HALO_FORCE = "cm[,stages[,split[,taps]]]" or "co[,stages[,split[,taps]]]", read per call
+  // CB_HALO_FORCE = "cm[,stages[,split[,taps]]]" or "co[,stages[,split[,taps[,subtiles]]]]", read per call
   HaloForce f;
   if (const char* e = std::getenv("CB_HALO_FORCE")) {
     if (e[0] == 'c' && e[1] == 'm') {
       f.cm = true;
       if (e[2] == ',') std::sscanf(e + 3, "%d,%d,%d", &f.nb, &f.split, &f.tps);
     } else {
-      std::sscanf(e, "%d,%d,%d,%d", &f.co, &f.nb, &f.split, &f.tps);
+      std::sscanf(e, "%d,%d,%d,%d,%d", &f.co, &f.nb, &f.split, &f.tps, &f.sub);
     }
   }
   return f;
@@ -661,70 +662,75 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
     if (kc == 16 && (sh.cm || sh.co > 128)) continue;
     if (kc == 16 && sh.co == 128 && stride == 1) continue;
     if (kc == 8 && (sh.cm || sh.co != 32)) continue;
-    for (int n_blk = min_blocks; n_blk <= min_blocks + 3 && n_blk <= OW; ++n_blk) {
-      const int blk_w = (OW + n_blk - 1) / n_blk;
-      const int wp = blk_w + (stride == 1 ? 2 : 1);
-      const int rows = halo_rows(wp, sh.px, stride);
-      if (rows * stride > 256) continue;
-      const int hb = halo_buffer_bytes(wp, sh.px, kc, stride);
-      int nb = 0, tps = 1;
-      if (!halo_ring(sh.co, hb, f.nb, f.tps, &nb, &tps, kc)) continue;
-      const long long m_tiles = static_cast<long long>(N) * n_blk * ((OH * wp + sh.px - 1) / sh.px);
-      const long long tiles = m_tiles * ((Co + sh.co - 1) / sh.co);
-      if (tiles >= (1LL << 31)) continue;
-      const long long grid = std::min<long long>(tiles, sms);
-      const long long per_cta = (tiles + grid - 1) / grid;
-      // Cycles per (tile, chunk): nine taps of kc / 8 MMAs, each about 120
-      // issue cycles for N <= 128 and 128 for N = 256 (measured), plus the
-      // barrier round trip per weight stage; against the copies (an SM
-      // completes about one per 400-700 cycles): one halo (four phase tiles
-      // at stride 2) and 9 / tps weight stages.  Plus the pipeline fill per
-      // tile and one exposed epilogue.
-      const int n = sh.cm ? sh.px : sh.co;
-      const double mma = 9.0 * (kc / 8) * (n > 128 ? 128.0 : 120.0) + (9.0 / tps) * 100.0;
-      // measured: ~550 cycles per stride-1 halo copy or weight copy of up to
-      // 256 rows (longer boxes in proportion), ~800 per phase tile (a wider
-      // strided box)
-      const double wcopy = 550.0 * std::max(1.0, sh.co * tps / 256.0);
-      const double copy = (stride == 1 ? 550.0 : 4.0 * 800.0) + 9.0 / tps * wcopy;
-      const double epi = sh.px * sh.co / 2.3;
-      const size_t smem = halo_smem_bytes(sh.co, hb, nb, tps, kc);
-      for (int split = 1; split <= 2; ++split) {
-        if (f.split && split != f.split) continue;
-        double cost;
-        if (split == 1) {
-          cost = static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 1500.0) + epi;
-        } else {
-          // one tile per CTA pair, each CTA half of the chunks; the partner's
-          // half accumulator comes over distributed shared memory (~16 B per
-          // clock) and each CTA stores half the tile
-          const size_t recv = halo_split_recv_bytes(sh.px, sh.co, sh.cm);
-          if (stride != 1 || kc != 32 || num_kc < 2 || (!sh.cm && sh.co < 64) ||
-              recv > 2 * static_cast<size_t>(hb) + nb * tps * sh.co * 128ull || 2 * tiles > sms ||
-              halo_max_pairs(sh.px, sh.co, sh.cm, smem) < tiles)
-            continue;
-          cost = (num_kc - num_kc / 2) * std::max(mma, copy) + 1500.0 + recv / 16.0 + 1000.0 + epi / 2;
+    for (int sub = 1; sub <= kHaloMaxSub; sub *= 2) {
+      if (f.sub && sub != f.sub) continue;
+      if (sub > 1 && (sh.cm || sh.co > 64)) continue;
+      for (int n_blk = min_blocks; n_blk <= min_blocks + 3 && n_blk <= OW; ++n_blk) {
+        const int blk_w = (OW + n_blk - 1) / n_blk;
+        const int wp = blk_w + (stride == 1 ? 2 : 1);
+        const int rows = halo_rows(wp, sh.px * sub, stride);
+        if (rows * stride > 256) continue;
+        const int hb = halo_buffer_bytes(wp, sh.px * sub, kc, stride);
+        int nb = 0, tps = 1;
+        if (!halo_ring(sh.co, hb, f.nb, f.tps, &nb, &tps, kc)) continue;
+        const long long px_tiles = (static_cast<long long>(OH) * wp + sh.px - 1) / sh.px;
+        const long long m_tiles = static_cast<long long>(N) * n_blk * ((px_tiles + sub - 1) / sub);
+        const long long tiles = m_tiles * ((Co + sh.co - 1) / sh.co);
+        if (tiles >= (1LL << 31)) continue;
+        const long long grid = std::min<long long>(tiles, sms);
+        const long long per_cta = (tiles + grid - 1) / grid;
+        // Cycles per (tile, chunk): nine taps of kc / 8 MMAs per sub-tile,
+        // each about 120 issue cycles for N <= 128 and 128 for N = 256
+        // (measured), plus the barrier round trip per weight stage; against
+        // the copies (an SM completes them one after another): the halo
+        // (~300 cycles + ~2 per row of the box; four phase tiles of ~800
+        // at stride 2) and 9 / tps weight copies of ~550 cycles per 256
+        // rows.  Plus the pipeline fill per tile and one exposed epilogue.
+        const int n = sh.cm ? sh.px : sh.co;
+        const double mma = sub * 9.0 * (kc / 8) * (n > 128 ? 128.0 : 120.0) + (9.0 / tps) * 100.0;
+        const double wcopy = 550.0 * std::max(1.0, sh.co * tps / 256.0);
+        const double hcopy = stride == 1 ? 300.0 + 2.0 * rows * wp : 4.0 * 800.0 * (1.0 + 0.5 * (sub - 1));
+        const double copy = hcopy + 9.0 / tps * wcopy;
+        const double epi = sh.px * sh.co / 2.3;
+        const size_t smem = halo_smem_bytes(sh.co, hb, nb, tps, kc);
+        for (int split = 1; split <= 2; ++split) {
+          if (f.split && split != f.split) continue;
+          double cost;
+          if (split == 1) {
+            cost = static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 1500.0) + epi;
+          } else {
+            // one tile per CTA pair, each CTA half of the chunks; the partner's
+            // half accumulator comes over distributed shared memory (~16 B per
+            // clock) and each CTA stores half the tile
+            const size_t recv = halo_split_recv_bytes(sh.px, sh.co, sh.cm);
+            if (sub != 1 || stride != 1 || kc != 32 || num_kc < 2 || (!sh.cm && sh.co < 64) ||
+                recv > 2 * static_cast<size_t>(hb) + nb * tps * sh.co * 128ull || 2 * tiles > sms ||
+                halo_max_pairs(sh.px, sh.co, sh.cm, smem) < tiles)
+              continue;
+            cost = (num_kc - num_kc / 2) * std::max(mma, copy) + 1500.0 + recv / 16.0 + 1000.0 + epi / 2;
+          }
+          cost *= 1.0 + 0.02 * (n_blk - min_blocks);  // fewer blocks: less halo overlap
+          if (cost < best * 0.97) {
+            best = cost;
+            plan.px = sh.px;
+            plan.co = sh.co;
+            plan.cm = sh.cm;
+            plan.nb = nb;
+            plan.tps = tps;
+            plan.kc = kc;
+            plan.stride = stride;
+            plan.blk_w = blk_w;
+            plan.n_blk = n_blk;
+            plan.wp = wp;
+            plan.sub = sub;
+            plan.split = split;
+            plan.grid = static_cast<int>(split == 2 ? 2 * tiles : grid);
+            plan.smem = smem;
+            plan.cost = cost;
+          }
         }
-        cost *= 1.0 + 0.02 * (n_blk - min_blocks);  // fewer blocks: less halo overlap
-        if (cost < best * 0.97) {
-          best = cost;
-          plan.px = sh.px;
-          plan.co = sh.co;
-          plan.cm = sh.cm;
-          plan.nb = nb;
-          plan.tps = tps;
-          plan.kc = kc;
-          plan.stride = stride;
-          plan.blk_w = blk_w;
-          plan.n_blk = n_blk;
-          plan.wp = wp;
-          plan.split = split;
-          plan.grid = static_cast<int>(split == 2 ? 2 * tiles : grid);
-          plan.smem = smem;
-          plan.cost = cost;
-        }
+        break;  // the fewest blocks that fit
       }
-      break;  // the fewest blocks that fit
     }
   }
   if (plan.px == 0) return false;
@@ -820,12 +826,14 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   a.Cout = Co;
   a.kc = plan.kc;
   a.num_kc = Ci / plan.kc;
-  a.tiles_per_blk = (a.OH * a.Wp + plan.px - 1) / plan.px;
+  a.px_tiles_per_blk = (a.OH * a.Wp + plan.px - 1) / plan.px;
+  a.sub = plan.sub;
+  a.tiles_per_blk = (a.px_tiles_per_blk + plan.sub - 1) / plan.sub;
   a.tiles_per_img = a.n_blk * a.tiles_per_blk;
   a.m_tiles = x->n * a.tiles_per_img;
   a.n_tiles = (Co + plan.co - 1) / plan.co;
-  a.rows = halo_rows(a.Wp, plan.px, plan.stride);
-  a.halo_bytes = halo_buffer_bytes(a.Wp, plan.px, plan.kc, plan.stride);
+  a.rows = halo_rows(a.Wp, plan.px * plan.sub, plan.stride);
+  a.halo_bytes = halo_buffer_bytes(a.Wp, plan.px * plan.sub, plan.kc, plan.stride);
   a.phase_bytes = plan.stride == 2 ? a.halo_bytes / 4 : 0;
   a.nb_stages = plan.nb;
   a.taps_per_stage = plan.tps;
@@ -845,10 +853,10 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   }
   if (std::getenv("CB_DEBUG_PLAN"))
     std::fprintf(stderr,
-                 "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d s=%d -> %s px=%d co=%d kc=%d nb=%d tps=%d split=%d "
-                 "blocks=%dx%d rows=%d halo=%d tiles=%d grid=%d smem=%zu\n",
-                 x->n, a.H, a.W, Ci, Co, plan.stride, plan.cm ? "channel-major" : "pixel-major", plan.px, plan.co,
-                 plan.kc, plan.nb, plan.tps, plan.split, plan.n_blk, plan.blk_w, a.rows, a.halo_bytes,
+                 "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d s=%d -> %s px=%dx%d co=%d kc=%d nb=%d tps=%d "
+                 "split=%d blocks=%dx%d rows=%d halo=%d tiles=%d grid=%d smem=%zu\n",
+                 x->n, a.H, a.W, Ci, Co, plan.stride, plan.cm ? "channel-major" : "pixel-major", plan.sub, plan.px,
+                 plan.co, plan.kc, plan.nb, plan.tps, plan.split, plan.n_blk, plan.blk_w, a.rows, a.halo_bytes,
                  a.m_tiles * a.n_tiles, plan.grid, plan.smem);
   CUtensorMap xmap, wmap;
   {
@@ -1115,12 +1123,15 @@ std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int 
     for (const Shape& sh : kShapes) {
       if (!sh.cm && sh.co > 2 * ((Co + 15) / 16 * 16)) continue;  // a tile mostly beyond Co
       for (int tps : {9, 3, 1})
-        for (int split : {1, 2}) {
+        for (int split : {1, 2})
+          for (int sb : {1, 2, 4}) {
+          if (sb > 1 && (sh.cm || sh.co > 64 || split == 2)) continue;
           HaloForce f;
           f.co = sh.cm ? 0 : sh.co;
           f.cm = sh.cm;
           f.tps = tps;
           f.split = split;
+          f.sub = sb;
           ConvPlan p;
           if (!plan_halo(x, y, stride, sms, f, &p.halo)) continue;
           p.path = p.halo.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;

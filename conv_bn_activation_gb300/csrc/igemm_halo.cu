@@ -26,7 +26,7 @@ int halo_buffer_bytes(int wp, int px, int kc, int stride) {
 size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages, int taps_per_stage, int kc) {
   return 1024 /*alignment slack*/ + 2 * static_cast<size_t>(halo_bytes) +
          static_cast<size_t>(nb_stages) * taps_per_stage * co * kc * 4 + kHaloStagingBytes +
-         (4 + 2 * nb_stages + 2 * 4 + 2) * sizeof(uint64_t) + 16;
+         (4 + 2 * nb_stages + 2 * 8 + 2) * sizeof(uint64_t) + 16;
 }
 
 size_t halo_split_recv_bytes(int px, int co, bool cm) { return static_cast<size_t>(cm ? px : co) / 2 * 128 * 4; }
@@ -103,6 +103,7 @@ cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, 
   if (a.taps_per_stage != 1 && a.taps_per_stage != 3 && a.taps_per_stage != 9) return cudaErrorInvalidValue;
   if (a.split_k != 1 && a.split_k != 2) return cudaErrorInvalidValue;
   if (a.stride != 1 && a.stride != 2) return cudaErrorInvalidValue;
+  if (a.sub < 1 || a.sub > kHaloMaxSub || (a.sub > 1 && (cm || co > 64 || a.split_k != 1))) return cudaErrorInvalidValue;
   if (a.stride == 2 && (a.kc != 16 || a.phase_bytes * 4 != a.halo_bytes || a.Wp * 2 > 256 || a.rows * 2 > 256))
     return cudaErrorInvalidValue;
   if (a.split_k == 2) {

@@ -72,8 +72,10 @@ constexpr int kHaloStagingBytes = 8 * TileStore<32>::kBufBytes;  // 8 epilogue w
 
 // TMEM accumulators per CTA (the epilogue of one tile overlaps the MMAs of
 // the next ones) and the power-of-two column count they occupy, for an
-// accumulator of acc_cols columns.
-__host__ __device__ constexpr int halo_naccs(int acc_cols) { return acc_cols >= 256 ? 2 : 4; }
+// accumulator of acc_cols columns.  Narrow tiles keep eight, so that a tile
+// of up to four 128-pixel sub-tiles (one halo copy for all of them) can run
+// while the previous one is stored.
+__host__ __device__ constexpr int halo_naccs(int acc_cols) { return acc_cols >= 256 ? 2 : acc_cols <= 64 ? 8 : 4; }
 __host__ __device__ constexpr int halo_tmem_cols(int acc_cols) {
   return halo_naccs(acc_cols) * acc_cols <= 128 ? 128 : halo_naccs(acc_cols) * acc_cols <= 256 ? 256 : 512;
 }
@@ -88,6 +90,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
                 "tile shape");
   const unsigned long long t_start = a.trace ? trace_globaltimer() : 0;
   constexpr int kAccCols = CM ? PX : CO;  // TMEM columns of one accumulator
+  // Sub-tiles: a tile of nsub x 128 consecutive pixels shares one halo copy;
+  // each 128-pixel sub-tile has its own accumulator (pixel-major only).
+  const int sub = CM ? 1 : a.sub;
   constexpr int NACC = halo_naccs(kAccCols);
   constexpr uint32_t kTmemCols = halo_tmem_cols(kAccCols);
   constexpr int kTapBytes = CO * KC * 4;  // one tap's weight slice
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
         const int n_img = m_tile / a.tiles_per_img;
         const int rem = m_tile - n_img * a.tiles_per_img;
         const int blk = rem / a.tiles_per_blk;
-        const int q0 = (rem - blk * a.tiles_per_blk) * PX;
+        const int q0 = (rem - blk * a.tiles_per_blk) * PX * sub;
         const int y_lo = q0 / a.Wp;
         const int x0 = blk * a.blk_w - 1;  // first column of the tile (phase column at stride 2)
         for (int kc = kc_begin; ok && kc < kc_end; ++kc) {
@@ -242,17 +247,21 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       bool ok = true;
       int local = 0;
       TraceBuf tr;
-      for (int tile = tile0; ok && tile < num_tiles; tile += tile_step, ++local) {
-        const int acc = local % NACC;
-        const uint32_t acc_phase = (local / NACC) & 1;
+      for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
         const int m_tile = tile / a.n_tiles;
         const int n_img = m_tile / a.tiles_per_img;
         const int rem = m_tile - n_img * a.tiles_per_img;
-        const int q0 = (rem - (rem / a.tiles_per_blk) * a.tiles_per_blk) * PX;
+        const int gi = rem - (rem / a.tiles_per_blk) * a.tiles_per_blk;
+        const int q0 = gi * PX * sub;
+        const int nsub = min(sub, a.px_tiles_per_blk - gi * sub);
         const int base_row = q0 - (q0 / a.Wp) * a.Wp;
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, wd)) break;
+        // the accumulators of this tile's sub-tiles
+        for (int i = 0; ok && i < nsub; ++i) {
+          const int acc = (local + i) % NACC;
+          if (!mbar_wait(&tempty[acc], (((local + i) / NACC) & 1) ^ 1u, wd)) ok = false;
+        }
+        if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         for (int kc = kc_begin; ok && kc < kc_end; ++kc) {
           if (!mbar_wait(&hfull[h], hphase, wd)) {
             ok = false;
@@ -279,12 +288,15 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
                 x_addr = halo_addr + static_cast<uint32_t>(ph * a.phase_bytes) +
                          static_cast<uint32_t>((base_row + (dy != 0) * a.Wp + (dx != 0)) * kRowBytes);
               }
-              const uint64_t xdesc = kmajor_swizzled_desc(x_addr, kRowBytes);
               const uint64_t wdesc = kmajor_swizzled_desc(smem_u32(sB + s * kBBytes + t * kTapBytes), kRowBytes);
-              const uint64_t adesc = CM ? wdesc : xdesc, bdesc = CM ? xdesc : wdesc;
+              for (int i = 0; i < nsub; ++i) {
+                const uint64_t xdesc = kmajor_swizzled_desc(x_addr + static_cast<uint32_t>(i * PX * kRowBytes), kRowBytes);
+                const uint64_t adesc = CM ? wdesc : xdesc, bdesc = CM ? xdesc : wdesc;
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(((local + i) % NACC) * kAccCols);
 #pragma unroll
-              for (int kk = 0; kk < KC / 8; ++kk)
-                mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kc != kc_begin || tap || kk) ? 1u : 0u);
+                for (int kk = 0; kk < KC / 8; ++kk)
+                  mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kc != kc_begin || tap || kk) ? 1u : 0u);
+              }
             }
             mma_commit(&bempty[s]);
             tr.add(tr_cta);
@@ -307,10 +319,14 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
-        const uint32_t tbit = 1u << acc;
-        tparity = (tcommitted & tbit) ? (tparity ^ tbit) : (tparity & ~tbit);
-        tcommitted |= tbit;
+        for (int i = 0; i < nsub; ++i) {
+          const int acc = (local + i) % NACC;
+          mma_commit(&tfull[acc]);
+          const uint32_t tbit = 1u << acc;
+          tparity = (tcommitted & tbit) ? (tparity ^ tbit) : (tparity & ~tbit);
+          tcommitted |= tbit;
+        }
+        local += nsub;
       }
       // Let every MMA this thread issued finish before TMEM is released.
       for (int ss = 0; ss < a.nb_stages; ++ss)
@@ -332,7 +348,19 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
     int local = 0;
     TraceBuf tr;
     const bool tr_on = tr_cta && warp == 2 && lane == 0;
-    for (int tile = tile0; tile < num_tiles; tile += tile_step, ++local) {
+    for (int tile = tile0, si = 0, nsub = 0; tile < num_tiles; ++local) {
+      // walk the sub-tiles of each tile in turn
+      if (si == nsub) {
+        if (nsub) {
+          tile += tile_step;
+          if (tile >= num_tiles) break;
+        }
+        const int mt = tile / a.n_tiles, rm = mt - (mt / a.tiles_per_img) * a.tiles_per_img;
+        const int g = rm - (rm / a.tiles_per_blk) * a.tiles_per_blk;
+        nsub = min(sub, a.px_tiles_per_blk - g * sub);
+        si = 0;
+      }
+      const int sub_i = si++;
       if (kSplitTiles && (local & 1) != group) continue;
       const int acc = local % NACC;
       const uint32_t acc_phase = (local / NACC) & 1;
@@ -340,7 +368,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       const int n_img = m_tile / a.tiles_per_img;
       const int rem = m_tile - n_img * a.tiles_per_img;
       const int blk = rem / a.tiles_per_blk;
-      const int q0 = (rem - blk * a.tiles_per_blk) * PX;
+      const int q0 = ((rem - blk * a.tiles_per_blk) * sub + sub_i) * PX;
       // Element offsets of output pixel q (-1: a padding column or past the image).
       auto pixel_offsets = [&](int qq, long long& yoff, long long& roff) {
         const int oy = qq / a.Wp, oxl = qq - (qq / a.Wp) * a.Wp;

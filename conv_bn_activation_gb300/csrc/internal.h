@@ -110,7 +110,9 @@ struct HaloArgs {
   int stride;          // 1 or 2
   int OH, OW;          // output height / width
   int blk_w, n_blk;    // output columns per block, blocks per image row
-  int tiles_per_blk;   // ceil(OH * Wp / PX)
+  int px_tiles_per_blk;  // ceil(OH * Wp / PX): PX-pixel sub-tiles per column block
+  int sub;             // sub-tiles per tile (one halo copy for all of them; pixel-major only)
+  int tiles_per_blk;   // ceil(px_tiles_per_blk / sub)
   int phase_bytes;     // stride 2: shared-memory bytes of one phase tile (halo_bytes = 4 of them)
   int Cout;
   int kc;              // input channels per chunk: 32, or 16 (64-byte rows)
@@ -134,6 +136,7 @@ struct HaloArgs {
 // Input rows one halo copy spans for a tile of px pixels at padded width
 // wp, and the buffer bytes (rows * wp pixels of 128 bytes, plus 8 rows that
 // only the discarded padding columns of the last rows read).
+constexpr int kHaloMaxSub = 4;  // 128-pixel sub-tiles per halo tile, at most
 int halo_rows(int wp, int px, int stride = 1);
 int halo_buffer_bytes(int wp, int px, int kc = 32, int stride = 1);
 size_t halo_smem_bytes(int co, int halo_bytes, int nb_stages, int taps_per_stage = 1, int kc = 32);

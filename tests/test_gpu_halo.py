@@ -345,3 +345,37 @@ def test_halo_8_channel_chunks(gpu, orc, case):
     y = _run(x, w, bn)
     ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_SILU)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+SUB_CASES = [
+    # N, H, W, Cin, Cout, stride, CB_HALO_FORCE: tiles of 2 or 4 sub-tiles of 128 pixels sharing one
+    # halo copy; sub-tile counts that do not divide the tiles of a block, column blocks, 8/16/32-channel
+    # chunks, stride 2
+    (2, 9, 40, 32, 32, 1, "32,0,0,0,2"), (1, 20, 20, 64, 64, 1, "64,0,0,0,4"), (2, 7, 160, 16, 16, 1, "32,0,0,0,4"),
+    (1, 5, 300, 16, 32, 1, "32,0,0,0,2"), (3, 11, 17, 24, 32, 1, "32,0,0,0,4"), (1, 1, 1, 32, 32, 1, "32,0,0,0,4"),
+    (2, 40, 64, 16, 32, 2, "32,0,0,0,2"), (1, 21, 23, 32, 64, 2, "64,0,0,0,2"),
+]
+
+
+@pytest.mark.parametrize("case", SUB_CASES, ids=lambda s: "x".join(map(str, s[:6])) + "-" + s[6])
+def test_halo_sub_tiles(gpu, orc, halo_force, case):
+    N, H, W, Ci, Co, st, force = case
+    halo_force(force)
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=sum(case[:6]) + 21)
+    y = _run(x, w, bn) if st == 1 else _run_s(x, w, bn, 2)
+    ref = orc.conv_bn_act(x, w, bn, stride=st, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+@pytest.mark.parametrize("act,res_mode", [(1, 1), (2, 2)])
+def test_halo_sub_tiles_epilogues_and_views(gpu, orc, halo_force, act, res_mode):
+    halo_force("32,0,0,0,4")
+    N, H, W, Ci, Co = 2, 13, 57, 32, 24
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=71 + act)
+    r = np.random.default_rng(13).standard_normal((N, H, W, Co)).astype(np.float32)
+    buf = canary_buffer((N, H, W + 3, Co + 12))
+    y = buf[:, :, :W, 4:4 + Co]
+    _run(x, w, bn, act=act, residual=to_dev(r), res_mode=res_mode, y=y)
+    ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=act, residual=r, res_mode=res_mode)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+    assert is_canary(buf[:, :, W:, :]) and is_canary(buf[:, :, :W, :4]) and is_canary(buf[:, :, :W, 4 + Co:])
