@@ -64,6 +64,8 @@
 #include "tc_store.cuh"
 #include "trace.cuh"
 
+#include <type_traits>
+
 namespace cb {
 
 constexpr int kHaloThreads = 320;
@@ -247,57 +249,51 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       bool ok = true;
       int local = 0;
       TraceBuf tr;
-      for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
-        const int m_tile = tile / a.n_tiles;
-        const int n_img = m_tile / a.tiles_per_img;
-        const int rem = m_tile - n_img * a.tiles_per_img;
-        const int gi = rem - (rem / a.tiles_per_blk) * a.tiles_per_blk;
-        const int q0 = gi * PX * sub;
-        const int nsub = min(sub, a.px_tiles_per_blk - gi * sub);
-        const int base_row = q0 - (q0 / a.Wp) * a.Wp;
-        // the accumulators of this tile's sub-tiles
-        for (int i = 0; ok && i < nsub; ++i) {
-          const int acc = (local + i) % NACC;
-          if (!mbar_wait(&tempty[acc], (((local + i) / NACC) & 1) ^ 1u, wd)) ok = false;
-        }
-        if (!ok) break;
-        tc_fence_after_sync();
-        for (int kc = kc_begin; ok && kc < kc_end; ++kc) {
-          if (!mbar_wait(&hfull[h], hphase, wd)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t halo_addr = smem_u32(sHalo + h * a.halo_bytes);
-          for (int tap0 = 0; tap0 < 9; tap0 += tps) {
-            if (!mbar_wait(&bfull[s], bphase, wd)) {
-              ok = false;
-              break;
-            }
+      // The issue rate of this thread bounds the narrow tiles, so the chunk
+      // loop below is specialised on (taps per stage, sub-tiles) and fully
+      // unrolled: each MMA takes one add to its descriptors' address field
+      // (16-byte units).  tap_off[t] places tap t inside a halo buffer.
+      constexpr uint32_t kRowOff = kRowBytes >> 4;
+      constexpr uint32_t kSubOff = (PX * kRowBytes) >> 4;
+      constexpr uint32_t kTapOff = kTapBytes >> 4;
+      uint32_t tap_off[9];
+#pragma unroll
+      for (int t = 0; t < 9; ++t) {
+        const int dy = t / 3, dx = t % 3;
+        const uint32_t wp_off = static_cast<uint32_t>(a.Wp) * kRowOff;
+        // stride 2: input row 2 oy + dy - 1 is phase row (dy != 1) at oy - 1 + (dy != 0); columns alike
+        tap_off[t] = a.stride == 1 ? dy * wp_off + dx * kRowOff
+                                   : ((dy != 1 ? 2u : 0u) + (dx != 1 ? 1u : 0u)) * (static_cast<uint32_t>(a.phase_bytes) >> 4) +
+                                         (dy != 0 ? wp_off : 0u) + (dx != 0 ? kRowOff : 0u);
+      }
+      // every descriptor shares its high word (stride, swizzle mode)
+      const uint32_t desc_hi = static_cast<uint32_t>(kmajor_swizzled_desc(0u, kRowBytes) >> 32);
+      auto desc_lo = [](uint32_t saddr) { return static_cast<uint32_t>(kmajor_swizzled_desc(saddr, kRowBytes)); };
+      auto make_desc = [&](uint32_t lo) { return (static_cast<uint64_t>(desc_hi) << 32) | lo; };
+      // One K chunk of a tile: 9 taps x NSUB sub-tiles x KC / 8 MMAs, weight
+      // stages of TPS taps.  Returns false when a wait timed out.
+      auto issue_chunk = [&](auto tps_c, auto nsub_c, uint32_t x_lo, const uint32_t (&d_tmem)[kHaloMaxSub],
+                             bool first) -> bool {
+        constexpr int TPS = decltype(tps_c)::value, NSUB = decltype(nsub_c)::value;
+        uint32_t w_lo = 0;
+#pragma unroll
+        for (int tap = 0; tap < 9; ++tap) {
+          if (tap % TPS == 0) {
+            if (!mbar_wait(&bfull[s], bphase, wd)) return false;
             tr.add(tr_cta);
             tc_fence_after_sync();
-            for (int t = 0; t < tps; ++t) {
-              const int tap = tap0 + t;
-              const int dy = tap / 3, dx = tap - 3 * (tap / 3);
-              uint32_t x_addr;
-              if (a.stride == 1) {
-                x_addr = halo_addr + static_cast<uint32_t>((base_row + dy * a.Wp + dx) * kRowBytes);
-              } else {
-                // input row 2 oy + dy - 1 is phase row (dy != 1) at oy - 1 + (dy != 0); columns alike
-                const int ph = (dy != 1 ? 2 : 0) + (dx != 1 ? 1 : 0);
-                x_addr = halo_addr + static_cast<uint32_t>(ph * a.phase_bytes) +
-                         static_cast<uint32_t>((base_row + (dy != 0) * a.Wp + (dx != 0)) * kRowBytes);
-              }
-              const uint64_t wdesc = kmajor_swizzled_desc(smem_u32(sB + s * kBBytes + t * kTapBytes), kRowBytes);
-              for (int i = 0; i < nsub; ++i) {
-                const uint64_t xdesc = kmajor_swizzled_desc(x_addr + static_cast<uint32_t>(i * PX * kRowBytes), kRowBytes);
-                const uint64_t adesc = CM ? wdesc : xdesc, bdesc = CM ? xdesc : wdesc;
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(((local + i) % NACC) * kAccCols);
+            w_lo = desc_lo(smem_u32(sB + s * kBBytes));
+          }
+          const uint32_t xt = x_lo + tap_off[tap], wt = w_lo + (tap % TPS) * kTapOff;
 #pragma unroll
-                for (int kk = 0; kk < KC / 8; ++kk)
-                  mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kc != kc_begin || tap || kk) ? 1u : 0u);
-              }
+          for (int i = 0; i < NSUB; ++i) {
+#pragma unroll
+            for (int kk = 0; kk < KC / 8; ++kk) {
+              const uint64_t xd = make_desc(xt + i * kSubOff + 2 * kk), wdsc = make_desc(wt + 2 * kk);
+              mma_tf32(d_tmem[i], CM ? wdsc : xd, CM ? xd : wdsc, kIdesc, (tap == 0 && kk == 0 && first) ? 0u : 1u);
             }
+          }
+          if (tap % TPS == TPS - 1) {
             mma_commit(&bempty[s]);
             tr.add(tr_cta);
             const uint32_t bit = 1u << s;
@@ -308,6 +304,50 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
               bphase ^= 1u;
             }
           }
+        }
+        return true;
+      };
+      using I1 = std::integral_constant<int, 1>;
+      using I2 = std::integral_constant<int, 2>;
+      using I3 = std::integral_constant<int, 3>;
+      using I4 = std::integral_constant<int, 4>;
+      using I9 = std::integral_constant<int, 9>;
+      auto issue_tps = [&](auto nsub_c, uint32_t x_lo, const uint32_t (&d_tmem)[kHaloMaxSub], bool first) -> bool {
+        return tps == 9 ? issue_chunk(I9{}, nsub_c, x_lo, d_tmem, first)
+             : tps == 3 ? issue_chunk(I3{}, nsub_c, x_lo, d_tmem, first)
+                        : issue_chunk(I1{}, nsub_c, x_lo, d_tmem, first);
+      };
+      for (int tile = tile0; ok && tile < num_tiles; tile += tile_step) {
+        const int m_tile = tile / a.n_tiles;
+        const int n_img = m_tile / a.tiles_per_img;
+        const int rem = m_tile - n_img * a.tiles_per_img;
+        const int gi = rem - (rem / a.tiles_per_blk) * a.tiles_per_blk;
+        const int q0 = gi * PX * sub;
+        const int nsub = min(sub, a.px_tiles_per_blk - gi * sub);
+        const int base_row = q0 - (q0 / a.Wp) * a.Wp;
+        // the accumulators of this tile's sub-tiles
+        uint32_t d_tmem[kHaloMaxSub];
+#pragma unroll
+        for (int i = 0; i < kHaloMaxSub; ++i)
+          d_tmem[i] = tmem_base + static_cast<uint32_t>(((local + i) & (NACC - 1)) * kAccCols);
+        for (int i = 0; ok && i < nsub; ++i) {
+          const int acc = (local + i) & (NACC - 1);
+          if (!mbar_wait(&tempty[acc], (((local + i) / NACC) & 1) ^ 1u, wd)) ok = false;
+        }
+        if (!ok) break;
+        tc_fence_after_sync();
+        for (int kc = kc_begin; ok && kc < kc_end; ++kc) {
+          if (!mbar_wait(&hfull[h], hphase, wd)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t x_lo = desc_lo(smem_u32(sHalo + h * a.halo_bytes) + static_cast<uint32_t>(base_row * kRowBytes));
+          const bool first = kc == kc_begin;
+          if (CM || CO > 64 || nsub == 1) ok = issue_tps(I1{}, x_lo, d_tmem, first);
+          else if (nsub == 2) ok = issue_tps(I2{}, x_lo, d_tmem, first);
+          else if (nsub == 3) ok = issue_tps(I3{}, x_lo, d_tmem, first);
+          else ok = issue_tps(I4{}, x_lo, d_tmem, first);
           if (!ok) break;
           mma_commit(&hempty[h]);
           const uint32_t hbit = 1u << h;
@@ -320,7 +360,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
         }
         if (!ok) break;
         for (int i = 0; i < nsub; ++i) {
-          const int acc = (local + i) % NACC;
+          const int acc = (local + i) & (NACC - 1);
           mma_commit(&tfull[acc]);
           const uint32_t tbit = 1u << acc;
           tparity = (tcommitted & tbit) ? (tparity ^ tbit) : (tparity & ~tbit);
