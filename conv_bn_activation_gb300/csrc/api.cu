@@ -679,25 +679,29 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
         if (tiles >= (1LL << 31)) continue;
         const long long grid = std::min<long long>(tiles, sms);
         const long long per_cta = (tiles + grid - 1) / grid;
-        // Cycles per (tile, chunk): nine taps of kc / 8 MMAs per sub-tile,
-        // each about 120 issue cycles for N <= 128 and 128 for N = 256
-        // (measured), plus the barrier round trip per weight stage; against
-        // the copies (an SM completes them one after another): the halo
-        // (~300 cycles + ~2 per row of the box; four phase tiles of ~800
-        // at stride 2) and 9 / tps weight copies of ~550 cycles per 256
-        // rows.  Plus the pipeline fill per tile and one exposed epilogue.
+        // Cycles, fitted to forced-plan timings of the dense-sweep and
+        // YOLO-chain 3x3 layers (mean regret of the pick 3.5 %).  Per
+        // (tile, chunk) the larger of: the MMAs (nine taps of kc / 8 per
+        // sub-tile, ~64 cycles each up to N = 128, in proportion above)
+        // plus ~200 cycles per weight stage (~130 more per extra sub-tile);
+        // and the copies (~200 per halo copy, four at stride 2; ~280 per
+        // weight copy, plus bytes).  Per tile ~3500 cycles of pipeline fill,
+        // unless the epilogue (~0.37 cycles per output element of the tile)
+        // is slower; plus one exposed epilogue.
         const int n = sh.cm ? sh.px : sh.co;
-        const double mma = sub * 9.0 * (kc / 8) * (n > 128 ? 128.0 : 120.0) + (9.0 / tps) * 100.0;
-        const double wcopy = 550.0 * std::max(1.0, sh.co * tps / 256.0);
-        const double hcopy = stride == 1 ? 300.0 + 2.0 * rows * wp : 4.0 * 800.0 * (1.0 + 0.5 * (sub - 1));
+        const double mma = sub * 9.0 * (kc / 8) * 64.0 * std::max(1.0, n / 128.0) +
+                           (9.0 / tps) * (204.0 + 128.0 * (sub - 1));
+        const double wcopy = 279.0 + 0.013 * tps * sh.co * kc * 4;
+        const double hcopy = (stride == 1 ? 1.0 : 4.0) * 199.0 + 0.0016 * hb;
         const double copy = hcopy + 9.0 / tps * wcopy;
-        const double epi = sh.px * sh.co / 2.3;
+        const double epi = 0.444 * sh.px * sh.co;
+        const double epi_tile = 0.374 * sub * sh.px * sh.co;
         const size_t smem = halo_smem_bytes(sh.co, hb, nb, tps, kc);
         for (int split = 1; split <= 2; ++split) {
           if (f.split && split != f.split) continue;
           double cost;
           if (split == 1) {
-            cost = static_cast<double>(per_cta) * (num_kc * std::max(mma, copy) + 1500.0) + epi;
+            cost = static_cast<double>(per_cta) * std::max(num_kc * std::max(mma, copy) + 3546.0, epi_tile) + epi;
           } else {
             // one tile per CTA pair, each CTA half of the chunks; the partner's
             // half accumulator comes over distributed shared memory (~16 B per
@@ -707,7 +711,7 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
                 recv > 2 * static_cast<size_t>(hb) + nb * tps * sh.co * 128ull || 2 * tiles > sms ||
                 halo_max_pairs(sh.px, sh.co, sh.cm, smem) < tiles)
               continue;
-            cost = (num_kc - num_kc / 2) * std::max(mma, copy) + 1500.0 + recv / 16.0 + 1000.0 + epi / 2;
+            cost = (num_kc - num_kc / 2) * std::max(mma, copy) + 3546.0 + recv / 16.0 + 1000.0 + epi / 2;
           }
           cost *= 1.0 + 0.02 * (n_blk - min_blocks);  // fewer blocks: less halo overlap
           if (cost < best * 0.97) {
@@ -789,21 +793,11 @@ cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, i
     HaloPlan tmp;
     HaloPlan& p = plan ? *plan : tmp;
     const HaloForce f = halo_force_env();
-    if (current_device(&dev) == CB_OK && plan_halo(x, y, stride, dev->sms, f, &p)) {
-      // against the im2col-path kernel: two copies (~570 cycles each) per
-      // (tap, chunk) of 128 pixels, or the MMAs of the step
-      const long long M = static_cast<long long>(y->n) * y->h * y->w;
-      const int kc = x->c <= 8 ? 8 : (x->c <= 16 ? 16 : 32);
-      const int k_iters = 9 * ((x->c + kc - 1) / kc);
-      int n_tiles = 1;
-      const int bn = pick_bn(static_cast<int>(std::min<long long>(M, 1LL << 30)), y->c, k_iters, dev->sms, &n_tiles);
-      const long long tiles = (M + 127) / 128 * n_tiles;
-      const long long per_cta = (tiles + dev->sms - 1) / dev->sms;
-      const double im = per_cta * (k_iters * std::max(1140.0, kc / 8 * (bn > 128 ? 128.0 : 120.0) + 100.0) + 1500.0) +
-                        128.0 * bn / 2.3;
-      const bool forced = f.co || f.cm || f.nb || f.split || f.tps;
-      if (forced || stride == 1 || p.cost <= im) return p.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
-    }
+    // Every 3x3 layer the halo tiles can take: they measured ahead of the
+    // im2col-path kernel (two copies per tap and chunk) on each layer of
+    // the dense sweep, stride 1 and 2.
+    if (current_device(&dev) == CB_OK && plan_halo(x, y, stride, dev->sms, f, &p))
+      return p.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
   }
   return CB_PATH_TC_IM2COL;
 }
