@@ -559,7 +559,43 @@ class PreprocessWorkload(Workload):
         return time.perf_counter() - t0, self.step_units() * n / self.batch, f"{n} of {self.batch} frames"
 
 
-WORKLOADS = {"depthwise": DepthwiseWorkload, "dense": DenseWorkload, "mnist": MnistWorkload,
+class DepthwiseBf16Workload(DepthwiseWorkload):
+    """The same layer with bf16 storage (x, y bf16; weights, scale, bias and arithmetic fp32)."""
+    profile = None
+
+    def __init__(self, torch, device, batch=64):
+        from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
+        from conv_bn_activation_gb300.nets import ConvBnAct
+        self.torch, self.batch = torch, batch
+        x, self.w, self.bn = synthetic.depthwise_layer(N=batch)
+        xb = torch.from_numpy(x).to(torch.bfloat16)
+        self.x_host = xb.float().numpy()          # the bf16 values, for the oracle
+        self.x_host_bf16 = xb
+        self.x = xb.to(device)
+        self.l1 = ConvBnAct(self.w, self.bn, 1, 1, cb.ACT_RELU, groups=384, device=device)
+        self.l2 = ConvBnAct(self.w, self.bn, 2, 1, cb.ACT_RELU, groups=384, device=device)
+        self.y1 = torch.empty(batch, 56, 56, 384, dtype=torch.bfloat16, device=device)
+        self.y2 = torch.empty(batch, 28, 28, 384, dtype=torch.bfloat16, device=device)
+        wl = workloads.depthwise_workload(N=batch, act_bytes=2)
+        self.launches = [
+            Launch("s1", lambda s: self.l1(self.x, self.y1, stream=s), wl["s1"],
+                   "cb::dw_tma_kernel<bf16,1,RELU,NONE>", "hbm"),
+            Launch("s2", lambda s: self.l2(self.x, self.y2, stream=s), wl["s2"],
+                   "cb::dw_tma_kernel<bf16,2,RELU,NONE>", "hbm"),
+        ]
+        self.config = {"workload": "depthwise 3x3 + BN + ReLU, NHWC bf16 storage (fp32 arithmetic), "
+                                   "N=64 C=384 56x56, stride 1 and 2",
+                       "batch": batch, "l2": "inputs_larger_than_l2 (154 MB input, 129 MB L2)"}
+
+    def e2e_setup(self):
+        t = self.torch
+        self.x_pin = self.x_host_bf16.pin_memory()
+        self.y1_pin = t.empty(tuple(self.y1.shape), dtype=t.bfloat16, pin_memory=True)
+        self.y2_pin = t.empty(tuple(self.y2.shape), dtype=t.bfloat16, pin_memory=True)
+        return self.x_pin.numel() * 2, (self.y1_pin.numel() + self.y2_pin.numel()) * 2
+
+
+WORKLOADS = {"depthwise": DepthwiseWorkload, "depthwise_bf16": DepthwiseBf16Workload, "dense": DenseWorkload, "mnist": MnistWorkload,
              "yolo": YoloWorkload, "preprocess": PreprocessWorkload}
 
 

@@ -21,6 +21,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_TIMEOUT, ERR_
 ACT_NONE, ACT_RELU, ACT_SILU = 0, 1, 2
 RES_NONE, RES_PRE_ACT, RES_POST_ACT = 0, 1, 2
 LAYOUT_NHWC, LAYOUT_NCHW = 0, 1
+DTYPE_F32, DTYPE_BF16 = 0, 1
 PATH_DIRECT, PATH_DEPTHWISE, PATH_TC_IM2COL, PATH_TC_HALO, PATH_TC_HALO_CM, PATH_POINTWISE, PATH_STEM = range(1, 8)
 
 EXPORTED = (
@@ -40,7 +41,7 @@ class CbTensor(ctypes.Structure):
         ("n", ctypes.c_int), ("h", ctypes.c_int), ("w", ctypes.c_int), ("c", ctypes.c_int),
         ("stride_n", ctypes.c_longlong), ("stride_h", ctypes.c_longlong),
         ("stride_w", ctypes.c_longlong), ("stride_c", ctypes.c_longlong),
-        ("layout", ctypes.c_int),
+        ("layout", ctypes.c_int), ("dtype", ctypes.c_int),
     ]
 
 
@@ -116,19 +117,29 @@ def _stream_ptr(stream):
 
 
 # ----------------------------------------------------------------- views
+def dtype_code(t) -> int:
+    """cb_dtype of a torch tensor: float32 -> DTYPE_F32, bfloat16 -> DTYPE_BF16."""
+    import torch
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"activation tensors are float32 or bfloat16, got {t.dtype}")
+
+
 def nhwc(t, n=None, h=None, w=None, c=None) -> CbTensor:
     """View of a torch tensor indexed [N, H, W, C] (any strides, unit channel stride)."""
     N, H, W, C = t.shape
     sn, sh, sw, sc = t.stride()
     return CbTensor(t.data_ptr(), N if n is None else n, H if h is None else h, W if w is None else w,
-                    C if c is None else c, sn, sh, sw, sc, LAYOUT_NHWC)
+                    C if c is None else c, sn, sh, sw, sc, LAYOUT_NHWC, dtype_code(t))
 
 
 def nchw(t) -> CbTensor:
     """View of a torch tensor indexed [N, C, H, W] (unit W stride)."""
     N, C, H, W = t.shape
     sn, sc, sh, sw = t.stride()
-    return CbTensor(t.data_ptr(), N, H, W, C, sn, sh, sw, sc, LAYOUT_NCHW)
+    return CbTensor(t.data_ptr(), N, H, W, C, sn, sh, sw, sc, LAYOUT_NCHW, dtype_code(t))
 
 
 # ----------------------------------------------------------- host helpers

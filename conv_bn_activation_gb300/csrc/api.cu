@@ -20,7 +20,7 @@
 #include "internal.h"
 
 namespace cb {
-int dw_tma_blocks_per_sm(int stride, int threads, size_t smem);
+int dw_tma_blocks_per_sm(int stride, int threads, size_t smem, bool bf16);
 int igemm_read_spans_halo(unsigned long long* out, int max_ctas);
 }
 
@@ -140,15 +140,16 @@ void store_map(const std::string& key, const CUtensorMap& m) {
 
 // fp32 tiled map of rank <= 5 (no interleave, 256-byte L2 promotion, zero fill).
 CUresult tiled_map(CUtensorMap* out, int rank, const void* ptr, const cuuint64_t* dims, const cuuint64_t* strides,
-                   const cuuint32_t* box, const cuuint32_t* estr, CUtensorMapSwizzle swz) {
+                   const cuuint32_t* box, const cuuint32_t* estr, CUtensorMapSwizzle swz,
+                   CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT32) {
   cuuint64_t d[5] = {}, st[4] = {};
   cuuint32_t b[5] = {}, e[5] = {};
   for (int i = 0; i < rank; ++i) d[i] = dims[i], b[i] = box[i], e[i] = estr[i];
   for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
-  const int kind = 0;
+  const int kind = dtype == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 0 : 16 + static_cast<int>(dtype);
   const std::string key = map_key(kind, rank, ptr, d, st, b, e, swz);
   if (cached_map(key, out)) return CUDA_SUCCESS;
-  const CUresult r = encode_tiled()(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, static_cast<cuuint32_t>(rank),
+  const CUresult r = encode_tiled()(out, dtype, static_cast<cuuint32_t>(rank),
                                     const_cast<void*>(ptr), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r == CUDA_SUCCESS) store_map(key, *out);
@@ -177,8 +178,13 @@ CUresult im2col_map(CUtensorMap* out, const void* ptr, const cuuint64_t* dims, c
 // ------------------------------------------------------------------ validation
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Bytes per element of a view.
+size_t elem_bytes(const cb_tensor* t) { return t->dtype == CB_DTYPE_BF16 ? 2 : 4; }
+bool is_f32(const cb_tensor* t) { return t->dtype == CB_DTYPE_F32; }
+
 bool view_ok(const cb_tensor* t) {
   if (!t) return false;
+  if (t->dtype != CB_DTYPE_F32 && t->dtype != CB_DTYPE_BF16) return false;
   if (t->n < 0 || t->h < 1 || t->w < 1 || t->c < 1) return false;
   if (t->layout != CB_LAYOUT_NHWC && t->layout != CB_LAYOUT_NCHW) return false;
   if (t->stride_n < 0 || t->stride_h < 0 || t->stride_w < 0 || t->stride_c < 0) return false;
@@ -193,22 +199,23 @@ void view_range(const cb_tensor* t, uintptr_t* lo, uintptr_t* hi) {
   const long long last = (static_cast<long long>(t->n) - 1) * t->stride_n + (t->h - 1LL) * t->stride_h +
                          (t->w - 1LL) * t->stride_w + (t->c - 1LL) * t->stride_c;
   *lo = reinterpret_cast<uintptr_t>(t->data);
-  *hi = *lo + static_cast<uintptr_t>(last + 1) * sizeof(float);
+  *hi = *lo + static_cast<uintptr_t>(last + 1) * elem_bytes(t);
 }
 
 // Disjoint channel slices of one NHWC buffer (same n/h/w strides, both
 // slices inside one pixel's stride_w elements, every stride a multiple of
 // stride_w) share no element even though their byte ranges interleave.
 bool disjoint_channel_slices(const cb_tensor* a, const cb_tensor* b) {
-  if (a->layout != CB_LAYOUT_NHWC || b->layout != CB_LAYOUT_NHWC) return false;
+  if (a->layout != CB_LAYOUT_NHWC || b->layout != CB_LAYOUT_NHWC || a->dtype != b->dtype) return false;
+  const uintptr_t eb = elem_bytes(a);
   if (a->stride_n != b->stride_n || a->stride_h != b->stride_h || a->stride_w != b->stride_w) return false;
   const long long sw = a->stride_w;
   if (sw <= 0 || a->stride_h % sw != 0 || a->stride_n % sw != 0) return false;
   const uintptr_t pa = reinterpret_cast<uintptr_t>(a->data), pb = reinterpret_cast<uintptr_t>(b->data);
   const uintptr_t base = pa < pb ? pa : pb;
-  if ((pa - base) % sizeof(float) != 0 || (pb - base) % sizeof(float) != 0) return false;
-  const long long da = static_cast<long long>((pa - base) / sizeof(float));
-  const long long db = static_cast<long long>((pb - base) / sizeof(float));
+  if ((pa - base) % eb != 0 || (pb - base) % eb != 0) return false;
+  const long long da = static_cast<long long>((pa - base) / eb);
+  const long long db = static_cast<long long>((pb - base) / eb);
   if (da + a->c > sw || db + b->c > sw) return false;
   return da + a->c <= db || db + b->c <= da;
 }
@@ -225,7 +232,7 @@ bool overlap(const cb_tensor* a, const cb_tensor* b) {
 bool same_view(const cb_tensor* a, const cb_tensor* b) {
   return a->data == b->data && a->n == b->n && a->h == b->h && a->w == b->w && a->c == b->c &&
          a->stride_n == b->stride_n && a->stride_h == b->stride_h && a->stride_w == b->stride_w &&
-         a->stride_c == b->stride_c && a->layout == b->layout;
+         a->stride_c == b->stride_c && a->layout == b->layout && a->dtype == b->dtype;
 }
 
 bool strides_mult4(const cb_tensor* t) {
@@ -290,10 +297,20 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
   a.pad = pad;
   a.out = make_out(y);
   a.ep = ep;
+  a.bf16 = x->dtype == CB_DTYPE_BF16 ? 1 : 0;
+  const int policy = g_policy.load();
+  if (a.bf16) {
+    // bf16 storage: the TMA kernel only (16-byte pixel rows of 8 channels)
+    auto mult8 = [](const cb_tensor* t) { return t->stride_n % 8 == 0 && t->stride_h % 8 == 0 && t->stride_w % 8 == 0; };
+    if (a.C % 8 != 0 || !aligned16(a.x) || !aligned16(w) || !aligned16(ep.scale) || !aligned16(ep.bias) ||
+        !aligned16(a.out.y) || !mult8(x) || !mult8(y) ||
+        (ep.res_mode != 0 && (!aligned16(ep.r) || ep.rs_n % 8 != 0 || ep.rs_h % 8 != 0 || ep.rs_w % 8 != 0)))
+      return CB_ERR_ALIGNMENT;
+    if (policy == 1 || encode_tiled() == nullptr) return CB_ERR_UNSUPPORTED;
+  }
   const bool vec = a.C % 4 == 0 && aligned16(a.x) && aligned16(w) && aligned16(ep.scale) && aligned16(ep.bias) &&
                    aligned16(a.out.y) && strides_mult4(x) && strides_mult4(y) &&
                    (ep.res_mode == 0 || (aligned16(ep.r) && ep.rs_n % 4 == 0 && ep.rs_h % 4 == 0 && ep.rs_w % 4 == 0));
-  const int policy = g_policy.load();
   const bool tma_ok = vec && policy != 1 && encode_tiled() != nullptr && a.OW >= 1;
   if (!tma_ok) {
     cudaError_t e = launch_dw_simple(a, vec, s);
@@ -301,31 +318,37 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
   }
 
   // Plan.  Output-column tiles of at most 120 columns (8 consumer threads
-  // per column pair), 32-channel chunks and short strips of output rows:
-  // measured on the 64x56x56x384 layer, 4-row strips with two CTAs per SM
-  // beat longer strips (which stage fewer halo rows) by 10-15%, because the
-  // CTAs in flight then cover a narrow band of rows whose halos hit in L2.
-  // Strips shrink further when a layer has too few items to fill the GPU.
-  const int chunks = (a.C + 31) / 32;
+  // per column pair; bf16: 60 columns, 16 threads per pair), 128-byte
+  // chunks of each pixel (32 fp32 or 64 bf16 channels: an SM completes its
+  // row copies one after another, so the copy count, not their bytes, sets
+  // the pace) and short strips of output rows: measured on the
+  // 64x56x56x384 layer, 4-row strips with two CTAs per SM beat longer
+  // strips (which stage fewer halo rows) by 10-15%, because the CTAs in
+  // flight then cover a narrow band of rows whose halos hit in L2.  Strips
+  // shrink further when a layer has too few items to fill the GPU.
+  const int ch = a.bf16 ? 64 : 32, tpp = ch / 4, max_tile = a.bf16 ? 60 : 120;
+  const int chunks = (a.C + ch - 1) / ch;
   // Tuning override (CB_DW_FORCE="rows,tile_w,ctas_per_sm"; 0 = free), read per call.
   int force_r = 0, force_tw = 0, force_cps = 0;
   if (const char* f = std::getenv("CB_DW_FORCE")) std::sscanf(f, "%d,%d,%d", &force_r, &force_tw, &force_cps);
   DwTmaPlan best{};
   {
-    const int wt = (a.OW + 119) / 120;
-    const int tile_w = force_tw > 0 ? std::min(force_tw, a.OW) : (a.OW + wt - 1) / wt;
+    const int wt = (a.OW + max_tile - 1) / max_tile;
+    const int tile_w = force_tw > 0 ? std::min({force_tw, a.OW, max_tile}) : (a.OW + wt - 1) / wt;
     const int wtiles = (a.OW + tile_w - 1) / tile_w;
     const int pairs = (tile_w + 1) / 2;
     const int box_w = (2 * pairs - 1) * stride + 3;  // both columns of the last pair are covered
-    const int consumer_warps = (pairs * 8 + 31) / 32;
+    const int consumer_warps = (pairs * tpp + 31) / 32;
     const int threads = 32 * (1 + consumer_warps);
-    int cps = dw_tma_blocks_per_sm(stride, threads, 96 * 1024) >= 2 ? 2 : 1;
+    int cps = dw_tma_blocks_per_sm(stride, threads, 96 * 1024, a.bf16 != 0) >= 2 ? 2 : 1;
     if (force_cps == 1 || force_cps == 2) cps = force_cps;
-    const int stage_bytes = box_w * 128;
+    const int stage_bytes = box_w * 128;  // a ring slot: one row of 128-byte pixel chunks
     const size_t ring = cps == 2 ? 96 * 1024 : 192 * 1024;
     const int stages = static_cast<int>(std::min<size_t>(32, ring / stage_bytes));
     const int cap = dev->sms * cps;
-    int R = force_r > 0 ? std::min(force_r, a.OH) : std::min(a.OH, 4);
+    // bf16 at stride 1: 8-row strips (the kernel is bound by its instruction
+    // issue there, and a longer strip re-reads fewer halo rows per output row)
+    int R = force_r > 0 ? std::min(force_r, a.OH) : std::min(a.OH, a.bf16 && stride == 1 ? 8 : 4);
     auto items_for = [&](int r) {
       return static_cast<long long>(a.N) * chunks * wtiles * ((a.OH + r - 1) / r);
     };
@@ -347,18 +370,22 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
                  a.N, a.H, a.W, a.C, stride, best.rows_per_item, best.num_items, best.box_w, best.stages, best.grid,
                  best.consumer_warps, best.smem_bytes);
   if (best.grid == 0) {
+    if (a.bf16) return CB_ERR_UNSUPPORTED;
     cudaError_t e = launch_dw_simple(a, vec, s);
     return e == cudaSuccess ? CB_OK : cuda_fail(e);
   }
   CUtensorMap map;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(a.C), static_cast<cuuint64_t>(a.W), static_cast<cuuint64_t>(a.H),
                         static_cast<cuuint64_t>(a.N)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(a.xs_w) * 4, static_cast<cuuint64_t>(a.xs_h) * 4,
-                           static_cast<cuuint64_t>(a.xs_n) * 4};
-  cuuint32_t box[4] = {32, static_cast<cuuint32_t>(best.box_w), 1, 1};
+  const cuuint64_t eb = a.bf16 ? 2 : 4;
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(a.xs_w) * eb, static_cast<cuuint64_t>(a.xs_h) * eb,
+                           static_cast<cuuint64_t>(a.xs_n) * eb};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(ch), static_cast<cuuint32_t>(best.box_w), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = tiled_map(&map, 4, a.x, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE);
+  CUresult r = tiled_map(&map, 4, a.x, dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         a.bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
   if (r != CUDA_SUCCESS) {
+    if (a.bf16) return CB_ERR_UNSUPPORTED;
     cudaError_t e = launch_dw_simple(a, vec, s);
     return e == cudaSuccess ? CB_OK : cuda_fail(e);
   }
@@ -1053,8 +1080,11 @@ cb_status validate_conv(const cb_tensor* x, const float* w, const float* scale, 
   if (y->n != x->n || y->h != OH || y->w != OW) return CB_ERR_INVALID_ARG;
   const bool depthwise = groups == x->c && groups == y->c && groups > 1;
   if (!depthwise && groups != 1) return CB_ERR_UNSUPPORTED;
+  if (x->dtype != y->dtype) return CB_ERR_INVALID_ARG;
+  if (!is_f32(x) && !depthwise) return CB_ERR_UNSUPPORTED;  // bf16 storage: the depthwise kernel only
   if (res_mode != CB_RES_NONE) {
-    if (!view_ok(residual) || residual->layout != CB_LAYOUT_NHWC) return CB_ERR_INVALID_ARG;
+    if (!view_ok(residual) || residual->layout != CB_LAYOUT_NHWC || residual->dtype != y->dtype)
+      return CB_ERR_INVALID_ARG;
     if (residual->n != y->n || residual->h != y->h || residual->w != y->w || residual->c != y->c)
       return CB_ERR_INVALID_ARG;
     if (!same_view(residual, y) && overlap(residual, y)) return CB_ERR_INVALID_ARG;
@@ -1254,12 +1284,13 @@ bool dw_block_fusable(const cb_tensor* x, const cb_tensor* y, const float* pw_w,
 }  // namespace
 
 int cb_dw_separable_block_fused(const cb_tensor* x, const cb_tensor* y, const float* pw_w, const float* skip_w) {
-  if (!view_ok(x) || !view_ok(y) || !pw_w) return 0;
+  if (!view_ok(x) || !view_ok(y) || !pw_w || !is_f32(x) || !is_f32(y)) return 0;
   return dw_block_fusable(x, y, pw_w, skip_w) ? 1 : 0;
 }
 
 cb_status cb_dw_separable_block_workspace(const cb_tensor* x, int c_out, int stride, size_t* bytes) {
   if (!view_ok(x) || !bytes || c_out < 1 || (stride != 1 && stride != 2)) return CB_ERR_INVALID_ARG;
+  if (!is_f32(x)) return CB_ERR_UNSUPPORTED;
   const long long OH = (x->h + 2 - 3) / stride + 1, OW = (x->w + 2 - 3) / stride + 1;
   if (x->h < 1 || x->w < 1 || OH < 1 || OW < 1) return CB_ERR_INVALID_ARG;
   const long long pix = static_cast<long long>(x->n) * OH * OW;
@@ -1275,6 +1306,7 @@ cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const flo
                                 void* workspace, size_t workspace_bytes, void* stream) {
   if (!view_ok(x) || !view_ok(y) || !dw_w || !dw_scale || !dw_bias || !pw_w || !pw_scale || !pw_bias)
     return CB_ERR_INVALID_ARG;
+  if (!is_f32(x) || !is_f32(y)) return CB_ERR_UNSUPPORTED;
   if (x->layout != CB_LAYOUT_NHWC || y->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
   if (stride != 1 && stride != 2) return CB_ERR_UNSUPPORTED;
   const int Ci = x->c, Co = y->c;
@@ -1373,6 +1405,7 @@ cb_status cb_dw_separable_block_static(const cb_tensor* x, const float* dw_w, co
                                        const float* pw_bias, const float* skip_w, const float* skip_scale,
                                        const float* skip_bias, int stride, cb_tensor* y, void* stream) {
   if (!view_ok(x) || !view_ok(y)) return CB_ERR_INVALID_ARG;
+  if (!is_f32(x) || !is_f32(y)) return CB_ERR_UNSUPPORTED;
   size_t need = 0;
   cb_status st = cb_dw_separable_block_workspace(x, y->c, stride, &need);
   if (st != CB_OK) return st;
@@ -1400,6 +1433,7 @@ cb_status cb_avgpool_linear(const cb_tensor* x, const float* fc_w, const float* 
                             void* stream) {
   if (!view_ok(x) || x->layout != CB_LAYOUT_NHWC || !fc_w || !fc_b || !out || out_features < 1)
     return CB_ERR_INVALID_ARG;
+  if (!is_f32(x)) return CB_ERR_UNSUPPORTED;
   if (x->c > 12 * 1024) return CB_ERR_UNSUPPORTED;
   if (x->n == 0) return CB_OK;
   PoolFcArgs a{};
@@ -1445,6 +1479,7 @@ cb_status cb_preprocess_stem_u8(const unsigned char* src, int n, int src_h, int 
                                 cb_tensor* y, void* stream) {
   if (!src || !w || !scale || !bias || !view_ok(y) || n < 0 || src_h < 1 || src_w < 1 || dst_h < 1 || dst_w < 1)
     return CB_ERR_INVALID_ARG;
+  if (!is_f32(y)) return CB_ERR_UNSUPPORTED;
   if (src_pitch < 3LL * src_w || act < CB_ACT_NONE || act > CB_ACT_SILU) return CB_ERR_INVALID_ARG;
   if (y->layout != CB_LAYOUT_NHWC || y->n != n || y->c != 16 || y->h != (dst_h - 1) / 2 + 1 ||
       y->w != (dst_w - 1) / 2 + 1)
@@ -1569,8 +1604,8 @@ int cb_debug_igemm_spans(unsigned long long* out, int max_ctas) {
 int cb_conv_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, int groups) {
   if (!view_ok(x) || !view_ok(y) || (kh != 1 && kh != 3) || (stride != 1 && stride != 2)) return 0;
   if (pad < 0 || pad > kh / 2) return 0;
-  if (groups == x->c && groups == y->c && groups > 1) return kh == 3 ? CB_PATH_DEPTHWISE : 0;
-  if (groups != 1) return 0;
+  if (groups == x->c && groups == y->c && groups > 1) return kh == 3 && x->dtype == y->dtype ? CB_PATH_DEPTHWISE : 0;
+  if (groups != 1 || !is_f32(x) || !is_f32(y)) return 0;
   return dense_path(x, y, kh, stride, pad, nullptr);
 }
 

@@ -15,9 +15,14 @@
 //    thread owns one (output column, 4 channels) pair, reads the three
 //    columns of its window from each ring row once, and slides the 3x3
 //    window down the strip in registers.
+//    With bf16 storage the same kernel moves 128-byte pixel chunks of 64
+//    channels: values are widened to fp32 as they leave shared memory and
+//    the fp32 result is rounded to bf16 (nearest even) at the store.
 //  * dw_simple_kernel: one thread per (output pixel, 4 channels) or per
 //    channel, direct global loads.  Used for views the TMA path cannot
 //    describe (unaligned data, channel counts that are not multiples of 4).
+#include <cuda_bf16.h>
+
 #include "epilogue.cuh"
 #include "launch_util.h"
 #include "internal.h"
@@ -88,6 +93,7 @@ cudaError_t launch_dw_simple(const DwArgs& a, bool vec4, cudaStream_t s) {
 struct DwTmaParams {
   DwArgs a;
   int rows_per_item, num_items, box_w, stages;
+  int ch;  // channels per chunk: one 128-byte pixel row (32 fp32 or 64 bf16)
   int chunks, strips, wtiles, tile_w;
   int* err;
   uint64_t timeout_ns;
@@ -108,7 +114,7 @@ __device__ __forceinline__ DwItem dw_decode(const DwTmaParams& p, int item) {
   rest /= p.wtiles;
   const int st = rest % p.strips;
   it.n = rest / p.strips;
-  it.c0 = ch * 32;
+  it.c0 = ch * p.ch;
   it.oh0 = st * p.rows_per_item;
   it.oh1 = min(it.oh0 + p.rows_per_item, p.a.OH);
   it.ow0 = wt * p.tile_w;
@@ -117,6 +123,31 @@ __device__ __forceinline__ DwItem dw_decode(const DwTmaParams& p, int item) {
 }
 
 constexpr int kDwProducerLanes = 4;
+
+// Four consecutive channels as fp32, from fp32 or bf16 storage (a bf16 value
+// is the upper half of the fp32 with the same bits: widening is exact).
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
+                     __uint_as_float(v.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&lo);
+  u.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// acc += a * b on four lanes as two packed fp32 FMAs (each lane rounded as
+// one fmaf: the same bits as fma4, half the instructions).
+__device__ __forceinline__ void fma4_packed(float4& acc, float4 a, float4 b) {
+  const float2 lo = __ffma2_rn(make_float2(a.x, a.y), make_float2(b.x, b.y), make_float2(acc.x, acc.y));
+  const float2 hi = __ffma2_rn(make_float2(a.z, a.w), make_float2(b.z, b.w), make_float2(acc.z, acc.w));
+  acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+}
 
 template <int ACT, int RES>
 __device__ __forceinline__ float epi_c(float acc, float sc, float bi, float r) {
@@ -129,12 +160,20 @@ __device__ __forceinline__ float epi_c(float acc, float sc, float bi, float r) {
 }
 
 // Each consumer thread owns two adjacent output columns x 4 channels; its
-// window needs NC = S + 3 input columns per row.
-template <int S, int ACT, int RES>
+// window needs NC = S + 3 input columns per row.  T: the storage type of x,
+// y and the residual (float or bf16).
+template <typename T, int S, int ACT, int RES>
 __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ CUtensorMap xmap,
                                                         const DwTmaParams p) {
   constexpr int NC = S + 3;
   extern __shared__ __align__(128) uint8_t smem_raw[];
+  // One ring slot: a row copy of box_w pixels of one chunk, 128 bytes each
+  // (32 fp32 or 64 bf16 channels: an SM completes its copies one after
+  // another, so a bf16 chunk is as wide as an fp32 one in bytes, not in
+  // channels, and the layer takes half the copies).
+  constexpr int CH = 128 / static_cast<int>(sizeof(T));  // channels per chunk
+  constexpr bool kPacked = sizeof(T) == 2;                 // packed FMAs (bf16 storage)
+  constexpr int TPP = CH / 4;                              // threads per column pair
   const int stage_bytes = p.box_w * 128;
   uint8_t* ring = smem_raw;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + p.stages * stage_bytes);
@@ -199,7 +238,7 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
 
   // ------------------------------------------------------------ consumers
   const int t = threadIdx.x - 32;
-  const int pair = t >> 3, c4 = t & 7;
+  const int pair = t / TPP, c4 = t % TPP;
   int slot = 0;
   uint32_t phase = 0;
   bool ok = true;
@@ -215,10 +254,9 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
       return;
     }
     if (read) {
-      const float4* row =
-          reinterpret_cast<const float4*>(ring + slot * stage_bytes) + (2 * pair * S) * 8 + c4;
+      const T* row = reinterpret_cast<const T*>(ring + slot * stage_bytes) + (2 * pair * S) * CH + c4 * 4;
 #pragma unroll
-      for (int k = 0; k < NC; ++k) dst[k] = row[k * 8];
+      for (int k = 0; k < NC; ++k) dst[k] = load4(row + k * CH);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
@@ -246,8 +284,9 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
 #pragma unroll
       for (int k = 0; k < 9; ++k) wv[k] = sc;
     }
-    float* yp = a.out.y + it.n * a.out.ys_n + it.oh0 * a.out.ys_h + ow * a.out.ys_w + c;
-    const float* rp = RES ? a.ep.r + it.n * a.ep.rs_n + it.oh0 * a.ep.rs_h + ow * a.ep.rs_w + c : nullptr;
+    T* yp = reinterpret_cast<T*>(a.out.y) + it.n * a.out.ys_n + it.oh0 * a.out.ys_h + ow * a.out.ys_w + c;
+    const T* rp = RES ? reinterpret_cast<const T*>(a.ep.r) + it.n * a.ep.rs_n + it.oh0 * a.ep.rs_h + ow * a.ep.rs_w + c
+                      : nullptr;
 
     // One output row from the window (top, mid, bottom); advances yp / rp.
     auto compute = [&](const float4(&T)[NC], const float4(&M)[NC], const float4(&B)[NC]) {
@@ -257,19 +296,27 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int kw = 0; kw < 3; ++kw) {
-            fma4(acc, T[j * S + kw], wv[kw]);
-            fma4(acc, M[j * S + kw], wv[3 + kw]);
-            fma4(acc, B[j * S + kw], wv[6 + kw]);
+            if constexpr (kPacked) {
+              // bf16 storage moves half the bytes per output: the arithmetic
+              // must keep up, so the FMAs go out packed
+              fma4_packed(acc, T[j * S + kw], wv[kw]);
+              fma4_packed(acc, M[j * S + kw], wv[3 + kw]);
+              fma4_packed(acc, B[j * S + kw], wv[6 + kw]);
+            } else {
+              fma4(acc, T[j * S + kw], wv[kw]);
+              fma4(acc, M[j * S + kw], wv[3 + kw]);
+              fma4(acc, B[j * S + kw], wv[6 + kw]);
+            }
           }
           if (j == 0 || second) {
             float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (RES) r = *reinterpret_cast<const float4*>(rp + j * a.ep.rs_w);
+            if (RES) r = load4(rp + j * a.ep.rs_w);
             float4 o;
             o.x = epi_c<ACT, RES>(acc.x, sc.x, bi.x, r.x);
             o.y = epi_c<ACT, RES>(acc.y, sc.y, bi.y, r.y);
             o.z = epi_c<ACT, RES>(acc.z, sc.z, bi.z, r.z);
             o.w = epi_c<ACT, RES>(acc.w, sc.w, bi.w, r.w);
-            *reinterpret_cast<float4*>(yp + j * a.out.ys_w) = o;
+            store4(yp + j * a.out.ys_w, o);
           }
         }
       }
@@ -315,19 +362,19 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
   }
 }
 
-template <int S, int ACT, int RES>
+template <typename T, int S, int ACT, int RES>
 static void dw_tma_launch(const CUtensorMap& xmap, const DwTmaParams& p, int grid, int threads, size_t smem,
                           cudaStream_t s) {
-  if (smem_attr_once<dw_tma_kernel<S, ACT, RES>>(smem) != cudaSuccess) return;
-  launch_pdl(dw_tma_kernel<S, ACT, RES>, dim3(grid), dim3(threads), smem, s, xmap, p);
+  if (smem_attr_once<dw_tma_kernel<T, S, ACT, RES>>(smem) != cudaSuccess) return;
+  launch_pdl(dw_tma_kernel<T, S, ACT, RES>, dim3(grid), dim3(threads), smem, s, xmap, p);
 }
 
-template <int S>
+template <typename T, int S>
 static void dw_tma_dispatch(const CUtensorMap& xmap, const DwTmaParams& p, int grid, int threads, size_t smem,
                             cudaStream_t s) {
   const int act = p.a.ep.act, res = p.a.ep.res_mode;
 #define CB_DW_CASE(A, R) \
-  if (act == A && res == R) return dw_tma_launch<S, A, R>(xmap, p, grid, threads, smem, s);
+  if (act == A && res == R) return dw_tma_launch<T, S, A, R>(xmap, p, grid, threads, smem, s);
   CB_DW_CASE(0, 0) CB_DW_CASE(1, 0) CB_DW_CASE(2, 0)
   CB_DW_CASE(0, 1) CB_DW_CASE(1, 1) CB_DW_CASE(2, 1)
   CB_DW_CASE(0, 2) CB_DW_CASE(1, 2) CB_DW_CASE(2, 2)
@@ -342,39 +389,51 @@ cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaP
   p.num_items = plan.num_items;
   p.box_w = plan.box_w;
   p.stages = plan.stages;
-  p.chunks = (a.C + 31) / 32;
+  p.ch = a.bf16 ? 64 : 32;
+  p.chunks = (a.C + p.ch - 1) / p.ch;
   p.strips = (a.OH + plan.rows_per_item - 1) / plan.rows_per_item;
   p.tile_w = plan.tile_w;
   p.wtiles = (a.OW + p.tile_w - 1) / p.tile_w;
   p.err = err;
   p.timeout_ns = timeout_ns;
   const int threads = 32 * (1 + plan.consumer_warps);
-  if (a.stride == 1)
-    dw_tma_dispatch<1>(xmap, p, plan.grid, threads, plan.smem_bytes, s);
-  else
-    dw_tma_dispatch<2>(xmap, p, plan.grid, threads, plan.smem_bytes, s);
+  if (a.bf16) {
+    if (a.stride == 1)
+      dw_tma_dispatch<__nv_bfloat16, 1>(xmap, p, plan.grid, threads, plan.smem_bytes, s);
+    else
+      dw_tma_dispatch<__nv_bfloat16, 2>(xmap, p, plan.grid, threads, plan.smem_bytes, s);
+  } else if (a.stride == 1) {
+    dw_tma_dispatch<float, 1>(xmap, p, plan.grid, threads, plan.smem_bytes, s);
+  } else {
+    dw_tma_dispatch<float, 2>(xmap, p, plan.grid, threads, plan.smem_bytes, s);
+  }
   return cudaGetLastError();
+}
+
+template <typename T, int S>
+static int dw_tma_occupancy(int threads, size_t smem) {
+  int n = 0;
+  smem_attr_once<dw_tma_kernel<T, S, 1, 0>>(smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dw_tma_kernel<T, S, 1, 0>, threads, smem);
+  return n;
 }
 
 // Occupancy query used by the planner (registers decide how many CTAs fit).
 // Cached per (stride, warps, shared-memory size in KB): occupancy is a
 // function of the kernel and these alone.
-int dw_tma_blocks_per_sm(int stride, int threads, size_t smem) {
-  static std::atomic<int> cache[2][33][229];
-  const int si = stride == 1 ? 0 : 1, wi = threads / 32, ki = static_cast<int>(smem / 1024);
+int dw_tma_blocks_per_sm(int stride, int threads, size_t smem, bool bf16) {
+  static std::atomic<int> cache[4][33][229];
+  const int si = (stride == 1 ? 0 : 1) + (bf16 ? 2 : 0), wi = threads / 32, ki = static_cast<int>(smem / 1024);
   const bool cacheable = threads % 32 == 0 && wi <= 32 && smem % 1024 == 0 && ki <= 228;
   if (cacheable) {
     const int v = cache[si][wi][ki].load(std::memory_order_relaxed);
     if (v > 0) return v - 1;
   }
   int n = 0;
-  if (stride == 1) {
-    smem_attr_once<dw_tma_kernel<1, 1, 0>>(smem);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dw_tma_kernel<1, 1, 0>, threads, smem);
-  } else {
-    smem_attr_once<dw_tma_kernel<2, 1, 0>>(smem);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dw_tma_kernel<2, 1, 0>, threads, smem);
-  }
+  if (bf16 && stride == 1) n = dw_tma_occupancy<__nv_bfloat16, 1>(threads, smem);
+  else if (bf16) n = dw_tma_occupancy<__nv_bfloat16, 2>(threads, smem);
+  else if (stride == 1) n = dw_tma_occupancy<float, 1>(threads, smem);
+  else n = dw_tma_occupancy<float, 2>(threads, smem);
   if (cacheable) cache[si][wi][ki].store(n + 1, std::memory_order_relaxed);
   return n;
 }

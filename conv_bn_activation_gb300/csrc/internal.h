@@ -31,6 +31,7 @@ struct DwArgs {
   int N, H, W, C, OH, OW, stride, pad;
   OutView out;
   Epilogue ep;
+  int bf16;  // x, y and r hold bfloat16 (TMA kernel only); w, scale, bias fp32
 };
 // Plain CUDA-core kernel: one thread per (output pixel, 4 or 1 channels).
 cudaError_t launch_dw_simple(const DwArgs& a, bool vec4, cudaStream_t s);

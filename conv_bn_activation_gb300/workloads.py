@@ -38,11 +38,12 @@ class Work:
         return Work(self.bytes + other.bytes, self.flops + other.flops)
 
 
-def conv_layer(N, H, W, Cin, Cout, k, s, p, groups=1, residual=False) -> Work:
-    """Fused conv + folded BN (+ residual) + activation: in + out (+ r) + w + scale/bias."""
+def conv_layer(N, H, W, Cin, Cout, k, s, p, groups=1, residual=False, act_bytes=F32) -> Work:
+    """Fused conv + folded BN (+ residual) + activation: in + out (+ r) + w + scale/bias.
+    act_bytes: bytes per activation element (4 fp32, 2 bf16 storage); weights stay fp32."""
     OH, OW = out_size(H, k, s, p), out_size(W, k, s, p)
-    x = N * H * W * Cin * F32
-    y = N * OH * OW * Cout * F32
+    x = N * H * W * Cin * act_bytes
+    y = N * OH * OW * Cout * act_bytes
     w = Cout * (Cin // groups) * k * k * F32
     sb = 2 * Cout * F32
     r = y if residual else 0
@@ -50,8 +51,8 @@ def conv_layer(N, H, W, Cin, Cout, k, s, p, groups=1, residual=False) -> Work:
     return Work(x + y + w + sb + r, 2 * macs)
 
 
-def depthwise_layer(N, H, W, C, s, k=3, p=1) -> Work:
-    return conv_layer(N, H, W, C, C, k, s, p, groups=C)
+def depthwise_layer(N, H, W, C, s, k=3, p=1, act_bytes=F32) -> Work:
+    return conv_layer(N, H, W, C, C, k, s, p, groups=C, act_bytes=act_bytes)
 
 
 # --- preprocess ledger ("A fused Ampere preprocess kernel", the theory) -----
@@ -85,9 +86,10 @@ def preprocess_unfused(N, Hs, Ws, Hd, Wd) -> Work:
 
 
 # --- whole workloads -------------------------------------------------------
-def depthwise_workload(N=64, H=56, W=56, C=384):
+def depthwise_workload(N=64, H=56, W=56, C=384, act_bytes=F32):
     """The depthwise 3x3 + BN + ReLU layer at stride 1 and stride 2."""
-    return {"s1": depthwise_layer(N, H, W, C, 1), "s2": depthwise_layer(N, H, W, C, 2)}
+    return {"s1": depthwise_layer(N, H, W, C, 1, act_bytes=act_bytes),
+            "s2": depthwise_layer(N, H, W, C, 2, act_bytes=act_bytes)}
 
 
 def mnist_layers(N=64):

@@ -58,7 +58,21 @@ typedef enum { CB_RES_NONE = 0, CB_RES_PRE_ACT = 1, CB_RES_POST_ACT = 2 } cb_res
 typedef enum { CB_LAYOUT_NHWC = 0, CB_LAYOUT_NCHW = 1 } cb_layout;
 
 /*
- * A 4-D fp32 activation tensor view.  Logical dims (n, h, w, c); element
+ * Element type of an activation view.  CB_DTYPE_F32 (0, the default of a
+ * zero-initialised view) everywhere; CB_DTYPE_BF16 (bfloat16: the upper half
+ * of an fp32) is the half-size storage variant, taken by the depthwise 3x3
+ * layers of cb_conv_bn_act: a 16-bit main data type is the first of the
+ * next steps "How I sped up convolutions" lists (ideas and next steps), and
+ * those layers are memory-bound, so halving their bytes halves their time.
+ * Arithmetic stays fp32; a BF16 output is the fp32 result rounded to
+ * nearest even.
+ * Entry points that do not take BF16 views return CB_ERR_UNSUPPORTED.
+ */
+typedef enum { CB_DTYPE_F32 = 0, CB_DTYPE_BF16 = 1 } cb_dtype;
+
+/*
+ * A 4-D activation tensor view (fp32, or bf16 where `dtype` says so).
+ * Logical dims (n, h, w, c); element
  * (n, h, w, c) lives at data + n*stride_n + h*stride_h + w*stride_w + c*stride_c
  * (strides in ELEMENTS).  NHWC views need stride_c == 1; NCHW views need
  * stride_w == 1.  A channel slice of a wider buffer (the producer side of a
@@ -71,6 +85,7 @@ typedef struct {
   int n, h, w, c;
   long long stride_n, stride_h, stride_w, stride_c;
   cb_layout layout;
+  cb_dtype dtype;
 } cb_tensor;
 
 /*
@@ -126,7 +141,12 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
  * for all nine taps; the others gather one tile per tap.  1x1 stride-1
  * layers with Ci and Co in {4, 8, 16, 32} run instead on a streaming fp32
  * CUDA-core kernel (HBM-bound at these widths);
- * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;
+ * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel, in
+ * fp32 or with bf16 storage (x, y and residual all CB_DTYPE_BF16; weights,
+ * scale and bias stay fp32 and the arithmetic fp32; needs C % 8 == 0,
+ * 16-byte aligned x, y, residual, w, scale and bias, and NHWC strides that
+ * are multiples of 8 elements: else CB_ERR_ALIGNMENT; dense bf16 layers
+ * return CB_ERR_UNSUPPORTED);
  * 3 -> 16 channel 3x3 stride-2 pad-1 stems run on a dedicated fp32 CUDA-core
  * kernel when the input is planar (NCHW) or packed NHWC (stride_w == 3) with
  * W % 4 == 0, 16-byte aligned data and n / h (/ c) strides that are

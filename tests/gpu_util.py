@@ -6,6 +6,7 @@ from conv_bn_activation_gb300 import binding as cb
 
 TOL_FP32 = 1e-5   # CUDA-core fp32 kernels: max|gpu - oracle| / max|oracle|
 TOL_TF32 = 5e-3   # tensor-core TF32 kernels with fp32 accumulate
+TOL_BF16 = 5e-3   # bf16 storage (fp32 arithmetic): max|gpu - oracle| / max|oracle|
 
 
 def rel_err(got, ref):
@@ -35,3 +36,32 @@ def is_canary(t):
 def sync_check():
     torch.cuda.synchronize()
     assert cb.get_device_error() == cb.OK
+
+
+def to_dev_bf16(a, device="cuda"):
+    """(bf16 device tensor, the fp32 numpy array of its exact values): the input the kernel and
+    the oracle both see."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.to(device), t.float().numpy()
+
+
+def bf16_within_half_ulp(got, ref):
+    """max over elements of |got - ref| / (2^-8 |ref| + 1e-5 max|ref|): at most 1 when every
+    output is the fp32 result rounded to bf16 (half a unit in the last of bf16's 8 significant
+    bits is at most 2^-8 of the value) up to fp32 arithmetic error."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape and np.all(np.isfinite(got))
+    bound = 2.0 ** -8 * np.abs(ref) + TOL_FP32 * max(float(np.max(np.abs(ref))), 1e-30)
+    return float(np.max(np.abs(got - ref) / bound))
+
+
+def canary_buffer_bf16(shape, device="cuda"):
+    """A bf16 buffer filled with a NaN bit pattern no kernel produces."""
+    t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    t.view(torch.int16).fill_(0x7FDD)
+    return t
+
+
+def is_canary_bf16(t):
+    return bool((t.contiguous().view(torch.int16) == 0x7FDD).all().item())

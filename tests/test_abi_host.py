@@ -105,6 +105,46 @@ def test_conv_rejects_invalid_arguments_before_launch(cblib):
     assert call(_view(base, 0, 8, 8, 16), _view(base + (1 << 16), 0, 8, 8, 16)) == cblib.OK
 
 
+def test_bf16_views_validated_before_launch(cblib):
+    """bf16 storage: depthwise only, every view the same element type, unknown element types
+    rejected -- all decided on the host (fake pointers, never dereferenced)."""
+    lib = cblib.load()
+    T = ctypes.byref
+    base = 1 << 20
+    w = s = b = base + (1 << 18)
+
+    def v(data, n, h, w_, c, dtype):
+        t = _view(data, n, h, w_, c)
+        t.dtype = dtype
+        return t
+    x16 = v(base, 1, 8, 8, 16, cblib.DTYPE_BF16)
+    y16 = v(base + (1 << 16), 1, 8, 8, 16, cblib.DTYPE_BF16)
+    y32 = v(base + (1 << 16), 1, 8, 8, 16, cblib.DTYPE_F32)
+    call = lambda xv, yv, g=1, r=None, rm=0: lib.cb_conv_bn_act(
+        T(xv), w, s, b, 3, 3, 1, 1, g, 0, T(r) if r is not None else None, rm, T(yv), None)
+    assert call(x16, y16, g=1) == cblib.ERR_UNSUPPORTED                      # dense bf16
+    assert call(x16, y32, g=16) == cblib.ERR_INVALID_ARG                     # mixed element types
+    assert call(x16, y16, g=16, r=v(base + (1 << 17), 1, 8, 8, 16, cblib.DTYPE_F32), rm=2) == cblib.ERR_INVALID_ARG
+    assert call(v(base, 1, 8, 8, 16, 7), v(base + (1 << 16), 1, 8, 8, 16, 7), g=16) == cblib.ERR_INVALID_ARG
+    assert lib.cb_conv_path(T(x16), T(y16), 3, 1, 1, 16) == cblib.PATH_DEPTHWISE
+    assert lib.cb_conv_path(T(x16), T(y16), 3, 1, 1, 1) == 0
+    assert lib.cb_conv_path(T(x16), T(y32), 3, 1, 1, 16) == 0
+    # empty bf16 depthwise batch: valid, nothing to launch
+    assert call(v(base, 0, 8, 8, 16, cblib.DTYPE_BF16), v(base + 8 * 8 * 16 * 2, 0, 8, 8, 16, cblib.DTYPE_BF16),
+                g=16) == cblib.OK
+    n = ctypes.c_size_t(0)
+    assert lib.cb_dw_separable_block_workspace(T(x16), 16, 1, T(n)) == cblib.ERR_UNSUPPORTED
+
+
+def test_binding_dtype_codes(cblib):
+    import torch
+    assert cblib.dtype_code(torch.empty(1)) == cblib.DTYPE_F32
+    assert cblib.dtype_code(torch.empty(1, dtype=torch.bfloat16)) == cblib.DTYPE_BF16
+    with pytest.raises(TypeError):
+        cblib.dtype_code(torch.empty(1, dtype=torch.float16))
+    assert cblib.nhwc(torch.empty(1, 2, 3, 8, dtype=torch.bfloat16)).dtype == cblib.DTYPE_BF16
+
+
 def test_block_and_preprocess_validation(cblib):
     lib = cblib.load()
     T = ctypes.byref
