@@ -561,7 +561,8 @@ class PreprocessWorkload(Workload):
 
 class DepthwiseBf16Workload(DepthwiseWorkload):
     """The same layer with bf16 storage (x, y bf16; weights, scale, bias and arithmetic fp32)."""
-    profile = None
+    profile = ("dw_tma_kernel_depthwise_bf16_64x56x56x384.md",
+               ["dw_conv.cu", "ptx.cuh", "epilogue.cuh", "launch_util.h"])
 
     def __init__(self, torch, device, batch=64):
         from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
