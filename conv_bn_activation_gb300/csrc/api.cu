@@ -949,8 +949,7 @@ cb_status run_pointwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
   a.ep = ep;
   const bool flat = pixel_flat(x) && pixel_flat(y) && (ep.res_mode == 0 || pixel_flat(residual));
   cudaError_t e = launch_pointwise_small(a, flat, dev->sms, s);
-  // a residual ring that does not fit in shared memory (4 input channels with
-  // 16 or more outputs): the direct kernel
+  // a shape the kernel does not take: the direct kernel
   if (e == cudaErrorInvalidValue) return run_direct(x, w, ep, 1, 1, 0, y, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }

@@ -12,8 +12,11 @@
 // bytes are in flight to cover HBM latency); then each thread computes
 // 4 pixels x 4 output channels from shared memory (register blocking: 64
 // FMAs per 8 shared loads) and stores each pixel's four channels as one
-// 16-byte store, so a warp's stores are whole pixel segments.  The weights
-// sit in shared memory as [ci][co/4] float4s.
+// 16-byte store, so a warp's stores are whole pixel segments.  The residual
+// is read straight into registers, issued before the FMAs that it then
+// overlaps: staging it beside the input doubled the ring and held the
+// residual layers to one CTA per SM.  The weights sit in shared memory as
+// [ci][co/4] float4s.
 #include "epilogue.cuh"
 #include "internal.h"
 #include "launch_util.h"
@@ -67,39 +70,36 @@ struct PwShape {
   static constexpr int G = CO / 4;                                // channel groups of 4 outputs
   static constexpr int kVec = CI / 4;                             // 16-byte input pieces per pixel
   static constexpr int kPitch = kVec >= 4 ? kVec + 1 : kVec;      // staged input row, float4s (padded)
-  static constexpr int kRPitch = G >= 4 ? G + 1 : G;              // staged residual row, float4s
   static constexpr int kTile = 4096 / CI;                         // pixels per tile (16 KB of input)
   static constexpr int kGroups = kTile / kPwU;                    // pixel groups per tile
   static constexpr int kItems = kGroups * G;                      // (pixel group, channel group) items
   static constexpr int kXFloat4 = kTile * kPitch;
-  static constexpr int kRFloat4 = kTile * kRPitch;
-  static size_t smem_bytes(bool res) {
-    return 16 * (static_cast<size_t>(CI) * G + 2 * G +
-                 static_cast<size_t>(kPwStages) * (kXFloat4 + (res ? kRFloat4 : 0)));
+  static size_t smem_bytes() {
+    return 16 * (static_cast<size_t>(CI) * G + 2 * G + static_cast<size_t>(kPwStages) * kXFloat4);
   }
 };
 
 // A ring of kPwStages tiles per CTA: a tile is kTile pixels whose CI inputs
-// are 16 KB (plus their residual rows when there is a residual), copied
+// are 16 KB, copied
 // with 16-byte cp.async by all threads (different bytes per thread).  The
 // staged rows of 64 bytes or more are padded by 16 bytes so that the
 // pixel-strided reads below hit distinct bank groups.  Each thread computes
 // 4 pixels x 4 output channels: per 4 input channels it reads 4 pixel
 // float4s and 4 weight float4s and does 64 FMAs.
-template <int CI, int CO>
+template <int CI, int CO, bool RES>
 __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a, int flat) {
   static_assert(CI % 4 == 0 && CO % 4 == 0 && CI <= 32 && CO <= 32, "channel counts");
   using Sh = PwShape<CI, CO>;
-  constexpr int G = Sh::G, kVec = Sh::kVec, kPitch = Sh::kPitch, kRPitch = Sh::kRPitch;
+  constexpr int G = Sh::G, kVec = Sh::kVec, kPitch = Sh::kPitch;
   constexpr int kTile = Sh::kTile, kGroups = Sh::kGroups, kItems = Sh::kItems;
   static_assert(kTile * kVec == 4 * kPwThreads && kPwThreads % G == 0, "tile shape");
   extern __shared__ float4 pw_smem[];
-  const bool res = a.ep.res_mode != 0;
+  constexpr bool res = RES;  // a residual (its placement is a.ep.res_mode)
   float4* ws = pw_smem;             // [CI][G]
   float4* ssc = ws + CI * G;        // [G]
   float4* sbi = ssc + G;            // [G]
-  float4* ring = sbi + G;           // kPwStages x (x tile, residual tile)
-  const int stage_f4 = Sh::kXFloat4 + (res ? Sh::kRFloat4 : 0);
+  float4* ring = sbi + G;           // kPwStages x tile
+  constexpr int stage_f4 = Sh::kXFloat4;
   pdl_wait();
   pdl_launch_dependents();
   for (int i = threadIdx.x; i < CI * G; i += kPwThreads) {
@@ -133,16 +133,6 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
       const float* src = in ? a.x + pixel_off(p, a.xs_n, a.xs_h, a.xs_w) + 4 * lj : a.x;
       cp_async16(&xs[lp * kPitch + lj], src, in ? 16 : 0);
     }
-    if (res) {
-      float4* rs = xs + Sh::kXFloat4;
-      for (int piece = threadIdx.x; piece < kTile * G; piece += kPwThreads) {
-        const int lp = piece / G, lg = piece - (piece / G) * G;
-        const long long p = tile * kTile + lp;
-        const bool in = p < M;
-        const float* src = in ? a.ep.r + pixel_off(p, a.ep.rs_n, a.ep.rs_h, a.ep.rs_w) + 4 * lg : a.x;
-        cp_async16(&rs[lp * kRPitch + lg], src, in ? 16 : 0);
-      }
-    }
   };
 
   // prologue: the first kPwStages - 1 tiles of this CTA in flight
@@ -162,10 +152,19 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
     asm volatile("cp.async.wait_group %0;" ::"n"(kPwStages - 1) : "memory");  // this tile has landed
     __syncthreads();
     const float4* xs = ring + slot * stage_f4;
-    const float4* rs = xs + Sh::kXFloat4;
 #pragma unroll
     for (int item = threadIdx.x; item < kItems; item += kPwThreads) {
       const int pg = item / G, g = item - (item / G) * G;  // pixels pg + u * kGroups
+      // the residual's four pixels, in flight during the FMAs (a plain load:
+      // the residual may be y itself, each element read before it is written)
+      float4 rv[kPwU];
+#pragma unroll
+      for (int u = 0; u < kPwU; ++u) {
+        const long long p = tile * kTile + pg + u * kGroups;
+        rv[u] = (res && p < M) ? *reinterpret_cast<const float4*>(
+                                     a.ep.r + pixel_off(p, a.ep.rs_n, a.ep.rs_h, a.ep.rs_w) + 4 * g)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       float4 acc[kPwU];
 #pragma unroll
       for (int u = 0; u < kPwU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -193,9 +192,8 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
         const int lp = pg + u * kGroups;
         const long long p = tile * kTile + lp;
         if (p >= M) continue;
-        const float4 r = res ? rs[lp * kRPitch + g] : make_float4(0.f, 0.f, 0.f, 0.f);
         *reinterpret_cast<float4*>(a.out.y + pixel_off(p, a.out.ys_n, a.out.ys_h, a.out.ys_w) + 4 * g) =
-            pw_epilogue(acc[u], sc, bi, r, a.ep.act, a.ep.res_mode);
+            pw_epilogue(acc[u], sc, bi, rv[u], a.ep.act, a.ep.res_mode);
       }
     }
     __syncthreads();  // a later iteration's copies overwrite this slot
@@ -203,22 +201,27 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-template <int CI, int CO>
-cudaError_t pw_launch(const DirectArgs& a, int flat, int sms, cudaStream_t s) {
+template <int CI, int CO, bool RES>
+cudaError_t pw_launch_res(const DirectArgs& a, int flat, int sms, cudaStream_t s) {
   using Sh = PwShape<CI, CO>;
-  const size_t smem = Sh::smem_bytes(a.ep.res_mode != 0);
+  const size_t smem = Sh::smem_bytes();
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = smem_attr_once<pw_small_kernel<CI, CO>>(smem);
+  cudaError_t e = smem_attr_once<pw_small_kernel<CI, CO, RES>>(smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pw_small_kernel<CI, CO>, kPwThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pw_small_kernel<CI, CO, RES>, kPwThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const long long M = static_cast<long long>(a.N) * a.H * a.W;
   const long long tiles = (M + Sh::kTile - 1) / Sh::kTile;
   const long long cap = static_cast<long long>(sms) * per_sm;
   const unsigned blocks = static_cast<unsigned>(tiles < cap ? tiles : cap);
-  return launch_pdl(pw_small_kernel<CI, CO>, dim3(blocks), dim3(kPwThreads), smem, s, a, flat);
+  return launch_pdl(pw_small_kernel<CI, CO, RES>, dim3(blocks), dim3(kPwThreads), smem, s, a, flat);
+}
+
+template <int CI, int CO>
+cudaError_t pw_launch(const DirectArgs& a, int flat, int sms, cudaStream_t s) {
+  return a.ep.res_mode != 0 ? pw_launch_res<CI, CO, true>(a, flat, sms, s) : pw_launch_res<CI, CO, false>(a, flat, sms, s);
 }
 
 template <int CI>
