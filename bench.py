@@ -596,7 +596,75 @@ class DepthwiseBf16Workload(DepthwiseWorkload):
         return self.x_pin.numel() * 2, (self.y1_pin.numel() + self.y2_pin.numel()) * 2
 
 
-WORKLOADS = {"depthwise": DepthwiseWorkload, "depthwise_bf16": DepthwiseBf16Workload, "dense": DenseWorkload, "mnist": MnistWorkload,
+class PointwiseWorkload(Workload):
+    """The two widest 1x1 layers of the YOLO-style chain at batch 32, 320x320: 16 -> 8 (+ SiLU) and
+    16 -> 16 + SiLU with the post-activation residual; fp32 storage, or bf16 with bf16=True."""
+    dominant = "cv3"
+    bf16 = False
+
+    def __init__(self, torch, device, batch=32):
+        from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
+        from conv_bn_activation_gb300.nets import ConvBnAct
+        self.torch, self.batch = torch, batch
+        dt = torch.bfloat16 if self.bf16 else torch.float32
+        eb = 2 if self.bf16 else 4
+        H = 320
+        x1, w1, bn1 = synthetic.dense_layer(16, 8, H, N=batch, k=1, seed=31)
+        x3, w3, bn3 = synthetic.dense_layer(16, 16, H, N=batch, k=1, seed=33)
+        r3 = synthetic.normal(synthetic.rng(35), (batch, H, H, 16))
+        cast = lambda a: torch.from_numpy(a).to(dt)
+        self.host = {"x1": cast(x1), "x3": cast(x3), "r3": cast(r3)}
+        self.oracle_in = {k: v.float().numpy() for k, v in self.host.items()}
+        self.w = {"cv1": (w1, bn1), "cv3": (w3, bn3)}
+        self.x1, self.x3, self.r3 = (self.host[k].to(device) for k in ("x1", "x3", "r3"))
+        self.l1 = ConvBnAct(w1, bn1, 1, 0, cb.ACT_SILU, device=device)
+        self.l3 = ConvBnAct(w3, bn3, 1, 0, cb.ACT_SILU, device=device)
+        self.y1 = torch.empty(batch, H, H, 8, dtype=dt, device=device)
+        self.y3 = torch.empty(batch, H, H, 16, dtype=dt, device=device)
+        self.launches = [
+            Launch("cv1", lambda s: self.l1(self.x1, self.y1, stream=s),
+                   workloads.conv_layer(batch, H, H, 16, 8, 1, 1, 0, act_bytes=eb),
+                   f"cb::pw_small_kernel<16,8,{'bf16' if self.bf16 else 'f32'}>", "hbm"),
+            Launch("cv3", lambda s: self.l3(self.x3, self.y3, residual=self.r3, res_mode=cb.RES_POST_ACT, stream=s),
+                   workloads.conv_layer(batch, H, H, 16, 16, 1, 1, 0, residual=True, act_bytes=eb),
+                   f"cb::pw_small_kernel<16,16,res,{'bf16' if self.bf16 else 'f32'}>", "hbm"),
+        ]
+        self.config = {"workload": f"pointwise 1x1 + BN + SiLU (YOLO stage-0 shapes 16->8 and 16->16 + residual), "
+                                   f"NHWC {'bf16 storage (fp32 arithmetic)' if self.bf16 else 'fp32'}, N={batch} 320x320",
+                       "batch": batch, "l2": "inputs_larger_than_l2"}
+
+    def e2e_setup(self):
+        t = self.torch
+        self.pin = {k: v.pin_memory() for k, v in self.host.items()}
+        self.y1_pin = t.empty(tuple(self.y1.shape), dtype=self.y1.dtype, pin_memory=True)
+        self.y3_pin = t.empty(tuple(self.y3.shape), dtype=self.y3.dtype, pin_memory=True)
+        eb = self.y1.element_size()
+        return sum(v.numel() for v in self.pin.values()) * eb, (self.y1.numel() + self.y3.numel()) * eb
+
+    def e2e_step(self, stream):
+        self.x1.copy_(self.pin["x1"], non_blocking=True)
+        self.x3.copy_(self.pin["x3"], non_blocking=True)
+        self.r3.copy_(self.pin["r3"], non_blocking=True)
+        self.run(stream)
+        self.y1_pin.copy_(self.y1, non_blocking=True)
+        self.y3_pin.copy_(self.y3, non_blocking=True)
+
+    def cpu_sample(self, n):
+        import oracle
+        o = self.oracle_in
+        t0 = time.perf_counter()
+        oracle.conv_bn_act(o["x1"][:n], *self.w["cv1"], stride=1, pad=0, act=oracle.ACT_SILU)
+        oracle.conv_bn_act(o["x3"][:n], *self.w["cv3"], stride=1, pad=0, act=oracle.ACT_SILU, residual=o["r3"][:n],
+                           res_mode=oracle.RES_POST_ACT)
+        return time.perf_counter() - t0, self.step_units() * n / self.batch, f"{n} of {self.batch} images"
+
+
+class PointwiseBf16Workload(PointwiseWorkload):
+    bf16 = True
+
+
+WORKLOADS = {"depthwise": DepthwiseWorkload, "depthwise_bf16": DepthwiseBf16Workload, "pointwise": PointwiseWorkload,
+             "pointwise_bf16": PointwiseBf16Workload, "dense": DenseWorkload, "mnist": MnistWorkload,
              "yolo": YoloWorkload, "preprocess": PreprocessWorkload}
 
 

@@ -794,8 +794,19 @@ bool tc_shape(int ci, int co, int kh, int stride, int pad) {
          !pointwise_shape(ci, co, kh, stride, pad);
 }
 
+// bf16 storage on a dense layer: the pointwise kernel's 1x1 shapes with
+// 16-byte aligned NHWC views; x is copied in 16-byte pieces (strides that
+// are multiples of 8 elements), y written 4 channels (8 bytes) at a time
+// (multiples of 4).
+bool pointwise_bf16_views(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad) {
+  auto mult8 = [](const cb_tensor* t) { return t->stride_n % 8 == 0 && t->stride_h % 8 == 0 && t->stride_w % 8 == 0; };
+  return g_policy.load() != 1 && kh == 1 && stride == 1 && pad == 0 && pointwise_small_ok(x->c, y->c, true) &&
+         x->layout == CB_LAYOUT_NHWC && aligned16(x->data) && aligned16(y->data) && mult8(x) && strides_mult4(y);
+}
+
 cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan, ImPlan* im) {
   const int policy = g_policy.load();
+  if (!is_f32(x)) return pointwise_bf16_views(x, y, kh, stride, pad) ? CB_PATH_POINTWISE : static_cast<cb_path>(0);
   {
     ConvPlan cp;
     const bool tc_views = policy != 1 && x->layout == CB_LAYOUT_NHWC && aligned16(x->data) && strides_mult4(x) &&
@@ -947,10 +958,11 @@ cb_status run_pointwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
   a.pad = 0;
   a.out = make_out(y);
   a.ep = ep;
+  a.bf16 = x->dtype == CB_DTYPE_BF16 ? 1 : 0;
   const bool flat = pixel_flat(x) && pixel_flat(y) && (ep.res_mode == 0 || pixel_flat(residual));
   cudaError_t e = launch_pointwise_small(a, flat, dev->sms, s);
-  // a shape the kernel does not take: the direct kernel
-  if (e == cudaErrorInvalidValue) return run_direct(x, w, ep, 1, 1, 0, y, s);
+  // a shape the kernel does not take: the direct kernel (fp32 views only)
+  if (e == cudaErrorInvalidValue) return a.bf16 ? CB_ERR_UNSUPPORTED : run_direct(x, w, ep, 1, 1, 0, y, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
 
@@ -1080,7 +1092,10 @@ cb_status validate_conv(const cb_tensor* x, const float* w, const float* scale, 
   const bool depthwise = groups == x->c && groups == y->c && groups > 1;
   if (!depthwise && groups != 1) return CB_ERR_UNSUPPORTED;
   if (x->dtype != y->dtype) return CB_ERR_INVALID_ARG;
-  if (!is_f32(x) && !depthwise) return CB_ERR_UNSUPPORTED;  // bf16 storage: the depthwise kernel only
+  // bf16 storage: the depthwise kernel and the pointwise kernel's 1x1 shapes
+  if (!is_f32(x) && !depthwise &&
+      (g_policy.load() == 1 || kh != 1 || stride != 1 || pad != 0 || !pointwise_small_ok(x->c, y->c, true)))
+    return CB_ERR_UNSUPPORTED;
   if (res_mode != CB_RES_NONE) {
     if (!view_ok(residual) || residual->layout != CB_LAYOUT_NHWC || residual->dtype != y->dtype)
       return CB_ERR_INVALID_ARG;
@@ -1104,6 +1119,14 @@ cb_status launch_conv(const cb_tensor* x, const float* w, const float* scale, co
                       const cb_tensor* y, cudaStream_t s, const ConvPlan* force) {
   const Epilogue ep = make_epilogue(scale, bias, act, residual, res_mode);
   if (depthwise) return run_depthwise(x, w, ep, stride, pad, y, s);
+  if (!is_f32(x)) {
+    // bf16 storage (a pointwise shape, checked in validation): aligned views
+    // and operands, else no kernel takes it
+    if (!pointwise_bf16_views(x, y, kh, stride, pad) || !aligned16(w) || !aligned16(scale) || !aligned16(bias) ||
+        (res_mode != CB_RES_NONE && (!aligned16(residual->data) || !strides_mult4(residual))))
+      return CB_ERR_ALIGNMENT;
+    return run_pointwise(x, w, ep, residual, y, s);
+  }
   HaloPlan plan;
   ImPlan im;
   const cb_path path = force ? force->path : dense_path(x, y, kh, stride, pad, &plan, &im);
@@ -1604,7 +1627,7 @@ int cb_conv_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int
   if (!view_ok(x) || !view_ok(y) || (kh != 1 && kh != 3) || (stride != 1 && stride != 2)) return 0;
   if (pad < 0 || pad > kh / 2) return 0;
   if (groups == x->c && groups == y->c && groups > 1) return kh == 3 && x->dtype == y->dtype ? CB_PATH_DEPTHWISE : 0;
-  if (groups != 1 || !is_f32(x) || !is_f32(y)) return 0;
+  if (groups != 1 || x->dtype != y->dtype) return 0;
   return dense_path(x, y, kh, stride, pad, nullptr);
 }
 

@@ -21,8 +21,6 @@
 //  * dw_simple_kernel: one thread per (output pixel, 4 channels) or per
 //    channel, direct global loads.  Used for views the TMA path cannot
 //    describe (unaligned data, channel counts that are not multiples of 4).
-#include <cuda_bf16.h>
-
 #include "epilogue.cuh"
 #include "launch_util.h"
 #include "internal.h"
@@ -123,23 +121,6 @@ __device__ __forceinline__ DwItem dw_decode(const DwTmaParams& p, int item) {
 }
 
 constexpr int kDwProducerLanes = 4;
-
-// Four consecutive channels as fp32, from fp32 or bf16 storage (a bf16 value
-// is the upper half of the fp32 with the same bits: widening is exact).
-__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
-  const uint2 v = *reinterpret_cast<const uint2*>(p);
-  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
-                     __uint_as_float(v.y & 0xFFFF0000u));
-}
-__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-  uint2 u;
-  u.x = *reinterpret_cast<const uint32_t*>(&lo);
-  u.y = *reinterpret_cast<const uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(p) = u;
-}
 
 // acc += a * b on four lanes as two packed fp32 FMAs (each lane rounded as
 // one fmaf: the same bits as fma4, half the instructions).
@@ -289,7 +270,7 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
                       : nullptr;
 
     // One output row from the window (top, mid, bottom); advances yp / rp.
-    auto compute = [&](const float4(&T)[NC], const float4(&M)[NC], const float4(&B)[NC]) {
+    auto compute = [&](const float4(&top)[NC], const float4(&mid)[NC], const float4(&bot)[NC]) {
       if (ok && active) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -299,13 +280,13 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
             if constexpr (kPacked) {
               // bf16 storage moves half the bytes per output: the arithmetic
               // must keep up, so the FMAs go out packed
-              fma4_packed(acc, T[j * S + kw], wv[kw]);
-              fma4_packed(acc, M[j * S + kw], wv[3 + kw]);
-              fma4_packed(acc, B[j * S + kw], wv[6 + kw]);
+              fma4_packed(acc, top[j * S + kw], wv[kw]);
+              fma4_packed(acc, mid[j * S + kw], wv[3 + kw]);
+              fma4_packed(acc, bot[j * S + kw], wv[6 + kw]);
             } else {
-              fma4(acc, T[j * S + kw], wv[kw]);
-              fma4(acc, M[j * S + kw], wv[3 + kw]);
-              fma4(acc, B[j * S + kw], wv[6 + kw]);
+              fma4(acc, top[j * S + kw], wv[kw]);
+              fma4(acc, mid[j * S + kw], wv[3 + kw]);
+              fma4(acc, bot[j * S + kw], wv[6 + kw]);
             }
           }
           if (j == 0 || second) {

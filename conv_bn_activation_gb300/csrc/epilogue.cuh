@@ -4,7 +4,10 @@
 // the 1e-5 bar of the fp32 paths).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cstdint>
 
 namespace cb {
 
@@ -48,6 +51,24 @@ __device__ __forceinline__ void fma4(float4& acc, float4 a, float4 b) {
   acc.y = fmaf(a.y, b.y, acc.y);
   acc.z = fmaf(a.z, b.z, acc.z);
   acc.w = fmaf(a.w, b.w, acc.w);
+}
+
+// Four consecutive channels as fp32, from fp32 or bf16 storage (a bf16 value
+// is the upper half of the fp32 with the same bits: widening is exact), and
+// back (bf16: rounded to nearest even).
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
+                     __uint_as_float(v.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&lo);
+  u.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
 }
 
 }  // namespace cb

@@ -61,12 +61,14 @@ struct DirectArgs {
   int N, H, W, Ci, Co, OH, OW, kh, kw, stride, pad;
   OutView out;
   Epilogue ep;
+  int bf16;  // x, y and r hold bfloat16 (pointwise kernel only); w, scale, bias fp32
 };
 cudaError_t launch_direct(const DirectArgs& a, int sms, cudaStream_t s);
 // 1x1 stride-1 layers with Ci, Co in {4, 8, 16, 32} (pointwise.cu): needs
 // NHWC views with 16-byte aligned pixels; flat = every view's pixels are
-// evenly spaced (stride_h = W * stride_w, stride_n = H * stride_h).
-bool pointwise_small_ok(int ci, int co);
+// evenly spaced (stride_h = W * stride_w, stride_n = H * stride_h).  With
+// bf16 storage Ci >= 8 (a pixel holds at least one 16-byte piece).
+bool pointwise_small_ok(int ci, int co, bool bf16 = false);
 cudaError_t launch_pointwise_small(const DirectArgs& a, bool flat, int sms, cudaStream_t s);
 
 // ------------------------------------------------------- implicit GEMM (tcgen05)

@@ -59,18 +59,18 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 constexpr int kPwThreads = 256;
 constexpr int kPwU = 4;       // pixels per thread (register blocking)
 constexpr int kPwStages = 3;  // tiles in flight per CTA (ring depth)
 
-template <int CI, int CO>
+template <int CI, int CO, typename T>
 struct PwShape {
   static constexpr int G = CO / 4;                                // channel groups of 4 outputs
-  static constexpr int kVec = CI / 4;                             // 16-byte input pieces per pixel
-  static constexpr int kPitch = kVec >= 4 ? kVec + 1 : kVec;      // staged input row, float4s (padded)
-  static constexpr int kTile = 4096 / CI;                         // pixels per tile (16 KB of input)
+  static constexpr int kEpp = 16 / static_cast<int>(sizeof(T));   // elements per 16-byte piece
+  static constexpr int kVec = CI / kEpp;                          // 16-byte input pieces per pixel
+  static constexpr int kPitch = kVec >= 4 ? kVec + 1 : kVec;      // staged input row, 16-byte units (padded)
+  static constexpr int kTile = 4096 / CI;  // pixels per tile (16 KB of fp32 input, 8 KB of bf16)
   static constexpr int kGroups = kTile / kPwU;                    // pixel groups per tile
   static constexpr int kItems = kGroups * G;                      // (pixel group, channel group) items
   static constexpr int kXFloat4 = kTile * kPitch;
@@ -80,19 +80,22 @@ struct PwShape {
 };
 
 // A ring of kPwStages tiles per CTA: a tile is kTile pixels whose CI inputs
-// are 16 KB, copied
+// are 16 KB (8 KB in bf16), copied
 // with 16-byte cp.async by all threads (different bytes per thread).  The
 // staged rows of 64 bytes or more are padded by 16 bytes so that the
 // pixel-strided reads below hit distinct bank groups.  Each thread computes
 // 4 pixels x 4 output channels: per 4 input channels it reads 4 pixel
-// float4s and 4 weight float4s and does 64 FMAs.
-template <int CI, int CO, bool RES>
+// float4s and 4 weight float4s and does 64 FMAs.  T: the storage type of x,
+// y and the residual (float, or bf16 widened to fp32 as it leaves shared
+// memory and rounded to nearest even at the store).
+template <int CI, int CO, bool RES, typename T>
 __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a, int flat) {
   static_assert(CI % 4 == 0 && CO % 4 == 0 && CI <= 32 && CO <= 32, "channel counts");
-  using Sh = PwShape<CI, CO>;
-  constexpr int G = Sh::G, kVec = Sh::kVec, kPitch = Sh::kPitch;
+  using Sh = PwShape<CI, CO, T>;
+  constexpr int G = Sh::G, kVec = Sh::kVec, kPitch = Sh::kPitch, kEpp = Sh::kEpp;
   constexpr int kTile = Sh::kTile, kGroups = Sh::kGroups, kItems = Sh::kItems;
-  static_assert(kTile * kVec == 4 * kPwThreads && kPwThreads % G == 0, "tile shape");
+  constexpr int kPieces = kTile * kVec / kPwThreads;  // 16-byte copies per thread per tile
+  static_assert(kVec >= 1 && kPieces * kPwThreads == kTile * kVec && kPwThreads % G == 0, "tile shape");
   extern __shared__ float4 pw_smem[];
   constexpr bool res = RES;  // a residual (its placement is a.ep.res_mode)
   float4* ws = pw_smem;             // [CI][G]
@@ -125,12 +128,13 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
   auto stage = [&](long long tile, int slot) {
     float4* xs = ring + slot * stage_f4;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kPieces; ++k) {
       const int piece = threadIdx.x + k * kPwThreads;
       const int lp = piece / kVec, lj = piece - (piece / kVec) * kVec;
       const long long p = tile * kTile + lp;
       const bool in = p < M;
-      const float* src = in ? a.x + pixel_off(p, a.xs_n, a.xs_h, a.xs_w) + 4 * lj : a.x;
+      const T* x = reinterpret_cast<const T*>(a.x);
+      const T* src = in ? x + pixel_off(p, a.xs_n, a.xs_h, a.xs_w) + kEpp * lj : x;
       cp_async16(&xs[lp * kPitch + lj], src, in ? 16 : 0);
     }
   };
@@ -152,7 +156,9 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
     asm volatile("cp.async.wait_group %0;" ::"n"(kPwStages - 1) : "memory");  // this tile has landed
     __syncthreads();
     const float4* xs = ring + slot * stage_f4;
-#pragma unroll
+    // one item per thread at a time (bf16 tiles hold two per thread; their
+    // loads hoisted together would double the live registers)
+#pragma unroll 1
     for (int item = threadIdx.x; item < kItems; item += kPwThreads) {
       const int pg = item / G, g = item - (item / G) * G;  // pixels pg + u * kGroups
       // the residual's four pixels, in flight during the FMAs (a plain load:
@@ -161,18 +167,19 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
 #pragma unroll
       for (int u = 0; u < kPwU; ++u) {
         const long long p = tile * kTile + pg + u * kGroups;
-        rv[u] = (res && p < M) ? *reinterpret_cast<const float4*>(
-                                     a.ep.r + pixel_off(p, a.ep.rs_n, a.ep.rs_h, a.ep.rs_w) + 4 * g)
+        rv[u] = (res && p < M) ? load4(reinterpret_cast<const T*>(a.ep.r) +
+                                       pixel_off(p, a.ep.rs_n, a.ep.rs_h, a.ep.rs_w) + 4 * g)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       float4 acc[kPwU];
 #pragma unroll
       for (int u = 0; u < kPwU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int c4 = 0; c4 < kVec; ++c4) {
+      for (int c4 = 0; c4 < CI / 4; ++c4) {
         float4 xv[kPwU];
 #pragma unroll
-        for (int u = 0; u < kPwU; ++u) xv[u] = xs[(pg + u * kGroups) * kPitch + c4];
+        for (int u = 0; u < kPwU; ++u)
+          xv[u] = load4(reinterpret_cast<const T*>(xs + (pg + u * kGroups) * kPitch) + 4 * c4);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float4 w4 = ws[(4 * c4 + e) * G + g];
@@ -192,8 +199,8 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
         const int lp = pg + u * kGroups;
         const long long p = tile * kTile + lp;
         if (p >= M) continue;
-        *reinterpret_cast<float4*>(a.out.y + pixel_off(p, a.out.ys_n, a.out.ys_h, a.out.ys_w) + 4 * g) =
-            pw_epilogue(acc[u], sc, bi, rv[u], a.ep.act, a.ep.res_mode);
+        store4(reinterpret_cast<T*>(a.out.y) + pixel_off(p, a.out.ys_n, a.out.ys_h, a.out.ys_w) + 4 * g,
+               pw_epilogue(acc[u], sc, bi, rv[u], a.ep.act, a.ep.res_mode));
       }
     }
     __syncthreads();  // a later iteration's copies overwrite this slot
@@ -201,27 +208,35 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-template <int CI, int CO, bool RES>
+template <int CI, int CO, bool RES, typename T>
 cudaError_t pw_launch_res(const DirectArgs& a, int flat, int sms, cudaStream_t s) {
-  using Sh = PwShape<CI, CO>;
+  using Sh = PwShape<CI, CO, T>;
   const size_t smem = Sh::smem_bytes();
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = smem_attr_once<pw_small_kernel<CI, CO, RES>>(smem);
+  cudaError_t e = smem_attr_once<pw_small_kernel<CI, CO, RES, T>>(smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pw_small_kernel<CI, CO, RES>, kPwThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pw_small_kernel<CI, CO, RES, T>, kPwThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const long long M = static_cast<long long>(a.N) * a.H * a.W;
   const long long tiles = (M + Sh::kTile - 1) / Sh::kTile;
   const long long cap = static_cast<long long>(sms) * per_sm;
   const unsigned blocks = static_cast<unsigned>(tiles < cap ? tiles : cap);
-  return launch_pdl(pw_small_kernel<CI, CO, RES>, dim3(blocks), dim3(kPwThreads), smem, s, a, flat);
+  return launch_pdl(pw_small_kernel<CI, CO, RES, T>, dim3(blocks), dim3(kPwThreads), smem, s, a, flat);
 }
 
 template <int CI, int CO>
 cudaError_t pw_launch(const DirectArgs& a, int flat, int sms, cudaStream_t s) {
-  return a.ep.res_mode != 0 ? pw_launch_res<CI, CO, true>(a, flat, sms, s) : pw_launch_res<CI, CO, false>(a, flat, sms, s);
+  const bool res = a.ep.res_mode != 0;
+  if (a.bf16) {
+    if constexpr (CI >= 8) {
+      return res ? pw_launch_res<CI, CO, true, __nv_bfloat16>(a, flat, sms, s)
+                 : pw_launch_res<CI, CO, false, __nv_bfloat16>(a, flat, sms, s);
+    }
+    return cudaErrorInvalidValue;
+  }
+  return res ? pw_launch_res<CI, CO, true, float>(a, flat, sms, s) : pw_launch_res<CI, CO, false, float>(a, flat, sms, s);
 }
 
 template <int CI>
@@ -237,8 +252,8 @@ cudaError_t pw_launch_co(const DirectArgs& a, int flat, int sms, cudaStream_t s)
 
 }  // namespace
 
-bool pointwise_small_ok(int ci, int co) {
-  return (ci == 4 || ci == 8 || ci == 16 || ci == 32) && (co == 4 || co == 8 || co == 16 || co == 32);
+bool pointwise_small_ok(int ci, int co, bool bf16) {
+  return (ci == 8 || ci == 16 || ci == 32 || (ci == 4 && !bf16)) && (co == 4 || co == 8 || co == 16 || co == 32);
 }
 
 cudaError_t launch_pointwise_small(const DirectArgs& a, bool flat, int sms, cudaStream_t s) {

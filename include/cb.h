@@ -61,7 +61,7 @@ typedef enum { CB_LAYOUT_NHWC = 0, CB_LAYOUT_NCHW = 1 } cb_layout;
  * Element type of an activation view.  CB_DTYPE_F32 (0, the default of a
  * zero-initialised view) everywhere; CB_DTYPE_BF16 (bfloat16: the upper half
  * of an fp32) is the half-size storage variant, taken by the depthwise 3x3
- * layers of cb_conv_bn_act: a 16-bit main data type is the first of the
+ * and the narrow 1x1 layers of cb_conv_bn_act: a 16-bit main data type is the first of the
  * next steps "How I sped up convolutions" lists (ideas and next steps), and
  * those layers are memory-bound, so halving their bytes halves their time.
  * Arithmetic stays fp32; a BF16 output is the fp32 result rounded to
@@ -141,12 +141,15 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
  * for all nine taps; the others gather one tile per tap.  1x1 stride-1
  * layers with Ci and Co in {4, 8, 16, 32} run instead on a streaming fp32
  * CUDA-core kernel (HBM-bound at these widths);
- * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel, in
- * fp32 or with bf16 storage (x, y and residual all CB_DTYPE_BF16; weights,
- * scale and bias stay fp32 and the arithmetic fp32; needs C % 8 == 0,
- * 16-byte aligned x, y, residual, w, scale and bias, and NHWC strides that
- * are multiples of 8 elements: else CB_ERR_ALIGNMENT; dense bf16 layers
- * return CB_ERR_UNSUPPORTED);
+ * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;
+ * bf16 storage (x, y and residual all CB_DTYPE_BF16; weights, scale and
+ * bias stay fp32, and so does the arithmetic) is taken by the depthwise 3x3
+ * layers (C % 8 == 0) and by the 1x1 stride-1 layers of the streaming
+ * kernel with Ci in {8, 16, 32} and Co in {4, 8, 16, 32}; both need 16-byte
+ * aligned x, y, residual, w, scale and bias, x strides that are multiples
+ * of 8 elements and y / residual strides that are multiples of 8 (depthwise)
+ * or 4 (1x1) elements (else CB_ERR_ALIGNMENT); any other bf16 layer
+ * returns CB_ERR_UNSUPPORTED;
  * 3 -> 16 channel 3x3 stride-2 pad-1 stems run on a dedicated fp32 CUDA-core
  * kernel when the input is planar (NCHW) or packed NHWC (stride_w == 3) with
  * W % 4 == 0, 16-byte aligned data and n / h (/ c) strides that are

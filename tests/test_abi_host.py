@@ -106,8 +106,8 @@ def test_conv_rejects_invalid_arguments_before_launch(cblib):
 
 
 def test_bf16_views_validated_before_launch(cblib):
-    """bf16 storage: depthwise only, every view the same element type, unknown element types
-    rejected -- all decided on the host (fake pointers, never dereferenced)."""
+    """bf16 storage: depthwise 3x3 and narrow 1x1 layers only, every view the same element type,
+    unknown element types rejected -- all decided on the host (fake pointers, never dereferenced)."""
     lib = cblib.load()
     T = ctypes.byref
     base = 1 << 20
@@ -127,6 +127,10 @@ def test_bf16_views_validated_before_launch(cblib):
     assert call(x16, y16, g=16, r=v(base + (1 << 17), 1, 8, 8, 16, cblib.DTYPE_F32), rm=2) == cblib.ERR_INVALID_ARG
     assert call(v(base, 1, 8, 8, 16, 7), v(base + (1 << 16), 1, 8, 8, 16, 7), g=16) == cblib.ERR_INVALID_ARG
     assert lib.cb_conv_path(T(x16), T(y16), 3, 1, 1, 16) == cblib.PATH_DEPTHWISE
+    assert lib.cb_conv_path(T(x16), T(y16), 1, 1, 0, 1) == cblib.PATH_POINTWISE   # 1x1 16 -> 16
+    x4 = v(base, 1, 8, 8, 4, cblib.DTYPE_BF16)
+    assert lib.cb_conv_bn_act(T(x4), w, s, b, 1, 1, 1, 0, 1, 0, None, 0, T(v(base + (1 << 16), 1, 8, 8, 16, cblib.DTYPE_BF16)),
+                              None) == cblib.ERR_UNSUPPORTED                   # 1x1 bf16 needs Ci >= 8
     assert lib.cb_conv_path(T(x16), T(y16), 3, 1, 1, 1) == 0
     assert lib.cb_conv_path(T(x16), T(y32), 3, 1, 1, 16) == 0
     # empty bf16 depthwise batch: valid, nothing to launch

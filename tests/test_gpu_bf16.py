@@ -1,5 +1,5 @@
-"""GPU parity of the bf16 storage variant: depthwise 3x3 + folded BN + activation (+ residual)
-with x, y and the residual held as bfloat16 and the arithmetic in fp32.
+"""GPU parity of the bf16 storage variant: depthwise 3x3 and narrow pointwise 1x1 + folded BN +
+activation (+ residual) with x, y and the residual held as bfloat16 and the arithmetic in fp32.
 
 The inputs are bf16 values; the oracle computes in fp64 on exactly those values.  Bars: every
 output within half a bf16 unit in the last place of the oracle (2^-8 of the value, plus the
@@ -146,4 +146,71 @@ def test_bf16_rejections(gpu):
     assert e.value.status == cb.ERR_UNSUPPORTED
     with pytest.raises(TypeError):
         cb.conv_path(torch.empty(1, 8, 8, 32, dtype=torch.float16, device=gpu), y16, 3, 1, 1)
+    sync_check()
+
+
+PW_CASES = [
+    # N, H, W, Ci, Co, act, res_mode
+    (2, 9, 13, 16, 8, cb.ACT_SILU, 0), (2, 9, 13, 16, 16, cb.ACT_SILU, 2), (1, 5, 40, 32, 16, cb.ACT_RELU, 0),
+    (2, 7, 7, 32, 32, cb.ACT_SILU, 2), (3, 4, 5, 8, 32, cb.ACT_RELU, 1), (1, 1, 1, 8, 4, cb.ACT_NONE, 0),
+    (2, 33, 31, 16, 16, cb.ACT_SILU, 1),
+]
+
+
+@pytest.mark.parametrize("case", PW_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_bf16_pointwise(gpu, orc, case):
+    N, H, W, Ci, Co, act, rm = case
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=1, seed=sum(case))
+    layer = ConvBnAct(w, bn, 1, 0, act)
+    xd, xv = to_dev_bf16(x)
+    r = np.random.default_rng(4).standard_normal((N, H, W, Co)).astype(np.float32)
+    rd, rv = to_dev_bf16(r)
+    y = torch.empty(N, H, W, Co, dtype=torch.bfloat16, device=gpu)
+    assert cb.conv_path(xd, y, 1, 1, 0) == cb.PATH_POINTWISE
+    layer(xd, y, residual=rd if rm else None, res_mode=rm)
+    sync_check()
+    ref = orc.conv_bn_act(xv, w, bn, stride=1, pad=0, act=act, residual=rv if rm else None, res_mode=rm)
+    got = y.float().cpu().numpy()
+    assert bf16_within_half_ulp(got, ref) <= 1.0
+    assert rel_err(got, ref) <= TOL_BF16
+    # the fp32 kernel runs the same sums: its output rounded to bf16 is this one, bit for bit
+    y32 = torch.empty(N, H, W, Co, device=gpu)
+    layer(torch.from_numpy(xv).to(gpu), y32, residual=torch.from_numpy(rv).to(gpu) if rm else None, res_mode=rm)
+    sync_check()
+    assert torch.equal(y.view(torch.int16), y32.to(torch.bfloat16).view(torch.int16))
+
+
+def test_bf16_pointwise_in_place_residual_and_views(gpu, orc):
+    """Residual added in place (r is y) and the output a channel slice of a wider bf16 buffer."""
+    N, H, W, Ci, Co = 2, 6, 10, 16, 16
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=1, seed=21)
+    layer = ConvBnAct(w, bn, 1, 0, cb.ACT_SILU)
+    xd, xv = to_dev_bf16(x)
+    r = np.random.default_rng(6).standard_normal((N, H, W, Co)).astype(np.float32)
+    rd, rv = to_dev_bf16(r)
+    buf = canary_buffer_bf16((N, H, W, Co + 16))
+    y = buf[..., 8:8 + Co]
+    y.copy_(rd)
+    layer(xd, y, residual=y, res_mode=cb.RES_POST_ACT)
+    sync_check()
+    ref = orc.conv_bn_act(xv, w, bn, stride=1, pad=0, act=orc.ACT_SILU, residual=rv, res_mode=orc.RES_POST_ACT)
+    assert bf16_within_half_ulp(y.float().cpu().numpy(), ref) <= 1.0
+    assert is_canary_bf16(buf[..., :8]) and is_canary_bf16(buf[..., 8 + Co:])
+
+
+def test_bf16_pointwise_rejections(gpu):
+    x, w, bn = synthetic.dense_layer(48, 32, 6, N=1, k=1, seed=2)  # a tensor-core 1x1 shape
+    layer = ConvBnAct(w, bn, 1, 0, cb.ACT_SILU)
+    xd, _ = to_dev_bf16(x)
+    y = torch.empty(1, 6, 6, 32, dtype=torch.bfloat16, device=gpu)
+    assert cb.conv_path(xd, y, 1, 1, 0) == 0
+    with pytest.raises(cb.CbError) as e:
+        layer(xd, y)
+    assert e.value.status == cb.ERR_UNSUPPORTED
+    x, w, bn = synthetic.dense_layer(16, 16, 6, N=1, k=1, seed=3)
+    layer = ConvBnAct(w, bn, 1, 0, cb.ACT_SILU)
+    xs = torch.empty(1, 6, 6, 20, dtype=torch.bfloat16, device=gpu)[..., 2:18]  # 4-byte aligned pixels
+    with pytest.raises(cb.CbError) as e:
+        layer(xs, torch.empty(1, 6, 6, 16, dtype=torch.bfloat16, device=gpu))
+    assert e.value.status == cb.ERR_ALIGNMENT
     sync_check()
