@@ -317,8 +317,9 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
     return e == cudaSuccess ? CB_OK : cuda_fail(e);
   }
 
-  // Plan.  Output-column tiles of at most 120 columns (8 consumer threads
-  // per column pair; bf16: 60 columns, 16 threads per pair), 128-byte
+  // Plan.  Output-column tiles of at most 120 columns (fp32: 8 consumer
+  // threads per column pair; bf16: 16 threads per group of 4 columns at
+  // stride 1, of 2 columns (tiles of 60) at stride 2), 128-byte
   // chunks of each pixel (32 fp32 or 64 bf16 channels: an SM completes its
   // row copies one after another, so the copy count, not their bytes, sets
   // the pace) and short strips of output rows: measured on the
@@ -326,7 +327,9 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
   // strips (which stage fewer halo rows) by 10-15%, because the CTAs in
   // flight then cover a narrow band of rows whose halos hit in L2.  Strips
   // shrink further when a layer has too few items to fill the GPU.
-  const int ch = a.bf16 ? 64 : 32, tpp = ch / 4, max_tile = a.bf16 ? 60 : 120;
+  const int ch = a.bf16 ? 64 : 32, tpp = ch / 4;
+  const int cols = a.bf16 && stride == 1 ? 4 : 2;  // output columns per consumer thread (the kernel's rule)
+  const int max_tile = a.bf16 && stride == 2 ? 60 : 120;  // at most 480 consumer threads
   const int chunks = (a.C + ch - 1) / ch;
   // Tuning override (CB_DW_FORCE="rows,tile_w,ctas_per_sm"; 0 = free), read per call.
   int force_r = 0, force_tw = 0, force_cps = 0;
@@ -336,14 +339,16 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
     const int wt = (a.OW + max_tile - 1) / max_tile;
     const int tile_w = force_tw > 0 ? std::min({force_tw, a.OW, max_tile}) : (a.OW + wt - 1) / wt;
     const int wtiles = (a.OW + tile_w - 1) / tile_w;
-    const int pairs = (tile_w + 1) / 2;
-    const int box_w = (2 * pairs - 1) * stride + 3;  // both columns of the last pair are covered
-    const int consumer_warps = (pairs * tpp + 31) / 32;
+    const int groups = (tile_w + cols - 1) / cols;
+    const int box_w = (cols * groups - 1) * stride + 3;  // every column of the last group is covered
+    const int consumer_warps = (groups * tpp + 31) / 32;
     const int threads = 32 * (1 + consumer_warps);
     int cps = dw_tma_blocks_per_sm(stride, threads, 96 * 1024, a.bf16 != 0) >= 2 ? 2 : 1;
     if (force_cps == 1 || force_cps == 2) cps = force_cps;
     const int stage_bytes = box_w * 128;  // a ring slot: one row of 128-byte pixel chunks
-    const size_t ring = cps == 2 ? 96 * 1024 : 192 * 1024;
+    // four-column threads read the taps from shared memory when they fit
+    const size_t w_bytes = cols == 4 && 36ull * a.C <= 48 * 1024 ? 36ull * a.C : 0;
+    const size_t ring = (cps == 2 ? 96 * 1024 : 192 * 1024) - w_bytes;
     const int stages = static_cast<int>(std::min<size_t>(32, ring / stage_bytes));
     const int cap = dev->sms * cps;
     // bf16 at stride 1: 8-row strips (the kernel is bound by its instruction
@@ -362,7 +367,8 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
       best.stages = stages;
       best.grid = static_cast<int>(std::min<long long>(items, cap));
       best.consumer_warps = consumer_warps;
-      best.smem_bytes = static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t) + 16;
+      best.w_smem = w_bytes ? 1 : 0;
+      best.smem_bytes = static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t) + 16 + w_bytes;
     }
   }
   if (std::getenv("CB_DEBUG_PLAN"))

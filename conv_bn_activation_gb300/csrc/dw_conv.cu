@@ -91,7 +91,8 @@ cudaError_t launch_dw_simple(const DwArgs& a, bool vec4, cudaStream_t s) {
 struct DwTmaParams {
   DwArgs a;
   int rows_per_item, num_items, box_w, stages;
-  int ch;  // channels per chunk: one 128-byte pixel row (32 fp32 or 64 bf16)
+  int ch;      // channels per chunk: one 128-byte pixel row (32 fp32 or 64 bf16)
+  int w_smem;  // bf16 at stride 1: the taps [9][C] staged in shared memory after the barriers
   int chunks, strips, wtiles, tile_w;
   int* err;
   uint64_t timeout_ns;
@@ -140,13 +141,20 @@ __device__ __forceinline__ float epi_c(float acc, float sc, float bi, float r) {
   return z;
 }
 
-// Each consumer thread owns two adjacent output columns x 4 channels; its
-// window needs NC = S + 3 input columns per row.  T: the storage type of x,
-// y and the residual (float or bf16).
+// Output columns per consumer thread: 4 for bf16 at stride 1, else 2.  bf16
+// carries twice the outputs per byte, so the per-row costs (barrier wait,
+// loads, widening) must be shared by more of them.
+template <typename T, int S>
+__host__ __device__ constexpr int dw_cols() { return sizeof(T) == 2 && S == 1 ? 4 : 2; }
+
+// Each consumer thread owns COLS adjacent output columns x 4 channels; its
+// window needs NC = (COLS - 1) S + 3 input columns per row.  T: the storage
+// type of x, y and the residual (float or bf16).
 template <typename T, int S, int ACT, int RES>
 __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ CUtensorMap xmap,
                                                         const DwTmaParams p) {
-  constexpr int NC = S + 3;
+  constexpr int COLS = dw_cols<T, S>();
+  constexpr int NC = (COLS - 1) * S + 3;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // One ring slot: a row copy of box_w pixels of one chunk, 128 bytes each
   // (32 fp32 or 64 bf16 channels: an SM completes its copies one after
@@ -154,7 +162,7 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
   // channels, and the layer takes half the copies).
   constexpr int CH = 128 / static_cast<int>(sizeof(T));  // channels per chunk
   constexpr bool kPacked = sizeof(T) == 2;                 // packed FMAs (bf16 storage)
-  constexpr int TPP = CH / 4;                              // threads per column pair
+  constexpr int TPP = CH / 4;                              // threads per column group
   const int stage_bytes = p.box_w * 128;
   uint8_t* ring = smem_raw;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + p.stages * stage_bytes);
@@ -176,6 +184,19 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
   pdl_wait();
   const Watchdog wd{p.err, abort_flag, p.timeout_ns};
   const DwArgs& a = p.a;
+  // Four-column threads read each tap once per input row for all four
+  // columns: the taps come from shared memory (staged once per CTA) or, for
+  // a layer too wide to stage, from L1.
+  float* sw = reinterpret_cast<float*>(reinterpret_cast<uintptr_t>(abort_flag) + 16);  // 16-byte aligned
+  const float* wsrc = a.w;
+  if constexpr (COLS == 4) {
+    if (p.w_smem) {
+      for (int i = threadIdx.x; i < 9 * a.C / 4; i += blockDim.x)
+        reinterpret_cast<float4*>(sw)[i] = ldg4(a.w + 4 * i);
+      __syncthreads();
+      wsrc = sw;
+    }
+  }
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -219,7 +240,7 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
 
   // ------------------------------------------------------------ consumers
   const int t = threadIdx.x - 32;
-  const int pair = t / TPP, c4 = t % TPP;
+  const int grp = t / TPP, c4 = t % TPP;
   int slot = 0;
   uint32_t phase = 0;
   bool ok = true;
@@ -235,7 +256,7 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
       return;
     }
     if (read) {
-      const T* row = reinterpret_cast<const T*>(ring + slot * stage_bytes) + (2 * pair * S) * CH + c4 * 4;
+      const T* row = reinterpret_cast<const T*>(ring + slot * stage_bytes) + (COLS * grp * S) * CH + c4 * 4;
 #pragma unroll
       for (int k = 0; k < NC; ++k) dst[k] = load4(row + k * CH);
     }
@@ -249,19 +270,21 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
 
   for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
     const DwItem it = dw_decode(p, item);
-    const int ow = it.ow0 + 2 * pair;
+    const int ow = it.ow0 + COLS * grp;
     const int c = it.c0 + c4 * 4;
-    const bool in_tile = ow < it.ow1;            // the box covers both columns of every pair
+    const bool in_tile = ow < it.ow1;            // the box covers every column of every group
     const bool active = in_tile && c < a.C;
     const bool second = active && ow + 1 < it.ow1;
-    float4 wv[9];
+    float4 wv[COLS == 2 ? 9 : 1];
     float4 sc = make_float4(0.f, 0.f, 0.f, 0.f), bi = sc;
     if (active) {
+      if constexpr (COLS == 2) {
 #pragma unroll
-      for (int k = 0; k < 9; ++k) wv[k] = ldg4(a.w + k * a.C + c);
+        for (int k = 0; k < 9; ++k) wv[k] = ldg4(a.w + k * a.C + c);
+      }
       sc = ldg4(a.ep.scale + c);
       bi = ldg4(a.ep.bias + c);
-    } else {
+    } else if constexpr (COLS == 2) {
 #pragma unroll
       for (int k = 0; k < 9; ++k) wv[k] = sc;
     }
@@ -271,7 +294,40 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
 
     // One output row from the window (top, mid, bottom); advances yp / rp.
     auto compute = [&](const float4(&top)[NC], const float4(&mid)[NC], const float4(&bot)[NC]) {
-      if (ok && active) {
+      if constexpr (COLS == 4) {
+        if (ok && active) {
+          // the same sum order as the two-column path: tap columns kw, and
+          // within each the top, middle and bottom rows
+          float4 acc[COLS];
+#pragma unroll
+          for (int j = 0; j < COLS; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int kw = 0; kw < 3; ++kw) {
+            const float4 wt = *reinterpret_cast<const float4*>(wsrc + kw * a.C + c);
+            const float4 wm = *reinterpret_cast<const float4*>(wsrc + (3 + kw) * a.C + c);
+            const float4 wb = *reinterpret_cast<const float4*>(wsrc + (6 + kw) * a.C + c);
+#pragma unroll
+            for (int j = 0; j < COLS; ++j) {
+              fma4_packed(acc[j], top[j * S + kw], wt);
+              fma4_packed(acc[j], mid[j * S + kw], wm);
+              fma4_packed(acc[j], bot[j * S + kw], wb);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < COLS; ++j) {
+            if (ow + j < it.ow1) {
+              float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (RES) r = load4(rp + j * a.ep.rs_w);
+              float4 o;
+              o.x = epi_c<ACT, RES>(acc[j].x, sc.x, bi.x, r.x);
+              o.y = epi_c<ACT, RES>(acc[j].y, sc.y, bi.y, r.y);
+              o.z = epi_c<ACT, RES>(acc[j].z, sc.z, bi.z, r.z);
+              o.w = epi_c<ACT, RES>(acc[j].w, sc.w, bi.w, r.w);
+              store4(yp + j * a.out.ys_w, o);
+            }
+          }
+        }
+      } else if (ok && active) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -371,6 +427,7 @@ cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaP
   p.box_w = plan.box_w;
   p.stages = plan.stages;
   p.ch = a.bf16 ? 64 : 32;
+  p.w_smem = plan.w_smem;
   p.chunks = (a.C + p.ch - 1) / p.ch;
   p.strips = (a.OH + plan.rows_per_item - 1) / plan.rows_per_item;
   p.tile_w = plan.tile_w;

@@ -48,6 +48,7 @@ struct DwTmaPlan {
   int stages;
   int grid;
   int consumer_warps;
+  int w_smem;  // bf16 at stride 1: the 9 x C taps staged in shared memory after the barriers
   size_t smem_bytes;
 };
 cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaPlan& plan, int* err,
