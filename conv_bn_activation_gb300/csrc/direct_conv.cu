@@ -289,7 +289,9 @@ namespace {
 
 template <int S, int KS, int COB, int CI>
 cudaError_t launch_tile(const DirectArgs& a, int vec_out, int sms, cudaStream_t s) {
-  constexpr int PX = 2;
+  // output rows per thread: 4 for the 8 -> (at most) 8 channel 3x3 stride-1
+  // layer (each staged weight float4 then feeds more FMAs), else 2
+  constexpr int PX = (S == 1 && KS == 3 && CI == 8 && COB == 8) ? 4 : 2;
   const int co_pad = (a.Co + COB - 1) / COB * COB;
   // Tile height: the tallest (up to 8 row groups of PX rows, 256 threads)
   // whose two staged tiles and weights fit in 100 KB (two CTAs per SM), else

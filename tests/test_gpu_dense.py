@@ -25,6 +25,8 @@ DENSE = [
     (2, 17, 13, 8, 8, 3, 1), (2, 16, 16, 8, 16, 3, 2), (2, 11, 9, 16, 8, 1, 1), (1, 12, 12, 12, 20, 3, 1),
     (2, 10, 10, 4, 16, 3, 1), (1, 9, 9, 24, 32, 1, 2), (1, 40, 40, 16, 16, 1, 1),
     (2, 9, 11, 8, 24, 1, 1), (1, 7, 9, 12, 16, 1, 1), (2, 33, 35, 3, 16, 3, 2), (1, 21, 19, 16, 40, 3, 1),
+    # 8 -> <= 8 channel 3x3 stride 1 (four output rows per thread): ragged tile rows and columns
+    (1, 37, 70, 8, 8, 3, 1), (2, 9, 33, 8, 4, 3, 1),
 ]
 
 
