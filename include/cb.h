@@ -136,9 +136,12 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
  * and Ci >= 16 (3x3) or Ci >= 8 (1x1) run as an implicit GEMM on the tcgen05
  * tensor cores (TF32 inputs, fp32 accumulate, outputs rounded to the nearest
  * TF32 value; needs 16-byte aligned x/w and strides that are multiples of 4
- * elements).  Among those, 3x3 stride-1 pad-1 layers with Ci % 16 == 0 and
- * W <= 254 take one shared-memory halo tile per 32- (or 16-) channel chunk
- * for all nine taps; the others gather one tile per tap.  1x1 stride-1
+ * elements).  Among those, 3x3 pad-1 layers take one shared-memory halo
+ * tile per 32-, 16- or 8-channel chunk for all nine taps: at stride 1 with
+ * Ci % 8 == 0, at stride 2 with Ci % 16 == 0 (four phase tiles of the
+ * input's even and odd rows and columns); images wider than one copy box
+ * are cut into column blocks.  The other tensor-core layers gather one tile
+ * per tap.  1x1 stride-1
  * layers with Ci and Co in {4, 8, 16, 32} run instead on a streaming fp32
  * CUDA-core kernel (HBM-bound at these widths);
  * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;
