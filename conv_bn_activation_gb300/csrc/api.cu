@@ -409,7 +409,8 @@ struct HaloPlan {
   int kc = 32;         // input channels per chunk (32, or 16 for Ci % 32 == 16 and for stride 2)
   int stride = 1;      // 2: four phase tiles per chunk
   int blk_w = 0, n_blk = 1, wp = 0;  // column blocks and the padded width of the pixel numbering
-  int sub = 1;         // 128-pixel sub-tiles per tile sharing one halo copy
+  int sub = 1;
+  bool resident = false;  // weights loaded once per CTA (one chunk, one channel tile)         // 128-pixel sub-tiles per tile sharing one halo copy
   size_t smem = 0;
   double cost = 0;     // the cost model's cycles per CTA
 };
@@ -423,6 +424,7 @@ struct HaloForce {
   int co = 0;
   bool cm = false;
   int nb = 0, split = 0, tps = 0, sub = 0;
+  int res = -1;  // resident weights: -1 the model's choice, 0 off, 1 on
 };
 HaloForce halo_force_env();
 bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, const HaloForce& f, HaloPlan* out);
@@ -654,14 +656,14 @@ bool halo_ring(int co, int hb, int force_nb, int force_tps, int* nb_out, int* tp
 }
 
 HaloForce halo_force_env() {
-  // CB_HALO_FORCE = "cm[,stages[,split[,taps]]]" or "co[,stages[,split[,taps[,subtiles]]]]", read per call
+  // CB_HALO_FORCE = "cm[,stages[,split[,taps]]]" or "co[,stages[,split[,taps[,subtiles[,resident]]]]]", read per call
   HaloForce f;
   if (const char* e = std::getenv("CB_HALO_FORCE")) {
     if (e[0] == 'c' && e[1] == 'm') {
       f.cm = true;
       if (e[2] == ',') std::sscanf(e + 3, "%d,%d,%d", &f.nb, &f.split, &f.tps);
     } else {
-      std::sscanf(e, "%d,%d,%d,%d,%d", &f.co, &f.nb, &f.split, &f.tps, &f.sub);
+      std::sscanf(e, "%d,%d,%d,%d,%d,%d", &f.co, &f.nb, &f.split, &f.tps, &f.sub, &f.res);
     }
   }
   return f;
@@ -705,7 +707,14 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
         if (rows * stride > 256) continue;
         const int hb = halo_buffer_bytes(wp, sh.px * sub, kc, stride);
         int nb = 0, tps = 1;
-        if (!halo_ring(sh.co, hb, f.nb, f.tps, &nb, &tps, kc)) continue;
+        // Resident weights: a layer of one channel chunk and one channel tile
+        // may keep its nine taps in a single stage, copied once per CTA; each
+        // tile then costs its MMAs (one stage) against its halo copy alone.
+        const bool res_ok = num_kc == 1 && Co <= sh.co && f.res != 0 && (f.split == 0 || f.split == 1) &&
+                            (f.tps == 0 || f.tps == 9) && (f.nb == 0 || f.nb == 1) &&
+                            halo_smem_bytes(sh.co, hb, 1, 9, kc) <= kSmemMax;
+        const bool ring_ok = f.res != 1 && halo_ring(sh.co, hb, f.nb, f.tps, &nb, &tps, kc);
+        if (!ring_ok && !res_ok) continue;
         const long long px_tiles = (static_cast<long long>(OH) * wp + sh.px - 1) / sh.px;
         const long long m_tiles = static_cast<long long>(N) * n_blk * ((px_tiles + sub - 1) / sub);
         const long long tiles = m_tiles * ((Co + sh.co - 1) / sh.co);
@@ -730,7 +739,34 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
         const double epi = 0.444 * sh.px * sh.co;
         const double epi_tile = 0.374 * sub * sh.px * sh.co;
         const size_t smem = halo_smem_bytes(sh.co, hb, nb, tps, kc);
-        for (int split = 1; split <= 2; ++split) {
+        if (res_ok) {
+          const size_t smem_r = halo_smem_bytes(sh.co, hb, 1, 9, kc);
+          {
+            const double mma_r = sub * 9.0 * (kc / 8) * 64.0 * std::max(1.0, n / 128.0) + 204.0;
+            double cost = static_cast<double>(per_cta) * std::max(std::max(mma_r, hcopy) + 3546.0, epi_tile) + epi;
+            cost *= 1.0 + 0.02 * (n_blk - min_blocks);
+            if (cost < best * 0.97) {
+              best = cost;
+              plan.px = sh.px;
+              plan.co = sh.co;
+              plan.cm = sh.cm;
+              plan.nb = 1;
+              plan.tps = 9;
+              plan.kc = kc;
+              plan.stride = stride;
+              plan.blk_w = blk_w;
+              plan.n_blk = n_blk;
+              plan.wp = wp;
+              plan.sub = sub;
+              plan.split = 1;
+              plan.resident = true;
+              plan.grid = static_cast<int>(grid);
+              plan.smem = smem_r;
+              plan.cost = cost;
+            }
+          }
+        }
+        for (int split = 1; ring_ok && split <= 2; ++split) {
           if (f.split && split != f.split) continue;
           double cost;
           if (split == 1) {
@@ -760,6 +796,7 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
             plan.n_blk = n_blk;
             plan.wp = wp;
             plan.sub = sub;
+            plan.resident = false;
             plan.split = split;
             plan.grid = static_cast<int>(split == 2 ? 2 * tiles : grid);
             plan.smem = smem;
@@ -875,6 +912,7 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   a.phase_bytes = plan.stride == 2 ? a.halo_bytes / 4 : 0;
   a.nb_stages = plan.nb;
   a.taps_per_stage = plan.tps;
+  a.w_resident = plan.resident ? 1 : 0;
   a.split_k = plan.split;
   a.out = make_out(y);
   a.ep = ep;
@@ -892,9 +930,10 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   if (std::getenv("CB_DEBUG_PLAN"))
     std::fprintf(stderr,
                  "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d s=%d -> %s px=%dx%d co=%d kc=%d nb=%d tps=%d "
-                 "split=%d blocks=%dx%d rows=%d halo=%d tiles=%d grid=%d smem=%zu\n",
+                 "split=%d%s blocks=%dx%d rows=%d halo=%d tiles=%d grid=%d smem=%zu\n",
                  x->n, a.H, a.W, Ci, Co, plan.stride, plan.cm ? "channel-major" : "pixel-major", plan.sub, plan.px,
-                 plan.co, plan.kc, plan.nb, plan.tps, plan.split, plan.n_blk, plan.blk_w, a.rows, a.halo_bytes,
+                 plan.co, plan.kc, plan.nb, plan.tps, plan.split, plan.resident ? " resident" : "", plan.n_blk, plan.blk_w,
+                 a.rows, a.halo_bytes,
                  a.m_tiles * a.n_tiles, plan.grid, plan.smem);
   CUtensorMap xmap, wmap;
   {
@@ -1184,11 +1223,25 @@ std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int 
           f.tps = tps;
           f.split = split;
           f.sub = sb;
+          f.res = 0;
           ConvPlan p;
           if (!plan_halo(x, y, stride, sms, f, &p.halo)) continue;
           p.path = p.halo.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
           out.push_back(p);
         }
+      // resident weights (one chunk, one channel tile)
+      for (int sb : {1, 2, 4}) {
+        if (sb > 1 && (sh.cm || sh.co > 64)) continue;
+        HaloForce f;
+        f.co = sh.cm ? 0 : sh.co;
+        f.cm = sh.cm;
+        f.sub = sb;
+        f.res = 1;
+        ConvPlan p;
+        if (!plan_halo(x, y, stride, sms, f, &p.halo)) continue;
+        p.path = p.halo.cm ? CB_PATH_TC_HALO_CM : CB_PATH_TC_HALO;
+        out.push_back(p);
+      }
     }
   }
   for (int bn : {16, 32, 48, 64, 96, 128, 192, 256}) {

@@ -99,11 +99,14 @@ cudaError_t launch_igemm_halo_kc8(const CUtensorMap& xmap, const CUtensorMap& wm
 
 cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
                               bool cm, int grid, size_t smem, cudaStream_t s) {
-  if (a.nb_stages < 2 || a.nb_stages > 16) return cudaErrorInvalidValue;
+  if (a.nb_stages < (a.w_resident ? 1 : 2) || a.nb_stages > 16) return cudaErrorInvalidValue;
   if (a.taps_per_stage != 1 && a.taps_per_stage != 3 && a.taps_per_stage != 9) return cudaErrorInvalidValue;
   if (a.split_k != 1 && a.split_k != 2) return cudaErrorInvalidValue;
   if (a.stride != 1 && a.stride != 2) return cudaErrorInvalidValue;
   if (a.sub < 1 || a.sub > kHaloMaxSub || (a.sub > 1 && (cm || co > 64 || a.split_k != 1))) return cudaErrorInvalidValue;
+  if (a.w_resident &&
+      (a.num_kc != 1 || a.n_tiles != 1 || a.split_k != 1 || a.taps_per_stage != 9 || a.nb_stages != 1))
+    return cudaErrorInvalidValue;
   if (a.stride == 2 && (a.kc != 16 || a.phase_bytes * 4 != a.halo_bytes || a.Wp * 2 > 256 || a.rows * 2 > 256))
     return cudaErrorInvalidValue;
   if (a.split_k == 2) {

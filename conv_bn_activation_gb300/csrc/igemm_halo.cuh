@@ -167,6 +167,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   const Watchdog wd{a.err, abort_flag, a.timeout_ns};
   const int num_tiles = a.m_tiles * a.n_tiles;
   const uint32_t halo_tx = static_cast<uint32_t>(kRowBytes * a.Wp * a.rows * (a.stride == 2 ? 4 : 1));
+  // resident weights: the layer's whole weight tensor is one stage of nine
+  // taps (one channel chunk, one channel tile), copied once per CTA
+  const bool resident = a.w_resident != 0;
   const bool tr_cta = a.trace && blockIdx.x == a.trace_cta;
 
   if (warp == 0) {
@@ -211,6 +214,16 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
             hphase ^= 1u;
           }
           for (int tap = 0; tap < 9; tap += tps) {
+            if (resident) {
+              // one chunk, one channel tile: every tile takes the same nine
+              // taps, loaded once into the single stage and kept
+              if (lane == 1 && tile == tile0) {
+                mbar_arrive_expect_tx(&bfull[0], static_cast<uint32_t>(kBBytes));
+                tma_load_3d(sB, &wmap, &bfull[0], kc * KC, n_tile * CO, 0);
+                issued |= 1u;
+              }
+              continue;
+            }
             if (lane != 0 && s % kBLanes == lane - 1) {
               if (!mbar_wait(&bempty[s], bphase ^ 1u, wd)) {
                 ok = false;
@@ -272,6 +285,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
       auto make_desc = [&](uint32_t lo) { return (static_cast<uint64_t>(desc_hi) << 32) | lo; };
       // One K chunk of a tile: 9 taps x NSUB sub-tiles x KC / 8 MMAs, weight
       // stages of TPS taps.  Returns false when a wait timed out.
+      bool w_ready = false;  // resident weights: landed (waited for once)
       auto issue_chunk = [&](auto tps_c, auto nsub_c, uint32_t x_lo, const uint32_t (&d_tmem)[kHaloMaxSub],
                              bool first) -> bool {
         constexpr int TPS = decltype(tps_c)::value, NSUB = decltype(nsub_c)::value;
@@ -279,9 +293,12 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
 #pragma unroll
         for (int tap = 0; tap < 9; ++tap) {
           if (tap % TPS == 0) {
-            if (!mbar_wait(&bfull[s], bphase, wd)) return false;
-            tr.add(tr_cta);
-            tc_fence_after_sync();
+            if (!w_ready) {
+              if (!mbar_wait(&bfull[s], bphase, wd)) return false;
+              tr.add(tr_cta);
+              tc_fence_after_sync();
+              w_ready = resident;
+            }
             w_lo = desc_lo(smem_u32(sB + s * kBBytes));
           }
           const uint32_t xt = x_lo + tap_off[tap], wt = w_lo + (tap % TPS) * kTapOff;
@@ -293,7 +310,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
               mma_tf32(d_tmem[i], CM ? wdsc : xd, CM ? xd : wdsc, kIdesc, (tap == 0 && kk == 0 && first) ? 0u : 1u);
             }
           }
-          if (tap % TPS == TPS - 1) {
+          if (tap % TPS == TPS - 1 && !resident) {
             mma_commit(&bempty[s]);
             tr.add(tr_cta);
             const uint32_t bit = 1u << s;

@@ -128,6 +128,7 @@ struct HaloArgs {
   int halo_bytes;      // shared-memory bytes of one halo buffer (multiple of 1024)
   int nb_stages;       // weight-slice ring depth
   int taps_per_stage;  // filter taps per weight-ring stage (1, 3 or 9): one copy each
+  int w_resident;      // 1: one chunk and one channel tile; the nine taps stay in the single stage
   int split_k;         // 1, or 2: clusters of two CTAs split each tile's chunks (one tile per cluster)
   int vec_store;       // 1 when y / r rows allow 16-byte vector access
   OutView out;

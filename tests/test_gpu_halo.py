@@ -379,3 +379,36 @@ def test_halo_sub_tiles_epilogues_and_views(gpu, orc, halo_force, act, res_mode)
     ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=act, residual=r, res_mode=res_mode)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
     assert is_canary(buf[:, :, W:, :]) and is_canary(buf[:, :, :W, :4]) and is_canary(buf[:, :, :W, 4 + Co:])
+
+
+RES_CASES = [
+    # N, H, W, Cin, Cout, stride, CB_HALO_FORCE with resident weights: one channel chunk and one
+    # channel tile, the nine taps copied once per CTA; sub-tiles, column blocks, stride 2, a ragged
+    # channel tile, more tiles than CTAs
+    (2, 20, 20, 16, 32, 1, "32,0,0,0,1,1"), (2, 21, 17, 32, 32, 1, "32,0,0,0,2,1"),
+    (2, 40, 40, 16, 32, 2, "32,0,0,0,2,1"), (1, 7, 300, 16, 16, 1, "32,0,0,0,4,1"),
+    (2, 12, 12, 32, 64, 1, "64,0,0,0,1,1"), (1, 9, 11, 32, 24, 1, "32,0,0,0,1,1"),
+    (16, 40, 40, 32, 32, 1, "32,0,0,0,2,1"), (1, 21, 23, 16, 64, 2, "64,0,0,0,1,1"),
+]
+
+
+@pytest.mark.parametrize("case", RES_CASES, ids=lambda s: "x".join(map(str, s[:6])) + "-" + s[6])
+def test_halo_resident_weights(gpu, orc, halo_force, case):
+    N, H, W, Ci, Co, st, force = case
+    halo_force(force)
+    x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=sum(case[:6]) + 33)
+    xd = to_dev(x)
+    OH, OW = (H - 1) // st + 1, (W - 1) // st + 1
+    assert cb.conv_path(xd, torch.empty(N, OH, OW, Co, device="cuda"), 3, st, 1) in (cb.PATH_TC_HALO,)
+    y = _run(x, w, bn) if st == 1 else _run_s(x, w, bn, 2)
+    ref = orc.conv_bn_act(x, w, bn, stride=st, pad=1, act=orc.ACT_SILU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+
+
+def test_halo_resident_weights_not_taken_for_several_chunks(gpu, halo_force):
+    """Resident weights need one channel chunk and one channel tile: a forced request with 64 input
+    channels (two 32-channel chunks) finds no plan, so the layer leaves the halo kernels."""
+    halo_force("32,0,0,0,1,1")
+    x = torch.empty(1, 10, 10, 64, device="cuda")
+    y = torch.empty(1, 10, 10, 32, device="cuda")
+    assert cb.conv_path(x, y, 3, 1, 1) not in (cb.PATH_TC_HALO, cb.PATH_TC_HALO_CM)
