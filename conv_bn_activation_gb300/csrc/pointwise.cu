@@ -61,7 +61,7 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 constexpr int kPwThreads = 256;
-constexpr int kPwU = 4;       // pixels per thread (register blocking)
+constexpr int kPwU = 4;       // pixels per thread at most (register blocking)
 constexpr int kPwStages = 3;  // tiles in flight per CTA (ring depth)
 
 template <int CI, int CO, typename T>
@@ -71,7 +71,10 @@ struct PwShape {
   static constexpr int kVec = CI / kEpp;                          // 16-byte input pieces per pixel
   static constexpr int kPitch = kVec >= 4 ? kVec + 1 : kVec;      // staged input row, 16-byte units (padded)
   static constexpr int kTile = 4096 / CI;  // pixels per tile (16 KB of fp32 input, 8 KB of bf16)
-  static constexpr int kGroups = kTile / kPwU;                    // pixel groups per tile
+  // pixels per thread: 4, fewer when a tile has too few (pixel group,
+  // channel group) items to give every thread one (narrow outputs)
+  static constexpr int kU = kTile * G / kPwThreads >= kPwU ? kPwU : (kTile * G / kPwThreads >= 2 ? 2 : 1);
+  static constexpr int kGroups = kTile / kU;                      // pixel groups per tile
   static constexpr int kItems = kGroups * G;                      // (pixel group, channel group) items
   static constexpr int kXFloat4 = kTile * kPitch;
   static size_t smem_bytes() {
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
   static_assert(CI % 4 == 0 && CO % 4 == 0 && CI <= 32 && CO <= 32, "channel counts");
   using Sh = PwShape<CI, CO, T>;
   constexpr int G = Sh::G, kVec = Sh::kVec, kPitch = Sh::kPitch, kEpp = Sh::kEpp;
-  constexpr int kTile = Sh::kTile, kGroups = Sh::kGroups, kItems = Sh::kItems;
+  constexpr int kTile = Sh::kTile, kGroups = Sh::kGroups, kItems = Sh::kItems, kU = Sh::kU;
   constexpr int kPieces = kTile * kVec / kPwThreads;  // 16-byte copies per thread per tile
   static_assert(kVec >= 1 && kPieces * kPwThreads == kTile * kVec && kPwThreads % G == 0, "tile shape");
   extern __shared__ float4 pw_smem[];
@@ -163,28 +166,28 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
       const int pg = item / G, g = item - (item / G) * G;  // pixels pg + u * kGroups
       // the residual's four pixels, in flight during the FMAs (a plain load:
       // the residual may be y itself, each element read before it is written)
-      float4 rv[kPwU];
+      float4 rv[kU];
 #pragma unroll
-      for (int u = 0; u < kPwU; ++u) {
+      for (int u = 0; u < kU; ++u) {
         const long long p = tile * kTile + pg + u * kGroups;
         rv[u] = (res && p < M) ? load4(reinterpret_cast<const T*>(a.ep.r) +
                                        pixel_off(p, a.ep.rs_n, a.ep.rs_h, a.ep.rs_w) + 4 * g)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      float4 acc[kPwU];
+      float4 acc[kU];
 #pragma unroll
-      for (int u = 0; u < kPwU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int c4 = 0; c4 < CI / 4; ++c4) {
-        float4 xv[kPwU];
+        float4 xv[kU];
 #pragma unroll
-        for (int u = 0; u < kPwU; ++u)
+        for (int u = 0; u < kU; ++u)
           xv[u] = load4(reinterpret_cast<const T*>(xs + (pg + u * kGroups) * kPitch) + 4 * c4);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float4 w4 = ws[(4 * c4 + e) * G + g];
 #pragma unroll
-          for (int u = 0; u < kPwU; ++u) {
+          for (int u = 0; u < kU; ++u) {
             const float xsv = comp(xv[u], e);
             acc[u].x = fmaf(xsv, w4.x, acc[u].x);
             acc[u].y = fmaf(xsv, w4.y, acc[u].y);
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
       }
       const float4 sc = ssc[g], bi = sbi[g];
 #pragma unroll
-      for (int u = 0; u < kPwU; ++u) {
+      for (int u = 0; u < kU; ++u) {
         const int lp = pg + u * kGroups;
         const long long p = tile * kTile + lp;
         if (p >= M) continue;
