@@ -70,7 +70,15 @@ struct PwShape {
   static constexpr int kEpp = 16 / static_cast<int>(sizeof(T));   // elements per 16-byte piece
   static constexpr int kVec = CI / kEpp;                          // 16-byte input pieces per pixel
   static constexpr int kPitch = kVec >= 4 ? kVec + 1 : kVec;      // staged input row, 16-byte units (padded)
-  static constexpr int kTile = 4096 / CI;  // pixels per tile (16 KB of fp32 input, 8 KB of bf16)
+  // pixels per tile: 16 KB of fp32 input (8 KB of bf16), or up to twice that
+  // when narrow outputs would otherwise leave threads without 4 pixels' work
+  // and the three-tile ring stays within 112 KB (two CTAs per SM; measured:
+  // 32 -> 16 at 160x160 42.4 -> 37.5 us, while 16 -> 8, whose ring would
+  // grow to 120 KB and one CTA per SM, went from 57.5 to 71.2 us)
+  static constexpr int kTile0 = 4096 / CI;
+  static constexpr int kTileBig = 1024 / G < 2 * kTile0 ? 1024 / G : 2 * kTile0;
+  static constexpr int kTile =
+      kTile0 < 1024 / G && kPwStages * kTileBig * kPitch * 16 <= 112 * 1024 ? kTileBig : kTile0;
   // pixels per thread: 4, fewer when a tile has too few (pixel group,
   // channel group) items to give every thread one (narrow outputs)
   static constexpr int kU = kTile * G / kPwThreads >= kPwU ? kPwU : (kTile * G / kPwThreads >= 2 ? 2 : 1);
@@ -83,7 +91,7 @@ struct PwShape {
 };
 
 // A ring of kPwStages tiles per CTA: a tile is kTile pixels whose CI inputs
-// are 16 KB (8 KB in bf16), copied
+// are 16 or 32 KB (half that in bf16), copied
 // with 16-byte cp.async by all threads (different bytes per thread).  The
 // staged rows of 64 bytes or more are padded by 16 bytes so that the
 // pixel-strided reads below hit distinct bank groups.  Each thread computes
