@@ -90,6 +90,21 @@ def test_depthwise_intensity_range():
     assert dw["s1"].bytes - 2 * 64 * 56 * 56 * 384 * 4 == 384 * 9 * 4 + 2 * 384 * 4
 
 
+def test_bf16_storage_byte_ledger():
+    """bf16 storage halves the activation bytes of a layer (input, output, residual) and leaves
+    the fp32 weights, scale and bias; the FLOPs do not change."""
+    f32, b16 = workloads.depthwise_workload(), workloads.depthwise_workload(act_bytes=2)
+    for k in ("s1", "s2"):
+        params = 384 * 9 * 4 + 2 * 384 * 4
+        assert b16[k].flops == f32[k].flops
+        assert b16[k].bytes - params == (f32[k].bytes - params) // 2
+    assert b16["s1"].bytes == 308298240  # the bench's algorithmic bytes for the bf16 stride-1 launch
+    pw32 = workloads.conv_layer(32, 320, 320, 16, 16, 1, 1, 0, residual=True)
+    pw16 = workloads.conv_layer(32, 320, 320, 16, 16, 1, 1, 0, residual=True, act_bytes=2)
+    params = 16 * 16 * 4 + 2 * 16 * 4
+    assert pw16.bytes - params == (pw32.bytes - params) // 2 == 3 * 32 * 320 * 320 * 16 * 2
+
+
 def _torch_stage(x, st):
     x1 = F.silu(_bn(F.conv2d(x, _t(st["down_w"]), stride=2, padding=1), st["down_bn"]))
     a = F.silu(_bn(F.conv2d(x1, _t(st["cv1_w"])), st["cv1_bn"]))
