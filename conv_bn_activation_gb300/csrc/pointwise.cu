@@ -196,11 +196,13 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
           const float4 w4 = ws[(4 * c4 + e) * G + g];
 #pragma unroll
           for (int u = 0; u < kU; ++u) {
+            // channel pairs through packed FMAs (each lane one fmaf; measured
+            // 2-30 % faster here, most with bf16 storage)
             const float xsv = comp(xv[u], e);
-            acc[u].x = fmaf(xsv, w4.x, acc[u].x);
-            acc[u].y = fmaf(xsv, w4.y, acc[u].y);
-            acc[u].z = fmaf(xsv, w4.z, acc[u].z);
-            acc[u].w = fmaf(xsv, w4.w, acc[u].w);
+            const float2 xx = make_float2(xsv, xsv);
+            const float2 lo = __ffma2_rn(xx, make_float2(w4.x, w4.y), make_float2(acc[u].x, acc[u].y));
+            const float2 hi = __ffma2_rn(xx, make_float2(w4.z, w4.w), make_float2(acc[u].z, acc[u].w));
+            acc[u] = make_float4(lo.x, lo.y, hi.x, hi.y);
           }
         }
       }
