@@ -51,6 +51,17 @@ __device__ __forceinline__ float tc_epi_t(float acc, float sc, float bi, float r
   return round_tf32(z);
 }
 
+// The epilogue after the folded BN (scale and bias applied by the caller,
+// two channels per packed FMA).
+template <int ACT, int RES>
+__device__ __forceinline__ float tc_epi_post(float z, float r) {
+  if constexpr (RES == 1) z += r;
+  if constexpr (ACT == 1) z = fmaxf(z, 0.0f);
+  if constexpr (ACT == 2) z = __fdividef(z, 1.0f + __expf(-z));
+  if constexpr (RES == 2) z += r;
+  return round_tf32(z);
+}
+
 // 32 lanes x 32 bits, 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
   __syncwarp();
@@ -229,7 +240,13 @@ struct TileStore {
 #pragma unroll
     for (int pass = 0; pass < kLpp; ++pass)
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) z[pass][jj] = tc_epi_t<ACT, RES>(z[pass][jj], k.sc[jj], k.bi[jj], r[pass][jj]);
+      for (int jj = 0; jj < 4; jj += 2) {
+        // scale and bias of two channels in one packed FMA (each lane one fmaf)
+        const float2 a = __ffma2_rn(make_float2(z[pass][jj], z[pass][jj + 1]), make_float2(k.sc[jj], k.sc[jj + 1]),
+                                    make_float2(k.bi[jj], k.bi[jj + 1]));
+        z[pass][jj] = tc_epi_post<ACT, RES>(a.x, r[pass][jj]);
+        z[pass][jj + 1] = tc_epi_post<ACT, RES>(a.y, r[pass][jj + 1]);
+      }
 #pragma unroll
     for (int pass = 0; pass < kLpp; ++pass) {
       if (yo[pass] < 0 || !k.cin) continue;
