@@ -202,7 +202,9 @@ def conv_bn_act(x, w, scale, bias, k, stride, pad, groups, act, y, residual=None
                 stream=None, x_layout=LAYOUT_NHWC):
     """cb_conv_bn_act on torch CUDA tensors.  x: [N,H,W,C] (or [N,C,H,W] with
     x_layout=LAYOUT_NCHW); y, residual: [N,OH,OW,Co] views; w, scale, bias:
-    device tensors in the cb_repack_weights / cb_fold_bn layouts."""
+    device tensors in the cb_repack_weights / cb_fold_bn layouts.  x, y and
+    residual are float32, or all bfloat16 for the layers that take bf16
+    storage (depthwise 3x3, narrow 1x1); weights, scale and bias stay float32."""
     xv = nchw(x) if x_layout == LAYOUT_NCHW else nhwc(x)
     yv = nhwc(y)
     rv = nhwc(residual) if residual is not None else None
