@@ -31,6 +31,7 @@ EXPORTED = (
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_layer_uses_tensor_cores",
     "cb_dw_separable_block_static", "cb_conv_path", "cb_debug_timeout_probe", "cb_autotune_conv",
     "cb_autotune_clear", "cb_autotune_entries", "cb_preprocess_stem_u8", "cb_dw_separable_block_fused",
+    "cb_set_tuning", "cb_last_launch",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
@@ -43,6 +44,11 @@ class CbTensor(ctypes.Structure):
         ("stride_w", ctypes.c_longlong), ("stride_c", ctypes.c_longlong),
         ("layout", ctypes.c_int), ("dtype", ctypes.c_int),
     ]
+
+
+class CbLaunchInfo(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
+                ("cluster", ctypes.c_int), ("blocks_per_sm", ctypes.c_int)]
 
 
 class CbError(RuntimeError):
@@ -89,6 +95,8 @@ def load():
                 "cb_preprocess_stem_u8": [P, I, I, I, LL, I, I, P, P, P, I, T, P],
                 "cb_dw_separable_block_fused": [T, T, P, P],
                 "cb_autotune_entries": [],
+                "cb_set_tuning": [ctypes.c_char_p, ctypes.c_char_p],
+                "cb_last_launch": [ctypes.POINTER(CbLaunchInfo)],
                 "cb_status_string": [I],
                 "cb_version": [],
             }
@@ -171,6 +179,34 @@ def set_kernel_policy(policy: int):
 
 def get_kernel_policy() -> int:
     return load().cb_get_kernel_policy()
+
+
+def set_tuning(name: str, value=None):
+    """cb_set_tuning: set a plan override (CB_HALO_FORCE, CB_IGEMM_FORCE, ...); None restores the default."""
+    _check(load().cb_set_tuning(name.encode(), None if value is None else str(value).encode()), "cb_set_tuning")
+
+
+class tuning:
+    """Context manager: a plan override for the calls inside the block, restored to the default on exit."""
+
+    def __init__(self, name: str, value):
+        self.name, self.value = name, value
+
+    def __enter__(self):
+        set_tuning(self.name, self.value)
+        return self
+
+    def __exit__(self, *exc):
+        set_tuning(self.name, None)
+        return False
+
+
+def last_launch() -> dict:
+    """cb_last_launch: launch configuration and occupancy (CTAs per SM) of this thread's last kernel."""
+    info = CbLaunchInfo()
+    _check(load().cb_last_launch(ctypes.byref(info)), "cb_last_launch")
+    return {"grid": info.grid, "threads": info.threads, "smem_bytes": int(info.smem_bytes), "cluster": info.cluster,
+            "blocks_per_sm": info.blocks_per_sm}
 
 
 def round_weights_tf32(w):

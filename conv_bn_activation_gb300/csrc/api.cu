@@ -18,6 +18,7 @@
 
 #include "cb.h"
 #include "internal.h"
+#include "launch_util.h"
 
 namespace cb {
 int dw_tma_blocks_per_sm(int stride, int threads, size_t smem, bool bf16);
@@ -275,6 +276,92 @@ bool tc_channels_ok(int ci, int k, int stride) {
   return k == 1 ? ci >= 8 : ci >= 16;
 }
 
+// ----------------------------------------------------------- tuning overrides
+// Constraints on a halo plan (0 / false = free): tile shape, ring depth,
+// split K, taps per weight stage.
+struct HaloForce {
+  int co = 0;
+  bool cm = false;
+  int nb = 0, split = 0, tps = 0, sub = 0;
+  int res = -1;  // resident weights: -1 the model's choice, 0 off, 1 on
+};
+
+// Plan overrides and profiling aids (none is needed for normal use).  Each
+// starts from the environment variable of the same name, read once per
+// process on first use; afterwards only cb_set_tuning changes it.  The hot
+// path never calls getenv, and a test can switch plans without writing to
+// the environment of a live process.
+struct Tuning {
+  int dw_force[3] = {0, 0, 0};     // CB_DW_FORCE = "rows,tile_w,ctas_per_sm" (0 = free)
+  int igemm_force[3] = {0, 0, 0};  // CB_IGEMM_FORCE = "bn,stages,grid"
+  int igemm_blocks = -1;           // CB_IGEMM_BLOCKS = 0 / 1 (-1: the planner's choice)
+  HaloForce halo;                  // CB_HALO_FORCE = "cm[,stages[,split[,taps]]]" or
+                                   //   "co[,stages[,split[,taps[,subtiles[,resident]]]]]"
+  int dw_block = -1;               // CB_DW_BLOCK_FORCE = 0 / 1 (-1: the shape rule)
+  bool debug_plan = false;         // CB_DEBUG_PLAN: print each plan to stderr
+  int trace_cta = -1;              // CB_IGEMM_TRACE = cta (trace builds: timeline of one CTA)
+  int span_slot = 1;               // CB_SPAN_SLOT = 1 / 2 (trace builds)
+};
+
+const char* const kTuningNames[] = {"CB_DW_FORCE",       "CB_IGEMM_FORCE", "CB_IGEMM_BLOCKS", "CB_HALO_FORCE",
+                                    "CB_DW_BLOCK_FORCE", "CB_DEBUG_PLAN",  "CB_IGEMM_TRACE",  "CB_SPAN_SLOT"};
+
+// Sets knob `name` of *t from `v` (NULL or "" restores the knob's default);
+// false for an unknown name.
+bool parse_tuning(Tuning* t, const char* name, const char* v) {
+  const Tuning d;
+  const bool unset = v == nullptr || v[0] == '\0';
+  if (!std::strcmp(name, "CB_DW_FORCE")) {
+    std::memcpy(t->dw_force, d.dw_force, sizeof(d.dw_force));
+    if (!unset) std::sscanf(v, "%d,%d,%d", &t->dw_force[0], &t->dw_force[1], &t->dw_force[2]);
+  } else if (!std::strcmp(name, "CB_IGEMM_FORCE")) {
+    std::memcpy(t->igemm_force, d.igemm_force, sizeof(d.igemm_force));
+    if (!unset) std::sscanf(v, "%d,%d,%d", &t->igemm_force[0], &t->igemm_force[1], &t->igemm_force[2]);
+  } else if (!std::strcmp(name, "CB_IGEMM_BLOCKS")) {
+    t->igemm_blocks = unset ? d.igemm_blocks : (v[0] == '1' ? 1 : 0);
+  } else if (!std::strcmp(name, "CB_HALO_FORCE")) {
+    HaloForce f;
+    if (!unset) {
+      if (v[0] == 'c' && v[1] == 'm') {
+        f.cm = true;
+        if (v[2] == ',') std::sscanf(v + 3, "%d,%d,%d", &f.nb, &f.split, &f.tps);
+      } else {
+        std::sscanf(v, "%d,%d,%d,%d,%d,%d", &f.co, &f.nb, &f.split, &f.tps, &f.sub, &f.res);
+      }
+    }
+    t->halo = f;
+  } else if (!std::strcmp(name, "CB_DW_BLOCK_FORCE")) {
+    t->dw_block = unset ? d.dw_block : (v[0] == '1' ? 1 : 0);
+  } else if (!std::strcmp(name, "CB_DEBUG_PLAN")) {
+    t->debug_plan = !unset;
+  } else if (!std::strcmp(name, "CB_IGEMM_TRACE")) {
+    t->trace_cta = unset ? d.trace_cta : std::atoi(v);
+  } else if (!std::strcmp(name, "CB_SPAN_SLOT")) {
+    t->span_slot = unset ? d.span_slot : (std::atoi(v) == 2 ? 2 : 1);
+  } else {
+    return false;
+  }
+  return true;
+}
+
+std::mutex g_tuning_mu;
+Tuning* g_tuning = nullptr;  // guarded by g_tuning_mu; created from the environment on first use
+
+Tuning& tuning_locked() {
+  if (!g_tuning) {
+    static Tuning t;
+    for (const char* n : kTuningNames) parse_tuning(&t, n, std::getenv(n));
+    g_tuning = &t;
+  }
+  return *g_tuning;
+}
+
+// A copy of the current overrides (a few dozen bytes under an uncontended lock).
+Tuning tuning() {
+  std::lock_guard<std::mutex> lock(g_tuning_mu);
+  return tuning_locked();
+}
+
 // ----------------------------------------------------------------- depthwise
 cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, int stride, int pad,
                         const cb_tensor* y, cudaStream_t s) {
@@ -331,9 +418,9 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
   const int cols = a.bf16 && stride == 1 ? 4 : 2;  // output columns per consumer thread (the kernel's rule)
   const int max_tile = a.bf16 && stride == 2 ? 60 : 120;  // at most 480 consumer threads
   const int chunks = (a.C + ch - 1) / ch;
-  // Tuning override (CB_DW_FORCE="rows,tile_w,ctas_per_sm"; 0 = free), read per call.
-  int force_r = 0, force_tw = 0, force_cps = 0;
-  if (const char* f = std::getenv("CB_DW_FORCE")) std::sscanf(f, "%d,%d,%d", &force_r, &force_tw, &force_cps);
+  // Tuning override (CB_DW_FORCE="rows,tile_w,ctas_per_sm"; 0 = free).
+  const Tuning tu = tuning();
+  const int force_r = tu.dw_force[0], force_tw = tu.dw_force[1], force_cps = tu.dw_force[2];
   DwTmaPlan best{};
   {
     const int wt = (a.OW + max_tile - 1) / max_tile;
@@ -371,7 +458,7 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
       best.smem_bytes = static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t) + 16 + w_bytes;
     }
   }
-  if (std::getenv("CB_DEBUG_PLAN"))
+  if (tu.debug_plan)
     std::fprintf(stderr, "[cb] dw plan: N=%d H=%d W=%d C=%d s=%d -> rows=%d items=%d box_w=%d stages=%d grid=%d warps=%d smem=%zu\n",
                  a.N, a.H, a.W, a.C, stride, best.rows_per_item, best.num_items, best.box_w, best.stages, best.grid,
                  best.consumer_warps, best.smem_bytes);
@@ -418,15 +505,6 @@ struct ImPlan {        // im2col kernel choices (0 = the cost model's)
   int bn = 0, stages = 0;
   int blocks = 0;      // 1: 128 consecutive pixels (im2col copies); 2: pixel blocks (tiled copies)
 };
-// Constraints on a halo plan (0 / false = free): tile shape, ring depth,
-// split K, taps per weight stage.
-struct HaloForce {
-  int co = 0;
-  bool cm = false;
-  int nb = 0, split = 0, tps = 0, sub = 0;
-  int res = -1;  // resident weights: -1 the model's choice, 0 off, 1 on
-};
-HaloForce halo_force_env();
 bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, const HaloForce& f, HaloPlan* out);
 
 // ------------------------------------------------------------ autotuner
@@ -542,9 +620,10 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
   a.ep = ep;
   a.err = dev->err;
   a.timeout_ns = timeout_ns();
-  if (const char* t = std::getenv("CB_IGEMM_TRACE")) {  // profiling aid: timeline of one CTA
+  const Tuning tu = tuning();
+  if (tu.trace_cta >= 0) {  // profiling aid: timeline of one CTA
     a.trace = 1;
-    a.trace_cta = std::atoi(t);
+    a.trace_cta = tu.trace_cta;
   }
   a.vec_store = (aligned16(a.out.y) && strides_mult4(y) && aligned16(ep.scale) && aligned16(ep.bias) &&
                  (ep.res_mode == 0 || (aligned16(ep.r) && ep.rs_n % 4 == 0 && ep.rs_h % 4 == 0 && ep.rs_w % 4 == 0)))
@@ -554,8 +633,7 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
   int bn = pick_bn(a.M, Co, a.k_iters, dev->sms, &n_tiles);
   // Tuning override (a measured plan, else CB_IGEMM_FORCE="bn,stages,grid"; 0 = free).
   int force_bn = im.bn, force_stages = im.stages, force_grid = 0;
-  if (im.bn == 0)
-    if (const char* f = std::getenv("CB_IGEMM_FORCE")) std::sscanf(f, "%d,%d,%d", &force_bn, &force_stages, &force_grid);
+  if (im.bn == 0) force_bn = tu.igemm_force[0], force_stages = tu.igemm_force[1], force_grid = tu.igemm_force[2];
   if (force_bn == 16 || force_bn == 32 || force_bn == 48 || force_bn == 64 || force_bn == 96 || force_bn == 128 ||
       force_bn == 192 || force_bn == 256) {
     bn = force_bn;
@@ -563,14 +641,14 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
   }
   // Pixel blocks (tiled copies, ~1 row per clock) unless they would waste
   // more than 15 % of the tile rows on the image edges; then 128 consecutive
-  // pixels gathered in im2col mode.  CB_IGEMM_BLOCKS=0/1 overrides (per call).
+  // pixels gathered in im2col mode.  CB_IGEMM_BLOCKS=0/1 overrides.
   int bw = 0, bh = 0;
   double waste = 1e300;
   pick_blocks(y->h, y->w, stride, &bw, &bh, &waste);
   int blocks = im.blocks;
   if (blocks == 0) {
     blocks = waste <= 1.15 ? 2 : 1;
-    if (const char* f = std::getenv("CB_IGEMM_BLOCKS")) blocks = f[0] == '1' ? 2 : 1;
+    if (tu.igemm_blocks >= 0) blocks = tu.igemm_blocks == 1 ? 2 : 1;
   }
   if (blocks == 2 && bw > 0) {
     a.blk_w = bw;
@@ -590,7 +668,7 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
   const long long tiles = static_cast<long long>(a.m_tiles) * a.n_tiles;
   int grid = static_cast<int>(std::min<long long>(tiles, dev->sms));
   if (force_grid > 0 && force_grid < grid) grid = force_grid;
-  if (std::getenv("CB_DEBUG_PLAN"))
+  if (tu.debug_plan)
     std::fprintf(stderr,
                  "[cb] igemm plan: M=%d Ci=%d Co=%d k=%d s=%d -> bn=%d kc=%d n_tiles=%d m_tiles=%d stages=%d grid=%d "
                  "blocks=%dx%d\n",
@@ -655,19 +733,6 @@ bool halo_ring(int co, int hb, int force_nb, int force_tps, int* nb_out, int* tp
   return false;
 }
 
-HaloForce halo_force_env() {
-  // CB_HALO_FORCE = "cm[,stages[,split[,taps]]]" or "co[,stages[,split[,taps[,subtiles[,resident]]]]]", read per call
-  HaloForce f;
-  if (const char* e = std::getenv("CB_HALO_FORCE")) {
-    if (e[0] == 'c' && e[1] == 'm') {
-      f.cm = true;
-      if (e[2] == ',') std::sscanf(e + 3, "%d,%d,%d", &f.nb, &f.split, &f.tps);
-    } else {
-      std::sscanf(e, "%d,%d,%d,%d,%d,%d", &f.co, &f.nb, &f.split, &f.tps, &f.sub, &f.res);
-    }
-  }
-  return f;
-}
 
 bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, const HaloForce& f, HaloPlan* out) {
   const int N = x->n, Ci = x->c, Co = y->c, OH = y->h, OW = y->w;
@@ -873,7 +938,7 @@ cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, i
     DeviceInfo* dev = nullptr;
     HaloPlan tmp;
     HaloPlan& p = plan ? *plan : tmp;
-    const HaloForce f = halo_force_env();
+    const HaloForce f = tuning().halo;
     // Every 3x3 layer the halo tiles can take: they measured ahead of the
     // im2col-path kernel (two copies per tap and chunk) on each layer of
     // the dense sweep, stride 1 and 2.
@@ -922,12 +987,12 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
                  (ep.res_mode == 0 || (aligned16(ep.r) && ep.rs_n % 4 == 0 && ep.rs_h % 4 == 0 && ep.rs_w % 4 == 0)))
                     ? 1
                     : 0;
-  if (const char* t = std::getenv("CB_IGEMM_TRACE")) {  // profiling aid: timeline of one CTA
-    a.trace = 1;
-    a.trace_cta = std::atoi(t);
-    if (const char* sl = std::getenv("CB_SPAN_SLOT")) a.trace = std::atoi(sl) == 2 ? 2 : 1;
+  const Tuning tu = tuning();
+  if (tu.trace_cta >= 0) {  // profiling aid: timeline of one CTA
+    a.trace = tu.span_slot;
+    a.trace_cta = tu.trace_cta;
   }
-  if (std::getenv("CB_DEBUG_PLAN"))
+  if (tu.debug_plan)
     std::fprintf(stderr,
                  "[cb] halo plan: N=%d H=%d W=%d Ci=%d Co=%d s=%d -> %s px=%dx%d co=%d kc=%d nb=%d tps=%d "
                  "split=%d%s blocks=%dx%d rows=%d halo=%d tiles=%d grid=%d smem=%zu\n",
@@ -1272,7 +1337,11 @@ cb_status cb_autotune_conv(const cb_tensor* x, const float* w, const float* scal
   bool depthwise = false, empty = false;
   cb_status st = validate_conv(x, w, scale, bias, kh, kw, stride, pad, groups, act, residual, res_mode, y,
                                &depthwise, &empty);
-  if (st != CB_OK || empty) return st;
+  if (st != CB_OK) return st;
+  // Every candidate launch writes y: an in-place residual (residual == y)
+  // would be added again on each launch and be lost after the first.
+  if (res_mode != CB_RES_NONE && overlap(residual, y)) return CB_ERR_INVALID_ARG;
+  if (empty) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const ConvKey key = conv_key(x, y, kh, stride, pad);
   {
@@ -1322,7 +1391,7 @@ cb_status cb_autotune_conv(const cb_tensor* x, const float* w, const float* scal
     std::lock_guard<std::mutex> lock(g_tune_mu);
     g_tuned[key] = best;
   }
-  if (std::getenv("CB_DEBUG_PLAN") && found)
+  if (tuning().debug_plan && found)
     std::fprintf(stderr,
                  "[cb] autotune: Ci=%d Co=%d %dx%d k=%d s=%d -> path %d (px=%d co=%d nb=%d split=%d bn=%d) %.1f us\n",
                  x->c, y->c, x->h, x->w, kh, stride, static_cast<int>(best.path), best.halo.px, best.halo.co,
@@ -1352,11 +1421,12 @@ namespace {
 // round trip per pixel and chunk, so with fewer tiles (or only two layer
 // kernels to replace) the TMA-fed layer kernels win.
 // Tuning override: CB_DW_BLOCK_FORCE=1 takes the one kernel wherever its
-// shape rule allows, =0 never (read per call).
+// shape rule allows, =0 never.
 bool dw_block_fusable(const cb_tensor* x, const cb_tensor* y, const float* pw_w, const float* skip_w) {
   const long long pix = static_cast<long long>(y->n) * y->h * y->w;
   bool pick = skip_w && (pix + 127) / 128 >= 64;
-  if (const char* f = std::getenv("CB_DW_BLOCK_FORCE")) pick = f[0] == '1';
+  const int force = tuning().dw_block;
+  if (force >= 0) pick = force == 1;
   return g_policy.load() == 0 && pick && x->layout == CB_LAYOUT_NHWC && y->layout == CB_LAYOUT_NHWC && x->c % 4 == 0 &&
          x->c <= 1024 && y->c % 32 == 0 && y->c <= 256 && pix < (1LL << 31) && aligned16(x->data) &&
          strides_mult4(x) && aligned16(y->data) && strides_mult4(y) && aligned16(pw_w) &&
@@ -1438,9 +1508,10 @@ cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const flo
     a.out = make_out(y);
     a.err = dev->err;
     a.timeout_ns = timeout_ns();
-    if (const char* t = std::getenv("CB_IGEMM_TRACE")) {  // profiling aid: timeline of one CTA
+    const int trace_cta = tuning().trace_cta;
+    if (trace_cta >= 0) {  // profiling aid: timeline of one CTA
       a.trace = 1;
-      a.trace_cta = std::atoi(t);
+      a.trace_cta = trace_cta;
     }
     CUtensorMap pw_map, sk_map;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), 1, static_cast<cuuint64_t>(Co)};
@@ -1658,6 +1729,30 @@ const char* cb_status_string(cb_status s) {
 }
 
 int cb_version(void) { return kVersion; }
+
+cb_status cb_set_tuning(const char* name, const char* value) {
+  if (!name) return CB_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_tuning_mu);
+  Tuning t = tuning_locked();
+  if (!parse_tuning(&t, name, value)) return CB_ERR_INVALID_ARG;
+  tuning_locked() = t;
+  return CB_OK;
+}
+
+cb_status cb_last_launch(cb_launch_info* info) {
+  if (!info) return CB_ERR_INVALID_ARG;
+  const LaunchRecord& r = last_launch();
+  if (!r.kernel) return CB_ERR_INVALID_ARG;
+  info->grid = static_cast<int>(r.grid.x * r.grid.y * r.grid.z);
+  info->threads = static_cast<int>(r.block.x * r.block.y * r.block.z);
+  info->smem_bytes = r.smem;
+  info->cluster = r.cluster;
+  int per_sm = 0;
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, r.kernel, info->threads, r.smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  info->blocks_per_sm = per_sm;
+  return CB_OK;
+}
 
 cb_status cb_set_kernel_policy(int policy) {
   if (policy < 0 || policy > 2) return CB_ERR_INVALID_ARG;

@@ -40,6 +40,28 @@ inline bool pdl_enabled() {
   return on;
 }
 
+// The last kernel this host thread launched through launch_pdl (kernel,
+// grid, block, dynamic shared memory, cluster size): read back by
+// cb_last_launch for occupancy reports.
+struct LaunchRecord {
+  const void* kernel = nullptr;
+  dim3 grid, block;
+  size_t smem = 0;
+  int cluster = 1;
+};
+inline LaunchRecord& last_launch() {
+  static thread_local LaunchRecord r;
+  return r;
+}
+inline void record_launch(const void* kernel, dim3 grid, dim3 block, size_t smem, int cluster) {
+  LaunchRecord& r = last_launch();
+  r.kernel = kernel;
+  r.grid = grid;
+  r.block = block;
+  r.smem = smem;
+  r.cluster = cluster;
+}
+
 // Launches `kernel` on stream s with programmatic stream serialisation: the
 // kernel may be launched before the previous kernel of the stream has
 // finished and must call pdl_wait() before touching global memory.
@@ -56,6 +78,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  record_launch(reinterpret_cast<const void*>(kernel), grid, block, smem, 1);
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -77,6 +100,7 @@ cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  record_launch(reinterpret_cast<const void*>(kernel), grid, block, smem, cluster_x);
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

@@ -168,7 +168,10 @@ cb_status cb_conv_bn_act(const cb_tensor* x, const float* w, const float* scale,
 
 /*
  * Workspace bytes cb_dw_separable_block needs for input x, Co output
- * channels and the given stride (written to *bytes).
+ * channels and the given stride (written to *bytes): room for the block's
+ * two intermediates, the depthwise output t and the skip output s of the
+ * DepthwiseSeparableConv listing ("How I sped up convolutions", class
+ * listing), each rounded up to 256 bytes.  Host only; launches nothing.
  */
 cb_status cb_dw_separable_block_workspace(const cb_tensor* x, int c_out, int stride, size_t* bytes);
 
@@ -226,7 +229,10 @@ int cb_dw_separable_block_fused(const cb_tensor* x, const cb_tensor* y, const fl
  * keeps until the process exits.
  *  - The first call on a device looks the array's device address up
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.  Later calls reuse the address.
+ *    before any stream capture.  Later calls reuse the address, for the
+ *    life of the process: after cudaDeviceReset (or any reset of the
+ *    primary context) the cached address is stale, so do not call this
+ *    library on a device that was reset.
  *  - A block needing more scratch than CB_STATIC_SCRATCH_BYTES (see
  *    cb_dw_separable_block_workspace) is rejected with CB_ERR_WORKSPACE
  *    before anything runs.
@@ -267,12 +273,6 @@ cb_status cb_preprocess_u8(const unsigned char* src, int n, int src_h, int src_w
                            float* dst, int dst_h, int dst_w, void* stream);
 
 /*
- * The same preprocess as three passes ("A fused Ampere preprocess kernel",
- * path A: resize -> normalize -> layout), for comparison.  tmp_u8: DEVICE
- * [n, dst_h, dst_w, 3] u8; tmp_f32: DEVICE [n, dst_h, dst_w, 3] fp32; dst as
- * cb_preprocess_u8.  Produces bit-identical output to cb_preprocess_u8.
- */
-/*
  * The preprocess of cb_preprocess_u8 fused into the stem conv that reads its
  * output (conv 3 -> 16 channels, 3x3, stride 2, pad 1, folded BN, act): one
  * kernel reads the u8 frames and writes the stem's NHWC output; the fp32
@@ -293,6 +293,12 @@ cb_status cb_preprocess_stem_u8(const unsigned char* src, int n, int src_h, int 
                                 int dst_h, int dst_w, const float* w, const float* scale, const float* bias,
                                 cb_act act, cb_tensor* y, void* stream);
 
+/*
+ * The same preprocess as three passes ("A fused Ampere preprocess kernel",
+ * path A: resize -> normalize -> layout), for comparison.  tmp_u8: DEVICE
+ * [n, dst_h, dst_w, 3] u8; tmp_f32: DEVICE [n, dst_h, dst_w, 3] fp32; dst as
+ * cb_preprocess_u8.  Produces bit-identical output to cb_preprocess_u8.
+ */
 cb_status cb_preprocess_u8_three_pass(const unsigned char* src, int n, int src_h, int src_w,
                                       long long src_pitch, unsigned char* tmp_u8, float* tmp_f32,
                                       float* dst, int dst_h, int dst_w, void* stream);
@@ -301,6 +307,12 @@ cb_status cb_preprocess_u8_three_pass(const unsigned char* src, int n, int src_h
  * Synchronises `stream`, then reads and clears the library's device error
  * word: CB_ERR_TIMEOUT if a kernel gave up waiting on a barrier since the
  * last call, CB_ERR_CUDA if the stream reported an error, else CB_OK.
+ * The pages have no counterpart: this is the host end of the library's
+ * bounded waits.  The word's device address is looked up once per device
+ * and kept for the life of the process, like the scratch array of
+ * cb_dw_separable_block_static: after cudaDeviceReset (or any reset of the
+ * primary context) those cached addresses are stale, so a process that
+ * resets a device must not call this library on it again.
  */
 cb_status cb_get_device_error(void* stream);
 
@@ -375,6 +387,10 @@ int cb_conv_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int
  * computes the same TF32 products, so results stay within the tensor-core
  * tolerance of each other.  Other layers (depthwise, CUDA-core paths) have
  * one kernel and are launched once.  y holds the layer's result on return.
+ * Every candidate launch writes y, so a residual that overlaps y (the
+ * in-place residual cb_conv_bn_act accepts) is rejected with
+ * CB_ERR_INVALID_ARG: tune with a separate residual buffer of the same
+ * shape, then run the in-place layer through cb_conv_bn_act.
  * Synchronises `stream`; must not be called while the stream is being
  * captured into a graph.  Thread-safe; host table only, no device memory.
  */
@@ -388,6 +404,47 @@ void cb_autotune_clear(void);
 
 /* Number of layer shapes with a recorded plan. */
 int cb_autotune_entries(void);
+
+/*
+ * Plan overrides and profiling aids (no counterpart on the pages; none is
+ * needed for normal use).  `name` is one of
+ *   CB_DW_FORCE       "rows,tile_w,ctas_per_sm" of the depthwise kernel (0 = free)
+ *   CB_IGEMM_FORCE    "bn,stages,grid" of the im2col-path tensor-core kernel
+ *   CB_IGEMM_BLOCKS   "0" / "1": its A operand as im2col gathers / pixel blocks
+ *   CB_HALO_FORCE     "cm[,stages[,split[,taps]]]" or
+ *                     "co[,stages[,split[,taps[,subtiles[,resident]]]]]" of the halo kernel
+ *   CB_DW_BLOCK_FORCE "1" / "0": the one-kernel depthwise-separable block
+ *                     wherever its shape rule allows / never
+ *   CB_DEBUG_PLAN     any value: print each layer's plan to stderr
+ *   CB_IGEMM_TRACE, CB_SPAN_SLOT   CTA timelines (trace builds only)
+ * and `value` its setting (NULL or "" restores the default).  Each knob
+ * starts from the environment variable of the same name, read once per
+ * process; only this call changes it afterwards.  Plans recorded by
+ * cb_autotune_conv still take precedence for their shapes.  Process-wide
+ * and thread-safe; an override applies to calls made after it returns.
+ * Returns CB_ERR_INVALID_ARG for an unknown name.
+ */
+cb_status cb_set_tuning(const char* name, const char* value);
+
+/*
+ * The launch configuration of the last kernel this host thread enqueued
+ * through the library, and its occupancy: CTAs (grid), threads per CTA,
+ * dynamic shared memory per CTA, cluster size, and the CTAs per SM that
+ * cudaOccupancyMaxActiveBlocksPerMultiprocessor allows for that kernel and
+ * configuration.  Per-kernel occupancy is one of the figures "A fused Ampere
+ * preprocess kernel" reports for each of its kernels (occupancy section).
+ * Host only (the query launches nothing); CB_ERR_INVALID_ARG if this thread
+ * has launched nothing yet.
+ */
+typedef struct {
+  int grid;
+  int threads;
+  size_t smem_bytes;
+  int cluster;
+  int blocks_per_sm;
+} cb_launch_info;
+
+cb_status cb_last_launch(cb_launch_info* info);
 
 /* A static string naming a status code. */
 const char* cb_status_string(cb_status s);

@@ -188,3 +188,41 @@ def test_round_weights_tf32(cblib):
     assert cblib.round_weights_tf32(tie_even)[0] == 1.0
     assert cblib.round_weights_tf32(tie_odd).view(np.uint32)[0] == base + 0x4000
     assert np.isinf(cblib.round_weights_tf32(np.array([np.inf], np.float32))[0])
+
+
+def test_tuning_overrides_are_validated(cblib):
+    """cb_set_tuning knows its knobs by name (unknown names are refused) and resets each with NULL."""
+    lib = cblib.load()
+    for name, value in (("CB_HALO_FORCE", b"cm,2"), ("CB_IGEMM_FORCE", b"64,3,0"), ("CB_IGEMM_BLOCKS", b"1"),
+                        ("CB_DW_FORCE", b"4,0,2"), ("CB_DW_BLOCK_FORCE", b"0"), ("CB_DEBUG_PLAN", b"")):
+        assert lib.cb_set_tuning(name.encode(), value) == cblib.OK
+        assert lib.cb_set_tuning(name.encode(), None) == cblib.OK
+    assert lib.cb_set_tuning(b"CB_NO_SUCH_KNOB", b"1") == cblib.ERR_INVALID_ARG
+    assert lib.cb_set_tuning(None, b"1") == cblib.ERR_INVALID_ARG
+    with cblib.tuning("CB_DW_BLOCK_FORCE", "1"):
+        pass
+
+
+def test_last_launch_needs_a_launch(cblib):
+    """cb_last_launch reports this thread's last kernel; a thread that launched none gets INVALID_ARG."""
+    import threading
+    out = []
+    info = cblib.CbLaunchInfo()
+    t = threading.Thread(target=lambda: out.append(cblib.load().cb_last_launch(ctypes.byref(info))))
+    t.start()
+    t.join()
+    assert out == [cblib.ERR_INVALID_ARG]
+    assert cblib.load().cb_last_launch(None) == cblib.ERR_INVALID_ARG
+
+
+def test_autotune_rejects_in_place_residual(cblib):
+    """Each tuning launch writes y, so a residual on y would be added again and again: refused before
+    anything runs (fake pointers, never dereferenced)."""
+    lib = cblib.load()
+    T = ctypes.byref
+    base = 1 << 20
+    x = _view(base, 1, 8, 8, 32)
+    y = _view(base + (1 << 16), 1, 8, 8, 32)
+    w = s = b = base + (1 << 18)
+    assert lib.cb_autotune_conv(T(x), w, s, b, 3, 3, 1, 1, 1, 2, T(y), 2, T(y), None) == cblib.ERR_INVALID_ARG
+    assert lib.cb_autotune_conv(T(x), w, s, b, 3, 3, 1, 1, 1, 2, T(y), 1, T(y), None) == cblib.ERR_INVALID_ARG

@@ -6,8 +6,6 @@ bar against the fp64 oracle: the im2col tile widths are forced one by one here (
 shapes have their own forced tests); the tuned layer, and the layers launched after tuning, are
 checked against the oracle; the table is keyed by shape and policy and can be cleared.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -31,11 +29,9 @@ def fresh_table():
 
 @pytest.fixture
 def igemm_force():
-    old = os.environ.pop("CB_IGEMM_FORCE", None)
-    yield lambda v: os.environ.__setitem__("CB_IGEMM_FORCE", v)
-    os.environ.pop("CB_IGEMM_FORCE", None)
-    if old is not None:
-        os.environ["CB_IGEMM_FORCE"] = old
+    cb.set_tuning("CB_IGEMM_FORCE", None)
+    yield lambda v: cb.set_tuning("CB_IGEMM_FORCE", v)
+    cb.set_tuning("CB_IGEMM_FORCE", None)
 
 
 @pytest.mark.parametrize("bn", [16, 32, 48, 64, 96, 128, 192, 256])

@@ -7,8 +7,6 @@ Shapes: 3x3 and 1x1, stride 1 and 2, 8-, 16- and 32-channel chunks, blocks that 
 exactly and ragged ones, images smaller than a block, residuals, channel-slice output views with
 padded rows; each against the fp64 oracle at the TF32 bar, and against the im2col-mode tiles.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -30,11 +28,9 @@ def no_halo_tiles():
 
 @pytest.fixture
 def blocks_mode():
-    old = os.environ.pop("CB_IGEMM_BLOCKS", None)
-    yield lambda v: os.environ.__setitem__("CB_IGEMM_BLOCKS", v)
-    os.environ.pop("CB_IGEMM_BLOCKS", None)
-    if old is not None:
-        os.environ["CB_IGEMM_BLOCKS"] = old
+    cb.set_tuning("CB_IGEMM_BLOCKS", None)
+    yield lambda v: cb.set_tuning("CB_IGEMM_BLOCKS", v)
+    cb.set_tuning("CB_IGEMM_BLOCKS", None)
 
 
 CASES = [

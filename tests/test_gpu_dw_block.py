@@ -8,8 +8,6 @@ two batch sizes, channel counts that leave a partial 32-channel chunk, ragged 12
 256 output channels with a conv skip (two 256-column accumulators), a channel-slice output view
 with padded rows, and agreement with the three-call path (kernel policy 2).
 """
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -25,13 +23,9 @@ pytestmark = pytest.mark.gpu
 def force_one_kernel():
     """Every block of these tests takes the one kernel where its shape rule allows (the default
     choice also weighs the tile count and the skip); a test may switch it off."""
-    old = os.environ.get("CB_DW_BLOCK_FORCE")
-    os.environ["CB_DW_BLOCK_FORCE"] = "1"
+    cb.set_tuning("CB_DW_BLOCK_FORCE", "1")
     yield
-    if old is None:
-        os.environ.pop("CB_DW_BLOCK_FORCE", None)
-    else:
-        os.environ["CB_DW_BLOCK_FORCE"] = old
+    cb.set_tuning("CB_DW_BLOCK_FORCE", None)
 
 
 def _block_params(cin, cout, stride, seed):
@@ -127,7 +121,7 @@ def test_dw_block_one_kernel_not_taken(gpu):
 def test_dw_block_default_choice(gpu):
     """Without the override: one kernel for a conv-skip block with at least 64 tiles, three layer
     kernels for identity blocks and small grids."""
-    os.environ.pop("CB_DW_BLOCK_FORCE", None)
+    cb.set_tuning("CB_DW_BLOCK_FORCE", None)
     p = _block_params(48, 96, 2, seed=1)
     blk = DwBlock(p, 48, 96, 2)
     x = torch.empty(64, 28, 28, 48, device="cuda")  # 64 x 14 x 14 outputs: 98 tiles

@@ -8,8 +8,6 @@ than a tile row and wider than one, channel counts that leave a ragged last chan
 tile width the kernel has (forced through CB_HALO_FORCE), the epilogue variants, channel-slice
 output views with padded rows (canaries must survive) and the in-place residual.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -30,11 +28,9 @@ CASES = [
 
 @pytest.fixture
 def halo_force():
-    old = os.environ.pop("CB_HALO_FORCE", None)
-    yield lambda v: os.environ.__setitem__("CB_HALO_FORCE", v)
-    os.environ.pop("CB_HALO_FORCE", None)
-    if old is not None:
-        os.environ["CB_HALO_FORCE"] = old
+    cb.set_tuning("CB_HALO_FORCE", None)
+    yield lambda v: cb.set_tuning("CB_HALO_FORCE", v)
+    cb.set_tuning("CB_HALO_FORCE", None)
 
 
 def _run(x, w, bn, act=cb.ACT_SILU, residual=None, res_mode=0, y=None):
