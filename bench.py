@@ -1,16 +1,22 @@
 """Benchmark of the fused conv + BN + activation hot path on GB300.
 
-Default workload (N=1): the depthwise 3x3 + BN + ReLU layer, NHWC fp32,
-x = [64, 56, 56, 384] ~ N(0,1), at stride 1 and stride 2; one step = both
-launches over the batch.  ``value`` is algorithmic HBM bytes per second
-(input + output + weights + scale/bias, see conv_bn_activation_gb300/
-workloads.py) over the timed steps, whole job (all ranks).
+Default workload (N=1): the YOLO-style 20-conv chain, NHWC fp32, x =
+[32, 640, 640, 3] ~ U[0,1], five stages of conv3x3 s2 -> 1x1 -> 3x3 -> 1x1
+over the channel concat with a post-activation residual, every conv + BN +
+SiLU.  ``value`` is images per second over the timed steps, whole job (all
+ranks).  A step is R passes of the chain over the batch, R chosen so that
+the timed region lasts at least --min-timed-s (the pass count is in
+``config``); the R passes of a step are one CUDA graph.
 
-Other workloads (``--workload``) measure the rest of the hot path:
-  dense       the dense 3x3 + BN + SiLU sweep at batch 16 (TFLOP/s, tensor cores)
-  mnist       the DepthwiseMNIST forward at batch 64, replayed as a CUDA graph (images/s)
-  yolo        the 20-conv YOLO-style chain at batch 32, 640x640 (images/s)
+The same line carries, under ``configs``, the other configurations measured
+in the same run, each with its value, roofline and CPU baseline:
+  mnist       the DepthwiseMNIST forward at batch 64 (images/s)
+  depthwise   the depthwise 3x3 + BN + ReLU layer [64,56,56,384], stride 1 and 2 (GB/s)
+  dense       the dense 3x3 + BN + SiLU sweep at batch 16 and 1 (TFLOP/s, tensor cores)
+  yolo        the chain at batch 1
   preprocess  fused u8 preprocess -> stem conv at batch 32 (GB/s on the page's ledger)
+Each of these (and the bf16 storage and pointwise variants) can also be run
+alone with ``--workload``.
 
 Multi-GPU (torchrun): images are independent, so every rank runs its own
 batch (weak scaling, no data-path collective); ranks meet only at the
@@ -340,7 +346,8 @@ class DenseWorkload(Workload):
             kname, bound = kernel_of(cb, rec["x"], rec["y"], 3, s, 1)
             self.launches.append(Launch(name, (lambda r: lambda st: r["L"](r["x"], r["y"], stream=st))(rec),
                                         workloads.conv_layer(batch, H, H, ci, co, 3, s, 1), kname, bound))
-        self.config = {"workload": "dense 3x3 + BN + SiLU sweep, NHWC fp32 storage, TF32 tensor cores, batch 16",
+        self.config = {"workload": f"dense 3x3 + BN + SiLU sweep, NHWC fp32 storage, TF32 tensor cores, "
+                                   f"batch {batch}",
                        "batch": batch, "l2": "warm (per-layer working sets 15-180 MB; steps run back to back)",
                        "autotune": AUTOTUNE}
 
@@ -530,7 +537,12 @@ class PreprocessWorkload(Workload):
                                                              stream=stream))
         hbm = load_peaks()["hbm_gbs"]
         pre_gbs = self.pre.bytes / (pre_ms * 1e-3) / 1e9
-        return {"preprocess_kernel_us": round(pre_ms * 1e3, 2),
+        ledger = workloads_ledger_ratio()
+        return {"three_pass_over_fused_time": round(three_ms / pre_ms, 3),
+                "page_predicted_ratio": round(ledger, 3),
+                "ratio_note": "the page predicts the fused/unfused speed-up from its byte ledger "
+                              "(15,667,200 / 6,451,200 B per frame); measured = three-pass time / fused time",
+                "preprocess_kernel_us": round(pre_ms * 1e3, 2),
                 "preprocess_kernel_gbs_on_its_ledger": round(pre_gbs, 1),
                 "preprocess_kernel_frac": round(pre_gbs / hbm, 4),
                 "stem_kernel_planar_us": round(stem_ms * 1e3, 2),
@@ -557,6 +569,12 @@ class PreprocessWorkload(Workload):
         planar = oracle.preprocess_u8(self.frames_host[:n], 480, 640, oracle.PREC_F32)
         oracle.conv_bn_act(planar, self.sw, self.sbn, stride=2, pad=1, act=oracle.ACT_SILU, layout=oracle.NCHW)
         return time.perf_counter() - t0, self.step_units() * n / self.batch, f"{n} of {self.batch} frames"
+
+
+def workloads_ledger_ratio():
+    from conv_bn_activation_gb300 import workloads
+    led = workloads.preprocess_ledger(720, 1280, 480, 640)
+    return led["unfused"] / led["fused"]
 
 
 class DepthwiseBf16Workload(DepthwiseWorkload):
@@ -669,6 +687,231 @@ WORKLOADS = {"depthwise": DepthwiseWorkload, "depthwise_bf16": DepthwiseBf16Work
 
 
 # ------------------------------------------------------------ arms
+L2_FLUSH_BYTES = 320 << 20  # > 2x the 129 MB L2: written between cold-cache launch timings
+
+
+def _percentile(sorted_vals, q):
+    i = (len(sorted_vals) - 1) * q
+    lo, hi = int(np.floor(i)), int(np.ceil(i))
+    return sorted_vals[lo] + (sorted_vals[hi] - sorted_vals[lo]) * (i - lo)
+
+
+def pass_graph(torch, wl, device, passes):
+    """One CUDA graph of `passes` back-to-back passes of the workload (None for workloads that
+    replay their own graph)."""
+    if not wl.capture:
+        return None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cap = torch.cuda.current_stream(device)
+        for _ in range(passes):
+            wl.run(cap)
+    g.replay()
+    torch.cuda.synchronize()
+    return g
+
+
+def replay(wl, graph, stream, passes):
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(passes):
+            wl.run(stream)
+
+
+def pass_stats(torch, wl, device, stream, reps=200):
+    """Per-pass device time over `reps` single-pass replays with events between them: mean, P50,
+    P95, P99 and the coefficient of variation (the metric list of "How I sped up convolutions")."""
+    g = pass_graph(torch, wl, device, 1)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    for _ in range(3):
+        replay(wl, g, stream, 1)
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(reps):
+        replay(wl, g, stream, 1)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    ms = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
+    mean = statistics.fmean(ms)
+    return {"reps": reps, "mean_ms": round(mean, 4), "p50_ms": round(_percentile(ms, 0.50), 4),
+            "p95_ms": round(_percentile(ms, 0.95), 4), "p99_ms": round(_percentile(ms, 0.99), 4),
+            "cv": round(statistics.pstdev(ms) / mean, 4),
+            "how": "single-pass graph replays, events between them (one event gap per pass)"}
+
+
+def cold_launch_ms(torch, wl, device, stream, reps=7):
+    """ms per launch with a cold L2: before each timed launch a buffer larger than twice the L2 is
+    written (outside the events); median over reps."""
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    out = {}
+    for L in wl.launches:
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            L.fn(stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        out[L.name] = statistics.median(ts)
+    del flush
+    return out
+
+
+def launch_occupancy(torch, wl, stream):
+    """Per launch: grid, threads, shared memory and the CTAs per SM the occupancy calculator allows
+    for the kernel the library launched (cb_last_launch)."""
+    from conv_bn_activation_gb300 import binding
+    out = {}
+    if not wl.capture:
+        return out
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    for L in wl.launches:
+        L.fn(stream)
+        info = binding.last_launch()
+        warps = info["blocks_per_sm"] * ((info["threads"] + 31) // 32)
+        info["warps_per_sm"] = warps
+        info["theoretical_occupancy"] = round(warps / 64.0, 3)   # 64 resident warps per SM
+        info["waves"] = round(info["grid"] / max(1, info["blocks_per_sm"] * sms), 3)
+        out[L.name] = info
+    torch.cuda.synchronize()
+    return out
+
+
+def measure(torch, wl, device, stream, args, steps, warmup, min_timed_s, world, peaks, with_e2e, cpu_target_s):
+    """The timed run of one workload: K steps of R passes each (R chosen so that the timed region
+    lasts at least min_timed_s), with per-launch, cold-cache, statistics and occupancy figures."""
+    from conv_bn_activation_gb300 import binding
+    for _ in range(warmup):
+        wl.run(stream)
+    torch.cuda.synchronize()
+    if binding.get_device_error() != binding.OK:
+        raise RuntimeError("device error during warm-up")
+    # passes per step: enough that the K timed steps last min_timed_s
+    g1 = pass_graph(torch, wl, device, 1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(5):
+        replay(wl, g1, stream, 1)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    pass_ms = e0.elapsed_time(e1) / 5
+    del g1
+    passes = max(1, int(np.ceil(min_timed_s * 1e3 / (steps * max(pass_ms, 1e-3)))))
+    # The R passes of a step are captured as one CUDA graph with no event
+    # between launches: the library launches each kernel with programmatic
+    # dependent launch, and an event between two kernels would serialise
+    # them again.
+    graph = pass_graph(torch, wl, device, passes)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch, device.index or 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    e_start.record(stream)
+    for _ in range(steps):
+        replay(wl, graph, stream, passes)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = e_start.elapsed_time(e_end)
+    del graph
+    if binding.get_device_error() != binding.OK:
+        raise RuntimeError("device error during the timed steps")
+    # Per-kernel durations (the roofline's denominators): each launch of the
+    # pass repeated back to back, events around the repetitions only; and
+    # each launch alone after an L2 flush.
+    launch_ms = wl.time_launches(torch, stream, device, reps=args.launch_reps, eager=args.eager)
+    cold_ms = cold_launch_ms(torch, wl, device, stream) if wl.capture else {}
+    stats = pass_stats(torch, wl, device, stream)
+    occ = launch_occupancy(torch, wl, stream)
+    if binding.get_device_error() != binding.OK:
+        raise RuntimeError("device error while timing the launches")
+    extra = wl.extra(torch, stream, 20) if hasattr(wl, "extra") else None
+
+    # e2e: host buffers, copies inside the timed region, one pass per step
+    h2d = d2h = 0
+    e2e_ms = float("nan")
+    if with_e2e:
+        h2d, d2h = wl.e2e_setup()
+        for _ in range(3):
+            wl.e2e_step(stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(3, min(steps, 10))
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            wl.e2e_step(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    units = wl.step_units() * passes * steps
+    e2e_units = wl.step_units()
+    if world > 1:
+        total_ms, e2e_ms, units, e2e_units = aggregate_over_ranks(torch, total_ms, e2e_ms, units, e2e_units, device)
+    scale = UNIT_SCALE[wl.unit]
+    value = units / (total_ms * 1e-3) / scale
+    per_launch = wl.per_launch(launch_ms, peaks)
+    total_launch = sum(launch_ms.values())
+    for name, rec in per_launch.items():
+        rec["share"] = round(launch_ms[name] / total_launch, 4)
+        if name in cold_ms:
+            rec["us_cold_l2"] = round(cold_ms[name] * 1e3, 2)
+        if name in occ:
+            rec["occupancy"] = occ[name]
+    by_kernel = {}
+    for L in wl.launches:
+        k = L.kernel.split(" (")[0]
+        by_kernel.setdefault(k, [0, 0.0])
+        by_kernel[k][0] += 1
+        by_kernel[k][1] += launch_ms[L.name]
+    out = {
+        "value": round(value, 3), "unit": wl.unit, "steps": steps, "passes_per_step": passes,
+        "ms_per_step": round(total_ms / steps, 4), "timed_region_s": round(total_ms / 1e3, 3),
+        "config": dict(wl.config),
+        "images_per_s": round(wl.batch * world * passes * steps / (total_ms * 1e-3), 1),
+        "us_per_image": round(total_ms * 1e3 / (passes * steps) / wl.batch, 3),
+        "step_stats": stats,
+        "launches": per_launch,
+        "kernel_shares": {k: {"launches": n, "us": round(t * 1e3, 2), "share": round(t / total_launch, 4)}
+                          for k, (n, t) in sorted(by_kernel.items(), key=lambda kv: -kv[1][1])},
+        "roofline": wl.roofline(launch_ms, peaks),
+        "e2e": None if not with_e2e else {"value": round(e2e_units / (e2e_ms * 1e-3) / scale, 3), "unit": wl.unit,
+                                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                                          "ms_per_step": round(e2e_ms, 3),
+                                          "step": "one pass with its host copies (pinned memory)"},
+        "gpu_launches": getattr(wl, "kernels_per_step", len(wl.launches)) * passes * steps,
+        "timing": {"steps": f"one CUDA graph of {passes} passes per step, replayed {steps} times, events around "
+                            "all of them",
+                   "launches": f"each launch repeated {args.launch_reps}x back to back "
+                               f"({'eager' if args.eager or not wl.capture else 'one CUDA graph'}), "
+                               "events around the repetitions; us_cold_l2: one launch after a 320 MB write, "
+                               "median of 7"},
+        "clocks": clocks,
+    }
+    if extra:
+        out["comparison"] = extra
+    if world == 1 and cpu_target_s > 0:
+        out["cpu_baseline"] = cpu_baseline(wl, target_s=cpu_target_s, max_s=2.5 * cpu_target_s)
+    return out
+
+
+# The other configurations of the workload list, measured in the same run
+# beside the headline one: (key, workload, batch).
+EXTRA_CONFIGS = (("cfg0_mnist_b64", "mnist", 64), ("cfg1_depthwise_b64", "depthwise", 64),
+                 ("cfg2_dense_b16", "dense", 16), ("cfg2_dense_b1", "dense", 1),
+                 ("cfg3_yolo_b1", "yolo", 1), ("cfg4_preprocess_stem_b32", "preprocess", 32))
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_setup()
@@ -685,110 +928,52 @@ def run_ours(args):
 
     global AUTOTUNE
     AUTOTUNE = not args.no_autotune
-    wl = WORKLOADS[args.workload](torch, device, **({"batch": args.batch} if args.batch else {}))
     stream = torch.cuda.current_stream(device)
-    for _ in range(args.warmup):
-        wl.run(stream)
-    torch.cuda.synchronize()
-    if binding.get_device_error() != binding.OK:
-        raise RuntimeError("device error during warm-up")
-
-    nl = len(wl.launches)
-    graph = None
-    if wl.capture and not args.eager:
-        # The K timed steps are captured as one CUDA graph with no event
-        # between launches: the library launches each kernel with
-        # programmatic dependent launch, and an event between two kernels
-        # would serialise them again.
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            cap = torch.cuda.current_stream(device)
-            for _ in range(args.steps):
-                wl.run(cap)
-        graph.replay()
-        torch.cuda.synchronize()
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(torch, local)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    sampler.start()
-    e_start.record(stream)
-    if graph is not None:
-        graph.replay()
-    else:
-        for _ in range(args.steps):
+    wl = WORKLOADS[args.workload](torch, device, **({"batch": args.batch} if args.batch else {}))
+    if args.profile_pass:
+        # one pass inside an NVTX range, for profilers (ncu --nvtx --nvtx-include "profiled_pass/");
+        # nothing is timed
+        for _ in range(args.warmup):
             wl.run(stream)
-    e_end.record(stream)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = e_start.elapsed_time(e_end)
-    if binding.get_device_error() != binding.OK:
-        raise RuntimeError("device error during the timed steps")
-    # Per-kernel durations (the roofline's denominators): each launch of the
-    # step repeated back to back, events around the repetitions only.
-    launch_ms = wl.time_launches(torch, stream, device, reps=args.launch_reps, eager=args.eager)
-    if binding.get_device_error() != binding.OK:
-        raise RuntimeError("device error while timing the launches")
-    extra = wl.extra(torch, stream, args.steps) if hasattr(wl, "extra") else None
-
-    # e2e: host buffers, copies inside the timed region
-    h2d = d2h = 0
-    e2e_ms = float("nan")
-    if not args.no_e2e:
-        h2d, d2h = wl.e2e_setup()
-        for _ in range(3):
-            wl.e2e_step(stream)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2e_steps = max(1, min(args.steps, 10))
-        if world > 1:
-            torch.distributed.barrier()
+        torch.cuda.nvtx.range_push("profiled_pass")
+        wl.run(stream)
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            wl.e2e_step(stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-
-    units = wl.step_units() * args.steps
-    e2e_units = wl.step_units()
-    if world > 1:
-        total_ms, e2e_ms, units, e2e_units = aggregate_over_ranks(torch, total_ms, e2e_ms, units, e2e_units, device)
+        if binding.get_device_error() != binding.OK:
+            raise RuntimeError("device error in the profiled pass")
+        print(json.dumps({"profiled_pass": args.workload, "batch": wl.batch,
+                          "launches": [[L.name, L.kernel] for L in wl.launches]}), flush=True)
+        return
+    main = measure(torch, wl, device, stream, args, args.steps, args.warmup, args.min_timed_s, world, peaks,
+                   not args.no_e2e, 0 if args.no_cpu_baseline else 12.0)
+    del wl
+    extra = {}
+    if args.workload == "yolo" and not args.batch and not args.no_extra_configs:
+        for key, name, batch in EXTRA_CONFIGS:
+            w = WORKLOADS[name](torch, device, batch=batch)
+            r = measure(torch, w, device, stream, args, 10, 3, 0.3, world, peaks, False,
+                        0 if args.no_cpu_baseline else 3.0)
+            extra[key] = {k: r[k] for k in ("value", "unit", "config", "images_per_s", "us_per_image", "roofline",
+                                            "step_stats", "launches", "kernel_shares", "cpu_baseline", "comparison",
+                                            "passes_per_step", "ms_per_step")
+                          if k in r}
+            del w
+            torch.cuda.empty_cache()
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-
-    scale = UNIT_SCALE[wl.unit]
-    value = units / (total_ms * 1e-3) / scale
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": wl.unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "metric": METRIC, "value": main["value"], "unit": main["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(wl.config, parallelism=f"replicas x{world} (independent images, no collective)"),
-        "images_per_s": round(wl.batch * world * args.steps / (total_ms * 1e-3), 1),
-        "us_per_image": round(total_ms * 1e3 / args.steps / wl.batch, 3),
-        "launches": wl.per_launch(launch_ms, peaks),
-        "roofline": wl.roofline(launch_ms, peaks),
-        "e2e": None if args.no_e2e else {"value": round(e2e_units / (e2e_ms * 1e-3) / scale, 3), "unit": wl.unit,
-                                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                                         "ms_per_step": round(e2e_ms, 3)},
-        "gpu_launches": getattr(wl, "kernels_per_step", nl) * args.steps,
-        "timing": {"steps": "one CUDA graph of the K steps, events around it" if graph is not None
-                   else "K eager steps, events around them",
-                   "launches": f"each launch repeated {args.launch_reps}x back to back "
-                               f"({'eager' if args.eager or not wl.capture else 'one CUDA graph'}), "
-                               "events around the repetitions"},
-        "clocks": clocks,
+        "config": dict(main["config"], passes_per_step=main["passes_per_step"],
+                       parallelism=f"replicas x{world} (independent images, no collective)"),
     }
+    line.update({k: v for k, v in main.items() if k not in ("value", "unit", "steps", "ms_per_step", "config")})
     if extra:
-        line["comparison"] = extra
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["configs"] = extra
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -813,43 +998,61 @@ def cpu_baseline(wl, target_s=12.0, max_s=30.0):
 
 
 def run_reference(args):
-    """The oracle as the reference arm, on the host cores, rank 0 only."""
+    """The oracle as the reference arm, on the host cores, rank 0 only: the same workload, metric
+    and unit as our arm, each step a bounded sample (one image of the batch through the whole
+    chain for the YOLO-style workload)."""
     world, rank, local = dist_setup()
     if rank != 0:
         return
     import oracle
     oracle.build()
     from conv_bn_activation_gb300 import synthetic, workloads
-    if args.workload != "depthwise":
-        print(json.dumps({"impl": "reference", "unavailable": "the reference arm is timed on the default "
-                          "(depthwise) workload only"}))
+    if args.workload == "yolo":
+        stages = synthetic.yolo_params()
+        x = synthetic.yolo_input(32)
+        n = 1
+
+        def step(i):
+            h = x[i % 32:i % 32 + n]
+            for st in stages:
+                h = oracle.yolo_stage(h, st).astype(np.float32)
+
+        unit, per_step, sample = "images/s", n, f"{n} image of the 32-image batch per step, all 20 layers"
+        config = {"workload": "YOLO-style 20-conv chain (5 stages, concat via channel views, post-act residual), "
+                              "640x640x3 fp32", "batch": 32, "l2": "n/a (CPU)"}
+    elif args.workload == "depthwise":
+        xd, w, bn = synthetic.depthwise_layer()
+        wl = workloads.depthwise_workload()
+        n = 1
+
+        def step(i):
+            xs = xd[i % 64:i % 64 + n]
+            oracle.conv_bn_act(xs, w, bn, stride=1, pad=1, groups=384, act=oracle.ACT_RELU)
+            oracle.conv_bn_act(xs, w, bn, stride=2, pad=1, groups=384, act=oracle.ACT_RELU)
+
+        unit, per_step = "GB/s", (wl["s1"].bytes + wl["s2"].bytes) * n / 64 / 1e9
+        sample = f"{n} image of the 64-image batch per step, stride 1 and 2"
+        config = {"workload": "depthwise 3x3 + BN + ReLU, NHWC fp32, N=64 C=384 56x56, stride 1 and 2",
+                  "batch": 64, "l2": "n/a (CPU)"}
+    else:
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm is timed on the yolo (default) "
+                          "and depthwise workloads only"}))
         return
-    x, w, bn = synthetic.depthwise_layer()
-    wl = workloads.depthwise_workload()
-    n = 1
-    step_bytes = (wl["s1"].bytes + wl["s2"].bytes) * n // 64
-
-    def step():
-        xs = x[:n]
-        oracle.conv_bn_act(xs, w, bn, stride=1, pad=1, groups=384, act=oracle.ACT_RELU)
-        oracle.conv_bn_act(xs, w, bn, stride=2, pad=1, groups=384, act=oracle.ACT_RELU)
-
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        step(i)
     dt = time.perf_counter() - t0
-    value = step_bytes * args.steps / dt / 1e9
+    value = per_step * args.steps / dt
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "depthwise 3x3 + BN + ReLU, NHWC fp32, N=64 C=384 56x56, stride 1 and 2",
-                   "batch": 64, "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": f"{n} image of the 64-image batch per step, stride 1 and 2"},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": config,
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
@@ -861,12 +1064,18 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="depthwise", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="yolo", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of one captured graph")
     ap.add_argument("--launch-reps", type=int, default=20, help="back-to-back repetitions per kernel timing")
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="passes per step are scaled so that the K timed steps last at least this long")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="default (yolo) run: skip the other configurations measured beside it")
+    ap.add_argument("--profile-pass", action="store_true",
+                    help="set up, warm up, run one pass inside the NVTX range 'profiled_pass' and exit (profilers)")
     ap.add_argument("--no-autotune", action="store_true",
                     help="dense / yolo: keep the built-in tile cost model instead of measuring plans at setup")
     args = ap.parse_args()

@@ -31,7 +31,7 @@ EXPORTED = (
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_layer_uses_tensor_cores",
     "cb_dw_separable_block_static", "cb_conv_path", "cb_debug_timeout_probe", "cb_autotune_conv",
     "cb_autotune_clear", "cb_autotune_entries", "cb_preprocess_stem_u8", "cb_dw_separable_block_fused",
-    "cb_set_tuning", "cb_last_launch",
+    "cb_set_tuning", "cb_last_launch", "cb_debug_sample_coords",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
@@ -90,6 +90,7 @@ def load():
                 "cb_layer_uses_tensor_cores": [I, I, I, I, I],
                 "cb_conv_path": [T, T, I, I, I, I],
                 "cb_debug_timeout_probe": [I, P],
+                "cb_debug_sample_coords": [I, I, P, P, P, P],
                 "cb_autotune_conv": [T, P, P, P, I, I, I, I, I, I, T, I, T, P],
                 "cb_autotune_clear": [],
                 "cb_preprocess_stem_u8": [P, I, I, I, LL, I, I, P, P, P, I, T, P],
@@ -363,6 +364,18 @@ def preprocess_u8_three_pass(src, tmp_u8, tmp_f32, dst, stream=None):
 def debug_timeout_probe(timeout_ms, stream=None):
     """cb_debug_timeout_probe: a bounded wait that nothing satisfies (tests the timeout report)."""
     _check(load().cb_debug_timeout_probe(int(timeout_ms), _stream_ptr(stream)), "cb_debug_timeout_probe")
+
+
+def debug_sample_coords(src_extent, dst_extent, device="cuda", stream=None):
+    """cb_debug_sample_coords: the (i0, i1, frac) the preprocess kernels use along one axis, as numpy."""
+    import torch
+    i0 = torch.empty(dst_extent, dtype=torch.int32, device=device)
+    i1 = torch.empty(dst_extent, dtype=torch.int32, device=device)
+    a = torch.empty(dst_extent, dtype=torch.float32, device=device)
+    _check(load().cb_debug_sample_coords(int(src_extent), int(dst_extent), i0.data_ptr(), i1.data_ptr(),
+                                         a.data_ptr(), _stream_ptr(stream)), "cb_debug_sample_coords")
+    torch.cuda.synchronize()
+    return i0.cpu().numpy(), i1.cpu().numpy(), a.cpu().numpy()
 
 
 def get_device_error(stream=None) -> int:

@@ -1703,6 +1703,13 @@ cb_status cb_get_device_error(void* stream) {
   return CB_OK;
 }
 
+cb_status cb_debug_sample_coords(int src_extent, int dst_extent, int* i0, int* i1, float* frac, void* stream) {
+  if (src_extent < 1 || dst_extent < 1 || !i0 || !i1 || !frac) return CB_ERR_INVALID_ARG;
+  const cudaError_t e =
+      launch_sample_coords(src_extent, dst_extent, i0, i1, frac, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
 cb_status cb_debug_timeout_probe(int timeout_ms, void* stream) {
   if (timeout_ms < 1 || timeout_ms > 10000) return CB_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;

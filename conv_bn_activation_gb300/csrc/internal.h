@@ -213,6 +213,8 @@ cudaError_t launch_stem(const StemArgs& a, int src_kind, size_t smem, int sms, c
 // -------------------------------------------------------------- preprocess
 cudaError_t launch_preprocess_fused(const uint8_t* src, int n, int hs, int ws, long long pitch, float* dst,
                                     int hd, int wd, int sms, cudaStream_t s);
+// Sample coordinates (i0, i1, a) along one axis, as the preprocess kernels compute them.
+cudaError_t launch_sample_coords(int S, int D, int* i0, int* i1, float* a, cudaStream_t s);
 cudaError_t launch_preprocess_resize(const uint8_t* src, int n, int hs, int ws, long long pitch,
                                      uint8_t* out, int hd, int wd, cudaStream_t s);
 cudaError_t launch_preprocess_normalize(const uint8_t* in, long long count, float* out, cudaStream_t s);

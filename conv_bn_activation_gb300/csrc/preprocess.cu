@@ -393,4 +393,25 @@ cudaError_t launch_preprocess_layout(const float* in, int n, int h, int w, float
   return cudaGetLastError();
 }
 
+// The sample coordinates every preprocess kernel uses along one axis of
+// source extent S and destination extent D (one thread per destination
+// index), for checks of the resize's indexing.
+__global__ void __launch_bounds__(256) sample_coords_kernel(int S, int D, int* __restrict__ i0, int* __restrict__ i1,
+                                                            float* __restrict__ a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const float scale = __fdiv_rn(static_cast<float>(S), static_cast<float>(D));
+  for (int d = blockIdx.x * blockDim.x + threadIdx.x; d < D; d += gridDim.x * blockDim.x) {
+    const AxisSample s = axis_sample(d, S, scale);
+    i0[d] = s.i0;
+    i1[d] = s.i1;
+    a[d] = s.a;
+  }
+}
+
+cudaError_t launch_sample_coords(int S, int D, int* i0, int* i1, float* a, cudaStream_t s) {
+  const int blocks = (D + 255) / 256 < 1024 ? (D + 255) / 256 : 1024;
+  return launch_pdl(sample_coords_kernel, dim3(blocks), dim3(256), 0, s, S, D, i0, i1, a);
+}
+
 }  // namespace cb

@@ -317,6 +317,20 @@ cb_status cb_preprocess_u8_three_pass(const unsigned char* src, int n, int src_h
 cb_status cb_get_device_error(void* stream);
 
 /*
+ * Test hook for the resize's indexing: writes, for every destination index
+ * d < dst_extent of one axis, the sample coordinates the preprocess kernels
+ * (cb_preprocess_u8, its three-pass form and cb_preprocess_stem_u8) use --
+ * i0[d], i1[d] and the weight frac[d] of source index i1 -- computed on the
+ * GPU by the same device code: f = (d + 0.5) * (S / D) - 0.5 in IEEE fp32,
+ * i0 = floor(f) and frac = f - i0, clamped at the borders as documented for
+ * cb_preprocess_u8 ("A fused Ampere preprocess kernel": bilinear is a
+ * contract with the reference resize).  i0, i1: DEVICE int[dst_extent];
+ * frac: DEVICE float[dst_extent].  Asynchronous on `stream`; returns
+ * CB_ERR_INVALID_ARG for extents below 1 or NULL pointers.
+ */
+cb_status cb_debug_sample_coords(int src_extent, int dst_extent, int* i0, int* i1, float* frac, void* stream);
+
+/*
  * Test hook for the failure path of the bounded waits (no counterpart on the
  * pages): launches on `stream` one CTA that waits, with the same bounded
  * mbarrier wait every pipeline kernel uses, on a barrier nothing ever
