@@ -238,24 +238,59 @@ __global__ void __launch_bounds__(256, 2) direct_tile_kernel(const DirectArgs a,
 #pragma unroll
         for (int q = 0; q < COB; ++q) acc[p][q] = 0.0f;
 
-      for (int kh = 0; kh < KS; ++kh) {
+      if constexpr (S == 1 && KS == 3 && CI > 0) {
+        // Stride 1: a staged row is kTileW + 2 words (a compile-time pitch).
+        // Per (input channel, filter column) the thread loads the PX + 2
+        // input rows its PX outputs touch once and reuses them for the
+        // three filter rows: (PX + 2) + 3 * COB / 4 shared loads per
+        // 3 * PX * COB FMAs, all at immediate offsets from two pointers that
+        // advance once per channel.
+        constexpr int kPitch = kTileW + 2;
+        const float* xb = xs + rowg * kPitch + col;
+        const float* wb = ws + co0;
+#pragma unroll 1
+        for (int ci = 0; ci < CI; ++ci, xb += tg.plane, wb += co_pad) {
 #pragma unroll
-        for (int kw = 0; kw < KS; ++kw) {
-          const int sc = S == 2 ? (kw & 1) * tg.half + col + (kw >> 1) : col + kw;
-          const float* wp = ws + (kh * KS + kw) * Ci * co_pad + co0;
-          for (int ci = 0; ci < Ci; ++ci) {
-            float wv[COB];
+          for (int kw = 0; kw < 3; ++kw) {
+            float xv[PX + 2];
 #pragma unroll
-            for (int q = 0; q < COB; q += 4) {
-              const float4 t4 = *reinterpret_cast<const float4*>(wp + ci * co_pad + q);
-              wv[q] = t4.x, wv[q + 1] = t4.y, wv[q + 2] = t4.z, wv[q + 3] = t4.w;
+            for (int r = 0; r < PX + 2; ++r) xv[r] = xb[r * kPitch + kw];
+#pragma unroll
+            for (int kh = 0; kh < 3; ++kh) {
+              float wv[COB];
+              const float* wp = wb + (kh * 3 + kw) * CI * co_pad;
+#pragma unroll
+              for (int q = 0; q < COB; q += 4) {
+                const float4 t4 = *reinterpret_cast<const float4*>(wp + q);
+                wv[q] = t4.x, wv[q + 1] = t4.y, wv[q + 2] = t4.z, wv[q + 3] = t4.w;
+              }
+#pragma unroll
+              for (int p = 0; p < PX; ++p)
+#pragma unroll
+                for (int q = 0; q < COB; ++q) acc[p][q] = fmaf(xv[p + kh], wv[q], acc[p][q]);
             }
-            const float* xp = xs + ci * tg.plane + (rowg * S + kh) * tg.pitch + sc;
+          }
+        }
+      } else {
+        for (int kh = 0; kh < KS; ++kh) {
 #pragma unroll
-            for (int p = 0; p < PX; ++p) {
-              const float xv = xp[p * S * tg.pitch];
+          for (int kw = 0; kw < KS; ++kw) {
+            const int sc = S == 2 ? (kw & 1) * tg.half + col + (kw >> 1) : col + kw;
+            const float* wp = ws + (kh * KS + kw) * Ci * co_pad + co0;
+            for (int ci = 0; ci < Ci; ++ci) {
+              float wv[COB];
 #pragma unroll
-              for (int q = 0; q < COB; ++q) acc[p][q] = fmaf(xv, wv[q], acc[p][q]);
+              for (int q = 0; q < COB; q += 4) {
+                const float4 t4 = *reinterpret_cast<const float4*>(wp + ci * co_pad + q);
+                wv[q] = t4.x, wv[q + 1] = t4.y, wv[q + 2] = t4.z, wv[q + 3] = t4.w;
+              }
+              const float* xp = xs + ci * tg.plane + (rowg * S + kh) * tg.pitch + sc;
+#pragma unroll
+              for (int p = 0; p < PX; ++p) {
+                const float xv = xp[p * S * tg.pitch];
+#pragma unroll
+                for (int q = 0; q < COB; ++q) acc[p][q] = fmaf(xv, wv[q], acc[p][q]);
+              }
             }
           }
         }
