@@ -760,6 +760,25 @@ def cold_launch_ms(torch, wl, device, stream, reps=7):
     return out
 
 
+def short_kernel_name(mangled):
+    """'cb::conv3x3_c8_kernel' from an Itanium-mangled name such as
+    _ZN2cb12_GLOBAL__N_117conv3x3_c8_kernelILi2ELi0EEEvNS_10DirectArgsEii (anonymous namespaces
+    skipped); the input itself when it is not of that form."""
+    if not mangled or not mangled.startswith("_ZN"):
+        return mangled
+    parts, i = [], 3
+    while i < len(mangled) and mangled[i].isdigit():
+        j = i
+        while j < len(mangled) and mangled[j].isdigit():
+            j += 1
+        k = int(mangled[i:j])
+        name = mangled[j:j + k]
+        i = j + k
+        if not name.startswith("_GLOBAL__N"):
+            parts.append(name)
+    return "::".join(parts) if parts else mangled
+
+
 def launch_occupancy(torch, wl, stream):
     """Per launch: grid, threads, shared memory and the CTAs per SM the occupancy calculator allows
     for the kernel the library launched (cb_last_launch)."""
@@ -771,6 +790,7 @@ def launch_occupancy(torch, wl, stream):
     for L in wl.launches:
         L.fn(stream)
         info = binding.last_launch()
+        info["kernel"] = short_kernel_name(info["kernel"])
         warps = info["blocks_per_sm"] * ((info["threads"] + 31) // 32)
         info["warps_per_sm"] = warps
         info["theoretical_occupancy"] = round(warps / 64.0, 3)   # 64 resident warps per SM
@@ -860,6 +880,9 @@ def measure(torch, wl, device, stream, args, steps, warmup, min_timed_s, world, 
         total_ms, e2e_ms, units, e2e_units = aggregate_over_ranks(torch, total_ms, e2e_ms, units, e2e_units, device)
     scale = UNIT_SCALE[wl.unit]
     value = units / (total_ms * 1e-3) / scale
+    for L in wl.launches:  # label each launch with the kernel the library actually ran
+        if L.name in occ and occ[L.name]["kernel"] not in ("", "?"):
+            L.kernel = occ[L.name]["kernel"]
     per_launch = wl.per_launch(launch_ms, peaks)
     total_launch = sum(launch_ms.values())
     for name, rec in per_launch.items():

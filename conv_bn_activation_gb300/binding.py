@@ -48,7 +48,7 @@ class CbTensor(ctypes.Structure):
 
 class CbLaunchInfo(ctypes.Structure):
     _fields_ = [("grid", ctypes.c_int), ("threads", ctypes.c_int), ("smem_bytes", ctypes.c_size_t),
-                ("cluster", ctypes.c_int), ("blocks_per_sm", ctypes.c_int)]
+                ("cluster", ctypes.c_int), ("blocks_per_sm", ctypes.c_int), ("kernel", ctypes.c_char_p)]
 
 
 class CbError(RuntimeError):
@@ -203,11 +203,11 @@ class tuning:
 
 
 def last_launch() -> dict:
-    """cb_last_launch: launch configuration and occupancy (CTAs per SM) of this thread's last kernel."""
+    """cb_last_launch: launch configuration, occupancy (CTAs per SM) and name of this thread's last kernel."""
     info = CbLaunchInfo()
     _check(load().cb_last_launch(ctypes.byref(info)), "cb_last_launch")
     return {"grid": info.grid, "threads": info.threads, "smem_bytes": int(info.smem_bytes), "cluster": info.cluster,
-            "blocks_per_sm": info.blocks_per_sm}
+            "blocks_per_sm": info.blocks_per_sm, "kernel": (info.kernel or b"?").decode()}
 
 
 def round_weights_tf32(w):

@@ -1758,6 +1758,12 @@ cb_status cb_last_launch(cb_launch_info* info) {
   const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, r.kernel, info->threads, r.smem);
   if (e != cudaSuccess) return cuda_fail(e);
   info->blocks_per_sm = per_sm;
+  const char* name = nullptr;
+  if (cudaFuncGetName(&name, r.kernel) != cudaSuccess) {
+    cudaGetLastError();
+    name = nullptr;
+  }
+  info->kernel = name ? name : "?";
   return CB_OK;
 }
 

@@ -407,6 +407,7 @@ cudaError_t launch_direct(const DirectArgs& a, int sms, cudaStream_t s) {
                       (a.ep.res_mode == 0 || ((reinterpret_cast<uintptr_t>(a.ep.r) % 16 == 0) && a.ep.rs_w % 4 == 0 &&
                                               a.ep.rs_h % 4 == 0 && a.ep.rs_n % 4 == 0));
   const int vec = vec_ok ? 1 : 0;
+  if (conv3x3_c8_ok(a)) return launch_conv3x3_c8(a, sms, s);
   if (a.Ci <= 16 && a.kh == a.kw && (a.kh == 1 || a.kh == 3) && (a.stride == 1 || a.stride == 2)) {
     cudaError_t e;
     if (a.stride == 1)

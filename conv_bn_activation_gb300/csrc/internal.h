@@ -65,6 +65,11 @@ struct DirectArgs {
   int bf16;  // x, y and r hold bfloat16 (pointwise kernel only); w, scale, bias fp32
 };
 cudaError_t launch_direct(const DirectArgs& a, int sms, cudaStream_t s);
+// 3x3 stride-1 pad-1 layers with 8 input and 8 output channels (conv3x3_c8.cu):
+// NHWC fp32 x, y (and residual) with 16-byte aligned pixels and strides that
+// are multiples of 4 elements; cudaErrorInvalidValue for anything else.
+bool conv3x3_c8_ok(const DirectArgs& a);
+cudaError_t launch_conv3x3_c8(const DirectArgs& a, int sms, cudaStream_t s);
 // 1x1 stride-1 layers with Ci, Co in {4, 8, 16, 32} (pointwise.cu): needs
 // NHWC views with 16-byte aligned pixels; flat = every view's pixels are
 // evenly spaced (stride_h = W * stride_w, stride_n = H * stride_h).  With

@@ -445,7 +445,7 @@ cb_status cb_set_tuning(const char* name, const char* value);
  * through the library, and its occupancy: CTAs (grid), threads per CTA,
  * dynamic shared memory per CTA, cluster size, and the CTAs per SM that
  * cudaOccupancyMaxActiveBlocksPerMultiprocessor allows for that kernel and
- * configuration.  Per-kernel occupancy is one of the figures "A fused Ampere
+ * configuration, and the kernel's name.  Per-kernel occupancy is one of the figures "A fused Ampere
  * preprocess kernel" reports for each of its kernels (occupancy section).
  * Host only (the query launches nothing); CB_ERR_INVALID_ARG if this thread
  * has launched nothing yet.
@@ -456,6 +456,7 @@ typedef struct {
   size_t smem_bytes;
   int cluster;
   int blocks_per_sm;
+  const char* kernel;  /* the kernel's (mangled) name, a static string of the CUDA runtime */
 } cb_launch_info;
 
 cb_status cb_last_launch(cb_launch_info* info);
