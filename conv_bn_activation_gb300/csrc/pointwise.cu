@@ -45,7 +45,7 @@ __device__ __forceinline__ float4 pw_epilogue(float4 acc, float4 sc, float4 bi, 
     for (int i = 0; i < 4; ++i) z[i] = fmaxf(z[i], 0.0f);
   } else if (act == 2) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) z[i] = __fdividef(z[i], 1.0f + __expf(-z[i]));
+    for (int i = 0; i < 4; ++i) z[i] = silu(z[i]);
   }
   if (res_mode == 2)
 #pragma unroll

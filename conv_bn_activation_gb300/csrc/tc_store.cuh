@@ -18,13 +18,14 @@
 //      instruction now writes 32 / (CH/4) whole pixel segments.
 #pragma once
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace cb {
 
-// SiLU on the tensor-core path uses the fast exponential and division
-// (relative error ~1e-6, far inside this path's TF32 tolerance).  The
+// SiLU on the tensor-core path is epilogue.cuh's (relative error a few
+// 1e-7, far inside this path's TF32 tolerance).  The
 // result is rounded to the nearest TF32 value: the MMA truncates its fp32
 // operands to TF32, which biases every product toward zero; storing
 // round-to-nearest TF32 activations lets the next tensor-core layer read
@@ -33,7 +34,7 @@ __device__ __forceinline__ float tc_epi(float acc, float sc, float bi, float r, 
   float z = fmaf(acc, sc, bi);
   if (res_mode == 1) z += r;
   if (act == 1) z = fmaxf(z, 0.0f);
-  if (act == 2) z = __fdividef(z, 1.0f + __expf(-z));
+  if (act == 2) z = silu(z);
   if (res_mode == 2) z += r;
   return round_tf32(z);
 }
@@ -46,7 +47,7 @@ __device__ __forceinline__ float tc_epi_t(float acc, float sc, float bi, float r
   float z = fmaf(acc, sc, bi);
   if constexpr (RES == 1) z += r;
   if constexpr (ACT == 1) z = fmaxf(z, 0.0f);
-  if constexpr (ACT == 2) z = __fdividef(z, 1.0f + __expf(-z));
+  if constexpr (ACT == 2) z = silu(z);
   if constexpr (RES == 2) z += r;
   return round_tf32(z);
 }
@@ -57,7 +58,7 @@ template <int ACT, int RES>
 __device__ __forceinline__ float tc_epi_post(float z, float r) {
   if constexpr (RES == 1) z += r;
   if constexpr (ACT == 1) z = fmaxf(z, 0.0f);
-  if constexpr (ACT == 2) z = __fdividef(z, 1.0f + __expf(-z));
+  if constexpr (ACT == 2) z = silu(z);
   if constexpr (RES == 2) z += r;
   return round_tf32(z);
 }
