@@ -916,10 +916,15 @@ cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, i
   const int policy = g_policy.load();
   if (!is_f32(x)) return pointwise_bf16_views(x, y, kh, stride, pad) ? CB_PATH_POINTWISE : static_cast<cb_path>(0);
   {
+    // a measured plan for the shape, unless a plan override is set (an
+    // explicit override wins over the tuner's table)
+    const Tuning tu = tuning();
+    const bool forced = tu.halo.co || tu.halo.cm || tu.halo.nb || tu.halo.split || tu.halo.tps || tu.halo.sub ||
+                        tu.halo.res >= 0 || tu.igemm_force[0] || tu.igemm_blocks >= 0;
     ConvPlan cp;
     const bool tc_views = policy != 1 && x->layout == CB_LAYOUT_NHWC && aligned16(x->data) && strides_mult4(x) &&
                           x->n <= 65535 && x->w <= 65535 && x->h <= 65535 && encode_tiled() && encode_im2col();
-    if (tc_views && tuned_plan(conv_key(x, y, kh, stride, pad), &cp) &&
+    if (tc_views && !forced && tuned_plan(conv_key(x, y, kh, stride, pad), &cp) &&
         (cp.path == CB_PATH_TC_HALO || cp.path == CB_PATH_TC_HALO_CM || cp.path == CB_PATH_TC_IM2COL)) {
       if (plan) *plan = cp.halo;
       if (im) *im = cp.im;

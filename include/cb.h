@@ -433,8 +433,9 @@ int cb_autotune_entries(void);
  *   CB_IGEMM_TRACE, CB_SPAN_SLOT   CTA timelines (trace builds only)
  * and `value` its setting (NULL or "" restores the default).  Each knob
  * starts from the environment variable of the same name, read once per
- * process; only this call changes it afterwards.  Plans recorded by
- * cb_autotune_conv still take precedence for their shapes.  Process-wide
+ * process; only this call changes it afterwards.  While a plan override of
+ * the tensor-core kernels is set (CB_HALO_FORCE, CB_IGEMM_FORCE,
+ * CB_IGEMM_BLOCKS), it wins over the plans cb_autotune_conv recorded.  Process-wide
  * and thread-safe; an override applies to calls made after it returns.
  * Returns CB_ERR_INVALID_ARG for an unknown name.
  */

@@ -30,6 +30,15 @@ from gpu_util import TOL_FP32, TOL_TF32, rel_err, sync_check, to_dev
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
+@pytest.fixture(autouse=True)
+def fresh_tuning_table():
+    """These tests tune plans as the benchmark does; the table is process-wide, so it is cleared
+    before and after each of them."""
+    cb.autotune_clear()
+    yield
+    cb.autotune_clear()
+
+
 def _tol(ci, co, k, stride, groups=1):
     return TOL_TF32 if cb.layer_uses_tensor_cores(ci, co, k, stride, groups) else TOL_FP32
 
