@@ -326,6 +326,7 @@ class DepthwiseWorkload(Workload):
 class DenseWorkload(Workload):
     unit = "TFLOP/s"
     dominant = "256-256@20_s1"
+    bf16 = False
 
     def __init__(self, torch, device, batch=16):
         from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
@@ -333,21 +334,29 @@ class DenseWorkload(Workload):
         self.torch, self.batch = torch, batch
         self.layers = []
         self.launches = []
-        for (ci, co, H, s) in synthetic.DENSE_SWEEP:
+        dt = torch.bfloat16 if self.bf16 else torch.float32
+        eb = 2 if self.bf16 else 4
+        # bf16 storage: the tensor-core layers (the 3-channel stem has no bf16 kernel)
+        sweep = synthetic.DENSE_SWEEP[1:] if self.bf16 else synthetic.DENSE_SWEEP
+        for (ci, co, H, s) in sweep:
             x, w, bn = synthetic.dense_layer(ci, co, H, N=batch, k=3)
-            L = ConvBnAct(w, bn, s, 1, cb.ACT_SILU, device=device)
+            L = ConvBnAct(w, bn, s, 1, cb.ACT_SILU, device=device, dtype=dt)
             OH, OW = L.out_hw(H, H)
-            rec = {"x_host": x, "w": w, "bn": bn, "s": s, "x": _t(torch, x, device),
-                   "y": torch.empty(batch, OH, OW, co, device=device), "L": L}
+            xt = torch.from_numpy(x).to(dt)
+            rec = {"x_host": xt.float().numpy(), "x_pin_src": xt, "w": w, "bn": bn, "s": s, "x": xt.to(device),
+                   "y": torch.empty(batch, OH, OW, co, dtype=dt, device=device), "L": L}
             if AUTOTUNE:
                 L.autotune(rec["x"], rec["y"])
             self.layers.append(rec)
             name = f"{ci}-{co}@{H}_s{s}"
             kname, bound = kernel_of(cb, rec["x"], rec["y"], 3, s, 1)
+            tc = L.tc_weights
             self.launches.append(Launch(name, (lambda r: lambda st: r["L"](r["x"], r["y"], stream=st))(rec),
-                                        workloads.conv_layer(batch, H, H, ci, co, 3, s, 1), kname, bound))
-        self.config = {"workload": f"dense 3x3 + BN + SiLU sweep, NHWC fp32 storage, TF32 tensor cores, "
-                                   f"batch {batch}",
+                                        workloads.conv_layer(batch, H, H, ci, co, 3, s, 1, act_bytes=eb,
+                                                             w_bytes=eb if tc else 4), kname, bound))
+        storage = ("NHWC bf16 storage, bf16 tensor-core operands (fp32 accumulate), the 7 tensor-core layers"
+                   if self.bf16 else "NHWC fp32 storage, TF32 tensor cores")
+        self.config = {"workload": f"dense 3x3 + BN + SiLU sweep, {storage}, batch {batch}",
                        "batch": batch, "l2": "warm (per-layer working sets 15-180 MB; steps run back to back)",
                        "autotune": AUTOTUNE}
 
@@ -355,10 +364,10 @@ class DenseWorkload(Workload):
         t = self.torch
         h2d = d2h = 0
         for r in self.layers:
-            r["x_pin"] = t.from_numpy(r["x_host"]).pin_memory()
-            r["y_pin"] = t.empty(tuple(r["y"].shape), pin_memory=True)
-            h2d += r["x_pin"].numel() * 4
-            d2h += r["y_pin"].numel() * 4
+            r["x_pin"] = r["x_pin_src"].pin_memory()
+            r["y_pin"] = t.empty(tuple(r["y"].shape), dtype=r["y"].dtype, pin_memory=True)
+            h2d += r["x_pin"].numel() * r["x_pin"].element_size()
+            d2h += r["y_pin"].numel() * r["y_pin"].element_size()
         return h2d, d2h
 
     def e2e_step(self, stream):
@@ -374,6 +383,11 @@ class DenseWorkload(Workload):
         for r in self.layers:
             oracle.conv_bn_act(r["x_host"][:n], r["w"], r["bn"], stride=r["s"], pad=1, act=oracle.ACT_SILU)
         return time.perf_counter() - t0, self.step_units() * n / self.batch, f"{n} of {self.batch} images per layer"
+
+
+class DenseBf16Workload(DenseWorkload):
+    """The tensor-core layers of the dense sweep with bf16 storage and bf16 MMA operands."""
+    bf16 = True
 
 
 class MnistWorkload(Workload):
@@ -682,8 +696,8 @@ class PointwiseBf16Workload(PointwiseWorkload):
 
 
 WORKLOADS = {"depthwise": DepthwiseWorkload, "depthwise_bf16": DepthwiseBf16Workload, "pointwise": PointwiseWorkload,
-             "pointwise_bf16": PointwiseBf16Workload, "dense": DenseWorkload, "mnist": MnistWorkload,
-             "yolo": YoloWorkload, "preprocess": PreprocessWorkload}
+             "pointwise_bf16": PointwiseBf16Workload, "dense": DenseWorkload, "dense_bf16": DenseBf16Workload,
+             "mnist": MnistWorkload, "yolo": YoloWorkload, "preprocess": PreprocessWorkload}
 
 
 # ------------------------------------------------------------ arms
@@ -932,7 +946,9 @@ def measure(torch, wl, device, stream, args, steps, warmup, min_timed_s, world, 
 # beside the headline one: (key, workload, batch).
 EXTRA_CONFIGS = (("cfg0_mnist_b64", "mnist", 64), ("cfg1_depthwise_b64", "depthwise", 64),
                  ("cfg2_dense_b16", "dense", 16), ("cfg2_dense_b1", "dense", 1),
-                 ("cfg3_yolo_b1", "yolo", 1), ("cfg4_preprocess_stem_b32", "preprocess", 32))
+                 ("cfg3_yolo_b1", "yolo", 1), ("cfg4_preprocess_stem_b32", "preprocess", 32),
+                 ("bf16_dense_b16", "dense_bf16", 16), ("bf16_depthwise_b64", "depthwise_bf16", 64),
+                 ("bf16_pointwise_b32", "pointwise_bf16", 32))
 
 
 def run_ours(args):

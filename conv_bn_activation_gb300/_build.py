@@ -81,7 +81,7 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
         if force:
             for o in glob.glob(os.path.join(BUILD, "*.o")):
                 os.remove(o)
-        with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+        with ThreadPoolExecutor(max_workers=max(1, min(os.cpu_count() or 8, len(srcs)))) as ex:
             objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
         if force or _stale(LIB, objs):
             tmp = LIB + f".tmp{os.getpid()}"

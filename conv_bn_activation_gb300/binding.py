@@ -31,7 +31,7 @@ EXPORTED = (
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_layer_uses_tensor_cores",
     "cb_dw_separable_block_static", "cb_conv_path", "cb_debug_timeout_probe", "cb_autotune_conv",
     "cb_autotune_clear", "cb_autotune_entries", "cb_preprocess_stem_u8", "cb_dw_separable_block_fused",
-    "cb_set_tuning", "cb_last_launch", "cb_debug_sample_coords",
+    "cb_set_tuning", "cb_last_launch", "cb_debug_sample_coords", "cb_convert_weights_bf16",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
@@ -87,6 +87,7 @@ def load():
                 "cb_set_kernel_policy": [I],
                 "cb_get_kernel_policy": [],
                 "cb_round_weights_tf32": [P, LL, P],
+                "cb_convert_weights_bf16": [P, LL, P],
                 "cb_layer_uses_tensor_cores": [I, I, I, I, I],
                 "cb_conv_path": [T, T, I, I, I, I],
                 "cb_debug_timeout_probe": [I, P],
@@ -216,6 +217,15 @@ def round_weights_tf32(w):
     out = np.empty_like(a)
     _check(load().cb_round_weights_tf32(a.ctypes.data, a.size, out.ctypes.data), "cb_round_weights_tf32")
     return out
+
+
+def convert_weights_bf16(w):
+    """cb_convert_weights_bf16 on a host array (any shape) -> torch.bfloat16 CPU tensor of the same shape."""
+    import torch
+    a = np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _check(load().cb_convert_weights_bf16(a.ctypes.data, a.size, out.ctypes.data), "cb_convert_weights_bf16")
+    return torch.from_numpy(out.view(np.int16)).view(torch.bfloat16)
 
 
 def layer_uses_tensor_cores(ci, co, k, stride=1, groups=1) -> bool:

@@ -157,19 +157,20 @@ CUresult tiled_map(CUtensorMap* out, int rank, const void* ptr, const cuuint64_t
   return r;
 }
 
-// fp32 4-D im2col map (same fixed options as tiled_map).
+// 4-D im2col map (same fixed options as tiled_map).
 CUresult im2col_map(CUtensorMap* out, const void* ptr, const cuuint64_t* dims, const cuuint64_t* strides,
                     const int* lower, const int* upper, cuuint32_t channels, cuuint32_t pixels,
-                    const cuuint32_t* estr, CUtensorMapSwizzle swz) {
+                    const cuuint32_t* estr, CUtensorMapSwizzle swz,
+                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_FLOAT32) {
   cuuint64_t d[4], st[3];
   cuuint32_t e[4];
   int lo[2] = {lower[0], lower[1]}, up[2] = {upper[0], upper[1]};
   for (int i = 0; i < 4; ++i) d[i] = dims[i], e[i] = estr[i];
   for (int i = 0; i < 3; ++i) st[i] = strides[i];
-  const int kind = 1;
+  const int kind = 1 + 16 * static_cast<int>(dtype);
   const std::string key = map_key(kind, ptr, d, st, lo, up, channels, pixels, e, swz);
   if (cached_map(key, out)) return CUDA_SUCCESS;
-  const CUresult r = encode_im2col()(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), d, st, lo, up,
+  const CUresult r = encode_im2col()(out, dtype, 4, const_cast<void*>(ptr), d, st, lo, up,
                                      channels, pixels, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r == CUDA_SUCCESS) store_map(key, *out);
@@ -497,7 +498,8 @@ struct HaloPlan {
   int stride = 1;      // 2: four phase tiles per chunk
   int blk_w = 0, n_blk = 1, wp = 0;  // column blocks and the padded width of the pixel numbering
   int sub = 1;
-  bool resident = false;  // weights loaded once per CTA (one chunk, one channel tile)         // 128-pixel sub-tiles per tile sharing one halo copy
+  bool resident = false;  // weights loaded once per CTA (one chunk, one channel tile)
+  int eb = 4;             // bytes per element of x, w and y: 4 (fp32, TF32 MMAs) or 2 (bf16)
   size_t smem = 0;
   double cost = 0;     // the cost model's cycles per CTA
 };
@@ -518,7 +520,7 @@ struct ConvPlan {
   ImPlan im;
 };
 struct ConvKey {
-  int dev, policy, n, h, w, ci, co, kh, stride, pad;
+  int dev, policy, n, h, w, ci, co, kh, stride, pad, dtype;
   bool operator==(const ConvKey& o) const { return std::memcmp(this, &o, sizeof(ConvKey)) == 0; }
 };
 struct ConvKeyHash {
@@ -538,6 +540,7 @@ ConvKey conv_key(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int
   cudaGetDevice(&k.dev);
   k.policy = g_policy.load();
   k.n = x->n, k.h = x->h, k.w = x->w, k.ci = x->c, k.co = y->c, k.kh = kh, k.stride = stride, k.pad = pad;
+  k.dtype = static_cast<int>(x->dtype);
   return k;
 }
 
@@ -611,8 +614,13 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
   a.Cout = Co;
   a.kw = k;
   a.taps = k * k;
-  const int kc = Ci <= 8 ? 8 : (Ci <= 16 ? 16 : 32);  // channels per K step: no padding channels for 8 / 16
-  a.num_kc = (Ci + kc - 1) / kc;
+  // K step rows of kc x 4 bytes: kc fp32 or 2 kc bf16 channels (no padding
+  // channels for 8 / 16-channel fp32 or 16 / 32-channel bf16 layers)
+  const int eb = is_f32(x) ? 4 : 2, cpu = 4 / eb;
+  const int kc = Ci <= 8 * cpu ? 8 : (Ci <= 16 * cpu ? 16 : 32);
+  const int chan = kc * cpu;
+  a.num_kc = (Ci + chan - 1) / chan;
+  a.bf16 = eb == 2 ? 1 : 0;
   a.k_iters = a.taps * a.num_kc;
   a.stride = stride;
   a.pad = pad;
@@ -675,36 +683,34 @@ cb_status run_igemm(const cb_tensor* x, const float* w, const Epilogue& ep, int 
                  a.M, Ci, Co, k, stride, bn, kc, n_tiles, a.m_tiles, a.stages, grid, a.blk_h, a.blk_w);
 
   CUtensorMap amap, bmap;
+  const CUtensorMapDataType dt = eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapSwizzle swz = kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                            : CU_TENSOR_MAP_SWIZZLE_32B;
   {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(x->w), static_cast<cuuint64_t>(x->h),
                           static_cast<cuuint64_t>(x->n)};
-    cuuint64_t strides[3] = {static_cast<cuuint64_t>(x->stride_w) * 4, static_cast<cuuint64_t>(x->stride_h) * 4,
-                             static_cast<cuuint64_t>(x->stride_n) * 4};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(x->stride_w) * eb, static_cast<cuuint64_t>(x->stride_h) * eb,
+                             static_cast<cuuint64_t>(x->stride_n) * eb};
     int lower[2] = {-pad, -pad};
     int upper[2] = {pad - (k - 1), pad - (k - 1)};
     cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(stride), static_cast<cuuint32_t>(stride), 1};
-    const CUtensorMapSwizzle swz = kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                   : kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                              : CU_TENSOR_MAP_SWIZZLE_32B;
     CUresult r;
     if (a.blk_w) {
-      cuuint32_t box[4] = {static_cast<cuuint32_t>(kc), static_cast<cuuint32_t>(stride * a.blk_w),
+      cuuint32_t box[4] = {static_cast<cuuint32_t>(chan), static_cast<cuuint32_t>(stride * a.blk_w),
                            static_cast<cuuint32_t>(stride * a.blk_h), 1};
-      r = tiled_map(&amap, 4, x->data, dims, strides, box, estr, swz);
+      r = tiled_map(&amap, 4, x->data, dims, strides, box, estr, swz, dt);
     } else {
-      r = im2col_map(&amap, x->data, dims, strides, lower, upper, static_cast<cuuint32_t>(kc), 128, estr, swz);
+      r = im2col_map(&amap, x->data, dims, strides, lower, upper, static_cast<cuuint32_t>(chan), 128, estr, swz, dt);
     }
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(k * k), static_cast<cuuint64_t>(Co)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(Ci) * 4, static_cast<cuuint64_t>(k * k) * Ci * 4};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(kc), 1, static_cast<cuuint32_t>(bn)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(Ci) * eb, static_cast<cuuint64_t>(k * k) * Ci * eb};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(chan), 1, static_cast<cuuint32_t>(bn)};
     cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapSwizzle swz = kc == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                   : kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                              : CU_TENSOR_MAP_SWIZZLE_32B;
-    CUresult r = tiled_map(&bmap, 3, w, dims, strides, box, estr, swz);
+    CUresult r = tiled_map(&bmap, 3, w, dims, strides, box, estr, swz, dt);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   cudaError_t e = launch_igemm(amap, bmap, a, bn, kc, grid, smem, s);
@@ -739,9 +745,16 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
   // 32-channel chunks (128-byte rows); 16-channel chunks (64-byte rows) for
   // Ci % 32 == 16 and at stride 2 (four phase tiles per chunk), in the
   // pixel-major 128 x {32, 64, 128} tiles
-  const int kc = (stride == 1 && Ci % 32 == 0) ? 32 : Ci % 16 == 0 ? 16 : (stride == 1 && Ci % 8 == 0) ? 8 : 0;
+  // kc counts a chunk's pixel row in 4-byte units (32: 128-byte rows): kc
+  // fp32 channels, or 2 kc bf16 channels
+  const int eb = is_f32(x) ? 4 : 2;
+  const int cpu = 4 / eb;  // channels per 4-byte unit
+  const int kc = (stride == 1 && Ci % (32 * cpu) == 0) ? 32
+                 : Ci % (16 * cpu) == 0                ? 16
+                 : (stride == 1 && Ci % (8 * cpu) == 0) ? 8
+                                                         : 0;
   if (kc == 0) return false;
-  const int num_kc = Ci / kc;
+  const int num_kc = Ci / (kc * cpu);
   constexpr size_t kSmemMax = 227 * 1024;
   struct Shape {
     int px, co;
@@ -873,6 +886,7 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
     }
   }
   if (plan.px == 0) return false;
+  plan.eb = eb;
   *out = plan;
   return true;
 }
@@ -912,9 +926,23 @@ bool pointwise_bf16_views(const cb_tensor* x, const cb_tensor* y, int kh, int st
          x->layout == CB_LAYOUT_NHWC && aligned16(x->data) && aligned16(y->data) && mult8(x) && strides_mult4(y);
 }
 
+// bf16 storage on the tensor cores (kind::f16 MMAs): the tensor-core shape
+// rule with whole 16-byte rows per TMA element row (Ci % 8 == 0, x strides
+// multiples of 8 elements), NHWC views with 16-byte aligned data, y strides
+// multiples of 4 elements (8-byte stores of 4 channels).
+bool tc_bf16_views(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad) {
+  auto mult8 = [](const cb_tensor* t) { return t->stride_n % 8 == 0 && t->stride_h % 8 == 0 && t->stride_w % 8 == 0; };
+  return tc_shape(x->c, y->c, kh, stride, pad) && x->c % 8 == 0 && x->layout == CB_LAYOUT_NHWC &&
+         aligned16(x->data) && mult8(x) && aligned16(y->data) && strides_mult4(y) && x->n <= 65535 &&
+         x->w <= 65535 && x->h <= 65535 && encode_tiled() && encode_im2col();
+}
+
 cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan, ImPlan* im) {
   const int policy = g_policy.load();
-  if (!is_f32(x)) return pointwise_bf16_views(x, y, kh, stride, pad) ? CB_PATH_POINTWISE : static_cast<cb_path>(0);
+  if (!is_f32(x)) {
+    if (pointwise_bf16_views(x, y, kh, stride, pad)) return CB_PATH_POINTWISE;
+    if (!tc_bf16_views(x, y, kh, stride, pad)) return static_cast<cb_path>(0);
+  }
   {
     // a measured plan for the shape, unless a plan override is set (an
     // explicit override wins over the tuner's table)
@@ -931,14 +959,16 @@ cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, i
       return cp.path;
     }
   }
-  if (stem_path(x, y, kh, stride, pad)) return CB_PATH_STEM;
-  if (pointwise_shape(x->c, y->c, kh, stride, pad) && x->layout == CB_LAYOUT_NHWC && aligned16(x->data) &&
-      strides_mult4(x) && aligned16(y->data) && strides_mult4(y))
-    return CB_PATH_POINTWISE;
-  const bool tc_ok = tc_shape(x->c, y->c, kh, stride, pad) && x->layout == CB_LAYOUT_NHWC &&
-                     aligned16(x->data) && strides_mult4(x) && x->n <= 65535 && x->w <= 65535 &&
-                     x->h <= 65535 && encode_tiled() && encode_im2col();
-  if (!tc_ok) return CB_PATH_DIRECT;
+  if (is_f32(x)) {
+    if (stem_path(x, y, kh, stride, pad)) return CB_PATH_STEM;
+    if (pointwise_shape(x->c, y->c, kh, stride, pad) && x->layout == CB_LAYOUT_NHWC && aligned16(x->data) &&
+        strides_mult4(x) && aligned16(y->data) && strides_mult4(y))
+      return CB_PATH_POINTWISE;
+    const bool tc_ok = tc_shape(x->c, y->c, kh, stride, pad) && x->layout == CB_LAYOUT_NHWC &&
+                       aligned16(x->data) && strides_mult4(x) && x->n <= 65535 && x->w <= 65535 &&
+                       x->h <= 65535 && encode_tiled() && encode_im2col();
+    if (!tc_ok) return CB_PATH_DIRECT;
+  }
   if (policy == 0 && kh == 3 && pad == 1) {
     DeviceInfo* dev = nullptr;
     HaloPlan tmp;
@@ -970,7 +1000,9 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
   a.Wp = plan.wp;
   a.Cout = Co;
   a.kc = plan.kc;
-  a.num_kc = Ci / plan.kc;
+  const int chan = plan.kc * 4 / plan.eb;  // channels per chunk
+  a.num_kc = Ci / chan;
+  a.bf16 = plan.eb == 2 ? 1 : 0;
   a.px_tiles_per_blk = (a.OH * a.Wp + plan.px - 1) / plan.px;
   a.sub = plan.sub;
   a.tiles_per_blk = (a.px_tiles_per_blk + plan.sub - 1) / plan.sub;
@@ -1006,35 +1038,34 @@ cb_status run_igemm_halo(const cb_tensor* x, const float* w, const Epilogue& ep,
                  a.rows, a.halo_bytes,
                  a.m_tiles * a.n_tiles, plan.grid, plan.smem);
   CUtensorMap xmap, wmap;
+  const cuuint64_t eb = static_cast<cuuint64_t>(plan.eb);
+  const CUtensorMapDataType dt = plan.eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapSwizzle swz = plan.kc == 32   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : plan.kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                 : CU_TENSOR_MAP_SWIZZLE_32B;
   {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(x->w), static_cast<cuuint64_t>(x->h),
                           static_cast<cuuint64_t>(x->n)};
-    cuuint64_t strides[3] = {static_cast<cuuint64_t>(x->stride_w) * 4, static_cast<cuuint64_t>(x->stride_h) * 4,
-                             static_cast<cuuint64_t>(x->stride_n) * 4};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(x->stride_w) * eb, static_cast<cuuint64_t>(x->stride_h) * eb,
+                             static_cast<cuuint64_t>(x->stride_n) * eb};
     // stride 2: each phase tile traverses 2 Wp columns and 2 rows rows of the
     // input with element strides 2
     const cuuint32_t st = static_cast<cuuint32_t>(plan.stride);
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(plan.kc), st * static_cast<cuuint32_t>(a.Wp),
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(chan), st * static_cast<cuuint32_t>(a.Wp),
                          st * static_cast<cuuint32_t>(a.rows), 1};
     cuuint32_t estr[4] = {1, st, st, 1};
-    CUresult r = tiled_map(&xmap, 4, x->data, dims, strides, box, estr,
-                           plan.kc == 32   ? CU_TENSOR_MAP_SWIZZLE_128B
-                           : plan.kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                           : CU_TENSOR_MAP_SWIZZLE_32B);
+    CUresult r = tiled_map(&xmap, 4, x->data, dims, strides, box, estr, swz, dt);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   {
     // OHWI weights viewed as (Ci, Co, tap): a box of plan.tps taps lands as
-    // plan.tps consecutive [co x 32] slices
+    // plan.tps consecutive [co x chunk] slices
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(Ci), static_cast<cuuint64_t>(Co), 9};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(9) * Ci * 4, static_cast<cuuint64_t>(Ci) * 4};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(plan.kc), static_cast<cuuint32_t>(plan.co),
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(9) * Ci * eb, static_cast<cuuint64_t>(Ci) * eb};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(chan), static_cast<cuuint32_t>(plan.co),
                          static_cast<cuuint32_t>(plan.tps)};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = tiled_map(&wmap, 3, w, dims, strides, box, estr,
-                           plan.kc == 32   ? CU_TENSOR_MAP_SWIZZLE_128B
-                           : plan.kc == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                           : CU_TENSOR_MAP_SWIZZLE_32B);
+    CUresult r = tiled_map(&wmap, 3, w, dims, strides, box, estr, swz, dt);
     if (r != CUDA_SUCCESS) return CB_ERR_UNSUPPORTED;
   }
   cudaError_t e = launch_igemm_halo(xmap, wmap, a, plan.px, plan.co, plan.cm, plan.grid, plan.smem, s);
@@ -1189,6 +1220,23 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out) {
   return CB_OK;
 }
 
+cb_status cb_convert_weights_bf16(const float* w, long long n, void* out) {
+  if (!w || !out || n < 0) return CB_ERR_INVALID_ARG;
+  uint16_t* o = static_cast<uint16_t*>(out);
+  for (long long i = 0; i < n; ++i) {
+    uint32_t b;
+    std::memcpy(&b, &w[i], 4);
+    if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x007FFFFFu) != 0) {
+      o[i] = static_cast<uint16_t>((b >> 16) | 0x0040u);  // NaN stays a (quiet) NaN
+      continue;
+    }
+    // round to nearest, ties to even, on the upper 16 bits (an overflow carries into inf)
+    b += 0x7FFFu + ((b >> 16) & 1u);
+    o[i] = static_cast<uint16_t>(b >> 16);
+  }
+  return CB_OK;
+}
+
 namespace {
 // Argument checks of cb_conv_bn_act (no launch).  *empty: nothing to compute.
 cb_status validate_conv(const cb_tensor* x, const float* w, const float* scale, const float* bias, int kh, int kw,
@@ -1207,9 +1255,12 @@ cb_status validate_conv(const cb_tensor* x, const float* w, const float* scale, 
   const bool depthwise = groups == x->c && groups == y->c && groups > 1;
   if (!depthwise && groups != 1) return CB_ERR_UNSUPPORTED;
   if (x->dtype != y->dtype) return CB_ERR_INVALID_ARG;
-  // bf16 storage: the depthwise kernel and the pointwise kernel's 1x1 shapes
+  // bf16 storage: the depthwise kernel, the pointwise kernel's 1x1 shapes and
+  // the tensor-core shapes
   if (!is_f32(x) && !depthwise &&
-      (g_policy.load() == 1 || kh != 1 || stride != 1 || pad != 0 || !pointwise_small_ok(x->c, y->c, true)))
+      (g_policy.load() == 1 ||
+       !((kh == 1 && stride == 1 && pad == 0 && pointwise_small_ok(x->c, y->c, true)) ||
+         (tc_shape(x->c, y->c, kh, stride, pad) && x->c % 8 == 0))))
     return CB_ERR_UNSUPPORTED;
   if (res_mode != CB_RES_NONE) {
     if (!view_ok(residual) || residual->layout != CB_LAYOUT_NHWC || residual->dtype != y->dtype)
@@ -1235,12 +1286,13 @@ cb_status launch_conv(const cb_tensor* x, const float* w, const float* scale, co
   const Epilogue ep = make_epilogue(scale, bias, act, residual, res_mode);
   if (depthwise) return run_depthwise(x, w, ep, stride, pad, y, s);
   if (!is_f32(x)) {
-    // bf16 storage (a pointwise shape, checked in validation): aligned views
-    // and operands, else no kernel takes it
-    if (!pointwise_bf16_views(x, y, kh, stride, pad) || !aligned16(w) || !aligned16(scale) || !aligned16(bias) ||
+    // bf16 storage (a pointwise or tensor-core shape, checked in
+    // validation): aligned views and operands, else no kernel takes it
+    if (!aligned16(w) || !aligned16(scale) || !aligned16(bias) ||
         (res_mode != CB_RES_NONE && (!aligned16(residual->data) || !strides_mult4(residual))))
       return CB_ERR_ALIGNMENT;
-    return run_pointwise(x, w, ep, residual, y, s);
+    if (pointwise_bf16_views(x, y, kh, stride, pad)) return run_pointwise(x, w, ep, residual, y, s);
+    if (!tc_bf16_views(x, y, kh, stride, pad)) return CB_ERR_ALIGNMENT;
   }
   HaloPlan plan;
   ImPlan im;

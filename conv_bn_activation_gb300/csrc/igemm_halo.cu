@@ -97,6 +97,9 @@ cudaError_t launch_igemm_halo_kc16(const CUtensorMap& xmap, const CUtensorMap& w
 cudaError_t launch_igemm_halo_kc8(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int co,
                                   int grid, size_t smem, cudaStream_t s);
 
+cudaError_t launch_igemm_halo_bf16(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px,
+                                   int co, bool cm, int grid, size_t smem, cudaStream_t s);
+
 cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
                               bool cm, int grid, size_t smem, cudaStream_t s) {
   if (a.nb_stages < (a.w_resident ? 1 : 2) || a.nb_stages > 16) return cudaErrorInvalidValue;
@@ -117,6 +120,7 @@ cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, 
                                                 static_cast<size_t>(a.nb_stages) * a.taps_per_stage * co * a.kc * 4)
       return cudaErrorInvalidValue;
   }
+  if (a.bf16) return launch_igemm_halo_bf16(xmap, wmap, a, px, co, cm, grid, smem, s);
   if (a.kc == 16) return !cm && px == 128 ? launch_igemm_halo_kc16(xmap, wmap, a, co, grid, smem, s) : cudaErrorInvalidValue;
   if (a.kc == 8) return !cm && px == 128 ? launch_igemm_halo_kc8(xmap, wmap, a, co, grid, smem, s) : cudaErrorInvalidValue;
   if (a.kc != 32) return cudaErrorInvalidValue;

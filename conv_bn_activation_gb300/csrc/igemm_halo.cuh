@@ -82,12 +82,15 @@ __host__ __device__ constexpr int halo_tmem_cols(int acc_cols) {
   return halo_naccs(acc_cols) * acc_cols <= 128 ? 128 : halo_naccs(acc_cols) * acc_cols <= 256 ? 256 : 512;
 }
 
-template <int PX, int CO, bool CM, int KC = kHaloKc>
+template <int PX, int CO, bool CM, int KC = kHaloKc, typename T = float>
 __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                      const __grid_constant__ CUtensorMap wmap,
                                                                      const HaloArgs a) {
-  static_assert(KC == 32 || KC == 16 || KC == 8, "channels per chunk");
-  constexpr int kRowBytes = KC * 4;  // one pixel's chunk: 128, 64 or 32 bytes, swizzled to match
+  static_assert(KC == 32 || KC == 16 || KC == 8, "row bytes / 4 per chunk");
+  // KC sizes a chunk in 4-byte units: one pixel's chunk is kRowBytes = 128,
+  // 64 or 32 bytes (swizzled to match), i.e. KC fp32 or 2 KC bf16 channels.
+  constexpr int kRowBytes = KC * 4;
+  constexpr int kChan = kRowBytes / static_cast<int>(sizeof(T));  // channels per chunk
   static_assert(CM ? (PX == 256 && CO == 128) : (PX == 128 && (CO == 32 || CO == 64 || CO == 128 || CO == 256)),
                 "tile shape");
   const unsigned long long t_start = a.trace ? trace_globaltimer() : 0;
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   constexpr int kTapBytes = CO * KC * 4;  // one tap's weight slice
   const int tps = a.taps_per_stage;            // taps per weight-ring stage: 1, 3 or 9 (one copy each)
   const int kBBytes = tps * kTapBytes;
-  constexpr uint32_t kIdesc = CM ? idesc_tf32(CO, PX) : idesc_tf32(PX, CO);
+  constexpr uint32_t kIdesc = CM ? idesc_for<T>(CO, PX) : idesc_for<T>(PX, CO);
   // Epilogue split of a tile between the two groups of four warps:
   // pixel-major tiles of 32 channels alternate between the groups, wider
   // ones are split into column halves; channel-major tiles give the groups
@@ -199,11 +202,11 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
             }
             mbar_arrive_expect_tx(&hfull[h], halo_tx);
             if (a.stride == 1) {
-              tma_load_4d(sHalo + h * a.halo_bytes, &xmap, &hfull[h], kc * KC, x0, y_lo - 1, n_img);
+              tma_load_4d(sHalo + h * a.halo_bytes, &xmap, &hfull[h], kc * kChan, x0, y_lo - 1, n_img);
             } else {
               // four phase tiles: input rows 2i + py, columns 2j + px (element strides 2)
               for (int ph = 0; ph < 4; ++ph)
-                tma_load_4d(sHalo + h * a.halo_bytes + ph * a.phase_bytes, &xmap, &hfull[h], kc * KC,
+                tma_load_4d(sHalo + h * a.halo_bytes + ph * a.phase_bytes, &xmap, &hfull[h], kc * kChan,
                             2 * x0 + (ph & 1), 2 * (y_lo - 1) + (ph >> 1), n_img);
             }
             issued |= 1u << h;
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
               // taps, loaded once into the single stage and kept
               if (lane == 1 && tile == tile0) {
                 mbar_arrive_expect_tx(&bfull[0], static_cast<uint32_t>(kBBytes));
-                tma_load_3d(sB, &wmap, &bfull[0], kc * KC, n_tile * CO, 0);
+                tma_load_3d(sB, &wmap, &bfull[0], kc * kChan, n_tile * CO, 0);
                 issued |= 1u;
               }
               continue;
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
               }
               mbar_arrive_expect_tx(&bfull[s], static_cast<uint32_t>(kBBytes));
               // weights viewed as (Ci, Co, tap): one box of tps taps lands as tps [CO x 32] slices
-              tma_load_3d(sB + s * kBBytes, &wmap, &bfull[s], kc * KC, n_tile * CO, tap);
+              tma_load_3d(sB + s * kBBytes, &wmap, &bfull[s], kc * kChan, n_tile * CO, tap);
               tr.add(tr_cta && lane == 1);
               issued |= 1u << s;
               last_parity = (last_parity & ~(1u << s)) | (bphase << s);
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
 #pragma unroll
             for (int kk = 0; kk < KC / 8; ++kk) {
               const uint64_t xd = make_desc(xt + i * kSubOff + 2 * kk), wdsc = make_desc(wt + 2 * kk);
-              mma_tf32(d_tmem[i], CM ? wdsc : xd, CM ? xd : wdsc, kIdesc, (tap == 0 && kk == 0 && first) ? 0u : 1u);
+              mma_op<T>(d_tmem[i], CM ? wdsc : xd, CM ? xd : wdsc, kIdesc, (tap == 0 && kk == 0 && first) ? 0u : 1u);
             }
           }
           if (tap % TPS == TPS - 1 && !resident) {
@@ -494,13 +497,13 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
                 TileStore<32>::consts(lane, n_tile * CO + own0 + i * 32, a.Cout, vec, a.ep);
             TileStore<32>::stage(stage_buf, lane, v);
             __syncwarp();
-            TileStore<32>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+            TileStore<32>::template write<T>(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
           } else {
             pixel_offsets(q0 + own0 + i * 32 + lane, yoff, roff);
             const TileStore<32>::Consts k = TileStore<32>::consts(lane, n_tile * CO + q * 32, a.Cout, vec, a.ep);
             TileStore<32>::stage_columns(stage_buf, lane, v);
             __syncwarp();
-            TileStore<32>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+            TileStore<32>::template write<T>(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
           }
           tr.add(tr_on);
         }
@@ -531,7 +534,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
           __syncwarp();  // the previous chunk's readers are done with the staging buffer
           TileStore<32>::stage(stage_buf, lane, v);
           __syncwarp();
-          TileStore<32>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+          TileStore<32>::template write<T>(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
           k = kn;
         }
       } else {
@@ -558,7 +561,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
           TileStore<32>::stage_columns(stage_buf, lane, v);
           __syncwarp();
           tr.add(tr_on);
-          TileStore<32>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+          TileStore<32>::template write<T>(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
           tr.add(tr_on);
         }
       }

@@ -44,8 +44,21 @@ size_t igemm_smem_bytes(int bn, int kc, int stages) {
          (2 * stages + 2 * 4) * sizeof(uint64_t) + 16;
 }
 
+cudaError_t launch_igemm_bf16_kc8(const CUtensorMap&, const CUtensorMap&, const IgemmArgs&, int, int, size_t,
+                                  cudaStream_t);
+cudaError_t launch_igemm_bf16_kc16(const CUtensorMap&, const CUtensorMap&, const IgemmArgs&, int, int, size_t,
+                                   cudaStream_t);
+cudaError_t launch_igemm_bf16_kc32(const CUtensorMap&, const CUtensorMap&, const IgemmArgs&, int, int, size_t,
+                                   cudaStream_t);
+
 cudaError_t launch_igemm(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int bn, int kc,
                          int grid, size_t smem, cudaStream_t s) {
+  if (a.bf16) {
+    if (kc == 32) return launch_igemm_bf16_kc32(amap, bmap, a, bn, grid, smem, s);
+    if (kc == 16) return launch_igemm_bf16_kc16(amap, bmap, a, bn, grid, smem, s);
+    if (kc == 8) return launch_igemm_bf16_kc8(amap, bmap, a, bn, grid, smem, s);
+    return cudaErrorInvalidValue;
+  }
   if (kc == 32) return launch_igemm_kc32(amap, bmap, a, bn, grid, smem, s);
   if (kc == 16) return launch_igemm_kc16(amap, bmap, a, bn, grid, smem, s);
   if (kc == 8) return launch_igemm_kc8(amap, bmap, a, bn, grid, smem, s);

@@ -67,14 +67,16 @@ __host__ __device__ constexpr int tmem_cols_for(int cols) {
   return cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
 }
 
-template <int BN, int KC>
+template <int BN, int KC, typename T = float>
 __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __grid_constant__ CUtensorMap amap,
                                                                       const __grid_constant__ CUtensorMap bmap,
                                                                       const IgemmArgs a) {
   constexpr int kABytes = igemm_a_bytes(KC);
   constexpr int kBBytes = igemm_b_bytes(BN, KC);
+  // KC sizes a K step in 4-byte units: rows of KC * 4 bytes, KC fp32 or 2 KC bf16 channels
   constexpr int kRowBytes = KC * 4;
-  constexpr uint32_t kIdesc = idesc_tf32(kTileM, BN);
+  constexpr int kChan = kRowBytes / static_cast<int>(sizeof(T));
+  constexpr uint32_t kIdesc = idesc_for<T>(kTileM, BN);
   constexpr int NACC = igemm_naccs(BN);
   constexpr uint32_t kTmemCols = tmem_cols_for(NACC * BN);
   // Epilogue split: for narrow tiles the two 4-warp groups take alternate
@@ -173,10 +175,11 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
               }
               mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(kABytes + BN * KC * 4));
               if (a.blk_w)
-                tma_load_4d(sA + stage * kABytes, &amap, &full[stage], kc * KC, w0 + off_w, h0 + off_h, n_img);
+                tma_load_4d(sA + stage * kABytes, &amap, &full[stage], kc * kChan, w0 + off_w, h0 + off_h, n_img);
               else
-                tma_load_im2col_4d(sA + stage * kABytes, &amap, &full[stage], kc * KC, w0, h0, n_img, off_w, off_h);
-              tma_load_3d(sB + stage * kBBytes, &bmap, &full[stage], kc * KC, tap, n_tile * BN);
+                tma_load_im2col_4d(sA + stage * kABytes, &amap, &full[stage], kc * kChan, w0, h0, n_img, off_w,
+                                   off_h);
+              tma_load_3d(sB + stage * kBBytes, &bmap, &full[stage], kc * kChan, tap, n_tile * BN);
               tr.add(tr_cta && lane == 0);
               issued |= 1u << stage;
               last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -220,8 +223,8 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
           const uint64_t bdesc = kmajor_swizzled_desc(smem_u32(sB + stage * kBBytes), kRowBytes);
 #pragma unroll
           for (int kk = 0; kk < KC / 8; ++kk) {
-            // advance 8 tf32 (32 bytes) along K inside the swizzled row
-            mma_tf32(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (k | kk) != 0 ? 1u : 0u);
+            // advance 32 bytes (8 tf32 or 16 bf16) along K inside the swizzled row
+            mma_op<T>(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (k | kk) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
           tr.add(tr_cta);
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
         __syncwarp();  // the previous chunk's readers are done with the staging buffer
         TileStore<CH>::stage(stage_buf, lane, v);
         __syncwarp();
-        TileStore<CH>::write(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+        TileStore<CH>::template write<T>(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
         k = kn;
       }
       tr.add(tr_on);
@@ -334,26 +337,26 @@ __global__ void __launch_bounds__(kIgemmThreads, 1) igemm_tf32_kernel(const __gr
   }
 }
 
-template <int BN, int KC>
+template <int BN, int KC, typename T>
 cudaError_t igemm_launch_bn(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int grid,
                             size_t smem, cudaStream_t s) {
-  cudaError_t e = smem_attr_once<igemm_tf32_kernel<BN, KC>>(smem);
+  cudaError_t e = smem_attr_once<igemm_tf32_kernel<BN, KC, T>>(smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(igemm_tf32_kernel<BN, KC>, dim3(grid), dim3(kIgemmThreads), smem, s, amap, bmap, a);
+  return launch_pdl(igemm_tf32_kernel<BN, KC, T>, dim3(grid), dim3(kIgemmThreads), smem, s, amap, bmap, a);
 }
 
-template <int KC>
+template <int KC, typename T = float>
 cudaError_t igemm_launch_kc(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int bn, int grid,
                             size_t smem, cudaStream_t s) {
   switch (bn) {
-    case 16: return igemm_launch_bn<16, KC>(amap, bmap, a, grid, smem, s);
-    case 32: return igemm_launch_bn<32, KC>(amap, bmap, a, grid, smem, s);
-    case 48: return igemm_launch_bn<48, KC>(amap, bmap, a, grid, smem, s);
-    case 64: return igemm_launch_bn<64, KC>(amap, bmap, a, grid, smem, s);
-    case 96: return igemm_launch_bn<96, KC>(amap, bmap, a, grid, smem, s);
-    case 128: return igemm_launch_bn<128, KC>(amap, bmap, a, grid, smem, s);
-    case 192: return igemm_launch_bn<192, KC>(amap, bmap, a, grid, smem, s);
-    case 256: return igemm_launch_bn<256, KC>(amap, bmap, a, grid, smem, s);
+    case 16: return igemm_launch_bn<16, KC, T>(amap, bmap, a, grid, smem, s);
+    case 32: return igemm_launch_bn<32, KC, T>(amap, bmap, a, grid, smem, s);
+    case 48: return igemm_launch_bn<48, KC, T>(amap, bmap, a, grid, smem, s);
+    case 64: return igemm_launch_bn<64, KC, T>(amap, bmap, a, grid, smem, s);
+    case 96: return igemm_launch_bn<96, KC, T>(amap, bmap, a, grid, smem, s);
+    case 128: return igemm_launch_bn<128, KC, T>(amap, bmap, a, grid, smem, s);
+    case 192: return igemm_launch_bn<192, KC, T>(amap, bmap, a, grid, smem, s);
+    case 256: return igemm_launch_bn<256, KC, T>(amap, bmap, a, grid, smem, s);
     default: return cudaErrorInvalidValue;
   }
 }

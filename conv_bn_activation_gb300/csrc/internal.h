@@ -100,6 +100,7 @@ struct IgemmArgs {
   uint64_t timeout_ns;
   int trace;      // 1: record the pipeline timeline of CTA trace_cta (profiling aid)
   int trace_cta;
+  int bf16;       // 1: x, w, y and r hold bfloat16 (kind::f16 MMAs); kc then counts 4-byte units of a row
 };
 int igemm_read_trace(unsigned long long* out, int max_records);
 cudaError_t launch_igemm(const CUtensorMap& amap, const CUtensorMap& bmap, const IgemmArgs& a, int bn, int kc,
@@ -142,6 +143,7 @@ struct HaloArgs {
   uint64_t timeout_ns;
   int trace;           // 1: record the pipeline timeline of CTA trace_cta (profiling aid)
   int trace_cta;
+  int bf16;            // 1: x, w, y and r hold bfloat16 (kind::f16 MMAs); kc counts 4-byte units of a row
 };
 // Input rows one halo copy spans for a tile of px pixels at padded width
 // wp, and the buffer bytes (rows * wp pixels of 128 bytes, plus 8 rows that

@@ -249,6 +249,30 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 with bf16 operands (K = 16 per
+// instruction: 32 bytes of a K-major row, like kind::tf32's K = 8), one CTA.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The MMA for operands of element type T: kind::tf32 for fp32 storage (the
+// operands are read as TF32), kind::f16 with bf16 operands for bf16 storage.
+// Either consumes 32 bytes of each K-major row per instruction.
+template <typename T>
+__device__ __forceinline__ void mma_op(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  if constexpr (sizeof(T) == 4)
+    mma_tf32(d_tmem, a_desc, b_desc, idesc, accumulate);
+  else
+    mma_bf16(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+
 // Arrive (once) on `bar` when all tcgen05 operations issued so far by this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -312,6 +336,19 @@ __device__ __forceinline__ uint64_t kmajor_swizzled_desc(uint32_t saddr, int row
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16 with bf16 A and B (formats 1 in bits 7-9
+// and 10-12), D fp32, both K-major; N and M fields as above.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The instruction descriptor for operands of element type T (see mma_op).
+template <typename T>
+__host__ __device__ constexpr uint32_t idesc_for(int M, int N) {
+  return sizeof(T) == 4 ? idesc_tf32(M, N) : idesc_bf16(M, N);
 }
 
 }  // namespace cb

@@ -53,15 +53,23 @@ __device__ __forceinline__ float tc_epi_t(float acc, float sc, float bi, float r
 }
 
 // The epilogue after the folded BN (scale and bias applied by the caller,
-// two channels per packed FMA).
-template <int ACT, int RES>
+// two channels per packed FMA).  fp32 outputs (T = float) are rounded to the
+// nearest TF32 value; bf16 outputs are rounded to bf16 when stored.
+template <int ACT, int RES, typename T = float>
 __device__ __forceinline__ float tc_epi_post(float z, float r) {
   if constexpr (RES == 1) z += r;
   if constexpr (ACT == 1) z = fmaxf(z, 0.0f);
   if constexpr (ACT == 2) z = silu(z);
   if constexpr (RES == 2) z += r;
-  return round_tf32(z);
+  if constexpr (sizeof(T) == 4) return round_tf32(z);
+  return z;
 }
+
+// One element of type T widened to fp32, and stored from fp32 (bf16: nearest even).
+__device__ __forceinline__ float load1(const float* p) { return *p; }
+__device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void store1(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // 32 lanes x 32 bits, 32 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -183,26 +191,27 @@ struct TileStore {
 
   // yoff / roff: this lane's row's element offsets into y / r (yoff < 0:
   // row masked).  One uniform branch per chunk picks the compile-time
-  // epilogue.
+  // epilogue.  T: the element type of y and r (the views' storage type).
+  template <typename T = float>
   __device__ static __forceinline__ void write(const uint8_t* buf, int lane, long long yoff, long long roff,
                                                const Consts& k, int Cout, const OutView& out, const Epilogue& ep) {
     switch (ep.act * 3 + ep.res_mode) {
-      case 0: write_t<0, 0>(buf, lane, yoff, roff, k, Cout, out, ep); break;
-      case 1: write_t<0, 1>(buf, lane, yoff, roff, k, Cout, out, ep); break;
-      case 2: write_t<0, 2>(buf, lane, yoff, roff, k, Cout, out, ep); break;
-      case 3: write_t<1, 0>(buf, lane, yoff, roff, k, Cout, out, ep); break;
-      case 4: write_t<1, 1>(buf, lane, yoff, roff, k, Cout, out, ep); break;
-      case 5: write_t<1, 2>(buf, lane, yoff, roff, k, Cout, out, ep); break;
-      case 6: write_t<2, 0>(buf, lane, yoff, roff, k, Cout, out, ep); break;
-      case 7: write_t<2, 1>(buf, lane, yoff, roff, k, Cout, out, ep); break;
-      default: write_t<2, 2>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 0: write_t<0, 0, T>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 1: write_t<0, 1, T>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 2: write_t<0, 2, T>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 3: write_t<1, 0, T>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 4: write_t<1, 1, T>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 5: write_t<1, 2, T>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 6: write_t<2, 0, T>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      case 7: write_t<2, 1, T>(buf, lane, yoff, roff, k, Cout, out, ep); break;
+      default: write_t<2, 2, T>(buf, lane, yoff, roff, k, Cout, out, ep); break;
     }
   }
 
   // Straight-line over the kLpp passes: all loads first, then all the math,
   // then the (predicated) stores, so that the exponentials and reciprocals of
   // different pixels overlap instead of each pass waiting on the last.
-  template <int ACT, int RES>
+  template <int ACT, int RES, typename T>
   __device__ static __forceinline__ void write_t(const uint8_t* buf, int lane, long long yoff, long long roff,
                                                  const Consts& k, int Cout, const OutView& out,
                                                  const Epilogue& ep) {
@@ -226,14 +235,14 @@ struct TileStore {
       for (int jj = 0; jj < 4; ++jj) r[pass][jj] = 0.0f;
       if constexpr (RES != 0) {
         if (yo[pass] >= 0 && k.cin) {
-          const float* rp = ep.r + ro[pass] + c;
+          const T* rp = reinterpret_cast<const T*>(ep.r) + ro[pass] + c;
           if (k.cvec) {
-            const float4 t = *reinterpret_cast<const float4*>(rp);
+            const float4 t = load4(rp);
             r[pass][0] = t.x, r[pass][1] = t.y, r[pass][2] = t.z, r[pass][3] = t.w;
           } else {
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
-              if (c + jj < Cout) r[pass][jj] = rp[jj];
+              if (c + jj < Cout) r[pass][jj] = load1(rp + jj);
           }
         }
       }
@@ -245,19 +254,19 @@ struct TileStore {
         // scale and bias of two channels in one packed FMA (each lane one fmaf)
         const float2 a = __ffma2_rn(make_float2(z[pass][jj], z[pass][jj + 1]), make_float2(k.sc[jj], k.sc[jj + 1]),
                                     make_float2(k.bi[jj], k.bi[jj + 1]));
-        z[pass][jj] = tc_epi_post<ACT, RES>(a.x, r[pass][jj]);
-        z[pass][jj + 1] = tc_epi_post<ACT, RES>(a.y, r[pass][jj + 1]);
+        z[pass][jj] = tc_epi_post<ACT, RES, T>(a.x, r[pass][jj]);
+        z[pass][jj + 1] = tc_epi_post<ACT, RES, T>(a.y, r[pass][jj + 1]);
       }
 #pragma unroll
     for (int pass = 0; pass < kLpp; ++pass) {
       if (yo[pass] < 0 || !k.cin) continue;
-      float* yp = out.y + yo[pass] + c;
+      T* yp = reinterpret_cast<T*>(out.y) + yo[pass] + c;
       if (k.cvec) {
-        *reinterpret_cast<float4*>(yp) = make_float4(z[pass][0], z[pass][1], z[pass][2], z[pass][3]);
+        store4(yp, make_float4(z[pass][0], z[pass][1], z[pass][2], z[pass][3]));
       } else {
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
-          if (c + jj < Cout) yp[jj] = z[pass][jj];
+          if (c + jj < Cout) store1(yp + jj, z[pass][jj]);
       }
     }
   }

@@ -33,21 +33,28 @@ def _dev(a, device):
 class ConvBnAct:
     """One fused layer with folded BN and repacked weights on the device.
 
-    tc_weights: round the dense weights to the nearest TF32 value
-    (cb_round_weights_tf32) for the tensor-core path; None asks the library
-    (cb_layer_uses_tensor_cores) under the current kernel policy.
+    tc_weights: prepare the dense weights for the tensor-core path -- rounded
+    to the nearest TF32 value (cb_round_weights_tf32) for fp32 activations,
+    converted to bf16 (cb_convert_weights_bf16) for bf16 ones; None asks the
+    library (cb_layer_uses_tensor_cores) under the current kernel policy.
+    dtype: the activations' storage type (torch.float32 or torch.bfloat16).
     """
 
-    def __init__(self, w_oihw, bn, stride, pad, act, groups=1, device="cuda", eps=1e-5, tc_weights=None):
+    def __init__(self, w_oihw, bn, stride, pad, act, groups=1, device="cuda", eps=1e-5, tc_weights=None,
+                 dtype=torch.float32):
         scale, bias = cb.fold_bn(*bn, eps=eps)
         cin = w_oihw.shape[1] * groups
         if tc_weights is None:
             tc_weights = cb.layer_uses_tensor_cores(cin, w_oihw.shape[0], w_oihw.shape[2], stride, groups)
         w = cb.repack_weights(w_oihw, groups)
-        if tc_weights:
-            w = cb.round_weights_tf32(w)
         self.tc_weights = bool(tc_weights)
-        self.w = _dev(w, device).contiguous()
+        self.dtype = dtype
+        if tc_weights and dtype == torch.bfloat16:
+            self.w = cb.convert_weights_bf16(w).to(device).contiguous()
+        else:
+            if tc_weights:
+                w = cb.round_weights_tf32(w)
+            self.w = _dev(w, device).contiguous()
         self.scale = _dev(scale, device)
         self.bias = _dev(bias, device)
         self.cout, cin_g, self.k, _ = w_oihw.shape

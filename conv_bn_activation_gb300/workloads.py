@@ -38,13 +38,14 @@ class Work:
         return Work(self.bytes + other.bytes, self.flops + other.flops)
 
 
-def conv_layer(N, H, W, Cin, Cout, k, s, p, groups=1, residual=False, act_bytes=F32) -> Work:
+def conv_layer(N, H, W, Cin, Cout, k, s, p, groups=1, residual=False, act_bytes=F32, w_bytes=F32) -> Work:
     """Fused conv + folded BN (+ residual) + activation: in + out (+ r) + w + scale/bias.
-    act_bytes: bytes per activation element (4 fp32, 2 bf16 storage); weights stay fp32."""
+    act_bytes: bytes per activation element (4 fp32, 2 bf16 storage); w_bytes: bytes per weight
+    (4, or 2 for bf16 tensor-core layers, which multiply bf16 weights)."""
     OH, OW = out_size(H, k, s, p), out_size(W, k, s, p)
     x = N * H * W * Cin * act_bytes
     y = N * OH * OW * Cout * act_bytes
-    w = Cout * (Cin // groups) * k * k * F32
+    w = Cout * (Cin // groups) * k * k * w_bytes
     sb = 2 * Cout * F32
     r = y if residual else 0
     macs = N * OH * OW * Cout * (Cin // groups) * k * k

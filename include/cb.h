@@ -60,12 +60,13 @@ typedef enum { CB_LAYOUT_NHWC = 0, CB_LAYOUT_NCHW = 1 } cb_layout;
 /*
  * Element type of an activation view.  CB_DTYPE_F32 (0, the default of a
  * zero-initialised view) everywhere; CB_DTYPE_BF16 (bfloat16: the upper half
- * of an fp32) is the half-size storage variant, taken by the depthwise 3x3
- * and the narrow 1x1 layers of cb_conv_bn_act: a 16-bit main data type is the first of the
- * next steps "How I sped up convolutions" lists (ideas and next steps), and
- * those layers are memory-bound, so halving their bytes halves their time.
- * Arithmetic stays fp32; a BF16 output is the fp32 result rounded to
- * nearest even.
+ * of an fp32) is the half-size storage variant, taken by the depthwise 3x3,
+ * the narrow 1x1 and the tensor-core layers of cb_conv_bn_act: a 16-bit main
+ * data type is the first of the next steps "How I sped up convolutions"
+ * lists (ideas and next steps), and most of these layers are memory-bound,
+ * so halving their bytes shortens them.  Accumulation stays fp32 (the
+ * CUDA-core kernels compute in fp32; the tensor cores multiply the bf16
+ * values exactly); a BF16 output is the fp32 result rounded to nearest even.
  * Entry points that do not take BF16 views return CB_ERR_UNSUPPORTED.
  */
 typedef enum { CB_DTYPE_F32 = 0, CB_DTYPE_BF16 = 1 } cb_dtype;
@@ -123,6 +124,18 @@ cb_status cb_repack_weights(const float* w_oihw, int Co, int Ci_per_group, int k
 cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
 
 /*
+ * Convert n fp32 weights (HOST, any layout) to bfloat16 (HOST output of n
+ * 16-bit values), rounded to nearest with ties to even (NaN stays NaN).
+ * Layers with bf16 storage that run on the tensor cores multiply bf16
+ * operands (kind::f16 MMAs, fp32 accumulate), so their weights must be bf16
+ * in device memory: pass this output, uploaded, as cb_conv_bn_act's `w`.
+ * A 16-bit main data type is the first of the next steps "How I sped up
+ * convolutions" lists (ideas and next steps).  CB_ERR_INVALID_ARG for NULL
+ * pointers or n < 0.
+ */
+cb_status cb_convert_weights_bf16(const float* w, long long n, void* out);
+
+/*
  * The fused layer.  x: input view (NHWC, or NCHW for the small-channel stem
  * path); w: DEVICE weights in the cb_repack_weights layout; scale/bias:
  * DEVICE fp32 [Co] from cb_fold_bn; kernel kh x kw (1 or 3), stride 1 or 2,
@@ -145,14 +158,19 @@ cb_status cb_round_weights_tf32(const float* w, long long n, float* out);
  * layers with Ci and Co in {4, 8, 16, 32} run instead on a streaming fp32
  * CUDA-core kernel (HBM-bound at these widths);
  * depthwise 3x3 layers run on a channel-vectorised CUDA-core kernel;
- * bf16 storage (x, y and residual all CB_DTYPE_BF16; weights, scale and
- * bias stay fp32, and so does the arithmetic) is taken by the depthwise 3x3
- * layers (C % 8 == 0) and by the 1x1 stride-1 layers of the streaming
- * kernel with Ci in {8, 16, 32} and Co in {4, 8, 16, 32}; both need 16-byte
- * aligned x, y, residual, w, scale and bias, x strides that are multiples
- * of 8 elements and y / residual strides that are multiples of 8 (depthwise)
- * or 4 (1x1) elements (else CB_ERR_ALIGNMENT); any other bf16 layer
- * returns CB_ERR_UNSUPPORTED;
+ * bf16 storage (x, y and residual all CB_DTYPE_BF16; scale and bias stay
+ * fp32) is taken by the depthwise 3x3 layers (C % 8 == 0) and by the 1x1
+ * stride-1 layers of the streaming kernel with Ci in {8, 16, 32} and Co in
+ * {4, 8, 16, 32} -- fp32 weights and fp32 arithmetic on the CUDA cores --
+ * and by the tensor-core shapes above with Ci % 8 == 0, which multiply bf16
+ * operands with fp32 accumulation (tcgen05 kind::f16): their `w` holds bf16
+ * weights (cb_convert_weights_bf16), and a 3x3 pad-1 layer takes the halo
+ * tiles at stride 1 with Ci % 16 == 0 and at stride 2 with Ci % 32 == 0.
+ * A bf16 output is the fp32 result rounded to nearest even.  All need
+ * 16-byte aligned x, y, residual, w, scale and bias, x strides that are
+ * multiples of 8 elements and y / residual strides that are multiples of 8
+ * (depthwise) or 4 (the others) elements (else CB_ERR_ALIGNMENT); any other
+ * bf16 layer returns CB_ERR_UNSUPPORTED;
  * 3 -> 16 channel 3x3 stride-2 pad-1 stems run on a dedicated fp32 CUDA-core
  * kernel when the input is planar (NCHW) or packed NHWC (stride_w == 3) with
  * W % 4 == 0, 16-byte aligned data and n / h (/ c) strides that are

@@ -122,7 +122,8 @@ def test_bf16_views_validated_before_launch(cblib):
     y32 = v(base + (1 << 16), 1, 8, 8, 16, cblib.DTYPE_F32)
     call = lambda xv, yv, g=1, r=None, rm=0: lib.cb_conv_bn_act(
         T(xv), w, s, b, 3, 3, 1, 1, g, 0, T(r) if r is not None else None, rm, T(yv), None)
-    assert call(x16, y16, g=1) == cblib.ERR_UNSUPPORTED                      # dense bf16
+    x8 = v(base, 1, 8, 8, 8, cblib.DTYPE_BF16)
+    assert call(x8, v(base + (1 << 16), 1, 8, 8, 8, cblib.DTYPE_BF16), g=1) == cblib.ERR_UNSUPPORTED  # 3x3, 8 ch
     assert call(x16, y32, g=16) == cblib.ERR_INVALID_ARG                     # mixed element types
     assert call(x16, y16, g=16, r=v(base + (1 << 17), 1, 8, 8, 16, cblib.DTYPE_F32), rm=2) == cblib.ERR_INVALID_ARG
     assert call(v(base, 1, 8, 8, 16, 7), v(base + (1 << 16), 1, 8, 8, 16, 7), g=16) == cblib.ERR_INVALID_ARG
@@ -226,3 +227,20 @@ def test_autotune_rejects_in_place_residual(cblib):
     w = s = b = base + (1 << 18)
     assert lib.cb_autotune_conv(T(x), w, s, b, 3, 3, 1, 1, 1, 2, T(y), 2, T(y), None) == cblib.ERR_INVALID_ARG
     assert lib.cb_autotune_conv(T(x), w, s, b, 3, 3, 1, 1, 1, 2, T(y), 1, T(y), None) == cblib.ERR_INVALID_ARG
+
+
+def test_convert_weights_bf16_rounds_to_nearest_even(cblib):
+    """cb_convert_weights_bf16 equals torch's float32 -> bfloat16 conversion bit for bit (round to nearest,
+    ties to even), on random values over a wide range, exact ties, infinities and NaN."""
+    import torch
+    g = np.random.default_rng(5)
+    w = (g.standard_normal(20000) * np.exp(g.uniform(-30, 30, 20000))).astype(np.float32)
+    base = np.array([1.0, -3.0], np.float32).view(np.uint32)
+    ties = np.concatenate([base + 0x8000, base + 0x18000, base + 0x7FFF, base + 0x8001]).view(np.float32)
+    special = np.array([np.inf, -np.inf, 0.0, -0.0, 3.4e38, 1e-40], np.float32)
+    w = np.concatenate([w, ties, special])
+    got = cblib.convert_weights_bf16(w).view(torch.int16).numpy()
+    want = torch.from_numpy(w).to(torch.bfloat16).view(torch.int16).numpy()
+    np.testing.assert_array_equal(got, want)
+    nan = cblib.convert_weights_bf16(np.array([np.nan], np.float32)).float().numpy()
+    assert np.isnan(nan[0])
