@@ -187,6 +187,7 @@ class Launch:
 class Workload:
     """A step = the listed launches, in order, on one stream."""
     unit = "GB/s"
+    tc_dtype = "tf32"       # operand type of the tensor-core launches: the roofline takes that type's peak
     capture = True          # time the K steps as one CUDA graph (no host gaps between launches)
     profile = None          # (profiles/ file, kernel source files) for the roofline's traffic figure
     dominant = None         # launch name whose roofline is reported
@@ -239,7 +240,7 @@ class Workload:
     def launch_roofline(self, L, ms, peaks):
         if L.bound == "tensor":
             achieved = L.work.flops / (ms * 1e-3) / 1e12
-            peak = tf32_peak(peaks)
+            peak = peaks["bf16_tflops"] if self.tc_dtype == "bf16" else tf32_peak(peaks)
             bw_roof = L.work.bytes / (ms * 1e-3) / 1e9
             return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
                     "frac": round(achieved / peak, 4),
@@ -259,6 +260,8 @@ class Workload:
         r["traffic"] = profiled_traffic(*self.profile) if self.profile else None
         if r["bound"] == "hbm":
             r["peak_source"] = f"{peaks['source']} hbm_gbs (copy-kernel burst)"
+        elif self.tc_dtype == "bf16":
+            r["peak_source"] = f"{peaks['source']} bf16_tflops (cuBLAS bf16 burst)"
         else:
             r["peak_source"] = f"{peaks['source']} bf16_tflops x 1.1/2.25 (nominal TF32/BF16 ratio)"
         return r
@@ -388,6 +391,7 @@ class DenseWorkload(Workload):
 class DenseBf16Workload(DenseWorkload):
     """The tensor-core layers of the dense sweep with bf16 storage and bf16 MMA operands."""
     bf16 = True
+    tc_dtype = "bf16"
 
 
 class MnistWorkload(Workload):

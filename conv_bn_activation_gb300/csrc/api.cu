@@ -69,15 +69,7 @@ cb_status current_device(DeviceInfo** out) {
   return CB_OK;
 }
 
-uint64_t timeout_ns() {
-  static uint64_t v = [] {
-    const char* s = std::getenv("CB_TIMEOUT_MS");
-    long long ms = s ? std::atoll(s) : 2000;
-    if (ms <= 0) ms = 2000;
-    return static_cast<uint64_t>(ms) * 1000000ull;
-  }();
-  return v;
-}
+uint64_t timeout_ns();  // the CB_TIMEOUT_MS tuning knob, in nanoseconds
 
 // ---------------------------------------------------------- driver entry points
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -302,10 +294,13 @@ struct Tuning {
   bool debug_plan = false;         // CB_DEBUG_PLAN: print each plan to stderr
   int trace_cta = -1;              // CB_IGEMM_TRACE = cta (trace builds: timeline of one CTA)
   int span_slot = 1;               // CB_SPAN_SLOT = 1 / 2 (trace builds)
+  int timeout_ms = 2000;           // CB_TIMEOUT_MS: bound of every device wait
+  int dw_skip_row = 0;             // CB_DEBUG_DW_SKIP_ROW = 1: fault injection (see cb_set_tuning)
 };
 
-const char* const kTuningNames[] = {"CB_DW_FORCE",       "CB_IGEMM_FORCE", "CB_IGEMM_BLOCKS", "CB_HALO_FORCE",
-                                    "CB_DW_BLOCK_FORCE", "CB_DEBUG_PLAN",  "CB_IGEMM_TRACE",  "CB_SPAN_SLOT"};
+const char* const kTuningNames[] = {"CB_DW_FORCE",    "CB_IGEMM_FORCE", "CB_IGEMM_BLOCKS", "CB_HALO_FORCE",
+                                    "CB_DW_BLOCK_FORCE", "CB_DEBUG_PLAN", "CB_IGEMM_TRACE", "CB_SPAN_SLOT",
+                                    "CB_TIMEOUT_MS",  "CB_DEBUG_DW_SKIP_ROW"};
 
 // Sets knob `name` of *t from `v` (NULL or "" restores the knob's default);
 // false for an unknown name.
@@ -339,6 +334,11 @@ bool parse_tuning(Tuning* t, const char* name, const char* v) {
     t->trace_cta = unset ? d.trace_cta : std::atoi(v);
   } else if (!std::strcmp(name, "CB_SPAN_SLOT")) {
     t->span_slot = unset ? d.span_slot : (std::atoi(v) == 2 ? 2 : 1);
+  } else if (!std::strcmp(name, "CB_TIMEOUT_MS")) {
+    const int ms = unset ? 0 : std::atoi(v);
+    t->timeout_ms = ms > 0 ? ms : d.timeout_ms;
+  } else if (!std::strcmp(name, "CB_DEBUG_DW_SKIP_ROW")) {
+    t->dw_skip_row = unset ? 0 : (std::atoi(v) != 0 ? 1 : 0);
   } else {
     return false;
   }
@@ -362,6 +362,8 @@ Tuning tuning() {
   std::lock_guard<std::mutex> lock(g_tuning_mu);
   return tuning_locked();
 }
+
+uint64_t timeout_ns() { return static_cast<uint64_t>(tuning().timeout_ms) * 1000000ull; }
 
 // ----------------------------------------------------------------- depthwise
 cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, int stride, int pad,
@@ -483,7 +485,8 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
     cudaError_t e = launch_dw_simple(a, vec, s);
     return e == cudaSuccess ? CB_OK : cuda_fail(e);
   }
-  cudaError_t e = launch_dw_tma(map, a, best, dev->err, timeout_ns(), s);
+  cudaError_t e = launch_dw_tma(map, a, best, dev->err, static_cast<uint64_t>(tu.timeout_ms) * 1000000ull,
+                                tu.dw_skip_row, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
 
@@ -749,10 +752,11 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
   // fp32 channels, or 2 kc bf16 channels
   const int eb = is_f32(x) ? 4 : 2;
   const int cpu = 4 / eb;  // channels per 4-byte unit
-  const int kc = (stride == 1 && Ci % (32 * cpu) == 0) ? 32
-                 : Ci % (16 * cpu) == 0                ? 16
-                 : (stride == 1 && Ci % (8 * cpu) == 0) ? 8
-                                                         : 0;
+  // (bf16 at stride 2 may take 32-byte rows too: 16-channel layers)
+  const int kc = (stride == 1 && Ci % (32 * cpu) == 0)          ? 32
+                 : Ci % (16 * cpu) == 0                         ? 16
+                 : ((stride == 1 || eb == 2) && Ci % (8 * cpu) == 0) ? 8
+                                                                  : 0;
   if (kc == 0) return false;
   const int num_kc = Ci / (kc * cpu);
   constexpr size_t kSmemMax = 227 * 1024;

@@ -96,6 +96,7 @@ struct DwTmaParams {
   int chunks, strips, wtiles, tile_w;
   int* err;
   uint64_t timeout_ns;
+  int debug_skip_row;  // fault injection: CTA 0 withholds its first row copy (tests of the bounded waits)
 };
 
 struct DwItem {
@@ -215,7 +216,10 @@ __global__ void __launch_bounds__(512, 1) dw_tma_kernel(const __grid_constant__ 
         const int ih0 = it.oh0 * S - a.pad;
         const int iw0 = it.ow0 * S - a.pad;
         for (int r = 0; r < nrows; ++r) {
-          if (slot % kDwProducerLanes == lane) {
+          // fault injection: no copy and no arrive for CTA 0's first row, so
+          // that row's barrier phase never completes and its waits run out
+          const bool skip = p.debug_skip_row && blockIdx.x == 0 && item == 0 && r == 0;
+          if (slot % kDwProducerLanes == lane && !skip) {
             if (!mbar_wait(&empty[slot], phase ^ 1u, wd)) {
               ok = false;
               break;
@@ -419,7 +423,7 @@ static void dw_tma_dispatch(const CUtensorMap& xmap, const DwTmaParams& p, int g
 }
 
 cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaPlan& plan, int* err,
-                          uint64_t timeout_ns, cudaStream_t s) {
+                          uint64_t timeout_ns, int debug_skip_row, cudaStream_t s) {
   DwTmaParams p;
   p.a = a;
   p.rows_per_item = plan.rows_per_item;
@@ -434,6 +438,7 @@ cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaP
   p.wtiles = (a.OW + p.tile_w - 1) / p.tile_w;
   p.err = err;
   p.timeout_ns = timeout_ns;
+  p.debug_skip_row = debug_skip_row;
   const int threads = 32 * (1 + plan.consumer_warps);
   if (a.bf16) {
     if (a.stride == 1)

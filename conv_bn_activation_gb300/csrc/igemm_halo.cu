@@ -110,7 +110,8 @@ cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, 
   if (a.w_resident &&
       (a.num_kc != 1 || a.n_tiles != 1 || a.split_k != 1 || a.taps_per_stage != 9 || a.nb_stages != 1))
     return cudaErrorInvalidValue;
-  if (a.stride == 2 && (a.kc != 16 || a.phase_bytes * 4 != a.halo_bytes || a.Wp * 2 > 256 || a.rows * 2 > 256))
+  if (a.stride == 2 && ((a.kc != 16 && !(a.bf16 && a.kc == 8)) || a.phase_bytes * 4 != a.halo_bytes ||
+                        a.Wp * 2 > 256 || a.rows * 2 > 256))
     return cudaErrorInvalidValue;
   if (a.split_k == 2) {
     // one tile per cluster, a channel-chunk per CTA at least, the partner's

@@ -51,8 +51,12 @@ struct DwTmaPlan {
   int w_smem;  // bf16 at stride 1: the 9 x C taps staged in shared memory after the barriers
   size_t smem_bytes;
 };
+// debug_skip_row = 1 is fault injection for tests of the bounded waits: the
+// producer of CTA 0 withholds the copy (and the barrier arrive) of its first
+// input row, so the consumers' wait on it runs out, the kernel records
+// CB_ERR_TIMEOUT and returns.
 cudaError_t launch_dw_tma(const CUtensorMap& xmap, const DwArgs& a, const DwTmaPlan& plan, int* err,
-                          uint64_t timeout_ns, cudaStream_t s);
+                          uint64_t timeout_ns, int debug_skip_row, cudaStream_t s);
 
 // ---------------------------------------------------------- direct (CUDA core)
 struct DirectArgs {

@@ -449,6 +449,14 @@ int cb_autotune_entries(void);
  *                     wherever its shape rule allows / never
  *   CB_DEBUG_PLAN     any value: print each layer's plan to stderr
  *   CB_IGEMM_TRACE, CB_SPAN_SLOT   CTA timelines (trace builds only)
+ *   CB_TIMEOUT_MS     bound of every device wait in milliseconds (default 2000)
+ *   CB_DEBUG_DW_SKIP_ROW  "1": fault injection for tests of the bounded waits --
+ *                     in the TMA depthwise kernel, the producer of CTA 0 withholds
+ *                     the copy and barrier arrive of its first input row, so its
+ *                     consumers' wait runs out after CB_TIMEOUT_MS; the kernel
+ *                     records CB_ERR_TIMEOUT (cb_get_device_error), drains the
+ *                     copies it issued and returns; that layer's output is not
+ *                     valid.  Nothing faults or hangs.
  * and `value` its setting (NULL or "" restores the default).  Each knob
  * starts from the environment variable of the same name, read once per
  * process; only this call changes it afterwards.  While a plan override of

@@ -36,3 +36,29 @@ def test_timeout_probe_rejects_bad_limits(gpu):
     for bad in (0, -1, 10001):
         with pytest.raises(cb.CbError):
             cb.debug_timeout_probe(bad)
+
+
+@pytest.mark.parametrize("stride", [1, 2])
+def test_depthwise_pipeline_wait_runs_out(gpu, orc, stride):
+    """Inside a real pipeline: the TMA depthwise kernel's producer withholds one row (fault
+    injection through CB_DEBUG_DW_SKIP_ROW, nothing is issued against that barrier), so the
+    consumers' bounded wait runs out after CB_TIMEOUT_MS.  The kernel records CB_ERR_TIMEOUT,
+    drains its copies, frees nothing it does not hold and returns: no hang, no fault.  The error
+    reads once, and the same layer run again without the injection matches the oracle."""
+    x, w, bn = synthetic.depthwise_layer(2, 64, 20, 20, seed=stride)
+    layer = ConvBnAct(w, bn, stride, 1, cb.ACT_RELU, groups=64)
+    OH, OW = layer.out_hw(20, 20)
+    xd = to_dev(x)
+    y = torch.empty(2, OH, OW, 64, device="cuda")
+    assert cb.get_device_error() == cb.OK
+    with cb.tuning("CB_TIMEOUT_MS", "50"), cb.tuning("CB_DEBUG_DW_SKIP_ROW", "1"):
+        t0 = time.perf_counter()
+        layer(xd, y)
+        assert "dw_tma_kernel" in cb.last_launch()["kernel"]
+        assert cb.get_device_error() == cb.ERR_TIMEOUT
+        assert time.perf_counter() - t0 < 5.0
+    assert cb.get_device_error() == cb.OK  # reading cleared it
+    layer(xd, y)
+    sync_check()
+    ref = orc.conv_bn_act(x, w, bn, stride=stride, pad=1, groups=64, act=orc.ACT_RELU)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_FP32
