@@ -217,13 +217,18 @@ __device__ __forceinline__ void conv_tile(int t, const StemArgs& a, const float*
   for (int ci = 0; ci < 3; ++ci) {
 #pragma unroll
     for (int kh = 0; kh < 3; ++kh) {
-      // input columns 2*ow - 1 .. 2*ow + 3 of the thread's first pixel ow
+      // input columns 2*ow - 1 .. 2*ow + 3 of the thread's first pixel ow:
+      // one 16-byte load of columns 2*ow .. 2*ow + 3, and column 2*ow - 1
+      // from the lane to the left (its last column; lane 0 loads its own:
+      // a per-lane 4-byte load at a 16-byte stride would be a 4-way bank
+      // conflict)
       float v[2][5];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const float* rp = pl + ci * kPlane + (4 * ty + 2 * r + kh) * kCols + 4 * tx;
-        v[r][0] = rp[3];
         const float4 f = *reinterpret_cast<const float4*>(rp + 4);
+        v[r][0] = __shfl_up_sync(0xffffffffu, f.w, 1);
+        if (tx == 0) v[r][0] = rp[3];
         v[r][1] = f.x, v[r][2] = f.y, v[r][3] = f.z, v[r][4] = f.w;
       }
 #pragma unroll
