@@ -190,6 +190,7 @@ class Workload:
     tc_dtype = "tf32"       # operand type of the tensor-core launches: the roofline takes that type's peak
     capture = True          # time the K steps as one CUDA graph (no host gaps between launches)
     profile = None          # (profiles/ file, kernel source files) for the roofline's traffic figure
+    profiles = {}           # the same per launch name, for workloads whose dominant launch varies
     dominant = None         # launch name whose roofline is reported
 
     def run(self, stream, events=None):
@@ -257,7 +258,8 @@ class Workload:
         r["kernel"] = f"{L.kernel} ({L.name})"
         r["algorithmic_bytes" if r["bound"] == "hbm" else "algorithmic_flops"] = \
             L.work.bytes if r["bound"] == "hbm" else L.work.flops
-        r["traffic"] = profiled_traffic(*self.profile) if self.profile else None
+        prof = self.profiles.get(L.name, self.profile)
+        r["traffic"] = profiled_traffic(*prof) if prof else None
         if r["bound"] == "hbm":
             r["peak_source"] = f"{peaks['source']} hbm_gbs (copy-kernel burst)"
         elif self.tc_dtype == "bf16":
@@ -443,6 +445,15 @@ class MnistWorkload(Workload):
 
 class YoloWorkload(Workload):
     unit = "images/s"
+    # ncu summaries (DRAM traffic of one launch at batch 32) of the launches that can be the longest
+    profiles = {
+        "s0.down": ("stem_kernel_yolo_s0_down_b32.md",
+                    ["stem.cu", "resample.cuh", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
+        "s0.cv2": ("conv3x3_c8_kernel_yolo_s0_cv2_b32.md",
+                   ["conv3x3_c8.cu", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
+        "s0.cv3": ("pw_small_kernel_yolo_s0_cv3_b32.md",
+                   ["pointwise.cu", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
+    }
 
     def __init__(self, torch, device, batch=32):
         from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
