@@ -508,13 +508,14 @@ class YoloWorkload(Workload):
 
     def e2e_pipelined(self, stream, steps):
         """`steps` steps with host buffers, each: the H2D copy of its input (pinned), the chain, the
-        D2H copy of its output.  The input copies run on a second stream into two alternating
-        device buffers, one step ahead of the chain; the output copy follows the chain on its
-        stream (the next step's chain rewrites that buffer)."""
+        D2H copy of its output.  The copies run on a second stream: the input into two alternating
+        device buffers one step ahead of the chain, the output after the chain is done with it
+        (the next step's last layer, which rewrites that buffer, waits for the copy)."""
         t = self.torch
         copy = self.copy_stream
         h2d = [t.cuda.Event(), t.cuda.Event()]
         free = [t.cuda.Event(), t.cuda.Event()]
+        done, d2h = t.cuda.Event(), t.cuda.Event()
         copy.wait_stream(stream)
 
         def issue_h2d(i):
@@ -526,15 +527,23 @@ class YoloWorkload(Workload):
                 h2d[b].record(copy)
 
         issue_h2d(0)
+        last = len(self.launches) - 1
         for i in range(steps):
             if i + 1 < steps:
                 issue_h2d(i + 1)
             b = i & 1
             stream.wait_event(h2d[b])
             self.x = self.x_bufs[b]
-            self.run(stream)
+            for k, L in enumerate(self.launches):
+                if k == last and i > 0:
+                    stream.wait_event(d2h)            # step i - 1's output has been copied out
+                L.fn(stream)
             free[b].record(stream)
-            self.out_pin.copy_(self.chain.bufs[-1]["out"], non_blocking=True)
+            done.record(stream)
+            with t.cuda.stream(copy):
+                copy.wait_event(done)
+                self.out_pin.copy_(self.chain.bufs[-1]["out"], non_blocking=True)
+                d2h.record(copy)
         stream.wait_stream(copy)
         self.x = self.x_bufs[0]
 
@@ -984,8 +993,9 @@ def measure(torch, wl, device, stream, args, steps, warmup, min_timed_s, world, 
                                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                           "ms_per_step": round(e2e_ms, 3),
                                           "step": "one pass with its host copies (pinned memory)" +
-                                                  ("; the next step's input copy overlaps this step's chain "
-                                                   "(second stream, two device input buffers)"
+                                                  ("; both copies run on a second stream: the next step's "
+                                                   "input copy (two device input buffers) and this step's "
+                                                   "output copy overlap the chains"
                                                    if hasattr(wl, "e2e_pipelined") else "")},
         "gpu_launches": getattr(wl, "kernels_per_step", len(wl.launches)) * passes * steps,
         "timing": {"steps": f"one CUDA graph of {passes} passes per step, replayed {steps} times, events around "
