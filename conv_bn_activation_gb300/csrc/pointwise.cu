@@ -31,9 +31,7 @@ __device__ __forceinline__ float comp(const float4& v, int i) {
 }
 
 // Four output channels of one pixel; the activation is picked once per pixel
-// (a uniform branch) so the four exponentials overlap.  SiLU uses the fast
-// exponential and division (relative error ~1e-6, inside this fp32 path's
-// 1e-5 bar).
+// (a uniform branch) so the four exponentials overlap.
 __device__ __forceinline__ float4 pw_epilogue(float4 acc, float4 sc, float4 bi, float4 r, int act, int res_mode) {
   float z[4] = {fmaf(acc.x, sc.x, bi.x), fmaf(acc.y, sc.y, bi.y), fmaf(acc.z, sc.z, bi.z), fmaf(acc.w, sc.w, bi.w)};
   const float rr[4] = {r.x, r.y, r.z, r.w};
@@ -85,8 +83,18 @@ struct PwShape {
   static constexpr int kGroups = kTile / kU;                      // pixel groups per tile
   static constexpr int kItems = kGroups * G;                      // (pixel group, channel group) items
   static constexpr int kXFloat4 = kTile * kPitch;
-  static size_t smem_bytes() {
-    return 16 * (static_cast<size_t>(CI) * G + 2 * G + static_cast<size_t>(kPwStages) * kXFloat4);
+  // bf16 storage stages the residual in the ring too (16-byte copies): read
+  // straight into registers, its 8-byte loads kept too few bytes in flight
+  // to cover HBM latency (measured 120.5 us against 111 in fp32 for
+  // 16 -> 16 + residual); a bf16 tile and its residual take as much shared
+  // memory as an fp32 tile alone.
+  static constexpr int kRVec = CO / kEpp;                          // 16-byte residual pieces per pixel
+  static constexpr int kRPitch = kRVec >= 4 ? kRVec + 1 : kRVec;
+  static constexpr bool kRStaged = sizeof(T) == 2 && kRVec >= 1 && (kTile * kRVec) % kPwThreads == 0;
+  static constexpr int kRFloat4 = kRStaged ? kTile * kRPitch : 0;
+  static size_t smem_bytes(bool res) {
+    return 16 * (static_cast<size_t>(CI) * G + 2 * G +
+                 static_cast<size_t>(kPwStages) * (kXFloat4 + (res ? kRFloat4 : 0)));
   }
 };
 
@@ -107,13 +115,17 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
   constexpr int kTile = Sh::kTile, kGroups = Sh::kGroups, kItems = Sh::kItems, kU = Sh::kU;
   constexpr int kPieces = kTile * kVec / kPwThreads;  // 16-byte copies per thread per tile
   static_assert(kVec >= 1 && kPieces * kPwThreads == kTile * kVec && kPwThreads % G == 0, "tile shape");
+  constexpr bool kRStaged = RES && Sh::kRStaged;     // the residual staged beside the input (bf16)
+  constexpr int kRVec = Sh::kRVec, kRPitch = Sh::kRPitch;
+  constexpr int kRPieces = kRStaged ? kTile * kRVec / kPwThreads : 0;
+  static_assert(!kRStaged || (kRVec >= 1 && kRPieces * kPwThreads == kTile * kRVec), "residual tile shape");
   extern __shared__ float4 pw_smem[];
   constexpr bool res = RES;  // a residual (its placement is a.ep.res_mode)
   float4* ws = pw_smem;             // [CI][G]
   float4* ssc = ws + CI * G;        // [G]
   float4* sbi = ssc + G;            // [G]
   float4* ring = sbi + G;           // kPwStages x tile
-  constexpr int stage_f4 = Sh::kXFloat4;
+  constexpr int stage_f4 = Sh::kXFloat4 + (kRStaged ? Sh::kRFloat4 : 0);  // input tile, then its residual
   pdl_wait();
   pdl_launch_dependents();
   for (int i = threadIdx.x; i < CI * G; i += kPwThreads) {
@@ -148,6 +160,19 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
       const T* src = in ? x + pixel_off(p, a.xs_n, a.xs_h, a.xs_w) + kEpp * lj : x;
       cp_async16(&xs[lp * kPitch + lj], src, in ? 16 : 0);
     }
+    if constexpr (kRStaged) {
+      float4* rs = xs + Sh::kXFloat4;
+#pragma unroll
+      for (int k = 0; k < kRPieces; ++k) {
+        const int piece = threadIdx.x + k * kPwThreads;
+        const int lp = piece / kRVec, lj = piece - (piece / kRVec) * kRVec;
+        const long long p = tile * kTile + lp;
+        const bool in = p < M;
+        const T* r = reinterpret_cast<const T*>(a.ep.r);
+        const T* src = in ? r + pixel_off(p, a.ep.rs_n, a.ep.rs_h, a.ep.rs_w) + kEpp * lj : r;
+        cp_async16(&rs[lp * kRPitch + lj], src, in ? 16 : 0);
+      }
+    }
   };
 
   // prologue: the first kPwStages - 1 tiles of this CTA in flight
@@ -178,9 +203,13 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const long long p = tile * kTile + pg + u * kGroups;
-        rv[u] = (res && p < M) ? load4(reinterpret_cast<const T*>(a.ep.r) +
-                                       pixel_off(p, a.ep.rs_n, a.ep.rs_h, a.ep.rs_w) + 4 * g)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (kRStaged) {
+          rv[u] = load4(reinterpret_cast<const T*>(xs + Sh::kXFloat4 + (pg + u * kGroups) * kRPitch) + 4 * g);
+        } else {
+          rv[u] = (res && p < M) ? load4(reinterpret_cast<const T*>(a.ep.r) +
+                                         pixel_off(p, a.ep.rs_n, a.ep.rs_h, a.ep.rs_w) + 4 * g)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
       float4 acc[kU];
 #pragma unroll
@@ -224,7 +253,7 @@ __global__ void __launch_bounds__(kPwThreads) pw_small_kernel(const DirectArgs a
 template <int CI, int CO, bool RES, typename T>
 cudaError_t pw_launch_res(const DirectArgs& a, int flat, int sms, cudaStream_t s) {
   using Sh = PwShape<CI, CO, T>;
-  const size_t smem = Sh::smem_bytes();
+  const size_t smem = Sh::smem_bytes(RES);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   cudaError_t e = smem_attr_once<pw_small_kernel<CI, CO, RES, T>>(smem);
   if (e != cudaSuccess) return e;
