@@ -909,6 +909,9 @@ bool stem_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int p
   if (x->w % 4 != 0 || !aligned16(x->data) || !aligned16(y->data) || !strides_mult4(y)) return false;
   if (x->n > 65535 || static_cast<long long>(x->n) * ((y->h + 7) / 8) * ((y->w + 63) / 64) >= (1LL << 31))
     return false;
+  if (!is_f32(x))  // bf16: packed NHWC, 16-byte groups of 8 pixels, 16-byte rows
+    return x->layout == CB_LAYOUT_NHWC && x->stride_w == 3 && x->w % 8 == 0 && x->stride_n % 8 == 0 &&
+           x->stride_h % 8 == 0;
   if (x->layout == CB_LAYOUT_NCHW)
     return x->stride_n % 4 == 0 && x->stride_h % 4 == 0 && x->stride_c % 4 == 0;
   return x->stride_w == 3 && x->stride_n % 4 == 0 && x->stride_h % 4 == 0;
@@ -941,10 +944,21 @@ bool tc_bf16_views(const cb_tensor* x, const cb_tensor* y, int kh, int stride, i
          x->w <= 65535 && x->h <= 65535 && encode_tiled() && encode_im2col();
 }
 
+// bf16 storage on the 8 -> 8 channel 3x3 stride-1 kernel (conv3x3_c8.cu):
+// NHWC views, 16-byte aligned, x strides multiples of 8 elements (a pixel is
+// one 16-byte piece), y strides multiples of 4.
+bool c8_bf16_views(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad) {
+  auto mult8 = [](const cb_tensor* t) { return t->stride_n % 8 == 0 && t->stride_h % 8 == 0 && t->stride_w % 8 == 0; };
+  return g_policy.load() != 1 && x->c == 8 && y->c == 8 && kh == 3 && stride == 1 && pad == 1 &&
+         x->layout == CB_LAYOUT_NHWC && aligned16(x->data) && mult8(x) && aligned16(y->data) && strides_mult4(y);
+}
+
 cb_path dense_path(const cb_tensor* x, const cb_tensor* y, int kh, int stride, int pad, HaloPlan* plan, ImPlan* im) {
   const int policy = g_policy.load();
   if (!is_f32(x)) {
     if (pointwise_bf16_views(x, y, kh, stride, pad)) return CB_PATH_POINTWISE;
+    if (stem_path(x, y, kh, stride, pad)) return CB_PATH_STEM;
+    if (c8_bf16_views(x, y, kh, stride, pad)) return CB_PATH_DIRECT;
     if (!tc_bf16_views(x, y, kh, stride, pad)) return static_cast<cb_path>(0);
   }
   {
@@ -1134,7 +1148,7 @@ cb_status run_stem(const cb_tensor* x, const float* w, const Epilogue& ep, const
   a.ep = ep;
   a.out = make_out(y);
   stem_tile_grid(a.OH, a.OW, &a.tiles_y, &a.tiles_x);
-  const int kind = x->layout == CB_LAYOUT_NCHW ? 0 : 1;
+  const int kind = !is_f32(x) ? 3 : x->layout == CB_LAYOUT_NCHW ? 0 : 1;
   const cudaError_t e = launch_stem(a, kind, stem_smem_bytes(kind, 0, 0), dev->sms, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
@@ -1161,6 +1175,7 @@ cb_status run_direct(const cb_tensor* x, const float* w, const Epilogue& ep, int
   a.pad = pad;
   a.out = make_out(y);
   a.ep = ep;
+  a.bf16 = x->dtype == CB_DTYPE_BF16 ? 1 : 0;  // the 8-channel kernel only
   DeviceInfo* dev = nullptr;
   cb_status st = current_device(&dev);
   if (st != CB_OK) return st;
@@ -1264,7 +1279,9 @@ cb_status validate_conv(const cb_tensor* x, const float* w, const float* scale, 
   if (!is_f32(x) && !depthwise &&
       (g_policy.load() == 1 ||
        !((kh == 1 && stride == 1 && pad == 0 && pointwise_small_ok(x->c, y->c, true)) ||
-         (tc_shape(x->c, y->c, kh, stride, pad) && x->c % 8 == 0))))
+         (tc_shape(x->c, y->c, kh, stride, pad) && x->c % 8 == 0) ||
+         (x->c == 3 && y->c == 16 && kh == 3 && stride == 2 && pad == 1 && x->layout == CB_LAYOUT_NHWC) ||
+         (x->c == 8 && y->c == 8 && kh == 3 && stride == 1 && pad == 1 && x->layout == CB_LAYOUT_NHWC))))
     return CB_ERR_UNSUPPORTED;
   if (res_mode != CB_RES_NONE) {
     if (!view_ok(residual) || residual->layout != CB_LAYOUT_NHWC || residual->dtype != y->dtype)
@@ -1296,6 +1313,10 @@ cb_status launch_conv(const cb_tensor* x, const float* w, const float* scale, co
         (res_mode != CB_RES_NONE && (!aligned16(residual->data) || !strides_mult4(residual))))
       return CB_ERR_ALIGNMENT;
     if (pointwise_bf16_views(x, y, kh, stride, pad)) return run_pointwise(x, w, ep, residual, y, s);
+    if (x->c == 3 && y->c == 16 && kh == 3)  // the stem shape (validated): its bf16 kernel, else no kernel
+      return stem_path(x, y, kh, stride, pad) ? run_stem(x, w, ep, y, s) : CB_ERR_ALIGNMENT;
+    if (x->c == 8 && y->c == 8 && kh == 3)  // the 8-channel kernel
+      return c8_bf16_views(x, y, kh, stride, pad) ? run_direct(x, w, ep, kh, stride, pad, y, s) : CB_ERR_ALIGNMENT;
     if (!tc_bf16_views(x, y, kh, stride, pad)) return CB_ERR_ALIGNMENT;
   }
   HaloPlan plan;

@@ -408,6 +408,7 @@ cudaError_t launch_direct(const DirectArgs& a, int sms, cudaStream_t s) {
                                               a.ep.rs_h % 4 == 0 && a.ep.rs_n % 4 == 0));
   const int vec = vec_ok ? 1 : 0;
   if (conv3x3_c8_ok(a)) return launch_conv3x3_c8(a, sms, s);
+  if (a.bf16) return cudaErrorInvalidValue;  // bf16 storage: the 8-channel kernel only
   if (a.Ci <= 16 && a.kh == a.kw && (a.kh == 1 || a.kh == 3) && (a.stride == 1 || a.stride == 2)) {
     cudaError_t e;
     if (a.stride == 1)

@@ -198,8 +198,10 @@ cudaError_t launch_dw_block(const CUtensorMap& pw_map, const CUtensorMap& sk_map
 // ------------------------------------------------------------------- stem
 // 3 -> 16 channels, 3x3, stride 2, pad 1, CUDA cores (stem.cu).  Input:
 // planar fp32 (src_kind 0: x[n*xs_n + c*xs_c + h*xs_h + w]), packed NHWC
-// fp32 (1: x[n*xs_n + h*xs_h + 3*w + c]) or u8 frames preprocessed on the
-// fly (2: [n][hs][pitch] bytes, 3 channels per pixel, resized to H x W).
+// fp32 (1: x[n*xs_n + h*xs_h + 3*w + c]), u8 frames preprocessed on the
+// fly (2: [n][hs][pitch] bytes, 3 channels per pixel, resized to H x W), or
+// packed NHWC bf16 (3, with bf16 output and residual; W % 8 == 0, strides
+// multiples of 8 elements).
 // Needs W % 4 == 0, 16-byte aligned bases and strides that are multiples of
 // 4 elements (of 16 bytes for the frames, whose rows are a multiple of 16
 // bytes), a 16-byte aligned output view with strides that are multiples of 4.

@@ -34,6 +34,8 @@
 #include "ptx.cuh"
 #include "resample.cuh"
 
+#include <type_traits>
+
 namespace cb {
 
 namespace {
@@ -48,6 +50,12 @@ constexpr int kPlane = kRows * kCols;     // floats per channel plane
 constexpr int kTileF = 3 * kPlane;        // floats per staged tile (a multiple of 4)
 constexpr int kRawRow = 3 * kCols;        // floats per packed NHWC row of the tile
 constexpr int kFixedF = 27 * 16 + 16 + 16 + 256;  // weights, scale, bias, u8 / 255 table
+// bf16 NHWC input (SRC 3): rows staged from input column 2 * ow0 - 8, so that
+// the 6-byte pixels start on a 16-byte boundary; 136 pixels = 17 groups of 8
+// (48 bytes, three 16-byte copies), plane column = staged pixel - 4.
+constexpr int kBfGroups = (kCols + 4) / 8;
+constexpr int kBfRawRowB = kBfGroups * 48;        // bytes per staged bf16 row
+static_assert(kBfRawRowB <= kRawRow * 4, "a bf16 row fits in an fp32 row's room");
 
 static_assert(kTileF % 4 == 0 && kRawRow % 4 == 0 && kFixedF % 4 == 0, "16-byte aligned regions");
 
@@ -90,7 +98,8 @@ __device__ __forceinline__ SrcSpan src_span(const TilePos& p, const StemArgs& a,
 }
 
 // Issues the copies of tile t: planar input into `pl` (SRC 0), packed NHWC
-// rows into `raw` (SRC 1), source rows of the u8 frames into `raw` (SRC 2).
+// rows into `raw` (SRC 1; SRC 3 for bf16), source rows of the u8 frames into
+// `raw` (SRC 2).
 template <int SRC>
 __device__ __forceinline__ void issue_tile(int t, const StemArgs& a, float* pl, float* raw, float scale_y,
                                            float scale_x) {
@@ -123,6 +132,19 @@ __device__ __forceinline__ void issue_tile(int t, const StemArgs& a, float* pl, 
         cp_async16_z(d + 4 * k, ok ? x + base + 4 * k : x, ok);
       }
     }
+  } else if (SRC == 3) {
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.src);
+    for (int r = warp; r < kRows; r += kThreads / 32) {
+      const int ih = p.ih0 + r;
+      const bool row_ok = ih >= 0 && ih < a.H;
+      const long long base = p.n * a.xs_n + static_cast<long long>(ih) * a.xs_h + 3LL * (p.iw0 - 4);
+      uint8_t* d = reinterpret_cast<uint8_t*>(raw) + r * kBfRawRowB;
+      for (int k = lane; k < 3 * kBfGroups; k += 32) {
+        const int col = p.iw0 - 4 + 8 * (k / 3);  // first pixel of the 8-pixel group this chunk is in
+        const bool ok = row_ok && col >= 0 && col < a.W;
+        cp_async16_z(d + 16 * k, ok ? x + base + 8 * k : x, ok);
+      }
+    }
   } else {
     const uint8_t* src = static_cast<const uint8_t*>(a.src);
     const SrcSpan s = src_span(p, a, scale_y, scale_x);
@@ -138,11 +160,33 @@ __device__ __forceinline__ void issue_tile(int t, const StemArgs& a, float* pl, 
   }
 }
 
-// Builds the three input planes of tile t from the raw buffer (SRC 1, 2).
+// Builds the three input planes of tile t from the raw buffer (SRC 1, 2, 3).
 template <int SRC>
 __device__ __forceinline__ void fill_tile(int t, const StemArgs& a, const float* raw, float* pl, const float* inv255,
                                           float scale_y, float scale_x) {
-  if (SRC == 1) {
+  if (SRC == 3) {
+    // 8 bf16 pixels (24 values, three 16-byte loads) per group, widened to
+    // fp32 (exact) and split into the planes; plane column = staged pixel - 4
+    for (int i = threadIdx.x; i < kRows * kBfGroups; i += kThreads) {
+      const int r = i / kBfGroups, g = i - r * kBfGroups;
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(raw) + r * kBfRawRowB + 48 * g);
+      const uint4 u0 = src[0], u1 = src[1], u2 = src[2];
+      const uint32_t w[12] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w, u2.x, u2.y, u2.z, u2.w};
+      float f[24];
+#pragma unroll
+      for (int k = 0; k < 12; ++k) {
+        f[2 * k] = __uint_as_float(w[k] << 16);
+        f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+      float* d = pl + r * kCols + 8 * g - 4;
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        if (g > 0)
+          *reinterpret_cast<float4*>(d + c * kPlane) = make_float4(f[c], f[3 + c], f[6 + c], f[9 + c]);
+        *reinterpret_cast<float4*>(d + 4 + c * kPlane) = make_float4(f[12 + c], f[15 + c], f[18 + c], f[21 + c]);
+      }
+    }
+  } else if (SRC == 1) {
     for (int i = threadIdx.x; i < kRows * kChunks; i += kThreads) {
       const int r = i / kChunks, g = i - r * kChunks;
       const float4* s = reinterpret_cast<const float4*>(raw + r * kRawRow + 12 * g);
@@ -200,7 +244,7 @@ __device__ __forceinline__ void fill_tile(int t, const StemArgs& a, const float*
 
 // The 2 x 2 output pixels x 16 channels of thread (tx, ty) in tile t, from
 // the staged planes, through the epilogue to memory.
-template <int ACT, bool RES>
+template <int ACT, bool RES, typename TO = float>
 __device__ __forceinline__ void conv_tile(int t, const StemArgs& a, const float* pl, const float* ws,
                                           const float* sc, const float* bi) {
   const TilePos p = tile_pos(t, a);
@@ -254,7 +298,7 @@ __device__ __forceinline__ void conv_tile(int t, const StemArgs& a, const float*
     }
   }
 
-  float* const y = a.out.y + p.n * a.out.ys_n;
+  TO* const y = reinterpret_cast<TO*>(a.out.y) + p.n * a.out.ys_n;
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int oh = p.oh0 + 2 * ty + r;
@@ -263,8 +307,9 @@ __device__ __forceinline__ void conv_tile(int t, const StemArgs& a, const float*
     for (int q = 0; q < 2; ++q) {
       const int ow = p.ow0 + 2 * tx + q;
       if (ow >= a.OW) continue;
-      float* yp = y + oh * a.out.ys_h + ow * a.out.ys_w;
-      const float* rp = RES ? a.ep.r + p.n * a.ep.rs_n + oh * a.ep.rs_h + ow * a.ep.rs_w : nullptr;
+      TO* yp = y + oh * a.out.ys_h + ow * a.out.ys_w;
+      const TO* rp =
+          RES ? reinterpret_cast<const TO*>(a.ep.r) + p.n * a.ep.rs_n + oh * a.ep.rs_h + ow * a.ep.rs_w : nullptr;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float4 s4 = reinterpret_cast<const float4*>(sc)[j], b4 = reinterpret_cast<const float4*>(bi)[j];
@@ -274,7 +319,7 @@ __device__ __forceinline__ void conv_tile(int t, const StemArgs& a, const float*
           o = make_float4(epi_t<ACT, 0>(lo.x, s4.x, b4.x, 0.0f), epi_t<ACT, 0>(lo.y, s4.y, b4.y, 0.0f),
                           epi_t<ACT, 0>(hi.x, s4.z, b4.z, 0.0f), epi_t<ACT, 0>(hi.y, s4.w, b4.w, 0.0f));
         } else {
-          const float4 rv = *reinterpret_cast<const float4*>(rp + 4 * j);
+          const float4 rv = load4(rp + 4 * j);
           if (a.ep.res_mode == 1)
             o = make_float4(epi_t<ACT, 1>(lo.x, s4.x, b4.x, rv.x), epi_t<ACT, 1>(lo.y, s4.y, b4.y, rv.y),
                             epi_t<ACT, 1>(hi.x, s4.z, b4.z, rv.z), epi_t<ACT, 1>(hi.y, s4.w, b4.w, rv.w));
@@ -282,7 +327,7 @@ __device__ __forceinline__ void conv_tile(int t, const StemArgs& a, const float*
             o = make_float4(epi_t<ACT, 2>(lo.x, s4.x, b4.x, rv.x), epi_t<ACT, 2>(lo.y, s4.y, b4.y, rv.y),
                             epi_t<ACT, 2>(hi.x, s4.z, b4.z, rv.z), epi_t<ACT, 2>(hi.y, s4.w, b4.w, rv.w));
         }
-        *reinterpret_cast<float4*>(yp + 4 * j) = o;
+        store4(yp + 4 * j, o);
       }
     }
   }
@@ -339,8 +384,9 @@ __global__ void __launch_bounds__(kThreads, 4) stem_kernel(const StemArgs a) {
       const int next = tile + gridDim.x;
       if (next < num_tiles) issue_tile<SRC>(next, a, nullptr, pl1, scale_y, scale_x);
       asm volatile("cp.async.commit_group;" ::: "memory");
-      if (SRC != 2 && a.ep.res_mode) conv_tile<ACT, true>(tile, a, pl0, ws, sc, bi);  // frames: no residual
-      else conv_tile<ACT, false>(tile, a, pl0, ws, sc, bi);
+      using TO = std::conditional_t<SRC == 3, __nv_bfloat16, float>;  // bf16 input: bf16 output
+      if (SRC != 2 && a.ep.res_mode) conv_tile<ACT, true, TO>(tile, a, pl0, ws, sc, bi);  // frames: no residual
+      else conv_tile<ACT, false, TO>(tile, a, pl0, ws, sc, bi);
     }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
@@ -371,7 +417,7 @@ cudaError_t launch_src(const StemArgs& a, size_t smem, int sms, cudaStream_t s) 
 
 size_t stem_smem_bytes(int src_kind, int src_rows, int row_cap) {
   const size_t fixed = static_cast<size_t>(kFixedF + kTileF) * sizeof(float);
-  if (src_kind == 0 || src_kind == 1) return fixed + static_cast<size_t>(kTileF) * sizeof(float);
+  if (src_kind == 0 || src_kind == 1 || src_kind == 3) return fixed + static_cast<size_t>(kTileF) * sizeof(float);
   return fixed + static_cast<size_t>(src_rows) * row_cap;
 }
 
@@ -395,6 +441,7 @@ cudaError_t launch_stem(const StemArgs& a, int src_kind, size_t smem, int sms, c
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   if (src_kind == 0) return launch_src<0>(a, smem, sms, s);
   if (src_kind == 1) return launch_src<1>(a, smem, sms, s);
+  if (src_kind == 3) return launch_src<3>(a, smem, sms, s);
   return launch_src<2>(a, smem, sms, s);
 }
 

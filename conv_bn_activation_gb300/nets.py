@@ -131,8 +131,12 @@ class MnistNet:
 
 
 class YoloChain:
-    def __init__(self, stages, batch, size=640, device="cuda"):
+    """dtype: the activations' storage type (torch.float32, or torch.bfloat16: every layer then
+    reads and writes bf16, the tensor-core layers multiply bf16 weights)."""
+
+    def __init__(self, stages, batch, size=640, device="cuda", dtype=torch.float32):
         self.batch = batch
+        self.dtype = dtype
         self.layers = []
         self.bufs = []
         H = size
@@ -140,15 +144,16 @@ class YoloChain:
             c = st["down_w"].shape[0]
             h = c // 2
             OH = out_size(H, 3, 2, 1)
+            kw = dict(device=device, dtype=dtype)
             L = {
-                "down": ConvBnAct(st["down_w"], st["down_bn"], 2, 1, cb.ACT_SILU, device=device),
-                "cv1": ConvBnAct(st["cv1_w"], st["cv1_bn"], 1, 0, cb.ACT_SILU, device=device),
-                "cv2": ConvBnAct(st["cv2_w"], st["cv2_bn"], 1, 1, cb.ACT_SILU, device=device),
-                "cv3": ConvBnAct(st["cv3_w"], st["cv3_bn"], 1, 0, cb.ACT_SILU, device=device),
+                "down": ConvBnAct(st["down_w"], st["down_bn"], 2, 1, cb.ACT_SILU, **kw),
+                "cv1": ConvBnAct(st["cv1_w"], st["cv1_bn"], 1, 0, cb.ACT_SILU, **kw),
+                "cv2": ConvBnAct(st["cv2_w"], st["cv2_bn"], 1, 1, cb.ACT_SILU, **kw),
+                "cv3": ConvBnAct(st["cv3_w"], st["cv3_bn"], 1, 0, cb.ACT_SILU, **kw),
             }
-            B = {"x1": torch.empty(batch, OH, OH, c, device=device),
-                 "cat": torch.empty(batch, OH, OH, c, device=device),
-                 "out": torch.empty(batch, OH, OH, c, device=device), "half": h}
+            B = {"x1": torch.empty(batch, OH, OH, c, device=device, dtype=dtype),
+                 "cat": torch.empty(batch, OH, OH, c, device=device, dtype=dtype),
+                 "out": torch.empty(batch, OH, OH, c, device=device, dtype=dtype), "half": h}
             self.layers.append(L)
             self.bufs.append(B)
             H = OH

@@ -122,8 +122,8 @@ def test_bf16_views_validated_before_launch(cblib):
     y32 = v(base + (1 << 16), 1, 8, 8, 16, cblib.DTYPE_F32)
     call = lambda xv, yv, g=1, r=None, rm=0: lib.cb_conv_bn_act(
         T(xv), w, s, b, 3, 3, 1, 1, g, 0, T(r) if r is not None else None, rm, T(yv), None)
-    x8 = v(base, 1, 8, 8, 8, cblib.DTYPE_BF16)
-    assert call(x8, v(base + (1 << 16), 1, 8, 8, 8, cblib.DTYPE_BF16), g=1) == cblib.ERR_UNSUPPORTED  # 3x3, 8 ch
+    x12 = v(base, 1, 8, 8, 12, cblib.DTYPE_BF16)
+    assert call(x12, v(base + (1 << 16), 1, 8, 8, 12, cblib.DTYPE_BF16), g=1) == cblib.ERR_UNSUPPORTED  # 3x3, 12 ch
     assert call(x16, y32, g=16) == cblib.ERR_INVALID_ARG                     # mixed element types
     assert call(x16, y16, g=16, r=v(base + (1 << 17), 1, 8, 8, 16, cblib.DTYPE_F32), rm=2) == cblib.ERR_INVALID_ARG
     assert call(v(base, 1, 8, 8, 16, 7), v(base + (1 << 16), 1, 8, 8, 16, 7), g=16) == cblib.ERR_INVALID_ARG

@@ -136,10 +136,10 @@ def test_bf16_rejections(gpu):
     with pytest.raises(cb.CbError) as e:
         layer(xs, torch.empty(1, 6, 6, 16, dtype=torch.bfloat16, device=gpu))
     assert e.value.status == cb.ERR_ALIGNMENT
-    xdense, wd, bnd = synthetic.dense_layer(8, 8, 8, N=1, k=3)  # 3x3 with 8 channels: no bf16 kernel
+    xdense, wd, bnd = synthetic.dense_layer(12, 12, 8, N=1, k=3)  # 3x3 with 12 channels: no bf16 kernel
     dense = ConvBnAct(wd, bnd, 1, 1, cb.ACT_SILU)
     x16, _ = to_dev_bf16(xdense)
-    y16 = torch.empty(1, 8, 8, 8, dtype=torch.bfloat16, device=gpu)
+    y16 = torch.empty(1, 8, 8, 12, dtype=torch.bfloat16, device=gpu)
     assert cb.conv_path(x16, y16, 3, 1, 1) == 0
     with pytest.raises(cb.CbError) as e:
         dense(x16, y16)

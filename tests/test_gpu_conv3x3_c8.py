@@ -78,3 +78,31 @@ def test_c8_unaligned_views_take_the_generic_kernel(gpu, orc):
     assert "conv3x3_c8" not in cb.last_launch()["kernel"]
     ref = orc.conv_bn_act(x, w, bn, stride=1, pad=1, act=orc.ACT_RELU)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_FP32
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (2, 33, 33), (1, 5, 70), (3, 70, 5), (2, 64, 31)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("act,res_mode", [(2, 0), (1, 1), (2, 2)])
+def test_c8_bf16(gpu, orc, shape, act, res_mode):
+    """bf16 storage (x, y, residual bf16; fp32 weights and arithmetic): within half a bf16 ulp of the
+    oracle on the same bf16 values, and bit-equal to the fp32 kernel's output rounded to bf16 (the
+    two run the same fp32 sums)."""
+    from gpu_util import bf16_within_half_ulp, to_dev_bf16
+    N, H, W = shape
+    x, w, bn = synthetic.dense_layer(8, 8, H, W, N=N, k=3, seed=H + W + act)
+    r = np.random.default_rng(res_mode).standard_normal((N, H, W, 8)).astype(np.float32)
+    xd, xv = to_dev_bf16(x)
+    rd, rv = to_dev_bf16(r)
+    layer = ConvBnAct(w, bn, 1, 1, act)
+    y = torch.empty(N, H, W, 8, dtype=torch.bfloat16, device=gpu)
+    assert cb.conv_path(xd, y, 3, 1, 1) == cb.PATH_DIRECT
+    layer(xd, y, residual=rd if res_mode else None, res_mode=res_mode)
+    sync_check()
+    assert "conv3x3_c8" in cb.last_launch()["kernel"]
+    ref = orc.conv_bn_act(xv, w, bn, stride=1, pad=1, act=act, residual=rv if res_mode else None, res_mode=res_mode)
+    assert bf16_within_half_ulp(y.float().cpu().numpy(), ref) <= 1.0
+    y32 = torch.empty(N, H, W, 8, device=gpu)
+    layer(torch.from_numpy(xv).to(gpu), y32, residual=torch.from_numpy(rv).to(gpu) if res_mode else None,
+          res_mode=res_mode)
+    sync_check()
+    assert torch.equal(y.view(torch.int16), y32.to(torch.bfloat16).view(torch.int16))

@@ -218,3 +218,45 @@ def test_preprocess_stem_fused_rejects(gpu):
         cb.preprocess_stem_u8(src, (8, 14), layer.w, layer.scale, layer.bias, cb.ACT_SILU,
                               torch.empty(1, 4, 7, 16, device="cuda"))
     assert e.value.status == cb.ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("shape", [(2, 64, 64), (1, 30, 56), (3, 17, 136), (1, 2, 8), (2, 40, 200), (1, 33, 264)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("act,res_mode", [(2, 0), (1, 1), (2, 2)])
+def test_stem_bf16(gpu, orc, shape, act, res_mode):
+    """bf16 storage (packed NHWC bf16 input, bf16 output and residual; fp32 weights and arithmetic):
+    rows staged from a 16-byte boundary 8 pixels to the left of the fp32 kernel's; within half a bf16
+    ulp of the oracle on the same bf16 values, and bit-equal to the fp32 kernel's output rounded."""
+    from gpu_util import bf16_within_half_ulp, to_dev_bf16
+    N, H, W = shape
+    x = np.random.default_rng(H * W + act).standard_normal((N, H, W, 3)).astype(np.float32)
+    w, bn = _stem(N + H + res_mode)
+    layer = ConvBnAct(w, bn, 2, 1, act)
+    OH, OW = layer.out_hw(H, W)
+    r = np.random.default_rng(res_mode).standard_normal((N, OH, OW, 16)).astype(np.float32)
+    xd, xv = to_dev_bf16(x)
+    rd, rv = to_dev_bf16(r)
+    y = torch.empty(N, OH, OW, 16, dtype=torch.bfloat16, device=gpu)
+    assert cb.conv_path(xd, y, 3, 2, 1) == cb.PATH_STEM
+    layer(xd, y, residual=rd if res_mode else None, res_mode=res_mode)
+    sync_check()
+    ref = orc.conv_bn_act(xv, w, bn, stride=2, pad=1, act=act, residual=rv if res_mode else None,
+                          res_mode=res_mode)
+    assert bf16_within_half_ulp(y.float().cpu().numpy(), ref) <= 1.0
+    y32 = torch.empty(N, OH, OW, 16, device=gpu)
+    layer(torch.from_numpy(xv).to(gpu), y32, residual=torch.from_numpy(rv).to(gpu) if res_mode else None,
+          res_mode=res_mode)
+    sync_check()
+    assert torch.equal(y.view(torch.int16), y32.to(torch.bfloat16).view(torch.int16))
+
+
+def test_stem_bf16_needs_width_multiple_of_8(gpu):
+    """bf16 rows are staged in 16-byte groups of 8 pixels: other widths have no bf16 stem kernel."""
+    w, bn = _stem(1)
+    layer = ConvBnAct(w, bn, 2, 1, cb.ACT_SILU)
+    x = torch.zeros(1, 8, 12, 3, dtype=torch.bfloat16, device=gpu)
+    y = torch.empty(1, 4, 6, 16, dtype=torch.bfloat16, device=gpu)
+    assert cb.conv_path(x, y, 3, 2, 1) == 0
+    with pytest.raises(cb.CbError) as e:
+        layer(x, y)
+    assert e.value.status == cb.ERR_ALIGNMENT

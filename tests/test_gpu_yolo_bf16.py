@@ -1,0 +1,70 @@
+"""GPU parity of the YOLO-style chain with bf16 storage: every layer reads and writes bfloat16 --
+the stem and the 8-channel 3x3 layer on the CUDA cores (fp32 arithmetic), the narrow 1x1 layers on
+the streaming kernel (fp32 arithmetic), the other layers on the tensor cores with bf16 weights and
+fp32 accumulation.
+
+Per layer, the oracle is fed the GPU's own bf16 input and the weights the kernel uses (bf16 for
+the tensor-core layers, fp32 for the others); every output must lie within half a bf16 unit in the
+last place of it (2^-8 of the value plus the fp32 accumulation bar), and within 5e-3 of max|oracle|
+of the oracle with the fp32 weights.  The chain is checked at 96 x 96 (batch 2) and at its stated
+size, 640 x 640 batch 32.
+"""
+import numpy as np
+import pytest
+import torch
+
+from conv_bn_activation_gb300 import binding as cb, synthetic
+from conv_bn_activation_gb300.nets import YoloChain
+from gpu_util import TOL_BF16, bf16_within_half_ulp, rel_err, sync_check
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16_input(batch, size):
+    x = synthetic.yolo_input(batch, size=size)
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    return xt, xt.float().numpy()
+
+
+def _check_chain(orc, chain, stages, xv):
+    h = xv
+    for i, (st, L, B) in enumerate(zip(stages, chain.layers, chain.bufs)):
+        half = B["half"]
+        x1 = B["x1"].float().cpu().numpy()
+        cat = B["cat"].float().cpu().numpy()
+        out = B["out"].float().cpu().numpy()
+        a = np.ascontiguousarray(cat[..., :half])
+        checks = [
+            ("down", h, "down", 2, 1, x1, None),
+            ("cv1", x1, "cv1", 1, 0, a, None),
+            ("cv2", a, "cv2", 1, 1, np.ascontiguousarray(cat[..., half:]), None),
+            ("cv3", cat, "cv3", 1, 0, out, x1),
+        ]
+        for name, inp, key, s, p, got, res in checks:
+            w, bn = st[key + "_w"], st[key + "_bn"]
+            wk = cb.convert_weights_bf16(w).float().numpy() if L[key].tc_weights else w
+            kw = dict(stride=s, pad=p, act=orc.ACT_SILU, residual=res,
+                      res_mode=orc.RES_POST_ACT if res is not None else orc.RES_NONE)
+            ulp = bf16_within_half_ulp(got, orc.conv_bn_act(inp, wk, bn, **kw))
+            assert ulp <= 1.0, f"s{i}.{name}: {ulp:.3g} half-ulps"
+            err = rel_err(got, orc.conv_bn_act(inp, w, bn, **kw))
+            assert err <= TOL_BF16, f"s{i}.{name}: {err:.3g}"
+        h = out
+
+
+@pytest.mark.parametrize("batch,size", [(2, 96), (32, 640)], ids=["2x96", "32x640"])
+def test_yolo_chain_bf16_every_layer(gpu, orc, batch, size):
+    stages = synthetic.yolo_params()
+    xt, xv = _bf16_input(batch, size)
+    chain = YoloChain(stages, batch, size=size, dtype=torch.bfloat16)
+    xd = xt.to(gpu)
+    kinds = []
+    for L, B, x_in in zip(chain.layers, chain.bufs, [xd] + [b["out"] for b in chain.bufs[:-1]]):
+        half = B["half"]
+        for key, xi, yo in (("down", x_in, B["x1"]), ("cv1", B["x1"], B["cat"][..., :half]),
+                            ("cv2", B["cat"][..., :half], B["cat"][..., half:]), ("cv3", B["cat"], B["out"])):
+            kinds.append(cb.conv_path(xi, yo, L[key].k, L[key].stride, L[key].pad))
+    assert all(k != 0 for k in kinds)
+    chain.forward(xd)
+    sync_check()
+    _check_chain(orc, chain, stages, xv)
