@@ -455,17 +455,24 @@ class YoloWorkload(Workload):
                    ["pointwise.cu", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
     }
 
+    bf16 = False
+
     def __init__(self, torch, device, batch=32):
         from conv_bn_activation_gb300 import binding as cb, synthetic, workloads
         from conv_bn_activation_gb300.nets import YoloChain
         self.torch, self.batch = torch, batch
         self.stages = synthetic.yolo_params()
-        self.x_host = synthetic.yolo_input(batch)
-        self.x = _t(torch, self.x_host, device)
-        self.chain = YoloChain(self.stages, batch, device=device)
+        dt = torch.bfloat16 if self.bf16 else torch.float32
+        self.x_src = torch.from_numpy(synthetic.yolo_input(batch)).to(dt)
+        self.x_host = self.x_src.float().numpy()  # the values the chain reads, for the oracle
+        self.x = self.x_src.to(device)
+        self.chain = YoloChain(self.stages, batch, device=device, dtype=dt)
         if AUTOTUNE:
             self.chain.forward(self.x, tune=True)
-        works = dict(workloads.yolo_layers(N=batch))
+        eb = 2 if self.bf16 else 4
+        works = dict(workloads.yolo_layers(
+            N=batch, act_bytes=eb,
+            tc_w_bytes=lambda ci, co, k, s: eb if cb.layer_uses_tensor_cores(ci, co, k, s) else 4))
         self.launches = []
         prev = lambda: self.x
         for i, (L, B) in enumerate(zip(self.chain.layers, self.chain.bufs)):
@@ -485,21 +492,25 @@ class YoloWorkload(Workload):
                 kname, bound = kernel_of(cb, xv, yv, L[nm].k, L[nm].stride, L[nm].pad)
                 self.launches.append(Launch(f"s{i}.{nm}", fn, works[f"s{i}.{nm}"], kname, bound))
             prev = (lambda B=B: lambda: B["out"])()
+        storage = ("bf16 storage: every layer reads and writes bf16, tensor-core layers multiply bf16 "
+                   "weights, fp32 accumulation" if self.bf16 else "fp32")
         self.config = {"workload": "YOLO-style 20-conv chain (5 stages, concat via channel views, post-act "
-                                   "residual), 640x640x3 fp32", "batch": batch,
-                       "l2": "inputs_larger_than_l2 (157 MB input, 1.2 GB of activations per step)",
+                                   f"residual), 640x640x3, {storage}", "batch": batch,
+                       "l2": f"inputs_larger_than_l2 ({157 * eb // 4} MB input, {1.2 * eb / 4:.1f} GB of "
+                             "activations per step)",
                        "autotune": AUTOTUNE}
 
     def e2e_setup(self):
         t = self.torch
-        self.x_pin = t.from_numpy(self.x_host).pin_memory()
+        self.x_pin = self.x_src.pin_memory()
         out = self.chain.bufs[-1]["out"]
-        self.out_pin = t.empty(tuple(out.shape), pin_memory=True)
+        self.out_pin = t.empty(tuple(out.shape), dtype=out.dtype, pin_memory=True)
         # a second device input buffer and a copy stream: step i + 1's input
         # crosses the link while step i computes
         self.x_bufs = [self.x, t.empty_like(self.x)]
         self.copy_stream = t.cuda.Stream(self.x.device)
-        return self.x_pin.numel() * 4, self.out_pin.numel() * 4
+        return (self.x_pin.numel() * self.x_pin.element_size(),
+                self.out_pin.numel() * self.out_pin.element_size())
 
     def e2e_step(self, stream):
         self.x.copy_(self.x_pin, non_blocking=True)
@@ -554,6 +565,12 @@ class YoloWorkload(Workload):
         for st in self.stages:
             h = oracle.yolo_stage(h, st).astype(np.float32)
         return time.perf_counter() - t0, n, f"{n} of {self.batch} images"
+
+
+class YoloBf16Workload(YoloWorkload):
+    """The YOLO-style chain with bf16 storage."""
+    bf16 = True
+    tc_dtype = "bf16"
 
 
 class PreprocessWorkload(Workload):
@@ -758,7 +775,8 @@ class PointwiseBf16Workload(PointwiseWorkload):
 
 WORKLOADS = {"depthwise": DepthwiseWorkload, "depthwise_bf16": DepthwiseBf16Workload, "pointwise": PointwiseWorkload,
              "pointwise_bf16": PointwiseBf16Workload, "dense": DenseWorkload, "dense_bf16": DenseBf16Workload,
-             "mnist": MnistWorkload, "yolo": YoloWorkload, "preprocess": PreprocessWorkload}
+             "mnist": MnistWorkload, "yolo": YoloWorkload, "yolo_bf16": YoloBf16Workload,
+             "preprocess": PreprocessWorkload}
 
 
 # ------------------------------------------------------------ arms
@@ -1018,7 +1036,8 @@ def measure(torch, wl, device, stream, args, steps, warmup, min_timed_s, world, 
 EXTRA_CONFIGS = (("cfg0_mnist_b64", "mnist", 64), ("cfg1_depthwise_b64", "depthwise", 64),
                  ("cfg2_dense_b16", "dense", 16), ("cfg2_dense_b1", "dense", 1),
                  ("cfg3_yolo_b1", "yolo", 1), ("cfg4_preprocess_stem_b32", "preprocess", 32),
-                 ("bf16_dense_b16", "dense_bf16", 16), ("bf16_depthwise_b64", "depthwise_bf16", 64),
+                 ("bf16_yolo_b32", "yolo_bf16", 32), ("bf16_dense_b16", "dense_bf16", 16),
+                 ("bf16_depthwise_b64", "depthwise_bf16", 64),
                  ("bf16_pointwise_b32", "pointwise_bf16", 32))
 
 

@@ -112,18 +112,22 @@ def mnist_layers(N=64):
     return layers
 
 
-def yolo_layers(N=1, size=640):
-    """Per-layer work of the 20-conv YOLO-style chain."""
+def yolo_layers(N=1, size=640, act_bytes=F32, tc_w_bytes=None):
+    """Per-layer work of the 20-conv YOLO-style chain.  act_bytes: bytes per activation element;
+    tc_w_bytes(cin, cout, k, stride) -> bytes per weight of that layer (default 4)."""
     from .synthetic import YOLO_STAGES
+    wb = tc_w_bytes or (lambda ci, co, k, s: F32)
     layers = []
     H = size
     for i, (cin, c) in enumerate(YOLO_STAGES):
         h = c // 2
         OH = out_size(H, 3, 2, 1)
-        layers.append((f"s{i}.down", conv_layer(N, H, H, cin, c, 3, 2, 1)))
-        layers.append((f"s{i}.cv1", conv_layer(N, OH, OH, c, h, 1, 1, 0)))
-        layers.append((f"s{i}.cv2", conv_layer(N, OH, OH, h, h, 3, 1, 1)))
-        layers.append((f"s{i}.cv3", conv_layer(N, OH, OH, c, c, 1, 1, 0, residual=True)))
+        kw = dict(act_bytes=act_bytes)
+        layers.append((f"s{i}.down", conv_layer(N, H, H, cin, c, 3, 2, 1, w_bytes=wb(cin, c, 3, 2), **kw)))
+        layers.append((f"s{i}.cv1", conv_layer(N, OH, OH, c, h, 1, 1, 0, w_bytes=wb(c, h, 1, 1), **kw)))
+        layers.append((f"s{i}.cv2", conv_layer(N, OH, OH, h, h, 3, 1, 1, w_bytes=wb(h, h, 3, 1), **kw)))
+        layers.append((f"s{i}.cv3", conv_layer(N, OH, OH, c, c, 1, 1, 0, residual=True, w_bytes=wb(c, c, 1, 1),
+                                               **kw)))
         H = OH
     return layers
 
