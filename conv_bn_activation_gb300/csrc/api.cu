@@ -296,11 +296,12 @@ struct Tuning {
   int span_slot = 1;               // CB_SPAN_SLOT = 1 / 2 (trace builds)
   int timeout_ms = 2000;           // CB_TIMEOUT_MS: bound of every device wait
   int dw_skip_row = 0;             // CB_DEBUG_DW_SKIP_ROW = 1: fault injection (see cb_set_tuning)
+  int stem_kernel = 0;             // CB_STEM_KERNEL = "cuda" / "tc" (0: tensor cores for NHWC input)
 };
 
 const char* const kTuningNames[] = {"CB_DW_FORCE",    "CB_IGEMM_FORCE", "CB_IGEMM_BLOCKS", "CB_HALO_FORCE",
                                     "CB_DW_BLOCK_FORCE", "CB_DEBUG_PLAN", "CB_IGEMM_TRACE", "CB_SPAN_SLOT",
-                                    "CB_TIMEOUT_MS",  "CB_DEBUG_DW_SKIP_ROW"};
+                                    "CB_TIMEOUT_MS",  "CB_DEBUG_DW_SKIP_ROW", "CB_STEM_KERNEL"};
 
 // Sets knob `name` of *t from `v` (NULL or "" restores the knob's default);
 // false for an unknown name.
@@ -339,6 +340,8 @@ bool parse_tuning(Tuning* t, const char* name, const char* v) {
     t->timeout_ms = ms > 0 ? ms : d.timeout_ms;
   } else if (!std::strcmp(name, "CB_DEBUG_DW_SKIP_ROW")) {
     t->dw_skip_row = unset ? 0 : (std::atoi(v) != 0 ? 1 : 0);
+  } else if (!std::strcmp(name, "CB_STEM_KERNEL")) {
+    t->stem_kernel = unset ? 0 : !std::strcmp(v, "cuda") ? 1 : !std::strcmp(v, "tc") ? 2 : 0;
   } else {
     return false;
   }
@@ -1148,8 +1151,14 @@ cb_status run_stem(const cb_tensor* x, const float* w, const Epilogue& ep, const
   a.ep = ep;
   a.out = make_out(y);
   stem_tile_grid(a.OH, a.OW, &a.tiles_y, &a.tiles_x);
+  a.err = dev->err;
+  a.timeout_ns = timeout_ns();
   const int kind = !is_f32(x) ? 3 : x->layout == CB_LAYOUT_NCHW ? 0 : 1;
-  const cudaError_t e = launch_stem(a, kind, stem_smem_bytes(kind, 0, 0), dev->sms, s);
+  // packed NHWC input: the tensor-core kernel (fp32 accuracy from split TF32
+  // operands), unless CB_STEM_KERNEL = "cuda"; planar input: the CUDA-core kernel
+  const bool tc = (kind == 1 || kind == 3) && tuning().stem_kernel != 1 && stem_tc_ok(a);
+  const cudaError_t e =
+      tc ? launch_stem_tc(a, kind == 3, dev->sms, s) : launch_stem(a, kind, stem_smem_bytes(kind, 0, 0), dev->sms, s);
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
 }
 

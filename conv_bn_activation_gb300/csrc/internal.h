@@ -216,12 +216,20 @@ struct StemArgs {
   Epilogue ep;         // residual (if any): 16-byte aligned, strides multiples of 4
   OutView out;
   int tiles_x, tiles_y;
+  int* err;             // tensor-core kernel: device error word, bound of its waits
+  uint64_t timeout_ns;
 };
 void stem_tile_grid(int OH, int OW, int* tiles_y, int* tiles_x);
 // Staged source rows per tile and bytes per staged row for a hs x ws -> hd x wd resize.
 void stem_src_bounds(int hs, int ws, int hd, int wd, int* rows, int* row_cap);
 size_t stem_smem_bytes(int src_kind, int src_rows, int row_cap);
 cudaError_t launch_stem(const StemArgs& a, int src_kind, size_t smem, int sms, cudaStream_t s);
+// The same layer on the tensor cores (stem_tc.cu) at fp32 accuracy, for packed
+// NHWC input (src kinds 1 and 3: fp32, or bf16 storage with a bf16 output);
+// tiles_x / tiles_y are its own (2 x 64 output pixels).  stem_tc_ok: the tile
+// count fits the kernel's int tile index.
+bool stem_tc_ok(const StemArgs& a);
+cudaError_t launch_stem_tc(const StemArgs& a, bool bf16, int sms, cudaStream_t s);
 
 // -------------------------------------------------------------- preprocess
 cudaError_t launch_preprocess_fused(const uint8_t* src, int n, int hs, int ws, long long pitch, float* dst,

@@ -171,11 +171,14 @@ cb_status cb_convert_weights_bf16(const float* w, long long n, void* out);
  * multiples of 8 elements and y / residual strides that are multiples of 8
  * (depthwise) or 4 (the others) elements (else CB_ERR_ALIGNMENT); any other
  * bf16 layer returns CB_ERR_UNSUPPORTED;
- * 3 -> 16 channel 3x3 stride-2 pad-1 stems run on a dedicated fp32 CUDA-core
- * kernel when the input is planar (NCHW) or packed NHWC (stride_w == 3) with
+ * 3 -> 16 channel 3x3 stride-2 pad-1 stems run on a dedicated stem kernel
+ * when the input is planar (NCHW) or packed NHWC (stride_w == 3) with
  * W % 4 == 0, 16-byte aligned data and n / h (/ c) strides that are
  * multiples of 4 elements, and the output (and residual) is 16-byte aligned
- * with strides that are multiples of 4;
+ * with strides that are multiples of 4: for packed NHWC input on the tensor
+ * cores with each fp32 operand split into a TF32 head and tail (three
+ * products per term; bf16 input two), for planar input on CUDA cores; both
+ * are held to the fp32 bar (CB_STEM_KERNEL selects one for NHWC input);
  * everything else (stems with 1 or 3 input channels, NCHW input, odd channel
  * counts) runs on a direct CUDA-core kernel in fp32.
  */
@@ -396,7 +399,7 @@ typedef enum {
                              128 pixels x up to 256 channels per tile */
   CB_PATH_TC_HALO_CM = 5, /* the same with 256 pixels x 128 channels per tile, channels as the MMA's M */
   CB_PATH_POINTWISE = 6,  /* streaming fp32 CUDA-core 1x1 kernel for at most 32 input and output channels */
-  CB_PATH_STEM = 7        /* fp32 CUDA-core 3 -> 16 channel 3x3 stride-2 stem kernel */
+  CB_PATH_STEM = 7        /* 3 -> 16 channel 3x3 stride-2 stem kernel (fp32 accuracy) */
 } cb_path;
 
 /*
@@ -450,6 +453,8 @@ int cb_autotune_entries(void);
  *   CB_DEBUG_PLAN     any value: print each layer's plan to stderr
  *   CB_IGEMM_TRACE, CB_SPAN_SLOT   CTA timelines (trace builds only)
  *   CB_TIMEOUT_MS     bound of every device wait in milliseconds (default 2000)
+ *   CB_STEM_KERNEL    "cuda" / "tc": the 3 -> 16 stem of packed NHWC input on the
+ *                     CUDA-core kernel / the tensor-core kernel (the default)
  *   CB_DEBUG_DW_SKIP_ROW  "1": fault injection for tests of the bounded waits --
  *                     in the TMA depthwise kernel, the producer of CTA 0 withholds
  *                     the copy and barrier arrive of its first input row, so its

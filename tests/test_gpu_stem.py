@@ -1,9 +1,12 @@
-"""GPU parity of the 3 -> 16 channel stride-2 stem kernel and of the preprocess fused into it.
+"""GPU parity of the 3 -> 16 channel stride-2 stem kernels and of the preprocess fused into it.
 
-The stem kernel computes in fp32 on CUDA cores: the bar is the fp32 one (1e-5 of max|oracle|).
-Its inputs are planar NCHW (the preprocess output) or packed NHWC (the network input); shapes
-cover one and several 8 x 64 output tiles, ragged tile edges in both directions, tiny images, the
-epilogue variants, residuals and output views with padded rows.  The fused preprocess + stem
+Two kernels take the stem: on CUDA cores in fp32 (planar NCHW input -- the preprocess output --
+and, on request, packed NHWC), and on the tensor cores with each fp32 operand split into a TF32
+head and tail (packed NHWC input, the default there).  Both are held to the fp32 bar (1e-5 of
+max|oracle|); every NHWC case runs on both, and the test checks which kernel launched.  Shapes
+cover one and several output tiles (8 x 64 on CUDA cores, 2 x 64 on the tensor cores), ragged tile
+edges in both directions, tiny images, the epilogue variants, residuals and output views with
+padded rows.  The fused preprocess + stem
 kernel must produce, bit for bit, what the preprocess kernel followed by the stem kernel produce
 (the planar image it keeps in shared memory holds the preprocess's values and the convolution
 code is shared), and match the oracle's preprocess followed by the oracle's convolution.
@@ -26,19 +29,48 @@ def _stem(seed):
     return synthetic.kaiming(g, 16, 3, 3, 3), synthetic.bn_params(g, 16)
 
 
-def _run(x_dev, layer, OH, OW, layout, y=None, residual=None, res_mode=0):
+@pytest.fixture(params=["tc", "cuda"])
+def stem_kernel(request, gpu):
+    """The kernel packed NHWC stems take (CB_STEM_KERNEL); planar input always takes the CUDA-core one."""
+    with cb.tuning("CB_STEM_KERNEL", request.param):
+        yield request.param
+
+
+def _check_kernel(kernel, layout=cb.LAYOUT_NHWC):
+    name = cb.last_launch()["kernel"]
+    assert "stem" in name, name
+    assert ("stem_tc_kernel" in name) == (kernel == "tc" and layout == cb.LAYOUT_NHWC), name
+
+
+def _run(x_dev, layer, OH, OW, layout, y=None, residual=None, res_mode=0, kernel=None):
     N = x_dev.shape[0]
     if y is None:
         y = torch.empty(N, OH, OW, 16, device="cuda")
     assert cb.conv_path(x_dev, y, 3, 2, 1, x_layout=layout) == cb.PATH_STEM
     layer(x_dev, y, residual=residual, res_mode=res_mode, x_layout=layout)
+    if kernel is not None:
+        _check_kernel(kernel, layout)
     sync_check()
     return y
 
 
+def test_stem_nhwc_default_is_tensor_core(gpu, orc):
+    """With no override, packed NHWC fp32 and bf16 stems launch the tensor-core kernel, planar ones
+    the CUDA-core kernel."""
+    w, bn = _stem(2)
+    layer = ConvBnAct(w, bn, 2, 1, cb.ACT_SILU)
+    x = np.random.default_rng(2).standard_normal((1, 32, 64, 3)).astype(np.float32)
+    _run(to_dev(x), layer, 16, 32, cb.LAYOUT_NHWC, kernel="tc")
+    _run(to_dev(np.ascontiguousarray(x.transpose(0, 3, 1, 2))), layer, 16, 32, cb.LAYOUT_NCHW, kernel="tc")
+    y = torch.empty(1, 16, 32, 16, dtype=torch.bfloat16, device="cuda")
+    layer(to_dev(x).to(torch.bfloat16), y)
+    _check_kernel("tc")
+    sync_check()
+
+
 @pytest.mark.parametrize("layout", ["nhwc", "nchw"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_stem_silu(gpu, orc, layout, shape):
+def test_stem_silu(gpu, orc, stem_kernel, layout, shape):
     N, H, W = shape
     x = np.random.default_rng(H * W).standard_normal((N, H, W, 3)).astype(np.float32)
     w, bn = _stem(N + H)
@@ -46,28 +78,29 @@ def test_stem_silu(gpu, orc, layout, shape):
     OH, OW = layer.out_hw(H, W)
     if layout == "nchw":
         xp = np.ascontiguousarray(x.transpose(0, 3, 1, 2))
-        y = _run(to_dev(xp), layer, OH, OW, cb.LAYOUT_NCHW)
+        y = _run(to_dev(xp), layer, OH, OW, cb.LAYOUT_NCHW, kernel=stem_kernel)
         ref = orc.conv_bn_act(xp, w, bn, stride=2, pad=1, act=orc.ACT_SILU, layout=orc.NCHW)
     else:
-        y = _run(to_dev(x), layer, OH, OW, cb.LAYOUT_NHWC)
+        y = _run(to_dev(x), layer, OH, OW, cb.LAYOUT_NHWC, kernel=stem_kernel)
         ref = orc.conv_bn_act(x, w, bn, stride=2, pad=1, act=orc.ACT_SILU)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_FP32
 
 
 @pytest.mark.parametrize("act,res_mode", [(0, 0), (1, 0), (1, 1), (2, 2), (0, 2), (2, 1)])
-def test_stem_epilogues(gpu, orc, act, res_mode):
+def test_stem_epilogues(gpu, orc, stem_kernel, act, res_mode):
     N, H, W = 2, 26, 136
     x = np.random.default_rng(act).standard_normal((N, H, W, 3)).astype(np.float32)
     w, bn = _stem(7 + act)
     layer = ConvBnAct(w, bn, 2, 1, act)
     OH, OW = layer.out_hw(H, W)
     r = np.random.default_rng(5).standard_normal((N, OH, OW, 16)).astype(np.float32)
-    y = _run(to_dev(x), layer, OH, OW, cb.LAYOUT_NHWC, residual=to_dev(r) if res_mode else None, res_mode=res_mode)
+    y = _run(to_dev(x), layer, OH, OW, cb.LAYOUT_NHWC, residual=to_dev(r) if res_mode else None, res_mode=res_mode,
+             kernel=stem_kernel)
     ref = orc.conv_bn_act(x, w, bn, stride=2, pad=1, act=act, residual=r if res_mode else None, res_mode=res_mode)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_FP32
 
 
-def test_stem_output_slice_with_padded_rows(gpu, orc):
+def test_stem_output_slice_with_padded_rows(gpu, orc, stem_kernel):
     """Output into channels [16, 32) of a 40-channel buffer with padded rows: nothing else is written."""
     N, H, W = 2, 20, 100
     x = np.random.default_rng(3).standard_normal((N, H, W, 3)).astype(np.float32)
@@ -76,7 +109,7 @@ def test_stem_output_slice_with_padded_rows(gpu, orc):
     OH, OW = layer.out_hw(H, W)
     buf = canary_buffer((N, OH, OW + 7, 40))
     y = buf[:, :, :OW, 16:32]
-    _run(to_dev(x), layer, OH, OW, cb.LAYOUT_NHWC, y=y)
+    _run(to_dev(x), layer, OH, OW, cb.LAYOUT_NHWC, y=y, kernel=stem_kernel)
     ref = orc.conv_bn_act(x, w, bn, stride=2, pad=1, act=orc.ACT_SILU)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_FP32
     assert is_canary(buf[:, :, OW:, :]) and is_canary(buf[:, :, :OW, :16]) and is_canary(buf[:, :, :OW, 32:])
@@ -111,12 +144,12 @@ def test_stem_not_taken_outside_its_shapes(gpu, orc):
     assert rel_err(yy.cpu().numpy(), ref) <= TOL_FP32
 
 
-@pytest.mark.parametrize("case", ["yolo_640_b32", "preprocess_480x640_b32"])
+@pytest.mark.parametrize("case", ["yolo_640_b32", "yolo_640_b32_cuda", "preprocess_480x640_b32"])
 def test_stem_full_size_sampled(gpu, orc, case):
     """The workloads' stems at full size, in the launch configuration the benchmark times;
     sampled outputs against the oracle point by point (first and last included)."""
     rng = np.random.default_rng(11)
-    if case == "yolo_640_b32":
+    if case.startswith("yolo_640_b32"):
         x = rng.random((32, 640, 640, 3), dtype=np.float32)
         layout, okw = cb.LAYOUT_NHWC, {}
     else:
@@ -126,7 +159,9 @@ def test_stem_full_size_sampled(gpu, orc, case):
     layer = ConvBnAct(w, bn, 2, 1, cb.ACT_SILU)
     H, W = (x.shape[1], x.shape[2]) if layout == cb.LAYOUT_NHWC else (x.shape[2], x.shape[3])
     OH, OW = layer.out_hw(H, W)
-    y = _run(to_dev(x), layer, OH, OW, layout)
+    kernel = "cuda" if case.endswith("cuda") else "tc"
+    with cb.tuning("CB_STEM_KERNEL", kernel):
+        y = _run(to_dev(x), layer, OH, OW, layout, kernel=kernel)
     idx = rng.choice(y.numel(), 6000, replace=False)
     idx = np.concatenate([idx, [0, y.numel() - 1]])
     ref = orc.conv_bn_act_points(x, w, bn, idx, stride=2, pad=1, act=orc.ACT_SILU, **okw)
@@ -223,10 +258,12 @@ def test_preprocess_stem_fused_rejects(gpu):
 @pytest.mark.parametrize("shape", [(2, 64, 64), (1, 30, 56), (3, 17, 136), (1, 2, 8), (2, 40, 200), (1, 33, 264)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("act,res_mode", [(2, 0), (1, 1), (2, 2)])
-def test_stem_bf16(gpu, orc, shape, act, res_mode):
-    """bf16 storage (packed NHWC bf16 input, bf16 output and residual; fp32 weights and arithmetic):
-    rows staged from a 16-byte boundary 8 pixels to the left of the fp32 kernel's; within half a bf16
-    ulp of the oracle on the same bf16 values, and bit-equal to the fp32 kernel's output rounded."""
+def test_stem_bf16(gpu, orc, stem_kernel, shape, act, res_mode):
+    """bf16 storage (packed NHWC bf16 input, bf16 output and residual; fp32 weights, fp32-accurate
+    arithmetic): rows staged from a 16-byte boundary 8 pixels to the left of the fp32 kernel's;
+    within half a bf16 ulp of the oracle on the same bf16 values, and bit-equal to the same kernel's
+    fp32 output rounded (bf16 values have no TF32 tail: the fp32 tensor-core kernel's extra
+    product adds zeros)."""
     from gpu_util import bf16_within_half_ulp, to_dev_bf16
     N, H, W = shape
     x = np.random.default_rng(H * W + act).standard_normal((N, H, W, 3)).astype(np.float32)
@@ -239,6 +276,7 @@ def test_stem_bf16(gpu, orc, shape, act, res_mode):
     y = torch.empty(N, OH, OW, 16, dtype=torch.bfloat16, device=gpu)
     assert cb.conv_path(xd, y, 3, 2, 1) == cb.PATH_STEM
     layer(xd, y, residual=rd if res_mode else None, res_mode=res_mode)
+    _check_kernel(stem_kernel)
     sync_check()
     ref = orc.conv_bn_act(xv, w, bn, stride=2, pad=1, act=act, residual=rv if res_mode else None,
                           res_mode=res_mode)
