@@ -11,37 +11,43 @@
 //
 // fp32 accuracy from TF32 operands (the split-operand scheme of Markidis et
 // al. 2018 and Ootomo & Yokota 2022): each fp32 value v is split into a TF32
-// head h = tf32(v) and a TF32 tail l = tf32(v - h), so |v - h - l| <= 2^-22
-// |v|; the products of two TF32 values are exact in the fp32 accumulator, and
-// a_h*w_h + a_l*w_h + a_h*w_l misses a*w by at most about 2^-21 |a w| (the
-// dropped a_l*w_l and the two tails' rounding).  bf16 inputs are TF32 values
-// already (a_l = 0).  The result is held to the fp32 CUDA-core bar, not the
-// TF32 one.
+// head and tail, v = h + l; the products of two TF32 values are exact in the
+// fp32 accumulator, and a_h*w_h + a_l*w_h + a_h*w_l misses a*w only by the
+// dropped a_l*w_l and what the tails lose.  Weights: h = tf32(w) (nearest),
+// l = tf32(w - h), so |w - h - l| <= 2^-22 |w|.  Activations (per pixel, so
+// kept cheap): the MMA reads an fp32 operand as TF32 by ignoring its low 13
+// bits, so h is v itself (read as v truncated to TF32) and l = v - trunc(v)
+// (exact; one mask, one subtraction), which the MMA truncates in turn:
+// |v - h - l| < 2^-20 |v|.  Each product is then within about 2^-20 |a w|.
+// bf16 inputs are TF32 values already (a_l = 0).  The result is held to the
+// fp32 CUDA-core bar, not the TF32 one.
 //
 // Layout of the work:
 //  * one persistent CTA per SM (a kernel that allocates TMEM is placed one
-//    CTA per SM), made of independent 128-thread warpgroups (4 for fp32, 8
+//    CTA per SM), made of independent 128-thread warpgroups (6 for fp32, 8
 //    for bf16), each with its own staging ring, TMEM columns and mbarrier,
 //    synchronised by its own named barrier: while one warpgroup waits for
 //    its MMAs or its copies, the others build or store;
 //  * a warpgroup walks tiles of 2 output rows x 64 columns; a tile's input
 //    (5 rows x 132 pixels, from input column 2*ow0 - 4; bf16: 136 pixels
-//    from 2*ow0 - 8, so that copies start on 16-byte boundaries) is copied
-//    raw (16-byte cp.async, zero outside the image = the padding) into a
-//    ring of kStages buffers, kStages - 1 tiles ahead of the one computed;
+//    from 2*ow0 - 8, so that copies start on 16-byte boundaries) is staged
+//    raw into a ring of kStages buffers, kStages - 1 tiles ahead of the one
+//    computed: one bulk copy (cp.async.bulk) per input row for the part
+//    inside the image, completing on the slot's mbarrier, and zeros (the
+//    padding) stored by the warpgroup's first warp outside it;
 //  * thread t of a warpgroup gathers the A row of its output pixel (three
 //    runs of 9 consecutive staged values, one per filter row: 3 columns x 3
 //    channels), splits it into head and tail in registers and stores both
 //    into TMEM (tcgen05.st, lane t, 32 columns each): the MMAs read A from
 //    TMEM, so A costs no shared-memory bandwidth;
-//  * B is [w_h ; w_l] (32 rows, 128-byte swizzled K-major rows in shared
-//    memory, built once per CTA); the warpgroup's thread 0 issues, per
-//    tile, four MMAs A_h x [w_h ; w_l] (M = 128, N = 32, K = 8) and four
-//    A_l x w_h (N = 16) into one accumulator D (32 columns), committed to the
-//    warpgroup's mbarrier (bounded wait);
-//  * each warp reads its 32 TMEM lanes of D (thread t: pixel t), adds the
-//    halves (D[c] + D[16 + c] = a_h w_h + a_l w_h + a_h w_l), applies scale /
-//    bias / residual / activation and writes the pixel's 64 bytes (bf16: 32).
+//  * B is w_h (rows 0-15) and w_l (rows 16-31), 128-byte swizzled K-major
+//    rows in shared memory, built once per CTA; the warpgroup's thread 0
+//    issues, per tile, A_l x w_h, A_h x w_l and A_h x w_h (four MMAs each,
+//    M = 128, N = 16, K = 8; the small terms first) into one 16-column
+//    accumulator D, committed to the warpgroup's mbarrier (bounded wait);
+//  * each warp reads its 32 TMEM lanes of D (thread t: pixel t), applies
+//    scale / bias / residual / activation and writes the pixel's 64 bytes
+//    (bf16: 32).
 #include "epilogue.cuh"
 #include "internal.h"
 #include "launch_util.h"
@@ -61,8 +67,8 @@ constexpr int kWGThreads = kM;       // a warpgroup; its thread t: A row t, TMEM
 constexpr int kRows = 2 * kTH + 1;   // staged input rows
 constexpr int kStages = 4;           // staged tiles per warpgroup
 constexpr int kBRow = 128;           // bytes per B row (32 TF32 K entries)
-constexpr int kBBytes = 32 * kBRow;  // B = [w_h ; w_l]
-constexpr int kTmemCols = 512;       // the whole of TMEM: kWG x kWGCols
+constexpr int kBBytes = 32 * kBRow;  // B = w_h (rows 0-15), w_l (rows 16-31)
+constexpr int kTmemCols = 512;       // allocated whole (one CTA per SM); kWG x kWGCols of it used
 
 // Staging of one input row: groups of pixels that make 48 bytes (three
 // 16-byte copies), starting kFirst pixels left of input column 2 * ow0.
@@ -73,19 +79,20 @@ template <>
 struct Staging<float> {
   static constexpr int kFirst = 4, kGroupPx = 4, kGroups = 33;  // 132 pixels
   static constexpr bool kSplit = true;                           // head and tail A operands
-  static constexpr int kWG = 4;                                  // warpgroups per CTA
-  static constexpr int kWGCols = 128, kDCol = 64;
+  static constexpr int kWG = 6;                                  // warpgroups per CTA
+  static constexpr int kWGCols = 80, kDCol = 64;                 // A 0-63, D 64-79
 };
 template <>
 struct Staging<__nv_bfloat16> {
   static constexpr int kFirst = 8, kGroupPx = 8, kGroups = 17;  // 136 pixels
   static constexpr bool kSplit = false;                          // bf16 values are TF32 values
   static constexpr int kWG = 8;
-  static constexpr int kWGCols = 64, kDCol = 32;
+  static constexpr int kWGCols = 48, kDCol = 32;                 // A 0-31, D 32-47
 };
 
 // Shared memory: B, the warpgroups' staging rings, scale / bias, the
-// warpgroups' mbarriers, the TMEM slot and the abort flag.
+// warpgroups' mbarriers (MMA completion, staged slots), the TMEM slot and the
+// abort flag.
 template <typename T>
 struct Layout {
   static constexpr int kWG = Staging<T>::kWG;
@@ -94,10 +101,10 @@ struct Layout {
   static constexpr int kB = 0;
   static constexpr int kRaw = kB + kBBytes;
   static constexpr int kSB = kRaw + kWG * kStages * kRawBytes;
-  static constexpr int kBar = kSB + 32 * 4;
-  static constexpr int kEnd = kBar + 8 * kWG + 8;
+  static constexpr int kBar = kSB + 32 * 4;             // MMA barriers [kWG], staging barriers [kWG][kStages]
+  static constexpr int kEnd = kBar + 8 * kWG * (1 + kStages) + 8;
   static_assert(kRaw % 16 == 0 && kRawBytes % 16 == 0 && kBar % 8 == 0, "alignment");
-  static_assert(kWG * Staging<T>::kWGCols == kTmemCols, "TMEM split");
+  static_assert(kWG * Staging<T>::kWGCols <= kTmemCols, "TMEM split");
 };
 
 template <typename T>
@@ -105,8 +112,12 @@ constexpr size_t smem_bytes() {
   return 1024 + Layout<T>::kEnd;  // + alignment of the base to the 1024-byte swizzle atom
 }
 
-__device__ __forceinline__ void cp_async16_z(void* dst, const void* src, bool in) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(in ? 16 : 0)
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global to shared memory, completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
 
@@ -167,37 +178,74 @@ __device__ __forceinline__ void tmem_st_wait() {
 // operations only, off the conversion pipe.
 __device__ __forceinline__ uint32_t tf32_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
 
+// x minus x truncated to TF32 (the low 13 mantissa bits cleared): exact.
+__device__ __forceinline__ uint32_t tf32_tail_bits(float x) {
+  return __float_as_uint(x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u));
+}
+
 struct Tile {
   int n, oh0, ow0;
 };
 
-__device__ __forceinline__ Tile tile_of(int t, int tiles_x, int tiles_y) {
-  Tile p;
-  const int tx = t % tiles_x, rest = t / tiles_x;
-  p.n = rest / tiles_y;
-  p.oh0 = (rest - p.n * tiles_y) * kTH;
-  p.ow0 = tx * kTW;
-  return p;
-}
+// The tiles first, first + step, first + 2 step, ... (tile index
+// ((n * tiles_y) + ty) * tiles_x + tx) walked without divisions: the step's
+// own quotient and remainders are taken once, each advance adds them with
+// carries.
+struct TileWalk {
+  int tx, ty, n, dtx, dty, dn;
+  __device__ __forceinline__ void init(int first, int step, int tiles_x, int tiles_y) {
+    tx = first % tiles_x;
+    const int r = first / tiles_x;
+    ty = r % tiles_y;
+    n = r / tiles_y;
+    dtx = step % tiles_x;
+    const int dr = step / tiles_x;
+    dty = dr % tiles_y;
+    dn = dr / tiles_y;
+  }
+  __device__ __forceinline__ Tile tile() const { return Tile{n, ty * kTH, tx * kTW}; }
+  __device__ __forceinline__ void next(int tiles_x, int tiles_y) {
+    tx += dtx;
+    int c = tx >= tiles_x ? 1 : 0;
+    tx -= c * tiles_x;
+    ty += dty + c;
+    c = ty >= tiles_y ? 1 : 0;
+    ty -= c * tiles_y;
+    n += dn + c;
+  }
+};
 
-// Issues thread t's share of the copies of one tile's input rows into `raw`.
+// Stages one tile's input rows into `raw` (run by one whole warp): lane 0
+// arms `full` with the byte count and issues one bulk copy per input row
+// for the columns inside the image; the lanes store zeros everywhere else
+// (rows above or below the image, columns left or right of it).  Staged
+// pixel c holds input column c0 + c; the in-image span [lo, hi) starts and
+// ends on whole 48-byte pixel groups (W is a multiple of the group).
 template <typename T>
-__device__ __forceinline__ void stage_tile(const StemArgs& a, int tile, uint8_t* raw, int t) {
+__device__ __forceinline__ void stage_tile(const StemArgs& a, const Tile& p, uint8_t* raw, uint64_t* full, int lane) {
   using S = Staging<T>;
-  constexpr int kChunks = 3 * S::kGroups;  // 16-byte copies per row
-  constexpr int kElems = 16 / sizeof(T);   // elements per copy
-  const Tile p = tile_of(tile, a.tiles_x, a.tiles_y);
-  const T* x = static_cast<const T*>(a.src);
+  constexpr int kPx = S::kGroups * S::kGroupPx;  // staged pixels per row
+  constexpr int kPxBytes = 3 * sizeof(T);
+  constexpr int kUnits = Layout<T>::kRowBytes / 16;
   const int c0 = 2 * p.ow0 - S::kFirst;  // input column of staged pixel 0
   const int ih0 = 2 * p.oh0 - 1;
-  const T* base = x + p.n * a.xs_n + 3LL * c0;
-  for (int i = t; i < kRows * kChunks; i += kWGThreads) {
-    const int r = i / kChunks, k = i - r * kChunks;
-    const int ih = ih0 + r;
-    const int col = c0 + S::kGroupPx * (k / 3);  // first pixel of the group this copy is in (all in or all out)
-    const bool ok = ih >= 0 && ih < a.H && col >= 0 && col < a.W;
-    cp_async16_z(raw + r * Layout<T>::kRowBytes + 16 * k, ok ? base + ih * a.xs_h + kElems * k : x, ok);
+  const int lo = max(c0, 0), hi = min(c0 + kPx, a.W);
+  const uint32_t off = static_cast<uint32_t>((lo - c0) * kPxBytes), span = static_cast<uint32_t>((hi - lo) * kPxBytes);
+  const int r_lo = max(-ih0, 0), r_hi = min(a.H - ih0, kRows);  // staged rows inside the image
+  if (lane == 0) {
+    mbar_arrive_expect_tx(full, span * static_cast<uint32_t>(r_hi - r_lo));
+    const T* src = static_cast<const T*>(a.src) + p.n * a.xs_n + 3LL * lo;
+    for (int r = r_lo; r < r_hi; ++r) bulk_g2s(raw + r * Layout<T>::kRowBytes + off, src + (ih0 + r) * a.xs_h, span, full);
   }
+  if (r_lo > 0 || r_hi < kRows || off > 0 || off + span < static_cast<uint32_t>(Layout<T>::kRowBytes)) {
+    for (int i = lane; i < kRows * kUnits; i += 32) {
+      const int r = i / kUnits;
+      const uint32_t b = static_cast<uint32_t>(i - r * kUnits) * 16;
+      if (r < r_lo || r >= r_hi || b < off || b >= off + span)
+        *reinterpret_cast<uint4*>(raw + r * Layout<T>::kRowBytes + b) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  __syncwarp();
 }
 
 // The 10 staged values of one input row from which this thread's pixel
@@ -236,13 +284,14 @@ __global__ void __launch_bounds__(Staging<T>::kWG * kWGThreads, 1) stem_tc_kerne
   float* const sc = reinterpret_cast<float*>(smem + L::kSB);
   float* const bi = sc + 16;
   uint64_t* const bars = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [kWG]
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + kWG);
+  uint64_t* const full = bars + kWG + g * kStages;                      // this warpgroup's [kStages]
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + kWG * (1 + kStages));
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint64_t* const bar = bars + g;
   const int bar_id = 1 + g;  // named barrier of the warpgroup (0 is __syncthreads)
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kWG; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kWG * (1 + kStages); ++i) mbar_init(&bars[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -286,24 +335,36 @@ __global__ void __launch_bounds__(Staging<T>::kWG * kWGThreads, 1) stem_tc_kerne
   const int num_tiles = a.N * a.tiles_y * a.tiles_x;
   const int workers = static_cast<int>(gridDim.x) * kWG;
   const int first = g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
-  bool pending = false;  // thread 0: an MMA group whose completion nobody has seen
-  int it = 0;
-#pragma unroll
-  for (int s = 0; s < kStages - 1; ++s) {
-    const int tl = first + s * workers;
-    if (tl < num_tiles) stage_tile<T>(a, tl, ring + s * L::kRawBytes, t);
-    asm volatile("cp.async.commit_group;" ::: "memory");
+  bool pending = false;    // thread 0: an MMA group whose completion nobody has seen
+  int it = 0, staged = 0;  // tiles consumed / staged by this warpgroup (its tile q sits in slot q % kStages)
+  const bool stager = t < 32;  // the warpgroup's first warp stages
+  TileWalk cur, ahead;
+  cur.init(first, workers, a.tiles_x, a.tiles_y);
+  ahead = cur;
+  for (; staged < kStages - 1 && first + staged * workers < num_tiles; ++staged) {
+    if (stager) stage_tile<T>(a, ahead.tile(), ring + staged * L::kRawBytes, &full[staged], t);
+    ahead.next(a.tiles_x, a.tiles_y);
   }
-  for (int tile = first; tile < num_tiles; tile += workers, ++it) {
-    const Tile p = tile_of(tile, a.tiles_x, a.tiles_y);
+  // Two named barriers per tile: after A is in TMEM (then thread 0 issues the
+  // MMAs), and after thread 0 has seen the MMAs complete and the next tile's
+  // rows arrive (its waits; the others sleep in the barrier, which also
+  // carries thread 0's wait result).
+  bool in = true;
+  if (t == 0 && first < num_tiles) in = mbar_wait(&full[0], 0u, wd);
+  __syncwarp();  // warp 0 converged again before the aligned barrier
+  bool ok = group_sync_and(bar_id, in);
+  for (int tile = first; ok && tile < num_tiles; tile += workers, ++it) {
+    const Tile p = cur.tile();
+    cur.next(a.tiles_x, a.tiles_y);
     // the slot kStages - 1 tiles ahead was last read by the previous tile's
     // A gather, which every thread of the warpgroup finished before that
     // tile's MMA barrier
-    const int ahead = tile + (kStages - 1) * workers;
-    if (ahead < num_tiles) stage_tile<T>(a, ahead, ring + ((it + kStages - 1) % kStages) * L::kRawBytes, t);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");  // this tile's rows are in place
-    group_sync(bar_id);
+    if (first + staged * workers < num_tiles) {
+      const int q = staged % kStages;
+      if (stager) stage_tile<T>(a, ahead.tile(), ring + q * L::kRawBytes, &full[q], t);
+      ahead.next(a.tiles_x, a.tiles_y);
+      ++staged;
+    }
 
     // ------------------------------------------------ A row t into TMEM
     {
@@ -314,12 +375,12 @@ __global__ void __launch_bounds__(Staging<T>::kWG * kWGThreads, 1) stem_tc_kerne
       // K entry k = kh * 9 + j is v[kh][1 + j]; entries 27..31 are zero
       uint32_t h[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) h[k] = k < 27 ? tf32_bits(v[k / 9][1 + k % 9]) : 0u;
+      for (int k = 0; k < 32; ++k) h[k] = k < 27 ? __float_as_uint(v[k / 9][1 + k % 9]) : 0u;
       tmem_st_x32(tcol + tlane, h);
       if constexpr (S::kSplit) {
         uint32_t l[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) l[k] = k < 27 ? tf32_bits(v[k / 9][1 + k % 9] - __uint_as_float(h[k])) : 0u;
+        for (int k = 0; k < 32; ++k) l[k] = k < 27 ? tf32_tail_bits(v[k / 9][1 + k % 9]) : 0u;
         tmem_st_x32(tcol + tlane + 32, l);
       }
       tmem_st_wait();
@@ -327,28 +388,40 @@ __global__ void __launch_bounds__(Staging<T>::kWG * kWGThreads, 1) stem_tc_kerne
     tc_fence_before_sync();  // the TMEM stores (and the previous tile's TMEM loads) are done
     group_sync(bar_id);
 
-    // ---------------------------------------------------------- MMAs
+    // ------------------------------------------ MMAs, and the wait for them
+    bool got = true;
     if (t == 0) {
       tc_fence_after_sync();
       const uint32_t d = tcol + S::kDCol;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_tf32_tmem_a(d, tcol + 8 * kk, b_desc + 2 * kk, idesc_tf32(kM, 32), kk > 0 ? 1u : 0u);
+      constexpr uint32_t idesc = idesc_tf32(kM, 16);
+      const uint64_t b_tail = b_desc + ((16 * kBRow) >> 4);  // rows 16-31 (whole swizzle atoms)
+      uint32_t accumulate = 0;
       if constexpr (S::kSplit) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_tf32_tmem_a(d, tcol + 32 + 8 * kk, b_desc + 2 * kk, idesc_tf32(kM, 16), 1u);
+        for (int kk = 0; kk < 4; ++kk, accumulate = 1)
+          mma_tf32_tmem_a(d, tcol + 32 + 8 * kk, b_desc + 2 * kk, idesc, accumulate);
       }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk, accumulate = 1) mma_tf32_tmem_a(d, tcol + 8 * kk, b_tail + 2 * kk, idesc, accumulate);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) mma_tf32_tmem_a(d, tcol + 8 * kk, b_desc + 2 * kk, idesc, 1u);
       mma_commit(bar);
       pending = true;
+      got = mbar_wait(bar, static_cast<uint32_t>(it) & 1u, wd);
+      // the next tile's rows: the bulk copies (its slot's barrier) and the
+      // zeros (stored before an earlier barrier of the warpgroup)
+      if (got && tile + workers < num_tiles)
+        got = mbar_wait(&full[(it + 1) % kStages], static_cast<uint32_t>((it + 1) / kStages) & 1u, wd);
     }
-    const bool got = group_sync_and(bar_id, mbar_wait(bar, static_cast<uint32_t>(it) & 1u, wd));
-    if (!got) break;
+    __syncwarp();
+    ok = group_sync_and(bar_id, got);
+    if (!ok) break;
     pending = false;
     tc_fence_after_sync();
 
     // ---------------------------------------------------------- epilogue
-    uint32_t acc[32];
-    tmem_ld_x32(tcol + tlane + S::kDCol, acc);
+    uint32_t acc[16];
+    tmem_ld_x16(tcol + tlane + S::kDCol, acc);
     tmem_wait_regs(acc);
     const int oh = p.oh0 + ly, ow = p.ow0 + lx;
     if (oh < a.OH && ow < a.OW) {
@@ -360,7 +433,7 @@ __global__ void __launch_bounds__(Staging<T>::kWG * kWGThreads, 1) stem_tc_kerne
         const float4 s4 = reinterpret_cast<const float4*>(sc)[j], b4 = reinterpret_cast<const float4*>(bi)[j];
         float z[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) z[i] = __uint_as_float(acc[4 * j + i]) + __uint_as_float(acc[16 + 4 * j + i]);
+        for (int i = 0; i < 4; ++i) z[i] = __uint_as_float(acc[4 * j + i]);
         float4 o;
         if (!RES) {
           o = make_float4(epi_t<ACT, 0>(z[0], s4.x, b4.x, 0.0f), epi_t<ACT, 0>(z[1], s4.y, b4.y, 0.0f),
@@ -378,8 +451,11 @@ __global__ void __launch_bounds__(Staging<T>::kWG * kWGThreads, 1) stem_tc_kerne
       }
     }
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  // after a timeout: let an MMA group still in flight finish before TMEM is released
+  // after a timeout: let the copies and the MMA group still in flight finish
+  // before the shared memory and TMEM are released
+  if (t == 0)
+    for (int q = it; q < staged; ++q)
+      mbar_wait_drain(&full[q % kStages], static_cast<uint32_t>(q / kStages) & 1u, 20000000ull);
   if (pending) mbar_wait_drain(bar, static_cast<uint32_t>(it) & 1u, 20000000ull);
   tc_fence_before_sync();
   __syncthreads();
