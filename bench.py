@@ -171,7 +171,7 @@ def profiled_traffic(profile_name, src_files):
 PATH_KERNELS = {1: ("cb::direct_tile_kernel / direct_conv_kernel", "hbm"), 2: ("cb::dw_tma_kernel", "hbm"),
                 3: ("cb::igemm_tf32_kernel", "tensor"), 4: ("cb::igemm_halo_kernel (pixel-major)", "tensor"),
                 5: ("cb::igemm_halo_kernel (channel-major)", "tensor"), 6: ("cb::pw_small_kernel", "hbm"),
-                7: ("cb::stem_kernel", "hbm")}
+                7: ("cb::stem_tc_kernel / stem_kernel", "hbm")}
 
 
 def kernel_of(binding, x, y, k, stride, pad, x_layout=0):
@@ -447,8 +447,8 @@ class YoloWorkload(Workload):
     unit = "images/s"
     # ncu summaries (DRAM traffic of one launch at batch 32) of the launches that can be the longest
     profiles = {
-        "s0.down": ("stem_kernel_yolo_s0_down_b32.md",
-                    ["stem.cu", "resample.cuh", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
+        "s0.down": ("stem_tc_kernel_yolo_s0_down_b32.md",
+                    ["stem_tc.cu", "epilogue.cuh", "ptx.cuh", "tc_store.cuh", "launch_util.h", "internal.h"]),
         "s0.cv2": ("conv3x3_c8_kernel_yolo_s0_cv2_b32.md",
                    ["conv3x3_c8.cu", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
         "s0.cv3": ("pw_small_kernel_yolo_s0_cv3_b32.md",
@@ -1065,6 +1065,8 @@ def run_ours(args):
         for _ in range(args.warmup):
             wl.run(stream)
         torch.cuda.synchronize()
+        for L, info in zip(wl.launches, launch_occupancy(torch, wl, stream).values()):
+            L.kernel = info["kernel"] or L.kernel  # the kernel the library launched
         torch.cuda.nvtx.range_push("profiled_pass")
         wl.run(stream)
         torch.cuda.nvtx.range_pop()

@@ -86,6 +86,30 @@ def test_stem_silu(gpu, orc, stem_kernel, layout, shape):
     assert rel_err(y.cpu().numpy(), ref) <= TOL_FP32
 
 
+def _trunc_tf32(a):
+    """a with the low 13 mantissa bits cleared: how a TF32 multiply reads an fp32 value."""
+    return (np.asarray(a, np.float32).view(np.uint32) & np.uint32(0xFFFFE000)).view(np.float32)
+
+
+@pytest.mark.parametrize("seed", [21, 22])
+def test_stem_holds_fp32_bar_below_tf32_precision(gpu, orc, stem_kernel, seed):
+    """Inputs 1 + u 2^-12 (u ~ U[0,1)) carry their information below TF32 precision: TF32 reads
+    every one of them as 1.  A plain TF32 convolution then misses the fp32 bar by far (checked
+    here with the oracle on truncated operands); both stem kernels -- the tensor-core one through
+    its head / tail split of activations and weights -- meet it."""
+    rng = np.random.default_rng(seed)
+    N, H, W = 2, 34, 72
+    x = (1.0 + rng.random((N, H, W, 3)) * 2.0**-12).astype(np.float32)
+    w, bn = _stem(seed)
+    layer = ConvBnAct(w, bn, 2, 1, cb.ACT_NONE)
+    OH, OW = layer.out_hw(H, W)
+    ref = orc.conv_bn_act(x, w, bn, stride=2, pad=1, act=orc.ACT_NONE)
+    plain_tf32 = orc.conv_bn_act(_trunc_tf32(x), _trunc_tf32(w), bn, stride=2, pad=1, act=orc.ACT_NONE)
+    assert rel_err(plain_tf32, ref) > 20 * TOL_FP32
+    y = _run(to_dev(x), layer, OH, OW, cb.LAYOUT_NHWC, kernel=stem_kernel)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_FP32
+
+
 @pytest.mark.parametrize("act,res_mode", [(0, 0), (1, 0), (1, 1), (2, 2), (0, 2), (2, 1)])
 def test_stem_epilogues(gpu, orc, stem_kernel, act, res_mode):
     N, H, W = 2, 26, 136
