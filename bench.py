@@ -49,6 +49,10 @@ TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rates
 UNIT_SCALE = {"GB/s": 1e9, "TFLOP/s": 1e12, "images/s": 1.0}
 
 
+FP32_LANES_PER_SM = 128  # fp32 FMA lanes per SM (4 partitions x 32)
+MAX_SM_MHZ = 2070        # maximum SM clock of this part
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -247,6 +251,12 @@ class Workload:
                     "frac": round(achieved / peak, 4),
                     "frac_of_min_roof": round(achieved / min(peak, L.work.intensity * peaks["hbm_gbs"] / 1e3), 4),
                     "hbm_gbs": round(bw_roof, 1), "intensity": round(L.work.intensity, 2)}
+        if L.bound == "alu":  # fp32 FMAs on the CUDA cores: against the derived FMA peak
+            achieved = L.work.flops / (ms * 1e-3) / 1e12
+            return {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peaks["fp32_fma_tflops"], 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / peaks["fp32_fma_tflops"], 4),
+                    "hbm_gbs": round(L.work.bytes / (ms * 1e-3) / 1e9, 1),
+                    "hbm_frac": round(L.work.bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
         achieved = L.work.bytes / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4)}
@@ -258,10 +268,15 @@ class Workload:
         r["kernel"] = f"{L.kernel} ({L.name})"
         r["algorithmic_bytes" if r["bound"] == "hbm" else "algorithmic_flops"] = \
             L.work.bytes if r["bound"] == "hbm" else L.work.flops
+        if r["bound"] == "alu":
+            r["algorithmic_bytes"] = L.work.bytes
         prof = self.profiles.get(L.name, self.profile)
         r["traffic"] = profiled_traffic(*prof) if prof else None
         if r["bound"] == "hbm":
             r["peak_source"] = f"{peaks['source']} hbm_gbs (copy-kernel burst)"
+        elif r["bound"] == "alu":
+            r["peak_source"] = ("derived: SMs x 128 fp32 lanes x 2 FLOP per FMA x 2070 MHz maximum SM clock "
+                                f"({peaks['sms']} SMs)")
         elif self.tc_dtype == "bf16":
             r["peak_source"] = f"{peaks['source']} bf16_tflops (cuBLAS bf16 burst)"
         else:
@@ -487,15 +502,23 @@ class YoloWorkload(Workload):
                                                              res_mode=cb.RES_POST_ACT, stream=s))()),
             ]
             views = {"down": (x_in(), B["x1"]), "cv1": (B["x1"], a), "cv2": (a, b), "cv3": (B["cat"], B["out"])}
+            if self.chain.fused[i]:  # the stage body as one kernel (cb_stage_body): FMA-bound
+                x1 = B["x1"]
+                steps = steps[:1] + [("body", (lambda i=i: lambda s: self.chain.body(i, stream=s))())]
+                works[f"s{i}.body"] = workloads.stage_body(batch, x1.shape[1], x1.shape[2], x1.shape[3], eb)
             for nm, fn in steps:
-                xv, yv = views[nm]
-                kname, bound = kernel_of(cb, xv, yv, L[nm].k, L[nm].stride, L[nm].pad)
+                if nm == "body":
+                    kname, bound = "cb::stage_body_kernel", "alu"
+                else:
+                    xv, yv = views[nm]
+                    kname, bound = kernel_of(cb, xv, yv, L[nm].k, L[nm].stride, L[nm].pad)
                 self.launches.append(Launch(f"s{i}.{nm}", fn, works[f"s{i}.{nm}"], kname, bound))
             prev = (lambda B=B: lambda: B["out"])()
         storage = ("bf16 storage: every layer reads and writes bf16, tensor-core layers multiply bf16 "
                    "weights, fp32 accumulation" if self.bf16 else "fp32")
         self.config = {"workload": "YOLO-style 20-conv chain (5 stages, concat via channel views, post-act "
-                                   f"residual), 640x640x3, {storage}", "batch": batch,
+                                   f"residual; the 16-channel stage body as one kernel), 640x640x3, {storage}",
+                       "batch": batch,
                        "l2": f"inputs_larger_than_l2 ({157 * eb // 4} MB input, {1.2 * eb / 4:.1f} GB of "
                              "activations per step)",
                        "autotune": AUTOTUNE}
@@ -1054,6 +1077,8 @@ def run_ours(args):
     _build.build_library()
     binding.load()
     peaks = load_peaks()
+    peaks["sms"] = torch.cuda.get_device_properties(device).multi_processor_count
+    peaks["fp32_fma_tflops"] = peaks["sms"] * FP32_LANES_PER_SM * 2 * MAX_SM_MHZ * 1e6 / 1e12
 
     global AUTOTUNE
     AUTOTUNE = not args.no_autotune

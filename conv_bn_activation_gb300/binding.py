@@ -31,7 +31,7 @@ EXPORTED = (
     "cb_round_weights_tf32", "cb_get_kernel_policy", "cb_layer_uses_tensor_cores",
     "cb_dw_separable_block_static", "cb_conv_path", "cb_debug_timeout_probe", "cb_autotune_conv",
     "cb_autotune_clear", "cb_autotune_entries", "cb_preprocess_stem_u8", "cb_dw_separable_block_fused",
-    "cb_set_tuning", "cb_last_launch", "cb_debug_sample_coords", "cb_convert_weights_bf16",
+    "cb_set_tuning", "cb_last_launch", "cb_debug_sample_coords", "cb_convert_weights_bf16", "cb_stage_body",
 )
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # CB_STATIC_SCRATCH_BYTES
 
@@ -79,6 +79,7 @@ def load():
                 "cb_dw_separable_block_workspace": [T, I, I, ctypes.POINTER(S)],
                 "cb_dw_separable_block": [T, P, P, P, P, P, P, P, P, P, I, T, P, S, P],
                 "cb_dw_separable_block_static": [T, P, P, P, P, P, P, P, P, P, I, T, P],
+                "cb_stage_body": [T, P, P, P, P, P, P, P, P, P, I, T, P],
                 "cb_avgpool_linear": [T, P, P, I, P, P],
                 "cb_preprocess_u8": [P, I, I, I, LL, P, I, I, P],
                 "cb_preprocess_u8_three_pass": [P, I, I, I, LL, P, P, P, I, I, P],
@@ -306,6 +307,22 @@ def dw_separable_block(x, p, stride, y, workspace, stream=None):
         stride, ctypes.byref(yv), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _stream_ptr(stream))
     _check(st, "cb_dw_separable_block")
+    return y
+
+
+def stage_body(x1, layers, act, y, stream=None):
+    """cb_stage_body: the YOLO-style stage body (1x1 16->8, 3x3 8->8, 1x1 on the concat + x1) in one
+    kernel.  layers: three objects with HOST float32 arrays .w_host (OHWI), .scale_host, .bias_host
+    (ConvBnAct layers keep them): the call reads them and puts them in the launch."""
+    xv, yv = nhwc(x1), nhwc(y)
+    arrs = []
+    for L in layers:
+        for a in (L.w_host, L.scale_host, L.bias_host):
+            a = np.ascontiguousarray(a, dtype=np.float32)
+            arrs.append(a)
+    st = load().cb_stage_body(ctypes.byref(xv), *[a.ctypes.data for a in arrs], act, ctypes.byref(yv),
+                              _stream_ptr(stream))
+    _check(st, "cb_stage_body")
     return y
 
 

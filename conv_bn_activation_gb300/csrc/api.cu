@@ -1635,6 +1635,78 @@ cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const flo
   return cb_conv_bn_act(&t, pw_w, pw_scale, pw_bias, 1, 1, 1, 0, 1, CB_ACT_RELU, r, CB_RES_PRE_ACT, y, stream);
 }
 
+// ------------------------------------------------ YOLO-style stage body
+cb_status cb_stage_body(const cb_tensor* x1, const float* w1, const float* s1, const float* b1, const float* w2,
+                        const float* s2, const float* b2, const float* w3, const float* s3, const float* b3,
+                        cb_act act, cb_tensor* y, void* stream) {
+  if (!view_ok(x1) || !view_ok(y) || !w1 || !s1 || !b1 || !w2 || !s2 || !b2 || !w3 || !s3 || !b3)
+    return CB_ERR_INVALID_ARG;
+  if (act != CB_ACT_NONE && act != CB_ACT_RELU && act != CB_ACT_SILU) return CB_ERR_INVALID_ARG;
+  if (y->n != x1->n || y->h != x1->h || y->w != x1->w || y->c != x1->c || y->dtype != x1->dtype)
+    return CB_ERR_INVALID_ARG;
+  if (overlap(x1, y)) return CB_ERR_INVALID_ARG;
+  if (x1->c != 16 || x1->layout != CB_LAYOUT_NHWC || y->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
+  // x1 pixels in whole 16-byte pieces (the copy's strides), y in pieces of 4 channels
+  const long long xm = is_f32(x1) ? 4 : 8;
+  if (!aligned16(x1->data) || !aligned16(y->data) || x1->stride_w % xm != 0 || x1->stride_h % xm != 0 ||
+      x1->stride_n % xm != 0 || !strides_mult4(y))
+    return CB_ERR_ALIGNMENT;
+  if (x1->n == 0) return CB_OK;
+  if (x1->n > 65535 || x1->h > 65535 || x1->w > 65535 || !encode_tiled()) return CB_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
+  StageBodyArgs a{};
+  a.x = x1->data;
+  a.xs_n = x1->stride_n;
+  a.xs_h = x1->stride_h;
+  a.xs_w = x1->stride_w;
+  a.y = y->data;
+  a.ys_n = y->stride_n;
+  a.ys_h = y->stride_h;
+  a.ys_w = y->stride_w;
+  a.N = x1->n;
+  a.H = x1->h;
+  a.W = x1->w;
+  // weights (host OHWI) into the launch's parameter block, [ci pair][co][ci % 2] (per tap for w2)
+  for (int cp = 0; cp < 8; ++cp)
+    for (int co = 0; co < 8; ++co)
+      for (int e = 0; e < 2; ++e) a.w1[(cp * 8 + co) * 2 + e] = w1[co * 16 + 2 * cp + e];
+  for (int tap = 0; tap < 9; ++tap)
+    for (int cp = 0; cp < 4; ++cp)
+      for (int co = 0; co < 8; ++co)
+        for (int e = 0; e < 2; ++e) a.w2[((tap * 4 + cp) * 8 + co) * 2 + e] = w2[(co * 9 + tap) * 8 + 2 * cp + e];
+  for (int cp = 0; cp < 8; ++cp)
+    for (int co = 0; co < 16; ++co)
+      for (int e = 0; e < 2; ++e) a.w3[(cp * 16 + co) * 2 + e] = w3[co * 16 + 2 * cp + e];
+  for (int c = 0; c < 8; ++c) {
+    a.sb[c] = s1[c], a.sb[8 + c] = b1[c];
+    a.sb[16 + c] = s2[c], a.sb[24 + c] = b2[c];
+  }
+  for (int c = 0; c < 16; ++c) a.sb[32 + c] = s3[c], a.sb[48 + c] = b3[c];
+  a.act = static_cast<int>(act);
+  a.bf16 = is_f32(x1) ? 0 : 1;
+  a.err = dev->err;
+  a.timeout_ns = timeout_ns();
+  // x1 as (C = 16, W, H, N); one box is a tile's 18 x 34 haloed pixels
+  const cuuint64_t eb = elem_bytes(x1);
+  int bc = 0, bw = 0, bh = 0;
+  stage_body_box(&bc, &bw, &bh);
+  cuuint64_t dims[4] = {16, static_cast<cuuint64_t>(x1->w), static_cast<cuuint64_t>(x1->h),
+                        static_cast<cuuint64_t>(x1->n)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(x1->stride_w) * eb, static_cast<cuuint64_t>(x1->stride_h) * eb,
+                           static_cast<cuuint64_t>(x1->stride_n) * eb};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(bc), static_cast<cuuint32_t>(bw), static_cast<cuuint32_t>(bh), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMap xmap;
+  if (tiled_map(&xmap, 4, x1->data, dims, strides, box, estr,
+                is_f32(x1) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                is_f32(x1) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) != CUDA_SUCCESS)
+    return CB_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_stage_body(xmap, a, dev->sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
 // ------------------------------------------------ no-allocation block variant
 // The scratch of cb_dw_separable_block_static.  Host code cannot use this
 // name as a device address; it looks the address up per device below.

@@ -224,6 +224,34 @@ void stem_tile_grid(int OH, int OW, int* tiles_y, int* tiles_x);
 void stem_src_bounds(int hs, int ws, int hd, int wd, int* rows, int* row_cap);
 size_t stem_smem_bytes(int src_kind, int src_rows, int row_cap);
 cudaError_t launch_stem(const StemArgs& a, int src_kind, size_t smem, int sms, cudaStream_t s);
+// ------------------------------------------- YOLO-style stage body, C = 16
+// out = act(s3 * conv1x1([a | b]) + b3) + x1 with a = act(s1 * conv1x1(x1) + b1)
+// (16 -> 8) and b = act(s2 * conv3x3(a) + b2) (8 -> 8, pad 1), in one kernel
+// (stage_body.cu).  x1 and out are NHWC with 16 channels, fp32 or bf16
+// storage.  The weights and the folded BN travel in the launch's parameter
+// block (4 KB), each weight pair where the kernel's unrolled loops read it
+// by a constant offset: [input channel pair][output channel][2] (per tap
+// for w2).  The caller encodes xmap: x1 as a 4-D tensor (C = 16, W, H, N)
+// with the box stage_body_box gives and the 64-byte (fp32) or 32-byte
+// (bf16) swizzle.
+struct StageBodyArgs {
+  const void* x;
+  long long xs_n, xs_h, xs_w;
+  void* y;
+  long long ys_n, ys_h, ys_w;
+  int N, H, W;
+  int act;
+  int bf16;
+  int* err;  // device error word, bound of the kernel's waits
+  uint64_t timeout_ns;
+  float w1[8 * 8 * 2];      // 1x1 16 -> 8
+  float w2[9 * 4 * 8 * 2];  // 3x3 8 -> 8
+  float w3[8 * 16 * 2];     // 1x1 16 -> 16
+  float sb[2 * (8 + 8 + 16)];  // s1[8] b1[8] s2[8] b2[8] s3[16] b3[16]
+};
+void stage_body_box(int* box_c, int* box_w, int* box_h);
+cudaError_t launch_stage_body(const CUtensorMap& xmap, const StageBodyArgs& a, int sms, cudaStream_t s);
+
 // The same layer on the tensor cores (stem_tc.cu) at fp32 accuracy, for packed
 // NHWC input (src kinds 1 and 3: fp32, or bf16 storage with a bf16 output);
 // tiles_x / tiles_y are its own (2 x 64 output pixels).  stem_tc_ok: the tile

@@ -49,6 +49,9 @@ class ConvBnAct:
         w = cb.repack_weights(w_oihw, groups)
         self.tc_weights = bool(tc_weights)
         self.dtype = dtype
+        # host copies of the fp32 parameters as given, before any TF32 rounding or bf16 conversion
+        # (calls that take their parameters from the host: cb_stage_body)
+        self.w_host, self.scale_host, self.bias_host = w, scale, bias
         if tc_weights and dtype == torch.bfloat16:
             self.w = cb.convert_weights_bf16(w).to(device).contiguous()
         else:
@@ -132,13 +135,16 @@ class MnistNet:
 
 class YoloChain:
     """dtype: the activations' storage type (torch.float32, or torch.bfloat16: every layer then
-    reads and writes bf16, the tensor-core layers multiply bf16 weights)."""
+    reads and writes bf16, the tensor-core layers multiply bf16 weights).  fuse_body: a stage with
+    16 channels runs its body (cv1, cv2, cv3 with the concat and the residual) as one kernel
+    (cb_stage_body), so that a and b never reach memory; self.fused[i] says which stages do."""
 
-    def __init__(self, stages, batch, size=640, device="cuda", dtype=torch.float32):
+    def __init__(self, stages, batch, size=640, device="cuda", dtype=torch.float32, fuse_body=True):
         self.batch = batch
         self.dtype = dtype
         self.layers = []
         self.bufs = []
+        self.fused = []
         H = size
         for st in stages:
             c = st["down_w"].shape[0]
@@ -156,25 +162,35 @@ class YoloChain:
                  "out": torch.empty(batch, OH, OH, c, device=device, dtype=dtype), "half": h}
             self.layers.append(L)
             self.bufs.append(B)
+            self.fused.append(fuse_body and c == 16)
             H = OH
+
+    def body(self, i, stream=None, tune=False):
+        """Stage i after its stride-2 conv: x1 -> out (one kernel for a fused stage)."""
+        L, B = self.layers[i], self.bufs[i]
+        if self.fused[i]:
+            cb.stage_body(B["x1"], (L["cv1"], L["cv2"], L["cv3"]), L["cv1"].act, B["out"], stream=stream)
+            return
+        half = B["half"]
+        a, b = B["cat"][..., :half], B["cat"][..., half:]
+        run = {k: (v.autotune if tune else v) for k, v in L.items()}
+        run["cv1"](B["x1"], a, stream=stream)
+        run["cv2"](a, b, stream=stream)
+        run["cv3"](B["cat"], B["out"], residual=B["x1"], res_mode=cb.RES_POST_ACT, stream=stream)
 
     def forward(self, x, stream=None, tune=False):
         """The chain on x; tune=True measures each layer's tile plans on the way (cb_autotune_conv),
         synchronising after every layer, so that later forwards run the fastest."""
         h = x
-        for L, B in zip(self.layers, self.bufs):
-            half = B["half"]
-            a = B["cat"][..., :half]
-            b = B["cat"][..., half:]
-            run = {k: (v.autotune if tune else v) for k, v in L.items()}
-            run["down"](h, B["x1"], stream=stream)
-            run["cv1"](B["x1"], a, stream=stream)
-            run["cv2"](a, b, stream=stream)
-            run["cv3"](B["cat"], B["out"], residual=B["x1"], res_mode=cb.RES_POST_ACT, stream=stream)
+        for i, (L, B) in enumerate(zip(self.layers, self.bufs)):
+            (L["down"].autotune if tune else L["down"])(h, B["x1"], stream=stream)
+            self.body(i, stream=stream, tune=tune)
             h = B["out"]
         return h
 
-    launches_per_forward = 20
+    @property
+    def launches_per_forward(self):
+        return sum(2 if f else 4 for f in self.fused)
 
 
 class PreprocessStem:

@@ -132,6 +132,17 @@ def yolo_layers(N=1, size=640, act_bytes=F32, tc_w_bytes=None):
     return layers
 
 
+def stage_body(N, H, W, C=16, act_bytes=F32) -> Work:
+    """The YOLO-style stage body in one kernel (x1 -> out: 1x1 C -> C/2, 3x3 C/2 -> C/2, 1x1 on the
+    concat + x1): x1 read once, out written once, the three layers' weights and scale/bias; FLOPs of
+    the three convolutions (the 1x1 over the 3x3's halo, recomputed per tile, is not counted)."""
+    h = C // 2
+    px = N * H * W
+    w = (h * C + h * h * 9 + C * C) * F32
+    sb = 2 * (h + h + C) * F32
+    return Work(2 * px * C * act_bytes + w + sb, 2 * px * (h * C + h * h * 9 + C * C))
+
+
 def total(layers) -> Work:
     t = Work(0, 0)
     for _, w in layers:

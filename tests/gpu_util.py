@@ -65,3 +65,14 @@ def canary_buffer_bf16(shape, device="cuda"):
 
 def is_canary_bf16(t):
     return bool((t.contiguous().view(torch.int16) == 0x7FDD).all().item())
+
+
+def oracle_stage_body(orc, x1, st, act=2):
+    """The oracle's YOLO-style stage body from its stride-2 output x1 (NHWC): cv1 (1x1), cv2 (3x3,
+    pad 1) on cv1's output, cv3 (1x1) on the concat [a | b] with x1 added after the activation --
+    the three layers' definitions composed (the stage of oracle.yolo_stage after its down conv)."""
+    a = orc.conv_bn_act(x1, st["cv1_w"], st["cv1_bn"], stride=1, pad=0, act=act)
+    b = orc.conv_bn_act(a, st["cv2_w"], st["cv2_bn"], stride=1, pad=1, act=act)
+    cat = np.ascontiguousarray(np.concatenate([a, b], axis=-1))
+    return orc.conv_bn_act(cat, st["cv3_w"], st["cv3_bn"], stride=1, pad=0, act=act, residual=x1,
+                           res_mode=orc.RES_POST_ACT)

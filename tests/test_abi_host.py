@@ -171,6 +171,27 @@ def test_block_and_preprocess_validation(cblib):
     assert lib.cb_preprocess_u8(None, 1, 720, 1280, 3840, base, 480, 640, None) == cblib.ERR_INVALID_ARG
 
 
+def test_stage_body_validated_before_launch(cblib):
+    """cb_stage_body: NULL weights, shape, dtype and overlap errors, unsupported channel counts and
+    layouts, and misaligned strides are all decided on the host (fake pointers, never read)."""
+    lib = cblib.load()
+    T = ctypes.byref
+    base = 1 << 20
+    p = base + (1 << 24)
+    x = _view(base, 2, 16, 32, 16)
+    y = _view(base + (1 << 22), 2, 16, 32, 16)
+    call = lambda xv, yv, w=p, act=2: lib.cb_stage_body(T(xv), w, p, p, p, p, p, p, p, p, act, T(yv), None)
+    assert call(x, y, w=None) == cblib.ERR_INVALID_ARG                                   # NULL weights
+    assert call(x, y, act=5) == cblib.ERR_INVALID_ARG                                    # bad act
+    assert call(x, _view(base + (1 << 22), 2, 16, 31, 16)) == cblib.ERR_INVALID_ARG      # shape mismatch
+    assert call(x, _view(base + 64, 2, 16, 32, 16)) == cblib.ERR_INVALID_ARG             # y overlaps x1
+    assert call(_view(base, 2, 16, 32, 8), _view(base + (1 << 22), 2, 16, 32, 8)) == cblib.ERR_UNSUPPORTED
+    odd = _view(base, 2, 16, 32, 16)
+    odd.stride_w, odd.stride_h, odd.stride_n = 18, 18 * 32, 18 * 32 * 16                  # pixels 72 bytes apart
+    assert call(odd, y) == cblib.ERR_ALIGNMENT
+    assert call(_view(base, 0, 16, 32, 16), _view(base + (1 << 22), 0, 16, 32, 16)) == cblib.OK  # empty batch
+
+
 def test_round_weights_tf32(cblib):
     """Round to nearest TF32 (ties to even): low 13 mantissa bits clear, error <= half a TF32 ulp,
     idempotent, and the tie cases go to the even neighbour."""

@@ -10,7 +10,7 @@ import torch
 
 from conv_bn_activation_gb300 import binding as cb, synthetic
 from conv_bn_activation_gb300.nets import MnistNet, PreprocessStem, YoloChain
-from gpu_util import TOL_FP32, TOL_TF32, rel_err, sync_check, to_dev
+from gpu_util import TOL_FP32, TOL_TF32, oracle_stage_body, rel_err, sync_check, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -45,10 +45,15 @@ def test_mnist_graph_replay_matches_eager(gpu):
     assert torch.equal(net.logits, eager)
 
 
-def test_yolo_chain_small(gpu, orc):
+@pytest.mark.parametrize("fuse_body", [True, False], ids=["fused_body", "layers"])
+def test_yolo_chain_small(gpu, orc, fuse_body):
+    """The chain end to end at 96 x 96, with the 16-channel stage body as one kernel or as its
+    three layers."""
     stages = synthetic.yolo_params()
     x = synthetic.yolo_input(2, size=96)
-    chain = YoloChain(stages, 2, size=96)
+    chain = YoloChain(stages, 2, size=96, fuse_body=fuse_body)
+    assert chain.fused[0] == fuse_body and not any(chain.fused[1:])
+    assert chain.launches_per_forward == (18 if fuse_body else 20)
     out = chain.forward(to_dev(x))
     sync_check()
     h = x
@@ -66,17 +71,20 @@ def test_yolo_chain_full_size_per_layer(gpu, orc):
     sync_check()
     rng = np.random.default_rng(0)
     h = x
-    for st, B in zip(stages, chain.bufs):
+    for i, (st, B) in enumerate(zip(stages, chain.bufs)):
         half = B["half"]
         x1 = B["x1"].cpu().numpy()
         cat = B["cat"].cpu().numpy()
         out = B["out"].cpu().numpy()
-        checks = [
-            (h, st["down_w"], st["down_bn"], 2, 1, x1, None),
-            (x1, st["cv1_w"], st["cv1_bn"], 1, 0, cat[..., :half], None),
-            (np.ascontiguousarray(cat[..., :half]), st["cv2_w"], st["cv2_bn"], 1, 1, cat[..., half:], None),
-            (cat, st["cv3_w"], st["cv3_bn"], 1, 0, out, x1),
-        ]
+        checks = [(h, st["down_w"], st["down_bn"], 2, 1, x1, None)]
+        if chain.fused[i]:  # the body as one unit (a and b never reach memory)
+            assert rel_err(out, oracle_stage_body(orc, x1, st)) <= TOL_FP32
+        else:
+            checks += [
+                (x1, st["cv1_w"], st["cv1_bn"], 1, 0, cat[..., :half], None),
+                (np.ascontiguousarray(cat[..., :half]), st["cv2_w"], st["cv2_bn"], 1, 1, cat[..., half:], None),
+                (cat, st["cv3_w"], st["cv3_bn"], 1, 0, out, x1),
+            ]
         for inp, w, bn, s, p, got, res in checks:
             got = np.ascontiguousarray(got)
             idx = rng.choice(got.size, min(got.size, 3000), replace=False)

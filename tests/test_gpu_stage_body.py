@@ -1,0 +1,156 @@
+"""GPU parity of cb_stage_body: the body of a YOLO-style stage with 16 channels (1x1 16->8, 3x3
+8->8 on its output, 1x1 on the concat [a | b] with x1 added after the activation) in one kernel.
+
+The kernel computes in fp32 on the CUDA cores and keeps a and b in shared memory: the bar is the
+fp32 one (1e-5 of max|oracle|) against the oracle's three layers composed.  Shapes cover one and
+several 16 x 32 output tiles, ragged tile edges in both directions and images smaller than a tile
+(the 3x3's zero padding sits inside the tile there); the three activations; a channel-slice input
+and an output slice with canaries around it; bf16 storage (within half a bf16 ulp of the oracle on
+the same bf16 values, and bit-equal to the fp32 kernel's output rounded); the three-layer path;
+and the argument checks.
+"""
+import numpy as np
+import pytest
+import torch
+
+from conv_bn_activation_gb300 import binding as cb, synthetic
+from conv_bn_activation_gb300.nets import ConvBnAct
+from gpu_util import TOL_FP32, bf16_within_half_ulp, canary_buffer, canary_buffer_bf16, is_canary, \
+    is_canary_bf16, oracle_stage_body, rel_err, sync_check, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(2, 20, 40), (1, 16, 32), (3, 17, 33), (1, 1, 1), (1, 2, 3), (2, 40, 70), (1, 33, 95), (1, 48, 8)]
+
+
+def _stage(seed):
+    """Stage 0 of the YOLO-style chain's parameters (16 channels), reseeded."""
+    g = np.random.default_rng(seed)
+    st = {}
+    for key, (co, ci, k) in {"cv1": (8, 16, 1), "cv2": (8, 8, 3), "cv3": (16, 16, 1)}.items():
+        st[key + "_w"] = synthetic.kaiming(g, co, ci, k, k)
+        st[key + "_bn"] = synthetic.bn_params(g, co)
+    return st
+
+
+def _layers(st, act, dtype=torch.float32):
+    return (ConvBnAct(st["cv1_w"], st["cv1_bn"], 1, 0, act, dtype=dtype),
+            ConvBnAct(st["cv2_w"], st["cv2_bn"], 1, 1, act, dtype=dtype),
+            ConvBnAct(st["cv3_w"], st["cv3_bn"], 1, 0, act, dtype=dtype))
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_stage_body_silu(gpu, orc, shape):
+    N, H, W = shape
+    st = _stage(N + H + W)
+    x1 = np.random.default_rng(H * W).standard_normal((N, H, W, 16)).astype(np.float32)
+    y = torch.empty(N, H, W, 16, device=gpu)
+    cb.stage_body(to_dev(x1), _layers(st, cb.ACT_SILU), cb.ACT_SILU, y)
+    assert "stage_body_kernel" in cb.last_launch()["kernel"]
+    sync_check()
+    assert rel_err(y.cpu().numpy(), oracle_stage_body(orc, x1, st)) <= TOL_FP32
+
+
+@pytest.mark.parametrize("act", [cb.ACT_NONE, cb.ACT_RELU])
+def test_stage_body_activations(gpu, orc, act):
+    N, H, W = 2, 18, 36
+    st = _stage(act + 40)
+    x1 = np.random.default_rng(act).standard_normal((N, H, W, 16)).astype(np.float32)
+    y = torch.empty(N, H, W, 16, device=gpu)
+    cb.stage_body(to_dev(x1), _layers(st, act), act, y)
+    sync_check()
+    assert rel_err(y.cpu().numpy(), oracle_stage_body(orc, x1, st, act=act)) <= TOL_FP32
+
+
+def test_stage_body_matches_the_three_layers(gpu, orc):
+    """The fused body against the same body run as three cb_conv_bn_act calls (the pointwise and
+    8-channel 3x3 kernels, a and b through memory): both fp32, both within the fp32 bar."""
+    N, H, W = 4, 50, 64
+    st = _stage(7)
+    x1 = np.random.default_rng(7).standard_normal((N, H, W, 16)).astype(np.float32)
+    l1, l2, l3 = _layers(st, cb.ACT_SILU)
+    xd = to_dev(x1)
+    y = torch.empty(N, H, W, 16, device=gpu)
+    cb.stage_body(xd, (l1, l2, l3), cb.ACT_SILU, y)
+    cat = torch.empty(N, H, W, 16, device=gpu)
+    y3 = torch.empty_like(y)
+    l1(xd, cat[..., :8])
+    l2(cat[..., :8], cat[..., 8:])
+    l3(cat, y3, residual=xd, res_mode=cb.RES_POST_ACT)
+    sync_check()
+    ref = oracle_stage_body(orc, x1, st)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_FP32
+    assert rel_err(y.cpu().numpy(), y3.cpu().numpy()) <= 2 * TOL_FP32
+
+
+def test_stage_body_views(gpu, orc):
+    """x1 as channels [8, 24) of a 32-channel buffer; the output into channels [16, 32) of a
+    40-channel buffer with padded rows: nothing around it is written."""
+    N, H, W = 2, 19, 45
+    st = _stage(3)
+    wide = np.random.default_rng(3).standard_normal((N, H, W, 32)).astype(np.float32)
+    x1 = np.ascontiguousarray(wide[..., 8:24])
+    xd = to_dev(wide)[..., 8:24]
+    buf = canary_buffer((N, H, W + 5, 40))
+    y = buf[:, :, :W, 16:32]
+    cb.stage_body(xd, _layers(st, cb.ACT_SILU), cb.ACT_SILU, y)
+    sync_check()
+    assert rel_err(y.cpu().numpy(), oracle_stage_body(orc, x1, st)) <= TOL_FP32
+    assert is_canary(buf[..., :16]) and is_canary(buf[..., 32:]) and is_canary(buf[:, :, W:])
+
+
+@pytest.mark.parametrize("shape", [(2, 20, 40), (3, 17, 33), (1, 2, 3), (2, 40, 70)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_stage_body_bf16(gpu, orc, shape):
+    """bf16 storage: x1 read and the output written as bfloat16, the weights and every product and
+    sum in fp32 (a and b stay fp32 in shared memory)."""
+    N, H, W = shape
+    st = _stage(N * H + W)
+    x1 = np.random.default_rng(W).standard_normal((N, H, W, 16)).astype(np.float32)
+    xd, xv = to_dev_bf16(x1)
+    buf = canary_buffer_bf16((N, H, W, 32))
+    y = buf[..., 8:24]  # 16-byte aligned channel slice
+    cb.stage_body(xd, _layers(st, cb.ACT_SILU, dtype=torch.bfloat16), cb.ACT_SILU, y)
+    sync_check()
+    ref = oracle_stage_body(orc, xv, st)
+    got = y.float().cpu().numpy()
+    assert bf16_within_half_ulp(got, ref) <= 1.0
+    assert is_canary_bf16(buf[..., :8]) and is_canary_bf16(buf[..., 24:])
+    y32 = torch.empty(N, H, W, 16, device=gpu)
+    cb.stage_body(torch.from_numpy(xv).to(gpu), _layers(st, cb.ACT_SILU), cb.ACT_SILU, y32)
+    sync_check()
+    assert torch.equal(y.contiguous().view(torch.int16), y32.to(torch.bfloat16).view(torch.int16))
+
+
+def test_stage_body_full_size_stage0(gpu, orc):
+    """The chain's stage 0 body at its size (320 x 320, batch 32, the 640 x 640 input's stride-2
+    output), every output against the oracle."""
+    stages = synthetic.yolo_params()
+    st = stages[0]
+    x1 = np.random.default_rng(5).standard_normal((32, 320, 320, 16)).astype(np.float32)
+    y = torch.empty(32, 320, 320, 16, device=gpu)
+    cb.stage_body(to_dev(x1), _layers(st, cb.ACT_SILU), cb.ACT_SILU, y)
+    sync_check()
+    assert rel_err(y.cpu().numpy(), oracle_stage_body(orc, x1, st)) <= TOL_FP32
+
+
+def test_stage_body_rejects(gpu):
+    st = _stage(1)
+    layers = _layers(st, cb.ACT_SILU)
+    x1 = torch.zeros(1, 8, 8, 16, device=gpu)
+    with pytest.raises(cb.CbError) as e:  # in place: the output overlaps x1
+        cb.stage_body(x1, layers, cb.ACT_SILU, x1)
+    assert e.value.status == cb.ERR_INVALID_ARG
+    with pytest.raises(cb.CbError) as e:  # shape mismatch
+        cb.stage_body(x1, layers, cb.ACT_SILU, torch.empty(1, 8, 7, 16, device=gpu))
+    assert e.value.status == cb.ERR_INVALID_ARG
+    with pytest.raises(cb.CbError) as e:  # dtype mismatch
+        cb.stage_body(x1, layers, cb.ACT_SILU, torch.empty(1, 8, 8, 16, device=gpu, dtype=torch.bfloat16))
+    assert e.value.status == cb.ERR_INVALID_ARG
+    with pytest.raises(cb.CbError) as e:  # 8 channels: no kernel
+        cb.stage_body(torch.zeros(1, 8, 8, 8, device=gpu), layers, cb.ACT_SILU, torch.empty(1, 8, 8, 8, device=gpu))
+    assert e.value.status == cb.ERR_UNSUPPORTED
+    with pytest.raises(cb.CbError) as e:  # pixels 18 floats apart: not whole 16-byte pieces
+        cb.stage_body(torch.zeros(1, 8, 8, 18, device=gpu)[..., :16], layers, cb.ACT_SILU,
+                      torch.empty(1, 8, 8, 16, device=gpu))
+    assert e.value.status == cb.ERR_ALIGNMENT

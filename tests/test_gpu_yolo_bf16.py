@@ -1,7 +1,8 @@
 """GPU parity of the YOLO-style chain with bf16 storage: every layer reads and writes bfloat16 --
-the stem and the 8-channel 3x3 layer on the CUDA cores (fp32 arithmetic), the narrow 1x1 layers on
-the streaming kernel (fp32 arithmetic), the other layers on the tensor cores with bf16 weights and
-fp32 accumulation.
+the stem (tensor cores, split operands) and the 16-channel stage body (one kernel, CUDA cores) in
+fp32 arithmetic -- or that body as the 8-channel 3x3 layer and the narrow 1x1 layers, fp32
+arithmetic too -- and the other layers on the tensor cores with bf16 weights and fp32
+accumulation.
 
 Per layer, the oracle is fed the GPU's own bf16 input and the weights the kernel uses (bf16 for
 the tensor-core layers, fp32 for the others), as everywhere the oracle is fed the GPU's input:
@@ -18,7 +19,7 @@ import torch
 
 from conv_bn_activation_gb300 import binding as cb, synthetic
 from conv_bn_activation_gb300.nets import YoloChain
-from gpu_util import TOL_BF16, bf16_within_half_ulp, rel_err, sync_check
+from gpu_util import TOL_BF16, bf16_within_half_ulp, oracle_stage_body, rel_err, sync_check
 
 pytestmark = pytest.mark.gpu
 
@@ -37,12 +38,20 @@ def _check_chain(orc, chain, stages, xv):
         cat = B["cat"].float().cpu().numpy()
         out = B["out"].float().cpu().numpy()
         a = np.ascontiguousarray(cat[..., :half])
-        checks = [
-            ("down", h, "down", 2, 1, x1, None),
-            ("cv1", x1, "cv1", 1, 0, a, None),
-            ("cv2", a, "cv2", 1, 1, np.ascontiguousarray(cat[..., half:]), None),
-            ("cv3", cat, "cv3", 1, 0, out, x1),
-        ]
+        checks = [("down", h, "down", 2, 1, x1, None)]
+        if chain.fused[i]:
+            # the stage body in one kernel: fp32 weights and fp32 intermediates, only x1 and the
+            # output in bf16 -- within half a bf16 ulp of the oracle's composition on x1
+            ref = oracle_stage_body(orc, x1, st)
+            ulp = bf16_within_half_ulp(out, ref)
+            assert ulp <= 1.0, f"s{i}.body: {ulp:.3g} half-ulps"
+            assert rel_err(out, ref) <= TOL_BF16, f"s{i}.body"
+        else:
+            checks += [
+                ("cv1", x1, "cv1", 1, 0, a, None),
+                ("cv2", a, "cv2", 1, 1, np.ascontiguousarray(cat[..., half:]), None),
+                ("cv3", cat, "cv3", 1, 0, out, x1),
+            ]
         for name, inp, key, s, p, got, res in checks:
             w, bn = st[key + "_w"], st[key + "_bn"]
             wk = cb.convert_weights_bf16(w).float().numpy() if L[key].tc_weights else w
@@ -57,11 +66,12 @@ def _check_chain(orc, chain, stages, xv):
         h = out
 
 
-@pytest.mark.parametrize("batch,size", [(2, 96), (32, 640)], ids=["2x96", "32x640"])
-def test_yolo_chain_bf16_every_layer(gpu, orc, batch, size):
+@pytest.mark.parametrize("batch,size,fuse_body", [(2, 96, True), (2, 96, False), (32, 640, True)],
+                         ids=["2x96", "2x96-layers", "32x640"])
+def test_yolo_chain_bf16_every_layer(gpu, orc, batch, size, fuse_body):
     stages = synthetic.yolo_params()
     xt, xv = _bf16_input(batch, size)
-    chain = YoloChain(stages, batch, size=size, dtype=torch.bfloat16)
+    chain = YoloChain(stages, batch, size=size, dtype=torch.bfloat16, fuse_body=fuse_body)
     xd = xt.to(gpu)
     kinds = []
     for L, B, x_in in zip(chain.layers, chain.bufs, [xd] + [b["out"] for b in chain.bufs[:-1]]):
