@@ -464,6 +464,8 @@ class YoloWorkload(Workload):
     profiles = {
         "s0.down": ("stem_tc_kernel_yolo_s0_down_b32.md",
                     ["stem_tc.cu", "epilogue.cuh", "ptx.cuh", "tc_store.cuh", "launch_util.h", "internal.h"]),
+        "s0.body": ("stage_body_kernel_yolo_s0_body_b32.md",
+                    ["stage_body.cu", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
         "s0.cv2": ("conv3x3_c8_kernel_yolo_s0_cv2_b32.md",
                    ["conv3x3_c8.cu", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
         "s0.cv3": ("pw_small_kernel_yolo_s0_cv3_b32.md",
