@@ -132,8 +132,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
     const int tx = tile % tiles_x, rest = tile / tiles_x, ty = rest % tiles_y, n = rest / tiles_y;
     const int ih0 = ty * kTH - 1, iw0 = tx * kTW - 1;
-    // this tile's x1 (and, the first time, the weights) in place; the
-    // previous tile's phase 3 is done with a and b
+    // this tile's x1 in place; every thread's phase 3 of the previous tile
+    // is done with a
     if (!__syncthreads_and(mbar_wait(xfull, static_cast<uint32_t>(it) & 1u, wd))) break;
     if (threadIdx.x == 0) pending = false;
 

@@ -44,7 +44,10 @@
 //    rows in shared memory, built once per CTA; the warpgroup's thread 0
 //    issues, per tile, A_l x w_h, A_h x w_l and A_h x w_h (four MMAs each,
 //    M = 128, N = 16, K = 8; the small terms first) into one 16-column
-//    accumulator D, committed to the warpgroup's mbarrier (bounded wait);
+//    accumulator D, committed to the warpgroup's mbarrier; thread 0 alone
+//    waits for that commit and for the next tile's rows (bounded waits),
+//    while the others sleep in the warpgroup's named barrier: two barriers
+//    per tile, tile coordinates walked by additions;
 //  * each warp reads its 32 TMEM lanes of D (thread t: pixel t), applies
 //    scale / bias / residual / activation and writes the pixel's 64 bytes
 //    (bf16: 32).
