@@ -11,25 +11,28 @@
 // work is then about 985 multiply-adds per output pixel, so the FMA pipe,
 // not HBM, bounds it, and the design keeps the instructions around the
 // paired FMAs few:
-//  * Persistent CTAs of 128 threads walk 16 x 32 output tiles.  x1 over the
-//    tile and its 1-pixel halo (18 x 34 pixels x 16 channels) arrives by
-//    one TMA copy per tile (zero outside the image), with the 64-byte
+//  * Persistent CTAs of 128 threads walk 4 x 32 output tiles, eight CTAs
+//    per SM (20 KB of shared memory, at most 64 registers each): so many
+//    warps per SM outweigh the 1x1's work over the tiles' halos (6 x 34
+//    pixels for 4 x 32; measured at 320 x 320 batch 32: 179 us, against 195
+//    us with 16 x 32 tiles and three CTAs per SM, 182-189 us for the shapes
+//    in between).  x1 over the tile and its 1-pixel halo (16 channels)
+//    arrives by one TMA copy per tile (zero outside the image), with the 64-byte
 //    swizzle (bf16: 32-byte) that puts the k-th 16-byte piece of haloed
 //    pixel p at k ^ (p / 2 % 4) (bf16: k ^ (p / 4 % 2)): eight neighbouring
 //    pixels' pieces then fall in distinct banks.  The next tile's copy is
 //    issued as soon as phase 1 has read this one.
-//  * Phase 1: a over the haloed tile, two pixels per thread at a time, into
+//  * Phase 1: a over the haloed tile, two pixels per thread, into
 //    shared memory; zero outside the image, which is the 3x3's padding (not
 //    act(b1), what the 1x1 would give on the zero-filled x1).
 //  * Phase 2: b as in the 8-channel 3x3 kernel (conv3x3_c8.cu): a thread owns
-//    4 output rows of one column, loads each a row once per filter column
-//    and 4-channel half and reuses it for the 3 filter rows; b stays in the
-//    thread's registers.
-//  * Phase 3: out for the same 4 pixels, 8 output channels per pass, from a
+//    kRows output rows of one column (one at this tile height), loads each a
+//    row once per filter column and 4-channel half and reuses it for the 3
+//    filter rows; b stays in the thread's registers.
+//  * Phase 3: out for the same pixels, 8 output channels per pass, from a
 //    (the tile's centre, shared memory) and b (registers), the residual x1
 //    from global memory (L2: the tile was just read).  Two barriers per
-//    tile; 64 KB of shared memory and at most 168 registers per thread put
-//    three CTAs on an SM.
+//    tile.
 //  * Every product is a paired FMA (fma.rn.f32x2): an accumulator pair holds
 //    the sums over the even and the odd input channels of one (pixel,
 //    output channel), so that both operands come already paired: an input
@@ -50,11 +53,12 @@
 namespace cb {
 namespace {
 
-constexpr int kTW = 32, kTH = 16;              // output tile
-constexpr int kRows = 4;                       // output rows per thread (phases 2 and 3)
-constexpr int kThreads = 32 * kTH / kRows;     // 128: one warp per 4 rows x 32 columns
+constexpr int kTW = 32, kTH = 4;               // output tile
+constexpr int kRows = 1;                       // output rows per thread (phases 2 and 3)
+constexpr int kThreads = 32 * kTH / kRows;     // 128: one warp per kRows rows x 32 columns
+constexpr int kMinBlocks = 8;                  // CTAs per SM (registers: 65536 / (128 x 8) = 64)
 constexpr int kInW = kTW + 2, kInH = kTH + 2;  // the tile with its halo: where a is needed
-constexpr int kInPx = kInW * kInH;             // 612
+constexpr int kInPx = kInW * kInH;             // 204
 constexpr int kABytes = kInPx * 32;            // a: 8 fp32 channels over the haloed tile
 
 template <typename T>
@@ -95,7 +99,7 @@ __device__ __forceinline__ float act_t(float z) {
 }
 
 template <int ACT, typename T>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
     stage_body_kernel(const __grid_constant__ CUtensorMap xmap, const StageBodyArgs a, int tiles_x, int tiles_y) {
   using X = XTile<T>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];

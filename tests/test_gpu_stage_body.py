@@ -3,7 +3,7 @@
 
 The kernel computes in fp32 on the CUDA cores and keeps a and b in shared memory: the bar is the
 fp32 one (1e-5 of max|oracle|) against the oracle's three layers composed.  Shapes cover one and
-several 16 x 32 output tiles, ragged tile edges in both directions and images smaller than a tile
+several 4 x 32 output tiles, ragged tile edges in both directions and images smaller than a tile
 (the 3x3's zero padding sits inside the tile there); the three activations; a channel-slice input
 and an output slice with canaries around it; bf16 storage (within half a bf16 ulp of the oracle on
 the same bf16 values, and bit-equal to the fp32 kernel's output rounded); the three-layer path;
