@@ -466,6 +466,8 @@ class YoloWorkload(Workload):
                     ["stem_tc.cu", "epilogue.cuh", "ptx.cuh", "tc_store.cuh", "launch_util.h", "internal.h"]),
         "s0.body": ("stage_body_kernel_yolo_s0_body_b32.md",
                     ["stage_body.cu", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
+        "s1.body": ("stage_body_tc_kernel_yolo_s1_body_b32.md",
+                    ["stage_body_tc.cu", "epilogue.cuh", "ptx.cuh", "tc_store.cuh", "launch_util.h", "internal.h"]),
         "s0.cv2": ("conv3x3_c8_kernel_yolo_s0_cv2_b32.md",
                    ["conv3x3_c8.cu", "epilogue.cuh", "ptx.cuh", "launch_util.h", "internal.h"]),
         "s0.cv3": ("pw_small_kernel_yolo_s0_cv3_b32.md",
@@ -504,13 +506,14 @@ class YoloWorkload(Workload):
                                                              res_mode=cb.RES_POST_ACT, stream=s))()),
             ]
             views = {"down": (x_in(), B["x1"]), "cv1": (B["x1"], a), "cv2": (a, b), "cv3": (B["cat"], B["out"])}
-            if self.chain.fused[i]:  # the stage body as one kernel (cb_stage_body): FMA-bound
+            if self.chain.fused[i]:  # the stage body as one kernel (cb_stage_body)
                 x1 = B["x1"]
                 steps = steps[:1] + [("body", (lambda i=i: lambda s: self.chain.body(i, stream=s))())]
                 works[f"s{i}.body"] = workloads.stage_body(batch, x1.shape[1], x1.shape[2], x1.shape[3], eb)
             for nm, fn in steps:
-                if nm == "body":
-                    kname, bound = "cb::stage_body_kernel", "alu"
+                if nm == "body":  # 16 channels: fp32 FMAs on the CUDA cores; 32: the tensor cores
+                    kname, bound = (("cb::stage_body_kernel", "alu") if B["x1"].shape[3] == 16 else
+                                    ("cb::stage_body_tc_kernel", "tensor"))
                 else:
                     xv, yv = views[nm]
                     kname, bound = kernel_of(cb, xv, yv, L[nm].k, L[nm].stride, L[nm].pad)
@@ -519,7 +522,8 @@ class YoloWorkload(Workload):
         storage = ("bf16 storage: every layer reads and writes bf16, tensor-core layers multiply bf16 "
                    "weights, fp32 accumulation" if self.bf16 else "fp32")
         self.config = {"workload": "YOLO-style 20-conv chain (5 stages, concat via channel views, post-act "
-                                   f"residual; the 16-channel stage body as one kernel), 640x640x3, {storage}",
+                                   f"residual; the 16-channel{'' if self.bf16 else ' and 32-channel'} stage bodies as one kernel "
+                                   f"each), 640x640x3, {storage}",
                        "batch": batch,
                        "l2": f"inputs_larger_than_l2 ({157 * eb // 4} MB input, {1.2 * eb / 4:.1f} GB of "
                              "activations per step)",
@@ -531,9 +535,12 @@ class YoloWorkload(Workload):
         out = self.chain.bufs[-1]["out"]
         self.out_pin = t.empty(tuple(out.shape), dtype=out.dtype, pin_memory=True)
         # a second device input buffer and a copy stream: step i + 1's input
-        # crosses the link while step i computes
+        # crosses the link while step i computes; the outputs leave on a third
+        # stream, so that they do not queue behind the next input (the link
+        # carries both directions at once)
         self.x_bufs = [self.x, t.empty_like(self.x)]
         self.copy_stream = t.cuda.Stream(self.x.device)
+        self.d2h_stream = t.cuda.Stream(self.x.device)
         return (self.x_pin.numel() * self.x_pin.element_size(),
                 self.out_pin.numel() * self.out_pin.element_size())
 
@@ -544,15 +551,16 @@ class YoloWorkload(Workload):
 
     def e2e_pipelined(self, stream, steps):
         """`steps` steps with host buffers, each: the H2D copy of its input (pinned), the chain, the
-        D2H copy of its output.  The copies run on a second stream: the input into two alternating
+        D2H copy of its output.  The copies run on two more streams: the input into two alternating
         device buffers one step ahead of the chain, the output after the chain is done with it
         (the next step's last layer, which rewrites that buffer, waits for the copy)."""
         t = self.torch
-        copy = self.copy_stream
+        copy, out_s = self.copy_stream, self.d2h_stream
         h2d = [t.cuda.Event(), t.cuda.Event()]
         free = [t.cuda.Event(), t.cuda.Event()]
         done, d2h = t.cuda.Event(), t.cuda.Event()
         copy.wait_stream(stream)
+        out_s.wait_stream(stream)
 
         def issue_h2d(i):
             b = i & 1
@@ -576,11 +584,12 @@ class YoloWorkload(Workload):
                 L.fn(stream)
             free[b].record(stream)
             done.record(stream)
-            with t.cuda.stream(copy):
-                copy.wait_event(done)
+            with t.cuda.stream(out_s):
+                out_s.wait_event(done)
                 self.out_pin.copy_(self.chain.bufs[-1]["out"], non_blocking=True)
-                d2h.record(copy)
+                d2h.record(out_s)
         stream.wait_stream(copy)
+        stream.wait_stream(out_s)
         self.x = self.x_bufs[0]
 
     def cpu_sample(self, n):
@@ -1038,9 +1047,9 @@ def measure(torch, wl, device, stream, args, steps, warmup, min_timed_s, world, 
                                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                                           "ms_per_step": round(e2e_ms, 3),
                                           "step": "one pass with its host copies (pinned memory)" +
-                                                  ("; both copies run on a second stream: the next step's "
-                                                   "input copy (two device input buffers) and this step's "
-                                                   "output copy overlap the chains"
+                                                  ("; the copies run on two more streams, one per "
+                                                   "direction: the next step's input copy (two device input "
+                                                   "buffers) and this step's output copy overlap the chains"
                                                    if hasattr(wl, "e2e_pipelined") else "")},
         "gpu_launches": getattr(wl, "kernels_per_step", len(wl.launches)) * passes * steps,
         "timing": {"steps": f"one CUDA graph of {passes} passes per step, replayed {steps} times, events around "

@@ -311,9 +311,10 @@ def dw_separable_block(x, p, stride, y, workspace, stream=None):
 
 
 def stage_body(x1, layers, act, y, stream=None):
-    """cb_stage_body: the YOLO-style stage body (1x1 16->8, 3x3 8->8, 1x1 on the concat + x1) in one
-    kernel.  layers: three objects with HOST float32 arrays .w_host (OHWI), .scale_host, .bias_host
-    (ConvBnAct layers keep them): the call reads them and puts them in the launch."""
+    """cb_stage_body: the YOLO-style stage body (1x1 C->C/2, 3x3 C/2->C/2, 1x1 on the concat + x1)
+    in one kernel, C = 16 or 32.  layers: three objects with HOST float32 arrays .w_host (OHWI),
+    .scale_host, .bias_host (ConvBnAct layers keep them): the call reads them and puts them in the
+    launch."""
     xv, yv = nhwc(x1), nhwc(y)
     arrs = []
     for L in layers:

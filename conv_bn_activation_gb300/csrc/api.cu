@@ -1636,6 +1636,67 @@ cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const flo
 }
 
 // ------------------------------------------------ YOLO-style stage body
+// Nearest TF32 value of a finite fp32 value (ties to even), as fp32 bits.
+static uint32_t tf32_nearest_bits(float w) {
+  float r = 0.0f;
+  cb_round_weights_tf32(&w, 1, &r);
+  uint32_t b;
+  std::memcpy(&b, &r, sizeof(b));
+  return b;
+}
+
+// C = 32 (validated by cb_stage_body): the weights' shared-memory image, the
+// folded BN and the two tensor maps into the launch.
+static cb_status stage_body_tc(const cb_tensor* x1, const float* w1, const float* s1, const float* b1,
+                               const float* w2, const float* s2, const float* b2, const float* w3, const float* s3,
+                               const float* b3, cb_act act, cb_tensor* y, DeviceInfo* dev, void* stream) {
+  StageBodyTcArgs a{};
+  a.x = static_cast<const float*>(x1->data);
+  a.xs_n = x1->stride_n;
+  a.xs_h = x1->stride_h;
+  a.xs_w = x1->stride_w;
+  a.N = x1->n;
+  a.H = x1->h;
+  a.W = x1->w;
+  a.act = static_cast<int>(act);
+  a.err = dev->err;
+  a.timeout_ns = timeout_ns();
+  // element k of row r of a K-major operand at byte (r * rb + ((k / 4) ^ sw(r)) * 16 + k % 4 * 4)
+  auto put = [&a](int base, int rb, int r, int k, float w) {
+    const int sw = rb == 128 ? (r & 7) : ((r >> 1) & 3);
+    a.wimg[(base + r * rb + (((k >> 2) ^ sw) << 4) + ((k & 3) << 2)) / 4] = tf32_nearest_bits(w);
+  };
+  for (int co = 0; co < 16; ++co)
+    for (int ci = 0; ci < 32; ++ci) put(0, 128, co, ci, w1[co * 32 + ci]);
+  for (int tap = 0; tap < 9; ++tap)
+    for (int co = 0; co < 16; ++co)
+      for (int ci = 0; ci < 16; ++ci) put(2048 + 1024 * tap, 64, co, ci, w2[(co * 9 + tap) * 16 + ci]);
+  for (int co = 0; co < 32; ++co)
+    for (int ci = 0; ci < 32; ++ci) put(11264, 128, co, ci, w3[co * 32 + ci]);
+  for (int c = 0; c < 16; ++c) {
+    a.sb[c] = s1[c], a.sb[16 + c] = b1[c];
+    a.sb[32 + c] = s2[c], a.sb[48 + c] = b2[c];
+  }
+  for (int c = 0; c < 32; ++c) a.sb[64 + c] = s3[c], a.sb[96 + c] = b3[c];
+  int xw = 0, xh = 0, yw = 0, yh = 0;
+  stage_body_tc_boxes(&xw, &xh, &yw, &yh);
+  cuuint64_t xdims[4] = {32, static_cast<cuuint64_t>(x1->w), static_cast<cuuint64_t>(x1->h),
+                         static_cast<cuuint64_t>(x1->n)};
+  cuuint64_t xstr[3] = {static_cast<cuuint64_t>(x1->stride_w) * 4, static_cast<cuuint64_t>(x1->stride_h) * 4,
+                        static_cast<cuuint64_t>(x1->stride_n) * 4};
+  cuuint64_t ystr[3] = {static_cast<cuuint64_t>(y->stride_w) * 4, static_cast<cuuint64_t>(y->stride_h) * 4,
+                        static_cast<cuuint64_t>(y->stride_n) * 4};
+  cuuint32_t xbox[4] = {32, static_cast<cuuint32_t>(xw), static_cast<cuuint32_t>(xh), 1};
+  cuuint32_t ybox[4] = {32, static_cast<cuuint32_t>(yw), static_cast<cuuint32_t>(yh), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUtensorMap xmap, ymap;
+  if (tiled_map(&xmap, 4, x1->data, xdims, xstr, xbox, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+      tiled_map(&ymap, 4, y->data, xdims, ystr, ybox, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return CB_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_stage_body_tc(xmap, ymap, a, dev->sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CB_OK : cuda_fail(e);
+}
+
 cb_status cb_stage_body(const cb_tensor* x1, const float* w1, const float* s1, const float* b1, const float* w2,
                         const float* s2, const float* b2, const float* w3, const float* s3, const float* b3,
                         cb_act act, cb_tensor* y, void* stream) {
@@ -1645,7 +1706,9 @@ cb_status cb_stage_body(const cb_tensor* x1, const float* w1, const float* s1, c
   if (y->n != x1->n || y->h != x1->h || y->w != x1->w || y->c != x1->c || y->dtype != x1->dtype)
     return CB_ERR_INVALID_ARG;
   if (overlap(x1, y)) return CB_ERR_INVALID_ARG;
-  if (x1->c != 16 || x1->layout != CB_LAYOUT_NHWC || y->layout != CB_LAYOUT_NHWC) return CB_ERR_UNSUPPORTED;
+  if ((x1->c != 16 && x1->c != 32) || x1->layout != CB_LAYOUT_NHWC || y->layout != CB_LAYOUT_NHWC)
+    return CB_ERR_UNSUPPORTED;
+  if (x1->c == 32 && !is_f32(x1)) return CB_ERR_UNSUPPORTED;
   // x1 pixels in whole 16-byte pieces (the copy's strides), y in pieces of 4 channels
   const long long xm = is_f32(x1) ? 4 : 8;
   if (!aligned16(x1->data) || !aligned16(y->data) || x1->stride_w % xm != 0 || x1->stride_h % xm != 0 ||
@@ -1656,6 +1719,7 @@ cb_status cb_stage_body(const cb_tensor* x1, const float* w1, const float* s1, c
   DeviceInfo* dev = nullptr;
   cb_status st = current_device(&dev);
   if (st != CB_OK) return st;
+  if (x1->c == 32) return stage_body_tc(x1, w1, s1, b1, w2, s2, b2, w3, s3, b3, act, y, dev, stream);
   StageBodyArgs a{};
   a.x = x1->data;
   a.xs_n = x1->stride_n;
@@ -1688,7 +1752,7 @@ cb_status cb_stage_body(const cb_tensor* x1, const float* w1, const float* s1, c
   a.bf16 = is_f32(x1) ? 0 : 1;
   a.err = dev->err;
   a.timeout_ns = timeout_ns();
-  // x1 as (C = 16, W, H, N); one box is a tile's 18 x 34 haloed pixels
+  // x1 as (C = 16, W, H, N); one box is a tile's haloed pixels
   const cuuint64_t eb = elem_bytes(x1);
   int bc = 0, bw = 0, bh = 0;
   stage_body_box(&bc, &bw, &bh);

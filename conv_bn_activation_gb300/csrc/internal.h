@@ -252,6 +252,31 @@ struct StageBodyArgs {
 void stage_body_box(int* box_c, int* box_w, int* box_h);
 cudaError_t launch_stage_body(const CUtensorMap& xmap, const StageBodyArgs& a, int sms, cudaStream_t s);
 
+// The same body for C = 32 channels (h = 16) on the tensor cores
+// (stage_body_tc.cu), fp32 storage, TF32 operands.  wimg is the weights'
+// shared-memory image, TF32-rounded: the B operands as K-major rows with the
+// tensor core's swizzle (16-byte piece q of row r at q ^ (r % 8) for 128-byte
+// rows, q ^ (r / 2 % 4) for 64-byte rows): w1 [16 co][32 ci] (128-byte rows)
+// at byte 0, w2 per tap kh * 3 + kw [16 co][16 ci] (64-byte rows) at 2048 +
+// 1024 * tap, w3 [32 co][32 ci of a | b] (128-byte rows) at 11264.  The
+// caller encodes xmap (x1 as (C = 32, W, H, N), 128-byte swizzle, box
+// 32 x x_box_w x x_box_h x 1) and ymap (y likewise, box 32 x y_box_w x
+// y_box_h x 1) with the sizes stage_body_tc_boxes gives.
+constexpr int kStageTcWImgWords = (2048 + 9 * 1024 + 4096) / 4;
+struct StageBodyTcArgs {
+  const float* x;  // x1, for the residual
+  long long xs_n, xs_h, xs_w;
+  int N, H, W;
+  int act;
+  int* err;  // device error word, bound of the kernel's waits
+  uint64_t timeout_ns;
+  uint32_t wimg[kStageTcWImgWords];
+  float sb[2 * (16 + 16 + 32)];  // s1[16] b1[16] s2[16] b2[16] s3[32] b3[32]
+};
+void stage_body_tc_boxes(int* x_box_w, int* x_box_h, int* y_box_w, int* y_box_h);
+cudaError_t launch_stage_body_tc(const CUtensorMap& xmap, const CUtensorMap& ymap, const StageBodyTcArgs& a, int sms,
+                                 cudaStream_t s);
+
 // The same layer on the tensor cores (stem_tc.cu) at fp32 accuracy, for packed
 // NHWC input (src kinds 1 and 3: fp32, or bf16 storage with a bf16 output);
 // tiles_x / tiles_y are its own (2 x 64 output pixels).  stem_tc_ok: the tile

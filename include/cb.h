@@ -232,34 +232,40 @@ cb_status cb_dw_separable_block(const cb_tensor* x, const float* dw_w, const flo
 int cb_dw_separable_block_fused(const cb_tensor* x, const cb_tensor* y, const float* pw_w, const float* skip_w);
 
 /*
- * The body of a YOLO-style stage with C = 16 channels in one kernel: the
- * stage after its stride-2 conv ("YOLO26N Inference Optimisation": the
- * conv2d_bn_silu layers of the chain, here its first stage at 320 x 320):
- *     a   = act(s1 * conv1x1(x1) + b1)                 16 -> 8 channels
- *     b   = act(s2 * conv3x3(a) + b2)                  8 -> 8, stride 1, pad 1
- *     y   = act(s3 * conv1x1([a | b]) + b3) + x1       16 -> 16 (a's channels first),
+ * The body of a YOLO-style stage with C = 16 or 32 channels in one kernel:
+ * the stage after its stride-2 conv ("YOLO26N Inference Optimisation": the
+ * conv2d_bn_silu layers of the chain, here its first two stages, at 320 x 320
+ * and 160 x 160), with h = C / 2:
+ *     a   = act(s1 * conv1x1(x1) + b1)                 C -> h channels
+ *     b   = act(s2 * conv3x3(a) + b2)                  h -> h, stride 1, pad 1
+ *     y   = act(s3 * conv1x1([a | b]) + b3) + x1       C -> C (a's channels first),
  *                                                      x1 added after the activation
  * the same as cb_conv_bn_act three times (1x1, 3x3, then the 1x1 on the
  * concatenation with x1 as a CB_RES_POST_ACT residual), with a and b kept
- * in shared memory in fp32 instead of going through HBM.
- *  x1, y: NHWC views of N x H x W x 16, the same dtype (fp32, or bf16 storage:
- *         x1 read and y written as bf16, every product and sum in fp32);
- *         16-byte aligned data, x1 strides multiples of 4 (fp32) or 8 (bf16)
- *         elements, y strides multiples of 4; y must not overlap x1.
- *  w1, w2, w3: HOST fp32 weights, OHWI: [8][1][1][16], [8][3][3][8],
- *         [16][1][1][16] (input channels of w3: a's 8, then b's 8).
- *  s1/b1 (8), s2/b2 (8), s3/b3 (16): HOST fp32 folded BN (cb_fold_bn).
- *         Unlike the layer calls, this one takes its 1,024 parameters from
- *         host memory: they are read during the call and travel in the
- *         launch itself (the kernel reads them from the constant bank, which
- *         costs it no load instructions); a CUDA graph that captured the
- *         call replays the values of capture time.
+ * on the SM instead of going through HBM.
+ *  x1, y: NHWC views of N x H x W x C, the same dtype; 16-byte aligned data,
+ *         x1 strides multiples of 4 (fp32) or 8 (bf16) elements, y strides
+ *         multiples of 4; y must not overlap x1.
+ *  w1, w2, w3: HOST fp32 weights, OHWI: [h][1][1][C], [h][3][3][h],
+ *         [C][1][1][C] (input channels of w3: a's h, then b's h).
+ *  s1/b1 (h), s2/b2 (h), s3/b3 (C): HOST fp32 folded BN (cb_fold_bn).
+ *         Unlike the layer calls, this one takes its parameters from host
+ *         memory: they are read during the call and travel in the launch
+ *         itself (1,024 values for C = 16, 3,968 for C = 32); a CUDA graph
+ *         that captured the call replays the values of capture time.
  *  act:   applied after each of the three BNs.
- * fp32 on the CUDA cores; held to the fp32 bar against the three layers'
- * definition.  Returns CB_ERR_INVALID_ARG for NULL arguments, mismatched
- * shapes or dtypes and overlapping views, CB_ERR_UNSUPPORTED for C != 16 or
- * NCHW views, CB_ERR_ALIGNMENT for the alignment rules above; asynchronous
- * on `stream`.  The kernel's copy waits are bounded (CB_ERR_TIMEOUT through
+ * C = 16: fp32 on the CUDA cores (the weights read from the constant bank,
+ *         which costs the kernel no load instructions), fp32 or bf16 storage
+ *         (bf16: x1 read and y written as bf16, every product and sum in
+ *         fp32); held to the fp32 bar against the three layers' definition.
+ * C = 32: on the tensor cores (kind::tf32 MMAs, fp32 accumulate), fp32
+ *         storage: the precision of the tensor-core layers (weights rounded
+ *         to the nearest TF32 value, a, b and y rounded to the nearest TF32
+ *         value when formed); held to the TF32 bar.
+ * Returns CB_ERR_INVALID_ARG for NULL arguments, mismatched shapes or dtypes
+ * and overlapping views, CB_ERR_UNSUPPORTED for other C, NCHW views or bf16
+ * with C = 32, CB_ERR_ALIGNMENT for the alignment rules above; asynchronous
+ * on `stream`.  The kernels' waits are bounded (CB_ERR_TIMEOUT through
  * cb_get_device_error).
  */
 cb_status cb_stage_body(const cb_tensor* x1, const float* w1, const float* s1, const float* b1, const float* w2,

@@ -67,6 +67,11 @@ def is_canary_bf16(t):
     return bool((t.contiguous().view(torch.int16) == 0x7FDD).all().item())
 
 
+def stage_body_tol(c):
+    """The bar of cb_stage_body at C channels: fp32 on the CUDA cores (16), TF32 on the tensor cores (32)."""
+    return TOL_FP32 if c == 16 else TOL_TF32
+
+
 def oracle_stage_body(orc, x1, st, act=2):
     """The oracle's YOLO-style stage body from its stride-2 output x1 (NHWC): cv1 (1x1), cv2 (3x3,
     pad 1) on cv1's output, cv3 (1x1) on the concat [a | b] with x1 added after the activation --

@@ -25,7 +25,7 @@ import torch
 
 from conv_bn_activation_gb300 import binding as cb, synthetic
 from conv_bn_activation_gb300.nets import ConvBnAct, PreprocessStem, YoloChain
-from gpu_util import TOL_FP32, TOL_TF32, oracle_stage_body, rel_err, sync_check, to_dev
+from gpu_util import TOL_FP32, TOL_TF32, oracle_stage_body, rel_err, stage_body_tol, sync_check, to_dev
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -93,9 +93,10 @@ def test_yolo_chain_full_size_end_to_end(gpu, orc, batch):
 
 
 def test_yolo_chain_batch32_every_layer(gpu, orc):
-    """Batch 32, 640 x 640: each layer (the 16-channel stage body, one kernel, as one unit), whole
-    output, against the oracle fed the GPU's own input (per-layer tolerance class; the fused body
-    computes in fp32 on the CUDA cores: the fp32 bar)."""
+    """Batch 32, 640 x 640: each layer (the 16- and 32-channel stage bodies, one kernel each, as one
+    unit), whole output, against the oracle fed the GPU's own input (per-layer tolerance class; the
+    16-channel body computes in fp32 on the CUDA cores: the fp32 bar; the 32-channel one on the
+    tensor cores: the TF32 bar)."""
     stages = synthetic.yolo_params()
     x = synthetic.yolo_input(32)
     chain = YoloChain(stages, 32)
@@ -104,7 +105,7 @@ def test_yolo_chain_batch32_every_layer(gpu, orc):
     chain.forward(xd)
     sync_check()
     h = x
-    assert chain.fused[0]
+    assert chain.fused[0] and chain.fused[1]
     for i, (st, B) in enumerate(zip(stages, chain.bufs)):
         half = B["half"]
         x1 = B["x1"].cpu().numpy()
@@ -114,7 +115,7 @@ def test_yolo_chain_batch32_every_layer(gpu, orc):
         checks = [("down", h, st["down_w"], st["down_bn"], 2, 1, x1, None)]
         if chain.fused[i]:
             err = rel_err(out, oracle_stage_body(orc, x1, st))
-            assert err <= TOL_FP32, f"s{i}.body: {err:.3g}"
+            assert err <= stage_body_tol(out.shape[-1]), f"s{i}.body: {err:.3g}"
         else:
             checks += [
                 ("cv1", x1, st["cv1_w"], st["cv1_bn"], 1, 0, a, None),

@@ -10,7 +10,7 @@ import torch
 
 from conv_bn_activation_gb300 import binding as cb, synthetic
 from conv_bn_activation_gb300.nets import MnistNet, PreprocessStem, YoloChain
-from gpu_util import TOL_FP32, TOL_TF32, oracle_stage_body, rel_err, sync_check, to_dev
+from gpu_util import TOL_FP32, TOL_TF32, oracle_stage_body, rel_err, stage_body_tol, sync_check, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -47,13 +47,13 @@ def test_mnist_graph_replay_matches_eager(gpu):
 
 @pytest.mark.parametrize("fuse_body", [True, False], ids=["fused_body", "layers"])
 def test_yolo_chain_small(gpu, orc, fuse_body):
-    """The chain end to end at 96 x 96, with the 16-channel stage body as one kernel or as its
-    three layers."""
+    """The chain end to end at 96 x 96, with the 16- and 32-channel stage bodies as one kernel each
+    or as their three layers."""
     stages = synthetic.yolo_params()
     x = synthetic.yolo_input(2, size=96)
     chain = YoloChain(stages, 2, size=96, fuse_body=fuse_body)
-    assert chain.fused[0] == fuse_body and not any(chain.fused[1:])
-    assert chain.launches_per_forward == (18 if fuse_body else 20)
+    assert chain.fused[:2] == [fuse_body] * 2 and not any(chain.fused[2:])
+    assert chain.launches_per_forward == (16 if fuse_body else 20)
     out = chain.forward(to_dev(x))
     sync_check()
     h = x
@@ -78,7 +78,7 @@ def test_yolo_chain_full_size_per_layer(gpu, orc):
         out = B["out"].cpu().numpy()
         checks = [(h, st["down_w"], st["down_bn"], 2, 1, x1, None)]
         if chain.fused[i]:  # the body as one unit (a and b never reach memory)
-            assert rel_err(out, oracle_stage_body(orc, x1, st)) <= TOL_FP32
+            assert rel_err(out, oracle_stage_body(orc, x1, st)) <= stage_body_tol(out.shape[-1])
         else:
             checks += [
                 (x1, st["cv1_w"], st["cv1_bn"], 1, 0, cat[..., :half], None),

@@ -1,5 +1,7 @@
-"""GPU parity of cb_stage_body: the body of a YOLO-style stage with 16 channels (1x1 16->8, 3x3
-8->8 on its output, 1x1 on the concat [a | b] with x1 added after the activation) in one kernel.
+"""GPU parity of cb_stage_body: the body of a YOLO-style stage (1x1 C->C/2, 3x3 C/2->C/2 on its
+output, 1x1 on the concat [a | b] with x1 added after the activation) in one kernel.
+
+C = 16 (stage 0 of the chain):
 
 The kernel computes in fp32 on the CUDA cores and keeps a and b in shared memory: the bar is the
 fp32 one (1e-5 of max|oracle|) against the oracle's three layers composed.  Shapes cover one and
@@ -8,6 +10,12 @@ several 4 x 32 output tiles, ragged tile edges in both directions and images sma
 and an output slice with canaries around it; bf16 storage (within half a bf16 ulp of the oracle on
 the same bf16 values, and bit-equal to the fp32 kernel's output rounded); the three-layer path;
 and the argument checks.
+
+C = 32 (stage 1) runs on the tensor cores with TF32 operands, the precision of the tensor-core
+layers: the bar is the TF32 one (5e-3 of max|oracle|), every output is a TF32 value (the low 13
+mantissa bits clear), and the shapes add one with more tiles than the grid has warpgroups, so that
+each warpgroup walks several tiles (the next tile's copy issued early, the output store of one tile
+in flight while the next is computed).
 """
 import numpy as np
 import pytest
@@ -15,7 +23,7 @@ import torch
 
 from conv_bn_activation_gb300 import binding as cb, synthetic
 from conv_bn_activation_gb300.nets import ConvBnAct
-from gpu_util import TOL_FP32, bf16_within_half_ulp, canary_buffer, canary_buffer_bf16, is_canary, \
+from gpu_util import TOL_FP32, TOL_TF32, bf16_within_half_ulp, canary_buffer, canary_buffer_bf16, is_canary, \
     is_canary_bf16, oracle_stage_body, rel_err, sync_check, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
@@ -23,11 +31,12 @@ pytestmark = pytest.mark.gpu
 SHAPES = [(2, 20, 40), (1, 16, 32), (3, 17, 33), (1, 1, 1), (1, 2, 3), (2, 40, 70), (1, 33, 95), (1, 48, 8)]
 
 
-def _stage(seed):
-    """Stage 0 of the YOLO-style chain's parameters (16 channels), reseeded."""
+def _stage(seed, C=16):
+    """A stage body's parameters with C channels (stage 0 of the chain: 16, stage 1: 32), reseeded."""
     g = np.random.default_rng(seed)
     st = {}
-    for key, (co, ci, k) in {"cv1": (8, 16, 1), "cv2": (8, 8, 3), "cv3": (16, 16, 1)}.items():
+    h = C // 2
+    for key, (co, ci, k) in {"cv1": (h, C, 1), "cv2": (h, h, 3), "cv3": (C, C, 1)}.items():
         st[key + "_w"] = synthetic.kaiming(g, co, ci, k, k)
         st[key + "_bn"] = synthetic.bn_params(g, co)
     return st
@@ -153,4 +162,103 @@ def test_stage_body_rejects(gpu):
     with pytest.raises(cb.CbError) as e:  # pixels 18 floats apart: not whole 16-byte pieces
         cb.stage_body(torch.zeros(1, 8, 8, 18, device=gpu)[..., :16], layers, cb.ACT_SILU,
                       torch.empty(1, 8, 8, 16, device=gpu))
+    assert e.value.status == cb.ERR_ALIGNMENT
+
+
+# ----------------------------------------------------------------- C = 32: tensor cores
+SHAPES32 = [(2, 20, 40), (1, 4, 32), (3, 17, 33), (1, 1, 1), (1, 2, 3), (2, 40, 70), (1, 33, 95), (1, 48, 8),
+            (8, 102, 130)]
+
+
+def _is_tf32(t):
+    return bool(((t.contiguous().view(torch.int32) & 0x1FFF) == 0).all().item())
+
+
+@pytest.mark.parametrize("shape", SHAPES32, ids=lambda s: "x".join(map(str, s)))
+def test_stage_body_c32(gpu, orc, shape):
+    N, H, W = shape
+    st = _stage(N + H + W, C=32)
+    x1 = np.random.default_rng(H * W + 1).standard_normal((N, H, W, 32)).astype(np.float32)
+    y = torch.empty(N, H, W, 32, device=gpu)
+    cb.stage_body(to_dev(x1), _layers(st, cb.ACT_SILU), cb.ACT_SILU, y)
+    assert "stage_body_tc_kernel" in cb.last_launch()["kernel"]
+    sync_check()
+    assert rel_err(y.cpu().numpy(), oracle_stage_body(orc, x1, st)) <= TOL_TF32
+    assert _is_tf32(y)
+
+
+@pytest.mark.parametrize("act", [cb.ACT_NONE, cb.ACT_RELU])
+def test_stage_body_c32_activations(gpu, orc, act):
+    N, H, W = 2, 18, 36
+    st = _stage(act + 60, C=32)
+    x1 = np.random.default_rng(act + 9).standard_normal((N, H, W, 32)).astype(np.float32)
+    y = torch.empty(N, H, W, 32, device=gpu)
+    cb.stage_body(to_dev(x1), _layers(st, act), act, y)
+    sync_check()
+    assert rel_err(y.cpu().numpy(), oracle_stage_body(orc, x1, st, act=act)) <= TOL_TF32
+
+
+def test_stage_body_c32_matches_the_three_layers(gpu, orc):
+    """The fused body against the same body run as three cb_conv_bn_act calls (a and b through
+    memory): both within the TF32 bar of the oracle and of each other."""
+    N, H, W = 4, 50, 64
+    st = _stage(8, C=32)
+    x1 = np.random.default_rng(8).standard_normal((N, H, W, 32)).astype(np.float32)
+    l1, l2, l3 = _layers(st, cb.ACT_SILU)
+    xd = to_dev(x1)
+    y = torch.empty(N, H, W, 32, device=gpu)
+    cb.stage_body(xd, (l1, l2, l3), cb.ACT_SILU, y)
+    cat = torch.empty(N, H, W, 32, device=gpu)
+    y3 = torch.empty_like(y)
+    l1(xd, cat[..., :16])
+    l2(cat[..., :16], cat[..., 16:])
+    l3(cat, y3, residual=xd, res_mode=cb.RES_POST_ACT)
+    sync_check()
+    ref = oracle_stage_body(orc, x1, st)
+    assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
+    assert rel_err(y.cpu().numpy(), y3.cpu().numpy()) <= 2 * TOL_TF32
+
+
+def test_stage_body_c32_views(gpu, orc):
+    """x1 as channels [16, 48) of a 64-channel buffer; the output into channels [4, 36) of a
+    40-channel buffer with padded rows: the tensor store writes nothing around it."""
+    N, H, W = 2, 19, 45
+    st = _stage(4, C=32)
+    wide = np.random.default_rng(4).standard_normal((N, H, W, 64)).astype(np.float32)
+    x1 = np.ascontiguousarray(wide[..., 16:48])
+    xd = to_dev(wide)[..., 16:48]
+    buf = canary_buffer((N, H, W + 5, 40))
+    y = buf[:, :, :W, 4:36]
+    cb.stage_body(xd, _layers(st, cb.ACT_SILU), cb.ACT_SILU, y)
+    sync_check()
+    assert rel_err(y.cpu().numpy(), oracle_stage_body(orc, x1, st)) <= TOL_TF32
+    assert is_canary(buf[..., :4]) and is_canary(buf[..., 36:]) and is_canary(buf[:, :, W:])
+
+
+def test_stage_body_c32_full_size_stage1(gpu, orc):
+    """The chain's stage 1 body at its size (160 x 160, batch 32, the 640 x 640 input's second
+    stride-2 output), every output against the oracle."""
+    st = synthetic.yolo_params()[1]
+    x1 = np.random.default_rng(6).standard_normal((32, 160, 160, 32)).astype(np.float32)
+    y = torch.empty(32, 160, 160, 32, device=gpu)
+    cb.stage_body(to_dev(x1), _layers(st, cb.ACT_SILU), cb.ACT_SILU, y)
+    sync_check()
+    assert rel_err(y.cpu().numpy(), oracle_stage_body(orc, x1, st)) <= TOL_TF32
+
+
+def test_stage_body_c32_rejects(gpu):
+    layers = _layers(_stage(2, C=32), cb.ACT_SILU)
+    with pytest.raises(cb.CbError) as e:  # bf16 storage: no 32-channel kernel
+        cb.stage_body(torch.zeros(1, 8, 8, 32, device=gpu, dtype=torch.bfloat16), layers, cb.ACT_SILU,
+                      torch.empty(1, 8, 8, 32, device=gpu, dtype=torch.bfloat16))
+    assert e.value.status == cb.ERR_UNSUPPORTED
+    with pytest.raises(cb.CbError) as e:  # 24 channels: no kernel
+        cb.stage_body(torch.zeros(1, 8, 8, 24, device=gpu), layers, cb.ACT_SILU, torch.empty(1, 8, 8, 24, device=gpu))
+    assert e.value.status == cb.ERR_UNSUPPORTED
+    x1 = torch.zeros(1, 8, 8, 32, device=gpu)
+    with pytest.raises(cb.CbError) as e:  # in place
+        cb.stage_body(x1, layers, cb.ACT_SILU, x1)
+    assert e.value.status == cb.ERR_INVALID_ARG
+    with pytest.raises(cb.CbError) as e:  # output rows 34 floats apart: not whole 16-byte pieces
+        cb.stage_body(x1, layers, cb.ACT_SILU, torch.empty(1, 8, 8, 34, device=gpu)[..., :32])
     assert e.value.status == cb.ERR_ALIGNMENT
