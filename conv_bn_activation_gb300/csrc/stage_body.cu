@@ -175,10 +175,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         if (i == 1 && !live1) break;
         const int r = pp[i] / kInW, c = pp[i] - r * kInW;
         const int ih = ih0 + r, iw = iw0 + c;
-        const bool in = ih >= 0 && ih < a.H && iw >= 0 && iw < a.W;
+        // outside the image a is +0: every value computed, then masked (a select
+        // made the compiler branch around each value's exponential)
+        const uint32_t keep = ih >= 0 && ih < a.H && iw >= 0 && iw < a.W ? 0xFFFFFFFFu : 0u;
         float v[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = in ? act_t<ACT>(fmaf(acc[i][q].x + acc[i][q].y, sb[q], sb[8 + q])) : 0.0f;
+        for (int q = 0; q < 8; ++q)
+          v[q] = __uint_as_float(__float_as_uint(act_t<ACT>(fmaf(acc[i][q].x + acc[i][q].y, sb[q], sb[8 + q]))) & keep);
         *reinterpret_cast<float4*>(at + ab_off(r, c, kInW, 0)) = make_float4(v[0], v[1], v[2], v[3]);
         *reinterpret_cast<float4*>(at + ab_off(r, c, kInW, 1)) = make_float4(v[4], v[5], v[6], v[7]);
       }
