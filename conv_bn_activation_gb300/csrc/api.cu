@@ -297,11 +297,13 @@ struct Tuning {
   int timeout_ms = 2000;           // CB_TIMEOUT_MS: bound of every device wait
   int dw_skip_row = 0;             // CB_DEBUG_DW_SKIP_ROW = 1: fault injection (see cb_set_tuning)
   int stem_kernel = 0;             // CB_STEM_KERNEL = "cuda" / "tc" (0: tensor cores for NHWC input)
+  int stage_skip_x = 0;            // CB_DEBUG_STAGE_SKIP_X = 1: fault injection (see cb_set_tuning)
 };
 
 const char* const kTuningNames[] = {"CB_DW_FORCE",    "CB_IGEMM_FORCE", "CB_IGEMM_BLOCKS", "CB_HALO_FORCE",
                                     "CB_DW_BLOCK_FORCE", "CB_DEBUG_PLAN", "CB_IGEMM_TRACE", "CB_SPAN_SLOT",
-                                    "CB_TIMEOUT_MS",  "CB_DEBUG_DW_SKIP_ROW", "CB_STEM_KERNEL"};
+                                    "CB_TIMEOUT_MS",  "CB_DEBUG_DW_SKIP_ROW", "CB_STEM_KERNEL",
+                                    "CB_DEBUG_STAGE_SKIP_X"};
 
 // Sets knob `name` of *t from `v` (NULL or "" restores the knob's default);
 // false for an unknown name.
@@ -340,6 +342,8 @@ bool parse_tuning(Tuning* t, const char* name, const char* v) {
     t->timeout_ms = ms > 0 ? ms : d.timeout_ms;
   } else if (!std::strcmp(name, "CB_DEBUG_DW_SKIP_ROW")) {
     t->dw_skip_row = unset ? 0 : (std::atoi(v) != 0 ? 1 : 0);
+  } else if (!std::strcmp(name, "CB_DEBUG_STAGE_SKIP_X")) {
+    t->stage_skip_x = unset ? 0 : (std::atoi(v) != 0 ? 1 : 0);
   } else if (!std::strcmp(name, "CB_STEM_KERNEL")) {
     t->stem_kernel = unset ? 0 : !std::strcmp(v, "cuda") ? 1 : !std::strcmp(v, "tc") ? 2 : 0;
   } else {
@@ -1661,6 +1665,7 @@ static cb_status stage_body_tc(const cb_tensor* x1, const float* w1, const float
   a.act = static_cast<int>(act);
   a.err = dev->err;
   a.timeout_ns = timeout_ns();
+  a.debug_skip_x = tuning().stage_skip_x;
   // element k of row r of a K-major operand at byte (r * rb + ((k / 4) ^ sw(r)) * 16 + k % 4 * 4)
   auto put = [&a](int base, int rb, int r, int k, float w) {
     const int sw = rb == 128 ? (r & 7) : ((r >> 1) & 3);

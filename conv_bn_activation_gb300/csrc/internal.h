@@ -270,6 +270,7 @@ struct StageBodyTcArgs {
   int act;
   int* err;  // device error word, bound of the kernel's waits
   uint64_t timeout_ns;
+  int debug_skip_x;  // 1: fault injection for tests of the bounded waits (no warpgroup issues its first x1 copy)
   uint32_t wimg[kStageTcWImgWords];
   float sb[2 * (16 + 16 + 32)];  // s1[16] b1[16] s2[16] b2[16] s3[32] b3[32]
 };

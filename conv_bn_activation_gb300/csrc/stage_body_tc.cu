@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ++mma_done;
     return ok;
   };
-  if (leader && first < num_tiles) {
+  if (leader && first < num_tiles && !a.debug_skip_x) {  // (fault injection: nothing issued, the first wait runs out)
     issue_x(first);
     ++x_issued;
   }

@@ -503,6 +503,11 @@ int cb_autotune_entries(void);
  *                     records CB_ERR_TIMEOUT (cb_get_device_error), drains the
  *                     copies it issued and returns; that layer's output is not
  *                     valid.  Nothing faults or hangs.
+ *   CB_DEBUG_STAGE_SKIP_X  "1": the same for the 32-channel stage body
+ *                     (cb_stage_body): no warpgroup issues the copy or the barrier
+ *                     arrive of its first input tile, so each first wait runs out;
+ *                     the kernel records CB_ERR_TIMEOUT, frees its tensor memory
+ *                     and returns; the output is not valid.
  * and `value` its setting (NULL or "" restores the default).  Each knob
  * starts from the environment variable of the same name, read once per
  * process; only this call changes it afterwards.  While a plan override of

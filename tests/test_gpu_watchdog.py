@@ -7,6 +7,7 @@ usable: a layer launched afterwards still matches the oracle.
 """
 import time
 
+import numpy as np
 import pytest
 import torch
 
@@ -62,3 +63,30 @@ def test_depthwise_pipeline_wait_runs_out(gpu, orc, stride):
     sync_check()
     ref = orc.conv_bn_act(x, w, bn, stride=stride, pad=1, groups=64, act=orc.ACT_RELU)
     assert rel_err(y.cpu().numpy(), ref) <= TOL_FP32
+
+
+def test_stage_body_tc_wait_runs_out(gpu, orc):
+    """Inside the tensor-core stage body (32 channels): no warpgroup issues the copy or the barrier
+    arrive of its first x1 tile (fault injection through CB_DEBUG_STAGE_SKIP_X, nothing is issued
+    against that barrier), so each first wait runs out after CB_TIMEOUT_MS or sees the CTA's abort
+    flag.  The kernel records CB_ERR_TIMEOUT, frees its tensor memory and returns: no hang, no
+    fault.  The error reads once, and the same body run again without the injection matches the
+    oracle."""
+    from conv_bn_activation_gb300.nets import ConvBnAct as L
+    from gpu_util import oracle_stage_body
+    st = synthetic.yolo_params()[1]
+    layers = [L(st[k + "_w"], st[k + "_bn"], 1, p, cb.ACT_SILU) for k, p in (("cv1", 0), ("cv2", 1), ("cv3", 0))]
+    x1 = np.random.default_rng(11).standard_normal((2, 20, 40, 32)).astype(np.float32)
+    xd = to_dev(x1)
+    y = torch.empty(2, 20, 40, 32, device="cuda")
+    assert cb.get_device_error() == cb.OK
+    with cb.tuning("CB_TIMEOUT_MS", "50"), cb.tuning("CB_DEBUG_STAGE_SKIP_X", "1"):
+        t0 = time.perf_counter()
+        cb.stage_body(xd, layers, cb.ACT_SILU, y)
+        assert "stage_body_tc_kernel" in cb.last_launch()["kernel"]
+        assert cb.get_device_error() == cb.ERR_TIMEOUT
+        assert time.perf_counter() - t0 < 5.0
+    assert cb.get_device_error() == cb.OK  # reading cleared it
+    cb.stage_body(xd, layers, cb.ACT_SILU, y)
+    sync_check()
+    assert rel_err(y.cpu().numpy(), oracle_stage_body(orc, x1, st)) <= TOL_TF32
