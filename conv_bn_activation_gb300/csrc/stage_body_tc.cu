@@ -36,10 +36,12 @@
 //    read: L2; loaded while the 3x3's MMAs run) is staged in shared memory over the
 //    copies of a and leaves by one TMA tensor store, which clips the tile at
 //    the image's edges.
-//  * One thread of each warpgroup issues its TMA copies and MMAs and alone
-//    waits for them (bounded waits); the others wait in the warpgroup's named
-//    barrier.  The next tile's x1 is loaded as soon as this tile's first
-//    MMAs have read it.
+//  * Two threads of each warpgroup issue and wait (bounded waits); the others
+//    wait in the warpgroup's named barrier.  One issues the 3x3's and the
+//    last 1x1's MMAs and the output store; the other the x1 copies and the
+//    first 1x1's MMAs: it loads the next tile's x1 as soon as this tile's
+//    first MMAs have read it, and issues the next tile's 1x1 while this
+//    tile's 3x3 runs, so that the next tile starts at its first epilogue.
 //  * The epilogues compute every value unconditionally and mask the ones
 //    outside the image afterwards: a select around each value made the
 //    compiler branch around its exponential, one value after another.
@@ -59,14 +61,15 @@ constexpr int kHW = kTW + 2, kHH = kTH + 2;     // the haloed tile
 constexpr int kHPx = kHW * kHH;                 // 204 haloed pixels
 constexpr int kWG = 3;                          // warpgroups per CTA
 constexpr int kThreads = kWG * kM;
-constexpr int kXBytes = 26 * 1024;              // 204 rows x 128 bytes, rounded to the swizzle atom
+constexpr int kXBytes = 2 * kM * 128;           // the 1x1's two row blocks (rows past 204 never used)
 constexpr int kCopyRows = kHH * kTW;            // 192 rows per copy of a
 constexpr int kCopyBytes = kCopyRows * 64;      // 16 fp32 channels per row
 constexpr int kWGBytes = kXBytes + 3 * kCopyBytes;
 constexpr int kW1 = 0, kW2 = 2048, kW3 = 11264;  // the weights' image (StageBodyTcArgs::wimg)
 constexpr int kWBytes = kStageTcWImgWords * 4;
-constexpr int kBar = kWBytes + kWG * kWGBytes;  // MMA barriers [kWG], x1 barriers [kWG]
-constexpr int kSmemEnd = kBar + 16 * kWG + 8;
+constexpr int kBar = kWBytes + kWG * kWGBytes;  // per warpgroup: 3x3 / last 1x1, x1, first 1x1, two drains
+constexpr int kBarsPerWG = 5;
+constexpr int kSmemEnd = kBar + 8 * kBarsPerWG * kWG + 8;
 constexpr int kTmemCols = 256;                  // 80 per warpgroup: D1 (2 x 16), D2 (16), D3 (32)
 constexpr int kWGCols = 80;
 static_assert(kW3 + 32 * 128 == kWBytes, "weight image");
@@ -157,18 +160,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const xs = smem + kWBytes + g * kWGBytes;  // haloed x1
   uint8_t* const cp0 = xs + kXBytes;                   // copies of a (dx = 0, 1, 2); b over copy 0
   uint64_t* const bars = reinterpret_cast<uint64_t*>(smem + kBar);
-  uint64_t* const mbar = bars + g;         // this warpgroup's MMA completions
-  uint64_t* const xfull = bars + kWG + g;  // its x1 copies
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kWG);
+  uint64_t* const mbar = bars + kBarsPerWG * g;  // this warpgroup's 3x3 and last 1x1 completions
+  uint64_t* const xfull = mbar + 1;              // its x1 copies
+  uint64_t* const d1bar = mbar + 2;              // its first 1x1 completions
+  uint64_t* const drain = mbar + 3;              // [2]: the two issuing threads' MMAs, on the way out
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarsPerWG * kWG);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int bar_id = 1 + g;  // named barrier of the warpgroup (0 is __syncthreads)
-  // thread 0 of the warpgroup's last warp issues and waits: in the first
-  // epilogue that warp has one haloed pixel per thread where warps 0-1 have
-  // two, so the next tile's copy, issued there, costs the others no time
-  const bool leader = t == 96;
+  // Two threads of the warpgroup issue and wait, from warps that have one
+  // haloed pixel per thread in the first epilogue (warps 0-1 have two):
+  // the leader (warp 3) the 3x3's and the last 1x1's MMAs and the output
+  // store; the x1 thread (warp 2) the x1 copies and the first 1x1's MMAs,
+  // which it issues for the next tile while the leader issues this tile's
+  // 3x3 and the rest of the warpgroup waits.
+  const bool leader = t == 96, xthr = t == 64;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * kWG; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kBarsPerWG * kWG; ++i) mbar_init(&bars[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&xmap);
@@ -202,41 +210,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_tiles = a.N * tiles_y * tiles_x;
   const int workers = static_cast<int>(gridDim.x) * kWG;
   const int first = g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
-  auto issue_x = [&](int tile) {  // the leader: tile's haloed x1
+  auto issue_x = [&](int tile) {  // the x1 thread: tile's haloed x1
     const int tx = tile % tiles_x, rest = tile / tiles_x, ty = rest % tiles_y, n = rest / tiles_y;
     mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(kHPx * 128));
     tma_load_4d(xs, &xmap, xfull, 0, tx * kTW - 1, ty * kTH - 1, n);
   };
-  // the leader's bookkeeping: copies / MMA groups issued and waited for
-  int x_issued = 0, x_done = 0, mma_issued = 0, mma_done = 0;
-  bool stores = false;  // a tensor store whose source the next tile overwrites
+  // bookkeeping of the two issuing threads: copies issued / waited for (x1
+  // thread), MMA groups waited for (leader), whether either issued MMAs
+  int x_issued = 0, x_done = 0, mma_done = 0, d1_done = 0;
+  bool issued_mma = false;
+  bool stores = false;  // the leader: a tensor store whose source the next tile overwrites
   auto mma_wait = [&]() {  // the leader: commit the MMAs issued, wait for them
     mma_commit(mbar);
-    ++mma_issued;
     const bool ok = mbar_wait(mbar, static_cast<uint32_t>(mma_done) & 1u, wd);
     if (ok) ++mma_done;
     return ok;
   };
-  if (leader && first < num_tiles && !a.debug_skip_x) {  // (fault injection: nothing issued, the first wait runs out)
-    issue_x(first);
-    ++x_issued;
+  // the x1 thread: wait for the x1 of the tile to run next, issue its 1x1
+  // into D1, committed to d1bar (the leader waits for it before the epilogue
+  // that reads D1)
+  auto cv1 = [&]() {
+    if (!mbar_wait(xfull, static_cast<uint32_t>(x_done) & 1u, wd)) return false;
+    ++x_done;
+    tc_fence_after_sync();
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_tf32(tmem + 16 * m, dx1[m] + 2 * j, dw1 + 2 * j, id16, j > 0 ? 1u : 0u);
+    mma_commit(d1bar);
+    issued_mma = true;
+    return true;
+  };
+  bool xok = true;  // the x1 thread: the 1x1 of the tile about to run was issued
+  if (xthr && first < num_tiles) {
+    if (!a.debug_skip_x) {  // (fault injection: nothing issued, the first wait runs out)
+      issue_x(first);
+      ++x_issued;
+    }
+    xok = cv1();
   }
 
   for (int tile = first; tile < num_tiles; tile += workers) {
     const int tx = tile % tiles_x, rest = tile / tiles_x, ty = rest % tiles_y, n = rest / tiles_y;
-    // ---------------------------------------- a = 1x1 over the haloed tile
+    const bool more = tile + workers < num_tiles;
+    // ---------------------------------------- a = 1x1 over the haloed tile (issued ahead)
     bool ok = true;
+    if (xthr) ok = xok;
     if (leader) {
-      ok = mbar_wait(xfull, static_cast<uint32_t>(x_done) & 1u, wd);
-      if (ok) {
-        ++x_done;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) mma_tf32(tmem + 16 * m, dx1[m] + 2 * j, dw1 + 2 * j, id16, j > 0 ? 1u : 0u);
-        ok = mma_wait();
-      }
+      ok = mbar_wait(d1bar, static_cast<uint32_t>(d1_done) & 1u, wd);
+      if (ok) ++d1_done;
       if (ok && stores) {  // the previous tile's output has left the copies of a
         bulk_wait_read_all();
         stores = false;
@@ -244,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     if (!group_sync_and(bar_id, ok)) break;
-    if (leader && tile + workers < num_tiles) {  // x1 has been read: the next tile's
+    if (xthr && more) {  // x1 has been read: the next tile's
       issue_x(tile + workers);
       ++x_issued;
     }
@@ -304,7 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 2; ++j)
             mma_tf32(tmem + 32, dcp + dx * kCopyStep + dy * kDyStep + 2 * j, dw2 + (dy * 3 + dx) * kTapStep + 2 * j,
                      id16, (dy | dx | j) != 0 ? 1u : 0u);
+      issued_mma = true;
       ok = mma_wait();
+    }
+    if (xthr && more) {  // the next tile's 1x1 meanwhile: D1 and the x1 buffer are free
+      xok = cv1();
+      ok = xok;
     }
     __syncwarp();
     if (!group_sync_and(bar_id, ok)) break;
@@ -365,11 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // on the way out (also after a timeout): the copy and the MMA group still
   // in flight land, the stores complete, before the shared memory and TMEM
   // are released
-  if (leader) {
-    if (x_issued > x_done) mbar_wait_drain(xfull, static_cast<uint32_t>(x_done) & 1u, 20000000ull);
-    if (mma_issued > mma_done) mbar_wait_drain(mbar, static_cast<uint32_t>(mma_done) & 1u, 20000000ull);
-    bulk_wait_all();
+  if (xthr && x_issued > x_done) mbar_wait_drain(xfull, static_cast<uint32_t>(x_done) & 1u, 20000000ull);
+  if ((leader || xthr) && issued_mma) {  // a commit with nothing after it: all this thread's MMAs are done
+    uint64_t* const d = drain + (leader ? 0 : 1);
+    mma_commit(d);
+    mbar_wait_drain(d, 0u, 20000000ull);
   }
+  if (leader) bulk_wait_all();
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) {
