@@ -522,8 +522,8 @@ class YoloWorkload(Workload):
         storage = ("bf16 storage: every layer reads and writes bf16, tensor-core layers multiply bf16 "
                    "weights, fp32 accumulation" if self.bf16 else "fp32")
         self.config = {"workload": "YOLO-style 20-conv chain (5 stages, concat via channel views, post-act "
-                                   f"residual; the 16-channel{'' if self.bf16 else ' and 32-channel'} stage bodies as one kernel "
-                                   f"each), 640x640x3, {storage}",
+                                   "residual; the 16- and 32-channel stage bodies as one kernel each), "
+                                   f"640x640x3, {storage}",
                        "batch": batch,
                        "l2": f"inputs_larger_than_l2 ({157 * eb // 4} MB input, {1.2 * eb / 4:.1f} GB of "
                              "activations per step)",

@@ -1655,7 +1655,8 @@ static cb_status stage_body_tc(const cb_tensor* x1, const float* w1, const float
                                const float* w2, const float* s2, const float* b2, const float* w3, const float* s3,
                                const float* b3, cb_act act, cb_tensor* y, DeviceInfo* dev, void* stream) {
   StageBodyTcArgs a{};
-  a.x = static_cast<const float*>(x1->data);
+  const bool bf = !is_f32(x1);
+  a.x = x1->data;
   a.xs_n = x1->stride_n;
   a.xs_h = x1->stride_h;
   a.xs_w = x1->stride_w;
@@ -1665,19 +1666,47 @@ static cb_status stage_body_tc(const cb_tensor* x1, const float* w1, const float
   a.act = static_cast<int>(act);
   a.err = dev->err;
   a.timeout_ns = timeout_ns();
+  a.bf16 = bf ? 1 : 0;
   a.debug_skip_x = tuning().stage_skip_x;
-  // element k of row r of a K-major operand at byte (r * rb + ((k / 4) ^ sw(r)) * 16 + k % 4 * 4)
-  auto put = [&a](int base, int rb, int r, int k, float w) {
-    const int sw = rb == 128 ? (r & 7) : ((r >> 1) & 3);
-    a.wimg[(base + r * rb + (((k >> 2) ^ sw) << 4) + ((k & 3) << 2)) / 4] = tf32_nearest_bits(w);
+  // element k of row r of a K-major operand of rb-byte rows at byte r * rb +
+  // ((k * eb / 16) ^ sw(r)) * 16 + k * eb % 16, sw the swizzle of rb-byte rows
+  const int eb = bf ? 2 : 4;
+  uint8_t* const img = reinterpret_cast<uint8_t*>(a.wimg);
+  // lo: the bf16 tail w - bf16(w) of a split weight (the 1x1 layers with bf16 storage)
+  auto put = [img, eb](int base, int rb, int r, int k, float w, bool lo) {
+    const int sw = rb == 128 ? (r & 7) : rb == 64 ? ((r >> 1) & 3) : ((r >> 2) & 1);
+    const int at = base + r * rb + ((((k * eb) >> 4) ^ sw) << 4) + ((k * eb) & 15);
+    if (eb == 4) {
+      const uint32_t b = tf32_nearest_bits(w);
+      std::memcpy(img + at, &b, 4);
+    } else {
+      uint16_t h = 0;
+      cb_convert_weights_bf16(&w, 1, &h);  // nearest even
+      if (lo) {
+        const uint32_t hb = static_cast<uint32_t>(h) << 16;
+        float hf;
+        std::memcpy(&hf, &hb, 4);
+        const float l = w - hf;  // exact
+        cb_convert_weights_bf16(&l, 1, &h);
+      }
+      std::memcpy(img + at, &h, 2);
+    }
   };
+  const int xrow = 32 * eb, arow = 16 * eb;  // bytes of a 32- and a 16-channel row
+  const int w1_at = 0, w2_at = 2048, tap_bytes = bf ? 512 : 1024, w3_at = bf ? 7168 : 11264;
   for (int co = 0; co < 16; ++co)
-    for (int ci = 0; ci < 32; ++ci) put(0, 128, co, ci, w1[co * 32 + ci]);
+    for (int ci = 0; ci < 32; ++ci) {
+      put(w1_at, xrow, co, ci, w1[co * 32 + ci], false);
+      if (bf) put(1024, xrow, co, ci, w1[co * 32 + ci], true);
+    }
   for (int tap = 0; tap < 9; ++tap)
     for (int co = 0; co < 16; ++co)
-      for (int ci = 0; ci < 16; ++ci) put(2048 + 1024 * tap, 64, co, ci, w2[(co * 9 + tap) * 16 + ci]);
+      for (int ci = 0; ci < 16; ++ci) put(w2_at + tap_bytes * tap, arow, co, ci, w2[(co * 9 + tap) * 16 + ci], false);
   for (int co = 0; co < 32; ++co)
-    for (int ci = 0; ci < 32; ++ci) put(11264, 128, co, ci, w3[co * 32 + ci]);
+    for (int ci = 0; ci < 32; ++ci) {
+      put(w3_at, xrow, co, ci, w3[co * 32 + ci], false);
+      if (bf) put(9216, xrow, co, ci, w3[co * 32 + ci], true);
+    }
   for (int c = 0; c < 16; ++c) {
     a.sb[c] = s1[c], a.sb[16 + c] = b1[c];
     a.sb[32 + c] = s2[c], a.sb[48 + c] = b2[c];
@@ -1687,16 +1716,18 @@ static cb_status stage_body_tc(const cb_tensor* x1, const float* w1, const float
   stage_body_tc_boxes(&xw, &xh, &yw, &yh);
   cuuint64_t xdims[4] = {32, static_cast<cuuint64_t>(x1->w), static_cast<cuuint64_t>(x1->h),
                          static_cast<cuuint64_t>(x1->n)};
-  cuuint64_t xstr[3] = {static_cast<cuuint64_t>(x1->stride_w) * 4, static_cast<cuuint64_t>(x1->stride_h) * 4,
-                        static_cast<cuuint64_t>(x1->stride_n) * 4};
-  cuuint64_t ystr[3] = {static_cast<cuuint64_t>(y->stride_w) * 4, static_cast<cuuint64_t>(y->stride_h) * 4,
-                        static_cast<cuuint64_t>(y->stride_n) * 4};
+  cuuint64_t xstr[3] = {static_cast<cuuint64_t>(x1->stride_w) * eb, static_cast<cuuint64_t>(x1->stride_h) * eb,
+                        static_cast<cuuint64_t>(x1->stride_n) * eb};
+  cuuint64_t ystr[3] = {static_cast<cuuint64_t>(y->stride_w) * eb, static_cast<cuuint64_t>(y->stride_h) * eb,
+                        static_cast<cuuint64_t>(y->stride_n) * eb};
   cuuint32_t xbox[4] = {32, static_cast<cuuint32_t>(xw), static_cast<cuuint32_t>(xh), 1};
   cuuint32_t ybox[4] = {32, static_cast<cuuint32_t>(yw), static_cast<cuuint32_t>(yh), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUtensorMap xmap, ymap;
-  if (tiled_map(&xmap, 4, x1->data, xdims, xstr, xbox, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-      tiled_map(&ymap, 4, y->data, xdims, ystr, ybox, estr, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+  const CUtensorMapSwizzle swz = bf ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapDataType dt = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (tiled_map(&xmap, 4, x1->data, xdims, xstr, xbox, estr, swz, dt) != CUDA_SUCCESS ||
+      tiled_map(&ymap, 4, y->data, xdims, ystr, ybox, estr, swz, dt) != CUDA_SUCCESS)
     return CB_ERR_UNSUPPORTED;
   const cudaError_t e = launch_stage_body_tc(xmap, ymap, a, dev->sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CB_OK : cuda_fail(e);
@@ -1713,11 +1744,13 @@ cb_status cb_stage_body(const cb_tensor* x1, const float* w1, const float* s1, c
   if (overlap(x1, y)) return CB_ERR_INVALID_ARG;
   if ((x1->c != 16 && x1->c != 32) || x1->layout != CB_LAYOUT_NHWC || y->layout != CB_LAYOUT_NHWC)
     return CB_ERR_UNSUPPORTED;
-  if (x1->c == 32 && !is_f32(x1)) return CB_ERR_UNSUPPORTED;
   // x1 pixels in whole 16-byte pieces (the copy's strides), y in pieces of 4 channels
   const long long xm = is_f32(x1) ? 4 : 8;
   if (!aligned16(x1->data) || !aligned16(y->data) || x1->stride_w % xm != 0 || x1->stride_h % xm != 0 ||
       x1->stride_n % xm != 0 || !strides_mult4(y))
+    return CB_ERR_ALIGNMENT;
+  // the 32-channel kernel writes y by tensor stores: strides in whole 16-byte pieces
+  if (x1->c == 32 && (y->stride_w % xm != 0 || y->stride_h % xm != 0 || y->stride_n % xm != 0))
     return CB_ERR_ALIGNMENT;
   if (x1->n == 0) return CB_OK;
   if (x1->n > 65535 || x1->h > 65535 || x1->w > 65535 || !encode_tiled()) return CB_ERR_UNSUPPORTED;

@@ -253,23 +253,28 @@ void stage_body_box(int* box_c, int* box_w, int* box_h);
 cudaError_t launch_stage_body(const CUtensorMap& xmap, const StageBodyArgs& a, int sms, cudaStream_t s);
 
 // The same body for C = 32 channels (h = 16) on the tensor cores
-// (stage_body_tc.cu), fp32 storage, TF32 operands.  wimg is the weights'
-// shared-memory image, TF32-rounded: the B operands as K-major rows with the
-// tensor core's swizzle (16-byte piece q of row r at q ^ (r % 8) for 128-byte
-// rows, q ^ (r / 2 % 4) for 64-byte rows): w1 [16 co][32 ci] (128-byte rows)
-// at byte 0, w2 per tap kh * 3 + kw [16 co][16 ci] (64-byte rows) at 2048 +
-// 1024 * tap, w3 [32 co][32 ci of a | b] (128-byte rows) at 11264.  The
-// caller encodes xmap (x1 as (C = 32, W, H, N), 128-byte swizzle, box
-// 32 x x_box_w x x_box_h x 1) and ymap (y likewise, box 32 x y_box_w x
-// y_box_h x 1) with the sizes stage_body_tc_boxes gives.
+// (stage_body_tc.cu): fp32 storage with TF32 operands, or bf16 storage with
+// bf16 operands.  wimg is the weights' shared-memory image: the B operands as
+// K-major rows with the tensor core's swizzle (16-byte piece q of row r at
+// q ^ (r % 8) for 128-byte rows, q ^ (r / 2 % 4) for 64-byte rows,
+// q ^ (r / 4 % 2) for 32-byte rows).  fp32 (TF32-rounded): w1 [16 co][32 ci]
+// (128-byte rows) at byte 0, w2 per tap kh * 3 + kw [16 co][16 ci] (64-byte
+// rows) at 2048 + 1024 * tap, w3 [32 co][32 ci of a | b] (128-byte rows) at
+// 11264.  bf16 (nearest even; 64-byte rows for w1 and w3, 32-byte for w2):
+// w1 at 0 and its tail bf16(w1 - bf16(w1)) at 1024, w2 at 2048 + 512 * tap,
+// w3 at 7168 and its tail at 9216.  The caller encodes xmap (x1
+// as (C = 32, W, H, N) of the storage type, the swizzle of its rows: 128
+// bytes fp32, 64 bf16; box 32 x x_box_w x x_box_h x 1) and ymap (y likewise,
+// box 32 x y_box_w x y_box_h x 1) with the sizes stage_body_tc_boxes gives.
 constexpr int kStageTcWImgWords = (2048 + 9 * 1024 + 4096) / 4;
 struct StageBodyTcArgs {
-  const float* x;  // x1, for the residual
+  const void* x;  // x1, for the residual (fp32 or bf16)
   long long xs_n, xs_h, xs_w;
   int N, H, W;
   int act;
   int* err;  // device error word, bound of the kernel's waits
   uint64_t timeout_ns;
+  int bf16;          // x1, y and the weights' image hold bfloat16
   int debug_skip_x;  // 1: fault injection for tests of the bounded waits (no warpgroup issues its first x1 copy)
   uint32_t wimg[kStageTcWImgWords];
   float sb[2 * (16 + 16 + 32)];  // s1[16] b1[16] s2[16] b2[16] s3[32] b3[32]

@@ -51,6 +51,8 @@
 #include "ptx.cuh"
 #include "tc_store.cuh"
 
+#include <cuda_bf16.h>
+
 namespace cb {
 
 namespace {
@@ -59,26 +61,59 @@ constexpr int kTW = 32, kTH = 4;                // output tile
 constexpr int kM = kTW * kTH;                   // 128: the MMA's M, a warpgroup's threads
 constexpr int kHW = kTW + 2, kHH = kTH + 2;     // the haloed tile
 constexpr int kHPx = kHW * kHH;                 // 204 haloed pixels
-constexpr int kWG = 3;                          // warpgroups per CTA
-constexpr int kThreads = kWG * kM;
-constexpr int kXBytes = 2 * kM * 128;           // the 1x1's two row blocks (rows past 204 never used)
 constexpr int kCopyRows = kHH * kTW;            // 192 rows per copy of a
-constexpr int kCopyBytes = kCopyRows * 64;      // 16 fp32 channels per row
-constexpr int kWGBytes = kXBytes + 3 * kCopyBytes;
-constexpr int kW1 = 0, kW2 = 2048, kW3 = 11264;  // the weights' image (StageBodyTcArgs::wimg)
-constexpr int kWBytes = kStageTcWImgWords * 4;
-constexpr int kBar = kWBytes + kWG * kWGBytes;  // per warpgroup: 3x3 / last 1x1, x1, first 1x1, two drains
-constexpr int kBarsPerWG = 5;
-constexpr int kSmemEnd = kBar + 8 * kBarsPerWG * kWG + 8;
-constexpr int kTmemCols = 256;                  // 80 per warpgroup: D1 (2 x 16), D2 (16), D3 (32)
-constexpr int kWGCols = 80;
-static_assert(kW3 + 32 * 128 == kWBytes, "weight image");
-static_assert(kXBytes >= kHPx * 128 && kXBytes % 1024 == 0 && kCopyBytes % 1024 == 0 && kWBytes % 1024 == 0,
-              "1024-byte swizzle atoms");
-static_assert(2 * kCopyBytes >= kM * 128, "the output tile fits over copies 0 and 1");
-static_assert(kWG * kWGCols <= kTmemCols, "TMEM split");
+constexpr int kBarsPerWG = 5;                   // per warpgroup: 3x3 / last 1x1, x1, first 1x1, two drains
 
-constexpr size_t smem_bytes() { return 1024 + kSmemEnd; }
+// Storage type T: fp32 (kind::tf32 MMAs, K = 8 per instruction) or bf16
+// (kind::f16 with bf16 operands, K = 16); either way an MMA consumes 32
+// bytes of each K-major row.  Rows: x1 32 channels, a and b 16, out 32.
+template <typename T>
+struct Cfg;
+// bf16: the two 1x1 layers' weights are split into a bf16 head and tail
+// (w1 = h + l at kW1 and kW1L, w3 likewise), two MMAs each, so that they act
+// with fp32 accuracy as in the fp32-weight layer kernels; the 3x3 multiplies
+// bf16 weights like the bf16 tensor-core layers, and a and b are bf16 as in
+// the layers' bf16 storage.
+template <>
+struct Cfg<float> {
+  static constexpr int kWG = 3;                              // warpgroups per CTA
+  static constexpr int kXRow = 128, kARow = 64, kOutRow = 128;  // bytes; swizzle = row bytes
+  static constexpr bool kSplitW = false;
+  static constexpr int kW1 = 0, kW1L = 0, kW2 = 2048, kTap = 1024, kW3 = 11264, kW3L = 0, kWBytes = 15360;
+  static constexpr int kTmemCols = 256;
+};
+template <>
+struct Cfg<__nv_bfloat16> {
+  static constexpr int kWG = 4;
+  static constexpr int kXRow = 64, kARow = 32, kOutRow = 64;
+  static constexpr bool kSplitW = true;
+  static constexpr int kW1 = 0, kW1L = 1024, kW2 = 2048, kTap = 512, kW3 = 7168, kW3L = 9216, kWBytes = 11264;
+  static constexpr int kTmemCols = 512;
+};
+
+template <typename T>
+struct Lay {
+  using C = Cfg<T>;
+  static constexpr int kWG = C::kWG;
+  static constexpr int kThreads = kWG * kM;
+  static constexpr int kKX = C::kXRow / 32, kKA = C::kARow / 32;  // MMA K steps over an x1 row / an a row
+  static constexpr int kXBytes = 2 * kM * C::kXRow;               // the 1x1's two row blocks (rows past 204 never used)
+  static constexpr int kCopyBytes = kCopyRows * C::kARow;
+  static constexpr int kWGBytes = kXBytes + 3 * kCopyBytes;
+  static constexpr int kBar = C::kWBytes + kWG * kWGBytes;
+  static constexpr int kSmemEnd = kBar + 8 * kBarsPerWG * kWG + 8;
+  static constexpr int kWGCols = 80;                              // D1 (2 x 16), D2 (16), D3 (32)
+  static_assert((C::kSplitW ? C::kW3L : C::kW3) + 32 * C::kXRow == C::kWBytes && C::kWBytes <= kStageTcWImgWords * 4,
+                "weight image");
+  static_assert(kXBytes % 1024 == 0 && kCopyBytes % 1024 == 0 && C::kWBytes % 1024 == 0, "1024-byte swizzle atoms");
+  static_assert(2 * kCopyBytes >= kM * C::kOutRow, "the output tile fits over copies 0 and 1");
+  static_assert(kWG * kWGCols <= C::kTmemCols, "TMEM split");
+};
+
+template <typename T>
+constexpr size_t smem_bytes() {
+  return 1024 + Lay<T>::kSmemEnd;
+}
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -137,29 +172,77 @@ __device__ __forceinline__ void tmem_wait_regs32(uint32_t (&r)[2][16]) {
   tmem_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[0][0]));
 }
 
-// 16 fp32 values as one 64-byte row of a 64-byte-swizzled operand (16-byte
-// piece q of row r at q ^ (r / 2 % 4)).
-__device__ __forceinline__ void store_row64(uint8_t* base, int r, const float (&v)[16]) {
+// A row of a or b (16 channels) in the copies' layout: fp32 as a 64-byte row
+// of a 64-byte-swizzled operand (16-byte piece q of row r at q ^ (r / 2 % 4)),
+// bf16 (nearest even) as a 32-byte row of a 32-byte-swizzled one (q ^ (r / 4 % 2)).
+__device__ __forceinline__ void store_arow(uint8_t* base, int r, const float (&v)[16], float) {
   uint8_t* row = base + r * 64;
   const int s = (r >> 1) & 3;
 #pragma unroll
   for (int q = 0; q < 4; ++q)
     *reinterpret_cast<float4*>(row + ((q ^ s) << 4)) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void store_arow(uint8_t* base, int r, const float (&v)[16], __nv_bfloat16) {
+  uint8_t* row = base + r * 32;
+  const int s = (r >> 2) & 1;
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    *reinterpret_cast<uint4*>(row + ((q ^ s) << 4)) =
+        make_uint4(bf16x2_rn(v[8 * q], v[8 * q + 1]), bf16x2_rn(v[8 * q + 2], v[8 * q + 3]),
+                   bf16x2_rn(v[8 * q + 4], v[8 * q + 5]), bf16x2_rn(v[8 * q + 6], v[8 * q + 7]));
+}
 
-template <int ACT>
-__global__ void __launch_bounds__(kThreads, 1)
+// The value an operand holds: TF32 (nearest, ties away) for fp32 storage; for
+// bf16 storage the rounding happens when the row is stored.
+__device__ __forceinline__ float operand_value(float x, float) { return tf32_rna(x); }
+__device__ __forceinline__ float operand_value(float x, __nv_bfloat16) { return x; }
+
+// Channels 8k .. 8k + 7 of the residual pixel at p (fp32 or bf16).
+__device__ __forceinline__ void load8(const float* p, int k, float (&r)[8]) {
+  const float4 u = reinterpret_cast<const float4*>(p)[2 * k], v = reinterpret_cast<const float4*>(p)[2 * k + 1];
+  r[0] = u.x, r[1] = u.y, r[2] = u.z, r[3] = u.w, r[4] = v.x, r[5] = v.y, r[6] = v.z, r[7] = v.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, int k, float (&r)[8]) {
+  const uint4 u = reinterpret_cast<const uint4*>(p)[k];
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r[2 * i] = __uint_as_float(w[i] << 16), r[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+}
+
+// Output channels 8k .. 8k + 7 of tile pixel t into the staging tile (the
+// tensor store's box): fp32 128-byte rows, 128-byte swizzle (piece q of row
+// t at q ^ (t % 8)), two pieces; bf16 64-byte rows, 64-byte swizzle, one.
+__device__ __forceinline__ void stage8(uint8_t* tile, int t, int k, const float (&o)[8], float) {
+  uint8_t* row = tile + t * 128;
+  *reinterpret_cast<float4*>(row + (((2 * k) ^ (t & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<float4*>(row + (((2 * k + 1) ^ (t & 7)) << 4)) = make_float4(o[4], o[5], o[6], o[7]);
+}
+__device__ __forceinline__ void stage8(uint8_t* tile, int t, int k, const float (&o)[8], __nv_bfloat16) {
+  uint8_t* row = tile + t * 64;
+  *reinterpret_cast<uint4*>(row + ((k ^ ((t >> 1) & 3)) << 4)) =
+      make_uint4(bf16x2_rn(o[0], o[1]), bf16x2_rn(o[2], o[3]), bf16x2_rn(o[4], o[5]), bf16x2_rn(o[6], o[7]));
+}
+
+template <int ACT, typename T>
+__global__ void __launch_bounds__(Lay<T>::kThreads, 1)
     stage_body_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
                          const __grid_constant__ StageBodyTcArgs a, int tiles_x, int tiles_y) {
+  using C = Cfg<T>;
+  using L = Lay<T>;
+  constexpr int kWG = L::kWG;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* const smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int g = threadIdx.x / kM;  // warpgroup
   const int t = threadIdx.x % kM;  // its thread: output pixel t of the tile, TMEM lane t
   const int warp = threadIdx.x >> 5;
-  uint8_t* const xs = smem + kWBytes + g * kWGBytes;  // haloed x1
-  uint8_t* const cp0 = xs + kXBytes;                   // copies of a (dx = 0, 1, 2); b over copy 0
-  uint64_t* const bars = reinterpret_cast<uint64_t*>(smem + kBar);
+  uint8_t* const xs = smem + C::kWBytes + g * L::kWGBytes;  // haloed x1
+  uint8_t* const cp0 = xs + L::kXBytes;                      // copies of a (dx = 0, 1, 2); b over copy 0
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* const mbar = bars + kBarsPerWG * g;  // this warpgroup's 3x3 and last 1x1 completions
   uint64_t* const xfull = mbar + 1;              // its x1 copies
   uint64_t* const d1bar = mbar + 2;              // its first 1x1 completions
@@ -183,11 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&ymap);
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, C::kTmemCols);
     tmem_relinquish();
   }
-  // the weights' image (TF32, swizzled on the host) from the parameter block
-  for (int i = threadIdx.x; i < kStageTcWImgWords / 4; i += kThreads)
+  // the weights' image (TF32 or bf16, swizzled on the host) from the parameter block
+  for (int i = threadIdx.x; i < C::kWBytes / 16; i += L::kThreads)
     reinterpret_cast<uint4*>(smem)[i] = make_uint4(a.wimg[4 * i], a.wimg[4 * i + 1], a.wimg[4 * i + 2], a.wimg[4 * i + 3]);
   fence_proxy_async_smem();  // read by the tensor core
   tc_fence_before_sync();
@@ -196,23 +279,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
   pdl_wait();
 
-  const uint32_t tmem = *tmem_slot + static_cast<uint32_t>(g * kWGCols);
+  const uint32_t tmem = *tmem_slot + static_cast<uint32_t>(g * L::kWGCols);
   const uint32_t tlane = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const Watchdog wd{a.err, abort_flag, a.timeout_ns};
-  const uint64_t dx1[2] = {kmajor_swizzled_desc(smem_u32(xs), 128), kmajor_swizzled_desc(smem_u32(xs + 128 * 128), 128)};
-  const uint64_t dw1 = kmajor_swizzled_desc(smem_u32(smem + kW1), 128);
-  const uint64_t dw2 = kmajor_swizzled_desc(smem_u32(smem + kW2), 64);
-  const uint64_t dw3 = kmajor_swizzled_desc(smem_u32(smem + kW3), 128);
-  const uint64_t dcp = kmajor_swizzled_desc(smem_u32(cp0), 64);
-  constexpr uint32_t kCopyStep = kCopyBytes >> 4, kDyStep = (kTW * 64) >> 4, kTapStep = 1024 >> 4;
-  constexpr uint32_t id16 = idesc_tf32(kM, 16), id32 = idesc_tf32(kM, 32);
+  const uint64_t dx1[2] = {kmajor_swizzled_desc(smem_u32(xs), C::kXRow),
+                           kmajor_swizzled_desc(smem_u32(xs + kM * C::kXRow), C::kXRow)};
+  const uint64_t dw1 = kmajor_swizzled_desc(smem_u32(smem + C::kW1), C::kXRow);
+  const uint64_t dw1l = kmajor_swizzled_desc(smem_u32(smem + C::kW1L), C::kXRow);  // (bf16: the tails)
+  const uint64_t dw3l = kmajor_swizzled_desc(smem_u32(smem + C::kW3L), C::kXRow);
+  const uint64_t dw2 = kmajor_swizzled_desc(smem_u32(smem + C::kW2), C::kARow);
+  const uint64_t dw3 = kmajor_swizzled_desc(smem_u32(smem + C::kW3), C::kXRow);
+  const uint64_t dcp = kmajor_swizzled_desc(smem_u32(cp0), C::kARow);
+  constexpr uint32_t kCopyStep = L::kCopyBytes >> 4, kDyStep = (kTW * C::kARow) >> 4, kTapStep = C::kTap >> 4;
+  constexpr uint32_t id16 = idesc_for<T>(kM, 16), id32 = idesc_for<T>(kM, 32);
+  constexpr int kKX = L::kKX, kKA = L::kKA;
 
   const int num_tiles = a.N * tiles_y * tiles_x;
   const int workers = static_cast<int>(gridDim.x) * kWG;
   const int first = g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
   auto issue_x = [&](int tile) {  // the x1 thread: tile's haloed x1
     const int tx = tile % tiles_x, rest = tile / tiles_x, ty = rest % tiles_y, n = rest / tiles_y;
-    mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(kHPx * 128));
+    mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(kHPx * C::kXRow));
     tma_load_4d(xs, &xmap, xfull, 0, tx * kTW - 1, ty * kTH - 1, n);
   };
   // bookkeeping of the two issuing threads: copies issued / waited for (x1
@@ -236,7 +323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) mma_tf32(tmem + 16 * m, dx1[m] + 2 * j, dw1 + 2 * j, id16, j > 0 ? 1u : 0u);
+      for (int j = 0; j < kKX; ++j) {
+        if constexpr (C::kSplitW) mma_op<T>(tmem + 16 * m, dx1[m] + 2 * j, dw1l + 2 * j, id16, j > 0 ? 1u : 0u);
+        mma_op<T>(tmem + 16 * m, dx1[m] + 2 * j, dw1 + 2 * j, id16, (C::kSplitW || j > 0) ? 1u : 0u);
+      }
     mma_commit(d1bar);
     issued_mma = true;
     return true;
@@ -290,11 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           o[i] = __uint_as_float(
-              __float_as_uint(tf32_rna(act_t<ACT>(fmaf(__uint_as_float(v[i]), a.sb[i], a.sb[16 + i])))) & keep);
+              __float_as_uint(operand_value(act_t<ACT>(fmaf(__uint_as_float(v[i]), a.sb[i], a.sb[16 + i])), T{})) &
+              keep);
 #pragma unroll
         for (int dx = 0; dx < 3; ++dx) {
           const int c = hx - dx;
-          if (c >= 0 && c < kTW) store_row64(cp0 + dx * kCopyBytes, hy * kTW + c, o);
+          if (c >= 0 && c < kTW) store_arow(cp0 + dx * L::kCopyBytes, hy * kTW + c, o, T{});
         }
       }
     }
@@ -309,12 +400,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // barrier after them waits for the loads too
     const int oh = ty * kTH + t / kTW, ow = tx * kTW + t % kTW;
     const bool in = oh < a.H && ow < a.W;
-    float4 r[8];
+    float r[4][8];
     {
-      const float4* rp =
-          reinterpret_cast<const float4*>(a.x + n * a.xs_n + (in ? oh : 0) * a.xs_h + (in ? ow : 0) * a.xs_w);
+      const T* rp = static_cast<const T*>(a.x) + n * a.xs_n + (in ? oh : 0) * a.xs_h + (in ? ow : 0) * a.xs_w;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) r[q] = in ? rp[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < 4; ++k) {
+        if (in) {
+          load8(rp, k, r[k]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) r[k][i] = 0.0f;
+        }
+      }
     }
     if (leader) {
       tc_fence_after_sync();
@@ -323,9 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int dx = 0; dx < 3; ++dx)
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            mma_tf32(tmem + 32, dcp + dx * kCopyStep + dy * kDyStep + 2 * j, dw2 + (dy * 3 + dx) * kTapStep + 2 * j,
-                     id16, (dy | dx | j) != 0 ? 1u : 0u);
+          for (int j = 0; j < kKA; ++j)
+            mma_op<T>(tmem + 32, dcp + dx * kCopyStep + dy * kDyStep + 2 * j, dw2 + (dy * 3 + dx) * kTapStep + 2 * j,
+                      id16, (dy | dx | j) != 0 ? 1u : 0u);
       issued_mma = true;
       ok = mma_wait();
     }
@@ -342,8 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_regs(v);
       float o[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) o[i] = tf32_rna(act_t<ACT>(fmaf(__uint_as_float(v[i]), a.sb[32 + i], a.sb[48 + i])));
-      store_row64(cp0, t, o);  // b over copy 0
+      for (int i = 0; i < 16; ++i)
+        o[i] = operand_value(act_t<ACT>(fmaf(__uint_as_float(v[i]), a.sb[32 + i], a.sb[48 + i])), T{});
+      store_arow(cp0, t, o, T{});  // b over copy 0
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
@@ -353,10 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (leader) {
       tc_fence_after_sync();
 #pragma unroll
-      for (int j = 0; j < 2; ++j)  // a: the centre of copy 1 (haloed row hy = r + 1, column c + 1)
-        mma_tf32(tmem + 48, dcp + kCopyStep + kDyStep + 2 * j, dw3 + 2 * j, id32, j > 0 ? 1u : 0u);
+      for (int j = 0; j < kKA; ++j) {  // a: the centre of copy 1 (haloed row hy = r + 1, column c + 1)
+        if constexpr (C::kSplitW) mma_op<T>(tmem + 48, dcp + kCopyStep + kDyStep + 2 * j, dw3l + 2 * j, id32, j > 0 ? 1u : 0u);
+        mma_op<T>(tmem + 48, dcp + kCopyStep + kDyStep + 2 * j, dw3 + 2 * j, id32, (C::kSplitW || j > 0) ? 1u : 0u);
+      }
 #pragma unroll
-      for (int j = 0; j < 2; ++j) mma_tf32(tmem + 48, dcp + 2 * j, dw3 + 4 + 2 * j, id32, 1u);  // b
+      for (int j = 0; j < kKA; ++j) {  // b
+        if constexpr (C::kSplitW) mma_op<T>(tmem + 48, dcp + 2 * j, dw3l + 2 * kKA + 2 * j, id32, 1u);
+        mma_op<T>(tmem + 48, dcp + 2 * j, dw3 + 2 * kKA + 2 * j, id32, 1u);
+      }
       ok = mma_wait();
     }
     __syncwarp();
@@ -367,17 +470,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_x16(tmem + tlane + 48, v2[0]);
       tmem_ld_x16(tmem + tlane + 64, v2[1]);
       tmem_wait_regs32(v2);
-      uint8_t* const row = cp0 + t * 128;  // the output tile: 128-byte swizzled rows over copies 0 and 1
+      // the output tile, in the tensor store's box over copies 0 and 1
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {  // channels 4q .. 4q + 3
-        const float rr[4] = {r[q].x, r[q].y, r[q].z, r[q].w};
-        float o[4];
+      for (int k = 0; k < 4; ++k) {  // channels 8k .. 8k + 7
+        float o[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int k = 4 * q + i;
-          o[i] = tf32_rna(act_t<ACT>(fmaf(__uint_as_float(v2[q >> 2][k & 15]), a.sb[64 + k], a.sb[96 + k])) + rr[i]);
+        for (int i = 0; i < 8; ++i) {
+          const int c = 8 * k + i;
+          o[i] = operand_value(
+              act_t<ACT>(fmaf(__uint_as_float(v2[c >> 4][c & 15]), a.sb[64 + c], a.sb[96 + c])) + r[k][i], T{});
         }
-        *reinterpret_cast<float4*>(row + ((q ^ (t & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
+        stage8(cp0, t, k, o, T{});
       }
     }
     fence_proxy_async_smem();
@@ -403,22 +506,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after_sync();
-    tmem_dealloc(*tmem_slot, kTmemCols);
+    tmem_dealloc(*tmem_slot, C::kTmemCols);
   }
 }
 
-template <int ACT>
+template <int ACT, typename T>
 cudaError_t launch_t(const CUtensorMap& xmap, const CUtensorMap& ymap, const StageBodyTcArgs& a, int sms,
                      cudaStream_t s) {
-  constexpr size_t smem = smem_bytes();
-  cudaError_t e = smem_attr_once<stage_body_tc_kernel<ACT>>(smem);
+  constexpr size_t smem = smem_bytes<T>();
+  constexpr int kWG = Lay<T>::kWG;
+  cudaError_t e = smem_attr_once<stage_body_tc_kernel<ACT, T>>(smem);
   if (e != cudaSuccess) return e;
   const int tiles_x = (a.W + kTW - 1) / kTW, tiles_y = (a.H + kTH - 1) / kTH;
   const long long tiles = static_cast<long long>(a.N) * tiles_x * tiles_y;
   if (tiles >= (1LL << 31) - static_cast<long long>(sms) * kWG) return cudaErrorInvalidValue;
   const long long ctas = (tiles + kWG - 1) / kWG;
   const unsigned grid = static_cast<unsigned>(ctas < sms ? ctas : sms);
-  return launch_pdl(stage_body_tc_kernel<ACT>, dim3(grid), dim3(kThreads), smem, s, xmap, ymap, a, tiles_x, tiles_y);
+  return launch_pdl(stage_body_tc_kernel<ACT, T>, dim3(grid), dim3(Lay<T>::kThreads), smem, s, xmap, ymap, a, tiles_x,
+                    tiles_y);
+}
+
+template <typename T>
+cudaError_t launch_type(const CUtensorMap& xmap, const CUtensorMap& ymap, const StageBodyTcArgs& a, int sms,
+                        cudaStream_t s) {
+  if (a.act == 0) return launch_t<0, T>(xmap, ymap, a, sms, s);
+  if (a.act == 1) return launch_t<1, T>(xmap, ymap, a, sms, s);
+  return launch_t<2, T>(xmap, ymap, a, sms, s);
 }
 
 }  // namespace
@@ -433,9 +546,7 @@ void stage_body_tc_boxes(int* x_box_w, int* x_box_h, int* y_box_w, int* y_box_h)
 cudaError_t launch_stage_body_tc(const CUtensorMap& xmap, const CUtensorMap& ymap, const StageBodyTcArgs& a, int sms,
                                  cudaStream_t s) {
   if (a.N == 0 || a.H == 0 || a.W == 0) return cudaSuccess;
-  if (a.act == 0) return launch_t<0>(xmap, ymap, a, sms, s);
-  if (a.act == 1) return launch_t<1>(xmap, ymap, a, sms, s);
-  return launch_t<2>(xmap, ymap, a, sms, s);
+  return a.bf16 ? launch_type<__nv_bfloat16>(xmap, ymap, a, sms, s) : launch_type<float>(xmap, ymap, a, sms, s);
 }
 
 }  // namespace cb

@@ -136,9 +136,8 @@ class MnistNet:
 class YoloChain:
     """dtype: the activations' storage type (torch.float32, or torch.bfloat16: every layer then
     reads and writes bf16, the tensor-core layers multiply bf16 weights).  fuse_body: a stage with
-    16 channels (fp32 or bf16) or 32 channels (fp32) runs its body (cv1, cv2, cv3 with the concat
-    and the residual) as one kernel (cb_stage_body), so that a and b never reach memory;
-    self.fused[i] says which stages do."""
+    16 or 32 channels runs its body (cv1, cv2, cv3 with the concat and the residual) as one kernel
+    (cb_stage_body), so that a and b never reach memory; self.fused[i] says which stages do."""
 
     def __init__(self, stages, batch, size=640, device="cuda", dtype=torch.float32, fuse_body=True):
         self.batch = batch
@@ -163,7 +162,7 @@ class YoloChain:
                  "out": torch.empty(batch, OH, OH, c, device=device, dtype=dtype), "half": h}
             self.layers.append(L)
             self.bufs.append(B)
-            self.fused.append(fuse_body and (c == 16 or (c == 32 and dtype == torch.float32)))
+            self.fused.append(fuse_body and c in (16, 32))
             H = OH
 
     def body(self, i, stream=None, tune=False):

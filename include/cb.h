@@ -245,7 +245,8 @@ int cb_dw_separable_block_fused(const cb_tensor* x, const cb_tensor* y, const fl
  * on the SM instead of going through HBM.
  *  x1, y: NHWC views of N x H x W x C, the same dtype; 16-byte aligned data,
  *         x1 strides multiples of 4 (fp32) or 8 (bf16) elements, y strides
- *         multiples of 4; y must not overlap x1.
+ *         multiples of 4 (C = 16) or, as x1's, whole 16-byte pieces (C = 32);
+ *         y must not overlap x1.
  *  w1, w2, w3: HOST fp32 weights, OHWI: [h][1][1][C], [h][3][3][h],
  *         [C][1][1][C] (input channels of w3: a's h, then b's h).
  *  s1/b1 (h), s2/b2 (h), s3/b3 (C): HOST fp32 folded BN (cb_fold_bn).
@@ -258,13 +259,15 @@ int cb_dw_separable_block_fused(const cb_tensor* x, const cb_tensor* y, const fl
  *         which costs the kernel no load instructions), fp32 or bf16 storage
  *         (bf16: x1 read and y written as bf16, every product and sum in
  *         fp32); held to the fp32 bar against the three layers' definition.
- * C = 32: on the tensor cores (kind::tf32 MMAs, fp32 accumulate), fp32
- *         storage: the precision of the tensor-core layers (weights rounded
+ * C = 32: on the tensor cores, fp32 accumulate, the precision of the
+ *         tensor-core layers.  fp32 storage: kind::tf32 MMAs, weights rounded
  *         to the nearest TF32 value, a, b and y rounded to the nearest TF32
- *         value when formed); held to the TF32 bar.
+ *         value when formed; held to the TF32 bar.  bf16 storage: kind::f16
+ *         MMAs on bf16 operands (weights, x1, a and b rounded to bf16,
+ *         nearest even), y rounded to bf16; held to the bf16 bar.
  * Returns CB_ERR_INVALID_ARG for NULL arguments, mismatched shapes or dtypes
- * and overlapping views, CB_ERR_UNSUPPORTED for other C, NCHW views or bf16
- * with C = 32, CB_ERR_ALIGNMENT for the alignment rules above; asynchronous
+ * and overlapping views, CB_ERR_UNSUPPORTED for other C or NCHW views,
+ * CB_ERR_ALIGNMENT for the alignment rules above; asynchronous
  * on `stream`.  The kernels' waits are bounded (CB_ERR_TIMEOUT through
  * cb_get_device_error).
  */

@@ -72,6 +72,22 @@ def stage_body_tol(c):
     return TOL_FP32 if c == 16 else TOL_TF32
 
 
+def to_bf16_values(a):
+    """The bf16 values (nearest even) of an array, as float32."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def oracle_stage_body_bf16_storage(orc, x1, st, act=2):
+    """The stage body as its three layers compute it with bf16 storage: the oracle's layers composed,
+    with a and b rounded to bf16 where the layers store them and the 3x3's weights rounded to bf16
+    as the bf16 tensor-core layer multiplies them (the 1x1 layers multiply fp32 weights)."""
+    a = to_bf16_values(orc.conv_bn_act(x1, st["cv1_w"], st["cv1_bn"], stride=1, pad=0, act=act))
+    b = to_bf16_values(orc.conv_bn_act(a, to_bf16_values(st["cv2_w"]), st["cv2_bn"], stride=1, pad=1, act=act))
+    cat = np.ascontiguousarray(np.concatenate([a, b], axis=-1))
+    return orc.conv_bn_act(cat, st["cv3_w"], st["cv3_bn"], stride=1, pad=0, act=act, residual=x1,
+                           res_mode=orc.RES_POST_ACT)
+
+
 def oracle_stage_body(orc, x1, st, act=2):
     """The oracle's YOLO-style stage body from its stride-2 output x1 (NHWC): cv1 (1x1), cv2 (3x3,
     pad 1) on cv1's output, cv3 (1x1) on the concat [a | b] with x1 added after the activation --

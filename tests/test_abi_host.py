@@ -190,12 +190,13 @@ def test_stage_body_validated_before_launch(cblib):
     odd.stride_w, odd.stride_h, odd.stride_n = 18, 18 * 32, 18 * 32 * 16                  # pixels 72 bytes apart
     assert call(odd, y) == cblib.ERR_ALIGNMENT
     assert call(_view(base, 0, 16, 32, 16), _view(base + (1 << 22), 0, 16, 32, 16)) == cblib.OK  # empty batch
-    # 32 channels (the tensor-core body): fp32 only, the same alignment rules
+    # 32 channels (the tensor-core body): y strides in whole 16-byte pieces (its tensor stores)
     x32, y32 = _view(base, 2, 16, 32, 32), _view(base + (1 << 22), 2, 16, 32, 32)
     assert call(_view(base, 2, 16, 32, 24), _view(base + (1 << 22), 2, 16, 32, 24)) == cblib.ERR_UNSUPPORTED
     xb, yb = _view(base, 2, 16, 32, 32), _view(base + (1 << 22), 2, 16, 32, 32)
     xb.dtype = yb.dtype = cblib.DTYPE_BF16
-    assert call(xb, yb) == cblib.ERR_UNSUPPORTED
+    yb.stride_w, yb.stride_h, yb.stride_n = 36, 36 * 32, 36 * 32 * 16                   # bf16 y pixels 72 bytes apart
+    assert call(xb, yb) == cblib.ERR_ALIGNMENT
     odd32 = _view(base + (1 << 22), 2, 16, 32, 32)
     odd32.stride_w, odd32.stride_h, odd32.stride_n = 34, 34 * 32, 34 * 32 * 16              # y pixels 136 bytes apart
     assert call(x32, odd32) == cblib.ERR_ALIGNMENT

@@ -15,7 +15,12 @@ C = 32 (stage 1) runs on the tensor cores with TF32 operands, the precision of t
 layers: the bar is the TF32 one (5e-3 of max|oracle|), every output is a TF32 value (the low 13
 mantissa bits clear), and the shapes add one with more tiles than the grid has warpgroups, so that
 each warpgroup walks several tiles (the next tile's copy issued early, the output store of one tile
-in flight while the next is computed).
+in flight while the next is computed).  With bf16 storage it stores a and b as bf16 (nearest even),
+as the three layers store them, multiplies the 3x3's weights as bf16 like the bf16 tensor-core
+layer, and the 1x1 layers' weights split into a bf16 head and tail (fp32 accuracy, as the CUDA-core
+1x1 layers): held to the bf16 bar (5e-3 of max|oracle|) against the oracle composed with the same
+storage (a, b and the 3x3's weights rounded to bf16), and to twice that against the oracle without
+it (measured: bf16 storage of a and b alone moves the output by up to 3.6e-3).
 """
 import numpy as np
 import pytest
@@ -23,8 +28,8 @@ import torch
 
 from conv_bn_activation_gb300 import binding as cb, synthetic
 from conv_bn_activation_gb300.nets import ConvBnAct
-from gpu_util import TOL_FP32, TOL_TF32, bf16_within_half_ulp, canary_buffer, canary_buffer_bf16, is_canary, \
-    is_canary_bf16, oracle_stage_body, rel_err, sync_check, to_dev, to_dev_bf16
+from gpu_util import TOL_BF16, TOL_FP32, TOL_TF32, bf16_within_half_ulp, canary_buffer, canary_buffer_bf16, is_canary, \
+    is_canary_bf16, oracle_stage_body, oracle_stage_body_bf16_storage, rel_err, sync_check, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -248,10 +253,10 @@ def test_stage_body_c32_full_size_stage1(gpu, orc):
 
 def test_stage_body_c32_rejects(gpu):
     layers = _layers(_stage(2, C=32), cb.ACT_SILU)
-    with pytest.raises(cb.CbError) as e:  # bf16 storage: no 32-channel kernel
+    with pytest.raises(cb.CbError) as e:  # bf16 output pixels 36 elements (72 bytes) apart: no tensor store
         cb.stage_body(torch.zeros(1, 8, 8, 32, device=gpu, dtype=torch.bfloat16), layers, cb.ACT_SILU,
-                      torch.empty(1, 8, 8, 32, device=gpu, dtype=torch.bfloat16))
-    assert e.value.status == cb.ERR_UNSUPPORTED
+                      torch.empty(1, 8, 8, 36, device=gpu, dtype=torch.bfloat16)[..., :32])
+    assert e.value.status == cb.ERR_ALIGNMENT
     with pytest.raises(cb.CbError) as e:  # 24 channels: no kernel
         cb.stage_body(torch.zeros(1, 8, 8, 24, device=gpu), layers, cb.ACT_SILU, torch.empty(1, 8, 8, 24, device=gpu))
     assert e.value.status == cb.ERR_UNSUPPORTED
@@ -262,3 +267,37 @@ def test_stage_body_c32_rejects(gpu):
     with pytest.raises(cb.CbError) as e:  # output rows 34 floats apart: not whole 16-byte pieces
         cb.stage_body(x1, layers, cb.ACT_SILU, torch.empty(1, 8, 8, 34, device=gpu)[..., :32])
     assert e.value.status == cb.ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("shape", [(2, 20, 40), (1, 1, 1), (3, 17, 33), (1, 33, 95), (8, 102, 130)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_stage_body_c32_bf16(gpu, orc, shape):
+    """bf16 storage: x1 read and the output written as bfloat16 by the tensor-core body (bf16
+    operands, fp32 accumulate), against the oracle on the same bf16 x1; a channel slice of a wider
+    output buffer with canaries around it."""
+    N, H, W = shape
+    st = _stage(N * W + 5, C=32)
+    x1 = np.random.default_rng(H + 3).standard_normal((N, H, W, 32)).astype(np.float32)
+    xd, xv = to_dev_bf16(x1)
+    buf = canary_buffer_bf16((N, H, W, 48))
+    y = buf[..., 8:40]  # 16-byte aligned channel slice, pixels 96 bytes apart
+    cb.stage_body(xd, _layers(st, cb.ACT_SILU, dtype=torch.bfloat16), cb.ACT_SILU, y)
+    assert "stage_body_tc_kernel" in cb.last_launch()["kernel"]
+    sync_check()
+    got = y.float().cpu().numpy()
+    assert rel_err(got, oracle_stage_body_bf16_storage(orc, xv, st)) <= TOL_BF16
+    assert rel_err(got, oracle_stage_body(orc, xv, st)) <= 2 * TOL_BF16
+    assert is_canary_bf16(buf[..., :8]) and is_canary_bf16(buf[..., 40:])
+
+
+def test_stage_body_c32_bf16_full_size_stage1(gpu, orc):
+    """The bf16 chain's stage 1 body at its size (160 x 160, batch 32), every output."""
+    st = synthetic.yolo_params()[1]
+    x1 = np.random.default_rng(9).standard_normal((32, 160, 160, 32)).astype(np.float32)
+    xd, xv = to_dev_bf16(x1)
+    y = torch.empty(32, 160, 160, 32, device=gpu, dtype=torch.bfloat16)
+    cb.stage_body(xd, _layers(st, cb.ACT_SILU, dtype=torch.bfloat16), cb.ACT_SILU, y)
+    sync_check()
+    got = y.float().cpu().numpy()
+    assert rel_err(got, oracle_stage_body_bf16_storage(orc, xv, st)) <= TOL_BF16
+    assert rel_err(got, oracle_stage_body(orc, xv, st)) <= 2 * TOL_BF16
