@@ -605,6 +605,11 @@ class YoloBf16Workload(YoloWorkload):
     """The YOLO-style chain with bf16 storage."""
     bf16 = True
     tc_dtype = "bf16"
+    # the fp32 chain's summaries are of other kernel instances: only the bf16 ones apply
+    profiles = {
+        "s1.body": ("stage_body_tc_kernel_yolo_bf16_s1_body_b32.md",
+                    ["stage_body_tc.cu", "epilogue.cuh", "ptx.cuh", "tc_store.cuh", "launch_util.h", "internal.h"]),
+    }
 
 
 class PreprocessWorkload(Workload):

@@ -201,31 +201,20 @@ __device__ __forceinline__ void store_arow(uint8_t* base, int r, const float (&v
 __device__ __forceinline__ float operand_value(float x, float) { return tf32_rna(x); }
 __device__ __forceinline__ float operand_value(float x, __nv_bfloat16) { return x; }
 
-// Channels 8k .. 8k + 7 of the residual pixel at p (fp32 or bf16).
-__device__ __forceinline__ void load8(const float* p, int k, float (&r)[8]) {
-  const float4 u = reinterpret_cast<const float4*>(p)[2 * k], v = reinterpret_cast<const float4*>(p)[2 * k + 1];
-  r[0] = u.x, r[1] = u.y, r[2] = u.z, r[3] = u.w, r[4] = v.x, r[5] = v.y, r[6] = v.z, r[7] = v.w;
-}
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, int k, float (&r)[8]) {
-  const uint4 u = reinterpret_cast<const uint4*>(p)[k];
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) r[2 * i] = __uint_as_float(w[i] << 16), r[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-}
-
-// Output channels 8k .. 8k + 7 of tile pixel t into the staging tile (the
-// tensor store's box): fp32 128-byte rows, 128-byte swizzle (piece q of row
-// t at q ^ (t % 8)), two pieces; bf16 64-byte rows, 64-byte swizzle, one.
-__device__ __forceinline__ void stage8(uint8_t* tile, int t, int k, const float (&o)[8], float) {
-  uint8_t* row = tile + t * 128;
-  *reinterpret_cast<float4*>(row + (((2 * k) ^ (t & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
-  *reinterpret_cast<float4*>(row + (((2 * k + 1) ^ (t & 7)) << 4)) = make_float4(o[4], o[5], o[6], o[7]);
-}
-__device__ __forceinline__ void stage8(uint8_t* tile, int t, int k, const float (&o)[8], __nv_bfloat16) {
-  uint8_t* row = tile + t * 64;
-  *reinterpret_cast<uint4*>(row + ((k ^ ((t >> 1) & 3)) << 4)) =
-      make_uint4(bf16x2_rn(o[0], o[1]), bf16x2_rn(o[2], o[3]), bf16x2_rn(o[4], o[5]), bf16x2_rn(o[6], o[7]));
-}
+// The residual pixel as 16-byte pieces (fp32: 8 of 4 channels, bf16: 4 of 8),
+// unpacked in the last epilogue.
+template <typename T>
+struct Res {
+  using V = float4;
+  static constexpr int kN = 8;
+  __device__ static V zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+};
+template <>
+struct Res<__nv_bfloat16> {
+  using V = uint4;
+  static constexpr int kN = 4;
+  __device__ static V zero() { return make_uint4(0u, 0u, 0u, 0u); }
+};
 
 template <int ACT, typename T>
 __global__ void __launch_bounds__(Lay<T>::kThreads, 1)
@@ -400,18 +389,13 @@ __global__ void __launch_bounds__(Lay<T>::kThreads, 1)
     // barrier after them waits for the loads too
     const int oh = ty * kTH + t / kTW, ow = tx * kTW + t % kTW;
     const bool in = oh < a.H && ow < a.W;
-    float r[4][8];
+    using RV = typename Res<T>::V;
+    RV r[Res<T>::kN];
     {
-      const T* rp = static_cast<const T*>(a.x) + n * a.xs_n + (in ? oh : 0) * a.xs_h + (in ? ow : 0) * a.xs_w;
+      const RV* rp = reinterpret_cast<const RV*>(static_cast<const T*>(a.x) + n * a.xs_n + (in ? oh : 0) * a.xs_h +
+                                                 (in ? ow : 0) * a.xs_w);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (in) {
-          load8(rp, k, r[k]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) r[k][i] = 0.0f;
-        }
-      }
+      for (int q = 0; q < Res<T>::kN; ++q) r[q] = in ? rp[q] : Res<T>::zero();
     }
     if (leader) {
       tc_fence_after_sync();
@@ -470,17 +454,37 @@ __global__ void __launch_bounds__(Lay<T>::kThreads, 1)
       tmem_ld_x16(tmem + tlane + 48, v2[0]);
       tmem_ld_x16(tmem + tlane + 64, v2[1]);
       tmem_wait_regs32(v2);
-      // the output tile, in the tensor store's box over copies 0 and 1
+      // the output tile, in the tensor store's box over copies 0 and 1: fp32
+      // 128-byte rows with the 128-byte swizzle (piece q of row t at q ^ (t % 8)),
+      // bf16 64-byte rows with the 64-byte swizzle (q ^ (t / 2 % 4))
+      if constexpr (sizeof(T) == 4) {
+        uint8_t* const row = cp0 + t * 128;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {  // channels 8k .. 8k + 7
-        float o[8];
+        for (int q = 0; q < 8; ++q) {  // channels 4q .. 4q + 3
+          const float rr[4] = {r[q].x, r[q].y, r[q].z, r[q].w};
+          float o[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = 8 * k + i;
-          o[i] = operand_value(
-              act_t<ACT>(fmaf(__uint_as_float(v2[c >> 4][c & 15]), a.sb[64 + c], a.sb[96 + c])) + r[k][i], T{});
+          for (int i = 0; i < 4; ++i) {
+            const int c = 4 * q + i;
+            o[i] = tf32_rna(act_t<ACT>(fmaf(__uint_as_float(v2[q >> 2][c & 15]), a.sb[64 + c], a.sb[96 + c])) + rr[i]);
+          }
+          *reinterpret_cast<float4*>(row + ((q ^ (t & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
         }
-        stage8(cp0, t, k, o, T{});
+      } else {
+        uint8_t* const row = cp0 + t * 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // channels 8q .. 8q + 7
+          const uint32_t w[4] = {r[q].x, r[q].y, r[q].z, r[q].w};
+          float o[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c = 8 * q + i;
+            const float rr = __uint_as_float((i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16));
+            o[i] = act_t<ACT>(fmaf(__uint_as_float(v2[c >> 4][c & 15]), a.sb[64 + c], a.sb[96 + c])) + rr;
+          }
+          *reinterpret_cast<uint4*>(row + ((q ^ ((t >> 1) & 3)) << 4)) =
+              make_uint4(bf16x2_rn(o[0], o[1]), bf16x2_rn(o[2], o[3]), bf16x2_rn(o[4], o[5]), bf16x2_rn(o[6], o[7]));
+        }
       }
     }
     fence_proxy_async_smem();
