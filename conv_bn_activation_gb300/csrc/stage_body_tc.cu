@@ -6,36 +6,41 @@
 //     b   = act(s2 * conv3x3(a) + b2)                   16 -> 16, pad 1
 //     out = act(s3 * conv1x1([a | b]) + b3) + x1        32 -> 32, residual after the activation
 // At 3,840 multiply-adds per output pixel the body is a contraction: the
-// three convolutions run as tcgen05 MMAs (kind::tf32, fp32 accumulate in
-// TMEM) with TF32 operands, the precision of the library's other
-// tensor-core layers: weights rounded to the nearest TF32 once, a, b and
-// out rounded to the nearest TF32 when they are formed.  a and b never leave
-// the SM; the kernel reads x1 once (plus its tiles' halos, mostly from L2)
-// and writes out once, where the three layer launches move a, b and the
-// concat through HBM and read x1 twice.
+// three convolutions run as tcgen05 MMAs with fp32 accumulators in TMEM, at
+// the precision of the library's other tensor-core layers.  fp32 storage:
+// kind::tf32 on TF32 operands (weights rounded to the nearest TF32 once; a,
+// b and out rounded to the nearest TF32 when formed).  bf16 storage (the same
+// kernel, T = bf16): kind::f16 on bf16 operands; a and b stored as bf16 as
+// the layers store them, the 3x3's weights bf16 as the bf16 tensor-core
+// layer multiplies them, the 1x1 layers' weights split into a bf16 head and
+// tail (two MMAs each) so that they act with fp32 accuracy as in the 1x1
+// layer kernels.  a and b never leave the SM; the kernel reads x1 once (plus
+// its tiles' halos, mostly from L2) and writes out once, where the three
+// layer launches move a, b and the concat through HBM and read x1 twice.
 //
 // Work: tiles of 4 x 32 output pixels (the MMA's M = 128).
 //  * One CTA per SM (a kernel that allocates TMEM is placed one per SM)
-//    made of three independent 128-thread warpgroups, each with its own
-//    shared memory, TMEM columns, mbarriers and named barrier, walking its
-//    own tiles: while one waits for its MMAs, the others form operands.
+//    made of independent 128-thread warpgroups (three for fp32, four for
+//    bf16), each with its own shared memory, TMEM columns, mbarriers and
+//    named barrier, walking its own tiles: while one waits for its MMAs, the
+//    others form operands.
 //  * x1 over the tile and its 1-pixel halo (6 x 34 pixels x 32 channels)
-//    arrives by one TMA copy (zero outside the image), 128-byte swizzled
-//    K-major rows: the A operand of the 1x1 16 <- 32 over two M = 128 row
-//    blocks (rows past the 204 haloed pixels are never used).
+//    arrives by one TMA copy (zero outside the image), swizzled K-major rows
+//    (128 bytes fp32, 64 bf16): the A operand of the 1x1 16 <- 32 over two
+//    M = 128 row blocks (rows past the 204 haloed pixels are never used).
 //  * a is written three times into shared memory, copy dx holding haloed
-//    column c + dx at column c (6 rows x 32 columns each, 64-byte swizzled
-//    rows).  Tap (dy, dx) of the 3x3 then reads, for output pixel
-//    p = 32 r + c, row p + 32 dy of copy dx: a constant offset, so each tap
-//    is one descriptor start address and no output column is wasted.  Outside
-//    the image a is zero (the 3x3's padding, not act(b1)).
-//  * b (the 3x3's 18 MMAs) overwrites copy 0, which no MMA reads any more;
-//    the last 1x1 reads [a | b] as two K halves: the centre of copy 1 (rows
+//    column c + dx at column c (6 rows x 32 columns each, swizzled rows of 64
+//    bytes fp32, 32 bf16).  Tap (dy, dx) of the 3x3 then reads, for output
+//    pixel p = 32 r + c, row p + 32 dy of copy dx: a constant offset, so each
+//    tap is one descriptor start address and no output column is wasted.
+//    Outside the image a is zero (the 3x3's padding, not act(b1)).
+//  * b (the 3x3's MMAs) overwrites copy 0, which no MMA reads any more; the
+//    last 1x1 reads [a | b] as two K halves: the centre of copy 1 (rows
 //    32-159) and b.
 //  * out = act(bn(.)) + x1 (x1 from global memory, where its tile was just
-//    read: L2; loaded while the 3x3's MMAs run) is staged in shared memory over the
-//    copies of a and leaves by one TMA tensor store, which clips the tile at
-//    the image's edges.
+//    read: L2; loaded while the 3x3's MMAs run) is staged in shared memory
+//    over the copies of a and leaves by one TMA tensor store, which clips the
+//    tile at the image's edges.
 //  * Two threads of each warpgroup issue and wait (bounded waits); the others
 //    wait in the warpgroup's named barrier.  One issues the 3x3's and the
 //    last 1x1's MMAs and the output store; the other the x1 copies and the
