@@ -228,7 +228,9 @@ def test_tuning_overrides_are_validated(cblib):
     """cb_set_tuning knows its knobs by name (unknown names are refused) and resets each with NULL."""
     lib = cblib.load()
     for name, value in (("CB_HALO_FORCE", b"cm,2"), ("CB_IGEMM_FORCE", b"64,3,0"), ("CB_IGEMM_BLOCKS", b"1"),
-                        ("CB_DW_FORCE", b"4,0,2"), ("CB_DW_BLOCK_FORCE", b"0"), ("CB_DEBUG_PLAN", b"")):
+                        ("CB_DW_FORCE", b"4,0,2"), ("CB_DW_BLOCK_FORCE", b"0"), ("CB_DEBUG_PLAN", b""),
+                        ("CB_STEM_KERNEL", b"cuda"), ("CB_DEBUG_DW_SKIP_ROW", b"1"), ("CB_DEBUG_STAGE_SKIP_X", b"1"),
+                        ("CB_TIMEOUT_MS", b"50")):
         assert lib.cb_set_tuning(name.encode(), value) == cblib.OK
         assert lib.cb_set_tuning(name.encode(), None) == cblib.OK
     assert lib.cb_set_tuning(b"CB_NO_SUCH_KNOB", b"1") == cblib.ERR_INVALID_ARG
