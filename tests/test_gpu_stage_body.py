@@ -301,3 +301,43 @@ def test_stage_body_c32_bf16_full_size_stage1(gpu, orc):
     got = y.float().cpu().numpy()
     assert rel_err(got, oracle_stage_body_bf16_storage(orc, xv, st)) <= TOL_BF16
     assert rel_err(got, oracle_stage_body(orc, xv, st)) <= 2 * TOL_BF16
+
+
+@pytest.mark.parametrize("act", [cb.ACT_NONE, cb.ACT_RELU])
+def test_stage_body_c32_bf16_activations(gpu, orc, act):
+    N, H, W = 2, 18, 36
+    st = _stage(act + 80, C=32)
+    x1 = np.random.default_rng(act + 19).standard_normal((N, H, W, 32)).astype(np.float32)
+    xd, xv = to_dev_bf16(x1)
+    y = torch.empty(N, H, W, 32, device=gpu, dtype=torch.bfloat16)
+    cb.stage_body(xd, _layers(st, act, dtype=torch.bfloat16), act, y)
+    sync_check()
+    got = y.float().cpu().numpy()
+    assert rel_err(got, oracle_stage_body_bf16_storage(orc, xv, st, act=act)) <= TOL_BF16
+    assert rel_err(got, oracle_stage_body(orc, xv, st, act=act)) <= 2 * TOL_BF16
+
+
+@pytest.mark.parametrize("C,dtype", [(16, torch.float32), (32, torch.float32), (32, torch.bfloat16)],
+                         ids=["c16_fp32", "c32_fp32", "c32_bf16"])
+def test_stage_body_nan_propagates(gpu, orc, C, dtype):
+    """A NaN in x1 reaches exactly the outputs the oracle makes NaN -- the pixel's 3x3 neighbourhood
+    (through b) -- and no rounding or masking step turns it into a number; every other output
+    still meets the bar."""
+    N, H, W = 1, 12, 40
+    st = _stage(C + 5, C=C)
+    x1 = np.random.default_rng(C).standard_normal((N, H, W, C)).astype(np.float32)
+    x1[0, 5, 17, 3] = np.nan
+    if dtype == torch.bfloat16:
+        xd, xv = to_dev_bf16(x1)
+    else:
+        xd, xv = to_dev(x1), x1
+    y = torch.empty(N, H, W, C, device=gpu, dtype=dtype)
+    cb.stage_body(xd, _layers(st, cb.ACT_SILU, dtype=dtype), cb.ACT_SILU, y)
+    sync_check()
+    got = y.float().cpu().numpy()
+    ref = oracle_stage_body(orc, xv, st)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.isnan(ref[0, 4:7, 16:19]).all() and not np.isnan(ref[0, 8:, :]).any()
+    fin = ~np.isnan(ref)
+    tol = TOL_FP32 if C == 16 else (TOL_TF32 if dtype == torch.float32 else 2 * TOL_BF16)
+    assert np.max(np.abs(got[fin] - ref[fin])) <= tol * np.max(np.abs(ref[fin]))
