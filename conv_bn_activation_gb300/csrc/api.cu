@@ -275,6 +275,7 @@ bool tc_channels_ok(int ci, int k, int stride) {
 struct HaloForce {
   int co = 0;
   bool cm = false;
+  int px = 0;  // channel-major pixels per tile (256 or 192; 0: either)
   int nb = 0, split = 0, tps = 0, sub = 0;
   int res = -1;  // resident weights: -1 the model's choice, 0 off, 1 on
 };
@@ -322,8 +323,11 @@ bool parse_tuning(Tuning* t, const char* name, const char* v) {
     HaloForce f;
     if (!unset) {
       if (v[0] == 'c' && v[1] == 'm') {
+        // "cm[PX][,nb,split,tps]"
         f.cm = true;
-        if (v[2] == ',') std::sscanf(v + 3, "%d,%d,%d", &f.nb, &f.split, &f.tps);
+        const char* r = v + 2;
+        if (*r >= '0' && *r <= '9') f.px = static_cast<int>(std::strtol(r, const_cast<char**>(&r), 10));
+        if (*r == ',') std::sscanf(r + 1, "%d,%d,%d", &f.nb, &f.split, &f.tps);
       } else {
         std::sscanf(v, "%d,%d,%d,%d,%d,%d", &f.co, &f.nb, &f.split, &f.tps, &f.sub, &f.res);
       }
@@ -500,7 +504,7 @@ cb_status run_depthwise(const cb_tensor* x, const float* w, const Epilogue& ep, 
 // -------------------------------------------------------------------- dense
 struct HaloPlan {
   int px = 0, co = 0;  // tile: px pixels x co output channels
-  bool cm = false;     // channel-major accumulator (px = 256, co = 128)
+  bool cm = false;     // channel-major accumulator (px = 256 or 192, co = 128)
   int nb = 0, grid = 0;
   int split = 1;       // 2: clusters of two CTAs split each tile's channel chunks
   int tps = 1;         // filter taps per weight-ring stage (one copy per stage)
@@ -771,7 +775,7 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
     int px, co;
     bool cm;
   };
-  static const Shape kShapes[] = {{256, 128, true}, {128, 256, false}, {128, 128, false}, {128, 64, false},
+  static const Shape kShapes[] = {{256, 128, true}, {192, 128, true}, {128, 256, false}, {128, 128, false}, {128, 64, false},
                                   {128, 32, false}};
   // Column blocks: the padded width of the pixel numbering must fit a copy
   // box (256 elements traversed: blk_w + 2 at stride 1, 2 (blk_w + 1) at
@@ -782,6 +786,7 @@ bool plan_halo(const cb_tensor* x, const cb_tensor* y, int stride, int sms, cons
   HaloPlan plan;
   for (const Shape& sh : kShapes) {
     if (f.cm && !sh.cm) continue;
+    if (f.px && sh.cm && sh.px != f.px) continue;
     if (f.co && (sh.cm || sh.co != f.co)) continue;
     if (kc == 16 && (sh.cm || sh.co > 128)) continue;
     if (kc == 16 && sh.co == 128 && stride == 1) continue;
@@ -1369,8 +1374,10 @@ std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int 
     struct Shape {
       int co;
       bool cm;
+      int px;
     };
-    static const Shape kShapes[] = {{128, true}, {256, false}, {128, false}, {64, false}, {32, false}};
+    static const Shape kShapes[] = {{128, true, 256}, {128, true, 192}, {256, false, 128}, {128, false, 128},
+                                    {64, false, 128},  {32, false, 128}};
     for (const Shape& sh : kShapes) {
       if (!sh.cm && sh.co > 2 * ((Co + 15) / 16 * 16)) continue;  // a tile mostly beyond Co
       for (int tps : {9, 3, 1})
@@ -1380,6 +1387,7 @@ std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int 
           HaloForce f;
           f.co = sh.cm ? 0 : sh.co;
           f.cm = sh.cm;
+          f.px = sh.cm ? sh.px : 0;
           f.tps = tps;
           f.split = split;
           f.sub = sb;
@@ -1395,6 +1403,7 @@ std::vector<ConvPlan> tc_candidates(const cb_tensor* x, const cb_tensor* y, int 
         HaloForce f;
         f.co = sh.cm ? 0 : sh.co;
         f.cm = sh.cm;
+        f.px = sh.cm ? sh.px : 0;
         f.sub = sb;
         f.res = 1;
         ConvPlan p;

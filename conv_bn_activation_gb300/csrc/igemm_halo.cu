@@ -1,6 +1,7 @@
 // Host-side sizing and dispatch of the halo-tile implicit GEMM
 // (igemm_halo.cuh).  The pixel-major tiles are instantiated here, the
-// channel-major one in igemm_halo_cm.cu, so that they compile in parallel.
+// channel-major ones in igemm_halo_cm.cu and igemm_halo_cm192.cu, so that
+// they compile in parallel.
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -34,40 +35,8 @@ size_t halo_split_recv_bytes(int px, int co, bool cm) { return static_cast<size_
 int igemm_read_trace_halo(unsigned long long* out, int max_records) { return igemm_read_trace_tu(out, max_records); }
 int igemm_read_spans_halo(unsigned long long* out, int max_ctas) { return igemm_read_spans_tu(out, max_ctas); }
 
-template <int PX, int CO, bool CM>
-cudaError_t halo_launch(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int grid, size_t smem,
-                        cudaStream_t s) {
-  cudaError_t e = smem_attr_once<igemm_halo_kernel<PX, CO, CM>>(smem);
-  if (e != cudaSuccess) return e;
-  if (a.split_k == 2)
-    return launch_pdl_cluster(igemm_halo_kernel<PX, CO, CM>, dim3(grid), dim3(kHaloThreads), smem, s, 2, xmap, wmap,
-                              a);
-  return launch_pdl(igemm_halo_kernel<PX, CO, CM>, dim3(grid), dim3(kHaloThreads), smem, s, xmap, wmap, a);
-}
-
-template <int PX, int CO, bool CM>
-int halo_pairs(size_t smem) {
-  if (smem_attr_once<igemm_halo_kernel<PX, CO, CM>>(smem) != cudaSuccess) return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kHaloThreads);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, igemm_halo_kernel<PX, CO, CM>, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
-int halo_max_pairs_cm(size_t smem);
+int halo_max_pairs_cm256(size_t smem);
+int halo_max_pairs_cm192(size_t smem);
 
 int halo_max_pairs(int px, int co, bool cm, size_t smem) {
   static std::mutex mu;
@@ -81,7 +50,7 @@ int halo_max_pairs(int px, int co, bool cm, size_t smem) {
     if (it != cache.end()) return it->second;
   }
   int n = 0;
-  if (cm) n = px == 256 && co == 128 ? halo_max_pairs_cm(smem) : 0;
+  if (cm) n = co != 128 ? 0 : px == 256 ? halo_max_pairs_cm256(smem) : px == 192 ? halo_max_pairs_cm192(smem) : 0;
   else if (px == 128 && co == 64) n = halo_pairs<128, 64, false>(smem);
   else if (px == 128 && co == 128) n = halo_pairs<128, 128, false>(smem);
   else if (px == 128 && co == 256) n = halo_pairs<128, 256, false>(smem);
@@ -90,8 +59,10 @@ int halo_max_pairs(int px, int co, bool cm, size_t smem) {
   return n;
 }
 
-cudaError_t launch_igemm_halo_cm(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int grid,
-                                 size_t smem, cudaStream_t s);
+cudaError_t launch_igemm_halo_cm256(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int grid,
+                                    size_t smem, cudaStream_t s);
+cudaError_t launch_igemm_halo_cm192(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int grid,
+                                    size_t smem, cudaStream_t s);
 cudaError_t launch_igemm_halo_kc16(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int co,
                                    int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_igemm_halo_kc8(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int co,
@@ -121,11 +92,12 @@ cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, 
                                                 static_cast<size_t>(a.nb_stages) * a.taps_per_stage * co * a.kc * 4)
       return cudaErrorInvalidValue;
   }
+  if (cm && co == 128 && px == 192 && a.kc == 32) return launch_igemm_halo_cm192(xmap, wmap, a, grid, smem, s);
   if (a.bf16) return launch_igemm_halo_bf16(xmap, wmap, a, px, co, cm, grid, smem, s);
   if (a.kc == 16) return !cm && px == 128 ? launch_igemm_halo_kc16(xmap, wmap, a, co, grid, smem, s) : cudaErrorInvalidValue;
   if (a.kc == 8) return !cm && px == 128 ? launch_igemm_halo_kc8(xmap, wmap, a, co, grid, smem, s) : cudaErrorInvalidValue;
   if (a.kc != 32) return cudaErrorInvalidValue;
-  if (cm) return px == 256 && co == 128 ? launch_igemm_halo_cm(xmap, wmap, a, grid, smem, s) : cudaErrorInvalidValue;
+  if (cm) return px == 256 && co == 128 ? launch_igemm_halo_cm256(xmap, wmap, a, grid, smem, s) : cudaErrorInvalidValue;
   if (px != 128) return cudaErrorInvalidValue;
   switch (co) {
     case 32: return halo_launch<128, 32, false>(xmap, wmap, a, grid, smem, s);

@@ -24,13 +24,15 @@
 // Two operand orders share this kernel:
 //  * pixel-major (PX = 128, CO = BN in 32..256): the accumulator holds
 //    pixels x channels, A = shifted halo rows, B = weights (M = 128, N = BN);
-//  * channel-major (PX = 256, CO = 128): the accumulator holds channels x
-//    pixels, A = weights, B = shifted halo rows (M = 128, N = 256).  On
-//    GB300 a kind::tf32 MMA costs about the same issue time for N = 64 and
-//    N = 128 and only a little more for N = 256 (111 / 111 / 128 cycles per
-//    K = 8 step, measured), so a layer with 128 output channels runs its
+//  * channel-major (PX = 256 or 192, CO = 128): the accumulator holds
+//    channels x pixels, A = weights, B = shifted halo rows (M = 128, N = PX).
+//    On GB300 a kind::tf32 MMA costs about the same issue time for N = 64
+//    and N = 128 and only a little more for N = 256 (111 / 111 / 128 cycles
+//    per K = 8 step, measured), so a layer with 128 output channels runs its
 //    tensor cores ~1.7x faster with 256 pixels as N than with its 128
-//    channels as N.
+//    channels as N.  The 192-pixel tile gives a layer of about 100 256-pixel
+//    tiles (128 -> 128 channels at 40 x 40, batch 16) a tile for nearly
+//    every SM instead of leaving a third of them idle.
 //  * warp 0: TMA producer.  Lane 0 loads the halo tile of each (tile, chunk)
 //    -- a 4-D tiled copy of R input rows x Wp columns x 32 channels starting
 //    at (column -1, row y_lo - 1): rows and columns outside the image arrive
@@ -60,6 +62,7 @@
 #pragma once
 
 #include "internal.h"
+#include "launch_util.h"
 #include "ptx.cuh"
 #include "tc_store.cuh"
 #include "trace.cuh"
@@ -77,9 +80,57 @@ constexpr int kHaloStagingBytes = 8 * TileStore<32>::kBufBytes;  // 8 epilogue w
 // accumulator of acc_cols columns.  Narrow tiles keep eight, so that a tile
 // of up to four 128-pixel sub-tiles (one halo copy for all of them) can run
 // while the previous one is stored.
-__host__ __device__ constexpr int halo_naccs(int acc_cols) { return acc_cols >= 256 ? 2 : acc_cols <= 64 ? 8 : 4; }
+__host__ __device__ constexpr int halo_naccs(int acc_cols) { return acc_cols > 128 ? 2 : acc_cols <= 64 ? 8 : 4; }
 __host__ __device__ constexpr int halo_tmem_cols(int acc_cols) {
   return halo_naccs(acc_cols) * acc_cols <= 128 ? 128 : halo_naccs(acc_cols) * acc_cols <= 256 ? 256 : 512;
+}
+
+// Channel-major write-back of one 32-pixel chunk.  Thread `lane` holds
+// output channel c for the chunk's 32 pixels (v[p] = pixel p), so for each
+// pixel the warp's lanes hold 32 consecutive channels and one store
+// instruction writes a contiguous pixel segment: no transpose through shared
+// memory.  yoff / roff are pixel `lane`'s element offsets (yoff < 0: a
+// padding column or past the image), passed to every lane pixel by pixel.
+template <int ACT, int RES, typename T>
+__device__ __forceinline__ void cm_store_t(const uint32_t (&v)[32], long long yoff, long long roff, int c, bool cin,
+                                           float sc, float bi, const OutView& out, const Epilogue& ep) {
+  T* y = reinterpret_cast<T*>(out.y) + c;
+  const T* rb = reinterpret_cast<const T*>(ep.r) + c;
+#pragma unroll
+  for (int g = 0; g < 32; g += 8) {
+    long long yo[8];
+    float r[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      yo[i] = __shfl_sync(0xffffffffu, yoff, g + i);
+      r[i] = 0.0f;
+      if constexpr (RES != 0) {
+        const long long ro = __shfl_sync(0xffffffffu, roff, g + i);
+        if (yo[i] >= 0 && cin) r[i] = load1(rb + ro);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float z = tc_epi_post<ACT, RES, T>(fmaf(__uint_as_float(v[g + i]), sc, bi), r[i]);
+      if (yo[i] >= 0 && cin) store1(y + yo[i], z);
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void cm_store(const uint32_t (&v)[32], long long yoff, long long roff, int c, bool cin,
+                                         float sc, float bi, const OutView& out, const Epilogue& ep) {
+  switch (ep.act * 3 + ep.res_mode) {
+    case 0: cm_store_t<0, 0, T>(v, yoff, roff, c, cin, sc, bi, out, ep); break;
+    case 1: cm_store_t<0, 1, T>(v, yoff, roff, c, cin, sc, bi, out, ep); break;
+    case 2: cm_store_t<0, 2, T>(v, yoff, roff, c, cin, sc, bi, out, ep); break;
+    case 3: cm_store_t<1, 0, T>(v, yoff, roff, c, cin, sc, bi, out, ep); break;
+    case 4: cm_store_t<1, 1, T>(v, yoff, roff, c, cin, sc, bi, out, ep); break;
+    case 5: cm_store_t<1, 2, T>(v, yoff, roff, c, cin, sc, bi, out, ep); break;
+    case 6: cm_store_t<2, 0, T>(v, yoff, roff, c, cin, sc, bi, out, ep); break;
+    case 7: cm_store_t<2, 1, T>(v, yoff, roff, c, cin, sc, bi, out, ep); break;
+    default: cm_store_t<2, 2, T>(v, yoff, roff, c, cin, sc, bi, out, ep); break;
+  }
 }
 
 template <int PX, int CO, bool CM, int KC = kHaloKc, typename T = float>
@@ -91,15 +142,21 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   // 64 or 32 bytes (swizzled to match), i.e. KC fp32 or 2 KC bf16 channels.
   constexpr int kRowBytes = KC * 4;
   constexpr int kChan = kRowBytes / static_cast<int>(sizeof(T));  // channels per chunk
-  static_assert(CM ? (PX == 256 && CO == 128) : (PX == 128 && (CO == 32 || CO == 64 || CO == 128 || CO == 256)),
+  static_assert(CM ? ((PX == 256 || PX == 192) && CO == 128)
+                   : (PX == 128 && (CO == 32 || CO == 64 || CO == 128 || CO == 256)),
                 "tile shape");
   const unsigned long long t_start = a.trace ? trace_globaltimer() : 0;
   constexpr int kAccCols = CM ? PX : CO;  // TMEM columns of one accumulator
+  // column distance between accumulators: a wide one (two per CTA) starts on
+  // a 256-column boundary
+  constexpr int kAccStride = kAccCols > 128 ? 256 : kAccCols;
   // Sub-tiles: a tile of nsub x 128 consecutive pixels shares one halo copy;
   // each 128-pixel sub-tile has its own accumulator (pixel-major only).
   const int sub = CM ? 1 : a.sub;
   constexpr int NACC = halo_naccs(kAccCols);
   constexpr uint32_t kTmemCols = halo_tmem_cols(kAccCols);
+  static_assert(NACC * kAccStride <= static_cast<int>(kTmemCols) && kAccCols % 64 == 0 || kAccCols == 32,
+                "accumulators within the allocation; split halves of whole 32-column chunks");
   constexpr int kTapBytes = CO * KC * 4;  // one tap's weight slice
   const int tps = a.taps_per_stage;            // taps per weight-ring stage: 1, 3 or 9 (one copy each)
   const int kBBytes = tps * kTapBytes;
@@ -107,7 +164,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   // Epilogue split of a tile between the two groups of four warps:
   // pixel-major tiles of 32 channels alternate between the groups, wider
   // ones are split into column halves; channel-major tiles give the groups
-  // alternate 32-pixel chunks.  Either way in 32-column chunks.
+  // alternate 32-pixel chunks.  Either way in 32-column chunks.  Channel-major
+  // chunks are stored straight from registers (cm_store), pixel-major ones
+  // through the warp's staging buffer (TileStore).
   constexpr bool kSplitTiles = !CM && CO == 32;
   constexpr int kWidth = CM ? PX / 2 : (kSplitTiles ? CO : CO / 2);
   constexpr int kChunks = kWidth / 32;
@@ -349,7 +408,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
         uint32_t d_tmem[kHaloMaxSub];
 #pragma unroll
         for (int i = 0; i < kHaloMaxSub; ++i)
-          d_tmem[i] = tmem_base + static_cast<uint32_t>(((local + i) & (NACC - 1)) * kAccCols);
+          d_tmem[i] = tmem_base + static_cast<uint32_t>(((local + i) & (NACC - 1)) * kAccStride);
         for (int i = 0; ok && i < nsub; ++i) {
           const int acc = (local + i) & (NACC - 1);
           if (!mbar_wait(&tempty[acc], (((local + i) / NACC) & 1) ^ 1u, wd)) ok = false;
@@ -438,12 +497,17 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
         roff = (valid && res) ? n_img * a.ep.rs_n + oy * a.ep.rs_h + static_cast<long long>(ox) * a.ep.rs_w : 0;
       };
 
+      // channel-major: this thread's output channel and its folded-BN scale / bias, the same in every chunk (in flight
+      // while the accumulator is waited for)
+      const int cm_c = n_tile * CO + q * 32 + lane;
+      const bool cm_cin = CM && cm_c < a.Cout;
+      const float cm_sc = cm_cin ? __ldg(a.ep.scale + cm_c) : 0.0f, cm_bi = cm_cin ? __ldg(a.ep.bias + cm_c) : 0.0f;
       bool got = mbar_wait(&tfull[acc], acc_phase, wd);
       got = __all_sync(0xffffffffu, got);
       if (!got) break;
       tc_fence_after_sync();
       tr.add(tr_on);
-      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
+      const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kAccStride);
       if (!kSplitTiles && split == 2) {
         // One tile per cluster (the host guarantees it): exchange halves.
         constexpr int kHalf = kAccCols / 2, kHalfChunks = kHalf / 32;
@@ -500,10 +564,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
             TileStore<32>::template write<T>(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
           } else {
             pixel_offsets(q0 + own0 + i * 32 + lane, yoff, roff);
-            const TileStore<32>::Consts k = TileStore<32>::consts(lane, n_tile * CO + q * 32, a.Cout, vec, a.ep);
-            TileStore<32>::stage_columns(stage_buf, lane, v);
-            __syncwarp();
-            TileStore<32>::template write<T>(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+            cm_store<T>(v, yoff, roff, cm_c, cm_cin, cm_sc, cm_bi, a.out, a.ep);
           }
           tr.add(tr_on);
         }
@@ -538,30 +599,22 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
           k = kn;
         }
       } else {
-        // thread = output channel n_tile * CO + 32q + lane; chunks of 32
-        // pixels, group g taking chunks g, g + 2, ...
-        // This warp's 32 channels are the same in every chunk: their scale /
-        // bias are loaded once per tile.
-        const TileStore<32>::Consts k = TileStore<32>::consts(lane, n_tile * CO + q * 32, a.Cout, vec, a.ep);
+        // thread = output channel cm_c; chunks of 32 pixels, group g taking
+        // chunks g, g + 2, ...
 #pragma unroll 1
-        for (int kk = 0; kk < kChunks; ++kk) {
-          const int cidx = group + 2 * kk;
+        for (int cidx = group; cidx < PX / 32; cidx += 2) {
           uint32_t v[32];
           tmem_ld_cols<32>(lane_base + cidx * 32, v);
           tmem_wait_regs(v);
-          if (kk == kChunks - 1) {
+          if (cidx + 2 >= PX / 32) {
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
           }
           tr.add(tr_on);
           long long yoff, roff;
-          pixel_offsets(q0 + cidx * 32 + lane, yoff, roff);  // lane = pixel of the chunk for write()
-          __syncwarp();
-          TileStore<32>::stage_columns(stage_buf, lane, v);
-          __syncwarp();
-          tr.add(tr_on);
-          TileStore<32>::template write<T>(stage_buf, lane, yoff, roff, k, a.Cout, a.out, a.ep);
+          pixel_offsets(q0 + cidx * 32 + lane, yoff, roff);
+          cm_store<T>(v, yoff, roff, cm_c, cm_cin, cm_sc, cm_bi, a.out, a.ep);
           tr.add(tr_on);
         }
       }
@@ -581,6 +634,41 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
     trace_cta_span(a.trace, 0, t_start);
     trace_cta_span(a.trace, 1, trace_globaltimer());
   }
+}
+
+// Launch of one instantiation (clusters of two CTAs for split K), and how
+// many such clusters the device runs at once (0 if none).
+template <int PX, int CO, bool CM, int KC = kHaloKc, typename T = float>
+cudaError_t halo_launch(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int grid, size_t smem,
+                        cudaStream_t s) {
+  cudaError_t e = smem_attr_once<igemm_halo_kernel<PX, CO, CM, KC, T>>(smem);
+  if (e != cudaSuccess) return e;
+  if (a.split_k == 2)
+    return launch_pdl_cluster(igemm_halo_kernel<PX, CO, CM, KC, T>, dim3(grid), dim3(kHaloThreads), smem, s, 2, xmap,
+                              wmap, a);
+  return launch_pdl(igemm_halo_kernel<PX, CO, CM, KC, T>, dim3(grid), dim3(kHaloThreads), smem, s, xmap, wmap, a);
+}
+
+template <int PX, int CO, bool CM>
+int halo_pairs(size_t smem) {
+  if (smem_attr_once<igemm_halo_kernel<PX, CO, CM>>(smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kHaloThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, igemm_halo_kernel<PX, CO, CM>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 }  // namespace cb

@@ -15,6 +15,7 @@ int igemm_read_trace_kc16(unsigned long long* out, int max_records);
 int igemm_read_trace_kc32(unsigned long long* out, int max_records);
 int igemm_read_trace_halo(unsigned long long* out, int max_records);
 int igemm_read_trace_halo_cm(unsigned long long* out, int max_records);
+int igemm_read_trace_halo_cm192(unsigned long long* out, int max_records);
 int igemm_read_trace_halo_kc16(unsigned long long* out, int max_records);
 int dw_block_read_trace(unsigned long long* out, int max_records);
 
@@ -25,6 +26,7 @@ int igemm_read_trace(unsigned long long* out, int max_records) {
   if (n == 0) n = igemm_read_trace_kc8(out, max_records);
   if (n == 0) n = igemm_read_trace_halo(out, max_records);
   if (n == 0) n = igemm_read_trace_halo_cm(out, max_records);
+  if (n == 0) n = igemm_read_trace_halo_cm192(out, max_records);
   if (n == 0) n = igemm_read_trace_halo_kc16(out, max_records);
   if (n == 0) n = dw_block_read_trace(out, max_records);
   return n;

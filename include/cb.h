@@ -490,7 +490,7 @@ int cb_autotune_entries(void);
  *   CB_DW_FORCE       "rows,tile_w,ctas_per_sm" of the depthwise kernel (0 = free)
  *   CB_IGEMM_FORCE    "bn,stages,grid" of the im2col-path tensor-core kernel
  *   CB_IGEMM_BLOCKS   "0" / "1": its A operand as im2col gathers / pixel blocks
- *   CB_HALO_FORCE     "cm[,stages[,split[,taps]]]" or
+ *   CB_HALO_FORCE     "cm[px][,stages[,split[,taps]]]" (px 256 or 192 pixels per tile) or
  *                     "co[,stages[,split[,taps[,subtiles[,resident]]]]]" of the halo kernel
  *   CB_DW_BLOCK_FORCE "1" / "0": the one-kernel depthwise-separable block
  *                     wherever its shape rule allows / never

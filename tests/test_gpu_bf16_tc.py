@@ -82,7 +82,8 @@ def test_bf16_tc_epilogue_variants(gpu, orc, act, res_mode):
            res_mode=res_mode)
 
 
-@pytest.mark.parametrize("force", ["cm", "32", "64", "128", "256", "64,0,0,0,2", "128,0,2", "cm,0,2"])
+@pytest.mark.parametrize("force", ["cm", "cm192", "32", "64", "128", "256", "64,0,0,0,2", "128,0,2", "cm,0,2",
+                                   "cm192,0,2"])
 def test_bf16_halo_every_tile(gpu, orc, force):
     """Every halo tile shape (forced), incl. split K over CTA pairs and sub-tiles, in bf16."""
     case = (2, 20, 20, 128, 128, 3, 1)

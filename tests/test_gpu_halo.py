@@ -1,6 +1,6 @@
 """GPU parity of the halo-tile tensor-core kernel (3x3, stride 1, pad 1, Cin % 32 == 0), in both of
-its tile shapes: pixel-major (128 pixels x up to 256 channels) and channel-major (256 pixels x 128
-channels, the channels as the MMA's M).
+its tile shapes: pixel-major (128 pixels x up to 256 channels) and channel-major (256 or 192 pixels x
+128 channels, the channels as the MMA's M).
 
 Each output is checked against the fp64 oracle at the TF32 bar (5e-3 of max|oracle|).  The
 shapes cover one and several tiles per image, tiles that wrap across output rows, images narrower
@@ -54,10 +54,11 @@ def test_halo_silu(gpu, orc, case):
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
 
 
-@pytest.mark.parametrize("bn_force", ["32,0", "64,0", "128,0", "256,0", "128,3", "64,16", "cm", "cm,2",
+@pytest.mark.parametrize("bn_force", ["32,0", "64,0", "128,0", "256,0", "128,3", "64,16", "cm", "cm,2", "cm192",
+                                      "cm192,2",
                                       # taps per weight-ring stage (one copy each): 9, 3 and 1
                                       "32,0,1,9", "64,0,1,3", "128,0,1,3", "128,0,1,1", "cm,0,1,3", "cm,0,1,1",
-                                      "256,0,1,1"])
+                                      "cm192,0,1,3", "cm192,0,1,1", "256,0,1,1"])
 def test_halo_tile_widths(gpu, orc, halo_force, bn_force):
     halo_force(bn_force)
     x, w, bn = synthetic.dense_layer(64, 200, 10, 23, N=2, k=3, seed=3)
@@ -152,9 +153,10 @@ CM_CASES = [
 ]
 
 
+@pytest.mark.parametrize("px", [256, 192])
 @pytest.mark.parametrize("case", CM_CASES, ids=lambda s: "x".join(map(str, s)))
-def test_halo_channel_major(gpu, orc, halo_force, case):
-    halo_force("cm")
+def test_halo_channel_major(gpu, orc, halo_force, case, px):
+    halo_force(f"cm{px}")
     N, H, W, Ci, Co = case
     x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=sum(case) + 7)
     layer = ConvBnAct(w, bn, 1, 1, cb.ACT_SILU)
@@ -167,10 +169,11 @@ def test_halo_channel_major(gpu, orc, halo_force, case):
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
 
 
+@pytest.mark.parametrize("px", [256, 192])
 @pytest.mark.parametrize("act,res_mode", [(1, 1), (2, 2), (0, 0)])
-def test_halo_channel_major_epilogues_and_views(gpu, orc, halo_force, act, res_mode):
+def test_halo_channel_major_epilogues_and_views(gpu, orc, halo_force, act, res_mode, px):
     """Channel-major tiles into a channel slice of a padded buffer, with a residual."""
-    halo_force("cm")
+    halo_force(f"cm{px}")
     N, H, W, Ci, Co = 2, 11, 19, 64, 128
     x, w, bn = synthetic.dense_layer(Ci, Co, H, W, N=N, k=3, seed=31 + act)
     r = np.random.default_rng(6).standard_normal((N, H, W, Co)).astype(np.float32)
@@ -190,6 +193,7 @@ SPLIT_CASES = [
     # N, H, W, Cin, Cout, CB_HALO_FORCE: one tile per CTA pair, K chunks split between the pair
     (1, 20, 20, 128, 256, "256,0,2"), (1, 9, 13, 96, 128, "128,0,2"), (2, 5, 7, 64, 64, "64,0,2"),
     (1, 20, 20, 256, 256, "cm,0,2"), (1, 11, 17, 96, 200, "cm,0,2"), (2, 12, 12, 64, 100, "128,0,2"),
+    (1, 20, 20, 256, 256, "cm192,0,2"), (1, 11, 17, 96, 200, "cm192,0,2"), (1, 13, 15, 64, 128, "cm192,0,2"),
 ]
 
 
@@ -205,7 +209,7 @@ def test_halo_split_k(gpu, orc, halo_force, case):
     assert rel_err(y.cpu().numpy(), ref) <= TOL_TF32
 
 
-@pytest.mark.parametrize("force", ["128,0,2", "cm,0,2"])
+@pytest.mark.parametrize("force", ["128,0,2", "cm,0,2", "cm192,0,2"])
 @pytest.mark.parametrize("act,res_mode", [(1, 1), (2, 2)])
 def test_halo_split_k_epilogues_and_views(gpu, orc, halo_force, force, act, res_mode):
     """Split-K tiles into a channel slice of a padded buffer, with a residual: nothing outside
