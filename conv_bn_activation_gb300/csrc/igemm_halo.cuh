@@ -44,9 +44,11 @@
 //    into one of NACC TMEM accumulators; tcgen05.commit releases weight
 //    stages, halo tiles and, at the end of a tile, the accumulator.
 //  * warps 2-9: epilogue (two groups of four warps, one per TMEM lane
-//    quarter), written back through TileStore: coalesced pixel-major stores,
-//    columns ox >= W and rows past the image masked.  Channel-major tiles are
-//    transposed in the staging buffer (TileStore::stage_columns).
+//    quarter), columns ox >= W and rows past the image masked.  Pixel-major
+//    chunks are written back through TileStore (a transpose in shared memory
+//    that makes the stores coalesced); a channel-major chunk already holds
+//    32 consecutive channels of each pixel across a warp, so it is stored
+//    straight from registers (cm_store).
 // CTAs are persistent and stride over the (pixel tile, channel tile) pairs.
 //
 // Split K (split_k = 2, layers with fewer tiles than half the SMs): CTA

@@ -150,20 +150,10 @@ struct TileStore {
       *reinterpret_cast<uint4*>(rowp + ((j ^ s) << 4)) = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
   }
 
-  // The transpose of stage(): thread `lane` holds column `lane` (one output
-  // channel) for 32 rows (pixels), v[p] being row p; it lands where write()
-  // reads it.  For each p the 32 lanes hit 32 different banks.
-  __device__ static __forceinline__ void stage_columns(uint8_t* buf, int lane, const uint32_t (&v)[CH]) {
-    static_assert(CH == 32, "square 32 x 32 block");
-    const int j = lane >> 2, e = (lane & 3) * 4;
-#pragma unroll
-    for (int p = 0; p < 32; ++p) *reinterpret_cast<uint32_t*>(buf + p * kRowBytes + ((j ^ swz(p)) << 4) + e) = v[p];
-  }
-
   // Per-lane epilogue constants of one chunk: the lane's 16-byte channel
   // group c .. c + 3 (c = c0 + 4 * (lane % kLpp)) and its folded-BN scale
-  // and bias.  Loaded once per chunk position -- for a channel-major tile
-  // once per tile -- ahead of the chunk they serve.
+  // and bias.  Loaded once per chunk position, ahead of the chunk they
+  // serve.
   struct Consts {
     float sc[4], bi[4];
     int c;
