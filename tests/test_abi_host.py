@@ -227,7 +227,8 @@ def test_round_weights_tf32(cblib):
 def test_tuning_overrides_are_validated(cblib):
     """cb_set_tuning knows its knobs by name (unknown names are refused) and resets each with NULL."""
     lib = cblib.load()
-    for name, value in (("CB_HALO_FORCE", b"cm,2"), ("CB_IGEMM_FORCE", b"64,3,0"), ("CB_IGEMM_BLOCKS", b"1"),
+    for name, value in (("CB_HALO_FORCE", b"cm,2"), ("CB_HALO_FORCE", b"cm192"), ("CB_HALO_FORCE", b"cm192,0,1,3"),
+                        ("CB_HALO_FORCE", b"128,0,2"), ("CB_IGEMM_FORCE", b"64,3,0"), ("CB_IGEMM_BLOCKS", b"1"),
                         ("CB_DW_FORCE", b"4,0,2"), ("CB_DW_BLOCK_FORCE", b"0"), ("CB_DEBUG_PLAN", b""),
                         ("CB_STEM_KERNEL", b"cuda"), ("CB_DEBUG_DW_SKIP_ROW", b"1"), ("CB_DEBUG_STAGE_SKIP_X", b"1"),
                         ("CB_TIMEOUT_MS", b"50")):
