@@ -162,7 +162,7 @@ size_t halo_split_recv_bytes(int px, int co, bool cm);
 // Clusters of two CTAs of this tile shape and shared-memory size that the
 // device runs at once (0 if it cannot run them).
 int halo_max_pairs(int px, int co, bool cm, size_t smem_bytes);
-// px x co tile: 128 x {32, 64, 128, 256} pixel-major, or 256 x 128 channel-major (cm).
+// px x co tile: 128 x {32, 64, 128, 256} pixel-major, or 256 x 128 / 192 x 128 channel-major (cm).
 cudaError_t launch_igemm_halo(const CUtensorMap& xmap, const CUtensorMap& wmap, const HaloArgs& a, int px, int co,
                               bool cm, int grid, size_t smem_bytes, cudaStream_t s);
 
