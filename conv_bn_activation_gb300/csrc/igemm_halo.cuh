@@ -157,8 +157,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1) igemm_halo_kernel(const __gri
   const int sub = CM ? 1 : a.sub;
   constexpr int NACC = halo_naccs(kAccCols);
   constexpr uint32_t kTmemCols = halo_tmem_cols(kAccCols);
-  static_assert(NACC * kAccStride <= static_cast<int>(kTmemCols) && kAccCols % 64 == 0 || kAccCols == 32,
-                "accumulators within the allocation; split halves of whole 32-column chunks");
+  static_assert(NACC * kAccStride <= static_cast<int>(kTmemCols), "accumulators within the allocation");
+  static_assert(kAccCols % 64 == 0 || kAccCols == 32, "split-K halves of whole 32-column chunks");
   constexpr int kTapBytes = CO * KC * 4;  // one tap's weight slice
   const int tps = a.taps_per_stage;            // taps per weight-ring stage: 1, 3 or 9 (one copy each)
   const int kBBytes = tps * kTapBytes;
