@@ -38,7 +38,7 @@ def _rank(rank, world, port, out):
 
 def test_aggregate_over_two_gloo_ranks():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this multi-threaded process
         out = m.dict()
         mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
