@@ -46,6 +46,10 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 AUTOTUNE = True  # measure the tile plans of tensor-core layers at setup (cb_autotune_conv)
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rates
+# kind::tf32 MMAs (M = 128, N = 256, K = 8) issued back to back on all 152 SMs of a GB300 at
+# 2070 MHz, 128 cycles each: the rate the TF32 tensor pipe sustains, reported beside the peak
+# scaled from the bf16 measurement
+TF32_ISSUE_LOOP_TFLOPS = 1207.0
 UNIT_SCALE = {"GB/s": 1e9, "TFLOP/s": 1e12, "images/s": 1.0}
 
 
@@ -247,10 +251,13 @@ class Workload:
             achieved = L.work.flops / (ms * 1e-3) / 1e12
             peak = peaks["bf16_tflops"] if self.tc_dtype == "bf16" else tf32_peak(peaks)
             bw_roof = L.work.bytes / (ms * 1e-3) / 1e9
-            return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4),
-                    "frac_of_min_roof": round(achieved / min(peak, L.work.intensity * peaks["hbm_gbs"] / 1e3), 4),
-                    "hbm_gbs": round(bw_roof, 1), "intensity": round(L.work.intensity, 2)}
+            r = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                 "frac": round(achieved / peak, 4),
+                 "frac_of_min_roof": round(achieved / min(peak, L.work.intensity * peaks["hbm_gbs"] / 1e3), 4),
+                 "hbm_gbs": round(bw_roof, 1), "intensity": round(L.work.intensity, 2)}
+            if self.tc_dtype != "bf16":
+                r["frac_of_tf32_issue_loop"] = round(achieved / TF32_ISSUE_LOOP_TFLOPS, 4)
+            return r
         if L.bound == "alu":  # fp32 FMAs on the CUDA cores: against the derived FMA peak
             achieved = L.work.flops / (ms * 1e-3) / 1e12
             return {"bound": "alu", "achieved": round(achieved, 2), "peak": round(peaks["fp32_fma_tflops"], 1),
